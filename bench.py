@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA layer on GB300: prefill tokens/s and decode steps/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload layer_8k|varlen_16|long_1m] [--decode-steps K2]
+
+Prefill step: one kda_prefill call over the whole batch (every stage of the
+layer: conv + SiLU + L2, chunkwise gated delta rule, RMSNorm + gate, final
+states).  Decode step: one kda_decode_step over 256 sequences x 96 heads.
+Inputs are seeded synthetic data resident in HBM before the timed region;
+every prefill batch (>= 1.2 GB of inputs) and the decode state (1.6 GB) are
+larger than the 129 MB L2, so no flush is needed between iterations.
+
+One JSON line is printed by rank 0.  With N > 1 ranks (torchrun), every rank
+runs its own replica of the workload on its own GPU (units are independent:
+no collective on the data path); the timed region is bracketed by barriers
+and the slowest rank's time is used; value = all ranks' tokens / that time.
+
+``--impl reference`` times the fp64 CPU oracle (the reference for this
+layer) on the host cores, on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s (H=96,d=128) + decode steps/s; % of tensor/HBM roofline"
+PREFILL_FLOP_PER_TOKEN_HEAD = {(128, 64): 180_224}   # 2C(3dk+2dv) + 6 dk dv
+PREFILL_BYTES_PER_TOKEN_HEAD_BF16 = 1796             # q,k,v 768 + gate 256 + g 512 + beta 4 + y 256
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x: float, device) -> float:
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kimi_delta_attention_16_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if the kernels have not changed."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p)).get(kernel_key)
+    except (ValueError, OSError):
+        return None
+    if not d or d.get("source_hash") != kernel_source_hash():
+        return None
+    return d.get("bytes_per_launch")
+
+
+def prefill_path(inp):
+    from kimi_delta_attention_16_gb300 import kda_prefill_workspace_size
+    # The tensor-core path needs no fp32 staging of q|k|v; the SIMT path needs 16 T H D bytes.
+    simt_ws = kda_prefill_workspace_size(inp.T, inp.H, inp.D, chunk=inp.chunk, flags=1)
+    ws = kda_prefill_workspace_size(inp.T, inp.H, inp.D, chunk=inp.chunk)
+    return ("simt" if ws == simt_ws and ws > 0 else "tc"), ws
+
+
+def prefill_launches(path):
+    # kernels one kda_prefill call enqueues here (host cu_seqlens given, no conv_state_out):
+    # tensor-core path: the fused chunk kernel; SIMT path: conv, chunk recurrence, epilogue.
+    return 1 if path == "tc" else 3
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    import kimi_delta_attention_16_gb300 as kda
+    from kimi_delta_attention_16_gb300 import synth
+
+    world, rank, local, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    inp = synth.make_prefill(args.workload, seed=1, device=dev)
+    N, T, H, D = inp.N, inp.T, inp.H, inp.D
+    path, ws_bytes = prefill_path(inp)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((N, H, D, D), dtype=torch.float32, device=dev)
+    cu_dev = (torch.from_numpy(inp.cu_seqlens).to(dev), inp.cu_seqlens)  # (device, host)
+
+    def step():
+        kda.kda_prefill(inp.q, inp.k, inp.v, inp.conv_w, inp.g, inp.beta, cu_dev, chunk=inp.chunk,
+                        gate=inp.gate, rms_w=inp.rms_w, initial_state=inp.initial_state,
+                        final_state=fin, out=out, workspace=ws)
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(pg)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(pg, ms, dev)
+    tokens_per_s = world * T / (ms_max / 1e3)
+
+    # roofline of the prefill launch(es)
+    fl = PREFILL_FLOP_PER_TOKEN_HEAD.get((D, inp.chunk), 0) * T * H
+    state_bytes = N * H * D * D * 4 * (2 if inp.initial_state is not None else 1)
+    alg_bytes = T * H * PREFILL_BYTES_PER_TOKEN_HEAD_BF16 + state_bytes
+    gbs = alg_bytes / (ms / 1e3) / 1e9
+    tflops = fl / (ms / 1e3) / 1e12
+    roof = {"kernel": "kda_prefill (" + ("fused tcgen05 chunk kernel" if path == "tc" else
+                                         "SIMT path: conv + chunk recurrence + epilogue") + ")",
+            "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": peak_src,
+            "traffic": recorded_traffic(f"prefill_{path}_{args.workload}"),
+            "algorithmic_bytes": alg_bytes, "algorithmic_flops": fl,
+            "tensor_tflops": round(tflops, 1),
+            "tensor_frac": round(tflops / peaks["bf16_tflops"], 4)}
+
+    # end to end: host (pinned) inputs -> H2D -> kda_prefill -> D2H of out and final state
+    host = {}
+    for name in ("q", "k", "v", "gate", "g", "beta"):
+        t = getattr(inp, name)
+        host[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        host[name].copy_(t)
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    fin_h = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+    dev_in = {k: torch.empty_like(getattr(inp, k)) for k in host}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * fin_h.element_size()
+
+    def e2e_step():
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        kda.kda_prefill(dev_in["q"], dev_in["k"], dev_in["v"], inp.conv_w, dev_in["g"],
+                        dev_in["beta"], cu_dev, chunk=inp.chunk, gate=dev_in["gate"],
+                        rms_w=inp.rms_w, initial_state=inp.initial_state, final_state=fin,
+                        out=out, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        fin_h.copy_(fin, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(pg)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    e2e_ms = max_over_ranks(pg, e0.elapsed_time(e1) / e2e_steps, dev)
+    del host, dev_in, out_h, fin_h
+
+    # decode: 256 sequences x 96 heads, one launch per step
+    dec_obj = None
+    dec_launches = 0
+    if args.decode_steps > 0:
+        del ws
+        dec = synth.make_decode(seed=4, device=dev)
+        dout = torch.empty((dec.N, dec.H, dec.D), dtype=torch.bfloat16, device=dev)
+
+        def dstep(i):
+            j = i % dec.ring
+            kda.kda_decode_step(dec.q[j], dec.k[j], dec.v[j], dec.g[j], dec.beta[j], dec.conv_w,
+                                dec.state, dec.conv_state, gate=dec.gate[j], rms_w=dec.rms_w,
+                                out=dout)
+
+        for i in range(max(args.warmup, 3)):
+            dstep(i)
+        torch.cuda.synchronize()
+        barrier(pg)
+        e0.record(stream)
+        for i in range(args.decode_steps):
+            dstep(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(pg)
+        dms = e0.elapsed_time(e1) / args.decode_steps
+        dms_max = max_over_ranks(pg, dms, dev)
+        Nd, Hd, Dd = dec.N, dec.H, dec.D
+        dbytes = (2 * Nd * Hd * Dd * Dd * 4 + 2 * Nd * 3 * Hd * Dd * 3 * 2 + 4 * Nd * Hd * Dd * 2 +
+                  Nd * Hd * Dd * 4 + Nd * Hd * 4 + Nd * Hd * Dd * 2)
+        dgbs = dbytes / (dms / 1e3) / 1e9
+        dec_launches = args.decode_steps
+        dec_obj = {"metric": "KDA decode steps/s (256 seqs x 1 token, H=96, d=128)",
+                   "value": round(world / (dms_max / 1e3), 2), "unit": "steps/s",
+                   "tokens_per_s": round(world * Nd / (dms_max / 1e3), 1),
+                   "ms_per_step": round(dms_max, 4), "steps": args.decode_steps,
+                   "roofline": {"kernel": "k_decode", "bound": "hbm", "achieved": round(dgbs, 1),
+                                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                "frac": round(dgbs / peaks["hbm_gbs"], 4),
+                                "peak_source": peak_src,
+                                "traffic": recorded_traffic("decode_decode_256"),
+                                "algorithmic_bytes": dbytes}}
+    clk = clocks.stop()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, args.workload)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16" if path == "tc" else "fp32",
+                "data": "synthetic",
+                "config": {"workload": workload_desc(args.workload), "global_batch": N * world,
+                           "seq_len": T, "heads": H, "head_dim": D, "chunk": inp.chunk,
+                           "prefill_path": path, "l2": "inputs larger than L2 (no flush)",
+                           "parallelism": f"replicas x{world}"},
+                "roofline": roof,
+                "e2e": {"value": round(world * T / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                        "ms_per_step": round(e2e_ms, 4)},
+                "decode": dec_obj, "cpu_baseline": cpu, "clocks": clk,
+                "gpu_launches": prefill_launches(path) * args.steps + dec_launches}
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def workload_desc(name):
+    return {
+        "layer_8k": "layer_8k: one KDA layer prefill, B=1, T=8192, H=96, d=128, chunk 64, bf16 "
+                    "q/k/v/gate, fp32 g/beta/state, zero initial state",
+        "varlen_16": "varlen_16: 16 packed sequences, lengths log-uniform in [512,16384], H=96, "
+                     "d=128, bf16 I/O, initial states N(0,0.02^2)",
+        "long_1m": "long_1m: B=1, T=1048576, H=24, d=128, chunk 64, bf16 I/O",
+    }[name]
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def cpu_baseline(inp, workload, tokens=None):
+    """The fp64 oracle, as it stands, on a bounded sample of the same workload."""
+    import oracle
+    from kimi_delta_attention_16_gb300 import synth
+    import numpy as np
+    n_tok = tokens or min(inp.T, 2048)
+    s = slice(0, n_tok)
+    f = synth.to_f32_numpy
+    a = dict(q=f(inp.q[s]), k=f(inp.k[s]), v=f(inp.v[s]), conv_w=f(inp.conv_w),
+             cu_seqlens=np.array([0, n_tok], np.int32), g=f(inp.g[s]), beta=f(inp.beta[s]),
+             gate=f(inp.gate[s]) if inp.gate is not None else None, rms_w=f(inp.rms_w),
+             initial_state=None if inp.initial_state is None else f(inp.initial_state[:1]))
+    cores = min(oracle.num_cores(), inp.H)
+    t0 = time.perf_counter()
+    oracle.forward(**a, n_threads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": round(n_tok / dt, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n_tok} tokens of the first sequence, all {inp.H} heads "
+                      f"({workload}), fp64 token-sequential oracle, {dt:.2f} s"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch  # noqa: F401  (CPU tensors only)
+    from kimi_delta_attention_16_gb300 import synth
+    import oracle
+    w = synth.WORKLOADS[args.workload]
+    sample_tokens = 256
+    inp = synth.make_prefill(args.workload, seed=1, device="cpu",
+                             lengths=[sample_tokens], H=w["H"], D=w["D"])
+    times = []
+    res = None
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        res = cpu_baseline(inp, args.workload, tokens=sample_tokens)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    per_step = statistics.mean(times) if times else float("nan")
+    value = sample_tokens / per_step
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(per_step * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(args.workload), "seq_len": w.get("T"),
+                       "heads": w["H"], "head_dim": w["D"]},
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": res["cores"],
+                             "kind": "oracle",
+                             "sample": f"each step: {sample_tokens} tokens x {w['H']} heads of "
+                                       f"{args.workload} through the fp64 oracle"},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["layer_8k", "varlen_16", "long_1m"], default="layer_8k")
+    ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * kda.h -- C ABI of libkda.so: the Kimi Delta Attention (KDA) layer on one
+ * GB300 (sm_103a).
+ *
+ * What the layer computes, per head of width D (page "Kimi K3 / Architecture",
+ * panel "Kimi Delta Attention . one head at token t", and page "Animated Kimi
+ * K3 architecture diagram", section "LOCAL MEMORY: A FIXED MATRIX THAT
+ * PREDICTS, FORGETS, AND CORRECTS"):
+ *
+ *   short conv  u = sum_{j=0..3} w[j] x[t-3+j] per channel, then SiLU
+ *   L2 norm     q <- q / sqrt(|q|^2 + eps_l2), same for k (v is not normalised)
+ *   decay       S_bar = Diag(exp(g_t)) S_{t-1}           (g_t: log-decay per key channel)
+ *   correct     e_t = v_t - S_bar^T k_t
+ *   write       S_t = S_bar + beta_t k_t e_t^T          (beta_t: one scalar per token, head)
+ *   read        o_t = scale * S_t^T q_t
+ *   epilogue    y_t = o_t / sqrt(mean(o_t^2) + eps_rms) * w_rms * sigmoid(gate_t)
+ *
+ * The state S is a fixed D x D fp32 matrix per (sequence, head), row = key
+ * channel, column = value channel.
+ *
+ * Conventions for every entry point:
+ *  - Ownership: the caller owns every buffer.  The library allocates nothing
+ *    on the device and keeps no state between calls except a per-device cache
+ *    of kernel attributes.
+ *  - Asynchrony: calls only enqueue work on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream) and never synchronise.
+ *  - Errors: invalid arguments return before anything is launched.  A launch
+ *    failure returns KDA_ERR_CUDA.  Conditions found on the device (an
+ *    inconsistent cu_seqlens) are written to the optional `d_status` word
+ *    (a device int the caller zeroes) and the affected work is skipped; no
+ *    kernel traps or asserts.
+ *  - Value ranges: g is expected in [-5, 0] (the pages bound the log-decay
+ *    below by -5) and beta in [0, 1].  They are not range-checked on the
+ *    device; g > 0 may overflow.
+ *  - Shapes: D in {16, 32, 64, 128}; the tensor-core prefill path needs
+ *    D = 128, chunk = 64 and bf16 inputs, everything else takes the fp32 SIMT
+ *    path.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st* kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, aliasing, bad cu_seqlens */
+    KDA_ERR_UNSUPPORTED = 2, /* shape or dtype this library does not implement */
+    KDA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than kda_prefill_workspace_size */
+    KDA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+    KDA_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (reported via d_status) */
+    KDA_ERR_DEVICE_ARG = 6   /* the device copy of cu_seqlens was inconsistent (via d_status) */
+} kda_status;
+
+typedef enum { KDA_BF16 = 0, KDA_FP32 = 1 } kda_dtype;
+
+/* Static English text for a status code. */
+const char* kda_status_string(int status);
+
+/* Text describing the last error returned on the calling host thread. */
+const char* kda_last_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int kda_version(void);
+
+/* ------------------------------------------------------------------------
+ * kda_short_conv -- causal depthwise short convolution + SiLU (+ L2 on q, k).
+ * Page "Kimi K3 / Architecture", panel "KDA short convolution . one channel
+ * c at token t": window of width 4 over x[t-3..t] of one channel, only time
+ * is mixed, left padding keeps the length, SiLU after the 4-tap sum; Q and K
+ * are then L2-normalised per head, V is not.  Filter banks Wq, Wk, Wv; the
+ * rolling state keeps the previous 3 raw values per channel ([B,36864,3] for
+ * 96 heads of 128).
+ *
+ *   x         [T_total][row stride x_row_stride elements], channels q|k|v:
+ *             channel = part*H*D + h*D + d (part 0=q, 1=k, 2=v); io dtype.
+ *   w         [3*H*D][4] fp32; tap 3 multiplies x[t], tap 0 multiplies x[t-3].
+ *   cu_seqlens device int32 [N+1]: cu[0]=0, non-decreasing, cu[N]=T_total.
+ *             Sequences never see each other's tokens.
+ *   cu_seqlens_host optional host copy; when given it is validated on the
+ *             host (no device sync is ever needed).
+ *   conv_state_in  [N][3*H*D][3] io dtype, oldest first, or NULL (zeros).
+ *   conv_state_out [N][3*H*D][3] io dtype or NULL: the last 3 raw values of
+ *             each sequence (taking conv_state_in into account for short
+ *             sequences).  Must not overlap conv_state_in.
+ *   y         [T_total][y_row_stride elements] io dtype; must not overlap x.
+ *   l2norm_qk nonzero: L2-normalise the q and k parts per head with eps_l2.
+ * Alignment: x, y 16-byte aligned; row strides multiples of 8 elements (bf16)
+ * or 4 elements (fp32); D, H >= 1 with D in {16,32,64,128}.
+ * ------------------------------------------------------------------------ */
+kda_status kda_short_conv(const void* x, int64_t x_row_stride, const float* w,
+                          const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int N,
+                          int64_t T_total, int H, int D, const void* conv_state_in,
+                          void* conv_state_out, void* y, int64_t y_row_stride, int l2norm_qk,
+                          float eps_l2, kda_dtype io, int* d_status, kda_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * kda_prefill -- the whole layer over packed variable-length sequences.
+ * Page "Kimi K3 / Architecture", KDA panel: "recurrent across chunks,
+ * parallel within a chunk", "dense Tensor Core tiles in the chunkwise
+ * form"; page "Animated Kimi K3 architecture diagram": "carry S across
+ * chunks".  Chunks of `chunk` tokens start at every sequence start; the last
+ * chunk of a sequence may be partial.  The result does not depend on `chunk`
+ * beyond rounding.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    int N;                 /* sequences */
+    int H;                 /* heads */
+    int D;                 /* head width (dk = dv = D) */
+    int chunk;             /* 16, 32 or 64 */
+    int64_t T_total;       /* packed tokens */
+    kda_dtype io;          /* dtype of q, k, v, gate and the conv states */
+    kda_dtype out_dtype;   /* dtype of out */
+    const int32_t* cu_seqlens;       /* device [N+1] */
+    const int32_t* cu_seqlens_host;  /* host [N+1] or NULL (then only device-checked) */
+    const void* q;         /* [T_total][qkv_row_stride] raw projections, before the conv */
+    const void* k;         /* same layout as q */
+    const void* v;         /* same layout as q */
+    int64_t qkv_row_stride;/* elements between tokens of q/k/v; 0 means H*D */
+    const float* conv_w;   /* [3][H*D][4] fp32 (q, k, v filter banks) */
+    const void* conv_state_in;  /* [N][3*H*D][3] or NULL (zero left padding) */
+    void* conv_state_out;       /* [N][3*H*D][3] or NULL; must not overlap conv_state_in */
+    const float* g;        /* [T_total][H][D] fp32 log-decay, expected in [-5, 0] */
+    const float* beta;     /* [T_total][H] fp32, expected in [0, 1] */
+    const void* gate;      /* [T_total][H][D] pre-sigmoid output gate, io dtype, or NULL */
+    const float* rms_w;    /* [D] fp32 RMSNorm weight, or NULL (ones) */
+    float eps_l2;          /* typical 1e-6 */
+    float eps_rms;         /* typical 1e-6 */
+    float scale;           /* readout scale, typical 1.0 */
+    const float* initial_state; /* [N][H][D][D] fp32 or NULL (zeros) */
+    float* final_state;    /* [N][H][D][D] fp32 or NULL; may equal initial_state */
+    void* out;             /* [T_total][H][D] out_dtype; must not overlap any input */
+    void* workspace;       /* device scratch, 256-byte aligned, or NULL if size 0 */
+    size_t workspace_bytes;
+    int* d_status;         /* optional device int for device-side conditions */
+    int flags;             /* KDA_FLAG_* */
+} kda_prefill_args;
+
+#define KDA_FLAG_FORCE_SIMT 1 /* take the fp32 SIMT path even where tensor cores apply */
+
+/* Bytes of workspace kda_prefill needs for these arguments (0 allowed). */
+kda_status kda_prefill_workspace_size(const kda_prefill_args* args, size_t* bytes);
+
+kda_status kda_prefill(const kda_prefill_args* args, kda_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * kda_decode_step -- one new token for each of N sequences, states updated
+ * in place.  Page "Kimi K3 / Architecture", panel "KDA short convolution":
+ * "AUTOREGRESSIVE ROLLING STATE, previous 3 values / channel"; page
+ * "Animated Kimi K3 architecture diagram": the four moves on one token.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    int N, H, D;
+    kda_dtype io;          /* dtype of q, k, v, gate and conv_state */
+    kda_dtype out_dtype;   /* dtype of out */
+    const void* q;         /* [N][qkv_row_stride] raw new token, before the conv */
+    const void* k;
+    const void* v;
+    int64_t qkv_row_stride;/* 0 means H*D */
+    const void* gate;      /* [N][H][D] or NULL */
+    const float* g;        /* [N][H][D] */
+    const float* beta;     /* [N][H] */
+    const float* conv_w;   /* [3][H*D][4] */
+    const float* rms_w;    /* [D] or NULL */
+    float eps_l2, eps_rms, scale;
+    float* state;          /* [N][H][D][D] fp32, read and written in place */
+    void* conv_state;      /* [N][3*H*D][3] io dtype, rolled in place */
+    void* out;             /* [N][H][D] out_dtype */
+    int* d_status;
+} kda_decode_args;
+
+kda_status kda_decode_step(const kda_decode_args* args, kda_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

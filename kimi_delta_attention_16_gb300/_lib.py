@@ -1,0 +1,105 @@
+"""ctypes declarations of libkda.so's C ABI (include/kda.h).  Marshalling only."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_WORKSPACE = 3
+KDA_ERR_CUDA = 4
+KDA_ERR_TIMEOUT = 5
+KDA_ERR_DEVICE_ARG = 6
+KDA_BF16 = 0
+KDA_FP32 = 1
+KDA_FLAG_FORCE_SIMT = 1
+
+# Every symbol include/kda.h declares.
+EXPORTED = ("kda_status_string", "kda_last_error", "kda_version", "kda_short_conv",
+            "kda_prefill_workspace_size", "kda_prefill", "kda_decode_step")
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_f = ctypes.c_float
+
+
+class PrefillArgs(ctypes.Structure):
+    """Mirror of kda_prefill_args."""
+    _fields_ = [
+        ("N", _int), ("H", _int), ("D", _int), ("chunk", _int),
+        ("T_total", _i64),
+        ("io", _int), ("out_dtype", _int),
+        ("cu_seqlens", _vp), ("cu_seqlens_host", _vp),
+        ("q", _vp), ("k", _vp), ("v", _vp),
+        ("qkv_row_stride", _i64),
+        ("conv_w", _vp), ("conv_state_in", _vp), ("conv_state_out", _vp),
+        ("g", _vp), ("beta", _vp), ("gate", _vp), ("rms_w", _vp),
+        ("eps_l2", _f), ("eps_rms", _f), ("scale", _f),
+        ("initial_state", _vp), ("final_state", _vp), ("out", _vp),
+        ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+        ("d_status", _vp), ("flags", _int),
+    ]
+
+
+class DecodeArgs(ctypes.Structure):
+    """Mirror of kda_decode_args."""
+    _fields_ = [
+        ("N", _int), ("H", _int), ("D", _int),
+        ("io", _int), ("out_dtype", _int),
+        ("q", _vp), ("k", _vp), ("v", _vp),
+        ("qkv_row_stride", _i64),
+        ("gate", _vp), ("g", _vp), ("beta", _vp), ("conv_w", _vp), ("rms_w", _vp),
+        ("eps_l2", _f), ("eps_rms", _f), ("scale", _f),
+        ("state", _vp), ("conv_state", _vp), ("out", _vp), ("d_status", _vp),
+    ]
+
+
+def lib_path() -> str:
+    return _build.SO
+
+
+def load(auto_build: bool = True) -> ctypes.CDLL:
+    """Loads libkda.so (building it first if it is missing or stale and nvcc exists).
+
+    Raises if the library cannot be produced: there is no fallback path.
+    """
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.SO
+        if auto_build:
+            try:
+                path = _build.build()
+            except RuntimeError:
+                if not os.path.exists(path):
+                    raise
+        if not os.path.exists(path):
+            raise RuntimeError(f"libkda.so is not built ({path}); run kimi_delta_attention_16_gb300.build")
+        lib = ctypes.CDLL(path)
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_status_string.argtypes = [_int]
+        lib.kda_last_error.restype = ctypes.c_char_p
+        lib.kda_last_error.argtypes = []
+        lib.kda_version.restype = _int
+        lib.kda_version.argtypes = []
+        lib.kda_short_conv.restype = _int
+        lib.kda_short_conv.argtypes = [_vp, _i64, _vp, _vp, _vp, _int, _i64, _int, _int, _vp, _vp,
+                                       _vp, _i64, _int, _f, _int, _vp, _vp]
+        lib.kda_prefill_workspace_size.restype = _int
+        lib.kda_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs),
+                                                   ctypes.POINTER(ctypes.c_size_t)]
+        lib.kda_prefill.restype = _int
+        lib.kda_prefill.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
+        lib.kda_decode_step.restype = _int
+        lib.kda_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
+        _lib = lib
+        return lib

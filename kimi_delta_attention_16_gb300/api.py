@@ -1,0 +1,212 @@
+"""PyTorch-facing binding of libkda.so: argument marshalling only.
+
+Every step of the layer runs in the library's CUDA kernels; these functions
+only turn tensors into pointers, sizes and the current stream, allocate
+outputs and workspace with PyTorch (device memory is plumbing), and raise
+``KDAError`` when the library returns a status.  There is no CPU fallback:
+calling these without the built library or without a CUDA device fails.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import numpy as np
+import torch
+
+from . import _lib
+
+_DT = {torch.bfloat16: _lib.KDA_BF16, torch.float32: _lib.KDA_FP32}
+_TORCH = {_lib.KDA_BF16: torch.bfloat16, _lib.KDA_FP32: torch.float32}
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = _lib.load()
+        msg = lib.kda_last_error().decode() or lib.kda_status_string(status).decode()
+        super().__init__(f"{where}: status {status} ({lib.kda_status_string(status).decode()}): {msg}")
+        self.status = status
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _row_stride(t: torch.Tensor, H: int, D: int) -> int:
+    """Row stride (elements) of a [T, H, D] view whose (H, D) block is dense."""
+    if t.dim() != 3 or t.shape[1] != H or t.shape[2] != D:
+        raise ValueError(f"expected [T, {H}, {D}], got {tuple(t.shape)}")
+    if t.shape[0] > 0 and (t.stride(2) != 1 or t.stride(1) != D):
+        raise ValueError("the (H, D) block of each token row must be contiguous")
+    return t.stride(0) if t.shape[0] > 0 else H * D
+
+
+def _cu_pair(cu_seqlens, device) -> Tuple[torch.Tensor, np.ndarray]:
+    """(device int32 tensor, host int32 array) for cu_seqlens given as a tensor, a
+    host sequence, or an already prepared (device tensor, host array) pair (no copy)."""
+    if isinstance(cu_seqlens, tuple):
+        dev, host = cu_seqlens
+        return dev, np.ascontiguousarray(host, dtype=np.int32)
+    if isinstance(cu_seqlens, torch.Tensor):
+        host = cu_seqlens.detach().to("cpu", torch.int32).numpy()
+        dev = cu_seqlens.to(device=device, dtype=torch.int32)
+    else:
+        host = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+        dev = torch.from_numpy(host).to(device)
+    return dev.contiguous(), np.ascontiguousarray(host)
+
+
+def kda_short_conv(x: torch.Tensor, w: torch.Tensor, cu_seqlens, *, H: int, D: int,
+                   conv_state_in: Optional[torch.Tensor] = None,
+                   conv_state_out: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
+                   l2norm_qk: bool = True, eps_l2: float = 1e-6, d_status=None,
+                   check_cu_on_host: bool = True, stream=None) -> torch.Tensor:
+    """Causal width-4 short conv + SiLU (+ L2 on q, k) of [T, 3*H*D] rows (q | k | v)."""
+    lib = _lib.load()
+    io = _DT[x.dtype]
+    T = x.shape[0]
+    if y is None:
+        y = torch.empty((T, 3 * H * D), dtype=x.dtype, device=x.device)
+    cu_dev, cu_host = _cu_pair(cu_seqlens, x.device)
+    N = cu_host.shape[0] - 1
+    st = lib.kda_short_conv(_p(x), x.stride(0) if T else 3 * H * D, _p(w), _p(cu_dev),
+                            cu_host.ctypes.data_as(ctypes.c_void_p) if check_cu_on_host else None,
+                            N, T, H, D, _p(conv_state_in), _p(conv_state_out), _p(y),
+                            y.stride(0) if T else 3 * H * D, int(l2norm_qk), float(eps_l2), io,
+                            _p(d_status), _stream(stream))
+    if st:
+        raise KDAError(st, "kda_short_conv")
+    return y
+
+
+def _prefill_args(q, k, v, conv_w, g, beta, cu_dev, cu_host, *, chunk, gate, rms_w, eps_l2,
+                  eps_rms, scale, initial_state, final_state, conv_state_in, conv_state_out, out,
+                  workspace, d_status, flags, check_cu_on_host):
+    T, H, D = q.shape
+    xs = _row_stride(q, H, D)
+    if _row_stride(k, H, D) != xs or _row_stride(v, H, D) != xs:
+        raise ValueError("q, k and v must share one row stride")
+    a = _lib.PrefillArgs()
+    a.N = cu_host.shape[0] - 1
+    a.H, a.D, a.chunk, a.T_total = H, D, int(chunk), T
+    a.io = _DT[q.dtype]
+    a.out_dtype = _DT[out.dtype] if out is not None else a.io
+    a.cu_seqlens = cu_dev.data_ptr()
+    a.cu_seqlens_host = cu_host.ctypes.data if check_cu_on_host else None
+    a.q, a.k, a.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    a.qkv_row_stride = xs
+    a.conv_w = conv_w.data_ptr()
+    a.conv_state_in = conv_state_in.data_ptr() if conv_state_in is not None else None
+    a.conv_state_out = conv_state_out.data_ptr() if conv_state_out is not None else None
+    a.g, a.beta = g.data_ptr(), beta.data_ptr()
+    a.gate = gate.data_ptr() if gate is not None else None
+    a.rms_w = rms_w.data_ptr() if rms_w is not None else None
+    a.eps_l2, a.eps_rms, a.scale = float(eps_l2), float(eps_rms), float(scale)
+    a.initial_state = initial_state.data_ptr() if initial_state is not None else None
+    a.final_state = final_state.data_ptr() if final_state is not None else None
+    a.out = out.data_ptr() if out is not None else None
+    a.workspace = workspace.data_ptr() if workspace is not None else None
+    a.workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    a.d_status = d_status.data_ptr() if d_status is not None else None
+    a.flags = int(flags)
+    return a
+
+
+def kda_prefill_workspace_size(T_total: int, H: int, D: int, *, chunk: int = 64,
+                               io=torch.bfloat16, flags: int = 0) -> int:
+    lib = _lib.load()
+    a = _lib.PrefillArgs()
+    a.N, a.H, a.D, a.chunk, a.T_total = 1, H, D, chunk, T_total
+    a.io = _DT[io]
+    a.out_dtype = a.io
+    a.flags = flags
+    n = ctypes.c_size_t(0)
+    st = lib.kda_prefill_workspace_size(ctypes.byref(a), ctypes.byref(n))
+    if st:
+        raise KDAError(st, "kda_prefill_workspace_size")
+    return int(n.value)
+
+
+def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, conv_w: torch.Tensor,
+                g: torch.Tensor, beta: torch.Tensor, cu_seqlens, *, chunk: int = 64,
+                gate: Optional[torch.Tensor] = None, rms_w: Optional[torch.Tensor] = None,
+                eps_l2: float = 1e-6, eps_rms: float = 1e-6, scale: float = 1.0,
+                initial_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
+                final_state: Optional[torch.Tensor] = None,
+                conv_state_in: Optional[torch.Tensor] = None,
+                conv_state_out: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                out_dtype=None, workspace: Optional[torch.Tensor] = None, d_status=None,
+                flags: int = 0, check_cu_on_host: bool = True, stream=None):
+    """The whole KDA layer over packed sequences; returns (out, final_state or None).
+
+    q, k, v: [T, H, D] raw projections (bf16 or fp32; rows may be strided views of
+    one fused buffer); conv_w [3, H*D, 4] fp32; g [T, H, D] fp32; beta [T, H] fp32;
+    cu_seqlens [N+1] (tensor or sequence); gate [T, H, D] like q or None;
+    initial_state / final_state [N, H, D, D] fp32; conv states [N, 3*H*D, 3] like q.
+    """
+    lib = _lib.load()
+    T, H, D = q.shape
+    cu_dev, cu_host = _cu_pair(cu_seqlens, q.device)
+    N = cu_host.shape[0] - 1
+    if out is None:
+        out = torch.empty((T, H, D), dtype=out_dtype or q.dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, D, D), dtype=torch.float32, device=q.device)
+    a = _prefill_args(q, k, v, conv_w, g, beta, cu_dev, cu_host, chunk=chunk, gate=gate,
+                      rms_w=rms_w, eps_l2=eps_l2, eps_rms=eps_rms, scale=scale,
+                      initial_state=initial_state, final_state=final_state,
+                      conv_state_in=conv_state_in, conv_state_out=conv_state_out, out=out,
+                      workspace=workspace, d_status=d_status, flags=flags,
+                      check_cu_on_host=check_cu_on_host)
+    if workspace is None:
+        n = ctypes.c_size_t(0)
+        st = lib.kda_prefill_workspace_size(ctypes.byref(a), ctypes.byref(n))
+        if st:
+            raise KDAError(st, "kda_prefill_workspace_size")
+        if n.value:
+            workspace = torch.empty(n.value, dtype=torch.uint8, device=q.device)
+            a.workspace = workspace.data_ptr()
+            a.workspace_bytes = n.value
+    st = lib.kda_prefill(ctypes.byref(a), _stream(stream))
+    if st:
+        raise KDAError(st, "kda_prefill")
+    return out, final_state
+
+
+def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                    beta: torch.Tensor, conv_w: torch.Tensor, state: torch.Tensor,
+                    conv_state: torch.Tensor, *, gate: Optional[torch.Tensor] = None,
+                    rms_w: Optional[torch.Tensor] = None, eps_l2: float = 1e-6,
+                    eps_rms: float = 1e-6, scale: float = 1.0, out: Optional[torch.Tensor] = None,
+                    out_dtype=None, d_status=None, stream=None) -> torch.Tensor:
+    """One decode step for N sequences; state [N,H,D,D] fp32 and conv_state
+    [N,3*H*D,3] are updated in place.  q, k, v, gate: [N, H, D]; g [N,H,D]; beta [N,H]."""
+    lib = _lib.load()
+    N, H, D = q.shape
+    if out is None:
+        out = torch.empty((N, H, D), dtype=out_dtype or q.dtype, device=q.device)
+    a = _lib.DecodeArgs()
+    a.N, a.H, a.D = N, H, D
+    a.io = _DT[q.dtype]
+    a.out_dtype = _DT[out.dtype]
+    xs = _row_stride(q, H, D)
+    if _row_stride(k, H, D) != xs or _row_stride(v, H, D) != xs:
+        raise ValueError("q, k and v must share one row stride")
+    a.q, a.k, a.v = q.data_ptr(), k.data_ptr(), v.data_ptr()
+    a.qkv_row_stride = xs
+    a.gate = gate.data_ptr() if gate is not None else None
+    a.g, a.beta, a.conv_w = g.data_ptr(), beta.data_ptr(), conv_w.data_ptr()
+    a.rms_w = rms_w.data_ptr() if rms_w is not None else None
+    a.eps_l2, a.eps_rms, a.scale = float(eps_l2), float(eps_rms), float(scale)
+    a.state, a.conv_state, a.out = state.data_ptr(), conv_state.data_ptr(), out.data_ptr()
+    a.d_status = d_status.data_ptr() if d_status is not None else None
+    st = lib.kda_decode_step(ctypes.byref(a), _stream(stream))
+    if st:
+        raise KDAError(st, "kda_decode_step")
+    return out

@@ -1,0 +1,118 @@
+// kda_internal.cuh -- device helpers and internal launch declarations shared
+// by the libkda.so translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+using bf16 = __nv_bfloat16;
+
+// ------------------------------------------------------------------ math
+// SiLU and sigmoid through the CUDA math library's expf (no hand-written
+// approximations of library functions).
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float siluf_(float x) { return x / (1.0f + expf(-x)); }
+
+// ------------------------------------------------------------------ scalar I/O
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// ------------------------------------------------------------------ 8-wide vector I/O (16/32 B)
+__device__ __forceinline__ void load8(const float* p, float v[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0];
+    const float4 b = reinterpret_cast<const float4*>(p)[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const bf16* p, float v[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void store8(float* p, const float v[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&t);
+}
+__device__ __forceinline__ void store8(bf16* p, const float v[8]) {
+    uint4 u;
+    u.x = pack_bf16x2(v[0], v[1]);
+    u.y = pack_bf16x2(v[2], v[3]);
+    u.z = pack_bf16x2(v[4], v[5]);
+    u.w = pack_bf16x2(v[6], v[7]);
+    *reinterpret_cast<uint4*>(p) = u;
+}
+
+// ------------------------------------------------------------------ sequences
+// Clamped [start, end) of sequence n: every index stays inside [0, T_total)
+// even when the device copy of cu_seqlens is inconsistent.
+__device__ __forceinline__ void seq_range(const int32_t* cu, int n, int64_t T_total, int64_t& s,
+                                          int64_t& e) {
+    int64_t a = cu[n], b = cu[n + 1];
+    a = a < 0 ? 0 : (a > T_total ? T_total : a);
+    b = b < a ? a : (b > T_total ? T_total : b);
+    s = a;
+    e = b;
+}
+
+__device__ __forceinline__ void flag_status(int* d_status, int code) {
+    if (d_status) atomicMax(d_status, code);
+}
+
+// Base pointers of the q, k and v parts of a token row (they may be offsets
+// into one fused [T][3*H*D] buffer or three separate buffers sharing a row
+// stride).
+struct QKVParts {
+    const void* p[3];
+};
+
+// ------------------------------------------------------------------ internal launchers
+// Each returns cudaSuccess or the launch error; arguments are validated by the caller.
+
+// cu_seqlens consistency check on the device (used when no host copy was given).
+cudaError_t launch_check_cu(const int32_t* cu, int N, int64_t T_total, int* d_status,
+                            cudaStream_t s);
+
+// Conv + SiLU (+ L2 on channels < l2_limit).  x/y rows hold 3*H*D channels.
+cudaError_t launch_short_conv(QKVParts x, int64_t xs, kda_dtype in_dt, const float* w,
+                              const int32_t* cu, int N, int64_t T_total, int H, int D,
+                              const void* cs_in, void* y, int64_t ys, kda_dtype out_dt,
+                              int l2norm_qk, float eps, cudaStream_t s);
+
+// Last three raw inputs of every sequence (rolling conv state for the next call).
+cudaError_t launch_conv_state_out(QKVParts x, int64_t xs, kda_dtype dt, const int32_t* cu,
+                                  int N, int64_t T_total, int n_ch, const void* cs_in,
+                                  void* cs_out, cudaStream_t s);
+
+// fp32 SIMT chunkwise recurrence: reads convolved q|k|v rows (fp32, stride 3*H*D),
+// writes o before the epilogue (fp32 [T][H][D]) and the final state.
+cudaError_t launch_chunk_simt(const float* qkv, const float* g, const float* beta,
+                              const int32_t* cu, int N, int64_t T_total, int H, int D, int chunk,
+                              float scale, const float* S0, float* S_fin, float* o_pre,
+                              cudaStream_t s);
+bool chunk_simt_supported(int D, int chunk);
+
+// RMSNorm + sigmoid gate on fp32 o rows -> out.
+cudaError_t launch_rms_gate(const float* o, int64_t rows, int D, const void* gate,
+                            kda_dtype gate_dt, const float* rms_w, float eps, void* out,
+                            kda_dtype out_dt, cudaStream_t s);
+
+// Single-token decode step.
+cudaError_t launch_decode(const kda_decode_args& a, cudaStream_t s);
+
+}  // namespace kda

@@ -1,0 +1,157 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared
+symbol, and rejects bad arguments with a status before anything is launched.
+
+No GPU is needed: every call below fails host validation, so no CUDA call is
+made.  The pointers are never dereferenced on the host.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from kimi_delta_attention_16_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x7f0000000000  # a 256-byte aligned address that is never dereferenced on the host
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported():
+    lib = _lib.load()
+    names = _declared_functions()
+    assert set(names) == set(_lib.EXPORTED), names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version():
+    lib = _lib.load()
+    assert lib.kda_status_string(0) == b"ok"
+    assert b"workspace" in lib.kda_status_string(_lib.KDA_ERR_WORKSPACE)
+    assert lib.kda_version() >= 10000
+
+
+def _args(**kw):
+    a = _lib.PrefillArgs()
+    a.N, a.H, a.D, a.chunk, a.T_total = 1, 2, 128, 64, 64
+    a.io = a.out_dtype = _lib.KDA_BF16
+    cu = np.array([0, 64], np.int32)
+    a.cu_seqlens = FAKE
+    a.cu_seqlens_host = cu.ctypes.data
+    a.q, a.k, a.v = FAKE, FAKE + 0x100000, FAKE + 0x200000
+    a.qkv_row_stride = 0
+    a.conv_w = FAKE + 0x300000
+    a.g, a.beta, a.out = FAKE + 0x400000, FAKE + 0x500000, FAKE + 0x600000
+    a.eps_l2 = a.eps_rms = 1e-6
+    a.scale = 1.0
+    a.workspace = FAKE + 0x10000000
+    a.workspace_bytes = 1 << 40
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a, cu
+
+
+def _prefill(a):
+    lib = _lib.load()
+    return lib.kda_prefill(ctypes.byref(a), None)
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("D", 48, _lib.KDA_ERR_UNSUPPORTED),
+    ("chunk", 128, _lib.KDA_ERR_UNSUPPORTED),
+    ("io", 7, _lib.KDA_ERR_INVALID_ARG),
+    ("H", 0, _lib.KDA_ERR_INVALID_ARG),
+    ("T_total", 65, _lib.KDA_ERR_INVALID_ARG),       # cu[N] != T_total
+    ("q", None, _lib.KDA_ERR_INVALID_ARG),
+    ("g", None, _lib.KDA_ERR_INVALID_ARG),
+    ("q", FAKE + 2, _lib.KDA_ERR_INVALID_ARG),       # misaligned
+    ("qkv_row_stride", 100, _lib.KDA_ERR_INVALID_ARG),  # < H*D
+    ("qkv_row_stride", 260, _lib.KDA_ERR_INVALID_ARG),  # not a multiple of 8
+    ("workspace", None, _lib.KDA_ERR_WORKSPACE),
+    ("workspace_bytes", 16, _lib.KDA_ERR_WORKSPACE),
+    ("workspace", FAKE + 0x10000010, _lib.KDA_ERR_WORKSPACE),  # not 256-byte aligned
+    ("out", FAKE, _lib.KDA_ERR_INVALID_ARG),         # out aliases q
+])
+def test_prefill_rejects_bad_arguments(field, value, code):
+    a, cu = _args(**{field: value})
+    assert _prefill(a) == code
+    assert _lib.load().kda_last_error()
+
+
+def test_prefill_rejects_bad_host_cu_seqlens():
+    a, _ = _args(N=2)
+    for bad in ([1, 30, 64], [0, 40, 30], [0, 30, 63]):
+        cu = np.array(bad, np.int32)
+        a.cu_seqlens_host = cu.ctypes.data
+        assert _prefill(a) == _lib.KDA_ERR_INVALID_ARG
+
+
+def test_prefill_rejects_aliased_conv_states():
+    a, cu = _args(conv_state_in=FAKE + 0x800000, conv_state_out=FAKE + 0x800000 + 64)
+    assert _prefill(a) == _lib.KDA_ERR_INVALID_ARG
+
+
+def test_prefill_rejects_partially_overlapping_states():
+    a, cu = _args(initial_state=FAKE + 0x20000000, final_state=FAKE + 0x20000000 + 4096)
+    assert _prefill(a) == _lib.KDA_ERR_INVALID_ARG
+
+
+def test_workspace_size_matches_layout():
+    lib = _lib.load()
+    for T, H, D, chunk, flags in [(8192, 96, 128, 64, 1), (64, 2, 16, 16, 0), (0, 4, 32, 32, 0)]:
+        a, cu = _args(T_total=T, H=H, D=D, chunk=chunk, flags=flags)
+        n = ctypes.c_size_t()
+        assert lib.kda_prefill_workspace_size(ctypes.byref(a), ctypes.byref(n)) == 0
+        if flags & _lib.KDA_FLAG_FORCE_SIMT or D != 128:
+            r = lambda x: (x + 255) // 256 * 256  # noqa: E731
+            assert n.value == r(T * 3 * H * D * 4) + r(T * H * D * 4)
+
+
+def test_short_conv_rejects_bad_arguments():
+    lib = _lib.load()
+    cu = np.array([0, 10], np.int32)
+    base = dict(x=FAKE, xs=3 * 2 * 16, w=FAKE + 0x1000, cu=FAKE + 0x2000, cuh=cu.ctypes.data, N=1,
+                T=10, H=2, D=16, csi=None, cso=None, y=FAKE + 0x100000, ys=96, l2=1, eps=1e-6,
+                io=_lib.KDA_BF16)
+
+    def call(**kw):
+        b = dict(base, **kw)
+        return lib.kda_short_conv(b["x"], b["xs"], b["w"], b["cu"], b["cuh"], b["N"], b["T"], b["H"],
+                                  b["D"], b["csi"], b["cso"], b["y"], b["ys"], b["l2"], b["eps"],
+                                  b["io"], None, None)
+
+    assert call(D=24) == _lib.KDA_ERR_UNSUPPORTED
+    assert call(xs=90) == _lib.KDA_ERR_INVALID_ARG
+    assert call(y=FAKE + 8) == _lib.KDA_ERR_INVALID_ARG   # misaligned and overlapping
+    assert call(T=11) == _lib.KDA_ERR_INVALID_ARG         # cu[N] != T
+    assert call(w=None) == _lib.KDA_ERR_INVALID_ARG
+    assert call(csi=FAKE + 0x200000, cso=FAKE + 0x200000) == _lib.KDA_ERR_INVALID_ARG
+
+
+def test_decode_rejects_bad_arguments():
+    lib = _lib.load()
+
+    def call(**kw):
+        a = _lib.DecodeArgs()
+        a.N, a.H, a.D = 4, 2, 128
+        a.io = a.out_dtype = _lib.KDA_BF16
+        a.q, a.k, a.v = FAKE, FAKE + 0x1000, FAKE + 0x2000
+        a.g, a.beta, a.conv_w = FAKE + 0x3000, FAKE + 0x4000, FAKE + 0x5000
+        a.state, a.conv_state, a.out = FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return lib.kda_decode_step(ctypes.byref(a), None)
+
+    assert call(D=100) == _lib.KDA_ERR_UNSUPPORTED
+    assert call(state=None) == _lib.KDA_ERR_INVALID_ARG
+    assert call(state=FAKE + 0x100004) == _lib.KDA_ERR_INVALID_ARG
+    assert call(qkv_row_stride=10) == _lib.KDA_ERR_INVALID_ARG
+    assert call(out=FAKE + 0x100000) == _lib.KDA_ERR_INVALID_ARG
+    assert call(N=-1) == _lib.KDA_ERR_INVALID_ARG

@@ -1,0 +1,92 @@
+"""Parity at the full workload sizes, in the launch configuration the benchmark
+times (default path, chunk 64, bf16 I/O, fp32 state).  The oracle covers
+sampled heads (or sampled (sequence, head) pairs for decode) over the full
+length; that is exact, because every (sequence, head) unit is independent.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kimi_delta_attention_16_gb300 as kda
+from kimi_delta_attention_16_gb300 import synth
+from kda_testlib import TOL_OUT_BF16, TOL_STATE_BF16, check_out, oracle_prefill, per_head_rel, to_np
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+DEV = "cuda"
+
+
+def _run(inp):
+    out, fin = kda.kda_prefill(inp.q, inp.k, inp.v, inp.conv_w, inp.g, inp.beta, inp.cu_seqlens,
+                               chunk=inp.chunk, gate=inp.gate, rms_w=inp.rms_w,
+                               initial_state=inp.initial_state)
+    torch.cuda.synchronize()
+    return out, fin
+
+
+def _compare(inp, out, fin, heads):
+    ref = oracle_prefill(inp, heads=heads)
+    o = to_np(out[:, heads])
+    check_out(o, ref["out"], 1, TOL_OUT_BF16, bf16_out=True)
+    err = per_head_rel(to_np(fin[:, heads]), ref["final_state"], 1)
+    assert err.max() <= TOL_STATE_BF16, f"final state err {err.max():.3e}"
+
+
+def test_layer_8k_all_heads():
+    """B=1, T=8192, H=96, d=128, chunk 64, bf16 q/k/v/gate, fp32 state: every head."""
+    inp = synth.make_prefill("layer_8k", seed=1, device=DEV)
+    out, fin = _run(inp)
+    _compare(inp, out, fin, list(range(inp.H)))
+
+
+def test_varlen_16_sampled_heads():
+    """16 packed sequences, lengths log-uniform in [512, 16384], S0 ~ N(0, 0.02^2)."""
+    inp = synth.make_prefill("varlen_16", seed=2, device=DEV)
+    assert inp.N == 16 and inp.initial_state is not None
+    out, fin = _run(inp)
+    _compare(inp, out, fin, [0, 33, 66, 95])
+
+
+def test_long_1m_sampled_head():
+    """B=1, T=1,048,576, H=24, 16384 chunks of 64: the state carried across every chunk
+    of one sampled head, checked at every position and at the end."""
+    inp = synth.make_prefill("long_1m", seed=3, device=DEV)
+    out, fin = _run(inp)
+    _compare(inp, out, fin, [17])
+
+
+def test_decode_256_sampled_pairs_1000_steps():
+    """256 sequences x 1 token, H=96, d=128, 1000 consecutive steps from a ring of 32
+    step inputs; sampled (sequence, head) pairs checked at every step."""
+    dec = synth.make_decode(seed=4, device=DEV)
+    steps = synth.WORKLOADS["decode_256"]["steps"]
+    pairs = [(0, 0), (17, 5), (128, 47), (255, 95)]
+    ns = torch.tensor([p[0] for p in pairs], device=DEV)
+    hs = torch.tensor([p[1] for p in pairs], device=DEV)
+    st0 = dec.state[ns, hs].clone()                                      # [P, D, D]
+    cs0 = dec.conv_state.view(dec.N, 3, dec.H, dec.D, 3)[ns, :, hs].clone()  # [P, 3, D, 3]
+    rec = torch.empty((steps, len(pairs), dec.D), dtype=torch.bfloat16, device=DEV)
+    out = torch.empty((dec.N, dec.H, dec.D), dtype=torch.bfloat16, device=DEV)
+    R = dec.ring
+    for i in range(steps):
+        j = i % R
+        kda.kda_decode_step(dec.q[j], dec.k[j], dec.v[j], dec.g[j], dec.beta[j], dec.conv_w,
+                            dec.state, dec.conv_state, gate=dec.gate[j], rms_w=dec.rms_w, out=out)
+        rec[i] = out[ns, hs]
+    torch.cuda.synchronize()
+    idx = torch.arange(steps, device=DEV) % R
+    D = dec.D
+    for p, (n, h) in enumerate(pairs):
+        inp = synth.PrefillInputs(
+            N=1, H=1, D=D, chunk=64, io="bf16", cu_seqlens=synth.cu_from_lengths([steps]),
+            q=dec.q[idx, n, h][:, None], k=dec.k[idx, n, h][:, None], v=dec.v[idx, n, h][:, None],
+            conv_w=dec.conv_w.view(3, dec.H, D, 4)[:, h].contiguous(),
+            g=dec.g[idx, n, h][:, None], beta=dec.beta[idx, n, h][:, None],
+            gate=dec.gate[idx, n, h][:, None], rms_w=dec.rms_w,
+            initial_state=st0[p][None, None], conv_state_in=cs0[p].reshape(1, 3 * D, 3))
+        ref = oracle_prefill(inp)
+        check_out(to_np(rec[:, p])[:, None], ref["out"], 1, TOL_OUT_BF16, bf16_out=True)
+        err = per_head_rel(to_np(dec.state[n, h])[None], ref["final_state"][0], 0)
+        assert err.max() <= TOL_STATE_BF16
+        np.testing.assert_array_equal(
+            synth.to_f32_numpy(dec.conv_state.view(dec.N, 3, dec.H, D, 3)[n, :, h]).reshape(-1, 3),
+            ref["conv_state_out"][0].astype(np.float32))
