@@ -355,7 +355,8 @@ def cpu_baseline(inp, workload, tokens=None):
     import oracle
     from kimi_delta_attention_16_gb300 import synth
     import numpy as np
-    n_tok = tokens or min(inp.T, 2048)
+    # the first sequence, capped at 8192 tokens (about 1e11 fp64 flop at H=96, d=128)
+    n_tok = tokens or min(int(inp.cu_seqlens[1]), 8192)
     s = slice(0, n_tok)
     f = synth.to_f32_numpy
     a = dict(q=f(inp.q[s]), k=f(inp.k[s]), v=f(inp.v[s]), conv_w=f(inp.conv_w),
