@@ -20,8 +20,9 @@
  *
  * Conventions for every entry point:
  *  - Ownership: the caller owns every buffer.  The library allocates nothing
- *    on the device and keeps no state between calls except a per-device cache
- *    of kernel attributes.
+ *    on the device.  Its only device memory of its own is the fixed scratch
+ *    array of kda_prefill_noalloc (below), and its only state between calls is
+ *    that array's per-device address.
  *  - Asynchrony: calls only enqueue work on `stream` (a cudaStream_t; NULL is
  *    the legacy default stream) and never synchronise.
  *  - Errors: invalid arguments return before anything is launched.  A launch
@@ -149,6 +150,42 @@ typedef struct {
 kda_status kda_prefill_workspace_size(const kda_prefill_args* args, size_t* bytes);
 
 kda_status kda_prefill(const kda_prefill_args* args, kda_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * kda_prefill_noalloc -- kda_prefill for callers that cannot allocate device
+ * memory when they call it: a plugin inside a host application that owns
+ * every device allocation and hands over only input and output buffers, a
+ * service that reserved its whole memory budget at start-up, or a
+ * latency-critical loop that cannot afford the device-wide synchronisation
+ * of cudaMalloc/cudaFree.  The pages have no counterpart to this entry
+ * point; it is a packaging convenience of this library.
+ *
+ * It runs the fp32 SIMT path (the path that stages data in scratch) with its
+ * scratch taken from a fixed array of KDA_NOALLOC_SCRATCH_BYTES compiled
+ * into the library.  Every GPU that loads the library holds that array
+ * until the process exits.  args->workspace and args->workspace_bytes are
+ * ignored; everything else means what it means for kda_prefill, and the
+ * caller still provides every input and output buffer.  The call allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * Limit: the SIMT path needs 16*T_total*H*D bytes of scratch (two 256-byte
+ * aligned parts); a call needing more than KDA_NOALLOC_SCRATCH_BYTES returns
+ * KDA_ERR_WORKSPACE before launching anything (use kda_prefill with a
+ * workspace instead).
+ *
+ * Set-up: the first call on each device looks up the array's device
+ * address with that device current; later calls reuse it.  Make that first
+ * call before any stream capture begins.
+ *
+ * Sharing: all calls use the same array, which keeps the previous call's
+ * contents.  Nothing in it needs to start at zero (every scratch byte a call
+ * reads is written earlier in the same call).  Calls whose work overlaps on
+ * the GPU (different streams, or host threads without ordering between
+ * them) race on the array: order them on one stream.
+ * ------------------------------------------------------------------------ */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20) /* 64 MiB per device */
+
+kda_status kda_prefill_noalloc(const kda_prefill_args* args, kda_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * kda_decode_step -- one new token for each of N sequences, states updated

@@ -23,7 +23,8 @@ KDA_FLAG_FORCE_SIMT = 1
 
 # Every symbol include/kda.h declares.
 EXPORTED = ("kda_status_string", "kda_last_error", "kda_version", "kda_short_conv",
-            "kda_prefill_workspace_size", "kda_prefill", "kda_decode_step")
+            "kda_prefill_workspace_size", "kda_prefill", "kda_prefill_noalloc", "kda_decode_step")
+NOALLOC_SCRATCH_BYTES = 64 << 20  # KDA_NOALLOC_SCRATCH_BYTES in include/kda.h
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
@@ -99,6 +100,8 @@ def load(auto_build: bool = True) -> ctypes.CDLL:
                                                    ctypes.POINTER(ctypes.c_size_t)]
         lib.kda_prefill.restype = _int
         lib.kda_prefill.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
+        lib.kda_prefill_noalloc.restype = _int
+        lib.kda_prefill_noalloc.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
         lib.kda_decode_step.restype = _int
         lib.kda_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
         _lib = lib

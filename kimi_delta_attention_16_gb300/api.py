@@ -179,6 +179,35 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, conv_w: torch
     return out, final_state
 
 
+def kda_prefill_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, conv_w: torch.Tensor,
+                        g: torch.Tensor, beta: torch.Tensor, cu_seqlens, *, chunk: int = 64,
+                        gate: Optional[torch.Tensor] = None, rms_w: Optional[torch.Tensor] = None,
+                        eps_l2: float = 1e-6, eps_rms: float = 1e-6, scale: float = 1.0,
+                        initial_state: Optional[torch.Tensor] = None,
+                        final_state: Optional[torch.Tensor] = None,
+                        conv_state_in: Optional[torch.Tensor] = None,
+                        conv_state_out: Optional[torch.Tensor] = None,
+                        out: Optional[torch.Tensor] = None, d_status=None, stream=None):
+    """kda_prefill for callers that cannot allocate device memory at call time.
+
+    The caller passes every input and output buffer (``out`` and, if wanted,
+    ``final_state`` are required); the library takes its scratch from a fixed
+    array of ``NOALLOC_SCRATCH_BYTES`` per device and allocates nothing.
+    Problems needing more scratch than that raise KDAError (status 3).
+    """
+    lib = _lib.load()
+    cu_dev, cu_host = _cu_pair(cu_seqlens, q.device)
+    a = _prefill_args(q, k, v, conv_w, g, beta, cu_dev, cu_host, chunk=chunk, gate=gate,
+                      rms_w=rms_w, eps_l2=eps_l2, eps_rms=eps_rms, scale=scale,
+                      initial_state=initial_state, final_state=final_state,
+                      conv_state_in=conv_state_in, conv_state_out=conv_state_out, out=out,
+                      workspace=None, d_status=d_status, flags=0, check_cu_on_host=True)
+    st = lib.kda_prefill_noalloc(ctypes.byref(a), _stream(stream))
+    if st:
+        raise KDAError(st, "kda_prefill_noalloc")
+    return out, final_state
+
+
 def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
                     beta: torch.Tensor, conv_w: torch.Tensor, state: torch.Tensor,
                     conv_state: torch.Tensor, *, gate: Optional[torch.Tensor] = None,

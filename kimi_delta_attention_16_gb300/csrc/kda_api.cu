@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "kda_internal.cuh"
@@ -155,6 +156,33 @@ kda_status validate_prefill(const kda_prefill_args* a) {
     return KDA_OK;
 }
 
+// Fixed scratch of kda_prefill_noalloc (see include/kda.h).  In host code
+// this name is only a host-side stand-in: its device address comes from
+// cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 128;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the fixed scratch on the current device (looked up on first use).
+kda_status noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(KDA_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(fixed scratch)");
+        if (!p) return fail(KDA_ERR_CUDA, "fixed scratch has no device address");
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return KDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -271,6 +299,31 @@ kda_status kda_prefill(const kda_prefill_args* a, kda_stream_t stream) {
                                   a->eps_rms, a->out, a->out_dtype, s)))
         return cuda_fail(e, "epilogue");
     return ok();
+}
+
+kda_status kda_prefill_noalloc(const kda_prefill_args* args, kda_stream_t stream) {
+    if (!args) return fail(KDA_ERR_INVALID_ARG, "args is NULL");
+    kda_prefill_args a = *args;
+    a.flags |= KDA_FLAG_FORCE_SIMT;  // the SIMT path is the one that stages data in scratch
+    a.workspace = nullptr;
+    a.workspace_bytes = 0;
+    if (!supported_d(a.D) || !kda::chunk_simt_supported(a.D, a.chunk))
+        return fail(KDA_ERR_UNSUPPORTED, "unsupported D=%d / chunk=%d", a.D, a.chunk);
+    if (a.T_total < 0 || a.H < 1 || a.N < 0) return fail(KDA_ERR_INVALID_ARG, "bad sizes");
+    const size_t need = plan_prefill(a).total;
+    if (need > KDA_NOALLOC_SCRATCH_BYTES)
+        return fail(KDA_ERR_WORKSPACE,
+                    "kda_prefill_noalloc needs %zu bytes of scratch for T_total=%lld, H=%d, D=%d; "
+                    "its fixed scratch holds %zu bytes (use kda_prefill with a workspace)",
+                    need, (long long)a.T_total, a.H, a.D, (size_t)KDA_NOALLOC_SCRATCH_BYTES);
+    if (need > 0) {
+        void* p = nullptr;
+        kda_status st = noalloc_scratch(&p);
+        if (st) return st;
+        a.workspace = p;
+        a.workspace_bytes = KDA_NOALLOC_SCRATCH_BYTES;
+    }
+    return kda_prefill(&a, stream);
 }
 
 kda_status kda_decode_step(const kda_decode_args* a, kda_stream_t stream) {
