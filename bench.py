@@ -186,6 +186,10 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks, peak_src = load_peaks()
+    if args.mode == "decode":
+        return run_decode_only(args, world, rank, local, pg, dev, peaks, peak_src)
+    if args.mode == "prefill":
+        args.decode_steps = 0
     inp = synth.make_prefill(args.workload, seed=1, device=dev)
     N, T, H, D = inp.N, inp.T, inp.H, inp.D
     path, ws_bytes = prefill_path(inp)
@@ -275,7 +279,7 @@ def run_ours(args):
     dec_launches = 0
     if args.decode_steps > 0:
         del ws
-        dec = synth.make_decode(seed=4, device=dev)
+        dec = synth.make_decode(seed=4, device=dev, N=args.decode_n)
         dout = torch.empty((dec.N, dec.H, dec.D), dtype=torch.bfloat16, device=dev)
 
         def dstep(i):
@@ -336,6 +340,27 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+
+
+def run_decode_only(args, world, rank, local, pg, dev, peaks, peak_src):
+    """Profiling aid: only the decode loop (no JSON line; prints the step time)."""
+    import torch
+    import kimi_delta_attention_16_gb300 as kda
+    from kimi_delta_attention_16_gb300 import synth
+    dec = synth.make_decode(seed=4, device=dev, N=args.decode_n)
+    dout = torch.empty((dec.N, dec.H, dec.D), dtype=torch.bfloat16, device=dev)
+    n = max(args.warmup, 3) + args.decode_steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(n):
+        if i == n - args.decode_steps:
+            e0.record()
+        j = i % dec.ring
+        kda.kda_decode_step(dec.q[j], dec.k[j], dec.v[j], dec.g[j], dec.beta[j], dec.conv_w,
+                            dec.state, dec.conv_state, gate=dec.gate[j], rms_w=dec.rms_w, out=dout)
+    e1.record()
+    torch.cuda.synchronize()
+    if rank == 0:
+        print(f"decode N={dec.N}: {e0.elapsed_time(e1) / max(args.decode_steps, 1):.4f} ms/step")
 
 
 def workload_desc(name):
@@ -416,6 +441,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["layer_8k", "varlen_16", "long_1m"], default="layer_8k")
     ap.add_argument("--decode-steps", type=int, default=1000)
+    ap.add_argument("--decode-n", type=int, default=256, help="decode batch (sequences)")
+    ap.add_argument("--mode", choices=["all", "prefill", "decode"], default="all",
+                    help="profiling aid: run only one of the two measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
