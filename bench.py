@@ -138,12 +138,11 @@ def max_over_ranks(pg, x: float, device) -> float:
 
 # ----------------------------------------------------------------------------- helpers
 
-def kernel_source_hash():
+def kernel_source_hash(files):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "kimi_delta_attention_16_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, name), "rb").read())
+    for name in files:
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -156,7 +155,7 @@ def recorded_traffic(kernel_key: str):
         d = json.load(open(p)).get(kernel_key)
     except (ValueError, OSError):
         return None
-    if not d or d.get("source_hash") != kernel_source_hash():
+    if not d or d.get("source_hash") != kernel_source_hash(d.get("files", [])):
         return None
     return d.get("bytes_per_launch")
 
