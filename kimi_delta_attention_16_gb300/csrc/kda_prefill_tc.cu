@@ -1,14 +1,699 @@
-// kda_prefill_tc.cu -- tensor-core (tcgen05) chunkwise prefill.
+// kda_prefill_tc.cu -- fused KDA prefill on the Blackwell tensor cores
+// (tcgen05, accumulators in tensor memory), D = 128, chunk C = 64, bf16 inputs.
+//
+// Page "Kimi K3 / Architecture", KDA panel: "recurrent across chunks, parallel
+// within a chunk", "dense Tensor Core tiles in the chunkwise form"; page
+// "Animated Kimi K3 architecture diagram": "carry S across chunks".
+//
+// One CTA owns one (sequence, head) and walks its chunks in order; every
+// stage of the layer runs inside it (conv + SiLU + L2, the chunk algebra,
+// the state carry, RMSNorm + gate), so HBM sees only the layer's own inputs
+// and outputs.  Per chunk, with local token index r, G = cumulative log-decay,
+// w = beta e (all per key channel c, value channel j):
+//
+//   G1  [M ; A]  = X1 . B1^T          intra-chunk q.k and beta k.k with decay  (N = 96)
+//   G3  [P ; Q'] = S^T . [KG ; QG]^T  inter-chunk reads of the carried state  (N = 128)
+//   T   = (I + A)^-1                  unit lower triangular, SIMT in shared memory
+//   R   = beta (V - P)
+//   G4  W^T = R^T . T^T                                                       (N = 64)
+//   G5  O^T = Q'^T + W^T . M^T                                                (N = 64)
+//   G6  dS^T = W^T . Kt                                                       (N = 128)
+//   S  <- Diag(e^{G_last}) S + dS ;  y = RMSNorm(scale O) * w * sigmoid(gate)
+//
+// Decay factors e^{G_r - G_i} are split through anchors so that no factor
+// overflows: within each 32-token half the anchor is the half's middle
+// (factors <= e^{80} since the log-decay is bounded below by -5), and the
+// block (second half x first half) uses anchor G_47 on the row side and
+// e^{G_47 - G_i} <= 1 on the column side.  Factors that underflow do so only
+// where the exact product is below e^{-7} of its operands... and it is the
+// operand itself that vanishes, so the lost terms are negligible.
+//
+// Precision: every operand is split into bf16 hi + lo parts and products take
+// hi.hi + lo.hi + hi.lo (T . R takes T in bf16 alone), so each contraction is
+// accurate to about 2^-16 relative; the state stays in fp32 registers.
+//
+// TMEM (512 columns of 128 lanes):
+//   [  0,128)  S^T operand (hi 0-63, lo 64-127)  |  dS^T accumulator
+//   [128,256)  X1 operand (hi, lo)               |  R^T operand (128-191), W accumulator (192-255)
+//   [256,384)  P^T accumulator (256-319), then O^T (320-383)
+//   [384,480)  [M;A] accumulator                 |  W^T operand (384-447)
 #include "kda_tc.cuh"
+#include "kda_tc_ptx.cuh"
 
 namespace kda {
 
-bool tc_prefill_applies(const kda_prefill_args&) { return false; }
+namespace {
+
+using namespace tc;
+
+constexpr int kD = 128;
+constexpr int kC = 64;
+constexpr int kThreads = 256;
+
+// TMEM columns
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColX = 128;
+constexpr uint32_t kColR = 128;
+constexpr uint32_t kColW = 192;
+constexpr uint32_t kColP = 256;
+constexpr uint32_t kColO = 320;
+constexpr uint32_t kColAM = 384;
+constexpr uint32_t kColWop = 384;
+constexpr uint32_t kTmemCols = 512;
+
+// shared memory (bytes from a 1024-aligned base)
+constexpr uint32_t kTileB1 = 96 * 256;   // 96 rows x 128 bf16, K-major
+constexpr uint32_t kTileB3 = 128 * 256;  // 128 rows x 128 bf16, K-major
+constexpr uint32_t kTileKT = 16384;      // 128 (N) x 64 (K) bf16, MN-major
+constexpr uint32_t kKtLbo = 8192, kKtSbo = 1024;
+constexpr uint32_t kOffB1hi = 0;
+constexpr uint32_t kOffB1lo = kOffB1hi + kTileB1;
+constexpr uint32_t kOffB3hi = kOffB1lo + kTileB1;
+constexpr uint32_t kOffB3lo = kOffB3hi + kTileB3;
+constexpr uint32_t kOffKThi = kOffB3lo + kTileB3;
+constexpr uint32_t kOffKTlo = kOffKThi + kTileKT;
+constexpr uint32_t kOffR1 = kOffKTlo + kTileKT;   // G fp32 [64][128]  |  A fp32 [64][64] + T fp32 [64][64]
+constexpr uint32_t kOffR2 = kOffR1 + 32768;        // T bf16 [64][64] | M hi | M lo (K-major, 8 KB each)
+constexpr uint32_t kOffMisc = kOffR2 + 24576;
+// misc (floats)
+constexpr int kMiscConvW = 0;                  // [3][128][4]
+constexpr int kMiscConst = kMiscConvW + 1536;  // [9][128]
+constexpr int kMiscBeta = kMiscConst + 9 * 128;
+constexpr int kMiscSS = kMiscBeta + 64;        // [128 rows][2 halves]
+constexpr int kMiscRed = kMiscSS + 256;        // [4 quadrants][64 tokens]
+constexpr int kMiscInv = kMiscRed + 256;       // [64]
+constexpr int kMiscFloats = kMiscInv + 64;
+constexpr uint32_t kSmemBytes = kOffMisc + kMiscFloats * 4 + 1024;  // + alignment slack
+
+// per-channel constants, rows of sConst
+enum { cA0 = 0, cA1, cE0, cE1, cC2, cC3, cKt0, cKt1, cGam };
+
+__device__ __forceinline__ float ex(float x) { return __expf(x); }
+
+// hi/lo bf16 split of two floats, packed as bf16x2 words (first value in the low half)
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16x2(a, b);
+    const float ah = __uint_as_float(hi << 16), bh = __uint_as_float(hi & 0xffff0000u);
+    lo = pack_bf16x2(a - ah, b - bh);
+}
+
+// 8 floats -> hi and lo 16-byte chunks
+__device__ __forceinline__ void split8(const float v[8], uint4& hi, uint4& lo) {
+    split2(v[0], v[1], hi.x, lo.x);
+    split2(v[2], v[3], hi.y, lo.y);
+    split2(v[4], v[5], hi.z, lo.z);
+    split2(v[6], v[7], hi.w, lo.w);
+}
+
+__device__ __forceinline__ void sts128(uint8_t* base, uint32_t off, const uint4& v) {
+    *reinterpret_cast<uint4*>(base + off) = v;
+}
+
+template <typename To>
+__global__ void __launch_bounds__(kThreads, 1)
+k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16* __restrict__ v,
+             int64_t xs, const float* __restrict__ conv_w, const bf16* __restrict__ cs_in,
+             const float* __restrict__ g, const float* __restrict__ beta,
+             const bf16* __restrict__ gate, const float* __restrict__ rms_w, float eps_l2,
+             float eps_rms, float scale, const float* __restrict__ S0, float* __restrict__ S_fin,
+             To* __restrict__ out, const int32_t* __restrict__ cu, int64_t T_total, int H,
+             int* d_status) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t bars[4];  // G1 done, G3 done, G4 done, G5+G6 done
+    __shared__ uint32_t s_tbase;
+
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    const uint32_t sbase = smem_u32(sm);
+    float* sG = reinterpret_cast<float*>(sm + kOffR1);
+    float* sAf = reinterpret_cast<float*>(sm + kOffR1);           // [64][64]
+    float* sTf = reinterpret_cast<float*>(sm + kOffR1 + 16384);   // [64][64]
+    uint8_t* sTbf = sm + kOffR2;
+    uint8_t* sMhi = sm + kOffR2 + 8192;
+    uint8_t* sMlo = sm + kOffR2 + 16384;
+    float* misc = reinterpret_cast<float*>(sm + kOffMisc);
+    float* sConvW = misc + kMiscConvW;
+    float* sConst = misc + kMiscConst;
+    float* sBeta = misc + kMiscBeta;
+    float* sSS = misc + kMiscSS;
+    float* sRed = misc + kMiscRed;
+    float* sInv = misc + kMiscInv;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qd = warp & 3, hc = warp >> 2;      // TMEM lane quadrant, half (channels or tokens)
+    const int L = qd * 32 + lane;                 // this thread's TMEM lane
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
+    const int h = blockIdx.x % H, n = blockIdx.x / H;
+    const int64_t HD = (int64_t)H * kD;
+    int64_t s0, s1;
+    seq_range(cu, n, T_total, s0, s1);
+
+    if (warp == 0) {
+        tmem_alloc(&s_tbase, kTmemCols);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    for (int idx = tid; idx < 3 * kD * 4; idx += kThreads) {
+        const int part = idx / (kD * 4), rem = idx % (kD * 4);
+        sConvW[idx] = conv_w[(part * HD + (int64_t)h * kD) * 4 + rem];
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tb = s_tbase;
+
+    // ---- carried state: thread (lane j = L, half hc) keeps S[c][j] for c in [64hc, 64hc + 64)
+    const int j = L;
+    float Sreg[64];
+    {
+        const float* src = S0 ? S0 + (((int64_t)n * H + h) * kD) * kD : nullptr;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) Sreg[i] = src ? src[(int64_t)(64 * hc + i) * kD + j] : 0.f;
+    }
+    auto store_state_operand = [&]() {  // S^T hi/lo -> TMEM columns [0,128)
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) split2(Sreg[32 * part + 2 * i], Sreg[32 * part + 2 * i + 1], hi[i], lo[i]);
+            tmem_st16(tb + lane_off + kColS + 32 * hc + 16 * part, hi);
+            tmem_st16(tb + lane_off + kColS + 64 + 32 * hc + 16 * part, lo);
+        }
+        tmem_st_wait();
+    };
+    store_state_operand();
+
+    const uint32_t id_g1 = idesc_bf16(128, 96, false, false);
+    const uint32_t id_g3 = idesc_bf16(128, 128, false, false);
+    const uint32_t id_64 = idesc_bf16(128, 64, false, false);
+    const uint32_t id_g6 = idesc_bf16(128, 128, false, true);
+    bool failed = false;
+    const int n_chunks = (int)((s1 - s0 + kC - 1) / kC);
+
+    for (int ci = 0; ci < n_chunks && !failed; ++ci) {
+        const int64_t t0 = s0 + (int64_t)ci * kC;
+        const int Lc = (int)((s1 - t0) < kC ? (s1 - t0) : kC);
+        const uint32_t par = ci & 1;
+
+        // ------------------------------------------------ A1: G = cumsum(g), beta
+        if (tid < kD) {
+            const int c = tid;
+            float acc = 0.f;
+#pragma unroll 8
+            for (int r = 0; r < kC; ++r) {
+                const float gv = r < Lc ? g[((t0 + r) * H + h) * kD + c] : 0.f;
+                acc += gv;
+                sG[r * kD + c] = acc;
+            }
+        } else if (tid < kD + kC) {
+            const int r = tid - kD;
+            sBeta[r] = r < Lc ? beta[(t0 + r) * H + h] : 0.f;
+        }
+        __syncthreads();
+
+        // ------------------------------------------------ A2: per-channel anchors and factors
+        if (tid < kD) {
+            const int c = tid;
+            const float a0 = sG[15 * kD + c], a1 = sG[47 * kD + c], g31 = sG[31 * kD + c],
+                        gl = sG[63 * kD + c];
+            sConst[cA0 * kD + c] = a0;
+            sConst[cA1 * kD + c] = a1;
+            sConst[cE0 * kD + c] = ex(a0);
+            sConst[cE1 * kD + c] = ex(a1);
+            sConst[cC2 * kD + c] = ex(g31 - a0);
+            sConst[cC3 * kD + c] = ex(a1 - g31);
+            sConst[cKt0 * kD + c] = ex(gl - g31);
+            sConst[cKt1 * kD + c] = ex(gl - a1);
+            sConst[cGam * kD + c] = ex(gl);
+        }
+
+        // ------------------------------------------------ A3a: conv + SiLU of one q or k row (64 channels)
+        const bool isq = L < 64;
+        const int r = L & 63;
+        const bool rvalid = r < Lc;
+        const int c0 = 64 * hc;
+        float x[64];
+        {
+            const bf16* src = isq ? q : k;
+            const int part = isq ? 0 : 1;
+            const int64_t t = t0 + r;
+            float ss = 0.f;
+#pragma unroll
+            for (int g8 = 0; g8 < 8; ++g8) {
+                const int cc = c0 + 8 * g8;
+                float win[4][8];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int64_t p = t - 3 + m;
+                    if (!rvalid) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) win[m][e] = 0.f;
+                    } else if (p >= s0) {
+                        load8(src + p * xs + (int64_t)h * kD + cc, win[m]);
+                    } else {
+                        const int pos = (int)(p - s0);  // -3..-1
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            win[m][e] = cs_in ? to_f(cs_in[((int64_t)n * 3 * HD + part * HD + (int64_t)h * kD + cc + e) * 3 + 3 + pos]) : 0.f;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 w = *reinterpret_cast<const float4*>(&sConvW[(part * kD + cc + e) * 4]);
+                    const float u = w.x * win[0][e] + w.y * win[1][e] + w.z * win[2][e] + w.w * win[3][e];
+                    const float s = rvalid ? siluf_(u) : 0.f;
+                    x[8 * g8 + e] = s;
+                    ss += s * s;
+                }
+            }
+            sSS[L * 2 + hc] = ss;
+        }
+        __syncthreads();
+
+        // ------------------------------------------------ A3b: L2 norm, decay factors, operand tiles
+        {
+            const float inv = 1.0f / sqrtf(sSS[L * 2] + sSS[L * 2 + 1] + eps_l2);
+            const int hr = r >> 5;
+            const float* cA = sConst + (hr ? cA1 : cA0) * kD;
+            const float* cE = sConst + (hr ? cE1 : cE0) * kD;
+            const float bt = sBeta[r];
+#pragma unroll
+            for (int pass = 0; pass < 2; ++pass) {
+            uint32_t xhi[16], xlo[16];
+#pragma unroll
+            for (int gq = 0; gq < 4; ++gq) {
+                const int g8 = 4 * pass + gq;
+                const int cc = c0 + 8 * g8;
+                float xv[8], uu[8], gg[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    xv[e] = x[8 * g8 + e] * inv;
+                    gg[e] = sG[r * kD + cc + e];
+                    uu[e] = ex(gg[e] - cA[cc + e]);
+                }
+                float t8[8];
+                uint4 hi, lo;
+                if (isq) {
+                    // X1 row: q u ; QG row (B3 row 64 + r): q u E_h
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) t8[e] = xv[e] * uu[e];
+                    split8(t8, hi, lo);
+                    xhi[4 * gq + 0] = hi.x; xhi[4 * gq + 1] = hi.y; xhi[4 * gq + 2] = hi.z; xhi[4 * gq + 3] = hi.w;
+                    xlo[4 * gq + 0] = lo.x; xlo[4 * gq + 1] = lo.y; xlo[4 * gq + 2] = lo.z; xlo[4 * gq + 3] = lo.w;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) t8[e] = xv[e] * uu[e] * cE[cc + e];
+                    split8(t8, hi, lo);
+                    sts128(sm, kOffB3hi + kmajor_off(128, 64 + r, cc / 8), hi);
+                    sts128(sm, kOffB3lo + kmajor_off(128, 64 + r, cc / 8), lo);
+                } else {
+                    float vv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) vv[e] = ex(cA[cc + e] - gg[e]);
+                    // X1 row: beta k u
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) t8[e] = bt * xv[e] * uu[e];
+                    split8(t8, hi, lo);
+                    xhi[4 * gq + 0] = hi.x; xhi[4 * gq + 1] = hi.y; xhi[4 * gq + 2] = hi.z; xhi[4 * gq + 3] = hi.w;
+                    xlo[4 * gq + 0] = lo.x; xlo[4 * gq + 1] = lo.y; xlo[4 * gq + 2] = lo.z; xlo[4 * gq + 3] = lo.w;
+                    // B1 row r: k v (anchor of r's own half)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) t8[e] = xv[e] * vv[e];
+                    split8(t8, hi, lo);
+                    sts128(sm, kOffB1hi + kmajor_off(96, r, cc / 8), hi);
+                    sts128(sm, kOffB1lo + kmajor_off(96, r, cc / 8), lo);
+                    // B3 row r: k u E_h  (k e^{G_r})
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) t8[e] = xv[e] * uu[e] * cE[cc + e];
+                    split8(t8, hi, lo);
+                    sts128(sm, kOffB3hi + kmajor_off(128, r, cc / 8), hi);
+                    sts128(sm, kOffB3lo + kmajor_off(128, r, cc / 8), lo);
+                    if (r < 32) {
+                        // B1 row 64 + r: k e^{G_47 - G_r} = k (v c2) c3 ; Kt row r: k (v c2) e^{G_last - G_31}
+                        float w8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) w8[e] = xv[e] * (vv[e] * sConst[cC2 * kD + cc + e]);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) t8[e] = w8[e] * sConst[cC3 * kD + cc + e];
+                        split8(t8, hi, lo);
+                        sts128(sm, kOffB1hi + kmajor_off(96, 64 + r, cc / 8), hi);
+                        sts128(sm, kOffB1lo + kmajor_off(96, 64 + r, cc / 8), lo);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) t8[e] = w8[e] * sConst[cKt0 * kD + cc + e];
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) t8[e] = xv[e] * vv[e] * sConst[cKt1 * kD + cc + e];
+                    }
+                    split8(t8, hi, lo);
+                    sts128(sm, kOffKThi + mnmajor_off(kKtLbo, kKtSbo, cc / 8, r), hi);
+                    sts128(sm, kOffKTlo + mnmajor_off(kKtLbo, kKtSbo, cc / 8, r), lo);
+                }
+            }
+            // X1 row, 32 channels -> TMEM lane L (hi columns 128 + 32hc + 16pass, lo + 64)
+            tmem_st16(tb + lane_off + kColX + 32 * hc + 16 * pass, xhi);
+            tmem_st16(tb + lane_off + kColX + 64 + 32 * hc + 16 * pass, xlo);
+            }
+            tmem_st_wait();
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+
+        // ------------------------------------------------ B: issue G1 ([M;A]) and G3 (state reads)
+        if (tid == 0) {
+            fence_after_sync();
+            const uint32_t b1h = sbase + kOffB1hi, b1l = sbase + kOffB1lo;
+            const uint32_t b3h = sbase + kOffB3hi, b3l = sbase + kOffB3lo;
+#pragma unroll
+            for (int term = 0; term < 3; ++term) {
+                const uint32_t acol = kColX + (term == 1 ? 64 : 0);
+                const uint32_t bt1 = term == 2 ? b1l : b1h;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tb + kColAM, tb + acol + 8 * kk,
+                           desc_sw128(bt1 + (kk >> 2) * 96 * 128 + (kk & 3) * 32, 16, 1024), id_g1,
+                           (term | kk) != 0);
+            }
+            mma_commit(&bars[0]);
+#pragma unroll
+            for (int term = 0; term < 3; ++term) {
+                const uint32_t acol = kColS + (term == 1 ? 64 : 0);
+                const uint32_t bt3 = term == 2 ? b3l : b3h;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tb + kColP, tb + acol + 8 * kk,
+                           desc_sw128(bt3 + (kk >> 2) * 128 * 128 + (kk & 3) * 32, 16, 1024), id_g3,
+                           (term | kk) != 0);
+            }
+            mma_commit(&bars[1]);
+        }
+
+        // ------------------------------------------------ C: M and A from G1, T = (I + A)^-1
+        failed = !__syncthreads_and(mbar_wait(&bars[0], par));
+        if (failed) break;
+        fence_after_sync();
+        {
+            // this thread: row r (q rows -> M, k rows -> A), columns of its half
+            uint32_t dv[32];
+            tmem_ld32(tb + lane_off + kColAM + 32 * hc, dv);  // cols 32hc .. 32hc+31
+            uint32_t dx[32];
+            tmem_ld32(tb + lane_off + kColAM + 64, dx);        // cols 64..95 (i < 32, anchor G_47)
+            tmem_ld_wait();
+            const int hr = r >> 5;
+            float row[32];  // entries for i in [32hc, 32hc + 32)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int i = 32 * hc + e;
+                float val;
+                if (hc == hr) val = __uint_as_float(dv[e]);          // same half
+                else val = __uint_as_float(dx[e]);                   // r in second half, i in first
+                const bool keep = isq ? (i <= r) : (i < r);
+                row[e] = (keep && hc <= hr) ? val : 0.f;
+            }
+            if (isq) {
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    uint4 hi, lo;
+                    float t8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) t8[e] = row[8 * g8 + e];
+                    split8(t8, hi, lo);
+                    sts128(sMhi, kmajor_off(64, r, 4 * hc + g8), hi);
+                    sts128(sMlo, kmajor_off(64, r, 4 * hc + g8), lo);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) sAf[r * 64 + 32 * hc + e] = row[e];
+            }
+        }
+        __syncthreads();
+        // T: unit lower triangular inverse, blocks of 16
+        if (tid < 64) {
+            const int I = tid >> 4, jj = tid & 15, b0 = 16 * I;
+            for (int rr = 0; rr < 16; ++rr) {
+                float t = rr == jj ? 1.f : 0.f;
+                if (rr > jj)
+                    for (int ii = jj; ii < rr; ++ii) t -= sAf[(b0 + rr) * 64 + b0 + ii] * sTf[(b0 + ii) * 64 + b0 + jj];
+                sTf[(b0 + rr) * 64 + b0 + jj] = t;
+            }
+        }
+        __syncthreads();
+        for (int d = 1; d < 4; ++d) {
+            // X_IJ = sum_{K=J}^{I-1} A_IK T_KJ, stored transposed in A's upper triangle
+            for (int idx = tid; idx < (4 - d) * 256; idx += kThreads) {
+                const int J = idx >> 8, I = J + d, rr = (idx >> 4) & 15, jj = idx & 15;
+                float acc = 0.f;
+                for (int K = J; K < I; ++K)
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk)
+                        acc += sAf[(16 * I + rr) * 64 + 16 * K + kk] * sTf[(16 * K + kk) * 64 + 16 * J + jj];
+                sAf[(16 * J + jj) * 64 + 16 * I + rr] = acc;
+            }
+            __syncthreads();
+            for (int idx = tid; idx < (4 - d) * 256; idx += kThreads) {
+                const int J = idx >> 8, I = J + d, rr = (idx >> 4) & 15, jj = idx & 15;
+                float acc = 0.f;
+                for (int kk = 0; kk <= rr; ++kk)
+                    acc += sTf[(16 * I + rr) * 64 + 16 * I + kk] * sAf[(16 * J + jj) * 64 + 16 * I + kk];
+                sTf[(16 * I + rr) * 64 + 16 * J + jj] = -acc;
+            }
+            __syncthreads();
+        }
+        // T -> bf16, K-major [r][i]; the upper triangle is zero
+        for (int idx = tid; idx < 64 * 8; idx += kThreads) {
+            const int rr = idx >> 3, k8 = idx & 7;
+            float t8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int i = 8 * k8 + e;
+                t8[e] = i <= rr ? sTf[rr * 64 + i] : 0.f;
+            }
+            uint4 hv;
+            hv.x = pack_bf16x2(t8[0], t8[1]);
+            hv.y = pack_bf16x2(t8[2], t8[3]);
+            hv.z = pack_bf16x2(t8[4], t8[5]);
+            hv.w = pack_bf16x2(t8[6], t8[7]);
+            sts128(sTbf, kmajor_off(64, rr, k8), hv);
+        }
+        fence_async_smem();
+
+        // ------------------------------------------------ D: v conv, R = beta (V - P)
+        failed = !__syncthreads_and(mbar_wait(&bars[1], par));
+        if (failed) break;
+        fence_after_sync();
+        {
+            const int i0 = 32 * hc;
+            const float4 w = *reinterpret_cast<const float4*>(&sConvW[(2 * kD + j) * 4]);
+            float p0, p1, p2;
+            auto raw = [&](int64_t p) -> float {
+                if (p >= s0) return to_f(v[p * xs + (int64_t)h * kD + j]);
+                const int pos = (int)(p - s0);
+                return cs_in ? to_f(cs_in[((int64_t)n * 3 * HD + 2 * HD + (int64_t)h * kD + j) * 3 + 3 + pos]) : 0.f;
+            };
+            const int64_t tb0 = t0 + i0;
+            p0 = (i0 < Lc) ? raw(tb0 - 3) : 0.f;
+            p1 = (i0 < Lc) ? raw(tb0 - 2) : 0.f;
+            p2 = (i0 < Lc) ? raw(tb0 - 1) : 0.f;
+            uint32_t pv[32];
+            tmem_ld32(tb + lane_off + kColP + i0, pv);
+            tmem_ld_wait();
+            uint32_t rhi[16], rlo[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                float rv[2];
+#pragma unroll
+                for (int f = 0; f < 2; ++f) {
+                    const int i = i0 + e + f;
+                    float xr = 0.f, vr = 0.f;
+                    if (i < Lc) {
+                        xr = to_f(v[(t0 + i) * xs + (int64_t)h * kD + j]);
+                        vr = siluf_(w.x * p0 + w.y * p1 + w.z * p2 + w.w * xr);
+                    }
+                    p0 = p1; p1 = p2; p2 = xr;
+                    rv[f] = sBeta[i] * (vr - __uint_as_float(pv[e + f]));
+                }
+                split2(rv[0], rv[1], rhi[e / 2], rlo[e / 2]);
+            }
+            tmem_st16(tb + lane_off + kColR + 16 * hc, rhi);
+            tmem_st16(tb + lane_off + kColR + 32 + 16 * hc, rlo);
+            tmem_st_wait();
+        }
+        fence_before_sync();
+        __syncthreads();
+
+        // ------------------------------------------------ E: G4  W^T = R^T T^T
+        if (tid == 0) {
+            fence_after_sync();
+            const uint32_t tbf = sbase + kOffR2;
+#pragma unroll
+            for (int term = 0; term < 2; ++term)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ts(tb + kColW, tb + kColR + 32 * term + 8 * kk, desc_sw128(tbf + kk * 32, 16, 1024),
+                           id_64, (term | kk) != 0);
+            mma_commit(&bars[2]);
+        }
+        failed = !__syncthreads_and(mbar_wait(&bars[2], par));
+        if (failed) break;
+        fence_after_sync();
+
+        // ------------------------------------------------ F: W^T -> hi/lo operand
+        {
+            uint32_t wv[32];
+            tmem_ld32(tb + lane_off + kColW + 32 * hc, wv);
+            tmem_ld_wait();
+            uint32_t whi[16], wlo[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                split2(__uint_as_float(wv[2 * e]), __uint_as_float(wv[2 * e + 1]), whi[e], wlo[e]);
+            tmem_st16(tb + lane_off + kColWop + 16 * hc, whi);
+            tmem_st16(tb + lane_off + kColWop + 32 + 16 * hc, wlo);
+            tmem_st_wait();
+        }
+        fence_before_sync();
+        __syncthreads();
+
+        // ------------------------------------------------ G: G5 (O += W M^T), G6 (dS = W^T Kt)
+        if (tid == 0) {
+            fence_after_sync();
+            const uint32_t mh = sbase + kOffR2 + 8192, ml = sbase + kOffR2 + 16384;
+            const uint32_t kth = sbase + kOffKThi, ktl = sbase + kOffKTlo;
+#pragma unroll
+            for (int term = 0; term < 3; ++term) {
+                const uint32_t acol = kColWop + (term == 1 ? 32 : 0);
+                const uint32_t bm = term == 2 ? ml : mh;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ts(tb + kColO, tb + acol + 8 * kk, desc_sw128(bm + kk * 32, 16, 1024), id_64, 1);
+            }
+#pragma unroll
+            for (int term = 0; term < 3; ++term) {
+                const uint32_t acol = kColWop + (term == 1 ? 32 : 0);
+                const uint32_t bk = term == 2 ? ktl : kth;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ts(tb + kColS, tb + acol + 8 * kk, desc_sw128(bk + kk * 2 * kKtSbo, kKtLbo, kKtSbo),
+                           id_g6, (term | kk) != 0);
+            }
+            mma_commit(&bars[3]);
+        }
+        failed = !__syncthreads_and(mbar_wait(&bars[3], par));
+        if (failed) break;
+        fence_after_sync();
+
+        // ------------------------------------------------ H: state update, output epilogue
+        {
+            uint32_t dsv[32];
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                tmem_ld32(tb + lane_off + kColS + 64 * hc + 32 * part, dsv);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int ci2 = 32 * part + e;
+                    Sreg[ci2] = sConst[cGam * kD + 64 * hc + ci2] * Sreg[ci2] + __uint_as_float(dsv[e]);
+                }
+            }
+            uint32_t ov[32];
+            tmem_ld32(tb + lane_off + kColO + 32 * hc, ov);
+            tmem_ld_wait();
+            float o[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = scale * __uint_as_float(ov[e]);
+            // sum over the warp's 32 channels of o^2, for each of its 32 tokens (lane l ends with token l)
+            float sq[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sq[e] = o[e] * o[e];
+#pragma unroll
+            for (int s = 16; s >= 1; s >>= 1) {
+                const bool upper = (lane & s) != 0;
+#pragma unroll
+                for (int i = 0; i < s; ++i) {
+                    const float send = upper ? sq[i] : sq[i + s];
+                    const float keep = upper ? sq[i + s] : sq[i];
+                    sq[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+                }
+            }
+            sRed[qd * 64 + 32 * hc + lane] = sq[0];
+            __syncthreads();
+            if (tid < 64)
+                sInv[tid] = 1.0f / sqrtf((sRed[tid] + sRed[64 + tid] + sRed[128 + tid] + sRed[192 + tid]) / kD + eps_rms);
+            __syncthreads();
+            const float wj = rms_w ? rms_w[j] : 1.f;
+#pragma unroll 4
+            for (int e = 0; e < 32; ++e) {
+                const int rr = 32 * hc + e;
+                if (rr < Lc) {
+                    const int64_t row = (t0 + rr) * H + h;
+                    float yv = o[e] * sInv[rr] * wj;
+                    if (gate) yv *= sigmoidf_(to_f(gate[row * kD + j]));
+                    out[row * kD + j] = from_f<To>(yv);
+                }
+            }
+        }
+        fence_before_sync();
+        __syncthreads();  // every dS read is done before S^T overwrites those columns
+        fence_after_sync();
+        store_state_operand();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+    }
+
+    if (failed) {
+        if (tid == 0) flag_status(d_status, KDA_ERR_TIMEOUT);
+    } else if (S_fin) {
+        float* dst = S_fin + (((int64_t)n * H + h) * kD) * kD;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) dst[(int64_t)(64 * hc + i) * kD + j] = Sreg[i];
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, kTmemCols);
+}
+
+int g_tc_arch[64];  // per device: 0 unknown, 1 supported, 2 not supported
+
+bool device_supports_tc() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (g_tc_arch[dev] == 0) {
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        g_tc_arch[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    }
+    return g_tc_arch[dev] == 1;
+}
+
+template <typename To>
+cudaError_t tc_launch(const kda_prefill_args& a, cudaStream_t s) {
+    auto kern = k_tc_prefill<To>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int64_t xs = a.qkv_row_stride ? a.qkv_row_stride : (int64_t)a.H * a.D;
+    const unsigned grid = (unsigned)((int64_t)a.N * a.H);
+    kern<<<grid, kThreads, kSmemBytes, s>>>(
+        (const bf16*)a.q, (const bf16*)a.k, (const bf16*)a.v, xs, a.conv_w, (const bf16*)a.conv_state_in,
+        a.g, a.beta, (const bf16*)a.gate, a.rms_w, a.eps_l2, a.eps_rms, a.scale, a.initial_state,
+        a.final_state, (To*)a.out, a.cu_seqlens, a.T_total, a.H, a.d_status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_prefill_applies(const kda_prefill_args& a) {
+    return a.D == kD && a.chunk == kC && a.io == KDA_BF16 && (int64_t)a.N * a.H <= 0x7fffffffLL &&
+           device_supports_tc();
+}
 
 size_t tc_prefill_workspace(const kda_prefill_args&) { return 0; }
 
-cudaError_t launch_tc_prefill(const kda_prefill_args&, char*, cudaStream_t) {
-    return cudaErrorNotSupported;
+cudaError_t launch_tc_prefill(const kda_prefill_args& a, char*, cudaStream_t s) {
+    if ((int64_t)a.N * a.H == 0) return cudaSuccess;
+    return a.out_dtype == KDA_FP32 ? tc_launch<float>(a, s) : tc_launch<bf16>(a, s);
 }
 
 }  // namespace kda
