@@ -72,8 +72,11 @@ constexpr uint32_t kOffB3hi = kOffB1lo + kTileB1;
 constexpr uint32_t kOffB3lo = kOffB3hi + kTileB3;
 constexpr uint32_t kOffKThi = kOffB3lo + kTileB3;
 constexpr uint32_t kOffKTlo = kOffKThi + kTileKT;
-constexpr uint32_t kOffR1 = kOffKTlo + kTileKT;   // G fp32 [64][128]  |  A fp32 [64][64] + T fp32 [64][64]
-constexpr uint32_t kOffR2 = kOffR1 + 32768;        // T bf16 [64][64] | M hi | M lo (K-major, 8 KB each)
+constexpr int kGs = 132;   // padded row stride of G (floats): float4 rows, conflict-free row-per-lane reads
+constexpr int kAs = 65;    // padded row stride of A (floats) in the triangular solve
+constexpr uint32_t kOffR1 = kOffKTlo + kTileKT;   // G fp32 [64][132]  |  A fp32 [64][65] + T fp32 [64][64]
+constexpr uint32_t kR1Bytes = 64 * kGs * 4;        // 33792 >= 64*65*4 + 64*64*4
+constexpr uint32_t kOffR2 = kOffR1 + kR1Bytes;     // T bf16 [64][64] | M hi | M lo (K-major, 8 KB each)
 constexpr uint32_t kOffMisc = kOffR2 + 24576;
 // misc (floats)
 constexpr int kMiscConvW = 0;                  // [3][128][4]
@@ -89,6 +92,14 @@ constexpr uint32_t kSmemBytes = kOffMisc + kMiscFloats * 4 + 1024;  // + alignme
 enum { cA0 = 0, cA1, cE0, cE1, cC2, cC3, cKt0, cKt1, cGam };
 
 __device__ __forceinline__ float ex(float x) { return __expf(x); }
+// SiLU and sigmoid through the fast intrinsics (relative error ~1e-6, far inside
+// this path's tolerances); the fp32 SIMT path keeps the IEEE versions.
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // hi/lo bf16 split of two floats, packed as bf16x2 words (first value in the low half)
 __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
@@ -126,8 +137,8 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     uint8_t* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t sbase = smem_u32(sm);
     float* sG = reinterpret_cast<float*>(sm + kOffR1);
-    float* sAf = reinterpret_cast<float*>(sm + kOffR1);           // [64][64]
-    float* sTf = reinterpret_cast<float*>(sm + kOffR1 + 16384);   // [64][64]
+    float* sAf = reinterpret_cast<float*>(sm + kOffR1);                 // [64][kAs]
+    float* sTf = reinterpret_cast<float*>(sm + kOffR1 + 64 * kAs * 4);  // [64][64]
     uint8_t* sTbf = sm + kOffR2;
     uint8_t* sMhi = sm + kOffR2 + 8192;
     uint8_t* sMlo = sm + kOffR2 + 16384;
@@ -198,27 +209,55 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         const int Lc = (int)((s1 - t0) < kC ? (s1 - t0) : kC);
         const uint32_t par = ci & 1;
 
-        // ------------------------------------------------ A1: G = cumsum(g), beta
-        if (tid < kD) {
-            const int c = tid;
-            float acc = 0.f;
-#pragma unroll 8
-            for (int r = 0; r < kC; ++r) {
-                const float gv = r < Lc ? g[((t0 + r) * H + h) * kD + c] : 0.f;
-                acc += gv;
-                sG[r * kD + c] = acc;
+        // ------------------------------------------------ A0: L2 prefetch of the next chunk's rows
+        if (ci + 1 < n_chunks) {
+            const int64_t tn = t0 + kC;
+            const int rr = tid & 63;
+            if (tn + rr < s1) {
+                const int64_t row = tn + rr;
+                const int which = tid >> 6;  // 0 q, 1 k, 2 v, 3 g + gate
+                if (which == 0) prefetch_l2(q + row * xs + (int64_t)h * kD, 256);
+                else if (which == 1) prefetch_l2(k + row * xs + (int64_t)h * kD, 256);
+                else if (which == 2) prefetch_l2(v + row * xs + (int64_t)h * kD, 256);
+                else {
+                    prefetch_l2(g + (row * H + h) * kD, 512);
+                    if (gate) prefetch_l2(gate + (row * H + h) * kD, 256);
+                }
             }
-        } else if (tid < kD + kC) {
-            const int r = tid - kD;
-            sBeta[r] = r < Lc ? beta[(t0 + r) * H + h] : 0.f;
+        }
+
+        // ------------------------------------------------ A1: G = cumsum(g) (two halves of 32 tokens), beta
+        {
+            const int c = tid & (kD - 1), hh = tid >> 7;
+            float gv[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int rr = 32 * hh + e;
+                gv[e] = rr < Lc ? g[((t0 + rr) * H + h) * kD + c] : 0.f;
+            }
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                acc += gv[e];
+                sG[(32 * hh + e) * kGs + c] = acc;
+            }
+            if (hh == 0) sSS[c] = acc;  // first-half total per channel
+            if (tid < kC) sBeta[tid] = tid < Lc ? beta[(t0 + tid) * H + h] : 0.f;
+        }
+        __syncthreads();
+        if (tid >= kD) {
+            const int c = tid - kD;
+            const float base = sSS[c];
+#pragma unroll 8
+            for (int e = 0; e < 32; ++e) sG[(32 + e) * kGs + c] += base;
         }
         __syncthreads();
 
         // ------------------------------------------------ A2: per-channel anchors and factors
         if (tid < kD) {
             const int c = tid;
-            const float a0 = sG[15 * kD + c], a1 = sG[47 * kD + c], g31 = sG[31 * kD + c],
-                        gl = sG[63 * kD + c];
+            const float a0 = sG[15 * kGs + c], a1 = sG[47 * kGs + c], g31 = sG[31 * kGs + c],
+                        gl = sG[63 * kGs + c];
             sConst[cA0 * kD + c] = a0;
             sConst[cA1 * kD + c] = a1;
             sConst[cE0 * kD + c] = ex(a0);
@@ -264,7 +303,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 for (int e = 0; e < 8; ++e) {
                     const float4 w = *reinterpret_cast<const float4*>(&sConvW[(part * kD + cc + e) * 4]);
                     const float u = w.x * win[0][e] + w.y * win[1][e] + w.z * win[2][e] + w.w * win[3][e];
-                    const float s = rvalid ? siluf_(u) : 0.f;
+                    const float s = rvalid ? silu_fast(u) : 0.f;
                     x[8 * g8 + e] = s;
                     ss += s * s;
                 }
@@ -275,7 +314,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
 
         // ------------------------------------------------ A3b: L2 norm, decay factors, operand tiles
         {
-            const float inv = 1.0f / sqrtf(sSS[L * 2] + sSS[L * 2 + 1] + eps_l2);
+            const float inv = rsqrtf(sSS[L * 2] + sSS[L * 2 + 1] + eps_l2);
             const int hr = r >> 5;
             const float* cA = sConst + (hr ? cA1 : cA0) * kD;
             const float* cE = sConst + (hr ? cE1 : cE0) * kD;
@@ -287,12 +326,25 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             for (int gq = 0; gq < 4; ++gq) {
                 const int g8 = 4 * pass + gq;
                 const int cc = c0 + 8 * g8;
-                float xv[8], uu[8], gg[8];
+                float xv[8], uu[8], gg[8], aa[8], EE[8];
+                {
+                    const float4 g0 = *reinterpret_cast<const float4*>(&sG[r * kGs + cc]);
+                    const float4 g1 = *reinterpret_cast<const float4*>(&sG[r * kGs + cc + 4]);
+                    const float4 a0v = *reinterpret_cast<const float4*>(&cA[cc]);
+                    const float4 a1v = *reinterpret_cast<const float4*>(&cA[cc + 4]);
+                    const float4 e0v = *reinterpret_cast<const float4*>(&cE[cc]);
+                    const float4 e1v = *reinterpret_cast<const float4*>(&cE[cc + 4]);
+                    gg[0] = g0.x; gg[1] = g0.y; gg[2] = g0.z; gg[3] = g0.w;
+                    gg[4] = g1.x; gg[5] = g1.y; gg[6] = g1.z; gg[7] = g1.w;
+                    aa[0] = a0v.x; aa[1] = a0v.y; aa[2] = a0v.z; aa[3] = a0v.w;
+                    aa[4] = a1v.x; aa[5] = a1v.y; aa[6] = a1v.z; aa[7] = a1v.w;
+                    EE[0] = e0v.x; EE[1] = e0v.y; EE[2] = e0v.z; EE[3] = e0v.w;
+                    EE[4] = e1v.x; EE[5] = e1v.y; EE[6] = e1v.z; EE[7] = e1v.w;
+                }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     xv[e] = x[8 * g8 + e] * inv;
-                    gg[e] = sG[r * kD + cc + e];
-                    uu[e] = ex(gg[e] - cA[cc + e]);
+                    uu[e] = ex(gg[e] - aa[e]);
                 }
                 float t8[8];
                 uint4 hi, lo;
@@ -304,14 +356,14 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                     xhi[4 * gq + 0] = hi.x; xhi[4 * gq + 1] = hi.y; xhi[4 * gq + 2] = hi.z; xhi[4 * gq + 3] = hi.w;
                     xlo[4 * gq + 0] = lo.x; xlo[4 * gq + 1] = lo.y; xlo[4 * gq + 2] = lo.z; xlo[4 * gq + 3] = lo.w;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) t8[e] = xv[e] * uu[e] * cE[cc + e];
+                    for (int e = 0; e < 8; ++e) t8[e] = xv[e] * uu[e] * EE[e];
                     split8(t8, hi, lo);
                     sts128(sm, kOffB3hi + kmajor_off(128, 64 + r, cc / 8), hi);
                     sts128(sm, kOffB3lo + kmajor_off(128, 64 + r, cc / 8), lo);
                 } else {
                     float vv[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) vv[e] = ex(cA[cc + e] - gg[e]);
+                    for (int e = 0; e < 8; ++e) vv[e] = ex(aa[e] - gg[e]);
                     // X1 row: beta k u
 #pragma unroll
                     for (int e = 0; e < 8; ++e) t8[e] = bt * xv[e] * uu[e];
@@ -326,7 +378,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                     sts128(sm, kOffB1lo + kmajor_off(96, r, cc / 8), lo);
                     // B3 row r: k u E_h  (k e^{G_r})
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) t8[e] = xv[e] * uu[e] * cE[cc + e];
+                    for (int e = 0; e < 8; ++e) t8[e] = xv[e] * uu[e] * EE[e];
                     split8(t8, hi, lo);
                     sts128(sm, kOffB3hi + kmajor_off(128, r, cc / 8), hi);
                     sts128(sm, kOffB3lo + kmajor_off(128, r, cc / 8), lo);
@@ -425,7 +477,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) sAf[r * 64 + 32 * hc + e] = row[e];
+                for (int e = 0; e < 32; ++e) sAf[r * kAs + 32 * hc + e] = row[e];
             }
         }
         __syncthreads();
@@ -435,7 +487,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             for (int rr = 0; rr < 16; ++rr) {
                 float t = rr == jj ? 1.f : 0.f;
                 if (rr > jj)
-                    for (int ii = jj; ii < rr; ++ii) t -= sAf[(b0 + rr) * 64 + b0 + ii] * sTf[(b0 + ii) * 64 + b0 + jj];
+                    for (int ii = jj; ii < rr; ++ii) t -= sAf[(b0 + rr) * kAs + b0 + ii] * sTf[(b0 + ii) * 64 + b0 + jj];
                 sTf[(b0 + rr) * 64 + b0 + jj] = t;
             }
         }
@@ -448,15 +500,15 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 for (int K = J; K < I; ++K)
 #pragma unroll
                     for (int kk = 0; kk < 16; ++kk)
-                        acc += sAf[(16 * I + rr) * 64 + 16 * K + kk] * sTf[(16 * K + kk) * 64 + 16 * J + jj];
-                sAf[(16 * J + jj) * 64 + 16 * I + rr] = acc;
+                        acc += sAf[(16 * I + rr) * kAs + 16 * K + kk] * sTf[(16 * K + kk) * 64 + 16 * J + jj];
+                sAf[(16 * J + jj) * kAs + 16 * I + rr] = acc;
             }
             __syncthreads();
             for (int idx = tid; idx < (4 - d) * 256; idx += kThreads) {
                 const int J = idx >> 8, I = J + d, rr = (idx >> 4) & 15, jj = idx & 15;
                 float acc = 0.f;
                 for (int kk = 0; kk <= rr; ++kk)
-                    acc += sTf[(16 * I + rr) * 64 + 16 * I + kk] * sAf[(16 * J + jj) * 64 + 16 * I + kk];
+                    acc += sTf[(16 * I + rr) * 64 + 16 * I + kk] * sAf[(16 * J + jj) * kAs + 16 * I + kk];
                 sTf[(16 * I + rr) * 64 + 16 * J + jj] = -acc;
             }
             __syncthreads();
@@ -509,7 +561,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                     float xr = 0.f, vr = 0.f;
                     if (i < Lc) {
                         xr = to_f(v[(t0 + i) * xs + (int64_t)h * kD + j]);
-                        vr = siluf_(w.x * p0 + w.y * p1 + w.z * p2 + w.w * xr);
+                        vr = silu_fast(w.x * p0 + w.y * p1 + w.z * p2 + w.w * xr);
                     }
                     p0 = p1; p1 = p2; p2 = xr;
                     rv[f] = sBeta[i] * (vr - __uint_as_float(pv[e + f]));
@@ -619,7 +671,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             sRed[qd * 64 + 32 * hc + lane] = sq[0];
             __syncthreads();
             if (tid < 64)
-                sInv[tid] = 1.0f / sqrtf((sRed[tid] + sRed[64 + tid] + sRed[128 + tid] + sRed[192 + tid]) / kD + eps_rms);
+                sInv[tid] = rsqrtf((sRed[tid] + sRed[64 + tid] + sRed[128 + tid] + sRed[192 + tid]) * (1.0f / kD) + eps_rms);
             __syncthreads();
             const float wj = rms_w ? rms_w[j] : 1.f;
 #pragma unroll 4
@@ -628,7 +680,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 if (rr < Lc) {
                     const int64_t row = (t0 + rr) * H + h;
                     float yv = o[e] * sInv[rr] * wj;
-                    if (gate) yv *= sigmoidf_(to_f(gate[row * kD + j]));
+                    if (gate) yv *= sigmoid_fast(to_f(gate[row * kD + j]));
                     out[row * kD + j] = from_f<To>(yv);
                 }
             }
