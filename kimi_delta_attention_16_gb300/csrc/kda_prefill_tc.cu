@@ -78,6 +78,18 @@ constexpr uint32_t kOffR1 = kOffKTlo + kTileKT;   // G fp32 [64][132]  |  A fp32
 constexpr uint32_t kR1Bytes = 64 * kGs * 4;        // 33792 >= 64*65*4 + 64*64*4
 constexpr uint32_t kOffR2 = kOffR1 + kR1Bytes;     // T bf16 [64][64] | M hi | M lo (K-major, 8 KB each)
 constexpr uint32_t kOffMisc = kOffR2 + 24576;
+// Raw-row staging inside the B1 region while B1 is not an operand:
+//   chunk start .. A3a : q rows and k rows t0-3 .. t0+63 (67 rows each)
+//   after G1 .. H      : v rows t0-3 .. t0+63 and gate rows t0 .. t0+63
+// Rows are padded to 272 bytes so that one-row-per-lane 16-byte reads are conflict-free.
+constexpr uint32_t kRawStride = 272;
+constexpr int kRawRows = kC + 3;
+constexpr uint32_t kOffRawQ = kOffB1hi;
+constexpr uint32_t kOffRawK = kOffB1hi + 18432;
+constexpr uint32_t kOffRawV = kOffB1hi;
+constexpr uint32_t kOffGateT = kOffB1hi + 18432;  // [64][128] bf16, 256-byte rows
+static_assert(kOffRawK + kRawRows * kRawStride <= kOffB3hi, "q/k staging exceeds the B1 region");
+static_assert(kOffGateT + kC * 256 <= kOffB3hi, "gate staging exceeds the B1 region");
 // misc (floats)
 constexpr int kMiscConvW = 0;                  // [3][128][4]
 constexpr int kMiscConst = kMiscConvW + 1536;  // [9][128]
@@ -96,6 +108,12 @@ __device__ __forceinline__ float ex(float x) { return __expf(x); }
 // this path's tolerances); the fp32 SIMT path keeps the IEEE versions.
 __device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 __device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
@@ -209,7 +227,21 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         const int Lc = (int)((s1 - t0) < kC ? (s1 - t0) : kC);
         const uint32_t par = ci & 1;
 
-        // ------------------------------------------------ A0: L2 prefetch of the next chunk's rows
+        // ------------------------------------------------ A0: stage this chunk's q/k rows; L2 prefetch of the next
+        {
+            const int64_t plo = (t0 - 3) > s0 ? (t0 - 3) : s0;
+            const int64_t phi = (t0 + kC) < s1 ? (t0 + kC) : s1;
+            const int nrows = (int)(phi - plo);
+            const int trbase = (int)(plo - (t0 - 3));
+            for (int idx = tid; idx < 2 * nrows * 16; idx += kThreads) {
+                const int part = idx / (nrows * 16), rem = idx % (nrows * 16);
+                const int rr = rem >> 4, vec = rem & 15;
+                const int64_t pr = plo + rr;
+                const bf16* src = (part == 0 ? q : k) + pr * xs + (int64_t)h * kD + 8 * vec;
+                cp_async16(sbase + (part == 0 ? kOffRawQ : kOffRawK) + (trbase + rr) * kRawStride + 16 * vec, src);
+            }
+            cp_async_commit();
+        }
         if (ci + 1 < n_chunks) {
             const int64_t tn = t0 + kC;
             const int rr = tid & 63;
@@ -251,6 +283,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
 #pragma unroll 8
             for (int e = 0; e < 32; ++e) sG[(32 + e) * kGs + c] += base;
         }
+        cp_async_wait_all();
         __syncthreads();
 
         // ------------------------------------------------ A2: per-channel anchors and factors
@@ -276,7 +309,6 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         const int c0 = 64 * hc;
         float x[64];
         {
-            const bf16* src = isq ? q : k;
             const int part = isq ? 0 : 1;
             const int64_t t = t0 + r;
             float ss = 0.f;
@@ -291,7 +323,9 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
 #pragma unroll
                         for (int e = 0; e < 8; ++e) win[m][e] = 0.f;
                     } else if (p >= s0) {
-                        load8(src + p * xs + (int64_t)h * kD + cc, win[m]);
+                        load8(reinterpret_cast<const bf16*>(sm + (isq ? kOffRawQ : kOffRawK) +
+                                                            (uint32_t)(p - (t0 - 3)) * kRawStride + 2 * cc),
+                              win[m]);
                     } else {
                         const int pos = (int)(p - s0);  // -3..-1
 #pragma unroll
@@ -447,6 +481,24 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         if (failed) break;
         fence_after_sync();
         {
+            // G1 is done with B1: stage v rows t0-3 .. t0+63 and gate rows t0 .. t0+Lc-1 there
+            const int64_t plo = (t0 - 3) > s0 ? (t0 - 3) : s0;
+            const int64_t phi = (t0 + kC) < s1 ? (t0 + kC) : s1;
+            const int nv = (int)(phi - plo);
+            const int trbase = (int)(plo - (t0 - 3));
+            for (int idx = tid; idx < nv * 16; idx += kThreads) {
+                const int rr = idx >> 4, vec = idx & 15;
+                cp_async16(sbase + kOffRawV + (trbase + rr) * kRawStride + 16 * vec,
+                           v + (plo + rr) * xs + (int64_t)h * kD + 8 * vec);
+            }
+            if (gate)
+                for (int idx = tid; idx < Lc * 16; idx += kThreads) {
+                    const int rr = idx >> 4, vec = idx & 15;
+                    cp_async16(sbase + kOffGateT + rr * 256 + 16 * vec, gate + ((t0 + rr) * H + h) * kD + 8 * vec);
+                }
+            cp_async_commit();
+        }
+        {
             // this thread: row r (q rows -> M, k rows -> A), columns of its half
             uint32_t dv[32];
             tmem_ld32(tb + lane_off + kColAM + 32 * hc, dv);  // cols 32hc .. 32hc+31
@@ -481,14 +533,22 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             }
         }
         __syncthreads();
-        // T: unit lower triangular inverse, blocks of 16
-        if (tid < 64) {
-            const int I = tid >> 4, jj = tid & 15, b0 = 16 * I;
+        // T: unit lower triangular inverse.  Diagonal 16x16 blocks: one warp per block, lane jj
+        // (lanes 16..31 mirror 0..15) keeps column jj of the block in registers.
+        if (warp < 4) {
+            const int b0 = 16 * warp, jj = lane & 15;
+            float t[16];
+#pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
-                float t = rr == jj ? 1.f : 0.f;
-                if (rr > jj)
-                    for (int ii = jj; ii < rr; ++ii) t -= sAf[(b0 + rr) * kAs + b0 + ii] * sTf[(b0 + ii) * 64 + b0 + jj];
-                sTf[(b0 + rr) * 64 + b0 + jj] = t;
+                float acc = rr == jj ? 1.f : 0.f;
+                const float* arow = sAf + (b0 + rr) * kAs + b0;
+#pragma unroll
+                for (int ii = 0; ii < rr; ++ii) acc -= arow[ii] * t[ii];
+                t[rr] = acc;
+            }
+            if (lane < 16) {
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) sTf[(b0 + rr) * 64 + b0 + jj] = t[rr];
             }
         }
         __syncthreads();
@@ -532,6 +592,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         fence_async_smem();
 
         // ------------------------------------------------ D: v conv, R = beta (V - P)
+        cp_async_wait_all();
         failed = !__syncthreads_and(mbar_wait(&bars[1], par));
         if (failed) break;
         fence_after_sync();
@@ -539,8 +600,9 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             const int i0 = 32 * hc;
             const float4 w = *reinterpret_cast<const float4*>(&sConvW[(2 * kD + j) * 4]);
             float p0, p1, p2;
+            const bf16* vt = reinterpret_cast<const bf16*>(sm + kOffRawV);
             auto raw = [&](int64_t p) -> float {
-                if (p >= s0) return to_f(v[p * xs + (int64_t)h * kD + j]);
+                if (p >= s0) return to_f(vt[(uint32_t)(p - (t0 - 3)) * (kRawStride / 2) + j]);
                 const int pos = (int)(p - s0);
                 return cs_in ? to_f(cs_in[((int64_t)n * 3 * HD + 2 * HD + (int64_t)h * kD + j) * 3 + 3 + pos]) : 0.f;
             };
@@ -560,7 +622,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                     const int i = i0 + e + f;
                     float xr = 0.f, vr = 0.f;
                     if (i < Lc) {
-                        xr = to_f(v[(t0 + i) * xs + (int64_t)h * kD + j]);
+                        xr = to_f(vt[(uint32_t)(i + 3) * (kRawStride / 2) + j]);
                         vr = silu_fast(w.x * p0 + w.y * p1 + w.z * p2 + w.w * xr);
                     }
                     p0 = p1; p1 = p2; p2 = xr;
@@ -643,9 +705,13 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 tmem_ld32(tb + lane_off + kColS + 64 * hc + 32 * part, dsv);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
+                for (int e = 0; e < 32; e += 4) {
                     const int ci2 = 32 * part + e;
-                    Sreg[ci2] = sConst[cGam * kD + 64 * hc + ci2] * Sreg[ci2] + __uint_as_float(dsv[e]);
+                    const float4 gm = *reinterpret_cast<const float4*>(&sConst[cGam * kD + 64 * hc + ci2]);
+                    Sreg[ci2 + 0] = gm.x * Sreg[ci2 + 0] + __uint_as_float(dsv[e + 0]);
+                    Sreg[ci2 + 1] = gm.y * Sreg[ci2 + 1] + __uint_as_float(dsv[e + 1]);
+                    Sreg[ci2 + 2] = gm.z * Sreg[ci2 + 2] + __uint_as_float(dsv[e + 2]);
+                    Sreg[ci2 + 3] = gm.w * Sreg[ci2 + 3] + __uint_as_float(dsv[e + 3]);
                 }
             }
             uint32_t ov[32];
@@ -674,20 +740,29 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 sInv[tid] = rsqrtf((sRed[tid] + sRed[64 + tid] + sRed[128 + tid] + sRed[192 + tid]) * (1.0f / kD) + eps_rms);
             __syncthreads();
             const float wj = rms_w ? rms_w[j] : 1.f;
-#pragma unroll 4
+            const bf16* gt = reinterpret_cast<const bf16*>(sm + kOffGateT);
+            To* yt = reinterpret_cast<To*>(sm + kOffR1);  // [64][128] y tile (R1 is free after the solve)
+#pragma unroll 8
             for (int e = 0; e < 32; ++e) {
                 const int rr = 32 * hc + e;
-                if (rr < Lc) {
-                    const int64_t row = (t0 + rr) * H + h;
-                    float yv = o[e] * sInv[rr] * wj;
-                    if (gate) yv *= sigmoid_fast(to_f(gate[row * kD + j]));
-                    out[row * kD + j] = from_f<To>(yv);
-                }
+                float yv = o[e] * sInv[rr] * wj;
+                if (gate) yv *= sigmoid_fast(to_f(gt[rr * kD + j]));
+                yt[rr * kD + j] = from_f<To>(yv);
             }
         }
         fence_before_sync();
-        __syncthreads();  // every dS read is done before S^T overwrites those columns
+        __syncthreads();  // every dS read is done before S^T overwrites those columns; y tile complete
         fence_after_sync();
+        {
+            // y rows -> out, 16-byte coalesced stores
+            constexpr int kVpr = kD * (int)sizeof(To) / 16;
+            const uint4* yt = reinterpret_cast<const uint4*>(sm + kOffR1);
+            for (int idx = tid; idx < Lc * kVpr; idx += kThreads) {
+                const int rr = idx / kVpr, vec = idx % kVpr;
+                *reinterpret_cast<uint4*>(out + ((t0 + rr) * H + h) * kD + vec * (16 / (int)sizeof(To))) =
+                    yt[rr * kVpr + vec];
+            }
+        }
         store_state_operand();
         fence_before_sync();
         __syncthreads();
