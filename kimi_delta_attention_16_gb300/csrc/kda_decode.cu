@@ -17,6 +17,7 @@
 // S^T q) go through shared memory.  The kernel is HBM-bound: the state's
 // read + write is more than 95% of the bytes of a step.
 #include "kda_internal.cuh"
+#include "kda_tc_ptx.cuh"
 
 namespace kda {
 
@@ -40,8 +41,9 @@ k_decode(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __rest
          float* __restrict__ state, Tio* __restrict__ conv_state, To* __restrict__ out) {
     using Sh = DecodeShape<D>;
     constexpr int NT = Sh::NT, TPR = Sh::TPR, RG = Sh::RG, RPT = Sh::RPT;
-    __shared__ float sx[3][D];        // convolved q, k, v of this head
-    __shared__ float sred[RG][D];     // partial sums over row groups
+    // float4 accesses below: static shared arrays need an explicit 16-byte alignment
+    __shared__ __align__(16) float sx[3][D];     // convolved q, k, v of this head
+    __shared__ __align__(16) float sred[RG][D];  // partial sums over row groups
     __shared__ float sinv[2];         // 1/|q|, 1/|k|
 
     const int nh = blockIdx.x;        // n * H + h
@@ -159,6 +161,228 @@ k_decode(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __rest
     }
 }
 
+
+// ---------------------------------------------------------------------------------------
+// Pipelined decode for D = 128: persistent CTAs (one per SM) walk units (sequence, head)
+// with a 3-stage pipeline of 1D bulk copies (the TMA engine).  A unit's 64 KB state slice,
+// its three conv-state segments, raw q/k/v, gate and log-decay arrive in shared memory
+// two units ahead of the compute; the updated state and conv state leave with bulk
+// stores, so HBM always has loads and stores in flight while the SM computes.
+template <typename Tio>
+struct DecodeStage {
+    static constexpr uint32_t kState = 0;
+    static constexpr uint32_t kConv = 65536;                               // [3][128][3]
+    static constexpr uint32_t kConvPart = 128 * 3 * sizeof(Tio);
+    static constexpr uint32_t kRaw = kConv + 3 * kConvPart;                // [3][128]
+    static constexpr uint32_t kRawPart = 128 * sizeof(Tio);
+    static constexpr uint32_t kGate = kRaw + 3 * kRawPart;                 // [128]
+    static constexpr uint32_t kG = kGate + 128 * sizeof(Tio);              // [128] fp32
+    static constexpr uint32_t kBytes = (kG + 512 + 127) / 128 * 128;
+    static constexpr int kStages = 3;
+    static constexpr uint32_t kSmem = kStages * kBytes + 128;
+};
+
+template <typename Tio, typename To>
+__global__ void __launch_bounds__(256, 1)
+k_decode_tma(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __restrict__ v, int64_t xs,
+             const Tio* __restrict__ gate, const float* __restrict__ g, const float* __restrict__ beta,
+             const float* __restrict__ conv_w, const float* __restrict__ rms_w, float eps_l2,
+             float eps_rms, float scale, int H, int units, float* __restrict__ state,
+             Tio* __restrict__ conv_state, To* __restrict__ out, int* d_status) {
+    using St = DecodeStage<Tio>;
+    constexpr int D = 128;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t bars[St::kStages];
+    __shared__ __align__(16) float sx[3][D];
+    __shared__ __align__(16) float sred[8][D];  // float4 accesses: explicit 16-byte alignment
+    __shared__ float sinv[2];
+    const uint32_t raw_addr = tc::smem_u32(smem_raw);
+    uint8_t* sm = smem_raw + (((raw_addr + 127u) & ~127u) - raw_addr);
+    const uint32_t sbase = tc::smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t HD = (int64_t)H * D;
+    const int first = blockIdx.x, stride = gridDim.x;
+    const int my_units = first < units ? (units - first + stride - 1) / stride : 0;
+    const uint32_t tx_bytes = 65536 + 3 * St::kConvPart + 3 * St::kRawPart + (gate ? St::kRawPart : 0) + 512;
+
+    if (tid == 0) {
+        for (int i = 0; i < St::kStages; ++i) tc::mbar_init(&bars[i], 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto issue = [&](int i) {  // bulk loads of this CTA's i-th unit
+        const int u = first + i * stride, b = i % St::kStages;
+        const int n = u / H, h = u % H;
+        const uint32_t st = sbase + b * St::kBytes;
+        tc::mbar_expect_tx(&bars[b], tx_bytes);
+        tc::bulk_load(st + St::kState, state + (int64_t)u * D * D, 65536, &bars[b]);
+        const Tio* src[3] = {q, k, v};
+#pragma unroll
+        for (int p = 0; p < 3; ++p) {
+            tc::bulk_load(st + St::kConv + p * St::kConvPart,
+                          conv_state + (((int64_t)n * 3 + p) * HD + (int64_t)h * D) * 3, St::kConvPart, &bars[b]);
+            tc::bulk_load(st + St::kRaw + p * St::kRawPart, src[p] + (int64_t)n * xs + (int64_t)h * D,
+                          St::kRawPart, &bars[b]);
+        }
+        if (gate) tc::bulk_load(st + St::kGate, gate + (int64_t)u * D, St::kRawPart, &bars[b]);
+        tc::bulk_load(st + St::kG, g + (int64_t)u * D, 512, &bars[b]);
+    };
+    if (tid == 0)
+        for (int i = 0; i < St::kStages - 1 && i < my_units; ++i) issue(i);
+
+    const int cg = lane, rg = warp;  // 4 columns 4cg.., 16 rows 16rg..
+    const int c0 = 4 * cg, r0 = 16 * rg;
+    bool failed = false;
+    for (int i = 0; i < my_units; ++i) {
+        const int b = i % St::kStages;
+        const int u = first + i * stride, n = u / H, h = u % H;
+        uint8_t* st = sm + b * St::kBytes;
+        if (!__syncthreads_and(tc::mbar_wait(&bars[b], (i / St::kStages) & 1))) {
+            failed = true;
+            break;
+        }
+        float* S = reinterpret_cast<float*>(st + St::kState);
+        Tio* cs = reinterpret_cast<Tio*>(st + St::kConv);
+        const Tio* xr = reinterpret_cast<const Tio*>(st + St::kRaw);
+        // conv + SiLU on the new token; the rolled conv state stays in the stage for the store
+        for (int idx = tid; idx < 3 * D; idx += 256) {
+            const int part = idx >> 7, d = idx & (D - 1);
+            Tio* c3 = cs + (part * D + d) * 3;
+            const float x0 = to_f(c3[0]), x1 = to_f(c3[1]), x2 = to_f(c3[2]);
+            const Tio xn = xr[part * D + d];
+            const float4 w = *reinterpret_cast<const float4*>(conv_w + (part * HD + (int64_t)h * D + d) * 4);
+            const float uu = w.x * x0 + w.y * x1 + w.z * x2 + w.w * to_f(xn);
+            c3[0] = c3[1];
+            c3[1] = c3[2];
+            c3[2] = xn;
+            sx[part][d] = siluf_(uu);
+        }
+        __syncthreads();
+        if (warp < 2) {
+            float ss = 0.f;
+#pragma unroll
+            for (int d = lane; d < D; d += 32) ss += sx[warp][d] * sx[warp][d];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            if (lane == 0) sinv[warp] = 1.0f / sqrtf(ss + eps_l2);
+        }
+        __syncthreads();
+        const float iq = sinv[0], ik = sinv[1];
+        const float* gr = reinterpret_cast<const float*>(st + St::kG);
+        float4 s[16];
+        float kr[16], qr[16];
+        float4 p = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            s[e] = *reinterpret_cast<const float4*>(S + (r0 + e) * D + c0);
+            const float a = expf(gr[r0 + e]);
+            kr[e] = sx[1][r0 + e] * ik;
+            qr[e] = sx[0][r0 + e] * iq;
+            s[e].x *= a; s[e].y *= a; s[e].z *= a; s[e].w *= a;
+            p.x = fmaf(kr[e], s[e].x, p.x); p.y = fmaf(kr[e], s[e].y, p.y);
+            p.z = fmaf(kr[e], s[e].z, p.z); p.w = fmaf(kr[e], s[e].w, p.w);
+        }
+        *reinterpret_cast<float4*>(&sred[rg][c0]) = p;
+        __syncthreads();
+        float4 ev = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) {
+            const float4 t = *reinterpret_cast<const float4*>(&sred[rr][c0]);
+            ev.x += t.x; ev.y += t.y; ev.z += t.z; ev.w += t.w;
+        }
+        ev.x = sx[2][c0] - ev.x; ev.y = sx[2][c0 + 1] - ev.y; ev.z = sx[2][c0 + 2] - ev.z; ev.w = sx[2][c0 + 3] - ev.w;
+        const float bb = beta[u];
+        float4 po = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const float bk = bb * kr[e];
+            s[e].x = fmaf(bk, ev.x, s[e].x); s[e].y = fmaf(bk, ev.y, s[e].y);
+            s[e].z = fmaf(bk, ev.z, s[e].z); s[e].w = fmaf(bk, ev.w, s[e].w);
+            *reinterpret_cast<float4*>(S + (r0 + e) * D + c0) = s[e];
+            po.x = fmaf(qr[e], s[e].x, po.x); po.y = fmaf(qr[e], s[e].y, po.y);
+            po.z = fmaf(qr[e], s[e].z, po.z); po.w = fmaf(qr[e], s[e].w, po.w);
+        }
+        __syncthreads();  // everyone has read sred for e
+        *reinterpret_cast<float4*>(&sred[rg][c0]) = po;
+        tc::fence_async_smem();  // state and conv-state updates -> visible to the bulk store
+        __syncthreads();
+        if (tid == 0) {
+            tc::bulk_store(state + (int64_t)u * D * D, sbase + b * St::kBytes + St::kState, 65536);
+#pragma unroll
+            for (int pp = 0; pp < 3; ++pp)
+                tc::bulk_store(conv_state + (((int64_t)n * 3 + pp) * HD + (int64_t)h * D) * 3,
+                               sbase + b * St::kBytes + St::kConv + pp * St::kConvPart, St::kConvPart);
+            tc::bulk_commit();
+            if (i + St::kStages - 1 < my_units) {
+                tc::bulk_wait_read<1>();  // the store of the unit before this one has left its buffer
+                issue(i + St::kStages - 1);
+            }
+        }
+        if (rg == 0) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr) {
+                const float4 t = *reinterpret_cast<const float4*>(&sred[rr][c0]);
+                acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
+            }
+            const float o[4] = {scale * acc.x, scale * acc.y, scale * acc.z, scale * acc.w};
+            float ss = o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float inv = 1.0f / sqrtf(ss / D + eps_rms);
+            const Tio* gt = gate ? reinterpret_cast<const Tio*>(st + St::kGate) + c0 : nullptr;
+            To* dst = out + (int64_t)u * D + c0;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                float y = o[m] * inv;
+                if (rms_w) y *= rms_w[c0 + m];
+                if (gt) y *= sigmoidf_(to_f(gt[m]));
+                dst[m] = from_f<To>(y);
+            }
+        }
+    }
+    if (tid == 0) {
+        tc::bulk_wait_all();
+        if (failed) flag_status(d_status, KDA_ERR_TIMEOUT);
+    }
+    __syncthreads();
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int g_sm_count[64];
+
+template <typename Tio, typename To>
+cudaError_t decode_tma_launch(const kda_decode_args& a, cudaStream_t s) {
+    using St = DecodeStage<Tio>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && g_sm_count[dev] == 0)
+        cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    const int sms = (dev >= 0 && dev < 64 && g_sm_count[dev] > 0) ? g_sm_count[dev] : 148;
+    const int units = a.N * a.H;
+    auto kern = k_decode_tma<Tio, To>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)St::kSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t xs = a.qkv_row_stride ? a.qkv_row_stride : (int64_t)a.H * 128;
+    kern<<<units < sms ? units : sms, 256, St::kSmem, s>>>(
+        (const Tio*)a.q, (const Tio*)a.k, (const Tio*)a.v, xs, (const Tio*)a.gate, a.g, a.beta, a.conv_w,
+        a.rms_w, a.eps_l2, a.eps_rms, a.scale, a.H, units, a.state, (Tio*)a.conv_state, (To*)a.out,
+        a.d_status);
+    return cudaGetLastError();
+}
+
+template <typename Tio>
+bool decode_tma_ok(const kda_decode_args& a) {
+    const int64_t xs = a.qkv_row_stride ? a.qkv_row_stride : (int64_t)a.H * 128;
+    return a.D == 128 && (xs * (int64_t)sizeof(Tio)) % 16 == 0 && aligned16(a.q) && aligned16(a.k) &&
+           aligned16(a.v) && aligned16(a.g) && aligned16(a.state) && aligned16(a.conv_state) &&
+           aligned16(a.conv_w) &&
+           (!a.gate || aligned16(a.gate)) && (int64_t)a.N * a.H < 0x7fffffffLL;
+}
+
 template <int D, typename Tio, typename To>
 cudaError_t decode_launch(const kda_decode_args& a, cudaStream_t s) {
     const int64_t xs = a.qkv_row_stride ? a.qkv_row_stride : (int64_t)a.H * D;
@@ -173,6 +397,10 @@ cudaError_t decode_launch(const kda_decode_args& a, cudaStream_t s) {
 
 template <int D>
 cudaError_t decode_dt(const kda_decode_args& a, cudaStream_t s) {
+    if (D == 128 && a.io == KDA_BF16 && decode_tma_ok<bf16>(a))
+        return a.out_dtype == KDA_FP32 ? decode_tma_launch<bf16, float>(a, s) : decode_tma_launch<bf16, bf16>(a, s);
+    if (D == 128 && a.io == KDA_FP32 && decode_tma_ok<float>(a))
+        return a.out_dtype == KDA_FP32 ? decode_tma_launch<float, float>(a, s) : decode_tma_launch<float, bf16>(a, s);
     if (a.io == KDA_BF16 && a.out_dtype == KDA_BF16) return decode_launch<D, bf16, bf16>(a, s);
     if (a.io == KDA_BF16 && a.out_dtype == KDA_FP32) return decode_launch<D, bf16, float>(a, s);
     if (a.io == KDA_FP32 && a.out_dtype == KDA_FP32) return decode_launch<D, float, float>(a, s);

@@ -229,16 +229,14 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
 
         // ------------------------------------------------ A0: stage this chunk's q/k rows; L2 prefetch of the next
         {
-            const int64_t plo = (t0 - 3) > s0 ? (t0 - 3) : s0;
-            const int64_t phi = (t0 + kC) < s1 ? (t0 + kC) : s1;
-            const int nrows = (int)(phi - plo);
-            const int trbase = (int)(plo - (t0 - 3));
-            for (int idx = tid; idx < 2 * nrows * 16; idx += kThreads) {
-                const int part = idx / (nrows * 16), rem = idx % (nrows * 16);
-                const int rr = rem >> 4, vec = rem & 15;
-                const int64_t pr = plo + rr;
-                const bf16* src = (part == 0 ? q : k) + pr * xs + (int64_t)h * kD + 8 * vec;
-                cp_async16(sbase + (part == 0 ? kOffRawQ : kOffRawK) + (trbase + rr) * kRawStride + 16 * vec, src);
+            for (int idx = tid; idx < 2 * kRawRows * 16; idx += kThreads) {
+                const int part = idx >= kRawRows * 16 ? 1 : 0;
+                const int rem = idx - part * kRawRows * 16;
+                const int tr = rem >> 4, vec = rem & 15;
+                const int64_t pr = t0 - 3 + tr;
+                if (pr >= s0 && pr < s1)
+                    cp_async16(sbase + (part ? kOffRawK : kOffRawQ) + tr * kRawStride + 16 * vec,
+                               (part ? k : q) + pr * xs + (int64_t)h * kD + 8 * vec);
             }
             cp_async_commit();
         }
@@ -416,21 +414,31 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                     split8(t8, hi, lo);
                     sts128(sm, kOffB3hi + kmajor_off(128, r, cc / 8), hi);
                     sts128(sm, kOffB3lo + kmajor_off(128, r, cc / 8), lo);
+                    auto ld8 = [&](int row, float (&d)[8]) {
+                        const float4 a = *reinterpret_cast<const float4*>(&sConst[row * kD + cc]);
+                        const float4 b = *reinterpret_cast<const float4*>(&sConst[row * kD + cc + 4]);
+                        d[0] = a.x; d[1] = a.y; d[2] = a.z; d[3] = a.w; d[4] = b.x; d[5] = b.y; d[6] = b.z; d[7] = b.w;
+                    };
                     if (r < 32) {
                         // B1 row 64 + r: k e^{G_47 - G_r} = k (v c2) c3 ; Kt row r: k (v c2) e^{G_last - G_31}
-                        float w8[8];
+                        float w8[8], cst[8];
+                        ld8(cC2, cst);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) w8[e] = xv[e] * (vv[e] * sConst[cC2 * kD + cc + e]);
+                        for (int e = 0; e < 8; ++e) w8[e] = xv[e] * (vv[e] * cst[e]);
+                        ld8(cC3, cst);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) t8[e] = w8[e] * sConst[cC3 * kD + cc + e];
+                        for (int e = 0; e < 8; ++e) t8[e] = w8[e] * cst[e];
                         split8(t8, hi, lo);
                         sts128(sm, kOffB1hi + kmajor_off(96, 64 + r, cc / 8), hi);
                         sts128(sm, kOffB1lo + kmajor_off(96, 64 + r, cc / 8), lo);
+                        ld8(cKt0, cst);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) t8[e] = w8[e] * sConst[cKt0 * kD + cc + e];
+                        for (int e = 0; e < 8; ++e) t8[e] = w8[e] * cst[e];
                     } else {
+                        float cst[8];
+                        ld8(cKt1, cst);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) t8[e] = xv[e] * vv[e] * sConst[cKt1 * kD + cc + e];
+                        for (int e = 0; e < 8; ++e) t8[e] = xv[e] * vv[e] * cst[e];
                     }
                     split8(t8, hi, lo);
                     sts128(sm, kOffKThi + mnmajor_off(kKtLbo, kKtSbo, cc / 8, r), hi);
@@ -482,19 +490,17 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         fence_after_sync();
         {
             // G1 is done with B1: stage v rows t0-3 .. t0+63 and gate rows t0 .. t0+Lc-1 there
-            const int64_t plo = (t0 - 3) > s0 ? (t0 - 3) : s0;
-            const int64_t phi = (t0 + kC) < s1 ? (t0 + kC) : s1;
-            const int nv = (int)(phi - plo);
-            const int trbase = (int)(plo - (t0 - 3));
-            for (int idx = tid; idx < nv * 16; idx += kThreads) {
-                const int rr = idx >> 4, vec = idx & 15;
-                cp_async16(sbase + kOffRawV + (trbase + rr) * kRawStride + 16 * vec,
-                           v + (plo + rr) * xs + (int64_t)h * kD + 8 * vec);
+            for (int idx = tid; idx < kRawRows * 16; idx += kThreads) {
+                const int tr = idx >> 4, vec = idx & 15;
+                const int64_t pr = t0 - 3 + tr;
+                if (pr >= s0 && pr < s1)
+                    cp_async16(sbase + kOffRawV + tr * kRawStride + 16 * vec, v + pr * xs + (int64_t)h * kD + 8 * vec);
             }
             if (gate)
-                for (int idx = tid; idx < Lc * 16; idx += kThreads) {
+                for (int idx = tid; idx < kC * 16; idx += kThreads) {
                     const int rr = idx >> 4, vec = idx & 15;
-                    cp_async16(sbase + kOffGateT + rr * 256 + 16 * vec, gate + ((t0 + rr) * H + h) * kD + 8 * vec);
+                    if (rr < Lc)
+                        cp_async16(sbase + kOffGateT + rr * 256 + 16 * vec, gate + ((t0 + rr) * H + h) * kD + 8 * vec);
                 }
             cp_async_commit();
         }
