@@ -195,25 +195,42 @@ k_decode_tma(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __
     __shared__ uint64_t bars[St::kStages];
     __shared__ __align__(16) float sx[3][D];
     __shared__ __align__(16) float sred[8][D];  // float4 accesses: explicit 16-byte alignment
+    __shared__ __align__(16) float sW[3 * D * 4];  // conv taps of the current head
+    __shared__ float sRms[D];
+    __shared__ float sbeta[St::kStages];
     __shared__ float sinv[2];
+    __shared__ int s_head;
     const uint32_t raw_addr = tc::smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw_addr + 127u) & ~127u) - raw_addr);
     const uint32_t sbase = tc::smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t HD = (int64_t)H * D;
-    const int first = blockIdx.x, stride = gridDim.x;
-    const int my_units = first < units ? (units - first + stride - 1) / stride : 0;
+    // units in head-major order (j = h * N + n), one contiguous range per CTA, so a CTA meets
+    // few distinct heads and keeps the current head's conv taps in shared memory
+    const int per = (units + gridDim.x - 1) / gridDim.x;
+    const int first = blockIdx.x * per;
+    const int my_units = first < units ? (units - first < per ? units - first : per) : 0;
+    const int Nseq = units / H;
+    auto unit_of = [&](int i, int& n, int& h) {
+        const int jj = first + i;
+        h = jj / Nseq;
+        n = jj % Nseq;
+    };
     const uint32_t tx_bytes = 65536 + 3 * St::kConvPart + 3 * St::kRawPart + (gate ? St::kRawPart : 0) + 512;
 
     if (tid == 0) {
         for (int i = 0; i < St::kStages; ++i) tc::mbar_init(&bars[i], 1);
         tc::fence_mbar_init();
+        s_head = -1;
     }
+    for (int c = tid; c < D; c += 256) sRms[c] = rms_w ? rms_w[c] : 1.f;
     __syncthreads();
 
     auto issue = [&](int i) {  // bulk loads of this CTA's i-th unit
-        const int u = first + i * stride, b = i % St::kStages;
-        const int n = u / H, h = u % H;
+        const int b = i % St::kStages;
+        int n, h;
+        unit_of(i, n, h);
+        const int u = n * H + h;
         const uint32_t st = sbase + b * St::kBytes;
         tc::mbar_expect_tx(&bars[b], tx_bytes);
         tc::bulk_load(st + St::kState, state + (int64_t)u * D * D, 65536, &bars[b]);
@@ -230,17 +247,33 @@ k_decode_tma(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __
     };
     if (tid == 0)
         for (int i = 0; i < St::kStages - 1 && i < my_units; ++i) issue(i);
+    if (tid == 32)
+        for (int i = 0; i < St::kStages - 1 && i < my_units; ++i) {
+            int n, h;
+            unit_of(i, n, h);
+            sbeta[i % St::kStages] = beta[n * H + h];
+        }
 
     const int cg = lane, rg = warp;  // 4 columns 4cg.., 16 rows 16rg..
     const int c0 = 4 * cg, r0 = 16 * rg;
     bool failed = false;
     for (int i = 0; i < my_units; ++i) {
         const int b = i % St::kStages;
-        const int u = first + i * stride, n = u / H, h = u % H;
+        int n, h;
+        unit_of(i, n, h);
+        const int u = n * H + h;
         uint8_t* st = sm + b * St::kBytes;
         if (!__syncthreads_and(tc::mbar_wait(&bars[b], (i / St::kStages) & 1))) {
             failed = true;
             break;
+        }
+        if (h != s_head) {  // a new head: reload its conv taps (uniform branch)
+            for (int idx = tid; idx < 3 * D * 4; idx += 256) {
+                const int part = idx / (D * 4), rem = idx % (D * 4);
+                sW[idx] = conv_w[(part * HD + (int64_t)h * D) * 4 + rem];
+            }
+            __syncthreads();
+            if (tid == 0) s_head = h;
         }
         float* S = reinterpret_cast<float*>(st + St::kState);
         Tio* cs = reinterpret_cast<Tio*>(st + St::kConv);
@@ -251,7 +284,7 @@ k_decode_tma(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __
             Tio* c3 = cs + (part * D + d) * 3;
             const float x0 = to_f(c3[0]), x1 = to_f(c3[1]), x2 = to_f(c3[2]);
             const Tio xn = xr[part * D + d];
-            const float4 w = *reinterpret_cast<const float4*>(conv_w + (part * HD + (int64_t)h * D + d) * 4);
+            const float4 w = *reinterpret_cast<const float4*>(&sW[(part * D + d) * 4]);
             const float uu = w.x * x0 + w.y * x1 + w.z * x2 + w.w * to_f(xn);
             c3[0] = c3[1];
             c3[1] = c3[2];
@@ -292,7 +325,7 @@ k_decode_tma(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __
             ev.x += t.x; ev.y += t.y; ev.z += t.z; ev.w += t.w;
         }
         ev.x = sx[2][c0] - ev.x; ev.y = sx[2][c0 + 1] - ev.y; ev.z = sx[2][c0 + 2] - ev.z; ev.w = sx[2][c0 + 3] - ev.w;
-        const float bb = beta[u];
+        const float bb = sbeta[b];
         float4 po = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -319,6 +352,11 @@ k_decode_tma(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __
                 issue(i + St::kStages - 1);
             }
         }
+        if (tid == 32 && i + St::kStages - 1 < my_units) {  // beta two units ahead (read after later barriers)
+            int n2, h2;
+            unit_of(i + St::kStages - 1, n2, h2);
+            sbeta[(i + St::kStages - 1) % St::kStages] = beta[n2 * H + h2];
+        }
         if (rg == 0) {
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -336,7 +374,7 @@ k_decode_tma(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 float y = o[m] * inv;
-                if (rms_w) y *= rms_w[c0 + m];
+                y *= sRms[c0 + m];
                 if (gt) y *= sigmoidf_(to_f(gt[m]));
                 dst[m] = from_f<To>(y);
             }
