@@ -48,7 +48,7 @@ using namespace tc;
 
 constexpr int kD = 128;
 constexpr int kC = 64;
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 
 // TMEM columns
 constexpr uint32_t kColS = 0;
@@ -94,8 +94,8 @@ static_assert(kOffGateT + kC * 256 <= kOffB3hi, "gate staging exceeds the B1 reg
 constexpr int kMiscConvW = 0;                  // [3][128][4]
 constexpr int kMiscConst = kMiscConvW + 1536;  // [9][128]
 constexpr int kMiscBeta = kMiscConst + 9 * 128;
-constexpr int kMiscSS = kMiscBeta + 64;        // [128 rows][2 halves]
-constexpr int kMiscRed = kMiscSS + 256;        // [4 quadrants][64 tokens]
+constexpr int kMiscSS = kMiscBeta + 64;        // [128 rows][4 quarters]
+constexpr int kMiscRed = kMiscSS + 512;        // [4 quadrants][64 tokens]
 constexpr int kMiscInv = kMiscRed + 256;       // [64]
 constexpr int kMiscFloats = kMiscInv + 64;
 constexpr uint32_t kSmemBytes = kOffMisc + kMiscFloats * 4 + 1024;  // + alignment slack
@@ -164,12 +164,14 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     float* sConvW = misc + kMiscConvW;
     float* sConst = misc + kMiscConst;
     float* sBeta = misc + kMiscBeta;
-    float* sSS = misc + kMiscSS;
+    float* sSS = misc + kMiscSS;    // [128 rows][4 quarters]; also [4 quarters][128] column totals
     float* sRed = misc + kMiscRed;
     float* sInv = misc + kMiscInv;
 
+    // Thread layout: 16 warps.  Warp w reaches TMEM lanes 32 (w % 4) .. + 31 (quadrant qd) and
+    // owns quarter qt = w / 4 of the channels (64 rows x 128 channels tiles) or of the tokens.
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qd = warp & 3, hc = warp >> 2;      // TMEM lane quadrant, half (channels or tokens)
+    const int qd = warp & 3, qt = warp >> 2;
     const int L = qd * 32 + lane;                 // this thread's TMEM lane
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const int h = blockIdx.x % H, n = blockIdx.x / H;
@@ -194,23 +196,20 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     fence_after_sync();
     const uint32_t tb = s_tbase;
 
-    // ---- carried state: thread (lane j = L, half hc) keeps S[c][j] for c in [64hc, 64hc + 64)
+    // ---- carried state: thread (lane j = L, quarter qt) keeps S[c][j] for c in [32qt, 32qt + 32)
     const int j = L;
-    float Sreg[64];
+    float Sreg[32];
     {
         const float* src = S0 ? S0 + (((int64_t)n * H + h) * kD) * kD : nullptr;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) Sreg[i] = src ? src[(int64_t)(64 * hc + i) * kD + j] : 0.f;
+        for (int i = 0; i < 32; ++i) Sreg[i] = src ? src[(int64_t)(32 * qt + i) * kD + j] : 0.f;
     }
     auto store_state_operand = [&]() {  // S^T hi/lo -> TMEM columns [0,128)
+        uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            uint32_t hi[16], lo[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) split2(Sreg[32 * part + 2 * i], Sreg[32 * part + 2 * i + 1], hi[i], lo[i]);
-            tmem_st16(tb + lane_off + kColS + 32 * hc + 16 * part, hi);
-            tmem_st16(tb + lane_off + kColS + 64 + 32 * hc + 16 * part, lo);
-        }
+        for (int i = 0; i < 16; ++i) split2(Sreg[2 * i], Sreg[2 * i + 1], hi[i], lo[i]);
+        tmem_st16(tb + lane_off + kColS + 16 * qt, hi);
+        tmem_st16(tb + lane_off + kColS + 64 + 16 * qt, lo);
         tmem_st_wait();
     };
     store_state_operand();
@@ -228,19 +227,17 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         const uint32_t par = ci & 1;
 
         // ------------------------------------------------ A0: stage this chunk's q/k rows; L2 prefetch of the next
-        {
-            for (int idx = tid; idx < 2 * kRawRows * 16; idx += kThreads) {
-                const int part = idx >= kRawRows * 16 ? 1 : 0;
-                const int rem = idx - part * kRawRows * 16;
-                const int tr = rem >> 4, vec = rem & 15;
-                const int64_t pr = t0 - 3 + tr;
-                if (pr >= s0 && pr < s1)
-                    cp_async16(sbase + (part ? kOffRawK : kOffRawQ) + tr * kRawStride + 16 * vec,
-                               (part ? k : q) + pr * xs + (int64_t)h * kD + 8 * vec);
-            }
-            cp_async_commit();
+        for (int idx = tid; idx < 2 * kRawRows * 16; idx += kThreads) {
+            const int part = idx >= kRawRows * 16 ? 1 : 0;
+            const int rem = idx - part * kRawRows * 16;
+            const int tr = rem >> 4, vec = rem & 15;
+            const int64_t pr = t0 - 3 + tr;
+            if (pr >= s0 && pr < s1)
+                cp_async16(sbase + (part ? kOffRawK : kOffRawQ) + tr * kRawStride + 16 * vec,
+                           (part ? k : q) + pr * xs + (int64_t)h * kD + 8 * vec);
         }
-        if (ci + 1 < n_chunks) {
+        cp_async_commit();
+        if (ci + 1 < n_chunks && tid < 256) {
             const int64_t tn = t0 + kC;
             const int rr = tid & 63;
             if (tn + rr < s1) {
@@ -256,30 +253,28 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             }
         }
 
-        // ------------------------------------------------ A1: G = cumsum(g) (two halves of 32 tokens), beta
+        // ------------------------------------------------ A1: G = cumsum(g) (four quarters of 16 tokens), beta
         {
-            const int c = tid & (kD - 1), hh = tid >> 7;
-            float gv[32];
+            const int c = tid & (kD - 1), hq = tid >> 7;
+            float gv[16];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int rr = 32 * hh + e;
+            for (int e = 0; e < 16; ++e) {
+                const int rr = 16 * hq + e;
                 gv[e] = rr < Lc ? g[((t0 + rr) * H + h) * kD + c] : 0.f;
             }
             float acc = 0.f;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
+            for (int e = 0; e < 16; ++e) {
                 acc += gv[e];
-                sG[(32 * hh + e) * kGs + c] = acc;
+                gv[e] = acc;
             }
-            if (hh == 0) sSS[c] = acc;  // first-half total per channel
+            sSS[hq * kD + c] = acc;  // quarter total per channel
             if (tid < kC) sBeta[tid] = tid < Lc ? beta[(t0 + tid) * H + h] : 0.f;
-        }
-        __syncthreads();
-        if (tid >= kD) {
-            const int c = tid - kD;
-            const float base = sSS[c];
-#pragma unroll 8
-            for (int e = 0; e < 32; ++e) sG[(32 + e) * kGs + c] += base;
+            __syncthreads();
+            float base = 0.f;
+            for (int qq = 0; qq < hq; ++qq) base += sSS[qq * kD + c];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sG[(16 * hq + e) * kGs + c] = gv[e] + base;
         }
         cp_async_wait_all();
         __syncthreads();
@@ -300,18 +295,18 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             sConst[cGam * kD + c] = ex(gl);
         }
 
-        // ------------------------------------------------ A3a: conv + SiLU of one q or k row (64 channels)
+        // ------------------------------------------------ A3a: conv + SiLU of one q or k row (32 channels)
         const bool isq = L < 64;
         const int r = L & 63;
         const bool rvalid = r < Lc;
-        const int c0 = 64 * hc;
-        float x[64];
+        const int c0 = 32 * qt;
+        float x[32];
         {
             const int part = isq ? 0 : 1;
             const int64_t t = t0 + r;
             float ss = 0.f;
 #pragma unroll
-            for (int g8 = 0; g8 < 8; ++g8) {
+            for (int g8 = 0; g8 < 4; ++g8) {
                 const int cc = c0 + 8 * g8;
                 float win[4][8];
 #pragma unroll
@@ -335,28 +330,26 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 for (int e = 0; e < 8; ++e) {
                     const float4 w = *reinterpret_cast<const float4*>(&sConvW[(part * kD + cc + e) * 4]);
                     const float u = w.x * win[0][e] + w.y * win[1][e] + w.z * win[2][e] + w.w * win[3][e];
-                    const float s = rvalid ? silu_fast(u) : 0.f;
-                    x[8 * g8 + e] = s;
-                    ss += s * s;
+                    const float sv = rvalid ? silu_fast(u) : 0.f;
+                    x[8 * g8 + e] = sv;
+                    ss += sv * sv;
                 }
             }
-            sSS[L * 2 + hc] = ss;
+            sSS[L * 4 + qt] = ss;
         }
         __syncthreads();
 
         // ------------------------------------------------ A3b: L2 norm, decay factors, operand tiles
         {
-            const float inv = rsqrtf(sSS[L * 2] + sSS[L * 2 + 1] + eps_l2);
+            const float4 ssv = *reinterpret_cast<const float4*>(&sSS[L * 4]);
+            const float inv = rsqrtf(ssv.x + ssv.y + ssv.z + ssv.w + eps_l2);
             const int hr = r >> 5;
             const float* cA = sConst + (hr ? cA1 : cA0) * kD;
             const float* cE = sConst + (hr ? cE1 : cE0) * kD;
             const float bt = sBeta[r];
-#pragma unroll
-            for (int pass = 0; pass < 2; ++pass) {
             uint32_t xhi[16], xlo[16];
 #pragma unroll
-            for (int gq = 0; gq < 4; ++gq) {
-                const int g8 = 4 * pass + gq;
+            for (int g8 = 0; g8 < 4; ++g8) {
                 const int cc = c0 + 8 * g8;
                 float xv[8], uu[8], gg[8], aa[8], EE[8];
                 {
@@ -385,8 +378,8 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
 #pragma unroll
                     for (int e = 0; e < 8; ++e) t8[e] = xv[e] * uu[e];
                     split8(t8, hi, lo);
-                    xhi[4 * gq + 0] = hi.x; xhi[4 * gq + 1] = hi.y; xhi[4 * gq + 2] = hi.z; xhi[4 * gq + 3] = hi.w;
-                    xlo[4 * gq + 0] = lo.x; xlo[4 * gq + 1] = lo.y; xlo[4 * gq + 2] = lo.z; xlo[4 * gq + 3] = lo.w;
+                    xhi[4 * g8 + 0] = hi.x; xhi[4 * g8 + 1] = hi.y; xhi[4 * g8 + 2] = hi.z; xhi[4 * g8 + 3] = hi.w;
+                    xlo[4 * g8 + 0] = lo.x; xlo[4 * g8 + 1] = lo.y; xlo[4 * g8 + 2] = lo.z; xlo[4 * g8 + 3] = lo.w;
 #pragma unroll
                     for (int e = 0; e < 8; ++e) t8[e] = xv[e] * uu[e] * EE[e];
                     split8(t8, hi, lo);
@@ -400,8 +393,8 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
 #pragma unroll
                     for (int e = 0; e < 8; ++e) t8[e] = bt * xv[e] * uu[e];
                     split8(t8, hi, lo);
-                    xhi[4 * gq + 0] = hi.x; xhi[4 * gq + 1] = hi.y; xhi[4 * gq + 2] = hi.z; xhi[4 * gq + 3] = hi.w;
-                    xlo[4 * gq + 0] = lo.x; xlo[4 * gq + 1] = lo.y; xlo[4 * gq + 2] = lo.z; xlo[4 * gq + 3] = lo.w;
+                    xhi[4 * g8 + 0] = hi.x; xhi[4 * g8 + 1] = hi.y; xhi[4 * g8 + 2] = hi.z; xhi[4 * g8 + 3] = hi.w;
+                    xlo[4 * g8 + 0] = lo.x; xlo[4 * g8 + 1] = lo.y; xlo[4 * g8 + 2] = lo.z; xlo[4 * g8 + 3] = lo.w;
                     // B1 row r: k v (anchor of r's own half)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) t8[e] = xv[e] * vv[e];
@@ -445,10 +438,9 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                     sts128(sm, kOffKTlo + mnmajor_off(kKtLbo, kKtSbo, cc / 8, r), lo);
                 }
             }
-            // X1 row, 32 channels -> TMEM lane L (hi columns 128 + 32hc + 16pass, lo + 64)
-            tmem_st16(tb + lane_off + kColX + 32 * hc + 16 * pass, xhi);
-            tmem_st16(tb + lane_off + kColX + 64 + 32 * hc + 16 * pass, xlo);
-            }
+            // X1 row, 32 channels -> TMEM lane L (hi columns 128 + 16qt .., lo + 64)
+            tmem_st16(tb + lane_off + kColX + 16 * qt, xhi);
+            tmem_st16(tb + lane_off + kColX + 64 + 16 * qt, xlo);
             tmem_st_wait();
         }
         fence_async_smem();
@@ -505,37 +497,39 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             cp_async_commit();
         }
         {
-            // this thread: row r (q rows -> M, k rows -> A), columns of its half
-            uint32_t dv[32];
-            tmem_ld32(tb + lane_off + kColAM + 32 * hc, dv);  // cols 32hc .. 32hc+31
-            uint32_t dx[32];
-            tmem_ld32(tb + lane_off + kColAM + 64, dx);        // cols 64..95 (i < 32, anchor G_47)
-            tmem_ld_wait();
-            const int hr = r >> 5;
-            float row[32];  // entries for i in [32hc, 32hc + 32)
+            // thread: row r (q rows -> M, k rows -> A), columns i in [16qt, 16qt + 16).  The warp's rows
+            // share one half hr, so the source block is warp-uniform: same half -> columns i,
+            // row half 1 x column half 0 -> columns 64 + i (anchor G_47), otherwise zero.
+            const int hr = r >> 5, hi_half = qt >> 1;
+            float row[16];
+            if (hi_half <= hr) {
+                uint32_t dv[16];
+                tmem_ld16(tb + lane_off + kColAM + (hi_half == hr ? 16 * qt : 64 + 16 * qt), dv);
+                tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int i = 32 * hc + e;
-                float val;
-                if (hc == hr) val = __uint_as_float(dv[e]);          // same half
-                else val = __uint_as_float(dx[e]);                   // r in second half, i in first
-                const bool keep = isq ? (i <= r) : (i < r);
-                row[e] = (keep && hc <= hr) ? val : 0.f;
+                for (int e = 0; e < 16; ++e) {
+                    const int i = 16 * qt + e;
+                    const bool keep = isq ? (i <= r) : (i < r);
+                    row[e] = keep ? __uint_as_float(dv[e]) : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) row[e] = 0.f;
             }
             if (isq) {
 #pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8) {
+                for (int g8 = 0; g8 < 2; ++g8) {
                     uint4 hi, lo;
                     float t8[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) t8[e] = row[8 * g8 + e];
                     split8(t8, hi, lo);
-                    sts128(sMhi, kmajor_off(64, r, 4 * hc + g8), hi);
-                    sts128(sMlo, kmajor_off(64, r, 4 * hc + g8), lo);
+                    sts128(sMhi, kmajor_off(64, r, 2 * qt + g8), hi);
+                    sts128(sMlo, kmajor_off(64, r, 2 * qt + g8), lo);
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) sAf[r * kAs + 32 * hc + e] = row[e];
+                for (int e = 0; e < 16; ++e) sAf[r * kAs + 16 * qt + e] = row[e];
             }
         }
         __syncthreads();
@@ -603,9 +597,9 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         if (failed) break;
         fence_after_sync();
         {
-            const int i0 = 32 * hc;
+            // thread (lane j, quarter qt): tokens i in [16qt, 16qt + 16)
+            const int i0 = 16 * qt;
             const float4 w = *reinterpret_cast<const float4*>(&sConvW[(2 * kD + j) * 4]);
-            float p0, p1, p2;
             const bf16* vt = reinterpret_cast<const bf16*>(sm + kOffRawV);
             auto raw = [&](int64_t p) -> float {
                 if (p >= s0) return to_f(vt[(uint32_t)(p - (t0 - 3)) * (kRawStride / 2) + j]);
@@ -613,15 +607,15 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 return cs_in ? to_f(cs_in[((int64_t)n * 3 * HD + 2 * HD + (int64_t)h * kD + j) * 3 + 3 + pos]) : 0.f;
             };
             const int64_t tb0 = t0 + i0;
-            p0 = (i0 < Lc) ? raw(tb0 - 3) : 0.f;
-            p1 = (i0 < Lc) ? raw(tb0 - 2) : 0.f;
-            p2 = (i0 < Lc) ? raw(tb0 - 1) : 0.f;
-            uint32_t pv[32];
-            tmem_ld32(tb + lane_off + kColP + i0, pv);
+            float p0 = (i0 < Lc) ? raw(tb0 - 3) : 0.f;
+            float p1 = (i0 < Lc) ? raw(tb0 - 2) : 0.f;
+            float p2 = (i0 < Lc) ? raw(tb0 - 1) : 0.f;
+            uint32_t pv[16];
+            tmem_ld16(tb + lane_off + kColP + i0, pv);
             tmem_ld_wait();
-            uint32_t rhi[16], rlo[16];
+            uint32_t rhi[8], rlo[8];
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
+            for (int e = 0; e < 16; e += 2) {
                 float rv[2];
 #pragma unroll
                 for (int f = 0; f < 2; ++f) {
@@ -636,8 +630,8 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 }
                 split2(rv[0], rv[1], rhi[e / 2], rlo[e / 2]);
             }
-            tmem_st16(tb + lane_off + kColR + 16 * hc, rhi);
-            tmem_st16(tb + lane_off + kColR + 32 + 16 * hc, rlo);
+            tmem_st8(tb + lane_off + kColR + 8 * qt, rhi);
+            tmem_st8(tb + lane_off + kColR + 32 + 8 * qt, rlo);
             tmem_st_wait();
         }
         fence_before_sync();
@@ -661,15 +655,15 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
 
         // ------------------------------------------------ F: W^T -> hi/lo operand
         {
-            uint32_t wv[32];
-            tmem_ld32(tb + lane_off + kColW + 32 * hc, wv);
+            uint32_t wv[16];
+            tmem_ld16(tb + lane_off + kColW + 16 * qt, wv);
             tmem_ld_wait();
-            uint32_t whi[16], wlo[16];
+            uint32_t whi[8], wlo[8];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
+            for (int e = 0; e < 8; ++e)
                 split2(__uint_as_float(wv[2 * e]), __uint_as_float(wv[2 * e + 1]), whi[e], wlo[e]);
-            tmem_st16(tb + lane_off + kColWop + 16 * hc, whi);
-            tmem_st16(tb + lane_off + kColWop + 32 + 16 * hc, wlo);
+            tmem_st8(tb + lane_off + kColWop + 8 * qt, whi);
+            tmem_st8(tb + lane_off + kColWop + 32 + 8 * qt, wlo);
             tmem_st_wait();
         }
         fence_before_sync();
@@ -706,41 +700,39 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         // ------------------------------------------------ H: state update, output epilogue
         {
             uint32_t dsv[32];
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                tmem_ld32(tb + lane_off + kColS + 64 * hc + 32 * part, dsv);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const int ci2 = 32 * part + e;
-                    const float4 gm = *reinterpret_cast<const float4*>(&sConst[cGam * kD + 64 * hc + ci2]);
-                    Sreg[ci2 + 0] = gm.x * Sreg[ci2 + 0] + __uint_as_float(dsv[e + 0]);
-                    Sreg[ci2 + 1] = gm.y * Sreg[ci2 + 1] + __uint_as_float(dsv[e + 1]);
-                    Sreg[ci2 + 2] = gm.z * Sreg[ci2 + 2] + __uint_as_float(dsv[e + 2]);
-                    Sreg[ci2 + 3] = gm.w * Sreg[ci2 + 3] + __uint_as_float(dsv[e + 3]);
-                }
-            }
-            uint32_t ov[32];
-            tmem_ld32(tb + lane_off + kColO + 32 * hc, ov);
+            tmem_ld32(tb + lane_off + kColS + 32 * qt, dsv);
             tmem_ld_wait();
-            float o[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = scale * __uint_as_float(ov[e]);
-            // sum over the warp's 32 channels of o^2, for each of its 32 tokens (lane l ends with token l)
-            float sq[32];
+            for (int e = 0; e < 32; e += 4) {
+                const float4 gm = *reinterpret_cast<const float4*>(&sConst[cGam * kD + 32 * qt + e]);
+                Sreg[e + 0] = gm.x * Sreg[e + 0] + __uint_as_float(dsv[e + 0]);
+                Sreg[e + 1] = gm.y * Sreg[e + 1] + __uint_as_float(dsv[e + 1]);
+                Sreg[e + 2] = gm.z * Sreg[e + 2] + __uint_as_float(dsv[e + 2]);
+                Sreg[e + 3] = gm.w * Sreg[e + 3] + __uint_as_float(dsv[e + 3]);
+            }
+            uint32_t ov[16];
+            tmem_ld16(tb + lane_off + kColO + 16 * qt, ov);
+            tmem_ld_wait();
+            float o[16];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) sq[e] = o[e] * o[e];
+            for (int e = 0; e < 16; ++e) o[e] = scale * __uint_as_float(ov[e]);
+            // sum over the warp's 32 channels of o^2 for each of its 16 tokens:
+            // halve across lanes 8, 4, 2, 1 apart, then fold the two 16-lane halves
+            float sq[16];
 #pragma unroll
-            for (int s = 16; s >= 1; s >>= 1) {
-                const bool upper = (lane & s) != 0;
+            for (int e = 0; e < 16; ++e) sq[e] = o[e] * o[e];
 #pragma unroll
-                for (int i = 0; i < s; ++i) {
-                    const float send = upper ? sq[i] : sq[i + s];
-                    const float keep = upper ? sq[i + s] : sq[i];
-                    sq[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+            for (int sh = 8; sh >= 1; sh >>= 1) {
+                const bool upper = (lane & sh) != 0;
+#pragma unroll
+                for (int i = 0; i < sh; ++i) {
+                    const float send = upper ? sq[i] : sq[i + sh];
+                    const float keep = upper ? sq[i + sh] : sq[i];
+                    sq[i] = keep + __shfl_xor_sync(0xffffffffu, send, sh);
                 }
             }
-            sRed[qd * 64 + 32 * hc + lane] = sq[0];
+            sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], 16);  // lane l: token 16qt + (l & 15)
+            if (lane < 16) sRed[qd * 64 + 16 * qt + lane] = sq[0];
             __syncthreads();
             if (tid < 64)
                 sInv[tid] = rsqrtf((sRed[tid] + sRed[64 + tid] + sRed[128 + tid] + sRed[192 + tid]) * (1.0f / kD) + eps_rms);
@@ -748,9 +740,9 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             const float wj = rms_w ? rms_w[j] : 1.f;
             const bf16* gt = reinterpret_cast<const bf16*>(sm + kOffGateT);
             To* yt = reinterpret_cast<To*>(sm + kOffR1);  // [64][128] y tile (R1 is free after the solve)
-#pragma unroll 8
-            for (int e = 0; e < 32; ++e) {
-                const int rr = 32 * hc + e;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int rr = 16 * qt + e;
                 float yv = o[e] * sInv[rr] * wj;
                 if (gate) yv *= sigmoid_fast(to_f(gt[rr * kD + j]));
                 yt[rr * kD + j] = from_f<To>(yv);
@@ -780,7 +772,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     } else if (S_fin) {
         float* dst = S_fin + (((int64_t)n * H + h) * kD) * kD;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) dst[(int64_t)(64 * hc + i) * kD + j] = Sreg[i];
+        for (int i = 0; i < 32; ++i) dst[(int64_t)(32 * qt + i) * kD + j] = Sreg[i];
     }
     fence_before_sync();
     __syncthreads();
