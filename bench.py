@@ -127,6 +127,11 @@ def barrier(pg):
         pg.barrier()
 
 
+def aggregate_rate(world: int, units_per_rank: float, ms_max: float) -> float:
+    """Whole-job throughput: every rank processed units_per_rank; the slowest rank took ms_max."""
+    return world * units_per_rank / (ms_max / 1e3)
+
+
 def max_over_ranks(pg, x: float, device) -> float:
     if pg is None:
         return x
@@ -220,7 +225,7 @@ def run_ours(args):
     barrier(pg)
     ms = e0.elapsed_time(e1) / args.steps
     ms_max = max_over_ranks(pg, ms, dev)
-    tokens_per_s = world * T / (ms_max / 1e3)
+    tokens_per_s = aggregate_rate(world, T, ms_max)
 
     # roofline of the prefill launch(es)
     fl = PREFILL_FLOP_PER_TOKEN_HEAD.get((D, inp.chunk), 0) * T * H

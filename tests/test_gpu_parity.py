@@ -101,7 +101,9 @@ def test_prefill_fp32_shapes(D, chunk):
 
 # --------------------------------------------------------------------------- bf16, D = 128
 
-SMALL_LENGTHS = [[1], [2], [3], [5], [63], [64], [65], [127], [130], [1, 64, 3, 200, 65]]
+# the last entry is the multi-token continuation shape (8 sequences x 4 new tokens from carried
+# states and conv states, as in speculative verification)
+SMALL_LENGTHS = [[1], [2], [3], [5], [63], [64], [65], [127], [130], [1, 64, 3, 200, 65], [4] * 8]
 
 
 @pytest.mark.parametrize("lengths", SMALL_LENGTHS)
