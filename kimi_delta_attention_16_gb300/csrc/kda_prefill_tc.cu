@@ -115,8 +115,8 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+__device__ __forceinline__ void prefetch_line_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
 
 // hi/lo bf16 split of two floats, packed as bf16x2 words (first value in the low half)
@@ -237,19 +237,20 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                            (part ? k : q) + pr * xs + (int64_t)h * kD + 8 * vec);
         }
         cp_async_commit();
-        if (ci + 1 < n_chunks && tid < 256) {
+        if (ci + 1 < n_chunks) {
+            // next chunk's rows into L2, one 128-byte line per thread and step
             const int64_t tn = t0 + kC;
-            const int rr = tid & 63;
+            const int rr = tid & 63, which = tid >> 6;  // 8 line slots per row
             if (tn + rr < s1) {
                 const int64_t row = tn + rr;
-                const int which = tid >> 6;  // 0 q, 1 k, 2 v, 3 g + gate
-                if (which == 0) prefetch_l2(q + row * xs + (int64_t)h * kD, 256);
-                else if (which == 1) prefetch_l2(k + row * xs + (int64_t)h * kD, 256);
-                else if (which == 2) prefetch_l2(v + row * xs + (int64_t)h * kD, 256);
-                else {
-                    prefetch_l2(g + (row * H + h) * kD, 512);
-                    if (gate) prefetch_l2(gate + (row * H + h) * kD, 256);
-                }
+                const char* base;
+                if (which < 2) base = reinterpret_cast<const char*>(q + row * xs + (int64_t)h * kD) + 128 * which;
+                else if (which < 4) base = reinterpret_cast<const char*>(k + row * xs + (int64_t)h * kD) + 128 * (which - 2);
+                else if (which < 6) base = reinterpret_cast<const char*>(v + row * xs + (int64_t)h * kD) + 128 * (which - 4);
+                else base = reinterpret_cast<const char*>(g + (row * H + h) * kD) + 256 * (which - 6);
+                prefetch_line_l2(base);
+                if (which >= 6) prefetch_line_l2(base + 128);
+                if (gate && which < 2) prefetch_line_l2(reinterpret_cast<const char*>(gate + (row * H + h) * kD) + 128 * which);
             }
         }
 
@@ -552,26 +553,43 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             }
         }
         __syncthreads();
-        for (int d = 1; d < 4; ++d) {
-            // X_IJ = sum_{K=J}^{I-1} A_IK T_KJ, stored transposed in A's upper triangle
-            for (int idx = tid; idx < (4 - d) * 256; idx += kThreads) {
-                const int J = idx >> 8, I = J + d, rr = (idx >> 4) & 15, jj = idx & 15;
-                float acc = 0.f;
-                for (int K = J; K < I; ++K)
+        // Off-diagonal 16-blocks by block diagonal d: X_IJ = sum_{K=J}^{I-1} A_IK T_KJ, then
+        // T_IJ = -T_II X_IJ.  A thread makes four adjacent outputs (one broadcast load of A or
+        // T_II and one float4 load per k); X lives in the idle row-reduction scratch.
+        {
+            float* sX = sSS;  // [(4-d) blocks][16][16], 768 floats over sSS + sRed
+#pragma unroll 1
+            for (int d = 1; d < 4; ++d) {
+                const int nq = (4 - d) * 64;  // quads of outputs
+                if (tid < nq) {
+                    const int J = tid >> 6, I = J + d, rr = (tid >> 2) & 15, jq = tid & 3;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int K = J; K < I; ++K)
 #pragma unroll
-                    for (int kk = 0; kk < 16; ++kk)
-                        acc += sAf[(16 * I + rr) * kAs + 16 * K + kk] * sTf[(16 * K + kk) * 64 + 16 * J + jj];
-                sAf[(16 * J + jj) * kAs + 16 * I + rr] = acc;
+                        for (int kk = 0; kk < 16; ++kk) {
+                            const float a = sAf[(16 * I + rr) * kAs + 16 * K + kk];
+                            const float4 t4 = *reinterpret_cast<const float4*>(&sTf[(16 * K + kk) * 64 + 16 * J + 4 * jq]);
+                            acc.x += a * t4.x; acc.y += a * t4.y; acc.z += a * t4.z; acc.w += a * t4.w;
+                        }
+                    *reinterpret_cast<float4*>(&sX[(J * 16 + rr) * 16 + 4 * jq]) = acc;
+                }
+                __syncthreads();
+                if (tid < nq) {
+                    const int J = tid >> 6, I = J + d, rr = (tid >> 2) & 15, jq = tid & 3;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) {
+                        if (kk <= rr) {
+                            const float t = sTf[(16 * I + rr) * 64 + 16 * I + kk];
+                            const float4 x4 = *reinterpret_cast<const float4*>(&sX[(J * 16 + kk) * 16 + 4 * jq]);
+                            acc.x += t * x4.x; acc.y += t * x4.y; acc.z += t * x4.z; acc.w += t * x4.w;
+                        }
+                    }
+                    *reinterpret_cast<float4*>(&sTf[(16 * I + rr) * 64 + 16 * J + 4 * jq]) =
+                        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+                }
+                __syncthreads();
             }
-            __syncthreads();
-            for (int idx = tid; idx < (4 - d) * 256; idx += kThreads) {
-                const int J = idx >> 8, I = J + d, rr = (idx >> 4) & 15, jj = idx & 15;
-                float acc = 0.f;
-                for (int kk = 0; kk <= rr; ++kk)
-                    acc += sTf[(16 * I + rr) * 64 + 16 * I + kk] * sAf[(16 * J + jj) * kAs + 16 * I + kk];
-                sTf[(16 * I + rr) * 64 + 16 * J + jj] = -acc;
-            }
-            __syncthreads();
         }
         // T -> bf16, K-major [r][i]; the upper triangle is zero
         for (int idx = tid; idx < 64 * 8; idx += kThreads) {
