@@ -78,18 +78,21 @@ constexpr uint32_t kOffR1 = kOffKTlo + kTileKT;   // G fp32 [64][132]  |  A fp32
 constexpr uint32_t kR1Bytes = 64 * kGs * 4;        // 33792 >= 64*65*4 + 64*64*4
 constexpr uint32_t kOffR2 = kOffR1 + kR1Bytes;     // T bf16 [64][64] | M hi | M lo (K-major, 8 KB each)
 constexpr uint32_t kOffMisc = kOffR2 + 24576;
-// Raw-row staging inside the B1 region while B1 is not an operand:
-//   chunk start .. A3a : q rows and k rows t0-3 .. t0+63 (67 rows each)
-//   after G1 .. H      : v rows t0-3 .. t0+63 and gate rows t0 .. t0+63
+// Raw-row staging in operand regions while they are not operands:
+//   B3 region, from G3's completion in chunk n-1 to A3a of chunk n: q and k rows t0-3 .. t0+63
+//   B1 region, from G1's completion to the epilogue: v rows t0-3 .. t0+63, gate rows t0 .. t0+63
+//   K~ region, after G6: the y tile of the epilogue
 // Rows are padded to 272 bytes so that one-row-per-lane 16-byte reads are conflict-free.
 constexpr uint32_t kRawStride = 272;
 constexpr int kRawRows = kC + 3;
-constexpr uint32_t kOffRawQ = kOffB1hi;
-constexpr uint32_t kOffRawK = kOffB1hi + 18432;
+constexpr uint32_t kOffRawQ = kOffB3hi;
+constexpr uint32_t kOffRawK = kOffB3hi + 18432;
 constexpr uint32_t kOffRawV = kOffB1hi;
 constexpr uint32_t kOffGateT = kOffB1hi + 18432;  // [64][128] bf16, 256-byte rows
-static_assert(kOffRawK + kRawRows * kRawStride <= kOffB3hi, "q/k staging exceeds the B1 region");
+constexpr uint32_t kOffYT = kOffKThi;              // [64][128] y tile (bf16 or fp32)
+static_assert(kOffRawK + kRawRows * kRawStride <= kOffKThi, "q/k staging exceeds the B3 region");
 static_assert(kOffGateT + kC * 256 <= kOffB3hi, "gate staging exceeds the B1 region");
+static_assert(kOffYT + 64 * 128 * 4 <= kOffR1, "y tile exceeds the K~ region");
 // misc (floats)
 constexpr int kMiscConvW = 0;                  // [3][128][4]
 constexpr int kMiscConst = kMiscConvW + 1536;  // [9][128]
@@ -221,22 +224,56 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     bool failed = false;
     const int n_chunks = (int)((s1 - s0 + kC - 1) / kC);
 
-    for (int ci = 0; ci < n_chunks && !failed; ++ci) {
-        const int64_t t0 = s0 + (int64_t)ci * kC;
-        const int Lc = (int)((s1 - t0) < kC ? (s1 - t0) : kC);
-        const uint32_t par = ci & 1;
-
-        // ------------------------------------------------ A0: stage this chunk's q/k rows; L2 prefetch of the next
+    // q/k rows of chunk cj (t0-3 .. t0+63 within the sequence) -> B3 region, one cp.async group
+    auto stage_qk = [&](int cj) {
+        const int64_t tc0 = s0 + (int64_t)cj * kC;
         for (int idx = tid; idx < 2 * kRawRows * 16; idx += kThreads) {
             const int part = idx >= kRawRows * 16 ? 1 : 0;
             const int rem = idx - part * kRawRows * 16;
             const int tr = rem >> 4, vec = rem & 15;
-            const int64_t pr = t0 - 3 + tr;
+            const int64_t pr = tc0 - 3 + tr;
             if (pr >= s0 && pr < s1)
                 cp_async16(sbase + (part ? kOffRawK : kOffRawQ) + tr * kRawStride + 16 * vec,
                            (part ? k : q) + pr * xs + (int64_t)h * kD + 8 * vec);
         }
         cp_async_commit();
+    };
+    // G = cumsum(g) of chunk cj (four quarters of 16 tokens) into sG, beta into sBeta (one barrier inside)
+    auto compute_G = [&](int cj) {
+        const int64_t tc0 = s0 + (int64_t)cj * kC;
+        const int Lcj = (int)((s1 - tc0) < kC ? (s1 - tc0) : kC);
+        const int c = tid & (kD - 1), hq = tid >> 7;
+        float gv[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int rr = 16 * hq + e;
+            gv[e] = rr < Lcj ? g[((tc0 + rr) * H + h) * kD + c] : 0.f;
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            acc += gv[e];
+            gv[e] = acc;
+        }
+        sSS[hq * kD + c] = acc;  // quarter total per channel
+        if (tid < kC) sBeta[tid] = tid < Lcj ? beta[(tc0 + tid) * H + h] : 0.f;
+        __syncthreads();
+        float base = 0.f;
+        for (int qq = 0; qq < hq; ++qq) base += sSS[qq * kD + c];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sG[(16 * hq + e) * kGs + c] = gv[e] + base;
+    };
+    if (n_chunks > 0) {
+        stage_qk(0);
+        compute_G(0);
+    }
+
+    for (int ci = 0; ci < n_chunks && !failed; ++ci) {
+        const int64_t t0 = s0 + (int64_t)ci * kC;
+        const int Lc = (int)((s1 - t0) < kC ? (s1 - t0) : kC);
+        const uint32_t par = ci & 1;
+
+        // ------------------------------------------------ A0: L2 prefetch of the next chunk's rows
         if (ci + 1 < n_chunks) {
             // next chunk's rows into L2, one 128-byte line per thread and step
             const int64_t tn = t0 + kC;
@@ -254,29 +291,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             }
         }
 
-        // ------------------------------------------------ A1: G = cumsum(g) (four quarters of 16 tokens), beta
-        {
-            const int c = tid & (kD - 1), hq = tid >> 7;
-            float gv[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int rr = 16 * hq + e;
-                gv[e] = rr < Lc ? g[((t0 + rr) * H + h) * kD + c] : 0.f;
-            }
-            float acc = 0.f;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                acc += gv[e];
-                gv[e] = acc;
-            }
-            sSS[hq * kD + c] = acc;  // quarter total per channel
-            if (tid < kC) sBeta[tid] = tid < Lc ? beta[(t0 + tid) * H + h] : 0.f;
-            __syncthreads();
-            float base = 0.f;
-            for (int qq = 0; qq < hq; ++qq) base += sSS[qq * kD + c];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) sG[(16 * hq + e) * kGs + c] = gv[e] + base;
-        }
+        // q/k rows and G of this chunk were prepared during the previous chunk (or before the loop)
         cp_async_wait_all();
         __syncthreads();
 
@@ -655,7 +670,8 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         fence_before_sync();
         __syncthreads();
 
-        // ------------------------------------------------ E: G4  W^T = R^T T^T
+        // ------------------------------------------------ E: G4  W^T = R^T T^T; next chunk's q/k rows -> B3
+        if (ci + 1 < n_chunks) stage_qk(ci + 1);  // G3 finished with B3 (waited in D)
         if (tid == 0) {
             fence_after_sync();
             const uint32_t tbf = sbase + kOffR2;
@@ -711,6 +727,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             }
             mma_commit(&bars[3]);
         }
+        if (ci + 1 < n_chunks) compute_G(ci + 1);  // overlaps G5/G6; the A/T tile in R1 is dead
         failed = !__syncthreads_and(mbar_wait(&bars[3], par));
         if (failed) break;
         fence_after_sync();
@@ -757,7 +774,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             __syncthreads();
             const float wj = rms_w ? rms_w[j] : 1.f;
             const bf16* gt = reinterpret_cast<const bf16*>(sm + kOffGateT);
-            To* yt = reinterpret_cast<To*>(sm + kOffR1);  // [64][128] y tile (R1 is free after the solve)
+            To* yt = reinterpret_cast<To*>(sm + kOffYT);  // [64][128] y tile (K~ is free after G6)
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const int rr = 16 * qt + e;
@@ -772,7 +789,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         {
             // y rows -> out, 16-byte coalesced stores
             constexpr int kVpr = kD * (int)sizeof(To) / 16;
-            const uint4* yt = reinterpret_cast<const uint4*>(sm + kOffR1);
+            const uint4* yt = reinterpret_cast<const uint4*>(sm + kOffYT);
             for (int idx = tid; idx < Lc * kVpr; idx += kThreads) {
                 const int rr = idx / kVpr, vec = idx % kVpr;
                 *reinterpret_cast<uint4*>(out + ((t0 + rr) * H + h) * kD + vec * (16 / (int)sizeof(To))) =
