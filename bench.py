@@ -166,17 +166,20 @@ def recorded_traffic(kernel_key: str):
 
 
 def prefill_path(inp):
-    from kimi_delta_attention_16_gb300 import kda_prefill_workspace_size
-    # The tensor-core path needs no fp32 staging of q|k|v; the SIMT path needs 16 T H D bytes.
-    simt_ws = kda_prefill_workspace_size(inp.T, inp.H, inp.D, chunk=inp.chunk, flags=1)
-    ws = kda_prefill_workspace_size(inp.T, inp.H, inp.D, chunk=inp.chunk)
-    return ("simt" if ws == simt_ws and ws > 0 else "tc"), ws
+    """(path, segments, workspace bytes) of the kda_prefill calls on this batch."""
+    from kimi_delta_attention_16_gb300 import kda_prefill_plan, kda_prefill_workspace_size
+    path, segments = kda_prefill_plan(inp.T, inp.H, inp.D, N=inp.N, chunk=inp.chunk)
+    ws = kda_prefill_workspace_size(inp.T, inp.H, inp.D, N=inp.N, chunk=inp.chunk)
+    return path, segments, ws
 
 
-def prefill_launches(path):
+def prefill_launches(path, segments):
     # kernels one kda_prefill call enqueues here (host cu_seqlens given, no conv_state_out):
-    # tensor-core path: the fused chunk kernel; SIMT path: conv, chunk recurrence, epilogue.
-    return 1 if path == "tc" else 3
+    # tensor-core path: the fused chunk kernel, plus the segment composition and the output
+    # fix-up when sequences are cut into segments; SIMT path: conv, chunk recurrence, epilogue.
+    if path == "tc":
+        return 1 if segments == 1 else 3
+    return 3
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -196,7 +199,7 @@ def run_ours(args):
         args.decode_steps = 0
     inp = synth.make_prefill(args.workload, seed=1, device=dev)
     N, T, H, D = inp.N, inp.T, inp.H, inp.D
-    path, ws_bytes = prefill_path(inp)
+    path, segments, ws_bytes = prefill_path(inp)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
     fin = torch.empty((N, H, D, D), dtype=torch.float32, device=dev)
@@ -233,8 +236,10 @@ def run_ours(args):
     alg_bytes = T * H * PREFILL_BYTES_PER_TOKEN_HEAD_BF16 + state_bytes
     gbs = alg_bytes / (ms / 1e3) / 1e9
     tflops = fl / (ms / 1e3) / 1e12
-    roof = {"kernel": "kda_prefill (" + ("fused tcgen05 chunk kernel" if path == "tc" else
-                                         "SIMT path: conv + chunk recurrence + epilogue") + ")",
+    kname = ("fused tcgen05 chunk kernel" if segments == 1 else
+             f"fused tcgen05 chunk kernel, {segments} segments per sequence + composition + fix-up"
+             ) if path == "tc" else "SIMT path: conv + chunk recurrence + epilogue"
+    roof = {"kernel": "kda_prefill (" + kname + ")",
             "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": peak_src,
             "traffic": recorded_traffic(f"prefill_{path}_{args.workload}"),
@@ -333,14 +338,14 @@ def run_ours(args):
                 "data": "synthetic",
                 "config": {"workload": workload_desc(args.workload), "global_batch": N * world,
                            "seq_len": T, "heads": H, "head_dim": D, "chunk": inp.chunk,
-                           "prefill_path": path, "l2": "inputs larger than L2 (no flush)",
+                           "prefill_path": path, "segments": segments, "l2": "inputs larger than L2 (no flush)",
                            "parallelism": f"replicas x{world}"},
                 "roofline": roof,
                 "e2e": {"value": round(world * T / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "ms_per_step": round(e2e_ms, 4)},
                 "decode": dec_obj, "cpu_baseline": cpu, "clocks": clk,
-                "gpu_launches": prefill_launches(path) * args.steps + dec_launches}
+                "gpu_launches": prefill_launches(path, segments) * args.steps + dec_launches}
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()

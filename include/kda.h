@@ -142,14 +142,39 @@ typedef struct {
     size_t workspace_bytes;
     int* d_status;         /* optional device int for device-side conditions */
     int flags;             /* KDA_FLAG_* */
+    int segments;          /* tensor-core path: segments each sequence is cut into (below);
+                              0 = chosen from N*H and the SM count, 1 = none, 2..16 forced */
 } kda_prefill_args;
 
 #define KDA_FLAG_FORCE_SIMT 1 /* take the fp32 SIMT path even where tensor cores apply */
+
+/* Segment-parallel scan (tensor-core path).  One (sequence, head) is a chain
+ * of chunks, each depending on the state the previous one leaves.  When the
+ * batch has too few (sequence, head) units to fill the GPU, each sequence's
+ * chunks are cut into P contiguous segments of ceil(chunks / P) chunks.  Every
+ * step of the recurrence maps the state affinely, S -> (I - beta k k^T)
+ * Diag(e^g) S + beta k v^T, so a whole segment s maps its start state as
+ * S_{s+1} = M_s S_s + B_s, and each of its outputs as o_t = o_t' + S_s^T f_t.
+ * Segment 0 runs from the initial state as usual; every later segment runs
+ * twice, in parallel with the others: from a zero state (its outputs o_t'
+ * and B_s) and with v = 0 from the identity (f_t and M_s).  A second kernel
+ * composes S_1 .. S_{P-1} and the final state in order, and a third adds
+ * S_s^T f_t to o_t' and applies RMSNorm and the gate.  The results equal
+ * the single-pass ones up to rounding.  Workspace: 3 P N H D^2 + 2 T_total H D
+ * floats when P > 1, else none.  `segments` is ignored by the SIMT path. */
+#define KDA_MAX_SEGMENTS 16
 
 /* Bytes of workspace kda_prefill needs for these arguments (0 allowed). */
 kda_status kda_prefill_workspace_size(const kda_prefill_args* args, size_t* bytes);
 
 kda_status kda_prefill(const kda_prefill_args* args, kda_stream_t stream);
+
+/* The plan kda_prefill takes for these arguments on the current device:
+ * *tensor_core = 1 for the tcgen05 path, 0 for the fp32 SIMT path, and
+ * *segments = segments per sequence (1 on the SIMT path and when no
+ * segmenting applies).  Reads only the sizes, dtypes, flags and `segments`
+ * of args (no pointer is dereferenced); launches nothing. */
+kda_status kda_prefill_plan(const kda_prefill_args* args, int* tensor_core, int* segments);
 
 /* ------------------------------------------------------------------------
  * kda_prefill_noalloc -- kda_prefill for callers that cannot allocate device

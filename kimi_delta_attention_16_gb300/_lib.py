@@ -20,10 +20,13 @@ KDA_ERR_DEVICE_ARG = 6
 KDA_BF16 = 0
 KDA_FP32 = 1
 KDA_FLAG_FORCE_SIMT = 1
+KDA_MAX_SEGMENTS = 16
+ABI_VERSION = 10100  # kda_prefill_args with the `segments` field
 
 # Every symbol include/kda.h declares.
 EXPORTED = ("kda_status_string", "kda_last_error", "kda_version", "kda_short_conv",
-            "kda_prefill_workspace_size", "kda_prefill", "kda_prefill_noalloc", "kda_decode_step")
+            "kda_prefill_workspace_size", "kda_prefill", "kda_prefill_plan", "kda_prefill_noalloc",
+            "kda_decode_step")
 NOALLOC_SCRATCH_BYTES = 64 << 20  # KDA_NOALLOC_SCRATCH_BYTES in include/kda.h
 
 _vp = ctypes.c_void_p
@@ -46,7 +49,7 @@ class PrefillArgs(ctypes.Structure):
         ("eps_l2", _f), ("eps_rms", _f), ("scale", _f),
         ("initial_state", _vp), ("final_state", _vp), ("out", _vp),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
-        ("d_status", _vp), ("flags", _int),
+        ("d_status", _vp), ("flags", _int), ("segments", _int),
     ]
 
 
@@ -92,6 +95,9 @@ def load(auto_build: bool = True) -> ctypes.CDLL:
         lib.kda_last_error.argtypes = []
         lib.kda_version.restype = _int
         lib.kda_version.argtypes = []
+        if lib.kda_version() < ABI_VERSION:
+            raise RuntimeError(f"{path} has ABI version {lib.kda_version()}, this binding needs "
+                               f">= {ABI_VERSION}; rebuild it")
         lib.kda_short_conv.restype = _int
         lib.kda_short_conv.argtypes = [_vp, _i64, _vp, _vp, _vp, _int, _i64, _int, _int, _vp, _vp,
                                        _vp, _i64, _int, _f, _int, _vp, _vp]
@@ -100,6 +106,9 @@ def load(auto_build: bool = True) -> ctypes.CDLL:
                                                    ctypes.POINTER(ctypes.c_size_t)]
         lib.kda_prefill.restype = _int
         lib.kda_prefill.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
+        lib.kda_prefill_plan.restype = _int
+        lib.kda_prefill_plan.argtypes = [ctypes.POINTER(PrefillArgs), ctypes.POINTER(_int),
+                                         ctypes.POINTER(_int)]
         lib.kda_prefill_noalloc.restype = _int
         lib.kda_prefill_noalloc.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
         lib.kda_decode_step.restype = _int

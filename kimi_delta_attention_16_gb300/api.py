@@ -38,6 +38,23 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _same_cuda_device(**tensors) -> None:
+    """Every given tensor must live on one CUDA device: the library dereferences
+    these pointers only on the GPU, and a host pointer there would fault."""
+    dev = None
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError(f"{name} is on {t.device}; every tensor must be on a CUDA device")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, other tensors on {dev}")
+    if dev is not None and dev.index is not None and dev.index != torch.cuda.current_device():
+        raise ValueError(f"tensors are on {dev} but the current device is cuda:{torch.cuda.current_device()}")
+
+
 def _row_stride(t: torch.Tensor, H: int, D: int) -> int:
     """Row stride (elements) of a [T, H, D] view whose (H, D) block is dense."""
     if t.dim() != 3 or t.shape[1] != H or t.shape[2] != D:
@@ -74,6 +91,8 @@ def kda_short_conv(x: torch.Tensor, w: torch.Tensor, cu_seqlens, *, H: int, D: i
     if y is None:
         y = torch.empty((T, 3 * H * D), dtype=x.dtype, device=x.device)
     cu_dev, cu_host = _cu_pair(cu_seqlens, x.device)
+    _same_cuda_device(x=x, w=w, cu_seqlens=cu_dev, conv_state_in=conv_state_in,
+                      conv_state_out=conv_state_out, y=y, d_status=d_status)
     N = cu_host.shape[0] - 1
     st = lib.kda_short_conv(_p(x), x.stride(0) if T else 3 * H * D, _p(w), _p(cu_dev),
                             cu_host.ctypes.data_as(ctypes.c_void_p) if check_cu_on_host else None,
@@ -87,8 +106,12 @@ def kda_short_conv(x: torch.Tensor, w: torch.Tensor, cu_seqlens, *, H: int, D: i
 
 def _prefill_args(q, k, v, conv_w, g, beta, cu_dev, cu_host, *, chunk, gate, rms_w, eps_l2,
                   eps_rms, scale, initial_state, final_state, conv_state_in, conv_state_out, out,
-                  workspace, d_status, flags, check_cu_on_host):
+                  workspace, d_status, flags, check_cu_on_host, segments=0):
     T, H, D = q.shape
+    _same_cuda_device(q=q, k=k, v=v, conv_w=conv_w, g=g, beta=beta, cu_seqlens=cu_dev, gate=gate,
+                      rms_w=rms_w, initial_state=initial_state, final_state=final_state,
+                      conv_state_in=conv_state_in, conv_state_out=conv_state_out, out=out,
+                      workspace=workspace, d_status=d_status)
     xs = _row_stride(q, H, D)
     if _row_stride(k, H, D) != xs or _row_stride(v, H, D) != xs:
         raise ValueError("q, k and v must share one row stride")
@@ -115,22 +138,44 @@ def _prefill_args(q, k, v, conv_w, g, beta, cu_dev, cu_host, *, chunk, gate, rms
     a.workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     a.d_status = d_status.data_ptr() if d_status is not None else None
     a.flags = int(flags)
+    a.segments = int(segments)
     return a
 
 
-def kda_prefill_workspace_size(T_total: int, H: int, D: int, *, chunk: int = 64,
-                               io=torch.bfloat16, flags: int = 0) -> int:
+def kda_prefill_workspace_size(T_total: int, H: int, D: int, *, N: int = 1, chunk: int = 64,
+                               io=torch.bfloat16, flags: int = 0, segments: int = 0) -> int:
+    """Workspace bytes kda_prefill needs for N packed sequences of T_total tokens
+    in all (on the current device: the segment choice depends on its SM count)."""
     lib = _lib.load()
     a = _lib.PrefillArgs()
-    a.N, a.H, a.D, a.chunk, a.T_total = 1, H, D, chunk, T_total
+    a.N, a.H, a.D, a.chunk, a.T_total = N, H, D, chunk, T_total
     a.io = _DT[io]
     a.out_dtype = a.io
     a.flags = flags
+    a.segments = segments
     n = ctypes.c_size_t(0)
     st = lib.kda_prefill_workspace_size(ctypes.byref(a), ctypes.byref(n))
     if st:
         raise KDAError(st, "kda_prefill_workspace_size")
     return int(n.value)
+
+
+def kda_prefill_plan(T_total: int, H: int, D: int, *, N: int = 1, chunk: int = 64,
+                     io=torch.bfloat16, flags: int = 0, segments: int = 0):
+    """(path, segments) kda_prefill takes on the current device: path is "tc" for the
+    tcgen05 path or "simt" for the fp32 SIMT path; segments per sequence (1 = none)."""
+    lib = _lib.load()
+    a = _lib.PrefillArgs()
+    a.N, a.H, a.D, a.chunk, a.T_total = N, H, D, chunk, T_total
+    a.io = _DT[io]
+    a.out_dtype = a.io
+    a.flags = flags
+    a.segments = segments
+    tc, seg = ctypes.c_int(0), ctypes.c_int(1)
+    st = lib.kda_prefill_plan(ctypes.byref(a), ctypes.byref(tc), ctypes.byref(seg))
+    if st:
+        raise KDAError(st, "kda_prefill_plan")
+    return ("tc" if tc.value else "simt"), int(seg.value)
 
 
 def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, conv_w: torch.Tensor,
@@ -142,8 +187,12 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, conv_w: torch
                 conv_state_in: Optional[torch.Tensor] = None,
                 conv_state_out: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                 out_dtype=None, workspace: Optional[torch.Tensor] = None, d_status=None,
-                flags: int = 0, check_cu_on_host: bool = True, stream=None):
+                flags: int = 0, check_cu_on_host: bool = True, stream=None, segments: int = 0):
     """The whole KDA layer over packed sequences; returns (out, final_state or None).
+
+    segments: tensor-core path only -- 0 lets the library cut long sequences into
+    parallel segments when the batch has too few (sequence, head) units to fill the
+    GPU, 1 disables that, 2..16 forces that many segments per sequence.
 
     q, k, v: [T, H, D] raw projections (bf16 or fp32; rows may be strided views of
     one fused buffer); conv_w [3, H*D, 4] fp32; g [T, H, D] fp32; beta [T, H] fp32;
@@ -163,7 +212,7 @@ def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, conv_w: torch
                       initial_state=initial_state, final_state=final_state,
                       conv_state_in=conv_state_in, conv_state_out=conv_state_out, out=out,
                       workspace=workspace, d_status=d_status, flags=flags,
-                      check_cu_on_host=check_cu_on_host)
+                      check_cu_on_host=check_cu_on_host, segments=segments)
     if workspace is None:
         n = ctypes.c_size_t(0)
         st = lib.kda_prefill_workspace_size(ctypes.byref(a), ctypes.byref(n))
@@ -220,6 +269,8 @@ def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.
     N, H, D = q.shape
     if out is None:
         out = torch.empty((N, H, D), dtype=out_dtype or q.dtype, device=q.device)
+    _same_cuda_device(q=q, k=k, v=v, g=g, beta=beta, conv_w=conv_w, state=state,
+                      conv_state=conv_state, gate=gate, rms_w=rms_w, out=out, d_status=d_status)
     a = _lib.DecodeArgs()
     a.N, a.H, a.D = N, H, D
     a.io = _DT[q.dtype]

@@ -107,6 +107,8 @@ kda_status validate_prefill(const kda_prefill_args* a) {
         return fail(KDA_ERR_INVALID_ARG, "unknown dtype (io=%d out=%d)", (int)a->io, (int)a->out_dtype);
     if ((int64_t)a->H * a->D * 3 > (int64_t)1 << 30)
         return fail(KDA_ERR_UNSUPPORTED, "H*D too large");
+    if (a->segments < 0 || a->segments > KDA_MAX_SEGMENTS)
+        return fail(KDA_ERR_INVALID_ARG, "segments = %d not in [0, %d]", a->segments, KDA_MAX_SEGMENTS);
     if (a->N > 0 && !a->cu_seqlens) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is NULL");
     if (a->cu_seqlens_host) {
         kda_status st = check_host_cu(a->cu_seqlens_host, a->N, a->T_total);
@@ -202,7 +204,7 @@ const char* kda_status_string(int status) {
 
 const char* kda_last_error(void) { return g_last_error.c_str(); }
 
-int kda_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+int kda_version(void) { return 1 * 10000 + 1 * 100 + 0; }
 
 kda_status kda_short_conv(const void* x, int64_t x_row_stride, const float* w,
                           const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int N,
@@ -259,7 +261,24 @@ kda_status kda_prefill_workspace_size(const kda_prefill_args* args, size_t* byte
     if (!supported_d(args->D) || !kda::chunk_simt_supported(args->D, args->chunk))
         return fail(KDA_ERR_UNSUPPORTED, "unsupported D=%d / chunk=%d", args->D, args->chunk);
     if (args->T_total < 0 || args->H < 1 || args->N < 0) return fail(KDA_ERR_INVALID_ARG, "bad sizes");
+    if (args->segments < 0 || args->segments > KDA_MAX_SEGMENTS)
+        return fail(KDA_ERR_INVALID_ARG, "segments = %d not in [0, %d]", args->segments, KDA_MAX_SEGMENTS);
     *bytes = plan_prefill(*args).total;
+    return ok();
+}
+
+kda_status kda_prefill_plan(const kda_prefill_args* args, int* tensor_core, int* segments) {
+    if (!args || !tensor_core || !segments) return fail(KDA_ERR_INVALID_ARG, "NULL argument");
+    *tensor_core = 0;
+    *segments = 1;
+    if (!supported_d(args->D) || !kda::chunk_simt_supported(args->D, args->chunk))
+        return fail(KDA_ERR_UNSUPPORTED, "unsupported D=%d / chunk=%d", args->D, args->chunk);
+    if (args->T_total < 0 || args->H < 1 || args->N < 0) return fail(KDA_ERR_INVALID_ARG, "bad sizes");
+    if (args->segments < 0 || args->segments > KDA_MAX_SEGMENTS)
+        return fail(KDA_ERR_INVALID_ARG, "segments = %d not in [0, %d]", args->segments, KDA_MAX_SEGMENTS);
+    const PrefillPlan p = plan_prefill(*args);
+    *tensor_core = p.tc ? 1 : 0;
+    *segments = p.tc ? kda::tc_segments(*args) : 1;
     return ok();
 }
 

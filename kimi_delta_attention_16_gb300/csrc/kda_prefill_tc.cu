@@ -8,7 +8,11 @@
 // One CTA owns one (sequence, head) and walks its chunks in order; every
 // stage of the layer runs inside it (conv + SiLU + L2, the chunk algebra,
 // the state carry, RMSNorm + gate), so HBM sees only the layer's own inputs
-// and outputs.  Per chunk, with local token index r, G = cumulative log-decay,
+// and outputs.  With a segmented plan (P > 1, few units) the grid holds
+// 2P - 1 roles per unit: role 0 walks segment 0 from the initial state as
+// above; role 2s - 1 walks segment s from a zero state and role 2s walks it
+// with v = 0 from the identity.  Those two write scale * o in fp32 (no
+// epilogue) and their end states; the combine and fix-up kernels finish.  Per chunk, with local token index r, G = cumulative log-decay,
 // w = beta e (all per key channel c, value channel j):
 //
 //   G1  [M ; A]  = X1 . B1^T          intra-chunk q.k and beta k.k with decay  (N = 96)
@@ -149,7 +153,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
              const bf16* __restrict__ gate, const float* __restrict__ rms_w, float eps_l2,
              float eps_rms, float scale, const float* __restrict__ S0, float* __restrict__ S_fin,
              To* __restrict__ out, const int32_t* __restrict__ cu, int64_t T_total, int H,
-             int* d_status) {
+             int* d_status, SegPlan sp) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bars[4];  // G1 done, G3 done, G4 done, G5+G6 done
     __shared__ uint32_t s_tbase;
@@ -177,10 +181,20 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     const int qd = warp & 3, qt = warp >> 2;
     const int L = qd * 32 + lane;                 // this thread's TMEM lane
     const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
-    const int h = blockIdx.x % H, n = blockIdx.x / H;
+    // role of this CTA (the grid holds units * (2P - 1) CTAs)
+    const int units = (int)(gridDim.x / (2 * sp.P - 1));
+    const int role = (int)(blockIdx.x / units), u = (int)(blockIdx.x % units);
+    const int h = u % H, n = u / H;
+    const int seg = (role + 1) >> 1;
+    const bool zero_run = (role & 1) != 0;           // segment >= 1 from S = 0
+    const bool ident_run = role > 0 && !zero_run;    // segment >= 1 from S = I with v = 0
+    const bool raw_out = role > 0;                   // fp32 scale * o, no epilogue
+    const bf16* __restrict__ gate_p = raw_out ? nullptr : gate;
     const int64_t HD = (int64_t)H * kD;
     int64_t s0, s1;
     seq_range(cu, n, T_total, s0, s1);
+    int64_t cb, ce;  // this CTA's chunks [cb, ce) of the sequence
+    seg_chunk_range((s1 - s0 + kC - 1) / kC, sp.P, seg, cb, ce);
 
     if (warp == 0) {
         tmem_alloc(&s_tbase, kTmemCols);
@@ -203,9 +217,10 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     const int j = L;
     float Sreg[32];
     {
-        const float* src = S0 ? S0 + (((int64_t)n * H + h) * kD) * kD : nullptr;
+        const float* src = (role == 0 && S0) ? S0 + (((int64_t)n * H + h) * kD) * kD : nullptr;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) Sreg[i] = src ? src[(int64_t)(32 * qt + i) * kD + j] : 0.f;
+        for (int i = 0; i < 32; ++i)
+            Sreg[i] = src ? src[(int64_t)(32 * qt + i) * kD + j] : (ident_run && 32 * qt + i == j ? 1.f : 0.f);
     }
     auto store_state_operand = [&]() {  // S^T hi/lo -> TMEM columns [0,128)
         uint32_t hi[16], lo[16];
@@ -222,10 +237,9 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     const uint32_t id_64 = idesc_bf16(128, 64, false, false);
     const uint32_t id_g6 = idesc_bf16(128, 128, false, true);
     bool failed = false;
-    const int n_chunks = (int)((s1 - s0 + kC - 1) / kC);
 
     // q/k rows of chunk cj (t0-3 .. t0+63 within the sequence) -> B3 region, one cp.async group
-    auto stage_qk = [&](int cj) {
+    auto stage_qk = [&](int64_t cj) {
         const int64_t tc0 = s0 + (int64_t)cj * kC;
         for (int idx = tid; idx < 2 * kRawRows * 16; idx += kThreads) {
             const int part = idx >= kRawRows * 16 ? 1 : 0;
@@ -239,7 +253,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         cp_async_commit();
     };
     // G = cumsum(g) of chunk cj (four quarters of 16 tokens) into sG, beta into sBeta (one barrier inside)
-    auto compute_G = [&](int cj) {
+    auto compute_G = [&](int64_t cj) {
         const int64_t tc0 = s0 + (int64_t)cj * kC;
         const int Lcj = (int)((s1 - tc0) < kC ? (s1 - tc0) : kC);
         const int c = tid & (kD - 1), hq = tid >> 7;
@@ -263,18 +277,18 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
 #pragma unroll
         for (int e = 0; e < 16; ++e) sG[(16 * hq + e) * kGs + c] = gv[e] + base;
     };
-    if (n_chunks > 0) {
-        stage_qk(0);
-        compute_G(0);
+    if (cb < ce) {
+        stage_qk(cb);
+        compute_G(cb);
     }
 
-    for (int ci = 0; ci < n_chunks && !failed; ++ci) {
-        const int64_t t0 = s0 + (int64_t)ci * kC;
+    for (int64_t ci = cb; ci < ce && !failed; ++ci) {
+        const int64_t t0 = s0 + ci * kC;
         const int Lc = (int)((s1 - t0) < kC ? (s1 - t0) : kC);
-        const uint32_t par = ci & 1;
+        const uint32_t par = (uint32_t)(ci - cb) & 1u;
 
         // ------------------------------------------------ A0: L2 prefetch of the next chunk's rows
-        if (ci + 1 < n_chunks) {
+        if (ci + 1 < ce) {
             // next chunk's rows into L2, one 128-byte line per thread and step
             const int64_t tn = t0 + kC;
             const int rr = tid & 63, which = tid >> 6;  // 8 line slots per row
@@ -283,11 +297,11 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 const char* base;
                 if (which < 2) base = reinterpret_cast<const char*>(q + row * xs + (int64_t)h * kD) + 128 * which;
                 else if (which < 4) base = reinterpret_cast<const char*>(k + row * xs + (int64_t)h * kD) + 128 * (which - 2);
-                else if (which < 6) base = reinterpret_cast<const char*>(v + row * xs + (int64_t)h * kD) + 128 * (which - 4);
+                else if (which < 6) base = ident_run ? nullptr : reinterpret_cast<const char*>(v + row * xs + (int64_t)h * kD) + 128 * (which - 4);
                 else base = reinterpret_cast<const char*>(g + (row * H + h) * kD) + 256 * (which - 6);
-                prefetch_line_l2(base);
+                if (base) prefetch_line_l2(base);
                 if (which >= 6) prefetch_line_l2(base + 128);
-                if (gate && which < 2) prefetch_line_l2(reinterpret_cast<const char*>(gate + (row * H + h) * kD) + 128 * which);
+                if (gate_p && which < 2) prefetch_line_l2(reinterpret_cast<const char*>(gate_p + (row * H + h) * kD) + 128 * which);
             }
         }
 
@@ -498,17 +512,18 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         fence_after_sync();
         {
             // G1 is done with B1: stage v rows t0-3 .. t0+63 and gate rows t0 .. t0+Lc-1 there
-            for (int idx = tid; idx < kRawRows * 16; idx += kThreads) {
-                const int tr = idx >> 4, vec = idx & 15;
-                const int64_t pr = t0 - 3 + tr;
-                if (pr >= s0 && pr < s1)
-                    cp_async16(sbase + kOffRawV + tr * kRawStride + 16 * vec, v + pr * xs + (int64_t)h * kD + 8 * vec);
-            }
-            if (gate)
+            if (!ident_run)
+                for (int idx = tid; idx < kRawRows * 16; idx += kThreads) {
+                    const int tr = idx >> 4, vec = idx & 15;
+                    const int64_t pr = t0 - 3 + tr;
+                    if (pr >= s0 && pr < s1)
+                        cp_async16(sbase + kOffRawV + tr * kRawStride + 16 * vec, v + pr * xs + (int64_t)h * kD + 8 * vec);
+                }
+            if (gate_p)
                 for (int idx = tid; idx < kC * 16; idx += kThreads) {
                     const int rr = idx >> 4, vec = idx & 15;
                     if (rr < Lc)
-                        cp_async16(sbase + kOffGateT + rr * 256 + 16 * vec, gate + ((t0 + rr) * H + h) * kD + 8 * vec);
+                        cp_async16(sbase + kOffGateT + rr * 256 + 16 * vec, gate_p + ((t0 + rr) * H + h) * kD + 8 * vec);
                 }
             cp_async_commit();
         }
@@ -640,9 +655,10 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 return cs_in ? to_f(cs_in[((int64_t)n * 3 * HD + 2 * HD + (int64_t)h * kD + j) * 3 + 3 + pos]) : 0.f;
             };
             const int64_t tb0 = t0 + i0;
-            float p0 = (i0 < Lc) ? raw(tb0 - 3) : 0.f;
-            float p1 = (i0 < Lc) ? raw(tb0 - 2) : 0.f;
-            float p2 = (i0 < Lc) ? raw(tb0 - 1) : 0.f;
+            const bool vrows = i0 < Lc && !ident_run;  // the identity-start run takes v = 0
+            float p0 = vrows ? raw(tb0 - 3) : 0.f;
+            float p1 = vrows ? raw(tb0 - 2) : 0.f;
+            float p2 = vrows ? raw(tb0 - 1) : 0.f;
             uint32_t pv[16];
             tmem_ld16(tb + lane_off + kColP + i0, pv);
             tmem_ld_wait();
@@ -654,7 +670,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 for (int f = 0; f < 2; ++f) {
                     const int i = i0 + e + f;
                     float xr = 0.f, vr = 0.f;
-                    if (i < Lc) {
+                    if (i < Lc && !ident_run) {
                         xr = to_f(vt[(uint32_t)(i + 3) * (kRawStride / 2) + j]);
                         vr = silu_fast(w.x * p0 + w.y * p1 + w.z * p2 + w.w * xr);
                     }
@@ -671,7 +687,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         __syncthreads();
 
         // ------------------------------------------------ E: G4  W^T = R^T T^T; next chunk's q/k rows -> B3
-        if (ci + 1 < n_chunks) stage_qk(ci + 1);  // G3 finished with B3 (waited in D)
+        if (ci + 1 < ce) stage_qk(ci + 1);  // G3 finished with B3 (waited in D)
         if (tid == 0) {
             fence_after_sync();
             const uint32_t tbf = sbase + kOffR2;
@@ -727,7 +743,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             }
             mma_commit(&bars[3]);
         }
-        if (ci + 1 < n_chunks) compute_G(ci + 1);  // overlaps G5/G6; the A/T tile in R1 is dead
+        if (ci + 1 < ce) compute_G(ci + 1);  // overlaps G5/G6; the A/T tile in R1 is dead
         failed = !__syncthreads_and(mbar_wait(&bars[3], par));
         if (failed) break;
         fence_after_sync();
@@ -751,6 +767,11 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             float o[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) o[e] = scale * __uint_as_float(ov[e]);
+            if (raw_out) {
+                float* ot = reinterpret_cast<float*>(sm + kOffYT);  // [64][128] fp32 o tile
+#pragma unroll
+                for (int e = 0; e < 16; ++e) ot[(16 * qt + e) * kD + j] = o[e];
+            } else {
             // sum over the warp's 32 channels of o^2 for each of its 16 tokens:
             // halve across lanes 8, 4, 2, 1 apart, then fold the two 16-lane halves
             float sq[16];
@@ -779,14 +800,23 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             for (int e = 0; e < 16; ++e) {
                 const int rr = 16 * qt + e;
                 float yv = o[e] * sInv[rr] * wj;
-                if (gate) yv *= sigmoid_fast(to_f(gt[rr * kD + j]));
+                if (gate_p) yv *= sigmoid_fast(to_f(gt[rr * kD + j]));
                 yt[rr * kD + j] = from_f<To>(yv);
+            }
             }
         }
         fence_before_sync();
         __syncthreads();  // every dS read is done before S^T overwrites those columns; y tile complete
         fence_after_sync();
-        {
+        if (raw_out) {
+            // fp32 o rows -> the zero-start or identity-start buffer, 16-byte coalesced stores
+            float* dst = zero_run ? sp.o_loc : sp.f_tr;
+            const uint4* ot = reinterpret_cast<const uint4*>(sm + kOffYT);
+            for (int idx = tid; idx < Lc * 32; idx += kThreads) {
+                const int rr = idx >> 5, vec = idx & 31;
+                *reinterpret_cast<uint4*>(dst + ((t0 + rr) * H + h) * kD + 4 * vec) = ot[rr * 32 + vec];
+            }
+        } else {
             // y rows -> out, 16-byte coalesced stores
             constexpr int kVpr = kD * (int)sizeof(To) / 16;
             const uint4* yt = reinterpret_cast<const uint4*>(sm + kOffYT);
@@ -804,10 +834,13 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
 
     if (failed) {
         if (tid == 0) flag_status(d_status, KDA_ERR_TIMEOUT);
-    } else if (S_fin) {
-        float* dst = S_fin + (((int64_t)n * H + h) * kD) * kD;
+    } else {
+        float* dst = sp.P == 1 ? (S_fin ? S_fin + (((int64_t)n * H + h) * kD) * kD : nullptr)
+                               : (ident_run ? sp.trans : sp.end_state) + (((int64_t)u * sp.P + seg) * kD) * kD;
+        if (dst) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) dst[(int64_t)(32 * qt + i) * kD + j] = Sreg[i];
+            for (int i = 0; i < 32; ++i) dst[(int64_t)(32 * qt + i) * kD + j] = Sreg[i];
+        }
     }
     fence_before_sync();
     __syncthreads();
@@ -815,30 +848,64 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
 }
 
 int g_tc_arch[64];  // per device: 0 unknown, 1 supported, 2 not supported
+int g_sm_count[64];
 
 bool device_supports_tc() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
     if (g_tc_arch[dev] == 0) {
-        int major = 0, minor = 0;
+        int major = 0, minor = 0, sms = 0;
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        g_sm_count[dev] = sms > 0 ? sms : 1;
         g_tc_arch[dev] = (major == 10 && minor == 3) ? 1 : 2;
     }
     return g_tc_arch[dev] == 1;
 }
 
+int device_sm_count() {
+    int dev = 0;
+    if (!device_supports_tc() || cudaGetDevice(&dev) != cudaSuccess) return 1;
+    return g_sm_count[dev];
+}
+
+// Fewest chunks per segment the automatic choice allows: below this the fix-up
+// and the doubled runs cost more than the shorter chain saves.
+constexpr int64_t kMinSegChunks = 32;
+
+// Workspace layout of a segmented launch (offsets in bytes, 256-aligned).
+struct SegLayout {
+    size_t end_state, trans, start, o_loc, f_tr, total;
+};
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+SegLayout seg_layout(const kda_prefill_args& a, int P) {
+    SegLayout l{};
+    if (P <= 1) return l;
+    const size_t st = round256((size_t)a.N * a.H * P * kD * kD * sizeof(float));
+    const size_t ob = round256((size_t)a.T_total * a.H * kD * sizeof(float));
+    l.end_state = 0;
+    l.trans = st;
+    l.start = 2 * st;
+    l.o_loc = 3 * st;
+    l.f_tr = 3 * st + ob;
+    l.total = 3 * st + 2 * ob;
+    return l;
+}
+
 template <typename To>
-cudaError_t tc_launch(const kda_prefill_args& a, cudaStream_t s) {
+cudaError_t tc_launch(const kda_prefill_args& a, const SegPlan& sp, cudaStream_t s) {
     auto kern = k_tc_prefill<To>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t xs = a.qkv_row_stride ? a.qkv_row_stride : (int64_t)a.H * a.D;
-    const unsigned grid = (unsigned)((int64_t)a.N * a.H);
+    const unsigned grid = (unsigned)((int64_t)a.N * a.H * (2 * sp.P - 1));
     kern<<<grid, kThreads, kSmemBytes, s>>>(
         (const bf16*)a.q, (const bf16*)a.k, (const bf16*)a.v, xs, a.conv_w, (const bf16*)a.conv_state_in,
         a.g, a.beta, (const bf16*)a.gate, a.rms_w, a.eps_l2, a.eps_rms, a.scale, a.initial_state,
-        a.final_state, (To*)a.out, a.cu_seqlens, a.T_total, a.H, a.d_status);
+        a.final_state, (To*)a.out, a.cu_seqlens, a.T_total, a.H, a.d_status, sp);
     return cudaGetLastError();
 }
 
@@ -849,11 +916,40 @@ bool tc_prefill_applies(const kda_prefill_args& a) {
            device_supports_tc();
 }
 
-size_t tc_prefill_workspace(const kda_prefill_args&) { return 0; }
+int tc_segments(const kda_prefill_args& a) {
+    if (a.segments > 0) return a.segments < KDA_MAX_SEGMENTS ? a.segments : KDA_MAX_SEGMENTS;
+    const int64_t units = (int64_t)a.N * a.H;
+    if (units <= 0 || a.T_total <= 0) return 1;
+    // one wave of CTAs: 2P - 1 per unit must fit the SMs (one CTA per SM)
+    int64_t P = ((int64_t)device_sm_count() / units + 1) / 2;
+    const int64_t avg_chunks = a.T_total / ((int64_t)a.N * kC);
+    if (P > avg_chunks / kMinSegChunks) P = avg_chunks / kMinSegChunks;
+    if (P > KDA_MAX_SEGMENTS) P = KDA_MAX_SEGMENTS;
+    if (units * (2 * P - 1) > 0x7fffffffLL) P = 1;
+    return P < 1 ? 1 : (int)P;
+}
 
-cudaError_t launch_tc_prefill(const kda_prefill_args& a, char*, cudaStream_t s) {
-    if ((int64_t)a.N * a.H == 0) return cudaSuccess;
-    return a.out_dtype == KDA_FP32 ? tc_launch<float>(a, s) : tc_launch<bf16>(a, s);
+size_t tc_prefill_workspace(const kda_prefill_args& a) { return seg_layout(a, tc_segments(a)).total; }
+
+cudaError_t launch_tc_prefill(const kda_prefill_args& a, char* ws, cudaStream_t s) {
+    const int64_t units = (int64_t)a.N * a.H;
+    if (units == 0) return cudaSuccess;
+    const int P = tc_segments(a);
+    SegPlan sp{};
+    sp.P = P;
+    if (P > 1) {
+        const SegLayout l = seg_layout(a, P);
+        sp.end_state = reinterpret_cast<float*>(ws + l.end_state);
+        sp.trans = reinterpret_cast<float*>(ws + l.trans);
+        sp.start = reinterpret_cast<float*>(ws + l.start);
+        sp.o_loc = reinterpret_cast<float*>(ws + l.o_loc);
+        sp.f_tr = reinterpret_cast<float*>(ws + l.f_tr);
+    }
+    cudaError_t e = a.out_dtype == KDA_FP32 ? tc_launch<float>(a, sp, s) : tc_launch<bf16>(a, sp, s);
+    if (e != cudaSuccess || P == 1) return e;
+    if ((e = launch_seg_combine(sp, (int)units, a.final_state, s)) != cudaSuccess) return e;
+    return launch_seg_fixup(sp, a.cu_seqlens, a.N, a.T_total, a.H, (const bf16*)a.gate, a.rms_w,
+                            a.eps_rms, a.out, a.out_dtype, device_sm_count(), a.d_status, s);
 }
 
 }  // namespace kda

@@ -9,10 +9,49 @@ namespace kda {
 // bf16 inputs) and this device supports it.
 bool tc_prefill_applies(const kda_prefill_args& a);
 
+// Segments per (sequence, head) the tensor-core path cuts each sequence into
+// (1 = none): args.segments when set, else chosen so that the launch fills the
+// SMs in one wave.
+int tc_segments(const kda_prefill_args& a);
+
 // Scratch bytes the tensor-core path needs.
 size_t tc_prefill_workspace(const kda_prefill_args& a);
 
 // Enqueues the tensor-core prefill; `ws` has tc_prefill_workspace(a) bytes.
 cudaError_t launch_tc_prefill(const kda_prefill_args& a, char* ws, cudaStream_t s);
+
+// ---------------------------------------------------------------- segment-parallel scan
+// Buffers of one segmented launch (P > 1), all in the caller's workspace.  A
+// unit u = n * H + h is one (sequence, head).
+struct SegPlan {
+    int P;             // segments per unit; 1 = one CTA walks each whole sequence
+    float* end_state;  // [units][P][D][D]: segment 0's end state, then B_s (zero-start runs)
+    float* trans;      // [units][P][D][D]: M_s, the end states of the identity-start runs
+    float* start;      // [units][P][D][D]: S_s, the composed start state of segment s >= 1
+    float* o_loc;      // [T][H][D]: scale * o of the zero-start runs (tokens of segments >= 1)
+    float* f_tr;       // [T][H][D]: scale * o of the identity-start runs, v = 0
+};
+
+// Chunks [cb, ce) of segment s when a sequence of nc chunks is cut into P
+// segments of ceil(nc / P) chunks (trailing segments may be short or empty).
+__host__ __device__ __forceinline__ void seg_chunk_range(int64_t nc, int P, int s, int64_t& cb,
+                                                         int64_t& ce) {
+    const int64_t sl = (nc + P - 1) / P;
+    const int64_t b = (int64_t)s * sl;
+    cb = b < nc ? b : nc;
+    ce = cb + sl < nc ? cb + sl : nc;
+}
+
+// Composes, per unit and in segment order, S_1 = end_state[0] and
+// S_{s+1} = M_s S_s + B_s; writes S_1 .. S_{P-1} to sp.start and S_P to S_fin
+// (when non-NULL, [N][H][D][D]).
+cudaError_t launch_seg_combine(const SegPlan& sp, int units, float* S_fin, cudaStream_t s);
+
+// For every token of segments s >= 1: o = o_loc + S_s^T f (tensor cores), then
+// y = RMSNorm(o) * rms_w * sigmoid(gate) -> out (bf16 or fp32 rows [T][H][D]).
+// A tensor-core wait that times out sets KDA_ERR_TIMEOUT in d_status.
+cudaError_t launch_seg_fixup(const SegPlan& sp, const int32_t* cu, int N, int64_t T_total, int H,
+                             const bf16* gate, const float* rms_w, float eps_rms, void* out,
+                             kda_dtype out_dt, int sms, int* d_status, cudaStream_t s);
 
 }  // namespace kda

@@ -100,10 +100,12 @@ def _uniform(shape, lo, hi, gen, device):
 
 def make_prefill(name: str = "tiny_fp32", seed: int = 0, device="cpu", *, N=None, T=None,
                  lengths=None, H=None, D=None, chunk=None, io=None, gate=True, rms_w="ones",
-                 s0_std=None, conv_state=False) -> PrefillInputs:
+                 s0_std=None, conv_state=False, g_range=(-5.0, 0.0)) -> PrefillInputs:
     """Seeded prefill inputs for a named workload, with optional overrides.
 
     ``lengths`` (a list) overrides N/T with an explicit varlen mix.
+    ``g_range``: the log-decay law U[lo, hi]; a range near 0 (slow forgetting)
+    makes the state carry information across many chunks.
     ``rms_w``: "ones", "random" (1 + 0.1 N(0,1)) or None (no RMSNorm weight).
     ``conv_state``: also draw a rolling conv state ~N(0,1) per sequence.
     """
@@ -130,7 +132,7 @@ def make_prefill(name: str = "tiny_fp32", seed: int = 0, device="cpu", *, N=None
     k = _normal((Tt, H, D), 1.0, gen, device, dt)
     v = _normal((Tt, H, D), 1.0, gen, device, dt)
     conv_w = _normal((3, H * D, 4), 0.5, gen, device, torch.float32)
-    g = _uniform((Tt, H, D), -5.0, 0.0, gen, device)
+    g = _uniform((Tt, H, D), float(g_range[0]), float(g_range[1]), gen, device)
     beta = _uniform((Tt, H), 0.0, 1.0, gen, device)
     gt = _normal((Tt, H, D), 1.0, gen, device, dt) if gate else None
     if rms_w == "ones":

@@ -114,6 +114,32 @@ def test_workspace_size_matches_layout():
             assert n.value == r(T * 3 * H * D * 4) + r(T * H * D * 4)
 
 
+def test_segments_argument_is_range_checked():
+    lib = _lib.load()
+    for seg, want in [(-1, _lib.KDA_ERR_INVALID_ARG), (_lib.KDA_MAX_SEGMENTS + 1, _lib.KDA_ERR_INVALID_ARG),
+                      (0, 0), (1, 0), (_lib.KDA_MAX_SEGMENTS, 0)]:
+        a, cu = _args(T_total=8192, H=4, D=128, chunk=64)
+        a.segments = seg
+        n = ctypes.c_size_t()
+        assert lib.kda_prefill_workspace_size(ctypes.byref(a), ctypes.byref(n)) == want
+        tc, p = ctypes.c_int(-1), ctypes.c_int(-1)
+        assert lib.kda_prefill_plan(ctypes.byref(a), ctypes.byref(tc), ctypes.byref(p)) == want
+        if seg < 0 or seg > _lib.KDA_MAX_SEGMENTS:
+            assert _prefill(a) == _lib.KDA_ERR_INVALID_ARG
+
+
+def test_plan_without_a_tensor_core_device_is_simt():
+    """With no sm_103 device current (this host has none) every call plans the SIMT path."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    lib = _lib.load()
+    a, cu = _args(T_total=1 << 20, H=24, D=128, chunk=64)
+    tc, p = ctypes.c_int(-1), ctypes.c_int(-1)
+    assert lib.kda_prefill_plan(ctypes.byref(a), ctypes.byref(tc), ctypes.byref(p)) == 0
+    assert (tc.value, p.value) == (0, 1)
+
+
 def test_short_conv_rejects_bad_arguments():
     lib = _lib.load()
     cu = np.array([0, 10], np.int32)
@@ -155,3 +181,21 @@ def test_decode_rejects_bad_arguments():
     assert call(qkv_row_stride=10) == _lib.KDA_ERR_INVALID_ARG
     assert call(out=FAKE + 0x100000) == _lib.KDA_ERR_INVALID_ARG
     assert call(N=-1) == _lib.KDA_ERR_INVALID_ARG
+
+
+def test_binding_rejects_host_tensors_before_any_call():
+    """Host tensors never reach the library: it would hand their pointers to a kernel."""
+    import torch
+    import kimi_delta_attention_16_gb300 as kda
+    from kimi_delta_attention_16_gb300 import synth
+    inp = synth.make_prefill("tiny_fp32", seed=0)  # host tensors
+    with pytest.raises(ValueError, match="CUDA device"):
+        kda.kda_prefill(inp.q, inp.k, inp.v, inp.conv_w, inp.g, inp.beta, inp.cu_seqlens,
+                        chunk=inp.chunk, gate=inp.gate, rms_w=inp.rms_w)
+    x = torch.zeros((inp.T, 3 * inp.H * inp.D))
+    with pytest.raises(ValueError, match="CUDA device"):
+        kda.kda_short_conv(x, inp.conv_w.reshape(-1, 4), inp.cu_seqlens, H=inp.H, D=inp.D)
+    dec = synth.make_decode(seed=0, N=2, H=2, D=16, ring=1)
+    with pytest.raises(ValueError, match="CUDA device"):
+        kda.kda_decode_step(dec.q[0], dec.k[0], dec.v[0], dec.g[0], dec.beta[0], dec.conv_w,
+                            dec.state, dec.conv_state, gate=dec.gate[0], rms_w=dec.rms_w)
