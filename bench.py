@@ -195,8 +195,15 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     if args.mode == "decode":
         return run_decode_only(args, world, rank, local, pg, dev, peaks, peak_src)
+    if args.mode == "verify":  # profiling aid: only the multi-token decode loop
+        obj, _ = time_multi_token(args, pg, dev, torch.cuda.current_stream(), peaks, peak_src, world)
+        if rank == 0:
+            print(f"multi-token decode {obj['metric']}: {obj['ms_per_step']:.4f} ms/step, "
+                  f"{obj['roofline']['frac']:.3f} of HBM", flush=True)
+        return
     if args.mode == "prefill":
         args.decode_steps = 0
+        args.verify_steps = 0
     inp = synth.make_prefill(args.workload, seed=1, device=dev)
     N, T, H, D = inp.N, inp.T, inp.H, inp.D
     path, segments, ws_bytes = prefill_path(inp)
@@ -324,6 +331,11 @@ def run_ours(args):
                                 "peak_source": peak_src,
                                 "traffic": recorded_traffic("decode_decode_256"),
                                 "algorithmic_bytes": dbytes}}
+    # multi-token decode (speculative verification): 256 sequences x 4 new tokens per step
+    mt_obj = None
+    mt_launches = 0
+    if args.verify_steps > 0:
+        mt_obj, mt_launches = time_multi_token(args, pg, dev, stream, peaks, peak_src, world)
     clk = clocks.stop()
 
     cpu = None
@@ -344,11 +356,69 @@ def run_ours(args):
                 "e2e": {"value": round(world * T / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "ms_per_step": round(e2e_ms, 4)},
-                "decode": dec_obj, "cpu_baseline": cpu, "clocks": clk,
-                "gpu_launches": prefill_launches(path, segments) * args.steps + dec_launches}
+                "decode": dec_obj, "multi_token_decode": mt_obj, "cpu_baseline": cpu, "clocks": clk,
+                "gpu_launches": prefill_launches(path, segments) * args.steps + dec_launches + mt_launches}
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+
+
+def time_multi_token(args, pg, dev, stream, peaks, peak_src, world, t_new=4, ring=8):
+    """kda_prefill on 256 sequences x t_new tokens continuing from carried states and conv
+    states (the recurrent path): the decode workload's inputs, t_new consecutive tokens per
+    call, from a ring of `ring` packed steps (larger than L2 together with the states)."""
+    import torch
+    import kimi_delta_attention_16_gb300 as kda
+    from kimi_delta_attention_16_gb300 import synth
+    dec = synth.make_decode(seed=6, device=dev, N=args.decode_n, ring=t_new * ring)
+    N, H, D = dec.N, dec.H, dec.D
+
+    def pack(x, r):  # ring entries r*t_new .. +t_new-1 -> sequence-major token rows
+        y = x[r * t_new:(r + 1) * t_new]
+        return y.transpose(0, 1).reshape(N * t_new, *y.shape[2:]).contiguous()
+
+    steps_in = [{k: pack(getattr(dec, k), r) for k in ("q", "k", "v", "gate", "g", "beta")}
+                for r in range(ring)]
+    cu = synth.cu_from_lengths([t_new] * N)
+    cu_pair = (torch.from_numpy(cu).to(dev), cu)
+    path = kda.kda_prefill_plan(N * t_new, H, D, cu_seqlens=cu)[0]
+    out = torch.empty((N * t_new, H, D), dtype=torch.bfloat16, device=dev)
+    cs = [dec.conv_state, torch.empty_like(dec.conv_state)]
+
+    def mstep(i):
+        x = steps_in[i % ring]
+        kda.kda_prefill(x["q"], x["k"], x["v"], dec.conv_w, x["g"], x["beta"], cu_pair,
+                        gate=x["gate"], rms_w=dec.rms_w, initial_state=dec.state,
+                        final_state=dec.state, conv_state_in=cs[i % 2],
+                        conv_state_out=cs[(i + 1) % 2], out=out)
+
+    for i in range(max(args.warmup, 3)):
+        mstep(i)
+    torch.cuda.synchronize()
+    barrier(pg)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.verify_steps):
+        mstep(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    ms = max_over_ranks(pg, e0.elapsed_time(e1) / args.verify_steps, dev)
+    T = N * t_new
+    nbytes = (2 * N * H * D * D * 4 + 2 * N * 3 * H * D * 3 * 2 + 4 * T * H * D * 2 +
+              T * H * D * 4 + T * H * 4 + T * H * D * 2)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    obj = {"metric": f"KDA multi-token decode steps/s ({N} seqs x {t_new} tokens, H={H}, d={D})",
+           "value": round(world / (ms / 1e3), 2), "unit": "steps/s",
+           "tokens_per_s": round(world * T / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
+           "steps": args.verify_steps, "prefill_path": path,
+           "roofline": {"kernel": "k_prefill_short (recurrent path) + conv-state roll",
+                        "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                        "peak_source": peak_src, "traffic": recorded_traffic("short_verify_256x4"),
+                        "algorithmic_bytes": nbytes}}
+    del steps_in, dec
+    return obj, 2 * args.verify_steps
 
 
 def run_decode_only(args, world, rank, local, pg, dev, peaks, peak_src):
@@ -451,8 +521,11 @@ def main():
     ap.add_argument("--workload", choices=["layer_8k", "varlen_16", "long_1m"], default="layer_8k")
     ap.add_argument("--decode-steps", type=int, default=1000)
     ap.add_argument("--decode-n", type=int, default=256, help="decode batch (sequences)")
-    ap.add_argument("--mode", choices=["all", "prefill", "decode"], default="all",
-                    help="profiling aid: run only one of the two measurements")
+    ap.add_argument("--verify-steps", type=int, default=200,
+                    help="multi-token decode steps (256 sequences x 4 tokens) to time; 0 skips")
+    ap.add_argument("--mode", choices=["all", "prefill", "decode", "verify"], default="all",
+                    help="profiling aid: run only one of the measurements (verify = the "
+                         "multi-token decode loop)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps

@@ -146,7 +146,22 @@ typedef struct {
                               0 = chosen from N*H and the SM count, 1 = none, 2..16 forced */
 } kda_prefill_args;
 
-#define KDA_FLAG_FORCE_SIMT 1 /* take the fp32 SIMT path even where tensor cores apply */
+#define KDA_FLAG_FORCE_SIMT 1    /* take the fp32 SIMT path even where tensor cores apply */
+#define KDA_FLAG_NO_RECURRENT 2  /* never take the recurrent short-sequence path (below) */
+
+/* Paths of kda_prefill (reported by kda_prefill_plan):
+ *  KDA_PATH_SIMT         fp32 SIMT chunkwise path (any D, chunk, dtype);
+ *  KDA_PATH_TENSOR_CORE  tcgen05 chunkwise path (D = 128, chunk = 64, bf16 inputs);
+ *  KDA_PATH_RECURRENT    token-by-token path for batches of short sequences:
+ *                        D = 128, cu_seqlens_host given and every sequence at most
+ *                        KDA_RECURRENT_MAX_LEN tokens (multi-token decode, speculative
+ *                        verification); each (sequence, head) state is read and
+ *                        written once, no workspace.  `chunk` does not matter there:
+ *                        the result equals the chunkwise one up to rounding. */
+#define KDA_PATH_SIMT 0
+#define KDA_PATH_TENSOR_CORE 1
+#define KDA_PATH_RECURRENT 2
+#define KDA_RECURRENT_MAX_LEN 8
 
 /* Segment-parallel scan (tensor-core path).  One (sequence, head) is a chain
  * of chunks, each depending on the state the previous one leaves.  When the
@@ -170,11 +185,11 @@ kda_status kda_prefill_workspace_size(const kda_prefill_args* args, size_t* byte
 kda_status kda_prefill(const kda_prefill_args* args, kda_stream_t stream);
 
 /* The plan kda_prefill takes for these arguments on the current device:
- * *tensor_core = 1 for the tcgen05 path, 0 for the fp32 SIMT path, and
- * *segments = segments per sequence (1 on the SIMT path and when no
- * segmenting applies).  Reads only the sizes, dtypes, flags and `segments`
- * of args (no pointer is dereferenced); launches nothing. */
-kda_status kda_prefill_plan(const kda_prefill_args* args, int* tensor_core, int* segments);
+ * *path = one of KDA_PATH_*, and *segments = segments per sequence (1
+ * except on the tensor-core path when segmenting applies).  Reads the sizes,
+ * dtypes, flags, `segments`, the alignment of the state pointers and, when
+ * given, cu_seqlens_host; no device pointer is dereferenced; launches nothing. */
+kda_status kda_prefill_plan(const kda_prefill_args* args, int* path, int* segments);
 
 /* ------------------------------------------------------------------------
  * kda_prefill_noalloc -- kda_prefill for callers that cannot allocate device

@@ -20,6 +20,9 @@ KDA_ERR_DEVICE_ARG = 6
 KDA_BF16 = 0
 KDA_FP32 = 1
 KDA_FLAG_FORCE_SIMT = 1
+KDA_FLAG_NO_RECURRENT = 2
+KDA_PATH_SIMT, KDA_PATH_TENSOR_CORE, KDA_PATH_RECURRENT = 0, 1, 2
+KDA_RECURRENT_MAX_LEN = 8
 KDA_MAX_SEGMENTS = 16
 ABI_VERSION = 10100  # kda_prefill_args with the `segments` field
 

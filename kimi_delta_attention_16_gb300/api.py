@@ -160,10 +160,16 @@ def kda_prefill_workspace_size(T_total: int, H: int, D: int, *, N: int = 1, chun
     return int(n.value)
 
 
+_PATH_NAMES = {_lib.KDA_PATH_SIMT: "simt", _lib.KDA_PATH_TENSOR_CORE: "tc",
+               _lib.KDA_PATH_RECURRENT: "recurrent"}
+
+
 def kda_prefill_plan(T_total: int, H: int, D: int, *, N: int = 1, chunk: int = 64,
-                     io=torch.bfloat16, flags: int = 0, segments: int = 0):
-    """(path, segments) kda_prefill takes on the current device: path is "tc" for the
-    tcgen05 path or "simt" for the fp32 SIMT path; segments per sequence (1 = none)."""
+                     io=torch.bfloat16, flags: int = 0, segments: int = 0, cu_seqlens=None):
+    """(path, segments) kda_prefill takes on the current device: path is "tc" (tcgen05
+    chunkwise), "simt" (fp32 chunkwise) or "recurrent" (token by token, for batches whose
+    sequences all have at most 8 tokens; needs ``cu_seqlens`` to decide); segments per
+    sequence (1 = none)."""
     lib = _lib.load()
     a = _lib.PrefillArgs()
     a.N, a.H, a.D, a.chunk, a.T_total = N, H, D, chunk, T_total
@@ -171,11 +177,18 @@ def kda_prefill_plan(T_total: int, H: int, D: int, *, N: int = 1, chunk: int = 6
     a.out_dtype = a.io
     a.flags = flags
     a.segments = segments
-    tc, seg = ctypes.c_int(0), ctypes.c_int(1)
-    st = lib.kda_prefill_plan(ctypes.byref(a), ctypes.byref(tc), ctypes.byref(seg))
+    host = None
+    if cu_seqlens is not None:
+        host = np.ascontiguousarray(np.asarray(
+            cu_seqlens.detach().cpu() if isinstance(cu_seqlens, torch.Tensor) else cu_seqlens,
+            dtype=np.int32))
+        a.N = host.shape[0] - 1
+        a.cu_seqlens_host = host.ctypes.data
+    path, seg = ctypes.c_int(0), ctypes.c_int(1)
+    st = lib.kda_prefill_plan(ctypes.byref(a), ctypes.byref(path), ctypes.byref(seg))
     if st:
         raise KDAError(st, "kda_prefill_plan")
-    return ("tc" if tc.value else "simt"), int(seg.value)
+    return _PATH_NAMES[path.value], int(seg.value)
 
 
 def kda_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, conv_w: torch.Tensor,

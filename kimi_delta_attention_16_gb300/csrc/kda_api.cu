@@ -73,6 +73,7 @@ kda_status check_rows(const void* p, int64_t stride, int64_t min_stride, kda_dty
 }
 
 struct PrefillPlan {
+    int path;           // KDA_PATH_*
     bool tc;            // tensor-core path
     size_t ws_conv;     // bytes: convolved q|k|v rows, fp32 (SIMT path)
     size_t ws_o;        // bytes: o before the epilogue, fp32 (SIMT path)
@@ -82,7 +83,13 @@ struct PrefillPlan {
 
 PrefillPlan plan_prefill(const kda_prefill_args& a) {
     PrefillPlan p{};
-    p.tc = !(a.flags & KDA_FLAG_FORCE_SIMT) && kda::tc_prefill_applies(a);
+    const bool simt = (a.flags & KDA_FLAG_FORCE_SIMT) != 0;
+    if (!simt && !(a.flags & KDA_FLAG_NO_RECURRENT) && kda::short_prefill_applies(a)) {
+        p.path = KDA_PATH_RECURRENT;
+        return p;
+    }
+    p.tc = !simt && kda::tc_prefill_applies(a);
+    p.path = p.tc ? KDA_PATH_TENSOR_CORE : KDA_PATH_SIMT;
     const size_t T = (size_t)(a.T_total > 0 ? a.T_total : 0);
     const size_t HD = (size_t)a.H * a.D;
     if (p.tc) {
@@ -267,17 +274,21 @@ kda_status kda_prefill_workspace_size(const kda_prefill_args* args, size_t* byte
     return ok();
 }
 
-kda_status kda_prefill_plan(const kda_prefill_args* args, int* tensor_core, int* segments) {
-    if (!args || !tensor_core || !segments) return fail(KDA_ERR_INVALID_ARG, "NULL argument");
-    *tensor_core = 0;
+kda_status kda_prefill_plan(const kda_prefill_args* args, int* path, int* segments) {
+    if (!args || !path || !segments) return fail(KDA_ERR_INVALID_ARG, "NULL argument");
+    *path = KDA_PATH_SIMT;
     *segments = 1;
     if (!supported_d(args->D) || !kda::chunk_simt_supported(args->D, args->chunk))
         return fail(KDA_ERR_UNSUPPORTED, "unsupported D=%d / chunk=%d", args->D, args->chunk);
     if (args->T_total < 0 || args->H < 1 || args->N < 0) return fail(KDA_ERR_INVALID_ARG, "bad sizes");
     if (args->segments < 0 || args->segments > KDA_MAX_SEGMENTS)
         return fail(KDA_ERR_INVALID_ARG, "segments = %d not in [0, %d]", args->segments, KDA_MAX_SEGMENTS);
+    if (args->cu_seqlens_host && args->N > 0) {
+        kda_status st = check_host_cu(args->cu_seqlens_host, args->N, args->T_total);
+        if (st) return st;
+    }
     const PrefillPlan p = plan_prefill(*args);
-    *tensor_core = p.tc ? 1 : 0;
+    *path = p.path;
     *segments = p.tc ? kda::tc_segments(*args) : 1;
     return ok();
 }
@@ -299,6 +310,10 @@ kda_status kda_prefill(const kda_prefill_args* a, kda_stream_t stream) {
         (e = kda::launch_conv_state_out(parts, xs, a->io, a->cu_seqlens, a->N, a->T_total,
                                         (int)(3 * HD), a->conv_state_in, a->conv_state_out, s)))
         return cuda_fail(e, "conv state");
+    if (p.path == KDA_PATH_RECURRENT) {
+        if ((e = kda::launch_short_prefill(*a, s))) return cuda_fail(e, "recurrent prefill");
+        return ok();
+    }
     if (p.tc) {
         if ((e = kda::launch_tc_prefill(*a, static_cast<char*>(a->workspace), s)))
             return cuda_fail(e, "tensor-core prefill");

@@ -115,4 +115,10 @@ cudaError_t launch_rms_gate(const float* o, int64_t rows, int D, const void* gat
 // Single-token decode step.
 cudaError_t launch_decode(const kda_decode_args& a, cudaStream_t s);
 
+// Recurrent prefill for batches whose sequences all have at most kShortMaxL
+// tokens (D = 128; needs the host copy of cu_seqlens to decide).
+constexpr int kShortMaxL = 8;
+bool short_prefill_applies(const kda_prefill_args& a);
+cudaError_t launch_short_prefill(const kda_prefill_args& a, cudaStream_t s);
+
 }  // namespace kda

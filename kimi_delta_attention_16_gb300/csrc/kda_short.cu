@@ -1,0 +1,612 @@
+// kda_short.cu -- the recurrent path of kda_prefill for batches of short
+// sequences (every sequence at most kShortMaxL tokens): multi-token decode
+// and speculative verification, where a chunk of 64 would be mostly empty.
+//
+// Page "Animated Kimi K3 architecture diagram", section "LOCAL MEMORY: A
+// FIXED MATRIX THAT PREDICTS, FORGETS, AND CORRECTS": per token, DECAY
+// S_bar = Diag(alpha_t) S, PROBE/CORRECT e = v - S_bar^T k, WRITE
+// S = S_bar + beta k e^T; page "Kimi K3 / Architecture": the short conv with
+// its rolling window, the read o = S^T q, head RMSNorm and the sigmoid gate.
+//
+// Persistent CTAs (two per SM) walk contiguous head-major ranges of (sequence,
+// head) units.  A unit's D x D fp32 state is read into registers once, takes
+// the sequence's tokens one after another, and is written once; thread
+// (row group rg = warp, column group cg = lane) holds rows 16 rg .. 16 rg + 15
+// of columns 4 cg .. 4 cg + 3, so every state access is a coalesced 16-byte
+// one.  Everything that does not depend on the state (conv + SiLU, L2 norms,
+// decay factors) is done for all of the unit's tokens first; the token loop
+// then needs one barrier per token, because the readout of token t - 1 and
+// the decay and probe of token t share one pass over the state registers
+// (S_{t-1}^T q_{t-1} before the decay, S_bar_t^T k_t after it) and their
+// row-group partial sums are double-buffered.  While a unit computes, the next
+// unit's state, rows and conv window are prefetched into L2.
+#include "kda_internal.cuh"
+#include "kda_tc_ptx.cuh"
+
+namespace kda {
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kShortThreads = 256;
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
+template <typename Tio, typename To>
+__global__ void __launch_bounds__(kShortThreads, 2)
+k_prefill_short(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __restrict__ v,
+                int64_t xs, const Tio* __restrict__ gate, const float* __restrict__ g,
+                const float* __restrict__ beta, const float* __restrict__ conv_w,
+                const Tio* __restrict__ cs_in, const float* __restrict__ rms_w, float eps_l2,
+                float eps_rms, float scale, int N, int H, const int32_t* __restrict__ cu,
+                int64_t T_total, const float* S0, float* S_fin, To* __restrict__ out,
+                int* d_status) {
+    constexpr int L8 = kShortMaxL;
+    // sbuf: raw q, k, v rows [L][3][128] while convolving, then the row-group partial sums
+    // of the token loop: probe [2][8][128] and readout [2][8][128] (double-buffered by token)
+    __shared__ __align__(16) float sbuf[4 * 8 * kD];
+    __shared__ __align__(16) float sx[L8][3][kD];   // convolved q, k, v of every token
+    __shared__ __align__(16) float salpha[L8][kD];  // e^g of every token
+    __shared__ __align__(16) float sgate[L8][kD];
+    __shared__ __align__(16) float sW[3 * kD * 4];  // conv taps of the current head
+    __shared__ float sRms[kD];
+    __shared__ float snorm[L8][2];                  // 1/|q|, 1/|k| per token
+    __shared__ float sbeta[L8];
+    __shared__ int s_head;
+    float* sraw = sbuf;
+    float* sredP = sbuf;
+    float* sredO = sbuf + 2 * 8 * kD;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rg = warp, cg = lane;
+    const int r0 = 16 * rg, c0 = 4 * cg;
+    const int64_t HD = (int64_t)H * kD;
+    const int units = N * H;
+    const int per = (units + gridDim.x - 1) / gridDim.x;
+    const int first = blockIdx.x * per;
+    const int my_units = first < units ? (units - first < per ? units - first : per) : 0;
+    auto unit_of = [&](int i, int& n, int& h) {  // head-major: j = h * N + n
+        const int jj = first + i;
+        h = jj / N;
+        n = jj % N;
+    };
+    if (tid == 0) s_head = -1;
+    for (int c = tid; c < kD; c += kShortThreads) sRms[c] = rms_w ? rms_w[c] : 1.f;
+    __syncthreads();
+
+    // L2 prefetch of everything unit i reads (state, conv window, token rows)
+    auto prefetch_unit = [&](int i) {
+        int n, h;
+        unit_of(i, n, h);
+        int64_t a, b;
+        seq_range(cu, n, T_total, a, b);
+        const int L = (int)((b - a) < L8 ? (b - a) : L8);
+        const int u = n * H + h;
+        if (S0) {
+            const char* st = reinterpret_cast<const char*>(S0 + (int64_t)u * kD * kD);
+            prefetch_l2(st + 128 * tid);
+            prefetch_l2(st + 128 * (tid + kShortThreads));
+        }
+        // rows: per token q, k, v, gate (2 lines each for bf16, 4 for fp32) and g (4 lines)
+        constexpr int kLines = kD * (int)sizeof(Tio) / 128;
+        const int per_tok = 4 * kLines + 4;
+        if (tid < L * per_tok) {
+            const int tk = tid / per_tok, w = tid % per_tok;
+            const int64_t t = a + tk;
+            const char* p;
+            if (w < 4 * kLines) {
+                const int part = w / kLines, ln = w % kLines;
+                const Tio* src = part == 0 ? q : part == 1 ? k : part == 2 ? v : gate;
+                p = src ? reinterpret_cast<const char*>(src + (part < 3 ? t * xs : t * HD) + (int64_t)h * kD) + 128 * ln
+                        : nullptr;
+            } else {
+                p = reinterpret_cast<const char*>(g + (t * H + h) * kD) + 128 * (w - 4 * kLines);
+            }
+            if (p) prefetch_l2(p);
+        }
+        if (cs_in && tid < 3 * 3 * kLines) {  // 3 parts x 128 channels x 3 values
+            const int part = tid / (3 * kLines), ln = tid % (3 * kLines);
+            prefetch_l2(reinterpret_cast<const char*>(cs_in + (((int64_t)n * 3 + part) * HD + (int64_t)h * kD) * 3) +
+                        128 * ln);
+        }
+    };
+    if (my_units > 0) prefetch_unit(0);
+
+    for (int i = 0; i < my_units; ++i) {
+        int n, h;
+        unit_of(i, n, h);
+        const int u = n * H + h;
+        int64_t a, b;
+        seq_range(cu, n, T_total, a, b);
+        int L = (int)(b - a);
+        if (L > L8) {  // the host routes only sequences of at most kShortMaxL tokens here
+            if (tid == 0) flag_status(d_status, KDA_ERR_DEVICE_ARG);
+            L = L8;
+        }
+        if (i + 1 < my_units) prefetch_unit(i + 1);
+        if (h != s_head) {  // a new head: its conv taps (uniform branch; read after barrier A)
+            for (int idx = tid; idx < 3 * kD * 4; idx += kShortThreads) {
+                const int part = idx / (kD * 4), rem = idx % (kD * 4);
+                sW[idx] = conv_w[(part * HD + (int64_t)h * kD) * 4 + rem];
+            }
+        }
+        // ---- prologue: the unit's rows, decay factors and gates; its state into registers
+        for (int idx = tid; idx < L * 3 * kD; idx += kShortThreads) {
+            const int tau = idx / (3 * kD), ch = idx % (3 * kD), part = ch >> 7, d = ch & (kD - 1);
+            const Tio* src = part == 0 ? q : (part == 1 ? k : v);
+            sraw[idx] = to_f(src[(a + tau) * xs + (int64_t)h * kD + d]);
+        }
+        for (int idx = tid; idx < L * kD; idx += kShortThreads) {
+            const int tau = idx >> 7, d = idx & (kD - 1);
+            const int64_t row = ((a + tau) * H + h) * kD + d;
+            salpha[tau][d] = expf(g[row]);
+            sgate[tau][d] = gate ? to_f(gate[row]) : 0.f;
+        }
+        if (tid < L) sbeta[tid] = beta[(a + tid) * H + h];
+        float4 s[16];
+        {
+            const float* src = S0 ? S0 + (int64_t)u * kD * kD : nullptr;
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                s[e] = src ? *reinterpret_cast<const float4*>(src + (r0 + e) * kD + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncthreads();  // A: raw rows, conv taps
+        if (tid == 0) s_head = h;
+        // conv + SiLU of every token (the window reaches into the rolling conv state)
+        for (int idx = tid; idx < L * 3 * kD; idx += kShortThreads) {
+            const int tau = idx / (3 * kD), ch = idx % (3 * kD), part = ch >> 7, d = ch & (kD - 1);
+            const float4 w = *reinterpret_cast<const float4*>(&sW[ch * 4]);
+            float x[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int rel = tau - 3 + m;
+                x[m] = rel >= 0 ? sraw[rel * 3 * kD + ch]
+                                : (cs_in ? to_f(cs_in[(((int64_t)n * 3 + part) * HD + (int64_t)h * kD + d) * 3 + 3 + rel]) : 0.f);
+            }
+            sx[tau][part][d] = siluf_(w.x * x[0] + w.y * x[1] + w.z * x[2] + w.w * x[3]);
+        }
+        __syncthreads();  // B
+        // L2 norms: warp w takes (token, q or k) pairs w, w + 8, ...
+        for (int rr = warp; rr < 2 * L; rr += kShortThreads / 32) {
+            const int tau = rr >> 1, which = rr & 1;
+            float ss = 0.f;
+#pragma unroll
+            for (int d = lane; d < kD; d += 32) ss += sx[tau][which][d] * sx[tau][which][d];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            if (lane == 0) snorm[tau][which] = 1.0f / sqrtf(ss + eps_l2);
+        }
+        __syncthreads();  // C: the partial-sum buffers (aliasing the raw rows) are free now
+
+        // o of token tau (row group 0): sum of the readout partials, RMSNorm, gate, store
+        auto emit = [&](int tau, int buf) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr) {
+                const float4 tt = *reinterpret_cast<const float4*>(&sredO[(buf * 8 + rr) * kD + c0]);
+                acc.x += tt.x; acc.y += tt.y; acc.z += tt.z; acc.w += tt.w;
+            }
+            const float o[4] = {acc.x, acc.y, acc.z, acc.w};
+            float ss = o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float inv = 1.0f / sqrtf(ss / kD + eps_rms);
+            const int64_t row = ((a + tau) * H + h) * kD + c0;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                float y = o[m] * inv * sRms[c0 + m];
+                if (gate) y *= sigmoidf_(sgate[tau][c0 + m]);
+                out[row + m] = from_f<To>(y);
+            }
+        };
+        // ---- token loop, one barrier per token: the readout of token tau - 1 (its partials
+        // over this thread's rows) shares a pass over the state with token tau's decay and probe
+        for (int tau = 0; tau < L; ++tau) {
+            const int buf = tau & 1;
+            const float ik = snorm[tau][1];
+            const float iqp = tau > 0 ? snorm[tau - 1][0] * scale : 0.f;
+            float4 p = make_float4(0.f, 0.f, 0.f, 0.f), po = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                if (tau > 0) {
+                    const float qr = sx[tau - 1][0][r0 + e] * iqp;
+                    po.x = fmaf(qr, s[e].x, po.x); po.y = fmaf(qr, s[e].y, po.y);
+                    po.z = fmaf(qr, s[e].z, po.z); po.w = fmaf(qr, s[e].w, po.w);
+                }
+                const float al = salpha[tau][r0 + e];
+                const float kr = sx[tau][1][r0 + e] * ik;
+                s[e].x *= al; s[e].y *= al; s[e].z *= al; s[e].w *= al;
+                p.x = fmaf(kr, s[e].x, p.x); p.y = fmaf(kr, s[e].y, p.y);
+                p.z = fmaf(kr, s[e].z, p.z); p.w = fmaf(kr, s[e].w, p.w);
+            }
+            *reinterpret_cast<float4*>(&sredP[(buf * 8 + rg) * kD + c0]) = p;
+            if (tau > 0) *reinterpret_cast<float4*>(&sredO[(buf * 8 + rg) * kD + c0]) = po;
+            __syncthreads();
+            // correct: e = v - S_bar^T k; write: S = S_bar + beta k e^T
+            float4 ev = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int rr = 0; rr < 8; ++rr) {
+                const float4 tt = *reinterpret_cast<const float4*>(&sredP[(buf * 8 + rr) * kD + c0]);
+                ev.x += tt.x; ev.y += tt.y; ev.z += tt.z; ev.w += tt.w;
+            }
+            ev.x = sx[tau][2][c0] - ev.x; ev.y = sx[tau][2][c0 + 1] - ev.y;
+            ev.z = sx[tau][2][c0 + 2] - ev.z; ev.w = sx[tau][2][c0 + 3] - ev.w;
+            const float bb = sbeta[tau] * ik;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float bk = bb * sx[tau][1][r0 + e];
+                s[e].x = fmaf(bk, ev.x, s[e].x); s[e].y = fmaf(bk, ev.y, s[e].y);
+                s[e].z = fmaf(bk, ev.z, s[e].z); s[e].w = fmaf(bk, ev.w, s[e].w);
+            }
+            if (tau > 0 && rg == 0) emit(tau - 1, buf);
+        }
+        if (L > 0) {  // readout of the last token
+            const int buf = L & 1;
+            const float iq = snorm[L - 1][0] * scale;
+            float4 po = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float qr = sx[L - 1][0][r0 + e] * iq;
+                po.x = fmaf(qr, s[e].x, po.x); po.y = fmaf(qr, s[e].y, po.y);
+                po.z = fmaf(qr, s[e].z, po.z); po.w = fmaf(qr, s[e].w, po.w);
+            }
+            *reinterpret_cast<float4*>(&sredO[(buf * 8 + rg) * kD + c0]) = po;
+            __syncthreads();
+            if (rg == 0) emit(L - 1, buf);
+        }
+        if (S_fin) {
+            float* dst = S_fin + (int64_t)u * kD * kD;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) *reinterpret_cast<float4*>(dst + (r0 + e) * kD + c0) = s[e];
+        }
+        __syncthreads();  // D: every read of this unit's shared rows is done
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Pipelined variant for 16-byte aligned inputs: one CTA of 512 threads per SM and two stages
+// of shared memory filled by cp.async (every thread copies a few 16-byte pieces).  While a
+// unit computes, the next unit's state slice, conv window and token rows land in the other
+// stage; the state leaves from registers with coalesced stores, so a stage is free as soon as
+// its unit has read it.  Thread (row group rg = warp / 4, column c = 32 (warp % 4) + lane)
+// holds rows 32 rg .. 32 rg + 31 of column c: the sums over rows (S_bar^T k, S^T q) then take
+// four partials per column, and the per-row factors are warp-wide broadcasts.
+template <typename Tio>
+struct PipeStage {
+    static constexpr uint32_t kRowBytes = 128 * sizeof(Tio);
+    static constexpr uint32_t kState = 0;
+    static constexpr uint32_t kConv = 65536;                       // [3][128][3]
+    static constexpr uint32_t kConvPart = 128 * 3 * sizeof(Tio);
+    static constexpr uint32_t kRows = kConv + 3 * kConvPart;       // [L][4][128]: q, k, v, gate
+    static constexpr uint32_t kG = kRows + kShortMaxL * 4 * kRowBytes;  // [L][128] fp32
+    static constexpr uint32_t kBytes = (kG + kShortMaxL * 512 + 127) / 128 * 128;
+    static constexpr uint32_t kRed = 2 * kBytes;                   // probe, readout partials
+    static constexpr uint32_t kRedBytes = 2 * 4 * 128 * 4;          // [2 parities][4 row groups][128]
+    static constexpr uint32_t kSmem = kRed + 2 * kRedBytes + 128;
+};
+constexpr int kPipeThreads = 512;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+template <typename Tio, typename To>
+__global__ void __launch_bounds__(kPipeThreads, 1)
+k_prefill_short_pipe(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __restrict__ v,
+                     int64_t xs, const Tio* __restrict__ gate, const float* __restrict__ g,
+                     const float* __restrict__ beta, const float* __restrict__ conv_w,
+                     const Tio* __restrict__ cs_in, const float* __restrict__ rms_w, float eps_l2,
+                     float eps_rms, float scale, int N, int H, const int32_t* __restrict__ cu,
+                     int64_t T_total, const float* S0, float* S_fin, To* __restrict__ out,
+                     int* d_status) {
+    using St = PipeStage<Tio>;
+    constexpr int L8 = kShortMaxL;
+    constexpr int kChunksPerRow = (int)(St::kRowBytes / 16);
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(16) float sx[L8][3][kD];  // convolved q, k, v of every token
+    __shared__ __align__(16) float salpha[L8][kD];  // e^g of every token
+    __shared__ __align__(16) float sW[3 * kD * 4];  // conv taps of the current head
+    __shared__ float sRms[kD];
+    __shared__ float snorm[L8][2];
+    __shared__ float sbeta[2][L8];
+    __shared__ int s_head;
+    const uint32_t raw_addr = tc::smem_u32(smem_raw);
+    uint8_t* sm = smem_raw + (((raw_addr + 127u) & ~127u) - raw_addr);
+    const uint32_t sbase = tc::smem_u32(sm);
+    auto sredP = reinterpret_cast<float(*)[4][kD]>(sm + St::kRed);
+    auto sredO = reinterpret_cast<float(*)[4][kD]>(sm + St::kRed + St::kRedBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rg = warp >> 2, c = 32 * (warp & 3) + lane;
+    const int r0 = 32 * rg;
+    const int64_t HD = (int64_t)H * kD;
+    const int units = N * H;
+    const int per = (units + gridDim.x - 1) / gridDim.x;
+    const int first = blockIdx.x * per;
+    const int my_units = first < units ? (units - first < per ? units - first : per) : 0;
+    auto unit_of = [&](int i, int& n, int& h) {  // head-major: j = h * N + n
+        const int jj = first + i;
+        h = jj / N;
+        n = jj % N;
+    };
+    auto unit_rows = [&](int n, int64_t& a, int& L) {
+        int64_t b;
+        seq_range(cu, n, T_total, a, b);
+        L = (int)((b - a) < L8 ? (b - a) : L8);
+    };
+    if (tid == 0) s_head = -1;
+    for (int cc = tid; cc < kD; cc += kPipeThreads) sRms[cc] = rms_w ? rms_w[cc] : 1.f;
+
+    // unit i -> stage i % 2 (all threads, one cp.async group); its betas -> registers (thread 0)
+    float bnext[L8];
+    auto stage = [&](int i) {
+        int n, h, L;
+        int64_t a;
+        unit_of(i, n, h);
+        unit_rows(n, a, L);
+        const int u = n * H + h;
+        const uint32_t st = sbase + (uint32_t)(i & 1) * St::kBytes;
+        if (S0) {
+            const char* src = reinterpret_cast<const char*>(S0 + (int64_t)u * kD * kD);
+            for (int idx = tid; idx < 4096; idx += kPipeThreads) cp_async16(st + St::kState + 16 * idx, src + 16 * idx);
+        }
+        if (cs_in) {
+            constexpr int kc = (int)(St::kConvPart / 16);
+            for (int idx = tid; idx < 3 * kc; idx += kPipeThreads) {
+                const int p = idx / kc, w = idx % kc;
+                cp_async16(st + St::kConv + p * St::kConvPart + 16 * w,
+                           reinterpret_cast<const char*>(cs_in + (((int64_t)n * 3 + p) * HD + (int64_t)h * kD) * 3) + 16 * w);
+            }
+        }
+        const int nrow = L * 4 * kChunksPerRow;
+        for (int idx = tid; idx < nrow; idx += kPipeThreads) {
+            const int tau = idx / (4 * kChunksPerRow), rem = idx % (4 * kChunksPerRow);
+            const int p = rem / kChunksPerRow, w = rem % kChunksPerRow;
+            const int64_t t = a + tau;
+            const Tio* src = p == 0 ? q : p == 1 ? k : p == 2 ? v : gate;
+            if (src)
+                cp_async16(st + St::kRows + (tau * 4 + p) * St::kRowBytes + 16 * w,
+                           reinterpret_cast<const char*>(src + (p < 3 ? t * xs : t * HD) + (int64_t)h * kD) + 16 * w);
+        }
+        for (int idx = tid; idx < L * 32; idx += kPipeThreads) {
+            const int tau = idx >> 5, w = idx & 31;
+            cp_async16(st + St::kG + tau * 512 + 16 * w,
+                       reinterpret_cast<const char*>(g + ((a + tau) * H + h) * kD) + 16 * w);
+        }
+        cp_async_commit();
+        if (tid == 0) {
+#pragma unroll
+            for (int tau = 0; tau < L8; ++tau) bnext[tau] = tau < L ? beta[(a + tau) * H + h] : 0.f;
+        }
+    };
+    if (my_units > 0) stage(0);
+    if (tid == 0)
+#pragma unroll
+        for (int tau = 0; tau < L8; ++tau) sbeta[0][tau] = bnext[tau];
+    __syncthreads();
+
+    for (int i = 0; i < my_units; ++i) {
+        const int b = i & 1;
+        int n, h, L;
+        int64_t a;
+        unit_of(i, n, h);
+        unit_rows(n, a, L);
+        const int u = n * H + h;
+        {
+            int64_t a2, b2;
+            seq_range(cu, n, T_total, a2, b2);
+            if (b2 - a2 > L8 && tid == 0) flag_status(d_status, KDA_ERR_DEVICE_ARG);
+        }
+        if (h != s_head)  // a new head: its conv taps (uniform branch; read after barrier A)
+            for (int idx = tid; idx < 3 * kD * 4; idx += kPipeThreads) {
+                const int part = idx / (kD * 4), rem = idx % (kD * 4);
+                sW[idx] = conv_w[(part * HD + (int64_t)h * kD) * 4 + rem];
+            }
+        cp_async_wait_all();  // this unit's stage (the only group in flight)
+        __syncthreads();      // A
+        if (tid == 0) s_head = h;
+        // the other stage was read completely by unit i - 1: refill it for unit i + 1
+        if (i + 1 < my_units) stage(i + 1);
+        const uint8_t* st = sm + b * St::kBytes;
+        const Tio* rows = reinterpret_cast<const Tio*>(st + St::kRows);
+        const Tio* cst = reinterpret_cast<const Tio*>(st + St::kConv);
+        const float* grow = reinterpret_cast<const float*>(st + St::kG);
+        // ---- prologue: conv + SiLU and decay factors of every token; the state into registers
+        for (int idx = tid; idx < L * 3 * kD; idx += kPipeThreads) {
+            const int tau = idx / (3 * kD), ch = idx % (3 * kD), part = ch >> 7, d = ch & (kD - 1);
+            const float4 w = *reinterpret_cast<const float4*>(&sW[ch * 4]);
+            float x[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int rel = tau - 3 + m;
+                x[m] = rel >= 0 ? to_f(rows[(rel * 4 + part) * kD + d]) : (cs_in ? to_f(cst[ch * 3 + 3 + rel]) : 0.f);
+            }
+            sx[tau][part][d] = siluf_(w.x * x[0] + w.y * x[1] + w.z * x[2] + w.w * x[3]);
+        }
+        for (int idx = tid; idx < L * kD; idx += kPipeThreads) salpha[idx >> 7][idx & (kD - 1)] = expf(grow[idx]);
+        float s[32];
+        {
+            const float* Ss = reinterpret_cast<const float*>(st + St::kState);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) s[e] = S0 ? Ss[(r0 + e) * kD + c] : 0.f;
+        }
+        __syncthreads();  // B
+        if (tid == 0 && i + 1 < my_units)  // read by unit i + 1 after its barrier A
+#pragma unroll
+            for (int tau = 0; tau < L8; ++tau) sbeta[(i + 1) & 1][tau] = bnext[tau];
+        for (int rr = warp; rr < 2 * L; rr += kPipeThreads / 32) {  // L2 norms of q and k, per token
+            const int tau = rr >> 1, which = rr & 1;
+            float ss = 0.f;
+#pragma unroll
+            for (int d = lane; d < kD; d += 32) ss += sx[tau][which][d] * sx[tau][which][d];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            if (lane == 0) snorm[tau][which] = 1.0f / sqrtf(ss + eps_l2);
+        }
+        __syncthreads();  // C
+
+        auto emit = [&](int tau, int buf) {  // warp 0: o, RMSNorm, gate, store (columns 4 lane ..)
+            const int c4 = 4 * lane;
+            float o[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) o[m] = 0.f;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float4 tt = *reinterpret_cast<const float4*>(&sredO[buf][r][c4]);
+                o[0] += tt.x; o[1] += tt.y; o[2] += tt.z; o[3] += tt.w;
+            }
+            float ss = o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float inv = 1.0f / sqrtf(ss / kD + eps_rms);
+            const int64_t row = ((a + tau) * H + h) * kD + c4;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                float y = o[m] * inv * sRms[c4 + m];
+                if (gate) y *= sigmoidf_(to_f(rows[(tau * 4 + 3) * kD + c4 + m]));
+                out[row + m] = from_f<To>(y);
+            }
+        };
+        // ---- token loop, one barrier per token: the readout of token tau - 1 (before the decay)
+        // and the decay and probe of token tau share one pass over the state registers
+        for (int tau = 0; tau < L; ++tau) {
+            const int buf = tau & 1;
+            const float ik = snorm[tau][1];
+            const float iqp = tau > 0 ? snorm[tau - 1][0] * scale : 0.f;
+            float p = 0.f, po = 0.f;
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+                const float4 kq = *reinterpret_cast<const float4*>(&sx[tau][1][r0 + 4 * e4]);
+                const float4 al = *reinterpret_cast<const float4*>(&salpha[tau][r0 + 4 * e4]);
+                const float kk[4] = {kq.x, kq.y, kq.z, kq.w}, aa[4] = {al.x, al.y, al.z, al.w};
+                if (tau > 0) {
+                    const float4 qq = *reinterpret_cast<const float4*>(&sx[tau - 1][0][r0 + 4 * e4]);
+                    const float qv[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) po = fmaf(qv[m], s[4 * e4 + m], po);
+                }
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    s[4 * e4 + m] *= aa[m];
+                    p = fmaf(kk[m], s[4 * e4 + m], p);
+                }
+            }
+            sredP[buf][rg][c] = p * ik;
+            if (tau > 0) sredO[buf][rg][c] = po * iqp;
+            __syncthreads();
+            const float ev = sx[tau][2][c] - (sredP[buf][0][c] + sredP[buf][1][c] + sredP[buf][2][c] + sredP[buf][3][c]);
+            const float bb = sbeta[b][tau] * ik * ev;
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+                const float4 kq = *reinterpret_cast<const float4*>(&sx[tau][1][r0 + 4 * e4]);
+                s[4 * e4 + 0] = fmaf(bb, kq.x, s[4 * e4 + 0]);
+                s[4 * e4 + 1] = fmaf(bb, kq.y, s[4 * e4 + 1]);
+                s[4 * e4 + 2] = fmaf(bb, kq.z, s[4 * e4 + 2]);
+                s[4 * e4 + 3] = fmaf(bb, kq.w, s[4 * e4 + 3]);
+            }
+            if (tau > 0 && warp == 0) emit(tau - 1, buf);
+        }
+        if (L > 0) {  // readout of the last token
+            const int buf = L & 1;
+            float po = 0.f;
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+                const float4 qq = *reinterpret_cast<const float4*>(&sx[L - 1][0][r0 + 4 * e4]);
+                po = fmaf(qq.x, s[4 * e4 + 0], po);
+                po = fmaf(qq.y, s[4 * e4 + 1], po);
+                po = fmaf(qq.z, s[4 * e4 + 2], po);
+                po = fmaf(qq.w, s[4 * e4 + 3], po);
+            }
+            sredO[buf][rg][c] = po * snorm[L - 1][0] * scale;
+            __syncthreads();
+            if (warp == 0) emit(L - 1, buf);
+        }
+        if (S_fin) {
+            float* dst = S_fin + (int64_t)u * kD * kD;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) dst[(r0 + e) * kD + c] = s[e];
+        }
+        __syncthreads();  // D: stage b and the shared rows are no longer read
+    }
+    cp_async_wait_all();
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int g_short_sms[64];
+
+int device_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (g_short_sms[dev] == 0) cudaDeviceGetAttribute(&g_short_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    return g_short_sms[dev] > 0 ? g_short_sms[dev] : 148;
+}
+
+template <typename Tio, typename To>
+cudaError_t short_launch(const kda_prefill_args& a, cudaStream_t s) {
+    const int units = a.N * a.H;
+    const int sms = device_sms();
+    const int blocks = units < 2 * sms ? units : 2 * sms;
+    const int64_t xs = a.qkv_row_stride ? a.qkv_row_stride : (int64_t)a.H * kD;
+    k_prefill_short<Tio, To><<<blocks, kShortThreads, 0, s>>>(
+        (const Tio*)a.q, (const Tio*)a.k, (const Tio*)a.v, xs, (const Tio*)a.gate, a.g, a.beta, a.conv_w,
+        (const Tio*)a.conv_state_in, a.rms_w, a.eps_l2, a.eps_rms, a.scale, a.N, a.H, a.cu_seqlens,
+        a.T_total, a.initial_state, a.final_state, (To*)a.out, a.d_status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool short_prefill_applies(const kda_prefill_args& a) {
+    if (a.D != kD || !a.cu_seqlens_host || a.N < 1 || (int64_t)a.N * a.H > 0x7fffffffLL) return false;
+    for (int n = 0; n < a.N; ++n)
+        if (a.cu_seqlens_host[n + 1] - a.cu_seqlens_host[n] > kShortMaxL) return false;
+    // 16-byte state rows (float4); everything else is read with scalar loads
+    return (!a.initial_state || aligned16(a.initial_state)) && (!a.final_state || aligned16(a.final_state));
+}
+
+namespace {
+
+// The pipelined kernel copies 16-byte pieces: every source 16-byte aligned.
+bool short_pipe_ok(const kda_prefill_args& a) {
+    const int64_t xs = a.qkv_row_stride ? a.qkv_row_stride : (int64_t)a.H * kD;
+    const int64_t vec = a.io == KDA_BF16 ? 8 : 4;
+    return xs % vec == 0 && aligned16(a.q) && aligned16(a.k) && aligned16(a.v) && aligned16(a.g) &&
+           (!a.gate || aligned16(a.gate)) && (!a.conv_state_in || aligned16(a.conv_state_in)) &&
+           (!a.initial_state || aligned16(a.initial_state));
+}
+
+template <typename Tio, typename To>
+cudaError_t short_pipe_launch(const kda_prefill_args& a, cudaStream_t s) {
+    const int sms = device_sms();
+    const int units = a.N * a.H;
+    auto kern = k_prefill_short_pipe<Tio, To>;
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PipeStage<Tio>::kSmem)))
+        return e;
+    const int64_t xs = a.qkv_row_stride ? a.qkv_row_stride : (int64_t)a.H * kD;
+    kern<<<units < sms ? units : sms, kPipeThreads, PipeStage<Tio>::kSmem, s>>>(
+        (const Tio*)a.q, (const Tio*)a.k, (const Tio*)a.v, xs, (const Tio*)a.gate, a.g, a.beta, a.conv_w,
+        (const Tio*)a.conv_state_in, a.rms_w, a.eps_l2, a.eps_rms, a.scale, a.N, a.H, a.cu_seqlens,
+        a.T_total, a.initial_state, a.final_state, (To*)a.out, a.d_status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_short_prefill(const kda_prefill_args& a, cudaStream_t s) {
+    if ((int64_t)a.N * a.H == 0) return cudaSuccess;
+    const bool pipe = short_pipe_ok(a);
+    if (a.io == KDA_BF16) {
+        if (pipe) return a.out_dtype == KDA_FP32 ? short_pipe_launch<bf16, float>(a, s) : short_pipe_launch<bf16, bf16>(a, s);
+        return a.out_dtype == KDA_FP32 ? short_launch<bf16, float>(a, s) : short_launch<bf16, bf16>(a, s);
+    }
+    if (pipe) return a.out_dtype == KDA_FP32 ? short_pipe_launch<float, float>(a, s) : short_pipe_launch<float, bf16>(a, s);
+    return a.out_dtype == KDA_FP32 ? short_launch<float, float>(a, s) : short_launch<float, bf16>(a, s);
+}
+
+}  // namespace kda

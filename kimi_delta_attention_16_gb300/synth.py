@@ -15,6 +15,9 @@ convolution" -- width-4 taps, rolling state of 3 values per channel):
   long_1m       N=1, T=1,048,576, H=24, D=128, chunk 64, bf16 I/O
   decode_256    256 sequences x 1 token per step, H=96, D=128, states
                 ~N(0, 0.02^2), rolling conv state ~N(0,1) bf16
+  verify_256x4  256 sequences x 4 new tokens (a multi-token decode or
+                speculative-verification step), H=96, D=128, states
+                ~N(0, 0.02^2), rolling conv states ~N(0,1) bf16
 
 Value laws (all workloads): raw q, k, v ~ N(0,1); conv taps ~ N(0, 0.5^2);
 log-decay g ~ U[-5, 0] per (token, head, key channel); beta ~ U[0, 1) per
@@ -37,6 +40,8 @@ WORKLOADS = {
                       len_lo=512, len_hi=16384),
     "long_1m": dict(N=1, T=1_048_576, H=24, D=128, chunk=64, io="bf16", s0_std=0.0),
     "decode_256": dict(N=256, H=96, D=128, io="bf16", s0_std=0.02, steps=1000, ring=32),
+    "verify_256x4": dict(N=256, T=1024, H=96, D=128, chunk=64, io="bf16", s0_std=0.02,
+                         conv_state=True),
 }
 
 _TORCH_DT = {"bf16": torch.bfloat16, "fp32": torch.float32}
@@ -100,7 +105,7 @@ def _uniform(shape, lo, hi, gen, device):
 
 def make_prefill(name: str = "tiny_fp32", seed: int = 0, device="cpu", *, N=None, T=None,
                  lengths=None, H=None, D=None, chunk=None, io=None, gate=True, rms_w="ones",
-                 s0_std=None, conv_state=False, g_range=(-5.0, 0.0)) -> PrefillInputs:
+                 s0_std=None, conv_state=None, g_range=(-5.0, 0.0)) -> PrefillInputs:
     """Seeded prefill inputs for a named workload, with optional overrides.
 
     ``lengths`` (a list) overrides N/T with an explicit varlen mix.
@@ -115,6 +120,7 @@ def make_prefill(name: str = "tiny_fp32", seed: int = 0, device="cpu", *, N=None
     chunk = chunk or w.get("chunk", 64)
     io = io or w["io"]
     s0_std = w.get("s0_std", 0.0) if s0_std is None else s0_std
+    conv_state = w.get("conv_state", False) if conv_state is None else conv_state
     if lengths is None:
         if N is None and T is None and w.get("T") is None:
             lengths = varlen_lengths(w["N"], w["len_lo"], w["len_hi"], seed)

@@ -118,12 +118,12 @@ def test_segments_argument_is_range_checked():
     lib = _lib.load()
     for seg, want in [(-1, _lib.KDA_ERR_INVALID_ARG), (_lib.KDA_MAX_SEGMENTS + 1, _lib.KDA_ERR_INVALID_ARG),
                       (0, 0), (1, 0), (_lib.KDA_MAX_SEGMENTS, 0)]:
-        a, cu = _args(T_total=8192, H=4, D=128, chunk=64)
+        a, cu = _args(T_total=8192, H=4, D=128, chunk=64, cu_seqlens_host=None)
         a.segments = seg
         n = ctypes.c_size_t()
         assert lib.kda_prefill_workspace_size(ctypes.byref(a), ctypes.byref(n)) == want
-        tc, p = ctypes.c_int(-1), ctypes.c_int(-1)
-        assert lib.kda_prefill_plan(ctypes.byref(a), ctypes.byref(tc), ctypes.byref(p)) == want
+        path, p = ctypes.c_int(-1), ctypes.c_int(-1)
+        assert lib.kda_prefill_plan(ctypes.byref(a), ctypes.byref(path), ctypes.byref(p)) == want
         if seg < 0 or seg > _lib.KDA_MAX_SEGMENTS:
             assert _prefill(a) == _lib.KDA_ERR_INVALID_ARG
 
@@ -134,10 +134,34 @@ def test_plan_without_a_tensor_core_device_is_simt():
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     lib = _lib.load()
-    a, cu = _args(T_total=1 << 20, H=24, D=128, chunk=64)
-    tc, p = ctypes.c_int(-1), ctypes.c_int(-1)
-    assert lib.kda_prefill_plan(ctypes.byref(a), ctypes.byref(tc), ctypes.byref(p)) == 0
-    assert (tc.value, p.value) == (0, 1)
+    a, cu = _args(T_total=1 << 20, H=24, D=128, chunk=64, cu_seqlens_host=None)
+    path, p = ctypes.c_int(-1), ctypes.c_int(-1)
+    assert lib.kda_prefill_plan(ctypes.byref(a), ctypes.byref(path), ctypes.byref(p)) == 0
+    assert (path.value, p.value) == (_lib.KDA_PATH_SIMT, 1)
+
+
+def test_plan_takes_the_recurrent_path_for_short_batches():
+    """Every sequence of at most 8 tokens (host cu_seqlens given), D = 128: the recurrent
+    path, whatever the chunk; one longer sequence, D != 128, no host copy or the opt-out flag:
+    a chunkwise path."""
+    lib = _lib.load()
+
+    def plan(lengths, **kw):
+        cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+        a, _ = _args(T_total=int(cu[-1]), H=4, D=kw.pop("D", 128), chunk=kw.pop("chunk", 64), **kw)
+        a.N = len(lengths)
+        a.cu_seqlens_host = cu.ctypes.data
+        path, p = ctypes.c_int(-1), ctypes.c_int(-1)
+        assert lib.kda_prefill_plan(ctypes.byref(a), ctypes.byref(path), ctypes.byref(p)) == 0
+        return path.value
+
+    assert plan([4] * 8) == _lib.KDA_PATH_RECURRENT
+    assert plan([1, 8, 0, 3]) == _lib.KDA_PATH_RECURRENT
+    assert plan([1, 8, 0, 3], chunk=16) == _lib.KDA_PATH_RECURRENT
+    assert plan([1, 9]) != _lib.KDA_PATH_RECURRENT
+    assert plan([4] * 8, D=64) != _lib.KDA_PATH_RECURRENT
+    assert plan([4] * 8, flags=_lib.KDA_FLAG_NO_RECURRENT) != _lib.KDA_PATH_RECURRENT
+    assert plan([4] * 8, flags=_lib.KDA_FLAG_FORCE_SIMT) == _lib.KDA_PATH_SIMT
 
 
 def test_short_conv_rejects_bad_arguments():

@@ -106,8 +106,10 @@ def test_prefill_fp32_shapes(D, chunk):
 SMALL_LENGTHS = [[1], [2], [3], [5], [63], [64], [65], [127], [130], [1, 64, 3, 200, 65], [4] * 8]
 
 
+# flags: 0 = the library's own choice (the recurrent path when every sequence has at most 8
+# tokens, else the tensor-core path), NO_RECURRENT = the tensor-core path, FORCE_SIMT
 @pytest.mark.parametrize("lengths", SMALL_LENGTHS)
-@pytest.mark.parametrize("flags", [0, _lib.KDA_FLAG_FORCE_SIMT])
+@pytest.mark.parametrize("flags", [0, _lib.KDA_FLAG_NO_RECURRENT, _lib.KDA_FLAG_FORCE_SIMT])
 def test_prefill_bf16_small(lengths, flags):
     inp = synth.make_prefill("layer_8k", seed=sum(lengths), device=DEV, lengths=lengths, H=4,
                              s0_std=0.02, conv_state=True, rms_w="random")
@@ -130,10 +132,14 @@ def test_prefill_empty_sequences_and_zero_tokens():
     torch.testing.assert_close(fin[2], inp.initial_state[2], rtol=0, atol=0)
 
 
-@pytest.mark.parametrize("flags", [0, _lib.KDA_FLAG_FORCE_SIMT])
-def test_packed_equals_solo_bitwise(flags):
-    """cu_seqlens indexing: each sequence of a packed batch equals its solo run bit for bit."""
-    lengths = [70, 1, 128, 5, 64]
+@pytest.mark.parametrize("flags,lengths", [
+    (_lib.KDA_FLAG_NO_RECURRENT, [70, 1, 128, 5, 64]),
+    (_lib.KDA_FLAG_FORCE_SIMT, [70, 1, 128, 5, 64]),
+    (0, [1, 8, 3, 0, 5]),  # all short: the recurrent path for the batch and for each solo run
+])
+def test_packed_equals_solo_bitwise(flags, lengths):
+    """cu_seqlens indexing: each sequence of a packed batch equals its solo run bit for bit
+    (both through the same path)."""
     inp = synth.make_prefill("layer_8k", seed=9, device=DEV, lengths=lengths, H=3, s0_std=0.02,
                              conv_state=True)
     out, fin, _ = _prefill(inp, flags=flags)
