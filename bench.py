@@ -204,7 +204,11 @@ def run_ours(args):
     if args.mode == "prefill":
         args.decode_steps = 0
         args.verify_steps = 0
-    inp = synth.make_prefill(args.workload, seed=1, device=dev)
+    if args.tokens:  # a shorter case of the same workload (profiling captures)
+        inp = synth.make_prefill(args.workload, seed=1, device=dev, T=args.tokens,
+                                 N=synth.WORKLOADS[args.workload]["N"])
+    else:
+        inp = synth.make_prefill(args.workload, seed=1, device=dev)
     N, T, H, D = inp.N, inp.T, inp.H, inp.D
     path, segments, ws_bytes = prefill_path(inp)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
@@ -348,7 +352,9 @@ def run_ours(args):
                 "ms_per_step": round(ms_max, 4), "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16" if path == "tc" else "fp32",
                 "data": "synthetic",
-                "config": {"workload": workload_desc(args.workload), "global_batch": N * world,
+                "config": {"workload": workload_desc(args.workload) +
+                           (f" (shortened to T={T} for a profile)" if args.tokens else ""),
+                           "global_batch": N * world,
                            "seq_len": T, "heads": H, "head_dim": D, "chunk": inp.chunk,
                            "prefill_path": path, "segments": segments, "l2": "inputs larger than L2 (no flush)",
                            "parallelism": f"replicas x{world}"},
@@ -527,6 +533,8 @@ def main():
                     help="profiling aid: run only one of the measurements (verify = the "
                          "multi-token decode loop)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling aid: total tokens of a shorter case of --workload")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
