@@ -194,7 +194,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     int64_t s0, s1;
     seq_range(cu, n, T_total, s0, s1);
     int64_t cb, ce;  // this CTA's chunks [cb, ce) of the sequence
-    seg_chunk_range((s1 - s0 + kC - 1) / kC, sp.P, seg, cb, ce);
+    seg_chunk_range((s1 - s0 + kC - 1) / kC, sp.P, sp.w, seg, cb, ce);
 
     if (warp == 0) {
         tmem_alloc(&s_tbase, kTmemCols);
@@ -870,9 +870,18 @@ int device_sm_count() {
     return g_sm_count[dev];
 }
 
-// Fewest chunks per segment the automatic choice allows: below this the fix-up
-// and the doubled runs cost more than the shorter chain saves.
-constexpr int64_t kMinSegChunks = 32;
+// Cost model of the automatic segment choice, in units of one chunk step of one CTA
+// (about 21 us measured on GB300, the same for every role):
+//  - segment-0 CTAs occupy U SMs for its w / (w + P - 1) share of the chunks; the
+//    2 U (P - 1) shorter CTAs of the later segments run on the other SMs in
+//    w = ceil(2 U (P - 1) / (SMs - U)) waves, which the split balances;
+//  - the fix-up streams 1,536 bytes per token-head of the later segments, measured at
+//    about 39 ns per (unit, chunk), i.e. kFixupPerUnitChunk chunk steps, across the GPU;
+//  - each extra launch and CTA start-up costs about kSegOverhead chunk steps.
+constexpr double kFixupPerUnitChunk = 0.0019;
+constexpr double kSegOverhead = 2.0;
+// Fewest chunks per later segment the automatic choice allows.
+constexpr double kMinSegChunks = 8.0;
 
 // Workspace layout of a segmented launch (offsets in bytes, 256-aligned).
 struct SegLayout {
@@ -916,27 +925,41 @@ bool tc_prefill_applies(const kda_prefill_args& a) {
            device_supports_tc();
 }
 
-int tc_segments(const kda_prefill_args& a) {
-    if (a.segments > 0) return a.segments < KDA_MAX_SEGMENTS ? a.segments : KDA_MAX_SEGMENTS;
-    const int64_t units = (int64_t)a.N * a.H;
-    if (units <= 0 || a.T_total <= 0) return 1;
-    // one wave of CTAs: 2P - 1 per unit must fit the SMs (one CTA per SM)
-    int64_t P = ((int64_t)device_sm_count() / units + 1) / 2;
-    const int64_t avg_chunks = a.T_total / ((int64_t)a.N * kC);
-    if (P > avg_chunks / kMinSegChunks) P = avg_chunks / kMinSegChunks;
-    if (P > KDA_MAX_SEGMENTS) P = KDA_MAX_SEGMENTS;
-    if (units * (2 * P - 1) > 0x7fffffffLL) P = 1;
-    return P < 1 ? 1 : (int)P;
+SegChoice tc_seg_choice(const kda_prefill_args& a) {
+    if (a.segments > 0) return {a.segments < KDA_MAX_SEGMENTS ? a.segments : KDA_MAX_SEGMENTS, 1};
+    const int64_t U = (int64_t)a.N * a.H;
+    const int64_t S = device_sm_count();
+    if (U <= 0 || a.T_total <= 0 || a.N <= 0 || U >= S) return {1, 1};
+    const double C = (double)a.T_total / ((double)a.N * kC);  // mean chunks per sequence
+    SegChoice best{1, 1};
+    double best_cost = C;
+    for (int P = 2; P <= KDA_MAX_SEGMENTS; ++P) {
+        if (U * (2 * P - 1) > 0x7fffffffLL) break;
+        const int64_t w = (2 * U * (P - 1) + (S - U) - 1) / (S - U);
+        const double b = C / (double)(w + P - 1);  // chunks per later segment
+        if (b < kMinSegChunks) continue;
+        const double first = (double)w * b;
+        const double cost = first + kFixupPerUnitChunk * (double)U * (C - first) + kSegOverhead;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = {P, (int)w};
+        }
+    }
+    return best;
 }
+
+int tc_segments(const kda_prefill_args& a) { return tc_seg_choice(a).P; }
 
 size_t tc_prefill_workspace(const kda_prefill_args& a) { return seg_layout(a, tc_segments(a)).total; }
 
 cudaError_t launch_tc_prefill(const kda_prefill_args& a, char* ws, cudaStream_t s) {
     const int64_t units = (int64_t)a.N * a.H;
     if (units == 0) return cudaSuccess;
-    const int P = tc_segments(a);
+    const SegChoice sc = tc_seg_choice(a);
+    const int P = sc.P;
     SegPlan sp{};
     sp.P = P;
+    sp.w = sc.w;
     if (P > 1) {
         const SegLayout l = seg_layout(a, P);
         sp.end_state = reinterpret_cast<float*>(ws + l.end_state);
@@ -947,7 +970,7 @@ cudaError_t launch_tc_prefill(const kda_prefill_args& a, char* ws, cudaStream_t 
     }
     cudaError_t e = a.out_dtype == KDA_FP32 ? tc_launch<float>(a, sp, s) : tc_launch<bf16>(a, sp, s);
     if (e != cudaSuccess || P == 1) return e;
-    if ((e = launch_seg_combine(sp, (int)units, a.final_state, s)) != cudaSuccess) return e;
+    if ((e = launch_seg_combine(sp, (int)units, a.final_state, a.d_status, s)) != cudaSuccess) return e;
     return launch_seg_fixup(sp, a.cu_seqlens, a.N, a.T_total, a.H, (const bf16*)a.gate, a.rms_w,
                             a.eps_rms, a.out, a.out_dtype, device_sm_count(), a.d_status, s);
 }

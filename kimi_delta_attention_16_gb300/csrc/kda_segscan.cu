@@ -26,77 +26,176 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // ---------------------------------------------------------------- composition
-// Block (u, jb) composes value columns [16 jb, 16 jb + 16) of unit u; thread
-// (row c = tid % 128, half jh = tid / 128) makes 8 of them per step.  Shared
-// memory: M_s [128][129] (padded rows), then the current S columns [128][16].
-constexpr int kCombThreads = 256;
-constexpr int kMs = 129;
-constexpr size_t kCombSmem = (size_t)(kD * kMs + kD * 16) * sizeof(float);
+// One block of 512 threads per unit walks its segments in order on the tensor cores
+// (kind::f16, 3-term bf16 split, fp32 accumulate in TMEM):
+//
+//   S_{s+1}^T = S_s^T . M_s^T + B_s^T      A = S_s^T (TMEM, hi/lo), B = M_s (smem, hi/lo, K-major)
+//
+// Thread (lane j = 32 (warp % 4) + lane, quarter qt = warp / 4) owns rows c in
+// [32 qt, 32 qt + 32) of column j of the states: it adds B_s[c][j] to its accumulator
+// entries, stores S_{s+1}[c][j] (coalesced over j) and splits them back into the A operand
+// for the next step.  M_s arrives as coalesced 32-byte pieces, four per thread.
+constexpr int kCombThreads = 512;
+constexpr uint32_t kCombOffBhi = 0;
+constexpr uint32_t kCombOffBlo = 32768;
+constexpr size_t kCombSmem = 65536 + 1024;  // + alignment slack
+constexpr uint32_t kCombTmemCols = 256;     // S^T hi/lo [0,128), accumulator [128,256)
 
-__global__ void __launch_bounds__(kCombThreads) k_seg_combine(SegPlan sp, float* __restrict__ S_fin) {
-    extern __shared__ float csm[];
-    float* sM = csm;
-    float* sS = csm + kD * kMs;
-    const int u = blockIdx.x, jb = blockIdx.y;
-    const int tid = threadIdx.x, c = tid & (kD - 1), jh = tid >> 7;
+__device__ __forceinline__ void split2c(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16x2(a, b);
+    const float ah = __uint_as_float(hi << 16), bh = __uint_as_float(hi & 0xffff0000u);
+    lo = pack_bf16x2(a - ah, b - bh);
+}
+
+__global__ void __launch_bounds__(kCombThreads, 1)
+k_seg_combine(SegPlan sp, float* __restrict__ S_fin, int* d_status) {
+    using namespace tc;
+    extern __shared__ uint8_t csm_raw[];
+    __shared__ uint64_t bar;
+    __shared__ uint32_t s_tbase;
+    const uint32_t raw_addr = smem_u32(csm_raw);
+    uint8_t* sm = csm_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+    const uint32_t sbase = smem_u32(sm);
+    const int u = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int qd = warp & 3, qt = warp >> 2;
+    const int j = 32 * qd + lane;
+    const uint32_t lane_off = (uint32_t)(qd * 32) << 16;
     const int P = sp.P;
     const int64_t DD = (int64_t)kD * kD;
     const float* E = sp.end_state + (int64_t)u * P * DD;
     const float* M = sp.trans + (int64_t)u * P * DD;
     float* St = sp.start + (int64_t)u * P * DD;
-    for (int idx = tid; idx < kD * 16; idx += kCombThreads)  // S_1: end state of segment 0
-        sS[idx] = E[(idx >> 4) * kD + 16 * jb + (idx & 15)];
-    for (int s = 1; s < P; ++s) {
-        __syncthreads();  // sS holds S_s; the previous step's reads of sM are done
-        for (int idx = tid; idx < kD * 16; idx += kCombThreads)
-            St[s * DD + (idx >> 4) * kD + 16 * jb + (idx & 15)] = sS[idx];
-        for (int idx = tid; idx < kD * kD; idx += kCombThreads)
-            sM[(idx >> 7) * kMs + (idx & (kD - 1))] = M[s * DD + idx];
-        __syncthreads();
-        float acc[8];
-        const float* Bs = E + s * DD + (int64_t)c * kD + 16 * jb + 8 * jh;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = Bs[e];
-#pragma unroll 4
-        for (int k = 0; k < kD; ++k) {
-            const float m = sM[c * kMs + k];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = fmaf(m, sS[k * 16 + 8 * jh + e], acc[e]);
-        }
-        __syncthreads();  // every read of S_s is done
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sS[c * 16 + 8 * jh + e] = acc[e];
+
+    if (warp == 0) {
+        tmem_alloc(&s_tbase, kCombTmemCols);
+        tmem_relinquish();
     }
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    fence_before_sync();
     __syncthreads();
-    if (S_fin)
-        for (int idx = tid; idx < kD * 16; idx += kCombThreads)
-            S_fin[(int64_t)u * DD + (idx >> 4) * kD + 16 * jb + (idx & 15)] = sS[idx];
+    fence_after_sync();
+    const uint32_t tb = s_tbase;
+    const uint32_t idesc = idesc_bf16(128, 128, false, false);
+
+    // rows [32 qt, 32 qt + 32) of column j -> A operand columns of that K range
+    auto put_operand = [&](const float (&col)[32]) {
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) split2c(col[2 * i], col[2 * i + 1], hi[i], lo[i]);
+        tmem_st16(tb + lane_off + 16 * qt, hi);
+        tmem_st16(tb + lane_off + 64 + 16 * qt, lo);
+        tmem_st_wait();
+    };
+    {
+        float col[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) col[i] = E[(int64_t)(32 * qt + i) * kD + j];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) St[DD + (int64_t)(32 * qt + i) * kD + j] = col[i];  // S_1
+        put_operand(col);
+    }
+    bool failed = false;
+    for (int s = 1; s < P; ++s) {
+        // M_s -> B tile (K-major, 128-byte swizzle), hi and lo: piece (row c, k8) per thread
+        {
+            float4 a[4], b[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int idx = tid + t * kCombThreads, c = idx >> 4, k8 = idx & 15;
+                const float* src = M + s * DD + (int64_t)c * kD + 8 * k8;
+                a[t] = *reinterpret_cast<const float4*>(src);
+                b[t] = *reinterpret_cast<const float4*>(src + 4);
+            }
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int idx = tid + t * kCombThreads, c = idx >> 4, k8 = idx & 15;
+                uint4 hv, lv;
+                split2c(a[t].x, a[t].y, hv.x, lv.x);
+                split2c(a[t].z, a[t].w, hv.y, lv.y);
+                split2c(b[t].x, b[t].y, hv.z, lv.z);
+                split2c(b[t].z, b[t].w, hv.w, lv.w);
+                *reinterpret_cast<uint4*>(sm + kCombOffBhi + kmajor_off(128, c, k8)) = hv;
+                *reinterpret_cast<uint4*>(sm + kCombOffBlo + kmajor_off(128, c, k8)) = lv;
+            }
+        }
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            fence_after_sync();
+#pragma unroll
+            for (int term = 0; term < 3; ++term) {
+                const uint32_t acol = term == 1 ? 64 : 0;
+                const uint32_t bt = sbase + (term == 2 ? kCombOffBlo : kCombOffBhi);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tb + 128, tb + acol + 8 * kk, desc_sw128(bt + (kk >> 2) * 128 * 128 + (kk & 3) * 32, 16, 1024),
+                           idesc, (term | kk) != 0);
+            }
+            mma_commit(&bar);
+        }
+        // B_s entries of this thread, fetched while the tensor cores work
+        float col[32];
+        const float* Bs = E + s * DD;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) col[i] = Bs[(int64_t)(32 * qt + i) * kD + j];
+        failed = !__syncthreads_and(mbar_wait(&bar, (uint32_t)(s - 1) & 1u));
+        if (failed) break;
+        fence_after_sync();
+        {
+            uint32_t dv[32];
+            tmem_ld32(tb + lane_off + 128 + 32 * qt, dv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) col[i] += __uint_as_float(dv[i]);
+        }
+        // S_{s+1}[c][j] for c in [32 qt, 32 qt + 32)
+        float* dst = s + 1 < P ? St + (s + 1) * DD : (S_fin ? S_fin + (int64_t)u * DD : nullptr);
+        if (dst)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) dst[(int64_t)(32 * qt + i) * kD + j] = col[i];
+        fence_before_sync();
+        __syncthreads();  // every accumulator read and every read of the B tile is done
+        fence_after_sync();
+        if (s + 1 < P) put_operand(col);
+    }
+    if (failed && tid == 0) flag_status(d_status, KDA_ERR_TIMEOUT);
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tb, kCombTmemCols);
 }
 
 // ---------------------------------------------------------------- fix-up
 // Block (pair, y): pair = u * (P - 1) + s - 1 names (unit, segment s >= 1); the
-// block takes 128-token tiles y, y + gridDim.y, ... of that segment.  Per tile,
+// block takes 64-token tiles y, y + gridDim.y, ... of that segment.  Per tile,
 // on the tensor cores (kind::f16, fp32 accumulate in TMEM):
 //
 //   O^T[j][t] = sum_k S_s[k][j] F[t][k]      A = S_s^T (TMEM, hi/lo), B = F tile (smem, hi/lo)
 //
 // with the 3-term bf16 split hi.hi + lo.hi + hi.lo (about 2^-16 relative), then
 // o = o' + O, y = o / sqrt(mean_j o^2 + eps) * w_j * sigmoid(gate).  Thread
-// (lane j = 32 (warp % 4) + lane, quarter qt = warp / 4) finishes tokens
+// (lane j = 32 (warp % 4) + lane, half qt = warp / 4) finishes tokens
 // [32 qt, 32 qt + 32) of value channel j, so the o', gate and y rows are
 // read and written coalesced.  The next tile's F and gate rows are fetched
-// with cp.async while the current one is multiplied and finished.
-constexpr int kFixThreads = 512;
-constexpr int kFixTile = 128;                 // tokens per tile (MMA N)
+// with cp.async while the current one is multiplied and finished; two blocks
+// share an SM (about 101 KB of shared memory and 256 TMEM columns each) and
+// hide each other's load round-trips.
+constexpr int kFixThreads = 256;
+constexpr int kFixTile = 64;                  // tokens per tile (MMA N)
 constexpr uint32_t kFixRawStride = 528;       // fp32 F rows, padded: conflict-free 16-byte reads
 constexpr uint32_t kFixOffRaw = 0;
-constexpr uint32_t kFixOffBhi = 67584;        // 128 x 528, rounded to 1024
-constexpr uint32_t kFixOffBlo = kFixOffBhi + 32768;
-constexpr uint32_t kFixOffGate = kFixOffBlo + 32768;  // 2 x [128 tokens][128] bf16 (double buffer)
-constexpr uint32_t kFixOffRed = kFixOffGate + 65536;  // [4 quadrants][128 tokens] fp32
-constexpr uint32_t kFixOffInv = kFixOffRed + 2048;    // [128] fp32
-constexpr size_t kFixSmem = kFixOffInv + 512 + 1024;  // + alignment slack
-constexpr uint32_t kFixTmemCols = 256;        // S^T hi/lo [0,128), O^T [128,256)
+constexpr uint32_t kFixOffBhi = 34816;        // 64 x 528, rounded to 1024
+constexpr uint32_t kFixOffBlo = kFixOffBhi + kFixTile * 256;
+constexpr uint32_t kFixOffGate = kFixOffBlo + kFixTile * 256;  // 2 x [64 tokens][128] bf16
+constexpr uint32_t kFixOffRed = kFixOffGate + 2 * kFixTile * 256;  // [4 quadrants][64 tokens] fp32
+constexpr uint32_t kFixOffInv = kFixOffRed + 4 * kFixTile * 4;     // [64] fp32
+constexpr size_t kFixSmem = kFixOffInv + kFixTile * 4 + 1024;  // + alignment slack
+constexpr uint32_t kFixTmemCols = 256;        // S^T hi/lo [0,128), O^T [128,192)
+static_assert(kFixTile * kFixRawStride <= kFixOffBhi, "F staging overlaps the operand tile");
 
 __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
     hi = pack_bf16x2(a, b);
@@ -105,7 +204,7 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
 }
 
 template <typename To>
-__global__ void __launch_bounds__(kFixThreads, 1)
+__global__ void __launch_bounds__(kFixThreads, 2)
 k_seg_fixup(SegPlan sp, const int32_t* __restrict__ cu, int64_t T_total, int H,
             const bf16* __restrict__ gate, const float* __restrict__ rms_w, float eps_rms,
             To* __restrict__ out, int* d_status) {
@@ -119,7 +218,7 @@ k_seg_fixup(SegPlan sp, const int32_t* __restrict__ cu, int64_t T_total, int H,
     int64_t s0, s1;
     seq_range(cu, n, T_total, s0, s1);
     int64_t cb, ce;
-    seg_chunk_range((s1 - s0 + 63) / 64, sp.P, s, cb, ce);
+    seg_chunk_range((s1 - s0 + 63) / 64, sp.P, sp.w, s, cb, ce);
     const int64_t ta = s0 + cb * 64;
     const int64_t tz = s0 + ce * 64 < s1 ? s0 + ce * 64 : s1;
     const int64_t ntiles = tz > ta ? (tz - ta + kFixTile - 1) / kFixTile : 0;
@@ -157,7 +256,7 @@ k_seg_fixup(SegPlan sp, const int32_t* __restrict__ cu, int64_t T_total, int H,
             for (int idx = tid; idx < kFixTile * 16; idx += kFixThreads) {
                 const int row = idx >> 4, c8 = idx & 15;
                 if (tb + row < tz)
-                    cp_async16(sbase + kFixOffGate + gbuf * 32768 + row * 256 + 16 * c8,
+                    cp_async16(sbase + kFixOffGate + gbuf * (kFixTile * 256) + row * 256 + 16 * c8,
                                gate + ((tb + row) * H + h) * kD + 8 * c8);
             }
         cp_async_commit();
@@ -168,14 +267,17 @@ k_seg_fixup(SegPlan sp, const int32_t* __restrict__ cu, int64_t T_total, int H,
     fence_after_sync();
     const uint32_t tb = s_tbase;
     {
-        // S_s^T operand: lane j holds column j of S_s, K = key channels [32 qt, 32 qt + 32)
+        // S_s^T operand: lane j holds column j of S_s, K = key channels [64 qt, 64 qt + 64)
         const float* St = sp.start + ((int64_t)u * sp.P + s) * kD * kD;
-        uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            split2(St[(int64_t)(32 * qt + 2 * i) * kD + j], St[(int64_t)(32 * qt + 2 * i + 1) * kD + j], hi[i], lo[i]);
-        tmem_st16(tb + lane_off + 16 * qt, hi);
-        tmem_st16(tb + lane_off + 64 + 16 * qt, lo);
+        for (int part = 2 * qt; part < 2 * qt + 2; ++part) {
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                split2(St[(int64_t)(32 * part + 2 * i) * kD + j], St[(int64_t)(32 * part + 2 * i + 1) * kD + j], hi[i], lo[i]);
+            tmem_st16(tb + lane_off + 16 * part, hi);
+            tmem_st16(tb + lane_off + 64 + 16 * part, lo);
+        }
         tmem_st_wait();
     }
     const float wj = rms_w ? rms_w[j] : 1.f;
@@ -220,12 +322,13 @@ k_seg_fixup(SegPlan sp, const int32_t* __restrict__ cu, int64_t T_total, int H,
             mma_commit(&bar);
         }
         // o' of this thread's 32 tokens, fetched while the tensor cores work
+        const int64_t row0 = t0 + 32 * qt;                // first token of this thread
+        const int nvalid = (int)(tz - row0 < 32 ? (tz - row0 < 0 ? 0 : tz - row0) : 32);
+        const int64_t rstride = (int64_t)H * kD;          // elements between tokens
+        const float* op = sp.o_loc + (row0 * H + h) * kD + j;
         float o[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-            const int64_t t = t0 + 32 * qt + e;
-            o[e] = t < tz ? sp.o_loc[(t * H + h) * kD + j] : 0.f;
-        }
+        for (int e = 0; e < 32; ++e) o[e] = e < nvalid ? op[e * rstride] : 0.f;
         failed = !__syncthreads_and(mbar_wait(&bar, iter & 1u));
         if (failed) break;
         fence_after_sync();
@@ -265,15 +368,15 @@ k_seg_fixup(SegPlan sp, const int32_t* __restrict__ cu, int64_t T_total, int H,
             sInv[tid] = rsqrtf((sRed[tid] + sRed[kFixTile + tid] + sRed[2 * kFixTile + tid] +
                                 sRed[3 * kFixTile + tid]) * (1.0f / kD) + eps_rms);
         __syncthreads();
-        const bf16* gt = reinterpret_cast<const bf16*>(sm + kFixOffGate + (iter & 1u) * 32768);
+        const bf16* gt = reinterpret_cast<const bf16*>(sm + kFixOffGate + (iter & 1u) * (kFixTile * 256)) +
+                         32 * qt * kD + j;
+        To* yp = out + (row0 * H + h) * kD + j;
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-            const int r = 32 * qt + e;
-            const int64_t t = t0 + r;
-            if (t < tz) {
-                float y = o[e] * sInv[r] * wj;
-                if (gate) y *= 1.0f / (1.0f + __expf(-to_f(gt[r * kD + j])));
-                out[(t * H + h) * kD + j] = from_f<To>(y);
+            if (e < nvalid) {
+                float y = o[e] * sInv[32 * qt + e] * wj;
+                if (gate) y *= __fdividef(1.0f, 1.0f + __expf(-to_f(gt[e * kD])));
+                yp[e * rstride] = from_f<To>(y);
             }
         }
         fence_before_sync();  // this tile's TMEM reads precede the next tile's MMAs (barrier above them)
@@ -287,12 +390,12 @@ k_seg_fixup(SegPlan sp, const int32_t* __restrict__ cu, int64_t T_total, int H,
 
 }  // namespace
 
-cudaError_t launch_seg_combine(const SegPlan& sp, int units, float* S_fin, cudaStream_t s) {
+cudaError_t launch_seg_combine(const SegPlan& sp, int units, float* S_fin, int* d_status, cudaStream_t s) {
     if (sp.P <= 1 || units <= 0) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(k_seg_combine, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kCombSmem);
     if (e != cudaSuccess) return e;
-    k_seg_combine<<<dim3((unsigned)units, kD / 16), kCombThreads, kCombSmem, s>>>(sp, S_fin);
+    k_seg_combine<<<(unsigned)units, kCombThreads, kCombSmem, s>>>(sp, S_fin, d_status);
     return cudaGetLastError();
 }
 
@@ -301,8 +404,9 @@ cudaError_t launch_seg_fixup(const SegPlan& sp, const int32_t* cu, int N, int64_
                              kda_dtype out_dt, int sms, int* d_status, cudaStream_t s) {
     const int64_t pairs = (int64_t)N * H * (sp.P - 1);
     if (sp.P <= 1 || pairs <= 0 || T_total <= 0) return cudaSuccess;
-    // one block per SM (shared memory and TMEM allow no more), spread over the pairs
-    int64_t gy = sms / pairs;
+    // two blocks per SM (shared memory, TMEM and registers allow no more); about four
+    // blocks per SM over the pairs, so the last wave is short
+    int64_t gy = (4 * (int64_t)sms + pairs - 1) / pairs;
     const int64_t max_tiles = (T_total + kFixTile - 1) / kFixTile;
     if (gy > max_tiles) gy = max_tiles;
     if (gy > 65535) gy = 65535;

@@ -9,9 +9,15 @@ namespace kda {
 // bf16 inputs) and this device supports it.
 bool tc_prefill_applies(const kda_prefill_args& a);
 
-// Segments per (sequence, head) the tensor-core path cuts each sequence into
-// (1 = none): args.segments when set, else chosen so that the launch fills the
-// SMs in one wave.
+// How the tensor-core path cuts each sequence: P segments (1 = none); segment 0
+// holds the fraction w / (w + P - 1) of the chunks, the others share the rest
+// equally.  args.segments forces P (with w = 1: equal segments); otherwise
+// (P, w) minimise a cost model of the launch (see tc_seg_choice).
+struct SegChoice {
+    int P;
+    int w;
+};
+SegChoice tc_seg_choice(const kda_prefill_args& a);
 int tc_segments(const kda_prefill_args& a);
 
 // Scratch bytes the tensor-core path needs.
@@ -25,6 +31,7 @@ cudaError_t launch_tc_prefill(const kda_prefill_args& a, char* ws, cudaStream_t 
 // unit u = n * H + h is one (sequence, head).
 struct SegPlan {
     int P;             // segments per unit; 1 = one CTA walks each whole sequence
+    int w;             // segment 0 takes w / (w + P - 1) of the chunks
     float* end_state;  // [units][P][D][D]: segment 0's end state, then B_s (zero-start runs)
     float* trans;      // [units][P][D][D]: M_s, the end states of the identity-start runs
     float* start;      // [units][P][D][D]: S_s, the composed start state of segment s >= 1
@@ -33,19 +40,35 @@ struct SegPlan {
 };
 
 // Chunks [cb, ce) of segment s when a sequence of nc chunks is cut into P
-// segments of ceil(nc / P) chunks (trailing segments may be short or empty).
-__host__ __device__ __forceinline__ void seg_chunk_range(int64_t nc, int P, int s, int64_t& cb,
+// segments: segment 0 is the first ceil(nc * w / (w + P - 1)) chunks, the
+// others split the rest into runs of ceil(rest / (P - 1)) (trailing segments
+// may be short or empty).  w = 1 gives P segments of about nc / P.
+__host__ __device__ __forceinline__ void seg_chunk_range(int64_t nc, int P, int w, int s, int64_t& cb,
                                                          int64_t& ce) {
-    const int64_t sl = (nc + P - 1) / P;
-    const int64_t b = (int64_t)s * sl;
+    if (P <= 1) {
+        cb = 0;
+        ce = nc;
+        return;
+    }
+    const int64_t den = (int64_t)w + P - 1;
+    int64_t c0 = (nc * w + den - 1) / den;
+    c0 = c0 < nc ? c0 : nc;
+    if (s == 0) {
+        cb = 0;
+        ce = c0;
+        return;
+    }
+    const int64_t sl = (nc - c0 + P - 2) / (P - 1);
+    const int64_t b = c0 + (int64_t)(s - 1) * sl;
     cb = b < nc ? b : nc;
     ce = cb + sl < nc ? cb + sl : nc;
 }
 
 // Composes, per unit and in segment order, S_1 = end_state[0] and
-// S_{s+1} = M_s S_s + B_s; writes S_1 .. S_{P-1} to sp.start and S_P to S_fin
-// (when non-NULL, [N][H][D][D]).
-cudaError_t launch_seg_combine(const SegPlan& sp, int units, float* S_fin, cudaStream_t s);
+// S_{s+1} = M_s S_s + B_s (tensor cores); writes S_1 .. S_{P-1} to sp.start and
+// S_P to S_fin (when non-NULL, [N][H][D][D]).  A tensor-core wait that times out
+// sets KDA_ERR_TIMEOUT in d_status.
+cudaError_t launch_seg_combine(const SegPlan& sp, int units, float* S_fin, int* d_status, cudaStream_t s);
 
 // For every token of segments s >= 1: o = o_loc + S_s^T f (tensor cores), then
 // y = RMSNorm(o) * rms_w * sigmoid(gate) -> out (bf16 or fp32 rows [T][H][D]).

@@ -97,25 +97,34 @@ def test_segments_in_place_state():
 
 
 def test_auto_plan_fills_the_sms():
-    """The automatic choice: 2P - 1 CTAs per (sequence, head) in one wave of one CTA per SM,
-    at least 32 chunks per segment, at most 16 segments."""
+    """The automatic choice: batches with fewer (sequence, head) units than SMs are cut into
+    segments (at most 16), others are not; `segments` forces a count."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-
-    def expect(N, T, H):
-        p = (sms // (N * H) + 1) // 2
-        p = min(p, (T // (N * 64)) // 32, 16)
-        return max(p, 1)
-
     for name in ("long_1m", "layer_8k"):
         w = synth.WORKLOADS[name]
-        got = kda.kda_prefill_plan(w["T"], w["H"], w["D"], N=w["N"])
-        assert got == ("tc", expect(w["N"], w["T"], w["H"])), (name, got)
-    assert kda.kda_prefill_plan(1 << 20, 24, 128)[1] == expect(1, 1 << 20, 24)
-    assert kda.kda_prefill_plan(8192, 96, 128) == ("tc", 1)
+        path, P = kda.kda_prefill_plan(w["T"], w["H"], w["D"], N=w["N"])
+        assert path == "tc"
+        if w["N"] * w["H"] < sms:
+            assert 2 <= P <= 16, (name, P)
+    assert kda.kda_prefill_plan(73000, 96, 128, N=16) == ("tc", 1)       # 1,536 units
+    assert kda.kda_prefill_plan(8192, sms, 128) == ("tc", 1)             # units = SMs
     assert kda.kda_prefill_plan(1 << 20, 24, 128, segments=1) == ("tc", 1)
+    assert kda.kda_prefill_plan(1 << 20, 24, 128, segments=5) == ("tc", 5)
     assert kda.kda_prefill_plan(1 << 20, 24, 128, io=torch.float32)[0] == "simt"
-    if sms == 152:
-        assert kda.kda_prefill_plan(1 << 20, 24, 128) == ("tc", 3)
+    assert kda.kda_prefill_plan(256, 4, 128)[1] == 1                      # 4 chunks: too short
+
+
+def test_auto_plan_unequal_segments_parity():
+    """The automatic plan on a batch with fewer units than SMs (unequal segments: a long first
+    segment, short later ones) against the oracle, slow decay."""
+    inp = synth.make_prefill("layer_8k", seed=55, device=DEV, N=1, T=64 * 100 + 17, H=48,
+                             s0_std=0.02, conv_state=True, g_range=MILD)
+    assert _plan(inp)[1] >= 2
+    out, fin = _run(inp, 0)
+    heads = [0, 17, 47]
+    ref = oracle_prefill(inp, heads=heads)
+    check_out(to_np(out[:, heads]), ref["out"], 1, TOL_OUT_BF16, bf16_out=True)
+    assert per_head_rel(to_np(fin[:, heads]), ref["final_state"], 1).max() <= TOL_STATE_BF16
 
 
 @pytest.mark.slow
