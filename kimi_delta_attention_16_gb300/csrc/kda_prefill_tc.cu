@@ -141,6 +141,11 @@ __device__ __forceinline__ void split8(const float v[8], uint4& hi, uint4& lo) {
     split2(v[6], v[7], hi.w, lo.w);
 }
 
+// The triangular solve runs on warps 0..kSolveWarps-1 with their own named barrier (1);
+// barrier 0 is __syncthreads.
+constexpr int kSolveWarps = 6;
+__device__ __forceinline__ void solver_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kSolveWarps) : "memory"); }
+
 __device__ __forceinline__ void sts128(uint8_t* base, uint32_t off, const uint4& v) {
     *reinterpret_cast<uint4*>(base + off) = v;
 }
@@ -477,11 +482,12 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         fence_before_sync();
         __syncthreads();
 
-        // ------------------------------------------------ B: issue G1 ([M;A]) and G3 (state reads)
+        // ------------------------------------------------ B: issue G1 ([M;A])
+        // (G3, the state reads, is issued later by warp 15, which the solve leaves idle: the
+        // issuing thread waits while the tensor pipe accepts its MMAs, and G3 is needed only in D)
         if (tid == 0) {
             fence_after_sync();
             const uint32_t b1h = sbase + kOffB1hi, b1l = sbase + kOffB1lo;
-            const uint32_t b3h = sbase + kOffB3hi, b3l = sbase + kOffB3lo;
 #pragma unroll
             for (int term = 0; term < 3; ++term) {
                 const uint32_t acol = kColX + (term == 1 ? 64 : 0);
@@ -493,17 +499,6 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                            (term | kk) != 0);
             }
             mma_commit(&bars[0]);
-#pragma unroll
-            for (int term = 0; term < 3; ++term) {
-                const uint32_t acol = kColS + (term == 1 ? 64 : 0);
-                const uint32_t bt3 = term == 2 ? b3l : b3h;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tb + kColP, tb + acol + 8 * kk,
-                           desc_sw128(bt3 + (kk >> 2) * 128 * 128 + (kk & 3) * 32, 16, 1024), id_g3,
-                           (term | kk) != 0);
-            }
-            mma_commit(&bars[1]);
         }
 
         // ------------------------------------------------ C: M and A from G1, T = (I + A)^-1
@@ -563,34 +558,52 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 for (int e = 0; e < 16; ++e) sAf[r * kAs + 16 * qt + e] = row[e];
             }
         }
+        fence_before_sync();
         __syncthreads();
-        // T: unit lower triangular inverse.  Diagonal 16x16 blocks: one warp per block, lane jj
-        // (lanes 16..31 mirror 0..15) keeps column jj of the block in registers.
-        if (warp < 4) {
-            const int b0 = 16 * warp, jj = lane & 15;
-            float t[16];
+        // G3: [P ; Q'] = S^T . [KG ; QG]^T (state reads), from warp 15 while warps 0-5 solve
+        if (tid == kThreads - 32) {
+            fence_after_sync();
+            const uint32_t b3h = sbase + kOffB3hi, b3l = sbase + kOffB3lo;
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) {
-                float acc = rr == jj ? 1.f : 0.f;
-                const float* arow = sAf + (b0 + rr) * kAs + b0;
+            for (int term = 0; term < 3; ++term) {
+                const uint32_t acol = kColS + (term == 1 ? 64 : 0);
+                const uint32_t bt3 = term == 2 ? b3l : b3h;
 #pragma unroll
-                for (int ii = 0; ii < rr; ++ii) acc -= arow[ii] * t[ii];
-                t[rr] = acc;
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ts(tb + kColP, tb + acol + 8 * kk,
+                           desc_sw128(bt3 + (kk >> 2) * 128 * 128 + (kk & 3) * 32, 16, 1024), id_g3,
+                           (term | kk) != 0);
             }
-            if (lane < 16) {
-#pragma unroll
-                for (int rr = 0; rr < 16; ++rr) sTf[(b0 + rr) * 64 + b0 + jj] = t[rr];
-            }
+            mma_commit(&bars[1]);
         }
-        __syncthreads();
-        // Off-diagonal 16-blocks by block diagonal d: X_IJ = sum_{K=J}^{I-1} A_IK T_KJ, then
-        // T_IJ = -T_II X_IJ.  A thread makes four adjacent outputs (one broadcast load of A or
-        // T_II and one float4 load per k); X lives in the idle row-reduction scratch.
-        {
+        // T: unit lower triangular inverse, by warps 0-5 (their own named barrier: the other
+        // warps go on to D, and warp 15 issues G3 meanwhile).  Diagonal 16x16 blocks: one warp
+        // per block, lane jj (lanes 16..31 mirror 0..15) keeps column jj of the block in registers.
+        if (warp < kSolveWarps) {
+            if (warp < 4) {
+                const int b0 = 16 * warp, jj = lane & 15;
+                float t[16];
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) {
+                    float acc = rr == jj ? 1.f : 0.f;
+                    const float* arow = sAf + (b0 + rr) * kAs + b0;
+#pragma unroll
+                    for (int ii = 0; ii < rr; ++ii) acc -= arow[ii] * t[ii];
+                    t[rr] = acc;
+                }
+                if (lane < 16) {
+#pragma unroll
+                    for (int rr = 0; rr < 16; ++rr) sTf[(b0 + rr) * 64 + b0 + jj] = t[rr];
+                }
+            }
+            solver_sync();
+            // Off-diagonal 16-blocks by block diagonal d: X_IJ = sum_{K=J}^{I-1} A_IK T_KJ, then
+            // T_IJ = -T_II X_IJ.  A thread makes four adjacent outputs (one broadcast load of A or
+            // T_II and one float4 load per k); X lives in the idle row-reduction scratch.
             float* sX = sSS;  // [(4-d) blocks][16][16], 768 floats over sSS + sRed
 #pragma unroll 1
             for (int d = 1; d < 4; ++d) {
-                const int nq = (4 - d) * 64;  // quads of outputs
+                const int nq = (4 - d) * 64;  // quads of outputs (at most 32 * kSolveWarps)
                 if (tid < nq) {
                     const int J = tid >> 6, I = J + d, rr = (tid >> 2) & 15, jq = tid & 3;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -603,7 +616,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                         }
                     *reinterpret_cast<float4*>(&sX[(J * 16 + rr) * 16 + 4 * jq]) = acc;
                 }
-                __syncthreads();
+                solver_sync();
                 if (tid < nq) {
                     const int J = tid >> 6, I = J + d, rr = (tid >> 2) & 15, jq = tid & 3;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -618,26 +631,26 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                     *reinterpret_cast<float4*>(&sTf[(16 * I + rr) * 64 + 16 * J + 4 * jq]) =
                         make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
                 }
-                __syncthreads();
+                solver_sync();
             }
-        }
-        // T -> bf16, K-major [r][i]; the upper triangle is zero
-        for (int idx = tid; idx < 64 * 8; idx += kThreads) {
-            const int rr = idx >> 3, k8 = idx & 7;
-            float t8[8];
+            // T -> bf16, K-major [r][i]; the upper triangle is zero
+            for (int idx = tid; idx < 64 * 8; idx += 32 * kSolveWarps) {
+                const int rr = idx >> 3, k8 = idx & 7;
+                float t8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int i = 8 * k8 + e;
-                t8[e] = i <= rr ? sTf[rr * 64 + i] : 0.f;
+                for (int e = 0; e < 8; ++e) {
+                    const int i = 8 * k8 + e;
+                    t8[e] = i <= rr ? sTf[rr * 64 + i] : 0.f;
+                }
+                uint4 hv;
+                hv.x = pack_bf16x2(t8[0], t8[1]);
+                hv.y = pack_bf16x2(t8[2], t8[3]);
+                hv.z = pack_bf16x2(t8[4], t8[5]);
+                hv.w = pack_bf16x2(t8[6], t8[7]);
+                sts128(sTbf, kmajor_off(64, rr, k8), hv);
             }
-            uint4 hv;
-            hv.x = pack_bf16x2(t8[0], t8[1]);
-            hv.y = pack_bf16x2(t8[2], t8[3]);
-            hv.z = pack_bf16x2(t8[4], t8[5]);
-            hv.w = pack_bf16x2(t8[6], t8[7]);
-            sts128(sTbf, kmajor_off(64, rr, k8), hv);
+            fence_async_smem();
         }
-        fence_async_smem();
 
         // ------------------------------------------------ D: v conv, R = beta (V - P)
         cp_async_wait_all();
