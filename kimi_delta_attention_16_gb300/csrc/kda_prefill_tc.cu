@@ -141,6 +141,16 @@ __device__ __forceinline__ void split8(const float v[8], uint4& hi, uint4& lo) {
     split2(v[6], v[7], hi.w, lo.w);
 }
 
+// Waits for an MMA group's mbarrier and synchronises the CTA; true if the wait timed out.
+// Only the polling warp (the one that issued the group) spins on the mbarrier: every warp
+// spinning floods the shared-memory pipe the issuing thread needs.  The others sleep in the
+// barrier, which also carries the outcome to every thread.
+__device__ __forceinline__ bool wait_mma(uint64_t* bar, uint32_t parity, bool poller) {
+    bool ok = true;
+    if (poller) ok = mbar_wait(bar, parity);
+    return __syncthreads_or(!ok) != 0;
+}
+
 // The triangular solve runs on warps 0..kSolveWarps-1 with their own named barrier (1);
 // barrier 0 is __syncthreads.
 constexpr int kSolveWarps = 6;
@@ -382,7 +392,9 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             const float* cA = sConst + (hr ? cA1 : cA0) * kD;
             const float* cE = sConst + (hr ? cE1 : cE0) * kD;
             const float bt = sBeta[r];
-            uint32_t xhi[16], xlo[16];
+            // X1 row: each 8-channel group goes to TMEM as soon as it is formed (columns
+            // kColX + 16 qt + 4 g8 hi, + 64 lo), so the 64 KB of operand stores drain while the
+            // other tiles are built instead of in front of the G1 issue
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
                 const int cc = c0 + 8 * g8;
@@ -413,8 +425,8 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
 #pragma unroll
                     for (int e = 0; e < 8; ++e) t8[e] = xv[e] * uu[e];
                     split8(t8, hi, lo);
-                    xhi[4 * g8 + 0] = hi.x; xhi[4 * g8 + 1] = hi.y; xhi[4 * g8 + 2] = hi.z; xhi[4 * g8 + 3] = hi.w;
-                    xlo[4 * g8 + 0] = lo.x; xlo[4 * g8 + 1] = lo.y; xlo[4 * g8 + 2] = lo.z; xlo[4 * g8 + 3] = lo.w;
+                    tmem_st4(tb + lane_off + kColX + 16 * qt + 4 * g8, hi);
+                    tmem_st4(tb + lane_off + kColX + 64 + 16 * qt + 4 * g8, lo);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) t8[e] = xv[e] * uu[e] * EE[e];
                     split8(t8, hi, lo);
@@ -428,8 +440,8 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
 #pragma unroll
                     for (int e = 0; e < 8; ++e) t8[e] = bt * xv[e] * uu[e];
                     split8(t8, hi, lo);
-                    xhi[4 * g8 + 0] = hi.x; xhi[4 * g8 + 1] = hi.y; xhi[4 * g8 + 2] = hi.z; xhi[4 * g8 + 3] = hi.w;
-                    xlo[4 * g8 + 0] = lo.x; xlo[4 * g8 + 1] = lo.y; xlo[4 * g8 + 2] = lo.z; xlo[4 * g8 + 3] = lo.w;
+                    tmem_st4(tb + lane_off + kColX + 16 * qt + 4 * g8, hi);
+                    tmem_st4(tb + lane_off + kColX + 64 + 16 * qt + 4 * g8, lo);
                     // B1 row r: k v (anchor of r's own half)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) t8[e] = xv[e] * vv[e];
@@ -473,9 +485,6 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                     sts128(sm, kOffKTlo + mnmajor_off(kKtLbo, kKtSbo, cc / 8, r), lo);
                 }
             }
-            // X1 row, 32 channels -> TMEM lane L (hi columns 128 + 16qt .., lo + 64)
-            tmem_st16(tb + lane_off + kColX + 16 * qt, xhi);
-            tmem_st16(tb + lane_off + kColX + 64 + 16 * qt, xlo);
             tmem_st_wait();
         }
         fence_async_smem();
@@ -502,7 +511,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         }
 
         // ------------------------------------------------ C: M and A from G1, T = (I + A)^-1
-        failed = !__syncthreads_and(mbar_wait(&bars[0], par));
+        failed = wait_mma(&bars[0], par, warp == 0);
         if (failed) break;
         fence_after_sync();
         {
@@ -654,7 +663,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
 
         // ------------------------------------------------ D: v conv, R = beta (V - P)
         cp_async_wait_all();
-        failed = !__syncthreads_and(mbar_wait(&bars[1], par));
+        failed = wait_mma(&bars[1], par, warp == kThreads / 32 - 1);
         if (failed) break;
         fence_after_sync();
         {
@@ -712,7 +721,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                            id_64, (term | kk) != 0);
             mma_commit(&bars[2]);
         }
-        failed = !__syncthreads_and(mbar_wait(&bars[2], par));
+        failed = wait_mma(&bars[2], par, warp == 0);
         if (failed) break;
         fence_after_sync();
 
@@ -757,7 +766,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             mma_commit(&bars[3]);
         }
         if (ci + 1 < ce) compute_G(ci + 1);  // overlaps G5/G6; the A/T tile in R1 is dead
-        failed = !__syncthreads_and(mbar_wait(&bars[3], par));
+        failed = wait_mma(&bars[3], par, warp == 0);
         if (failed) break;
         fence_after_sync();
 
