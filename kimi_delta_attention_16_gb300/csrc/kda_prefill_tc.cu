@@ -111,21 +111,9 @@ constexpr uint32_t kSmemBytes = kOffMisc + kMiscFloats * 4 + 1024;  // + alignme
 enum { cA0 = 0, cA1, cE0, cE1, cC2, cC3, cKt0, cKt1, cGam };
 
 __device__ __forceinline__ float ex(float x) { return __expf(x); }
-// SiLU and sigmoid from one hardware tanh (one MUFU operation instead of an exponential
-// and a reciprocal): sigmoid(x) = 1/2 + tanh(x/2)/2, silu(x) = x sigmoid(x).  tanh.approx
-// has an absolute error of about 5e-4, so sigmoid is within ~2.5e-4 absolute and silu within
-// ~2.5e-4 |x|; after the L2 norm of q and k and the RMSNorm of o that stays well inside this
-// path's tolerances (the fp32 SIMT path keeps the IEEE functions).
-__device__ __forceinline__ float tanh_hw(float x) {
-    float y;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float silu_fast(float x) {
-    const float hx = 0.5f * x;
-    return fmaf(hx, tanh_hw(hx), hx);
-}
-__device__ __forceinline__ float sigmoid_fast(float x) { return fmaf(0.5f, tanh_hw(0.5f * x), 0.5f); }
+// SiLU and sigmoid: one hardware tanh each (silu_tanh / sigmoid_tanh, bf16-input paths).
+__device__ __forceinline__ float silu_fast(float x) { return silu_tanh(x); }
+__device__ __forceinline__ float sigmoid_fast(float x) { return sigmoid_tanh(x); }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");

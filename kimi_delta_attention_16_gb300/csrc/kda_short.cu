@@ -30,6 +30,18 @@ namespace {
 constexpr int kD = 128;
 constexpr int kShortThreads = 256;
 
+// Activations and decay factors: bf16 inputs take the one-MUFU tanh forms and the fast
+// exponential (tolerance 2e-3), fp32 inputs the IEEE functions (tolerance 1e-5).
+template <typename Tio> __device__ __forceinline__ float act_silu(float x) {
+    if constexpr (sizeof(Tio) == 2) return silu_tanh(x); else return siluf_(x);
+}
+template <typename Tio> __device__ __forceinline__ float act_sigmoid(float x) {
+    if constexpr (sizeof(Tio) == 2) return sigmoid_tanh(x); else return sigmoidf_(x);
+}
+template <typename Tio> __device__ __forceinline__ float decay_exp(float g) {
+    if constexpr (sizeof(Tio) == 2) return __expf(g); else return expf(g);
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
@@ -141,7 +153,7 @@ k_prefill_short(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio*
         for (int idx = tid; idx < L * kD; idx += kShortThreads) {
             const int tau = idx >> 7, d = idx & (kD - 1);
             const int64_t row = ((a + tau) * H + h) * kD + d;
-            salpha[tau][d] = expf(g[row]);
+            salpha[tau][d] = decay_exp<Tio>(g[row]);
             sgate[tau][d] = gate ? to_f(gate[row]) : 0.f;
         }
         if (tid < L) sbeta[tid] = beta[(a + tid) * H + h];
@@ -165,7 +177,7 @@ k_prefill_short(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio*
                 x[m] = rel >= 0 ? sraw[rel * 3 * kD + ch]
                                 : (cs_in ? to_f(cs_in[(((int64_t)n * 3 + part) * HD + (int64_t)h * kD + d) * 3 + 3 + rel]) : 0.f);
             }
-            sx[tau][part][d] = siluf_(w.x * x[0] + w.y * x[1] + w.z * x[2] + w.w * x[3]);
+            sx[tau][part][d] = act_silu<Tio>(w.x * x[0] + w.y * x[1] + w.z * x[2] + w.w * x[3]);
         }
         __syncthreads();  // B
         // L2 norms: warp w takes (token, q or k) pairs w, w + 8, ...
@@ -197,7 +209,7 @@ k_prefill_short(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio*
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 float y = o[m] * inv * sRms[c0 + m];
-                if (gate) y *= sigmoidf_(sgate[tau][c0 + m]);
+                if (gate) y *= act_sigmoid<Tio>(sgate[tau][c0 + m]);
                 out[row + m] = from_f<To>(y);
             }
         };
@@ -425,9 +437,9 @@ k_prefill_short_pipe(const Tio* __restrict__ q, const Tio* __restrict__ k, const
                 const int rel = tau - 3 + m;
                 x[m] = rel >= 0 ? to_f(rows[(rel * 4 + part) * kD + d]) : (cs_in ? to_f(cst[ch * 3 + 3 + rel]) : 0.f);
             }
-            sx[tau][part][d] = siluf_(w.x * x[0] + w.y * x[1] + w.z * x[2] + w.w * x[3]);
+            sx[tau][part][d] = act_silu<Tio>(w.x * x[0] + w.y * x[1] + w.z * x[2] + w.w * x[3]);
         }
-        for (int idx = tid; idx < L * kD; idx += kPipeThreads) salpha[idx >> 7][idx & (kD - 1)] = expf(grow[idx]);
+        for (int idx = tid; idx < L * kD; idx += kPipeThreads) salpha[idx >> 7][idx & (kD - 1)] = decay_exp<Tio>(grow[idx]);
         float s[32];
         {
             const float* Ss = reinterpret_cast<const float*>(st + St::kState);
@@ -467,7 +479,7 @@ k_prefill_short_pipe(const Tio* __restrict__ q, const Tio* __restrict__ k, const
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 float y = o[m] * inv * sRms[c4 + m];
-                if (gate) y *= sigmoidf_(to_f(rows[(tau * 4 + 3) * kD + c4 + m]));
+                if (gate) y *= act_sigmoid<Tio>(to_f(rows[(tau * 4 + 3) * kD + c4 + m]));
                 out[row + m] = from_f<To>(y);
             }
         };
