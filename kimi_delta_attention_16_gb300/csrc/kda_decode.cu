@@ -289,7 +289,7 @@ k_decode_tma(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __
             c3[0] = c3[1];
             c3[1] = c3[2];
             c3[2] = xn;
-            sx[part][d] = siluf_(uu);
+            sx[part][d] = act_silu<Tio>(uu);
         }
         __syncthreads();
         if (warp < 2) {
@@ -309,7 +309,7 @@ k_decode_tma(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
             s[e] = *reinterpret_cast<const float4*>(S + (r0 + e) * D + c0);
-            const float a = expf(gr[r0 + e]);
+            const float a = decay_exp<Tio>(gr[r0 + e]);
             kr[e] = sx[1][r0 + e] * ik;
             qr[e] = sx[0][r0 + e] * iq;
             s[e].x *= a; s[e].y *= a; s[e].z *= a; s[e].w *= a;
@@ -375,7 +375,7 @@ k_decode_tma(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __
             for (int m = 0; m < 4; ++m) {
                 float y = o[m] * inv;
                 y *= sRms[c0 + m];
-                if (gt) y *= sigmoidf_(to_f(gt[m]));
+                if (gt) y *= act_sigmoid<Tio>(to_f(gt[m]));
                 dst[m] = from_f<To>(y);
             }
         }

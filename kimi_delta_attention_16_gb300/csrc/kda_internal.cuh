@@ -34,6 +34,18 @@ __device__ __forceinline__ float silu_tanh(float x) {
 }
 __device__ __forceinline__ float sigmoid_tanh(float x) { return fmaf(0.5f, tanh_hw(0.5f * x), 0.5f); }
 
+// Activations and decay factors by input dtype: bf16 inputs take the one-MUFU tanh forms and
+// the fast exponential (tolerance 2e-3), fp32 inputs the IEEE functions (tolerance 1e-5).
+template <typename Tio> __device__ __forceinline__ float act_silu(float x) {
+    if constexpr (sizeof(Tio) == 2) return silu_tanh(x); else return siluf_(x);
+}
+template <typename Tio> __device__ __forceinline__ float act_sigmoid(float x) {
+    if constexpr (sizeof(Tio) == 2) return sigmoid_tanh(x); else return sigmoidf_(x);
+}
+template <typename Tio> __device__ __forceinline__ float decay_exp(float g) {
+    if constexpr (sizeof(Tio) == 2) return __expf(g); else return expf(g);
+}
+
 // ------------------------------------------------------------------ scalar I/O
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }

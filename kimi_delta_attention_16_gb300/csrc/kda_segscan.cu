@@ -375,7 +375,7 @@ k_seg_fixup(SegPlan sp, const int32_t* __restrict__ cu, int64_t T_total, int H,
         for (int e = 0; e < 32; ++e) {
             if (e < nvalid) {
                 float y = o[e] * sInv[32 * qt + e] * wj;
-                if (gate) y *= __fdividef(1.0f, 1.0f + __expf(-to_f(gt[e * kD])));
+                if (gate) y *= sigmoid_tanh(to_f(gt[e * kD]));
                 yp[e * rstride] = from_f<To>(y);
             }
         }

@@ -30,17 +30,6 @@ namespace {
 constexpr int kD = 128;
 constexpr int kShortThreads = 256;
 
-// Activations and decay factors: bf16 inputs take the one-MUFU tanh forms and the fast
-// exponential (tolerance 2e-3), fp32 inputs the IEEE functions (tolerance 1e-5).
-template <typename Tio> __device__ __forceinline__ float act_silu(float x) {
-    if constexpr (sizeof(Tio) == 2) return silu_tanh(x); else return siluf_(x);
-}
-template <typename Tio> __device__ __forceinline__ float act_sigmoid(float x) {
-    if constexpr (sizeof(Tio) == 2) return sigmoid_tanh(x); else return sigmoidf_(x);
-}
-template <typename Tio> __device__ __forceinline__ float decay_exp(float g) {
-    if constexpr (sizeof(Tio) == 2) return __expf(g); else return expf(g);
-}
 
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
