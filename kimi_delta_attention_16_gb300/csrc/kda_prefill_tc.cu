@@ -153,6 +153,10 @@ __device__ __forceinline__ bool wait_mma(uint64_t* bar, uint32_t parity, bool po
 // The triangular solve runs on warps 0..kSolveWarps-1 with their own named barrier (1);
 // barrier 0 is __syncthreads.
 constexpr int kSolveWarps = 6;
+// Barrier of warps kSolveWarps..15 (named barrier 2), the warps that form R meanwhile.
+__device__ __forceinline__ void d_sync() {
+    asm volatile("bar.sync 2, %0;" ::"n"(kThreads - 32 * kSolveWarps) : "memory");
+}
 __device__ __forceinline__ void solver_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kSolveWarps) : "memory"); }
 
 __device__ __forceinline__ void sts128(uint8_t* base, uint32_t off, const uint4& v) {
@@ -171,6 +175,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bars[4];  // G1 done, G3 done, G4 done, G5+G6 done
     __shared__ uint32_t s_tbase;
+    __shared__ int s_dfail;  // set by the warp that waits for G3
 
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -217,6 +222,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     if (tid == 0) {
         for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
+        s_dfail = 0;
     }
     for (int idx = tid; idx < 3 * kD * 4; idx += kThreads) {
         const int part = idx / (kD * 4), rem = idx % (kD * 4);
@@ -566,8 +572,9 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 for (int e = 0; e < 16; ++e) sAf[r * kAs + 16 * qt + e] = row[e];
             }
         }
+        cp_async_wait_all();  // this thread's v and gate rows (issued at the start of C)
         fence_before_sync();
-        __syncthreads();
+        __syncthreads();      // A, the M tiles and the v / gate rows are complete
         // G3: [P ; Q'] = S^T . [KG ; QG]^T (state reads), from warp 15 while warps 0-5 solve
         if (tid == kThreads - 32) {
             fence_after_sync();
@@ -660,52 +667,67 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             fence_async_smem();
         }
 
-        // ------------------------------------------------ D: v conv, R = beta (V - P)
-        cp_async_wait_all();
-        failed = wait_mma(&bars[1], par, warp == kThreads / 32 - 1);
-        if (failed) break;
-        fence_after_sync();
-        {
-            // thread (lane j, quarter qt): tokens i in [16qt, 16qt + 16)
-            const int i0 = 16 * qt;
-            const float4 w = *reinterpret_cast<const float4*>(&sConvW[(2 * kD + j) * 4]);
-            const bf16* vt = reinterpret_cast<const bf16*>(sm + kOffRawV);
-            auto raw = [&](int64_t p) -> float {
-                if (p >= s0) return to_f(vt[(uint32_t)(p - (t0 - 3)) * (kRawStride / 2) + j]);
-                const int pos = (int)(p - s0);
-                return cs_in ? to_f(cs_in[((int64_t)n * 3 * HD + 2 * HD + (int64_t)h * kD + j) * 3 + 3 + pos]) : 0.f;
-            };
-            const int64_t tb0 = t0 + i0;
-            const bool vrows = i0 < Lc && !ident_run;  // the identity-start run takes v = 0
-            float p0 = vrows ? raw(tb0 - 3) : 0.f;
-            float p1 = vrows ? raw(tb0 - 2) : 0.f;
-            float p2 = vrows ? raw(tb0 - 1) : 0.f;
-            uint32_t pv[16];
-            tmem_ld16(tb + lane_off + kColP + i0, pv);
-            tmem_ld_wait();
-            uint32_t rhi[8], rlo[8];
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-                float rv[2];
-#pragma unroll
-                for (int f = 0; f < 2; ++f) {
-                    const int i = i0 + e + f;
-                    float xr = 0.f, vr = 0.f;
-                    if (i < Lc && !ident_run) {
-                        xr = to_f(vt[(uint32_t)(i + 3) * (kRawStride / 2) + j]);
-                        vr = silu_fast(w.x * p0 + w.y * p1 + w.z * p2 + w.w * xr);
-                    }
-                    p0 = p1; p1 = p2; p2 = xr;
-                    rv[f] = sBeta[i] * (vr - __uint_as_float(pv[e + f]));
-                }
-                split2(rv[0], rv[1], rhi[e / 2], rlo[e / 2]);
+        // ------------------------------------------------ D: v conv, R = beta (V - P), by warps 6-15
+        // while warps 0-5 solve: D needs P from G3, not T.  Warp 15 (G3's issuer) waits for G3;
+        // a named barrier of the ten D warps passes that on.  Each warp forms R for its
+        // quadrant's lanes and one or two 16-token blocks (quadrants 0 and 1 have two D warps,
+        // quadrants 2 and 3 three).
+        if (warp >= kSolveWarps) {
+            bool ok = true;
+            if (warp == kThreads / 32 - 1) {
+                ok = mbar_wait(&bars[1], par);
+                if (lane == 0) s_dfail = ok ? 0 : 1;
             }
-            tmem_st8(tb + lane_off + kColR + 8 * qt, rhi);
-            tmem_st8(tb + lane_off + kColR + 32 + 8 * qt, rlo);
-            tmem_st_wait();
+            d_sync();
+            fence_after_sync();
+            if (s_dfail == 0) {
+                const int slot = (warp - kSolveWarps) >> 2;  // 0, 1 (quadrants 0, 1) or 0, 1, 2
+                int blk0, nblk;
+                if (qd < 2) { blk0 = 2 * slot; nblk = 2; }  // warps 8, 9 -> blocks 0-1; 12, 13 -> 2-3
+                else { blk0 = slot == 0 ? 0 : slot + 1; nblk = slot == 0 ? 2 : 1; }  // 6, 7 -> 0-1; 10, 11 -> 2; 14, 15 -> 3
+                const float4 w = *reinterpret_cast<const float4*>(&sConvW[(2 * kD + j) * 4]);
+                const bf16* vt = reinterpret_cast<const bf16*>(sm + kOffRawV);
+                auto raw = [&](int64_t p) -> float {
+                    if (p >= s0) return to_f(vt[(uint32_t)(p - (t0 - 3)) * (kRawStride / 2) + j]);
+                    const int pos = (int)(p - s0);
+                    return cs_in ? to_f(cs_in[((int64_t)n * 3 * HD + 2 * HD + (int64_t)h * kD + j) * 3 + 3 + pos]) : 0.f;
+                };
+                for (int bi = 0; bi < nblk; ++bi) {
+                    const int tbk = blk0 + bi, i0 = 16 * tbk;  // tokens i in [i0, i0 + 16)
+                    const int64_t tb0 = t0 + i0;
+                    const bool vrows = i0 < Lc && !ident_run;  // the identity-start run takes v = 0
+                    float p0 = vrows ? raw(tb0 - 3) : 0.f;
+                    float p1 = vrows ? raw(tb0 - 2) : 0.f;
+                    float p2 = vrows ? raw(tb0 - 1) : 0.f;
+                    uint32_t pv[16];
+                    tmem_ld16(tb + lane_off + kColP + i0, pv);
+                    tmem_ld_wait();
+                    uint32_t rhi[8], rlo[8];
+#pragma unroll
+                    for (int e = 0; e < 16; e += 2) {
+                        float rv[2];
+#pragma unroll
+                        for (int f = 0; f < 2; ++f) {
+                            const int i = i0 + e + f;
+                            float xr = 0.f, vr = 0.f;
+                            if (i < Lc && !ident_run) {
+                                xr = to_f(vt[(uint32_t)(i + 3) * (kRawStride / 2) + j]);
+                                vr = silu_fast(w.x * p0 + w.y * p1 + w.z * p2 + w.w * xr);
+                            }
+                            p0 = p1; p1 = p2; p2 = xr;
+                            rv[f] = sBeta[i] * (vr - __uint_as_float(pv[e + f]));
+                        }
+                        split2(rv[0], rv[1], rhi[e / 2], rlo[e / 2]);
+                    }
+                    tmem_st8(tb + lane_off + kColR + 8 * tbk, rhi);
+                    tmem_st8(tb + lane_off + kColR + 32 + 8 * tbk, rlo);
+                }
+                tmem_st_wait();
+            }
         }
         fence_before_sync();
-        __syncthreads();
+        failed = __syncthreads_or(s_dfail != 0) != 0;  // T (warps 0-5) and R (warps 6-15) complete
+        if (failed) break;
 
         // ------------------------------------------------ E: G4  W^T = R^T T^T; next chunk's q/k rows -> B3
         if (ci + 1 < ce) stage_qk(ci + 1);  // G3 finished with B3 (waited in D)
