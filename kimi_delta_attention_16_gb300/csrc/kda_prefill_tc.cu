@@ -157,6 +157,8 @@ constexpr int kSolveWarps = 6;
 __device__ __forceinline__ void d_sync() {
     asm volatile("bar.sync 2, %0;" ::"n"(kThreads - 32 * kSolveWarps) : "memory");
 }
+// Barrier of warps 0-3 only (named barrier 3): the last two levels of the solve.
+__device__ __forceinline__ void solver4_sync() { asm volatile("bar.sync 3, 128;" ::: "memory"); }
 __device__ __forceinline__ void solver_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kSolveWarps) : "memory"); }
 
 __device__ __forceinline__ void sts128(uint8_t* base, uint32_t off, const uint4& v) {
@@ -175,7 +177,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t bars[4];  // G1 done, G3 done, G4 done, G5+G6 done
     __shared__ uint32_t s_tbase;
-    __shared__ int s_dfail;  // set by the warp that waits for G3
+    __shared__ int s_dfail;  // set by warp 15 when it has waited for G3
 
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -591,9 +593,47 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             }
             mma_commit(&bars[1]);
         }
-        // T: unit lower triangular inverse, by warps 0-5 (their own named barrier: the other
-        // warps go on to D, and warp 15 issues G3 meanwhile).  Diagonal 16x16 blocks: one warp
-        // per block, lane jj (lanes 16..31 mirror 0..15) keeps column jj of the block in registers.
+        // T: unit lower triangular inverse, on named barriers of its own while the other warps
+        // form R (D) and warp 15 issues G3: warps 0-5 for the diagonal blocks and the first
+        // block level (192 quads of outputs), warps 0-3 for the other two levels (128 and 64
+        // quads) and the bf16 copy.  Diagonal 16x16 blocks: one warp per block, lane jj (lanes
+        // 16..31 mirror 0..15) keeps column jj of the block in registers.
+        float* sX = sSS;  // [(4-d) blocks][16][16] of X, 768 floats over sSS + sRed
+        // Off-diagonal 16-blocks of block diagonal d: X_IJ = sum_{K=J}^{I-1} A_IK T_KJ, then
+        // T_IJ = -T_II X_IJ.  A thread makes four adjacent outputs (one broadcast load of A or
+        // T_II and one float4 load per k).
+        auto level_x = [&](int d) {
+            const int nq = (4 - d) * 64;
+            if (tid < nq) {
+                const int J = tid >> 6, I = J + d, rr = (tid >> 2) & 15, jq = tid & 3;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int K = J; K < I; ++K)
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) {
+                        const float a = sAf[(16 * I + rr) * kAs + 16 * K + kk];
+                        const float4 t4 = *reinterpret_cast<const float4*>(&sTf[(16 * K + kk) * 64 + 16 * J + 4 * jq]);
+                        acc.x += a * t4.x; acc.y += a * t4.y; acc.z += a * t4.z; acc.w += a * t4.w;
+                    }
+                *reinterpret_cast<float4*>(&sX[(J * 16 + rr) * 16 + 4 * jq]) = acc;
+            }
+        };
+        auto level_t = [&](int d) {
+            const int nq = (4 - d) * 64;
+            if (tid < nq) {
+                const int J = tid >> 6, I = J + d, rr = (tid >> 2) & 15, jq = tid & 3;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int kk = 0; kk < 16; ++kk) {
+                    if (kk <= rr) {
+                        const float t = sTf[(16 * I + rr) * 64 + 16 * I + kk];
+                        const float4 x4 = *reinterpret_cast<const float4*>(&sX[(J * 16 + kk) * 16 + 4 * jq]);
+                        acc.x += t * x4.x; acc.y += t * x4.y; acc.z += t * x4.z; acc.w += t * x4.w;
+                    }
+                }
+                *reinterpret_cast<float4*>(&sTf[(16 * I + rr) * 64 + 16 * J + 4 * jq]) =
+                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            }
+        };
         if (warp < kSolveWarps) {
             if (warp < 4) {
                 const int b0 = 16 * warp, jj = lane & 15;
@@ -612,44 +652,22 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 }
             }
             solver_sync();
-            // Off-diagonal 16-blocks by block diagonal d: X_IJ = sum_{K=J}^{I-1} A_IK T_KJ, then
-            // T_IJ = -T_II X_IJ.  A thread makes four adjacent outputs (one broadcast load of A or
-            // T_II and one float4 load per k); X lives in the idle row-reduction scratch.
-            float* sX = sSS;  // [(4-d) blocks][16][16], 768 floats over sSS + sRed
-#pragma unroll 1
-            for (int d = 1; d < 4; ++d) {
-                const int nq = (4 - d) * 64;  // quads of outputs (at most 32 * kSolveWarps)
-                if (tid < nq) {
-                    const int J = tid >> 6, I = J + d, rr = (tid >> 2) & 15, jq = tid & 3;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int K = J; K < I; ++K)
-#pragma unroll
-                        for (int kk = 0; kk < 16; ++kk) {
-                            const float a = sAf[(16 * I + rr) * kAs + 16 * K + kk];
-                            const float4 t4 = *reinterpret_cast<const float4*>(&sTf[(16 * K + kk) * 64 + 16 * J + 4 * jq]);
-                            acc.x += a * t4.x; acc.y += a * t4.y; acc.z += a * t4.z; acc.w += a * t4.w;
-                        }
-                    *reinterpret_cast<float4*>(&sX[(J * 16 + rr) * 16 + 4 * jq]) = acc;
-                }
-                solver_sync();
-                if (tid < nq) {
-                    const int J = tid >> 6, I = J + d, rr = (tid >> 2) & 15, jq = tid & 3;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) {
-                        if (kk <= rr) {
-                            const float t = sTf[(16 * I + rr) * 64 + 16 * I + kk];
-                            const float4 x4 = *reinterpret_cast<const float4*>(&sX[(J * 16 + kk) * 16 + 4 * jq]);
-                            acc.x += t * x4.x; acc.y += t * x4.y; acc.z += t * x4.z; acc.w += t * x4.w;
-                        }
-                    }
-                    *reinterpret_cast<float4*>(&sTf[(16 * I + rr) * 64 + 16 * J + 4 * jq]) =
-                        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-                }
-                solver_sync();
-            }
+            level_x(1);
+            solver_sync();
+            level_t(1);
+            solver_sync();
+        }
+        if (warp < 4) {
+            level_x(2);
+            solver4_sync();
+            level_t(2);
+            solver4_sync();
+            level_x(3);
+            solver4_sync();
+            level_t(3);
+            solver4_sync();
             // T -> bf16, K-major [r][i]; the upper triangle is zero
-            for (int idx = tid; idx < 64 * 8; idx += 32 * kSolveWarps) {
+            for (int idx = tid; idx < 64 * 8; idx += 128) {
                 const int rr = idx >> 3, k8 = idx & 7;
                 float t8[8];
 #pragma unroll
@@ -667,24 +685,28 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             fence_async_smem();
         }
 
-        // ------------------------------------------------ D: v conv, R = beta (V - P), by warps 6-15
-        // while warps 0-5 solve: D needs P from G3, not T.  Warp 15 (G3's issuer) waits for G3;
-        // a named barrier of the ten D warps passes that on.  Each warp forms R for its
-        // quadrant's lanes and one or two 16-token blocks (quadrants 0 and 1 have two D warps,
-        // quadrants 2 and 3 three).
-        if (warp >= kSolveWarps) {
-            bool ok = true;
-            if (warp == kThreads / 32 - 1) {
-                ok = mbar_wait(&bars[1], par);
-                if (lane == 0) s_dfail = ok ? 0 : 1;
+        // ------------------------------------------------ D: v conv, R = beta (V - P), by warps 4-15
+        // while warps 0-3 finish T: D needs P from G3, not T.  Warp 15 (G3's issuer) waits for G3
+        // and a named barrier of warps 6-15 passes that on; warps 4 and 5 join after the first
+        // solve level and wait for G3 themselves.  Each quadrant's 64 tokens are 8 half-blocks
+        // of 8, shared by its three D warps as 3 + 3 + 2 (the late warps 4, 5 and G3's issuer 15
+        // take two).
+        bool dfail = false;
+        if (warp >= 4) {
+            if (warp >= kSolveWarps) {
+                if (warp == kThreads / 32 - 1) {
+                    const bool ok = mbar_wait(&bars[1], par);
+                    if (lane == 0) s_dfail = ok ? 0 : 1;
+                }
+                d_sync();
+                dfail = s_dfail != 0;
+            } else {
+                dfail = !mbar_wait(&bars[1], par);
             }
-            d_sync();
             fence_after_sync();
-            if (s_dfail == 0) {
-                const int slot = (warp - kSolveWarps) >> 2;  // 0, 1 (quadrants 0, 1) or 0, 1, 2
-                int blk0, nblk;
-                if (qd < 2) { blk0 = 2 * slot; nblk = 2; }  // warps 8, 9 -> blocks 0-1; 12, 13 -> 2-3
-                else { blk0 = slot == 0 ? 0 : slot + 1; nblk = slot == 0 ? 2 : 1; }  // 6, 7 -> 0-1; 10, 11 -> 2; 14, 15 -> 3
+            if (!dfail) {
+                const int rank = warp < kSolveWarps ? 2 : (warp - kSolveWarps) >> 2;
+                const int hb0 = 3 * rank, nhb = rank < 2 ? 3 : 2;
                 const float4 w = *reinterpret_cast<const float4*>(&sConvW[(2 * kD + j) * 4]);
                 const bf16* vt = reinterpret_cast<const bf16*>(sm + kOffRawV);
                 auto raw = [&](int64_t p) -> float {
@@ -692,19 +714,21 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                     const int pos = (int)(p - s0);
                     return cs_in ? to_f(cs_in[((int64_t)n * 3 * HD + 2 * HD + (int64_t)h * kD + j) * 3 + 3 + pos]) : 0.f;
                 };
-                for (int bi = 0; bi < nblk; ++bi) {
-                    const int tbk = blk0 + bi, i0 = 16 * tbk;  // tokens i in [i0, i0 + 16)
+                for (int hb = hb0; hb < hb0 + nhb; ++hb) {
+                    const int i0 = 8 * hb;  // tokens i in [i0, i0 + 8)
                     const int64_t tb0 = t0 + i0;
                     const bool vrows = i0 < Lc && !ident_run;  // the identity-start run takes v = 0
                     float p0 = vrows ? raw(tb0 - 3) : 0.f;
                     float p1 = vrows ? raw(tb0 - 2) : 0.f;
                     float p2 = vrows ? raw(tb0 - 1) : 0.f;
-                    uint32_t pv[16];
-                    tmem_ld16(tb + lane_off + kColP + i0, pv);
+                    uint32_t pv[8];
+                    tmem_ld8(tb + lane_off + kColP + i0, pv);
                     tmem_ld_wait();
-                    uint32_t rhi[8], rlo[8];
+                    uint4 rhi, rlo;
+                    uint32_t* rh = &rhi.x;
+                    uint32_t* rl = &rlo.x;
 #pragma unroll
-                    for (int e = 0; e < 16; e += 2) {
+                    for (int e = 0; e < 8; e += 2) {
                         float rv[2];
 #pragma unroll
                         for (int f = 0; f < 2; ++f) {
@@ -717,16 +741,16 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                             p0 = p1; p1 = p2; p2 = xr;
                             rv[f] = sBeta[i] * (vr - __uint_as_float(pv[e + f]));
                         }
-                        split2(rv[0], rv[1], rhi[e / 2], rlo[e / 2]);
+                        split2(rv[0], rv[1], rh[e / 2], rl[e / 2]);
                     }
-                    tmem_st8(tb + lane_off + kColR + 8 * tbk, rhi);
-                    tmem_st8(tb + lane_off + kColR + 32 + 8 * tbk, rlo);
+                    tmem_st4(tb + lane_off + kColR + 4 * hb, rhi);
+                    tmem_st4(tb + lane_off + kColR + 32 + 4 * hb, rlo);
                 }
                 tmem_st_wait();
             }
         }
         fence_before_sync();
-        failed = __syncthreads_or(s_dfail != 0) != 0;  // T (warps 0-5) and R (warps 6-15) complete
+        failed = __syncthreads_or(dfail) != 0;  // T (warps 0-3) and R (warps 4-15) complete
         if (failed) break;
 
         // ------------------------------------------------ E: G4  W^T = R^T T^T; next chunk's q/k rows -> B3
