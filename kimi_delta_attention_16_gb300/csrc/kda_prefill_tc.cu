@@ -81,9 +81,9 @@ constexpr int kAs = 65;    // padded row stride of A (floats) in the triangular 
 constexpr uint32_t kOffR1 = kOffKTlo + kTileKT;   // G fp32 [64][132]  |  A fp32 [64][65] + T fp32 [64][64]
 constexpr uint32_t kR1Bytes = 64 * kGs * 4;        // 33792 >= 64*65*4 + 64*64*4
 constexpr uint32_t kOffR2 = kOffR1 + kR1Bytes;     // T bf16 [64][64] | M hi | M lo (K-major, 8 KB each)
-constexpr uint32_t kOffMisc = kOffR2 + 24576;
 constexpr int kKnS = 132;  // row stride (floats) of the normalized k rows parked in R2 during A3b
-static_assert(32 * kKnS * 4 <= 24576, "normalized k rows exceed R2");
+constexpr uint32_t kR2Bytes = 64 * kKnS * 4;       // 33792 >= 3 x 8 KB
+constexpr uint32_t kOffMisc = kOffR2 + kR2Bytes;
 // Raw-row staging in operand regions while they are not operands:
 //   B3 region, from G3's completion in chunk n-1 to A3a of chunk n: q and k rows t0-3 .. t0+63
 //   B1 region, from G1's completion to the epilogue: v rows t0-3 .. t0+63, gate rows t0 .. t0+63
@@ -108,6 +108,7 @@ constexpr int kMiscRed = kMiscSS + 512;        // [4 quadrants][64 tokens]
 constexpr int kMiscInv = kMiscRed + 256;       // [64]
 constexpr int kMiscFloats = kMiscInv + 64;
 constexpr uint32_t kSmemBytes = kOffMisc + kMiscFloats * 4 + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448 - 1024, "shared memory above the per-block limit");
 
 // per-channel constants, rows of sConst
 enum { cA0 = 0, cA1, cE0, cE1, cC2, cC3, cKt0, cKt1, cGam };
@@ -159,10 +160,11 @@ constexpr int kSolveWarps = 6;
 __device__ __forceinline__ void d_sync() {
     asm volatile("bar.sync 2, %0;" ::"n"(kThreads - 32 * kSolveWarps) : "memory");
 }
-// Pair barriers of the operand phase (named barriers 4..7, one per quarter qt): warp
-// 4 qt + 2 arrives once its normalized k rows are in shared memory, warp 4 qt waits for them.
-__device__ __forceinline__ void pair_arrive(int qt) { asm volatile("bar.arrive %0, 64;" ::"r"(4 + qt) : "memory"); }
-__device__ __forceinline__ void pair_sync(int qt) { asm volatile("bar.sync %0, 64;" ::"r"(4 + qt) : "memory"); }
+// Pair barriers of the operand phase (named barriers 4..11): in pair p = qt + 4 (qd & 1),
+// k-row warp 4 qt + 2 + (qd & 1) arrives once its normalized k rows are in shared memory and
+// q-row warp 4 qt + (qd & 1) waits for them.
+__device__ __forceinline__ void pair_arrive(int p) { asm volatile("bar.arrive %0, 64;" ::"r"(4 + p) : "memory"); }
+__device__ __forceinline__ void pair_sync(int p) { asm volatile("bar.sync %0, 64;" ::"r"(4 + p) : "memory"); }
 
 // Barrier of warps 0-3 only (named barrier 3): the last two levels of the solve.
 __device__ __forceinline__ void solver4_sync() { asm volatile("bar.sync 3, 128;" ::: "memory"); }
@@ -406,19 +408,20 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             const float* cA = sConst + (hr ? cA1 : cA0) * kD;
             const float* cE = sConst + (hr ? cE1 : cE0) * kD;
             const float bt = sBeta[r];
-            // Load balance: the k rows 0-31 (quadrant 2) also build B1's upper block, so their
-            // B3 rows are built by the q-row warps of quadrant 0 (same tokens, same decay
-            // factors): quadrant 2 first leaves its normalized k in R2 (free until C) and
-            // arrives on the pair's named barrier, quadrant 0 waits on it.
-            float* sKn = reinterpret_cast<float*>(sm + kOffR2);  // [32][kKnS] normalized k, rows 0-31
-            if (qd == 2) {
+            // Load balance: the k rows also build B1 and K~, so their B3 rows (k e^{G_r}) are
+            // built by the q-row warps of the same tokens, which hold the same decay factors:
+            // the k-row warp leaves its normalized k in R2 (free until C) and arrives on the
+            // pair's named barrier, the q-row warp waits on it.
+            float* sKn = reinterpret_cast<float*>(sm + kOffR2);  // [64][kKnS] normalized k rows
+            const int pair = qt + 4 * (qd & 1);  // quadrants 0 + 2 and 1 + 3, per channel quarter
+            if (!isq) {
 #pragma unroll
                 for (int g8 = 0; g8 < 8; ++g8)
                     *reinterpret_cast<float4*>(&sKn[r * kKnS + c0 + 4 * g8]) =
                         make_float4(x[4 * g8] * inv, x[4 * g8 + 1] * inv, x[4 * g8 + 2] * inv, x[4 * g8 + 3] * inv);
-                pair_arrive(qt);
-            } else if (qd == 0) {
-                pair_sync(qt);
+                pair_arrive(pair);
+            } else {
+                pair_sync(pair);
             }
             // X1 row: each 8-channel group goes to TMEM as soon as it is formed (columns
             // kColX + 16 qt + 4 g8 hi, + 64 lo), so the 64 KB of operand stores drain while the
@@ -460,8 +463,8 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                     split8(t8, hi, lo);
                     sts128(sm, kOffB3hi + kmajor_off(128, 64 + r, cc / 8), hi);
                     sts128(sm, kOffB3lo + kmajor_off(128, 64 + r, cc / 8), lo);
-                    if (qd == 0) {
-                        // KG row of k row r (B3 row r), for quadrant 2
+                    {
+                        // KG row of k row r (B3 row r), for the k-row warp of the pair
                         const float4 k0 = *reinterpret_cast<const float4*>(&sKn[r * kKnS + cc]);
                         const float4 k1 = *reinterpret_cast<const float4*>(&sKn[r * kKnS + cc + 4]);
                         const float kn[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
@@ -487,14 +490,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                     split8(t8, hi, lo);
                     sts128(sm, kOffB1hi + kmajor_off(96, r, cc / 8), hi);
                     sts128(sm, kOffB1lo + kmajor_off(96, r, cc / 8), lo);
-                    // B3 row r: k u E_h  (k e^{G_r}); rows 0-31 are built by quadrant 0
-                    if (qd == 3) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) t8[e] = xv[e] * uu[e] * EE[e];
-                        split8(t8, hi, lo);
-                        sts128(sm, kOffB3hi + kmajor_off(128, r, cc / 8), hi);
-                        sts128(sm, kOffB3lo + kmajor_off(128, r, cc / 8), lo);
-                    }
+                    // (B3 row r, k u E_h = k e^{G_r}, is built by the q-row warp of the pair)
                     auto ld8 = [&](int row, float (&d)[8]) {
                         const float4 a = *reinterpret_cast<const float4*>(&sConst[row * kD + cc]);
                         const float4 b = *reinterpret_cast<const float4*>(&sConst[row * kD + cc + 4]);
