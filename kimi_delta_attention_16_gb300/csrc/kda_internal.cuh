@@ -34,6 +34,60 @@ __device__ __forceinline__ float silu_tanh(float x) {
 }
 __device__ __forceinline__ float sigmoid_tanh(float x) { return fmaf(0.5f, tanh_hw(0.5f * x), 0.5f); }
 
+// 2^x from the hardware base-2 exponential (ex2.approx, relative error ~2^-22); callers keep
+// their log-decays in base 2 (g log2 e) so that e^g = 2^(g log2 e) needs no scaling here.
+__device__ __forceinline__ float exp2_hw(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
+
+// ------------------------------------------------------------------ packed fp32 pairs
+// Two fp32 values in one 64-bit register pair.  sm_100-class SMs execute fma/mul/add/sub
+// on .f32x2 operands as one instruction per pair, each lane rounded exactly as the scalar
+// instruction (round to nearest, no flush), which halves the issue slots of elementwise fp32
+// arithmetic in the operand-building phases.
+struct f2 {
+    uint64_t v;
+};
+__device__ __forceinline__ f2 f2_of(float a, float b) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ f2 f2_dup(float a) { return f2_of(a, a); }
+__device__ __forceinline__ float f2_lo(f2 x) {
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x.v));
+    return a;
+}
+__device__ __forceinline__ float f2_hi(f2 x) {
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x.v));
+    return b;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {  // a * b + c
+    f2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+    return r;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+    f2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+    f2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+    f2 r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+
 // Activations and decay factors by input dtype: bf16 inputs take the one-MUFU tanh forms and
 // the fast exponential (tolerance 2e-3), fp32 inputs the IEEE functions (tolerance 1e-5).
 template <typename Tio> __device__ __forceinline__ float act_silu(float x) {

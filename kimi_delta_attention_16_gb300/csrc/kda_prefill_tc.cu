@@ -113,7 +113,6 @@ static_assert(kSmemBytes <= 232448 - 1024, "shared memory above the per-block li
 // per-channel constants, rows of sConst
 enum { cA0 = 0, cA1, cE0, cE1, cC2, cC3, cKt0, cKt1, cGam };
 
-__device__ __forceinline__ float ex(float x) { return __expf(x); }
 // SiLU and sigmoid: one hardware tanh each (silu_tanh / sigmoid_tanh, bf16-input paths).
 __device__ __forceinline__ float silu_fast(float x) { return silu_tanh(x); }
 __device__ __forceinline__ float sigmoid_fast(float x) { return sigmoid_tanh(x); }
@@ -128,12 +127,13 @@ __device__ __forceinline__ void prefetch_line_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
 
-// hi/lo bf16 split of two floats, packed as bf16x2 words (first value in the low half)
-__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
-    hi = pack_bf16x2(a, b);
-    const float ah = __uint_as_float(hi << 16), bh = __uint_as_float(hi & 0xffff0000u);
-    lo = pack_bf16x2(a - ah, b - bh);
+// hi/lo bf16 split of a pair of floats, packed as bf16x2 words (first value in the low half)
+__device__ __forceinline__ void split2p(f2 v, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16x2(f2_lo(v), f2_hi(v));
+    const f2 r = sub2(v, f2_of(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u)));
+    lo = pack_bf16x2(f2_lo(r), f2_hi(r));
 }
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) { split2p(f2_of(a, b), hi, lo); }
 
 // 8 floats -> hi and lo 16-byte chunks
 __device__ __forceinline__ void split8(const float v[8], uint4& hi, uint4& lo) {
@@ -141,6 +141,21 @@ __device__ __forceinline__ void split8(const float v[8], uint4& hi, uint4& lo) {
     split2(v[2], v[3], hi.y, lo.y);
     split2(v[4], v[5], hi.z, lo.z);
     split2(v[6], v[7], hi.w, lo.w);
+}
+__device__ __forceinline__ void split8(const f2 v[4], uint4& hi, uint4& lo) {
+    split2p(v[0], hi.x, lo.x);
+    split2p(v[1], hi.y, lo.y);
+    split2p(v[2], hi.z, lo.z);
+    split2p(v[3], hi.w, lo.w);
+}
+// 8 consecutive floats of shared memory (16-byte aligned) as four pairs
+__device__ __forceinline__ void ld_f2x4(const float* p, f2 (&d)[4]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0];
+    const float4 b = reinterpret_cast<const float4*>(p)[1];
+    d[0] = f2_of(a.x, a.y);
+    d[1] = f2_of(a.z, a.w);
+    d[2] = f2_of(b.x, b.y);
+    d[3] = f2_of(b.z, b.w);
 }
 
 // Waits for an MMA group's mbarrier and synchronises the CTA; true if the wait timed out.
@@ -235,9 +250,9 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         fence_mbar_init();
         s_dfail = 0;
     }
-    for (int idx = tid; idx < 3 * kD * 4; idx += kThreads) {
-        const int part = idx / (kD * 4), rem = idx % (kD * 4);
-        sConvW[idx] = conv_w[(part * HD + (int64_t)h * kD) * 4 + rem];
+    for (int idx = tid; idx < 3 * kD * 4; idx += kThreads) {  // [part][tap][channel]
+        const int part = idx / (kD * 4), tap = (idx / kD) & 3, c = idx % kD;
+        sConvW[idx] = conv_w[(part * HD + (int64_t)h * kD + c) * 4 + tap];
     }
     fence_before_sync();
     __syncthreads();
@@ -292,7 +307,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
             const int rr = 16 * hq + e;
-            gv[e] = rr < Lcj ? g[((tc0 + rr) * H + h) * kD + c] : 0.f;
+            gv[e] = rr < Lcj ? g[((tc0 + rr) * H + h) * kD + c] * kLog2e : 0.f;  // base 2
         }
         float acc = 0.f;
 #pragma unroll
@@ -347,13 +362,13 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                         gl = sG[63 * kGs + c];
             sConst[cA0 * kD + c] = a0;
             sConst[cA1 * kD + c] = a1;
-            sConst[cE0 * kD + c] = ex(a0);
-            sConst[cE1 * kD + c] = ex(a1);
-            sConst[cC2 * kD + c] = ex(g31 - a0);
-            sConst[cC3 * kD + c] = ex(a1 - g31);
-            sConst[cKt0 * kD + c] = ex(gl - g31);
-            sConst[cKt1 * kD + c] = ex(gl - a1);
-            sConst[cGam * kD + c] = ex(gl);
+            sConst[cE0 * kD + c] = exp2_hw(a0);
+            sConst[cE1 * kD + c] = exp2_hw(a1);
+            sConst[cC2 * kD + c] = exp2_hw(g31 - a0);
+            sConst[cC3 * kD + c] = exp2_hw(a1 - g31);
+            sConst[cKt0 * kD + c] = exp2_hw(gl - g31);
+            sConst[cKt1 * kD + c] = exp2_hw(gl - a1);
+            sConst[cGam * kD + c] = exp2_hw(gl);
         }
 
         // ------------------------------------------------ A3a: conv + SiLU of one q or k row (32 channels)
@@ -365,7 +380,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         {
             const int part = isq ? 0 : 1;
             const int64_t t = t0 + r;
-            float ss = 0.f;
+            f2 ss2 = f2_dup(0.f);
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
                 const int cc = c0 + 8 * g8;
@@ -387,16 +402,29 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                             win[m][e] = cs_in ? to_f(cs_in[((int64_t)n * 3 * HD + part * HD + (int64_t)h * kD + cc + e) * 3 + 3 + pos]) : 0.f;
                     }
                 }
+                // channel pairs in packed fp32 (an invalid row has a zero window: silu(0) = 0)
+                f2 u2[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float4 w = *reinterpret_cast<const float4*>(&sConvW[(part * kD + cc + e) * 4]);
-                    const float u = w.x * win[0][e] + w.y * win[1][e] + w.z * win[2][e] + w.w * win[3][e];
-                    const float sv = rvalid ? silu_fast(u) : 0.f;
-                    x[8 * g8 + e] = sv;
-                    ss += sv * sv;
+                for (int m = 0; m < 4; ++m) {
+                    const float4 wa = *reinterpret_cast<const float4*>(&sConvW[(part * 4 + m) * kD + cc]);
+                    const float4 wb = *reinterpret_cast<const float4*>(&sConvW[(part * 4 + m) * kD + cc + 4]);
+                    const f2 w2[4] = {f2_of(wa.x, wa.y), f2_of(wa.z, wa.w), f2_of(wb.x, wb.y), f2_of(wb.z, wb.w)};
+#pragma unroll
+                    for (int pp = 0; pp < 4; ++pp) {
+                        const f2 xw = f2_of(win[m][2 * pp], win[m][2 * pp + 1]);
+                        u2[pp] = m == 0 ? mul2(w2[pp], xw) : fma2(w2[pp], xw, u2[pp]);
+                    }
+                }
+#pragma unroll
+                for (int pp = 0; pp < 4; ++pp) {  // silu(u) = h + h tanh(h), h = u / 2
+                    const f2 hx = mul2(u2[pp], f2_dup(0.5f));
+                    const f2 sv = fma2(hx, f2_of(tanh_hw(f2_lo(hx)), tanh_hw(f2_hi(hx))), hx);
+                    x[8 * g8 + 2 * pp] = f2_lo(sv);
+                    x[8 * g8 + 2 * pp + 1] = f2_hi(sv);
+                    ss2 = fma2(sv, sv, ss2);
                 }
             }
-            sSS[L * 4 + qt] = ss;
+            sSS[L * 4 + qt] = f2_lo(ss2) + f2_hi(ss2);
         }
         __syncthreads();
 
@@ -408,6 +436,15 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             const float* cA = sConst + (hr ? cA1 : cA0) * kD;
             const float* cE = sConst + (hr ? cE1 : cE0) * kD;
             const float bt = sBeta[r];
+            {  // normalize the row in place
+                const f2 inv2 = f2_dup(inv);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const f2 y = mul2(f2_of(x[2 * i], x[2 * i + 1]), inv2);
+                    x[2 * i] = f2_lo(y);
+                    x[2 * i + 1] = f2_hi(y);
+                }
+            }
             // Load balance: the k rows also build B1 and K~, so their B3 rows (k e^{G_r}) are
             // built by the q-row warps of the same tokens, which hold the same decay factors:
             // the k-row warp leaves its normalized k in R2 (free until C) and arrives on the
@@ -418,104 +455,96 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
 #pragma unroll
                 for (int g8 = 0; g8 < 8; ++g8)
                     *reinterpret_cast<float4*>(&sKn[r * kKnS + c0 + 4 * g8]) =
-                        make_float4(x[4 * g8] * inv, x[4 * g8 + 1] * inv, x[4 * g8 + 2] * inv, x[4 * g8 + 3] * inv);
+                        make_float4(x[4 * g8], x[4 * g8 + 1], x[4 * g8 + 2], x[4 * g8 + 3]);
                 pair_arrive(pair);
             } else {
                 pair_sync(pair);
             }
             // X1 row: each 8-channel group goes to TMEM as soon as it is formed (columns
             // kColX + 16 qt + 4 g8 hi, + 64 lo), so the 64 KB of operand stores drain while the
-            // other tiles are built instead of in front of the G1 issue
+            // other tiles are built instead of in front of the G1 issue.  Channel pairs in
+            // packed fp32; log-decay sums in base 2.
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
                 const int cc = c0 + 8 * g8;
-                float xv[8], uu[8], gg[8], aa[8], EE[8];
+                f2 xv[4], dg[4], uu[4], EE[4];
                 {
-                    const float4 g0 = *reinterpret_cast<const float4*>(&sG[r * kGs + cc]);
-                    const float4 g1 = *reinterpret_cast<const float4*>(&sG[r * kGs + cc + 4]);
-                    const float4 a0v = *reinterpret_cast<const float4*>(&cA[cc]);
-                    const float4 a1v = *reinterpret_cast<const float4*>(&cA[cc + 4]);
-                    const float4 e0v = *reinterpret_cast<const float4*>(&cE[cc]);
-                    const float4 e1v = *reinterpret_cast<const float4*>(&cE[cc + 4]);
-                    gg[0] = g0.x; gg[1] = g0.y; gg[2] = g0.z; gg[3] = g0.w;
-                    gg[4] = g1.x; gg[5] = g1.y; gg[6] = g1.z; gg[7] = g1.w;
-                    aa[0] = a0v.x; aa[1] = a0v.y; aa[2] = a0v.z; aa[3] = a0v.w;
-                    aa[4] = a1v.x; aa[5] = a1v.y; aa[6] = a1v.z; aa[7] = a1v.w;
-                    EE[0] = e0v.x; EE[1] = e0v.y; EE[2] = e0v.z; EE[3] = e0v.w;
-                    EE[4] = e1v.x; EE[5] = e1v.y; EE[6] = e1v.z; EE[7] = e1v.w;
-                }
+                    f2 gg[4], aa[4];
+                    ld_f2x4(&sG[r * kGs + cc], gg);
+                    ld_f2x4(&cA[cc], aa);
+                    ld_f2x4(&cE[cc], EE);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    xv[e] = x[8 * g8 + e] * inv;
-                    uu[e] = ex(gg[e] - aa[e]);
+                    for (int pp = 0; pp < 4; ++pp) {
+                        xv[pp] = f2_of(x[8 * g8 + 2 * pp], x[8 * g8 + 2 * pp + 1]);
+                        dg[pp] = sub2(gg[pp], aa[pp]);  // G_r - G_anchor
+                        uu[pp] = f2_of(exp2_hw(f2_lo(dg[pp])), exp2_hw(f2_hi(dg[pp])));
+                    }
                 }
-                float t8[8];
+                f2 t8[4];
                 uint4 hi, lo;
                 if (isq) {
-                    // X1 row: q u ; QG row (B3 row 64 + r): q u E_h
+                    // X1 row: q u ; QG row (B3 row 64 + r): q u E_h = q e^{G_r}
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) t8[e] = xv[e] * uu[e];
+                    for (int pp = 0; pp < 4; ++pp) t8[pp] = mul2(xv[pp], uu[pp]);
                     split8(t8, hi, lo);
                     tmem_st4(tb + lane_off + kColX + 16 * qt + 4 * g8, hi);
                     tmem_st4(tb + lane_off + kColX + 64 + 16 * qt + 4 * g8, lo);
+                    f2 ue[4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) t8[e] = xv[e] * uu[e] * EE[e];
+                    for (int pp = 0; pp < 4; ++pp) {
+                        ue[pp] = mul2(uu[pp], EE[pp]);
+                        t8[pp] = mul2(xv[pp], ue[pp]);
+                    }
                     split8(t8, hi, lo);
                     sts128(sm, kOffB3hi + kmajor_off(128, 64 + r, cc / 8), hi);
                     sts128(sm, kOffB3lo + kmajor_off(128, 64 + r, cc / 8), lo);
                     {
                         // KG row of k row r (B3 row r), for the k-row warp of the pair
-                        const float4 k0 = *reinterpret_cast<const float4*>(&sKn[r * kKnS + cc]);
-                        const float4 k1 = *reinterpret_cast<const float4*>(&sKn[r * kKnS + cc + 4]);
-                        const float kn[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+                        f2 kn[4];
+                        ld_f2x4(&sKn[r * kKnS + cc], kn);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) t8[e] = kn[e] * uu[e] * EE[e];
+                        for (int pp = 0; pp < 4; ++pp) t8[pp] = mul2(kn[pp], ue[pp]);
                         split8(t8, hi, lo);
                         sts128(sm, kOffB3hi + kmajor_off(128, r, cc / 8), hi);
                         sts128(sm, kOffB3lo + kmajor_off(128, r, cc / 8), lo);
                     }
                 } else {
-                    float vv[8];
+                    f2 kv[4];
+                    const f2 bt2 = f2_dup(bt);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) vv[e] = ex(aa[e] - gg[e]);
-                    // X1 row: beta k u
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) t8[e] = bt * xv[e] * uu[e];
+                    for (int pp = 0; pp < 4; ++pp) {
+                        // X1 row: beta k u ; B1 row r: k v, v = e^{G_anchor - G_r}
+                        t8[pp] = mul2(mul2(bt2, xv[pp]), uu[pp]);
+                        kv[pp] = mul2(xv[pp], f2_of(exp2_hw(-f2_lo(dg[pp])), exp2_hw(-f2_hi(dg[pp]))));
+                    }
                     split8(t8, hi, lo);
                     tmem_st4(tb + lane_off + kColX + 16 * qt + 4 * g8, hi);
                     tmem_st4(tb + lane_off + kColX + 64 + 16 * qt + 4 * g8, lo);
-                    // B1 row r: k v (anchor of r's own half)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) t8[e] = xv[e] * vv[e];
-                    split8(t8, hi, lo);
+                    split8(kv, hi, lo);
                     sts128(sm, kOffB1hi + kmajor_off(96, r, cc / 8), hi);
                     sts128(sm, kOffB1lo + kmajor_off(96, r, cc / 8), lo);
                     // (B3 row r, k u E_h = k e^{G_r}, is built by the q-row warp of the pair)
-                    auto ld8 = [&](int row, float (&d)[8]) {
-                        const float4 a = *reinterpret_cast<const float4*>(&sConst[row * kD + cc]);
-                        const float4 b = *reinterpret_cast<const float4*>(&sConst[row * kD + cc + 4]);
-                        d[0] = a.x; d[1] = a.y; d[2] = a.z; d[3] = a.w; d[4] = b.x; d[5] = b.y; d[6] = b.z; d[7] = b.w;
-                    };
+                    f2 cst[4];
                     if (r < 32) {
-                        // B1 row 64 + r: k e^{G_47 - G_r} = k (v c2) c3 ; Kt row r: k (v c2) e^{G_last - G_31}
-                        float w8[8], cst[8];
-                        ld8(cC2, cst);
+                        // B1 row 64 + r: k e^{G_47 - G_r} = k v c2 c3 ; Kt row r: k v c2 e^{G_last - G_31}
+                        f2 w8[4];
+                        ld_f2x4(&sConst[cC2 * kD + cc], cst);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) w8[e] = xv[e] * (vv[e] * cst[e]);
-                        ld8(cC3, cst);
+                        for (int pp = 0; pp < 4; ++pp) w8[pp] = mul2(kv[pp], cst[pp]);
+                        ld_f2x4(&sConst[cC3 * kD + cc], cst);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) t8[e] = w8[e] * cst[e];
+                        for (int pp = 0; pp < 4; ++pp) t8[pp] = mul2(w8[pp], cst[pp]);
                         split8(t8, hi, lo);
                         sts128(sm, kOffB1hi + kmajor_off(96, 64 + r, cc / 8), hi);
                         sts128(sm, kOffB1lo + kmajor_off(96, 64 + r, cc / 8), lo);
-                        ld8(cKt0, cst);
+                        ld_f2x4(&sConst[cKt0 * kD + cc], cst);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) t8[e] = w8[e] * cst[e];
+                        for (int pp = 0; pp < 4; ++pp) t8[pp] = mul2(w8[pp], cst[pp]);
                     } else {
-                        float cst[8];
-                        ld8(cKt1, cst);
+                        // Kt row r: k v e^{G_last - G_47}
+                        ld_f2x4(&sConst[cKt1 * kD + cc], cst);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) t8[e] = xv[e] * vv[e] * cst[e];
+                        for (int pp = 0; pp < 4; ++pp) t8[pp] = mul2(kv[pp], cst[pp]);
                     }
                     split8(t8, hi, lo);
                     sts128(sm, kOffKThi + mnmajor_off(kKtLbo, kKtSbo, cc / 8, r), hi);
@@ -737,7 +766,8 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             if (!dfail) {
                 const int rank = warp < kSolveWarps ? 2 : (warp - kSolveWarps) >> 2;
                 const int hb0 = 3 * rank, nhb = rank < 2 ? 3 : 2;
-                const float4 w = *reinterpret_cast<const float4*>(&sConvW[(2 * kD + j) * 4]);
+                const f2 w0 = f2_dup(sConvW[8 * kD + j]), w1 = f2_dup(sConvW[9 * kD + j]),
+                         w2 = f2_dup(sConvW[10 * kD + j]), w3 = f2_dup(sConvW[11 * kD + j]);
                 const bf16* vt = reinterpret_cast<const bf16*>(sm + kOffRawV);
                 auto raw = [&](int64_t p) -> float {
                     if (p >= s0) return to_f(vt[(uint32_t)(p - (t0 - 3)) * (kRawStride / 2) + j]);
@@ -759,19 +789,25 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                     uint32_t* rl = &rlo.x;
 #pragma unroll
                     for (int e = 0; e < 8; e += 2) {
-                        float rv[2];
-#pragma unroll
-                        for (int f = 0; f < 2; ++f) {
-                            const int i = i0 + e + f;
-                            float xr = 0.f, vr = 0.f;
-                            if (i < Lc && !ident_run) {
-                                xr = to_f(vt[(uint32_t)(i + 3) * (kRawStride / 2) + j]);
-                                vr = silu_fast(w.x * p0 + w.y * p1 + w.z * p2 + w.w * xr);
-                            }
-                            p0 = p1; p1 = p2; p2 = xr;
-                            rv[f] = sBeta[i] * (vr - __uint_as_float(pv[e + f]));
-                        }
-                        split2(rv[0], rv[1], rh[e / 2], rl[e / 2]);
+                        // tokens i, i + 1 as a packed pair: conv, silu, R = beta (v - P)
+                        const int i = i0 + e;
+                        const bool ok0 = i < Lc && !ident_run, ok1 = i + 1 < Lc && !ident_run;
+                        const float x0 = ok0 ? to_f(vt[(uint32_t)(i + 3) * (kRawStride / 2) + j]) : 0.f;
+                        const float x1 = ok1 ? to_f(vt[(uint32_t)(i + 4) * (kRawStride / 2) + j]) : 0.f;
+                        f2 u = mul2(w0, f2_of(p0, p1));
+                        u = fma2(w1, f2_of(p1, p2), u);
+                        u = fma2(w2, f2_of(p2, x0), u);
+                        u = fma2(w3, f2_of(x0, x1), u);
+                        const f2 hx = mul2(u, f2_dup(0.5f));  // silu(u) = h + h tanh(h), h = u / 2
+                        const f2 sv = fma2(hx, f2_of(tanh_hw(f2_lo(hx)), tanh_hw(f2_hi(hx))), hx);
+                        const f2 vr = f2_of(ok0 ? f2_lo(sv) : 0.f, ok1 ? f2_hi(sv) : 0.f);
+                        const float2 b2 = *reinterpret_cast<const float2*>(&sBeta[i]);
+                        const f2 rv = mul2(f2_of(b2.x, b2.y),
+                                           sub2(vr, f2_of(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1]))));
+                        split2p(rv, rh[e / 2], rl[e / 2]);
+                        p0 = p2;
+                        p1 = x0;
+                        p2 = x1;
                     }
                     tmem_st4(tb + lane_off + kColR + 4 * hb, rhi);
                     tmem_st4(tb + lane_off + kColR + 32 + 4 * hb, rlo);
