@@ -665,32 +665,35 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             const int nq = (4 - d) * 64;
             if (tid < nq) {
                 const int J = tid >> 6, I = J + d, rr = (tid >> 2) & 15, jq = tid & 3;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                f2 acc0 = f2_dup(0.f), acc1 = f2_dup(0.f);
                 for (int K = J; K < I; ++K)
 #pragma unroll
                     for (int kk = 0; kk < 16; ++kk) {
-                        const float a = sAf[(16 * I + rr) * kAs + 16 * K + kk];
+                        const f2 a = f2_dup(sAf[(16 * I + rr) * kAs + 16 * K + kk]);
                         const float4 t4 = *reinterpret_cast<const float4*>(&sTf[(16 * K + kk) * 64 + 16 * J + 4 * jq]);
-                        acc.x += a * t4.x; acc.y += a * t4.y; acc.z += a * t4.z; acc.w += a * t4.w;
+                        acc0 = fma2(a, f2_of(t4.x, t4.y), acc0);
+                        acc1 = fma2(a, f2_of(t4.z, t4.w), acc1);
                     }
-                *reinterpret_cast<float4*>(&sX[(J * 16 + rr) * 16 + 4 * jq]) = acc;
+                *reinterpret_cast<float4*>(&sX[(J * 16 + rr) * 16 + 4 * jq]) =
+                    make_float4(f2_lo(acc0), f2_hi(acc0), f2_lo(acc1), f2_hi(acc1));
             }
         };
         auto level_t = [&](int d) {
             const int nq = (4 - d) * 64;
             if (tid < nq) {
                 const int J = tid >> 6, I = J + d, rr = (tid >> 2) & 15, jq = tid & 3;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                f2 acc0 = f2_dup(0.f), acc1 = f2_dup(0.f);
 #pragma unroll
                 for (int kk = 0; kk < 16; ++kk) {
                     if (kk <= rr) {
-                        const float t = sTf[(16 * I + rr) * 64 + 16 * I + kk];
+                        const f2 t = f2_dup(sTf[(16 * I + rr) * 64 + 16 * I + kk]);
                         const float4 x4 = *reinterpret_cast<const float4*>(&sX[(J * 16 + kk) * 16 + 4 * jq]);
-                        acc.x += t * x4.x; acc.y += t * x4.y; acc.z += t * x4.z; acc.w += t * x4.w;
+                        acc0 = fma2(t, f2_of(x4.x, x4.y), acc0);
+                        acc1 = fma2(t, f2_of(x4.z, x4.w), acc1);
                     }
                 }
                 *reinterpret_cast<float4*>(&sTf[(16 * I + rr) * 64 + 16 * J + 4 * jq]) =
-                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+                    make_float4(-f2_lo(acc0), -f2_hi(acc0), -f2_lo(acc1), -f2_hi(acc1));
             }
         };
         if (warp < kSolveWarps) {
@@ -887,19 +890,27 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             tmem_ld32(tb + lane_off + kColS + 32 * qt, dsv);
             tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) {
+            for (int e = 0; e < 32; e += 4) {  // S = Diag(gamma) S + dS, channel pairs packed
                 const float4 gm = *reinterpret_cast<const float4*>(&sConst[cGam * kD + 32 * qt + e]);
-                Sreg[e + 0] = gm.x * Sreg[e + 0] + __uint_as_float(dsv[e + 0]);
-                Sreg[e + 1] = gm.y * Sreg[e + 1] + __uint_as_float(dsv[e + 1]);
-                Sreg[e + 2] = gm.z * Sreg[e + 2] + __uint_as_float(dsv[e + 2]);
-                Sreg[e + 3] = gm.w * Sreg[e + 3] + __uint_as_float(dsv[e + 3]);
+                const f2 s01 = fma2(f2_of(gm.x, gm.y), f2_of(Sreg[e], Sreg[e + 1]),
+                                    f2_of(__uint_as_float(dsv[e]), __uint_as_float(dsv[e + 1])));
+                const f2 s23 = fma2(f2_of(gm.z, gm.w), f2_of(Sreg[e + 2], Sreg[e + 3]),
+                                    f2_of(__uint_as_float(dsv[e + 2]), __uint_as_float(dsv[e + 3])));
+                Sreg[e] = f2_lo(s01);
+                Sreg[e + 1] = f2_hi(s01);
+                Sreg[e + 2] = f2_lo(s23);
+                Sreg[e + 3] = f2_hi(s23);
             }
             uint32_t ov[16];
             tmem_ld16(tb + lane_off + kColO + 16 * qt, ov);
             tmem_ld_wait();
             float o[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) o[e] = scale * __uint_as_float(ov[e]);
+            for (int e = 0; e < 16; e += 2) {
+                const f2 o2 = mul2(f2_dup(scale), f2_of(__uint_as_float(ov[e]), __uint_as_float(ov[e + 1])));
+                o[e] = f2_lo(o2);
+                o[e + 1] = f2_hi(o2);
+            }
             if (raw_out) {
                 float* ot = reinterpret_cast<float*>(sm + kOffYT);  // [64][128] fp32 o tile
 #pragma unroll
@@ -909,7 +920,12 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             // halve across lanes 8, 4, 2, 1 apart, then fold the two 16-lane halves
             float sq[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) sq[e] = o[e] * o[e];
+            for (int e = 0; e < 16; e += 2) {
+                const f2 o2 = f2_of(o[e], o[e + 1]);
+                const f2 q2 = mul2(o2, o2);
+                sq[e] = f2_lo(q2);
+                sq[e + 1] = f2_hi(q2);
+            }
 #pragma unroll
             for (int sh = 8; sh >= 1; sh >>= 1) {
                 const bool upper = (lane & sh) != 0;
@@ -930,11 +946,16 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             const bf16* gt = reinterpret_cast<const bf16*>(sm + kOffGateT);
             To* yt = reinterpret_cast<To*>(sm + kOffYT);  // [64][128] y tile (K~ is free after G6)
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
+            for (int e = 0; e < 16; e += 2) {  // tokens rr, rr + 1 packed
                 const int rr = 16 * qt + e;
-                float yv = o[e] * sInv[rr] * wj;
-                if (gate_p) yv *= sigmoid_fast(to_f(gt[rr * kD + j]));
-                yt[rr * kD + j] = from_f<To>(yv);
+                const float2 iv = *reinterpret_cast<const float2*>(&sInv[rr]);
+                f2 y2 = mul2(mul2(f2_of(o[e], o[e + 1]), f2_of(iv.x, iv.y)), f2_dup(wj));
+                if (gate_p) {  // sigmoid(z) = 1/2 + tanh(z / 2) / 2
+                    const f2 hz = mul2(f2_of(to_f(gt[rr * kD + j]), to_f(gt[(rr + 1) * kD + j])), f2_dup(0.5f));
+                    y2 = mul2(y2, fma2(f2_dup(0.5f), f2_of(tanh_hw(f2_lo(hz)), tanh_hw(f2_hi(hz))), f2_dup(0.5f)));
+                }
+                yt[rr * kD + j] = from_f<To>(f2_lo(y2));
+                yt[(rr + 1) * kD + j] = from_f<To>(f2_hi(y2));
             }
             }
         }
