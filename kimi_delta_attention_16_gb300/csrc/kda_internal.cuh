@@ -57,16 +57,8 @@ __device__ __forceinline__ f2 f2_of(float a, float b) {
     return r;
 }
 __device__ __forceinline__ f2 f2_dup(float a) { return f2_of(a, a); }
-__device__ __forceinline__ float f2_lo(f2 x) {
-    float a, b;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x.v));
-    return a;
-}
-__device__ __forceinline__ float f2_hi(f2 x) {
-    float a, b;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x.v));
-    return b;
-}
+__device__ __forceinline__ float f2_lo(f2 x) { return __uint_as_float((uint32_t)x.v); }
+__device__ __forceinline__ float f2_hi(f2 x) { return __uint_as_float((uint32_t)(x.v >> 32)); }
 __device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {  // a * b + c
     f2 r;
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));

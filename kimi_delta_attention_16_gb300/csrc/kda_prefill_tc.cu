@@ -77,10 +77,13 @@ constexpr uint32_t kOffB3lo = kOffB3hi + kTileB3;
 constexpr uint32_t kOffKThi = kOffB3lo + kTileB3;
 constexpr uint32_t kOffKTlo = kOffKThi + kTileKT;
 constexpr int kGs = 132;   // padded row stride of G (floats): float4 rows, conflict-free row-per-lane reads
-constexpr int kAs = 65;    // padded row stride of A (floats) in the triangular solve
-constexpr uint32_t kOffR1 = kOffKTlo + kTileKT;   // G fp32 [64][132]  |  A fp32 [64][65] + T fp32 [64][64]
-constexpr uint32_t kR1Bytes = 64 * kGs * 4;        // 33792 >= 64*65*4 + 64*64*4
+constexpr int kAs = 68;    // padded row stride of A (floats) in the triangular solve: float4 rows,
+constexpr int kTs = 68;    // and of T: conflict-free when 8 lanes read 8 different rows
+constexpr uint32_t kOffR1 = kOffKTlo + kTileKT;   // G fp32 [64][kGs]  |  A fp32 [64][kAs] + T fp32 [64][kTs]
+constexpr uint32_t kR1Bytes = 64 * (kAs + kTs) * 4;
+static_assert(kR1Bytes >= 64 * kGs * 4, "G exceeds R1");
 constexpr uint32_t kOffR2 = kOffR1 + kR1Bytes;     // T bf16 [64][64] | M hi | M lo (K-major, 8 KB each)
+static_assert(kOffR2 % 1024 == 0, "R2 holds 128-byte-swizzled operand tiles");
 constexpr int kKnS = 132;  // row stride (floats) of the normalized k rows parked in R2 during A3b
 constexpr uint32_t kR2Bytes = 64 * kKnS * 4;       // 33792 >= 3 x 8 KB
 constexpr uint32_t kOffMisc = kOffR2 + kR2Bytes;
@@ -113,9 +116,6 @@ static_assert(kSmemBytes <= 232448 - 1024, "shared memory above the per-block li
 // per-channel constants, rows of sConst
 enum { cA0 = 0, cA1, cE0, cE1, cC2, cC3, cKt0, cKt1, cGam };
 
-// SiLU and sigmoid: one hardware tanh each (silu_tanh / sigmoid_tanh, bf16-input paths).
-__device__ __forceinline__ float silu_fast(float x) { return silu_tanh(x); }
-__device__ __forceinline__ float sigmoid_fast(float x) { return sigmoid_tanh(x); }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -208,7 +208,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     const uint32_t sbase = smem_u32(sm);
     float* sG = reinterpret_cast<float*>(sm + kOffR1);
     float* sAf = reinterpret_cast<float*>(sm + kOffR1);                 // [64][kAs]
-    float* sTf = reinterpret_cast<float*>(sm + kOffR1 + 64 * kAs * 4);  // [64][64]
+    float* sTf = reinterpret_cast<float*>(sm + kOffR1 + 64 * kAs * 4);  // [64][kTs]
     uint8_t* sTbf = sm + kOffR2;
     uint8_t* sMhi = sm + kOffR2 + 8192;
     uint8_t* sMlo = sm + kOffR2 + 16384;
@@ -630,7 +630,8 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) sAf[r * kAs + 16 * qt + e] = row[e];
+                for (int e = 0; e < 16; e += 4)
+                    *reinterpret_cast<float4*>(&sAf[r * kAs + 16 * qt + e]) = make_float4(row[e], row[e + 1], row[e + 2], row[e + 3]);
             }
         }
         cp_async_wait_all();  // this thread's v and gate rows (issued at the start of C)
@@ -657,86 +658,138 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         // block level (192 quads of outputs), warps 0-3 for the other two levels (128 and 64
         // quads) and the bf16 copy.  Diagonal 16x16 blocks: one warp per block, lane jj (lanes
         // 16..31 mirror 0..15) keeps column jj of the block in registers.
-        float* sX = sSS;  // [(4-d) blocks][16][16] of X, 768 floats over sSS + sRed
-        // Off-diagonal 16-blocks of block diagonal d: X_IJ = sum_{K=J}^{I-1} A_IK T_KJ, then
-        // T_IJ = -T_II X_IJ.  A thread makes four adjacent outputs (one broadcast load of A or
-        // T_II and one float4 load per k).
-        auto level_x = [&](int d) {
-            const int nq = (4 - d) * 64;
-            if (tid < nq) {
-                const int J = tid >> 6, I = J + d, rr = (tid >> 2) & 15, jq = tid & 3;
-                f2 acc0 = f2_dup(0.f), acc1 = f2_dup(0.f);
-                for (int K = J; K < I; ++K)
+        float* sX = sSS;  // 3 slots of [16][16] X floats, 768 floats over sSS + sRed
+        // Off-diagonal 16-blocks: X_IJ = sum_{K=J}^{I-1} A_IK T_KJ, then T_IJ = -T_II X_IJ.  A
+        // thread makes one quad (row rr, columns 4 jq .. 4 jq + 3) of a block; A rows and T rows
+        // come as float4 loads, the products in packed pairs on two chains (even / odd k).
+        // x_quad adds A_IK T_KJ for K in [K0, K1) to (x01, x23).
+        auto x_quad = [&](int I, int J, int K0, int K1, int rr, int jq, f2& x01, f2& x23) {
+            f2 a01 = x01, a23 = x23, b01 = f2_dup(0.f), b23 = f2_dup(0.f);
+            for (int K = K0; K < K1; ++K) {
 #pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) {
-                        const f2 a = f2_dup(sAf[(16 * I + rr) * kAs + 16 * K + kk]);
-                        const float4 t4 = *reinterpret_cast<const float4*>(&sTf[(16 * K + kk) * 64 + 16 * J + 4 * jq]);
-                        acc0 = fma2(a, f2_of(t4.x, t4.y), acc0);
-                        acc1 = fma2(a, f2_of(t4.z, t4.w), acc1);
-                    }
-                *reinterpret_cast<float4*>(&sX[(J * 16 + rr) * 16 + 4 * jq]) =
-                    make_float4(f2_lo(acc0), f2_hi(acc0), f2_lo(acc1), f2_hi(acc1));
-            }
-        };
-        auto level_t = [&](int d) {
-            const int nq = (4 - d) * 64;
-            if (tid < nq) {
-                const int J = tid >> 6, I = J + d, rr = (tid >> 2) & 15, jq = tid & 3;
-                f2 acc0 = f2_dup(0.f), acc1 = f2_dup(0.f);
+                for (int m = 0; m < 4; ++m) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(&sAf[(16 * I + rr) * kAs + 16 * K + 4 * m]);
+                    const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
-                    if (kk <= rr) {
-                        const f2 t = f2_dup(sTf[(16 * I + rr) * 64 + 16 * I + kk]);
-                        const float4 x4 = *reinterpret_cast<const float4*>(&sX[(J * 16 + kk) * 16 + 4 * jq]);
-                        acc0 = fma2(t, f2_of(x4.x, x4.y), acc0);
-                        acc1 = fma2(t, f2_of(x4.z, x4.w), acc1);
+                    for (int uu = 0; uu < 4; ++uu) {
+                        const float4 t4 =
+                            *reinterpret_cast<const float4*>(&sTf[(16 * K + 4 * m + uu) * kTs + 16 * J + 4 * jq]);
+                        const f2 aa = f2_dup(av[uu]);
+                        if (uu & 1) {
+                            b01 = fma2(aa, f2_of(t4.x, t4.y), b01);
+                            b23 = fma2(aa, f2_of(t4.z, t4.w), b23);
+                        } else {
+                            a01 = fma2(aa, f2_of(t4.x, t4.y), a01);
+                            a23 = fma2(aa, f2_of(t4.z, t4.w), a23);
+                        }
                     }
                 }
-                *reinterpret_cast<float4*>(&sTf[(16 * I + rr) * 64 + 16 * J + 4 * jq]) =
-                    make_float4(-f2_lo(acc0), -f2_hi(acc0), -f2_lo(acc1), -f2_hi(acc1));
             }
+            x01 = add2(a01, b01);
+            x23 = add2(a23, b23);
         };
+        // X quads live in sX block slot `slot` ([16][16] floats)
+        auto x_store = [&](int slot, int rr, int jq, f2 x01, f2 x23) {
+            *reinterpret_cast<float4*>(&sX[(slot * 16 + rr) * 16 + 4 * jq]) =
+                make_float4(f2_lo(x01), f2_hi(x01), f2_lo(x23), f2_hi(x23));
+        };
+        // T_IJ quad = -T_II X (X in slot J); T_II is lower triangular with exact zeros above
+        auto t_quad = [&](int I, int J, int rr, int jq) {
+            f2 a01 = f2_dup(0.f), a23 = f2_dup(0.f), b01 = f2_dup(0.f), b23 = f2_dup(0.f);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float4 t4 = *reinterpret_cast<const float4*>(&sTf[(16 * I + rr) * kTs + 16 * I + 4 * m]);
+                const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+                for (int uu = 0; uu < 4; ++uu) {
+                    const float4 x4 = *reinterpret_cast<const float4*>(&sX[(J * 16 + 4 * m + uu) * 16 + 4 * jq]);
+                    const f2 tt = f2_dup(tv[uu]);
+                    if (uu & 1) {
+                        b01 = fma2(tt, f2_of(x4.x, x4.y), b01);
+                        b23 = fma2(tt, f2_of(x4.z, x4.w), b23);
+                    } else {
+                        a01 = fma2(tt, f2_of(x4.x, x4.y), a01);
+                        a23 = fma2(tt, f2_of(x4.z, x4.w), a23);
+                    }
+                }
+            }
+            const f2 x01 = add2(a01, b01), x23 = add2(a23, b23);
+            *reinterpret_cast<float4*>(&sTf[(16 * I + rr) * kTs + 16 * J + 4 * jq]) =
+                make_float4(-f2_lo(x01), -f2_hi(x01), -f2_lo(x23), -f2_hi(x23));
+        };
+        const int q_rr = (tid >> 2) & 15, q_jq = tid & 3, q_blk = tid >> 6;
         if (warp < kSolveWarps) {
             if (warp < 4) {
+                // diagonal block b0: lane jj keeps column jj; row rr subtracts A_rr,ii t_ii
+                // for ii < rr on two chains, with the A row as float4 loads
                 const int b0 = 16 * warp, jj = lane & 15;
                 float t[16];
 #pragma unroll
                 for (int rr = 0; rr < 16; ++rr) {
-                    float acc = rr == jj ? 1.f : 0.f;
+                    float c0 = rr == jj ? 1.f : 0.f, c1 = 0.f;
                     const float* arow = sAf + (b0 + rr) * kAs + b0;
 #pragma unroll
-                    for (int ii = 0; ii < rr; ++ii) acc -= arow[ii] * t[ii];
-                    t[rr] = acc;
+                    for (int q4 = 0; q4 < (rr + 3) / 4; ++q4) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(&arow[4 * q4]);
+                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                        for (int uu = 0; uu < 4; ++uu) {
+                            const int ii = 4 * q4 + uu;
+                            if (ii < rr) {
+                                if (ii & 1) c1 -= av[uu] * t[ii];
+                                else c0 -= av[uu] * t[ii];
+                            }
+                        }
+                    }
+                    t[rr] = c0 + c1;
                 }
                 if (lane < 16) {
 #pragma unroll
-                    for (int rr = 0; rr < 16; ++rr) sTf[(b0 + rr) * 64 + b0 + jj] = t[rr];
+                    for (int rr = 0; rr < 16; ++rr) sTf[(b0 + rr) * kTs + b0 + jj] = t[rr];
                 }
             }
             solver_sync();
-            level_x(1);
+            {  // level 1: T_10, T_21, T_32 (192 quads)
+                f2 x01 = f2_dup(0.f), x23 = f2_dup(0.f);
+                x_quad(q_blk + 1, q_blk, q_blk, q_blk + 1, q_rr, q_jq, x01, x23);
+                x_store(q_blk, q_rr, q_jq, x01, x23);
+            }
             solver_sync();
-            level_t(1);
+            t_quad(q_blk + 1, q_blk, q_rr, q_jq);
             solver_sync();
         }
         if (warp < 4) {
-            level_x(2);
+            {  // level 2: X_20, X_31 (128 quads), and A_30 T_00 + A_31 T_10 of X_30 in slot 2 (64 quads)
+                f2 x01 = f2_dup(0.f), x23 = f2_dup(0.f);
+                x_quad(q_blk + 2, q_blk, q_blk, q_blk + 2, q_rr, q_jq, x01, x23);
+                x_store(q_blk, q_rr, q_jq, x01, x23);
+                if (tid < 64) {
+                    f2 y01 = f2_dup(0.f), y23 = f2_dup(0.f);
+                    x_quad(3, 0, 0, 2, q_rr, q_jq, y01, y23);
+                    x_store(2, q_rr, q_jq, y01, y23);
+                }
+            }
             solver4_sync();
-            level_t(2);
+            t_quad(q_blk + 2, q_blk, q_rr, q_jq);
             solver4_sync();
-            level_x(3);
+            if (tid < 64) {  // level 3: X_30 = (slot 2) + A_32 T_20
+                const float4 p4 = *reinterpret_cast<const float4*>(&sX[(2 * 16 + q_rr) * 16 + 4 * q_jq]);
+                f2 x01 = f2_of(p4.x, p4.y), x23 = f2_of(p4.z, p4.w);
+                x_quad(3, 0, 2, 3, q_rr, q_jq, x01, x23);
+                x_store(0, q_rr, q_jq, x01, x23);
+            }
             solver4_sync();
-            level_t(3);
+            if (tid < 64) t_quad(3, 0, q_rr, q_jq);
             solver4_sync();
-            // T -> bf16, K-major [r][i]; the upper triangle is zero
+            // T -> bf16, K-major [r][i]; blocks above the diagonal are zero
             for (int idx = tid; idx < 64 * 8; idx += 128) {
                 const int rr = idx >> 3, k8 = idx & 7;
+                const float4 u0 = *reinterpret_cast<const float4*>(&sTf[rr * kTs + 8 * k8]);
+                const float4 u1 = *reinterpret_cast<const float4*>(&sTf[rr * kTs + 8 * k8 + 4]);
+                const float tv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
                 float t8[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int i = 8 * k8 + e;
-                    t8[e] = i <= rr ? sTf[rr * 64 + i] : 0.f;
-                }
+                for (int e = 0; e < 8; ++e) t8[e] = 8 * k8 + e <= rr ? tv[e] : 0.f;
                 uint4 hv;
                 hv.x = pack_bf16x2(t8[0], t8[1]);
                 hv.y = pack_bf16x2(t8[2], t8[3]);
