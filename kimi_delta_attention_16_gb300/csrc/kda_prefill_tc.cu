@@ -120,6 +120,13 @@ enum { cA0 = 0, cA1, cE0, cE1, cC2, cC3, cKt0, cKt1, cGam };
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+// 16 (4) bytes, of which the first src_bytes come from global memory and the rest are zero
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async4_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
@@ -298,17 +305,32 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         }
         cp_async_commit();
     };
-    // G = cumsum(g) of chunk cj (four quarters of 16 tokens) into sG, beta into sBeta (one barrier inside)
-    auto compute_G = [&](int64_t cj) {
+    // raw g rows of chunk cj -> sG (row stride kGs) and its beta -> sBeta, by cp.async with zeros
+    // past the end of the sequence; one commit group.  Issued early, so that the scan below
+    // finds the rows in shared memory instead of waiting on global loads.
+    auto stage_G = [&](int64_t cj) {
         const int64_t tc0 = s0 + (int64_t)cj * kC;
         const int Lcj = (int)((s1 - tc0) < kC ? (s1 - tc0) : kC);
+        for (int idx = tid; idx < kC * (kD / 4); idx += kThreads) {
+            const int rr = idx >> 5, vec = idx & 31;
+            const bool ok = rr < Lcj;
+            cp_async16_zfill(sbase + kOffR1 + (uint32_t)(rr * kGs + 4 * vec) * 4u,
+                             ok ? g + ((tc0 + rr) * H + h) * kD + 4 * vec : g, ok ? 16u : 0u);
+        }
+        if (tid < kC) {
+            const bool ok = tid < Lcj;
+            cp_async4_zfill(sbase + kOffMisc + (uint32_t)(kMiscBeta + tid) * 4u, ok ? beta + (tc0 + tid) * H + h : beta,
+                            ok ? 4u : 0u);
+        }
+        cp_async_commit();
+    };
+    // G = cumsum(g log2 e) down each channel of the staged rows (four quarters of 16 tokens),
+    // in place; the caller has waited for the rows.  One barrier inside.
+    auto scan_G = [&]() {
         const int c = tid & (kD - 1), hq = tid >> 7;
         float gv[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int rr = 16 * hq + e;
-            gv[e] = rr < Lcj ? g[((tc0 + rr) * H + h) * kD + c] * kLog2e : 0.f;  // base 2
-        }
+        for (int e = 0; e < 16; ++e) gv[e] = sG[(16 * hq + e) * kGs + c] * kLog2e;  // base 2
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -316,7 +338,6 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             gv[e] = acc;
         }
         sSS[hq * kD + c] = acc;  // quarter total per channel
-        if (tid < kC) sBeta[tid] = tid < Lcj ? beta[(tc0 + tid) * H + h] : 0.f;
         __syncthreads();
         float base = 0.f;
         for (int qq = 0; qq < hq; ++qq) base += sSS[qq * kD + c];
@@ -325,7 +346,10 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     };
     if (cb < ce) {
         stage_qk(cb);
-        compute_G(cb);
+        stage_G(cb);
+        cp_async_wait_all();
+        __syncthreads();
+        scan_G();
     }
 
     for (int64_t ci = cb; ci < ce && !failed; ++ci) {
@@ -875,8 +899,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         failed = __syncthreads_or(dfail) != 0;  // T (warps 0-3) and R (warps 4-15) complete
         if (failed) break;
 
-        // ------------------------------------------------ E: G4  W^T = R^T T^T; next chunk's q/k rows -> B3
-        if (ci + 1 < ce) stage_qk(ci + 1);  // G3 finished with B3 (waited in D)
+        // ------------------------------------------------ E: G4  W^T = R^T T^T; next chunk's g, beta, q/k rows staged
         if (tid == 0) {
             fence_after_sync();
             const uint32_t tbf = sbase + kOffR2;
@@ -887,6 +910,12 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                     mma_ts(tb + kColW, tb + kColR + 32 * term + 8 * kk, desc_sw128(tbf + kk * 32, 16, 1024),
                            id_64, (term | kk) != 0);
             mma_commit(&bars[2]);
+        }
+        if (ci + 1 < ce) {
+            // next chunk: g rows and beta into R1 (the solve is done with A and T) and sBeta (D is
+            // done with it), q/k rows into B3 (G3 finished with it, waited in D)
+            stage_G(ci + 1);
+            stage_qk(ci + 1);
         }
         failed = wait_mma(&bars[2], par, warp == 0);
         if (failed) break;
@@ -932,7 +961,11 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             }
             mma_commit(&bars[3]);
         }
-        if (ci + 1 < ce) compute_G(ci + 1);  // overlaps G5/G6; the A/T tile in R1 is dead
+        if (ci + 1 < ce) {  // overlaps G5/G6: the next chunk's log-decay sums from its staged rows
+            cp_async_wait_all();
+            __syncthreads();
+            scan_G();
+        }
         failed = wait_mma(&bars[3], par, warp == 0);
         if (failed) break;
         fence_after_sync();
