@@ -41,6 +41,10 @@
 //   [128,256)  X1 operand (hi, lo)               |  R^T operand (128-191), W accumulator (192-255)
 //   [256,384)  P^T accumulator (256-319), then O^T (320-383)
 //   [384,480)  [M;A] accumulator                 |  W^T operand (384-447)
+#include <cuda.h>  // CUtensorMap (encoded through the runtime's driver entry point)
+#include <cudaTypedefs.h>
+#include <string.h>
+
 #include "kda_tc.cuh"
 #include "kda_tc_ptx.cuh"
 
@@ -76,32 +80,65 @@ constexpr uint32_t kOffB3hi = kOffB1lo + kTileB1;
 constexpr uint32_t kOffB3lo = kOffB3hi + kTileB3;
 constexpr uint32_t kOffKThi = kOffB3lo + kTileB3;
 constexpr uint32_t kOffKTlo = kOffKThi + kTileKT;
-constexpr int kGs = 132;   // padded row stride of G (floats): float4 rows, conflict-free row-per-lane reads
 constexpr int kAs = 68;    // padded row stride of A (floats) in the triangular solve: float4 rows,
 constexpr int kTs = 68;    // and of T: conflict-free when 8 lanes read 8 different rows
-constexpr uint32_t kOffR1 = kOffKTlo + kTileKT;   // G fp32 [64][kGs]  |  A fp32 [64][kAs] + T fp32 [64][kTs]
+constexpr uint32_t kOffR1 = kOffKTlo + kTileKT;   // G fp32 (4 swizzled boxes)  |  A fp32 [64][kAs] + T fp32 [64][kTs]
 constexpr uint32_t kR1Bytes = 64 * (kAs + kTs) * 4;
-static_assert(kR1Bytes >= 64 * kGs * 4, "G exceeds R1");
+static_assert(kR1Bytes >= 4 * 8192, "G exceeds R1");
 constexpr uint32_t kOffR2 = kOffR1 + kR1Bytes;     // T bf16 [64][64] | M hi | M lo (K-major, 8 KB each)
 static_assert(kOffR2 % 1024 == 0, "R2 holds 128-byte-swizzled operand tiles");
 constexpr int kKnS = 132;  // row stride (floats) of the normalized k rows parked in R2 during A3b
 constexpr uint32_t kR2Bytes = 64 * kKnS * 4;       // 33792 >= 3 x 8 KB
 constexpr uint32_t kOffMisc = kOffR2 + kR2Bytes;
-// Raw-row staging in operand regions while they are not operands:
+// Raw-row staging in operand regions while they are not operands, by 2D TMA boxes with the
+// 128-byte swizzle (a box row is 128 bytes; its 16-byte chunk j sits at chunk j ^ (row & 7),
+// so one-row-per-lane reads of the same columns are conflict-free):
 //   B3 region, from G3's completion in chunk n-1 to A3a of chunk n: q and k rows t0-3 .. t0+63
-//   B1 region, from G1's completion to the epilogue: v rows t0-3 .. t0+63, gate rows t0 .. t0+63
+//     (two 64-column boxes of 67 rows each, 9 KB apart)
+//   B1 region, from G1's completion to the epilogue: v rows t0-3 .. t0+63 (same shape), gate
+//     rows t0 .. t0+63 (two 64-column boxes of 64 rows, 8 KB apart)
+//   R1, from E of chunk n-1 to the end of A3b of chunk n: g rows t0 .. t0+63 (four 32-column
+//     fp32 boxes of 64 rows, 8 KB apart), scanned in place into G
 //   K~ region, after G6: the y tile of the epilogue
-// Rows are padded to 272 bytes so that one-row-per-lane 16-byte reads are conflict-free.
-constexpr uint32_t kRawStride = 272;
 constexpr int kRawRows = kC + 3;
+constexpr uint32_t kRawBox = 9216;    // 67 rows x 128 bytes, rounded up to the 1024-byte swizzle period
+constexpr uint32_t kGateBox = 8192;   // 64 rows x 128 bytes
+constexpr uint32_t kGBox = 8192;      // 64 rows x 32 fp32
 constexpr uint32_t kOffRawQ = kOffB3hi;
-constexpr uint32_t kOffRawK = kOffB3hi + 18432;
+constexpr uint32_t kOffRawK = kOffB3hi + 2 * kRawBox;
 constexpr uint32_t kOffRawV = kOffB1hi;
-constexpr uint32_t kOffGateT = kOffB1hi + 18432;  // [64][128] bf16, 256-byte rows
+constexpr uint32_t kOffGateT = kOffB1hi + 2 * kRawBox;
 constexpr uint32_t kOffYT = kOffKThi;              // [64][128] y tile (bf16 or fp32)
-static_assert(kOffRawK + kRawRows * kRawStride <= kOffKThi, "q/k staging exceeds the B3 region");
-static_assert(kOffGateT + kC * 256 <= kOffB3hi, "gate staging exceeds the B1 region");
+static_assert(kRawRows * 128 <= kRawBox, "raw box exceeds its slot");
+static_assert(kOffRawK + 2 * kRawBox <= kOffKThi, "q/k staging exceeds the B3 region");
+static_assert(kOffGateT + 2 * kGateBox <= kOffB3hi, "gate staging exceeds the B1 region");
 static_assert(kOffYT + 64 * 128 * 4 <= kOffR1, "y tile exceeds the K~ region");
+static_assert(kOffRawQ % 1024 == 0 && kOffRawK % 1024 == 0 && kOffRawV % 1024 == 0 && kOffGateT % 1024 == 0 &&
+                  kOffR1 % 1024 == 0 && kRawBox % 1024 == 0,
+              "swizzled TMA boxes start on 1024-byte boundaries");
+// Byte offsets inside the staged boxes: bf16 element c of raw row rr (64-column boxes of
+// box_bytes), and fp32 element c of g / G row rr (32-column boxes).
+__device__ __forceinline__ uint32_t swz128(int rr, int chunk) {
+    return (uint32_t)(rr * 128 + ((chunk ^ (rr & 7)) << 4));
+}
+__device__ __forceinline__ uint32_t raw_off(uint32_t box_bytes, int rr, int c) {
+    return (uint32_t)(c >> 6) * box_bytes + swz128(rr, (c & 63) >> 3) + (uint32_t)(c & 7) * 2u;
+}
+__device__ __forceinline__ uint32_t g_off(int rr, int c) {
+    return (uint32_t)(c >> 5) * kGBox + swz128(rr, (c & 31) >> 2) + (uint32_t)(c & 3) * 4u;
+}
+
+// Tensor maps of the staged inputs: [T rows][H * 128 columns], 128-byte swizzle, boxes as above.
+struct TmaMaps {
+    CUtensorMap q, k, v, gate, g;
+};
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // misc (floats)
 constexpr int kMiscConvW = 0;                  // [3][128][4]
 constexpr int kMiscConst = kMiscConvW + 1536;  // [9][128]
@@ -117,13 +154,7 @@ static_assert(kSmemBytes <= 232448 - 1024, "shared memory above the per-block li
 enum { cA0 = 0, cA1, cE0, cE1, cC2, cC3, cKt0, cKt1, cGam };
 
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-// 16 (4) bytes, of which the first src_bytes come from global memory and the rest are zero
-__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
+// 4 bytes, of which the first src_bytes come from global memory and the rest are zero
 __device__ __forceinline__ void cp_async4_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
@@ -204,16 +235,19 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
              const bf16* __restrict__ gate, const float* __restrict__ rms_w, float eps_l2,
              float eps_rms, float scale, const float* __restrict__ S0, float* __restrict__ S_fin,
              To* __restrict__ out, const int32_t* __restrict__ cu, int64_t T_total, int H,
-             int* d_status, SegPlan sp) {
+             int* d_status, SegPlan sp, const __grid_constant__ TmaMaps maps) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bars[4];  // G1 done, G3 done, G4 done, G5+G6 done
+    // G1 done, G3 done, G4 done, G5+G6 done; staged rows landed: g (next chunk), q/k (next
+    // chunk), v/gate (this chunk)
+    __shared__ uint64_t bars[7];
     __shared__ uint32_t s_tbase;
     __shared__ int s_dfail;  // set by warp 15 when it has waited for G3
 
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t sbase = smem_u32(sm);
-    float* sG = reinterpret_cast<float*>(sm + kOffR1);
+    // G element (row rr, channel c) in the swizzled g boxes of R1
+    auto sGat = [&](int rr, int c) -> float& { return *reinterpret_cast<float*>(sm + kOffR1 + g_off(rr, c)); };
     float* sAf = reinterpret_cast<float*>(sm + kOffR1);                 // [64][kAs]
     float* sTf = reinterpret_cast<float*>(sm + kOffR1 + 64 * kAs * 4);  // [64][kTs]
     uint8_t* sTbf = sm + kOffR2;
@@ -253,7 +287,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < 7; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         s_dfail = 0;
     }
@@ -291,46 +325,66 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     const uint32_t id_g6 = idesc_bf16(128, 128, false, true);
     bool failed = false;
 
-    // q/k rows of chunk cj (t0-3 .. t0+63 within the sequence) -> B3 region, one cp.async group
-    auto stage_qk = [&](int64_t cj) {
-        const int64_t tc0 = s0 + (int64_t)cj * kC;
-        for (int idx = tid; idx < 2 * kRawRows * 16; idx += kThreads) {
-            const int part = idx >= kRawRows * 16 ? 1 : 0;
-            const int rem = idx - part * kRawRows * 16;
-            const int tr = rem >> 4, vec = rem & 15;
-            const int64_t pr = tc0 - 3 + tr;
-            if (pr >= s0 && pr < s1)
-                cp_async16(sbase + (part ? kOffRawK : kOffRawQ) + tr * kRawStride + 16 * vec,
-                           (part ? k : q) + pr * xs + (int64_t)h * kD + 8 * vec);
+    // Row staging by the TMA engine: one warp issues 1D bulk copies of whole rows (256 bytes of
+    // bf16, 512 of fp32) and lane 0 arms the completion mbarrier for their bytes.  The rows of
+    // chunk cj complete phase (cj - cb) of their barrier (bars[4] g, bars[5] q/k, bars[6]
+    // v/gate), so every wait takes parity (cj - cb) & 1.  `pend` (uniform over the CTA) keeps,
+    // per barrier i, bit 2i = a completion in flight and bit 2i+1 = its parity, for the exit path.
+    uint32_t pend = 0;
+    auto pend_set = [&](int i, int64_t cj) { pend |= (1u | ((uint32_t)((cj - cb) & 1) << 1)) << (2 * i); };
+    auto pend_clear = [&](int i) { pend &= ~(3u << (2 * i)); };
+    // q/k rows t0-3 .. t0+63 of chunk cj -> B3 region, four boxes from thread 32 wq (rows
+    // outside the tensor read as zero; rows of a neighbouring sequence are never used)
+    auto stage_qk = [&](int64_t cj, int wq) {
+        if (tid == 32 * wq) {
+            const int y = (int)(s0 + (int64_t)cj * kC - 3), x = h * kD;
+            mbar_expect_tx(&bars[5], 4 * kRawRows * 128);
+            tma_load_2d(sbase + kOffRawQ, &maps.q, x, y, &bars[5]);
+            tma_load_2d(sbase + kOffRawQ + kRawBox, &maps.q, x + 64, y, &bars[5]);
+            tma_load_2d(sbase + kOffRawK, &maps.k, x, y, &bars[5]);
+            tma_load_2d(sbase + kOffRawK + kRawBox, &maps.k, x + 64, y, &bars[5]);
         }
-        cp_async_commit();
+        pend_set(1, cj);
     };
-    // raw g rows of chunk cj -> sG (row stride kGs) and its beta -> sBeta, by cp.async with zeros
-    // past the end of the sequence; one commit group.  Issued early, so that the scan below
-    // finds the rows in shared memory instead of waiting on global loads.
-    auto stage_G = [&](int64_t cj) {
+    // g rows of chunk cj -> R1, four boxes from thread 32 wq (bars[4]); its beta -> sBeta by
+    // cp.async of threads 64 wq .. 64 wq + 63 (zeros past the sequence end).  Issued early, so
+    // that the scan below finds the rows in shared memory.
+    auto stage_G = [&](int64_t cj, int wq) {
         const int64_t tc0 = s0 + (int64_t)cj * kC;
         const int Lcj = (int)((s1 - tc0) < kC ? (s1 - tc0) : kC);
-        for (int idx = tid; idx < kC * (kD / 4); idx += kThreads) {
-            const int rr = idx >> 5, vec = idx & 31;
-            const bool ok = rr < Lcj;
-            cp_async16_zfill(sbase + kOffR1 + (uint32_t)(rr * kGs + 4 * vec) * 4u,
-                             ok ? g + ((tc0 + rr) * H + h) * kD + 4 * vec : g, ok ? 16u : 0u);
+        if (tid == 32 * wq) {
+            mbar_expect_tx(&bars[4], 4 * kGBox);
+#pragma unroll
+            for (int b4 = 0; b4 < 4; ++b4)
+                tma_load_2d(sbase + kOffR1 + b4 * kGBox, &maps.g, h * kD + 32 * b4, (int)tc0, &bars[4]);
         }
-        if (tid < kC) {
-            const bool ok = tid < Lcj;
-            cp_async4_zfill(sbase + kOffMisc + (uint32_t)(kMiscBeta + tid) * 4u, ok ? beta + (tc0 + tid) * H + h : beta,
+        const int rb = tid - 64 * wq;
+        if (rb >= 0 && rb < kC) {
+            const bool ok = rb < Lcj;
+            cp_async4_zfill(sbase + kOffMisc + (uint32_t)(kMiscBeta + rb) * 4u, ok ? beta + (tc0 + rb) * H + h : beta,
                             ok ? 4u : 0u);
         }
         cp_async_commit();
+        pend_set(0, cj);
     };
-    // G = cumsum(g log2 e) down each channel of the staged rows (four quarters of 16 tokens),
-    // in place; the caller has waited for the rows.  One barrier inside.
-    auto scan_G = [&]() {
+    // Waits for stage_G(cj)'s rows (poller warp wq) and beta copies; false if the wait timed out.
+    auto wait_G = [&](int64_t cj, int wq) -> bool {
+        bool ok = true;
+        if (warp == wq) ok = mbar_wait(&bars[4], (uint32_t)((cj - cb) & 1));
+        pend_clear(0);
+        cp_async_wait_all();
+        return __syncthreads_or(!ok) == 0;
+    };
+    // G = cumsum(g log2 e) down each channel of the staged rows of chunk cj (four quarters of
+    // 16 tokens; rows past the sequence end count as zero), in place; the caller has waited for
+    // the rows.  One barrier inside.
+    auto scan_G = [&](int64_t cj) {
+        const int64_t tc0 = s0 + (int64_t)cj * kC;
+        const int Lcj = (int)((s1 - tc0) < kC ? (s1 - tc0) : kC);
         const int c = tid & (kD - 1), hq = tid >> 7;
         float gv[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) gv[e] = sG[(16 * hq + e) * kGs + c] * kLog2e;  // base 2
+        for (int e = 0; e < 16; ++e) gv[e] = 16 * hq + e < Lcj ? sGat(16 * hq + e, c) * kLog2e : 0.f;  // base 2
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -342,14 +396,13 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         float base = 0.f;
         for (int qq = 0; qq < hq; ++qq) base += sSS[qq * kD + c];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) sG[(16 * hq + e) * kGs + c] = gv[e] + base;
+        for (int e = 0; e < 16; ++e) sGat(16 * hq + e, c) = gv[e] + base;
     };
     if (cb < ce) {
-        stage_qk(cb);
-        stage_G(cb);
-        cp_async_wait_all();
-        __syncthreads();
-        scan_G();
+        stage_qk(cb, 2);
+        stage_G(cb, 1);
+        failed = !wait_G(cb, 1);
+        if (!failed) scan_G(cb);
     }
 
     for (int64_t ci = cb; ci < ce && !failed; ++ci) {
@@ -376,14 +429,18 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         }
 
         // q/k rows and G of this chunk were prepared during the previous chunk (or before the loop)
-        cp_async_wait_all();
-        __syncthreads();
+        {
+            bool ok = true;
+            if (warp == 0) ok = mbar_wait(&bars[5], par);
+            pend_clear(1);
+            failed = __syncthreads_or(!ok) != 0;
+            if (failed) break;
+        }
 
         // ------------------------------------------------ A2: per-channel anchors and factors
         if (tid < kD) {
             const int c = tid;
-            const float a0 = sG[15 * kGs + c], a1 = sG[47 * kGs + c], g31 = sG[31 * kGs + c],
-                        gl = sG[63 * kGs + c];
+            const float a0 = sGat(15, c), a1 = sGat(47, c), g31 = sGat(31, c), gl = sGat(63, c);
             sConst[cA0 * kD + c] = a0;
             sConst[cA1 * kD + c] = a1;
             sConst[cE0 * kD + c] = exp2_hw(a0);
@@ -417,7 +474,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                         for (int e = 0; e < 8; ++e) win[m][e] = 0.f;
                     } else if (p >= s0) {
                         load8(reinterpret_cast<const bf16*>(sm + (isq ? kOffRawQ : kOffRawK) +
-                                                            (uint32_t)(p - (t0 - 3)) * kRawStride + 2 * cc),
+                                                            raw_off(kRawBox, (int)(p - (t0 - 3)), cc)),
                               win[m]);
                     } else {
                         const int pos = (int)(p - s0);  // -3..-1
@@ -494,7 +551,14 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 f2 xv[4], dg[4], uu[4], EE[4];
                 {
                     f2 gg[4], aa[4];
-                    ld_f2x4(&sG[r * kGs + cc], gg);
+                    {  // G row r, columns cc .. cc + 7: two swizzled 16-byte chunks
+                        const float4 g0 = *reinterpret_cast<const float4*>(sm + kOffR1 + g_off(r, cc));
+                        const float4 g1 = *reinterpret_cast<const float4*>(sm + kOffR1 + g_off(r, cc + 4));
+                        gg[0] = f2_of(g0.x, g0.y);
+                        gg[1] = f2_of(g0.z, g0.w);
+                        gg[2] = f2_of(g1.x, g1.y);
+                        gg[3] = f2_of(g1.z, g1.w);
+                    }
                     ld_f2x4(&cA[cc], aa);
                     ld_f2x4(&cE[cc], EE);
 #pragma unroll
@@ -604,23 +668,22 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         failed = wait_mma(&bars[0], par, warp == 0);
         if (failed) break;
         fence_after_sync();
-        {
-            // G1 is done with B1: stage v rows t0-3 .. t0+63 and gate rows t0 .. t0+Lc-1 there
-            if (!ident_run)
-                for (int idx = tid; idx < kRawRows * 16; idx += kThreads) {
-                    const int tr = idx >> 4, vec = idx & 15;
-                    const int64_t pr = t0 - 3 + tr;
-                    if (pr >= s0 && pr < s1)
-                        cp_async16(sbase + kOffRawV + tr * kRawStride + 16 * vec, v + pr * xs + (int64_t)h * kD + 8 * vec);
-                }
-            if (gate_p)
-                for (int idx = tid; idx < kC * 16; idx += kThreads) {
-                    const int rr = idx >> 4, vec = idx & 15;
-                    if (rr < Lc)
-                        cp_async16(sbase + kOffGateT + rr * 256 + 16 * vec, gate_p + ((t0 + rr) * H + h) * kD + 8 * vec);
-                }
-            cp_async_commit();
+        // G1 is done with B1: v rows t0-3 .. t0+63 and gate rows t0 .. t0+63 there (boxes from
+        // thread 32, bars[6]); the identity-start runs take neither
+        const bool vg = !ident_run || gate_p;
+        if (vg && tid == 32) {
+            const int x = h * kD;
+            mbar_expect_tx(&bars[6], (ident_run ? 0u : 2u * kRawRows * 128u) + (gate_p ? 2u * kGateBox : 0u));
+            if (!ident_run) {
+                tma_load_2d(sbase + kOffRawV, &maps.v, x, (int)(t0 - 3), &bars[6]);
+                tma_load_2d(sbase + kOffRawV + kRawBox, &maps.v, x + 64, (int)(t0 - 3), &bars[6]);
+            }
+            if (gate_p) {
+                tma_load_2d(sbase + kOffGateT, &maps.gate, x, (int)t0, &bars[6]);
+                tma_load_2d(sbase + kOffGateT + kGateBox, &maps.gate, x + 64, (int)t0, &bars[6]);
+            }
         }
+        if (vg) pend_set(2, ci);
         {
             // thread: row r (q rows -> M, k rows -> A), columns i in [16qt, 16qt + 16).  The warp's rows
             // share one half hr, so the source block is warp-uniform: same half -> columns i,
@@ -658,9 +721,16 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                     *reinterpret_cast<float4*>(&sAf[r * kAs + 16 * qt + e]) = make_float4(row[e], row[e + 1], row[e + 2], row[e + 3]);
             }
         }
-        cp_async_wait_all();  // this thread's v and gate rows (issued at the start of C)
-        fence_before_sync();
-        __syncthreads();      // A, the M tiles and the v / gate rows are complete
+        {  // A and the M tiles are complete; the v / gate rows have landed
+            bool ok = true;
+            if (vg) {
+                if (warp == 1) ok = mbar_wait(&bars[6], par);
+                pend_clear(2);
+            }
+            fence_before_sync();
+            failed = __syncthreads_or(!ok) != 0;
+            if (failed) break;
+        }
         // G3: [P ; Q'] = S^T . [KG ; QG]^T (state reads), from warp 15 while warps 0-5 solve
         if (tid == kThreads - 32) {
             fence_after_sync();
@@ -848,9 +918,11 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 const int hb0 = 3 * rank, nhb = rank < 2 ? 3 : 2;
                 const f2 w0 = f2_dup(sConvW[8 * kD + j]), w1 = f2_dup(sConvW[9 * kD + j]),
                          w2 = f2_dup(sConvW[10 * kD + j]), w3 = f2_dup(sConvW[11 * kD + j]);
-                const bf16* vt = reinterpret_cast<const bf16*>(sm + kOffRawV);
+                auto vat = [&](int rr) -> float {  // staged v row rr (t0 - 3 + rr), channel j
+                    return to_f(*reinterpret_cast<const bf16*>(sm + kOffRawV + raw_off(kRawBox, rr, j)));
+                };
                 auto raw = [&](int64_t p) -> float {
-                    if (p >= s0) return to_f(vt[(uint32_t)(p - (t0 - 3)) * (kRawStride / 2) + j]);
+                    if (p >= s0) return vat((int)(p - (t0 - 3)));
                     const int pos = (int)(p - s0);
                     return cs_in ? to_f(cs_in[((int64_t)n * 3 * HD + 2 * HD + (int64_t)h * kD + j) * 3 + 3 + pos]) : 0.f;
                 };
@@ -872,8 +944,8 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                         // tokens i, i + 1 as a packed pair: conv, silu, R = beta (v - P)
                         const int i = i0 + e;
                         const bool ok0 = i < Lc && !ident_run, ok1 = i + 1 < Lc && !ident_run;
-                        const float x0 = ok0 ? to_f(vt[(uint32_t)(i + 3) * (kRawStride / 2) + j]) : 0.f;
-                        const float x1 = ok1 ? to_f(vt[(uint32_t)(i + 4) * (kRawStride / 2) + j]) : 0.f;
+                        const float x0 = ok0 ? vat(i + 3) : 0.f;
+                        const float x1 = ok1 ? vat(i + 4) : 0.f;
                         f2 u = mul2(w0, f2_of(p0, p1));
                         u = fma2(w1, f2_of(p1, p2), u);
                         u = fma2(w2, f2_of(p2, x0), u);
@@ -895,6 +967,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 tmem_st_wait();
             }
         }
+        fence_async_smem();  // generic accesses to R1 (A, T, G) ordered before E's bulk copies into it
         fence_before_sync();
         failed = __syncthreads_or(dfail) != 0;  // T (warps 0-3) and R (warps 4-15) complete
         if (failed) break;
@@ -911,12 +984,9 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                            id_64, (term | kk) != 0);
             mma_commit(&bars[2]);
         }
-        if (ci + 1 < ce) {
-            // next chunk: g rows and beta into R1 (the solve is done with A and T) and sBeta (D is
-            // done with it), q/k rows into B3 (G3 finished with it, waited in D)
-            stage_G(ci + 1);
-            stage_qk(ci + 1);
-        }
+        // next chunk: g rows and beta into R1 (the solve is done with A and T) and sBeta (D is
+        // done with it), by warp 1 (warp 0 polls G4)
+        if (ci + 1 < ce) stage_G(ci + 1, 1);
         failed = wait_mma(&bars[2], par, warp == 0);
         if (failed) break;
         fence_after_sync();
@@ -962,15 +1032,18 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             mma_commit(&bars[3]);
         }
         if (ci + 1 < ce) {  // overlaps G5/G6: the next chunk's log-decay sums from its staged rows
-            cp_async_wait_all();
-            __syncthreads();
-            scan_G();
+            failed = !wait_G(ci + 1, 1);
+            if (failed) break;
+            scan_G(ci + 1);
         }
         failed = wait_mma(&bars[3], par, warp == 0);
         if (failed) break;
         fence_after_sync();
 
         // ------------------------------------------------ H: state update, output epilogue
+        // the next chunk's q/k rows into B3 (G3 finished with it in D); they land while the
+        // epilogue runs
+        if (ci + 1 < ce) stage_qk(ci + 1, 3);
         {
             uint32_t dsv[32];
             tmem_ld32(tb + lane_off + kColS + 32 * qt, dsv);
@@ -1029,7 +1102,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 sInv[tid] = rsqrtf((sRed[tid] + sRed[64 + tid] + sRed[128 + tid] + sRed[192 + tid]) * (1.0f / kD) + eps_rms);
             __syncthreads();
             const float wj = rms_w ? rms_w[j] : 1.f;
-            const bf16* gt = reinterpret_cast<const bf16*>(sm + kOffGateT);
+            const uint8_t* gt = sm + kOffGateT;  // staged gate boxes
             To* yt = reinterpret_cast<To*>(sm + kOffYT);  // [64][128] y tile (K~ is free after G6)
 #pragma unroll
             for (int e = 0; e < 16; e += 2) {  // tokens rr, rr + 1 packed
@@ -1037,7 +1110,9 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 const float2 iv = *reinterpret_cast<const float2*>(&sInv[rr]);
                 f2 y2 = mul2(mul2(f2_of(o[e], o[e + 1]), f2_of(iv.x, iv.y)), f2_dup(wj));
                 if (gate_p) {  // sigmoid(z) = 1/2 + tanh(z / 2) / 2
-                    const f2 hz = mul2(f2_of(to_f(gt[rr * kD + j]), to_f(gt[(rr + 1) * kD + j])), f2_dup(0.5f));
+                    const f2 hz = mul2(f2_of(to_f(*reinterpret_cast<const bf16*>(gt + raw_off(kGateBox, rr, j))),
+                                             to_f(*reinterpret_cast<const bf16*>(gt + raw_off(kGateBox, rr + 1, j)))),
+                                       f2_dup(0.5f));
                     y2 = mul2(y2, fma2(f2_dup(0.5f), f2_of(tanh_hw(f2_lo(hz)), tanh_hw(f2_hi(hz))), f2_dup(0.5f)));
                 }
                 yt[rr * kD + j] = from_f<To>(f2_lo(y2));
@@ -1072,6 +1147,12 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         fence_after_sync();
     }
 
+    // row copies still in flight (a wait above timed out): wait for them, bounded, before the
+    // shared memory is released
+    if (tid == 0)
+        for (int i = 0; i < 3; ++i)
+            if ((pend >> (2 * i)) & 1u) mbar_wait(&bars[4 + i], (pend >> (2 * i + 1)) & 1u);
+    cp_async_wait_all();
     if (failed) {
         if (tid == 0) flag_status(d_status, KDA_ERR_TIMEOUT);
     } else {
@@ -1144,17 +1225,56 @@ SegLayout seg_layout(const kda_prefill_args& a, int P) {
     return l;
 }
 
+// cuTensorMapEncodeTiled from the driver, through the runtime (no link against libcuda)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// [rows][cols] row-major tensor of 2- or 4-byte elements with row pitch row_bytes, boxes of
+// box_c x box_r elements, 128-byte swizzle, zeros outside the tensor.
+bool encode_map(CUtensorMap* m, const void* base, bool fp32, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+                uint32_t box_c, uint32_t box_r) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_c, box_r};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+               dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename To>
 cudaError_t tc_launch(const kda_prefill_args& a, const SegPlan& sp, cudaStream_t s) {
     auto kern = k_tc_prefill<To>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t xs = a.qkv_row_stride ? a.qkv_row_stride : (int64_t)a.H * a.D;
+    TmaMaps maps;
+    memset(&maps, 0, sizeof(maps));  // maps of absent tensors are never used
+    if (a.T_total > 0) {
+        const uint64_t cols = (uint64_t)a.H * kD, rows = (uint64_t)a.T_total;
+        bool ok = encode_map(&maps.q, a.q, false, cols, rows, (uint64_t)xs * 2, 64, kRawRows) &&
+                  encode_map(&maps.k, a.k, false, cols, rows, (uint64_t)xs * 2, 64, kRawRows) &&
+                  encode_map(&maps.v, a.v, false, cols, rows, (uint64_t)xs * 2, 64, kRawRows) &&
+                  encode_map(&maps.g, a.g, true, cols, rows, cols * 4, 32, kC);
+        if (ok && a.gate) ok = encode_map(&maps.gate, a.gate, false, cols, rows, cols * 2, 64, kC);
+        if (!ok) return cudaErrorInvalidValue;
+    }
     const unsigned grid = (unsigned)((int64_t)a.N * a.H * (2 * sp.P - 1));
     kern<<<grid, kThreads, kSmemBytes, s>>>(
         (const bf16*)a.q, (const bf16*)a.k, (const bf16*)a.v, xs, a.conv_w, (const bf16*)a.conv_state_in,
         a.g, a.beta, (const bf16*)a.gate, a.rms_w, a.eps_l2, a.eps_rms, a.scale, a.initial_state,
-        a.final_state, (To*)a.out, a.cu_seqlens, a.T_total, a.H, a.d_status, sp);
+        a.final_state, (To*)a.out, a.cu_seqlens, a.T_total, a.H, a.d_status, sp, maps);
     return cudaGetLastError();
 }
 
