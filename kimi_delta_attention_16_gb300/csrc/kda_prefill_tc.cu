@@ -144,8 +144,8 @@ constexpr int kMiscConvW = 0;                  // [3][128][4]
 constexpr int kMiscConst = kMiscConvW + 1536;  // [9][128]
 constexpr int kMiscBeta = kMiscConst + 9 * 128;
 constexpr int kMiscSS = kMiscBeta + 64;        // [128 rows][4 quarters]
-constexpr int kMiscRed = kMiscSS + 512;        // [4 quadrants][64 tokens]
-constexpr int kMiscInv = kMiscRed + 256;       // [64]
+constexpr int kMiscRed = kMiscSS + 512;        // [64 tokens][4 quadrants]
+constexpr int kMiscInv = kMiscRed + 256;       // [64] (spare)
 constexpr int kMiscFloats = kMiscInv + 64;
 constexpr uint32_t kSmemBytes = kOffMisc + kMiscFloats * 4 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448 - 1024, "shared memory above the per-block limit");
@@ -219,6 +219,10 @@ __device__ __forceinline__ void d_sync() {
 __device__ __forceinline__ void pair_arrive(int p) { asm volatile("bar.arrive %0, 64;" ::"r"(4 + p) : "memory"); }
 __device__ __forceinline__ void pair_sync(int p) { asm volatile("bar.sync %0, 64;" ::"r"(4 + p) : "memory"); }
 
+// Barrier of the four warps 4 qt .. 4 qt + 3 of one token quarter (named barriers 12..15):
+// the RMSNorm partial sums of the epilogue.
+__device__ __forceinline__ void quarter_sync(int qt) { asm volatile("bar.sync %0, 128;" ::"r"(12 + qt) : "memory"); }
+
 // Barrier of warps 0-3 only (named barrier 3): the last two levels of the solve.
 __device__ __forceinline__ void solver4_sync() { asm volatile("bar.sync 3, 128;" ::: "memory"); }
 __device__ __forceinline__ void solver_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kSolveWarps) : "memory"); }
@@ -259,7 +263,6 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     float* sBeta = misc + kMiscBeta;
     float* sSS = misc + kMiscSS;    // [128 rows][4 quarters]; also [4 quarters][128] column totals
     float* sRed = misc + kMiscRed;
-    float* sInv = misc + kMiscInv;
 
     // Thread layout: 16 warps.  Warp w reaches TMEM lanes 32 (w % 4) .. + 31 (quadrant qd) and
     // owns quarter qt = w / 4 of the channels (64 rows x 128 channels tiles) or of the tokens.
@@ -782,6 +785,27 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             x01 = add2(a01, b01);
             x23 = add2(a23, b23);
         };
+        // The same for two block rows I1, I2 of one block column J: each T load feeds both.
+        auto x_quad2 = [&](int I1, int I2, int J, int K0, int K1, int rr, int jq, f2& x01, f2& x23, f2& y01, f2& y23) {
+            for (int K = K0; K < K1; ++K) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(&sAf[(16 * I1 + rr) * kAs + 16 * K + 4 * m]);
+                    const float4 b4 = *reinterpret_cast<const float4*>(&sAf[(16 * I2 + rr) * kAs + 16 * K + 4 * m]);
+                    const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                    for (int uu = 0; uu < 4; ++uu) {
+                        const float4 t4 =
+                            *reinterpret_cast<const float4*>(&sTf[(16 * K + 4 * m + uu) * kTs + 16 * J + 4 * jq]);
+                        const f2 t01 = f2_of(t4.x, t4.y), t23 = f2_of(t4.z, t4.w);
+                        x01 = fma2(f2_dup(av[uu]), t01, x01);
+                        x23 = fma2(f2_dup(av[uu]), t23, x23);
+                        y01 = fma2(f2_dup(bv[uu]), t01, y01);
+                        y23 = fma2(f2_dup(bv[uu]), t23, y23);
+                    }
+                }
+            }
+        };
         // X quads live in sX block slot `slot` ([16][16] floats)
         auto x_store = [&](int slot, int rr, int jq, f2 x01, f2 x23) {
             *reinterpret_cast<float4*>(&sX[(slot * 16 + rr) * 16 + 4 * jq]) =
@@ -853,15 +877,17 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             solver_sync();
         }
         if (warp < 4) {
-            {  // level 2: X_20, X_31 (128 quads), and A_30 T_00 + A_31 T_10 of X_30 in slot 2 (64 quads)
+            {  // level 2: X_20 with A_30 T_00 + A_31 T_10 of X_30 (slot 2), sharing the T loads
+               // (threads 0-63); X_31 (threads 64-127)
                 f2 x01 = f2_dup(0.f), x23 = f2_dup(0.f);
-                x_quad(q_blk + 2, q_blk, q_blk, q_blk + 2, q_rr, q_jq, x01, x23);
-                x_store(q_blk, q_rr, q_jq, x01, x23);
                 if (tid < 64) {
                     f2 y01 = f2_dup(0.f), y23 = f2_dup(0.f);
-                    x_quad(3, 0, 0, 2, q_rr, q_jq, y01, y23);
+                    x_quad2(2, 3, 0, 0, 2, q_rr, q_jq, x01, x23, y01, y23);
                     x_store(2, q_rr, q_jq, y01, y23);
+                } else {
+                    x_quad(3, 1, 1, 3, q_rr, q_jq, x01, x23);
                 }
+                x_store(q_blk, q_rr, q_jq, x01, x23);
             }
             solver4_sync();
             t_quad(q_blk + 2, q_blk, q_rr, q_jq);
@@ -1096,19 +1122,24 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 }
             }
             sq[0] += __shfl_xor_sync(0xffffffffu, sq[0], 16);  // lane l: token 16qt + (l & 15)
-            if (lane < 16) sRed[qd * 64 + 16 * qt + lane] = sq[0];
-            __syncthreads();
-            if (tid < 64)
-                sInv[tid] = rsqrtf((sRed[tid] + sRed[64 + tid] + sRed[128 + tid] + sRed[192 + tid]) * (1.0f / kD) + eps_rms);
-            __syncthreads();
+            // the four warps of token quarter qt (one per channel quadrant) exchange their
+            // partial sums on a named barrier of their own; lane l < 16 of every warp then
+            // forms 1 / rms of token 16 qt + l and the lanes pass it round by shuffles
+            if (lane < 16) sRed[(16 * qt + lane) * 4 + qd] = sq[0];
+            quarter_sync(qt);
+            float inv_l;
+            {
+                const float4 r4 = *reinterpret_cast<const float4*>(&sRed[(16 * qt + (lane & 15)) * 4]);
+                inv_l = rsqrtf((r4.x + r4.y + r4.z + r4.w) * (1.0f / kD) + eps_rms);
+            }
             const float wj = rms_w ? rms_w[j] : 1.f;
             const uint8_t* gt = sm + kOffGateT;  // staged gate boxes
             To* yt = reinterpret_cast<To*>(sm + kOffYT);  // [64][128] y tile (K~ is free after G6)
 #pragma unroll
             for (int e = 0; e < 16; e += 2) {  // tokens rr, rr + 1 packed
                 const int rr = 16 * qt + e;
-                const float2 iv = *reinterpret_cast<const float2*>(&sInv[rr]);
-                f2 y2 = mul2(mul2(f2_of(o[e], o[e + 1]), f2_of(iv.x, iv.y)), f2_dup(wj));
+                const f2 iv = f2_of(__shfl_sync(0xffffffffu, inv_l, e), __shfl_sync(0xffffffffu, inv_l, e + 1));
+                f2 y2 = mul2(mul2(f2_of(o[e], o[e + 1]), iv), f2_dup(wj));
                 if (gate_p) {  // sigmoid(z) = 1/2 + tanh(z / 2) / 2
                     const f2 hz = mul2(f2_of(to_f(*reinterpret_cast<const bf16*>(gt + raw_off(kGateBox, rr, j))),
                                              to_f(*reinterpret_cast<const bf16*>(gt + raw_off(kGateBox, rr + 1, j)))),
