@@ -132,6 +132,9 @@ __device__ __forceinline__ uint32_t g_off(int rr, int c) {
 struct TmaMaps {
     CUtensorMap q, k, v, gate, g;
 };
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
@@ -402,6 +405,13 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         for (int e = 0; e < 16; ++e) sGat(16 * hq + e, c) = gv[e] + base;
     };
     if (cb < ce) {
+        if (tid == 0) {  // descriptors into the TMA unit's cache ahead of their first use
+            prefetch_map(&maps.q);
+            prefetch_map(&maps.k);
+            prefetch_map(&maps.g);
+            if (!ident_run) prefetch_map(&maps.v);
+            if (gate_p) prefetch_map(&maps.gate);
+        }
         stage_qk(cb, 2);
         stage_G(cb, 1);
         failed = !wait_G(cb, 1);
@@ -1223,14 +1233,14 @@ int device_sm_count() {
 }
 
 // Cost model of the automatic segment choice, in units of one chunk step of one CTA
-// (about 21 us measured on GB300, the same for every role):
+// (about 15 us measured on GB300, the same for every role):
 //  - segment-0 CTAs occupy U SMs for its w / (w + P - 1) share of the chunks; the
 //    2 U (P - 1) shorter CTAs of the later segments run on the other SMs in
 //    w = ceil(2 U (P - 1) / (SMs - U)) waves, which the split balances;
 //  - the fix-up streams 1,536 bytes per token-head of the later segments, measured at
 //    about 39 ns per (unit, chunk), i.e. kFixupPerUnitChunk chunk steps, across the GPU;
 //  - each extra launch and CTA start-up costs about kSegOverhead chunk steps.
-constexpr double kFixupPerUnitChunk = 0.0019;
+constexpr double kFixupPerUnitChunk = 0.0027;
 constexpr double kSegOverhead = 2.0;
 // Fewest chunks per later segment the automatic choice allows.
 constexpr double kMinSegChunks = 8.0;
