@@ -226,6 +226,11 @@ __device__ __forceinline__ void pair_sync(int p) { asm volatile("bar.sync %0, 64
 // the RMSNorm partial sums of the epilogue.
 __device__ __forceinline__ void quarter_sync(int qt) { asm volatile("bar.sync %0, 128;" ::"r"(12 + qt) : "memory"); }
 
+// Warps 8-15 (named barrier 1, which the solve uses in another phase): the log-decay scan
+// that overlaps G5/G6.
+__device__ __forceinline__ void scan_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void scan_arrive() { asm volatile("bar.arrive 1, 256;" ::: "memory"); }
+
 // Barrier of warps 0-3 only (named barrier 3): the last two levels of the solve.
 __device__ __forceinline__ void solver4_sync() { asm volatile("bar.sync 3, 128;" ::: "memory"); }
 __device__ __forceinline__ void solver_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * kSolveWarps) : "memory"); }
@@ -403,6 +408,32 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         for (int qq = 0; qq < hq; ++qq) base += sSS[qq * kD + c];
 #pragma unroll
         for (int e = 0; e < 16; ++e) sGat(16 * hq + e, c) = gv[e] + base;
+    };
+    // The same scan on warps 8-15 alone, while thread 0 issues G5/G6: thread (channel c, half
+    // h2) sums rows 32 h2 .. 32 h2 + 31; the first half passes its total on named barrier 1
+    // (free in this phase of the chunk).
+    auto scan_G_half = [&](int64_t cj) {
+        const int64_t tc0 = s0 + (int64_t)cj * kC;
+        const int Lcj = (int)((s1 - tc0) < kC ? (s1 - tc0) : kC);
+        const int c = tid & (kD - 1), h2 = (tid >> 7) & 1, r0 = 32 * h2;
+        float gv[32];
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            acc += r0 + e < Lcj ? sGat(r0 + e, c) * kLog2e : 0.f;  // base 2
+            gv[e] = acc;
+        }
+        if (h2 == 0) {
+            sSS[c] = acc;
+            scan_arrive();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sGat(e, c) = gv[e];
+        } else {
+            scan_sync();
+            const float base = sSS[c];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sGat(32 + e, c) = gv[e] + base;
+        }
     };
     if (cb < ce) {
         if (tid == 0) {  // descriptors into the TMA unit's cache ahead of their first use
@@ -848,14 +879,16 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         const int q_rr = (tid >> 2) & 15, q_jq = tid & 3, q_blk = tid >> 6;
         if (warp < kSolveWarps) {
             if (warp < 4) {
-                // diagonal block b0: lane jj keeps column jj; row rr subtracts A_rr,ii t_ii
-                // for ii < rr on two chains, with the A row as float4 loads
-                const int b0 = 16 * warp, jj = lane & 15;
-                float t[16];
+                // Diagonal 16-block b0 as 2 x 2 blocks of 8: lanes (sub, c), sub = bit 3 of the
+                // lane, invert the 8 x 8 diagonal block sub (lane c keeps column c; row rr
+                // subtracts A_rr,ii t_ii for ii < rr on two chains); then the sub = 0 lanes form
+                // T_10 = -T_11 (A_10 T_00) from shared memory.  Lanes 16-31 mirror 0-15.
+                const int b0 = 16 * warp, sub = (lane >> 3) & 1, c8 = lane & 7, sb = b0 + 8 * sub;
+                float t[8];
 #pragma unroll
-                for (int rr = 0; rr < 16; ++rr) {
-                    float c0 = rr == jj ? 1.f : 0.f, c1 = 0.f;
-                    const float* arow = sAf + (b0 + rr) * kAs + b0;
+                for (int rr = 0; rr < 8; ++rr) {
+                    float c0 = rr == c8 ? 1.f : 0.f, c1 = 0.f;
+                    const float* arow = sAf + (sb + rr) * kAs + sb;
 #pragma unroll
                     for (int q4 = 0; q4 < (rr + 3) / 4; ++q4) {
                         const float4 a4 = *reinterpret_cast<const float4*>(&arow[4 * q4]);
@@ -873,7 +906,32 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 }
                 if (lane < 16) {
 #pragma unroll
-                    for (int rr = 0; rr < 16; ++rr) sTf[(b0 + rr) * kTs + b0 + jj] = t[rr];
+                    for (int rr = 0; rr < 8; ++rr) {
+                        sTf[(sb + rr) * kTs + sb + c8] = t[rr];
+                        if (sub == 0) sTf[(b0 + rr) * kTs + b0 + 8 + c8] = 0.f;  // above the diagonal
+                    }
+                }
+                __syncwarp();
+                if (sub == 0) {
+                    // X = A_10 T_00 (column c8 of T_00 is t), then T_10 = -T_11 X
+                    float x[8];
+#pragma unroll
+                    for (int r8 = 0; r8 < 8; ++r8) {
+                        const float* arow = sAf + (b0 + 8 + r8) * kAs + b0;
+                        const float4 a0 = *reinterpret_cast<const float4*>(arow);
+                        const float4 a1 = *reinterpret_cast<const float4*>(arow + 4);
+                        x[r8] = a0.x * t[0] + a0.y * t[1] + a0.z * t[2] + a0.w * t[3] +
+                                (a1.x * t[4] + a1.y * t[5] + a1.z * t[6] + a1.w * t[7]);
+                    }
+#pragma unroll
+                    for (int r8 = 0; r8 < 8; ++r8) {
+                        const float* trow = sTf + (b0 + 8 + r8) * kTs + b0 + 8;
+                        const float4 u0 = *reinterpret_cast<const float4*>(trow);
+                        const float4 u1 = *reinterpret_cast<const float4*>(trow + 4);
+                        const float v = u0.x * x[0] + u0.y * x[1] + u0.z * x[2] + u0.w * x[3] +
+                                        (u1.x * x[4] + u1.y * x[5] + u1.z * x[6] + u1.w * x[7]);
+                        if (lane < 16) sTf[(b0 + 8 + r8) * kTs + b0 + c8] = -v;
+                    }
                 }
             }
             solver_sync();
@@ -1067,13 +1125,22 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             }
             mma_commit(&bars[3]);
         }
-        if (ci + 1 < ce) {  // overlaps G5/G6: the next chunk's log-decay sums from its staged rows
-            failed = !wait_G(ci + 1, 1);
-            if (failed) break;
-            scan_G(ci + 1);
+        bool gok = true;
+        if (ci + 1 < ce) {  // the next chunk's log-decay sums, on warps 8-15 while G5/G6 are issued
+            if (warp >= 8) {
+                if (warp == 8) gok = mbar_wait(&bars[4], (uint32_t)((ci + 1 - cb) & 1));
+                scan_sync();  // the g rows have landed
+                scan_G_half(ci + 1);
+            }
+            cp_async_wait_all();  // beta (threads 64-127)
         }
-        failed = wait_mma(&bars[3], par, warp == 0);
-        if (failed) break;
+        {
+            bool ok = true;
+            if (warp == 0) ok = mbar_wait(&bars[3], par);
+            failed = __syncthreads_or(!ok || !gok) != 0;
+        }
+        if (failed) break;  // (the exit path waits for the g rows again, bounded)
+        if (ci + 1 < ce) pend_clear(0);
         fence_after_sync();
 
         // ------------------------------------------------ H: state update, output epilogue
