@@ -148,6 +148,12 @@ typedef struct {
 
 #define KDA_FLAG_FORCE_SIMT 1    /* take the fp32 SIMT path even where tensor cores apply */
 #define KDA_FLAG_NO_RECURRENT 2  /* never take the recurrent short-sequence path (below) */
+/* Test only: on the tensor-core path, the staging of each CTA's first q/k rows is never
+ * issued, so the mbarrier wait for them runs out (after about 2 s of GPU clock); the kernel
+ * then writes KDA_ERR_TIMEOUT to *d_status and returns without writing out or final_state.
+ * Exercises the device-side timeout path without a fault or a hang; ignored by the other
+ * paths. */
+#define KDA_FLAG_TEST_DROP_STAGING 4
 
 /* Paths of kda_prefill (reported by kda_prefill_plan):
  *  KDA_PATH_SIMT         fp32 SIMT chunkwise path (any D, chunk, dtype);

@@ -21,10 +21,11 @@ KDA_BF16 = 0
 KDA_FP32 = 1
 KDA_FLAG_FORCE_SIMT = 1
 KDA_FLAG_NO_RECURRENT = 2
+KDA_FLAG_TEST_DROP_STAGING = 4
 KDA_PATH_SIMT, KDA_PATH_TENSOR_CORE, KDA_PATH_RECURRENT = 0, 1, 2
 KDA_RECURRENT_MAX_LEN = 8
 KDA_MAX_SEGMENTS = 16
-ABI_VERSION = 10100  # kda_prefill_args with the `segments` field
+ABI_VERSION = 10200  # kda_prefill_args with the `segments` field; KDA_FLAG_TEST_DROP_STAGING
 
 # Every symbol include/kda.h declares.
 EXPORTED = ("kda_status_string", "kda_last_error", "kda_version", "kda_short_conv",

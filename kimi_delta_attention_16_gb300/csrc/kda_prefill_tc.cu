@@ -247,7 +247,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
              const bf16* __restrict__ gate, const float* __restrict__ rms_w, float eps_l2,
              float eps_rms, float scale, const float* __restrict__ S0, float* __restrict__ S_fin,
              To* __restrict__ out, const int32_t* __restrict__ cu, int64_t T_total, int H,
-             int* d_status, SegPlan sp, const __grid_constant__ TmaMaps maps) {
+             int* d_status, SegPlan sp, const __grid_constant__ TmaMaps maps, int flags) {
     extern __shared__ uint8_t smem_raw[];
     // G1 done, G3 done, G4 done, G5+G6 done; staged rows landed: g (next chunk), q/k (next
     // chunk), v/gate (this chunk)
@@ -347,6 +347,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     // q/k rows t0-3 .. t0+63 of chunk cj -> B3 region, four boxes from thread 32 wq (rows
     // outside the tensor read as zero; rows of a neighbouring sequence are never used)
     auto stage_qk = [&](int64_t cj, int wq) {
+        if (cj == cb && (flags & KDA_FLAG_TEST_DROP_STAGING)) return;  // test only: never arrives
         if (tid == 32 * wq) {
             const int y = (int)(s0 + (int64_t)cj * kC - 3), x = h * kD;
             mbar_expect_tx(&bars[5], 4 * kRawRows * 128);
@@ -1382,7 +1383,7 @@ cudaError_t tc_launch(const kda_prefill_args& a, const SegPlan& sp, cudaStream_t
     kern<<<grid, kThreads, kSmemBytes, s>>>(
         (const bf16*)a.q, (const bf16*)a.k, (const bf16*)a.v, xs, a.conv_w, (const bf16*)a.conv_state_in,
         a.g, a.beta, (const bf16*)a.gate, a.rms_w, a.eps_l2, a.eps_rms, a.scale, a.initial_state,
-        a.final_state, (To*)a.out, a.cu_seqlens, a.T_total, a.H, a.d_status, sp, maps);
+        a.final_state, (To*)a.out, a.cu_seqlens, a.T_total, a.H, a.d_status, sp, maps, a.flags);
     return cudaGetLastError();
 }
 

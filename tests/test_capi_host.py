@@ -35,7 +35,20 @@ def test_status_strings_and_version():
     lib = _lib.load()
     assert lib.kda_status_string(0) == b"ok"
     assert b"workspace" in lib.kda_status_string(_lib.KDA_ERR_WORKSPACE)
-    assert lib.kda_version() >= 10000
+    assert lib.kda_version() >= _lib.ABI_VERSION
+
+
+def test_header_constants_match_the_binding():
+    """Every #define and enum value of kda.h that the binding mirrors has the same value."""
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    defines = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define\s+(KDA_[A-Z_0-9]+)\s+(\d+)", src)}
+    enums = {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(KDA_[A-Z_0-9]+)\s*=\s*(\d+)", src)}
+    consts = {**enums, **defines}
+    mirrored = [n for n in dir(_lib) if n.startswith("KDA_") and isinstance(getattr(_lib, n), int)]
+    assert "KDA_FLAG_TEST_DROP_STAGING" in mirrored
+    for n in mirrored:
+        if n in consts:
+            assert getattr(_lib, n) == consts[n], n
 
 
 def _args(**kw):

@@ -217,6 +217,30 @@ def test_device_side_cu_check_flags_status():
     assert int(status.item()) == _lib.KDA_ERR_DEVICE_ARG
 
 
+def test_dropped_staging_times_out_and_reports():
+    """Failure detection without a fault: with KDA_FLAG_TEST_DROP_STAGING the tensor-core
+    kernel never issues its first q/k row staging, its bounded mbarrier wait runs out, and it
+    writes KDA_ERR_TIMEOUT to d_status and returns.  The context stays usable: the same call
+    without the flag then matches the oracle."""
+    inp = synth.make_prefill("layer_8k", seed=3, device=DEV, N=1, T=200, H=1, s0_std=0.02)
+    assert kda.kda_prefill_plan(inp.T, inp.H, inp.D, N=inp.N)[0] == "tc"
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda.kda_prefill(inp.q, inp.k, inp.v, inp.conv_w, inp.g, inp.beta, inp.cu_seqlens, gate=inp.gate,
+                    rms_w=inp.rms_w, initial_state=inp.initial_state, d_status=status,
+                    flags=_lib.KDA_FLAG_TEST_DROP_STAGING)
+    torch.cuda.synchronize()
+    assert int(status.item()) == _lib.KDA_ERR_TIMEOUT
+    status.zero_()
+    out, fin = kda.kda_prefill(inp.q, inp.k, inp.v, inp.conv_w, inp.g, inp.beta, inp.cu_seqlens,
+                               gate=inp.gate, rms_w=inp.rms_w, initial_state=inp.initial_state,
+                               d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle_prefill(inp)
+    check_out(to_np(out), ref["out"], 1, TOL_OUT_BF16, True)
+    assert per_head_rel(to_np(fin), ref["final_state"], 1).max() <= TOL_STATE_BF16
+
+
 # --------------------------------------------------------------------------- decode
 
 @pytest.mark.parametrize("D,io", [(128, "bf16"), (64, "bf16"), (16, "fp32"), (32, "fp32")])
