@@ -241,6 +241,56 @@ def test_dropped_staging_times_out_and_reports():
     assert per_head_rel(to_np(fin), ref["final_state"], 1).max() <= TOL_STATE_BF16
 
 
+def _guarded(shape, dtype, guard, fill):
+    """A tensor of `shape` inside a 1-D buffer with `guard` elements of `fill` on each side."""
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * guard,), fill, dtype=dtype, device=DEV)
+    return buf, buf[guard:guard + n].view(shape)
+
+
+@pytest.mark.parametrize("case", ["tensor_core_segments", "simt_fp32", "recurrent"])
+def test_guard_bands_and_poisoned_workspace(case):
+    """Every output lives inside guard bands that must come back untouched, and the workspace
+    is filled with NaN bytes (0xFF) first: a write out of bounds changes a guard, a read of
+    scratch the call did not write puts a NaN into the result."""
+    if case == "tensor_core_segments":
+        inp = synth.make_prefill("layer_8k", seed=81, device=DEV, N=1, T=64 * 20 + 13, H=2, s0_std=0.02,
+                                 conv_state=True, g_range=(-0.05, 0.0))
+        segments, path = 3, "tc"
+    elif case == "simt_fp32":
+        inp = synth.make_prefill("layer_8k", seed=82, device=DEV, lengths=[70, 1, 130], H=2, io="fp32",
+                                 s0_std=0.02, conv_state=True)
+        segments, path = 0, "simt"
+    else:
+        inp = synth.make_prefill("layer_8k", seed=83, device=DEV, lengths=[3, 8, 1], H=2, s0_std=0.02,
+                                 conv_state=True)
+        segments, path = 0, "recurrent"
+    assert kda.kda_prefill_plan(inp.T, inp.H, inp.D, N=inp.N, io=inp.q.dtype, segments=segments,
+                                cu_seqlens=inp.cu_seqlens)[0] == path
+    G = 4096
+    dt = inp.q.dtype
+    out_buf, out = _guarded((inp.T, inp.H, inp.D), dt, G, -7.0)
+    fin_buf, fin = _guarded((inp.N, inp.H, inp.D, inp.D), torch.float32, G, -7.0)
+    cso_buf, cso = _guarded((inp.N, 3 * inp.H * inp.D, 3), dt, G, -7.0)
+    n_ws = kda.kda_prefill_workspace_size(inp.T, inp.H, inp.D, N=inp.N, io=dt, segments=segments)
+    ws_buf = torch.full((n_ws + 2 * G,), 0xFF, dtype=torch.uint8, device=DEV)
+    ws = ws_buf[G:G + n_ws]
+    kda.kda_prefill(inp.q, inp.k, inp.v, inp.conv_w, inp.g, inp.beta, inp.cu_seqlens, chunk=inp.chunk,
+                    gate=inp.gate, rms_w=inp.rms_w, initial_state=inp.initial_state, final_state=fin,
+                    conv_state_in=inp.conv_state_in, conv_state_out=cso, out=out, workspace=ws,
+                    segments=segments)
+    torch.cuda.synchronize()
+    for buf in (out_buf, fin_buf, cso_buf):
+        assert bool((buf[:G] == -7.0).all()) and bool((buf[-G:] == -7.0).all())
+    assert bool((ws_buf[:G] == 0xFF).all()) and bool((ws_buf[-G:] == 0xFF).all())
+    assert bool(torch.isfinite(out.float()).all()) and bool(torch.isfinite(fin).all())
+    ref = oracle_prefill(inp)
+    tol_o, tol_s = (TOL_FP32, TOL_FP32) if dt == torch.float32 else (TOL_OUT_BF16, TOL_STATE_BF16)
+    check_out(to_np(out), ref["out"], 1, tol_o, bf16_out=dt == torch.bfloat16)
+    assert per_head_rel(to_np(fin), ref["final_state"], 1).max() <= tol_s
+    np.testing.assert_array_equal(synth.to_f32_numpy(cso), ref["conv_state_out"].astype(np.float32))
+
+
 # --------------------------------------------------------------------------- decode
 
 @pytest.mark.parametrize("D,io", [(128, "bf16"), (64, "bf16"), (16, "fp32"), (32, "fp32")])
