@@ -104,12 +104,12 @@ kda_status kda_short_conv(const void* x, int64_t x_row_stride, const float* w,
 
 /* ------------------------------------------------------------------------
  * kda_prefill -- the whole layer over packed variable-length sequences.
- * Page "Kimi K3 / Architecture", KDA panel: "recurrent across chunks,
- * parallel within a chunk", "dense Tensor Core tiles in the chunkwise
- * form"; page "Animated Kimi K3 architecture diagram": "carry S across
- * chunks".  Chunks of `chunk` tokens start at every sequence start; the last
- * chunk of a sequence may be partial.  The result does not depend on `chunk`
- * beyond rounding.
+ * Page "Kimi K3 / Architecture", KDA panel: the chunkwise form (the state
+ * recurs from chunk to chunk, the tokens of a chunk are taken together as
+ * dense tensor-core tiles); page "Animated Kimi K3 architecture diagram": the
+ * state is carried across chunks.  Chunks of `chunk` tokens start at every
+ * sequence start; the last chunk of a sequence may be partial.  The result
+ * does not depend on `chunk` beyond rounding.
  * ------------------------------------------------------------------------ */
 typedef struct {
     int N;                 /* sequences */
@@ -236,7 +236,7 @@ kda_status kda_prefill_noalloc(const kda_prefill_args* args, kda_stream_t stream
 /* ------------------------------------------------------------------------
  * kda_decode_step -- one new token for each of N sequences, states updated
  * in place.  Page "Kimi K3 / Architecture", panel "KDA short convolution":
- * "AUTOREGRESSIVE ROLLING STATE, previous 3 values / channel"; page
+ * the rolling state keeps the previous 3 raw values of every channel; page
  * "Animated Kimi K3 architecture diagram": the four moves on one token.
  * ------------------------------------------------------------------------ */
 typedef struct {

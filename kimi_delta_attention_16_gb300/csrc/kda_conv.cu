@@ -4,7 +4,7 @@
 // Page "Kimi K3 / Architecture", panel "KDA short convolution . one channel c
 // at token t": a width-4 causal window over x[t-3..t] of one channel, only
 // time is mixed, left padding keeps the length, SiLU after the 4-tap sum,
-// then "Q,K -> L2 normalize, V -> write content"; the autoregressive rolling
+// then q and k are L2-normalised and v is written as it is; the autoregressive rolling
 // state keeps the previous 3 values of every channel.
 //
 // Layout: each row of x / y holds 3*H*D channels (q | k | v, channel =

@@ -2,8 +2,9 @@
 // RMSNorm + sigmoid-gate epilogue.
 //
 // Page "Kimi K3 / Architecture", panel "Kimi Delta Attention . one head at
-// token t": "recurrent across chunks, parallel within a chunk"; page
-// "Animated Kimi K3 architecture diagram": "carry S across chunks".  Within a
+// token t": the state recurs from chunk to chunk while the tokens of a chunk are
+// taken together; page "Animated Kimi K3 architecture diagram": the state is
+// carried across chunks.  Within a
 // chunk of Lc tokens (local index r, G_r = sum_{s<=r} g_s per key channel,
 // w_i = beta_i e_i):
 //   A_ri = beta_r sum_c k_rc k_ic e^{G_rc - G_ic}        (i < r)

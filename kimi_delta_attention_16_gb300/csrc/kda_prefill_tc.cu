@@ -1,9 +1,10 @@
 // kda_prefill_tc.cu -- fused KDA prefill on the Blackwell tensor cores
 // (tcgen05, accumulators in tensor memory), D = 128, chunk C = 64, bf16 inputs.
 //
-// Page "Kimi K3 / Architecture", KDA panel: "recurrent across chunks, parallel
-// within a chunk", "dense Tensor Core tiles in the chunkwise form"; page
-// "Animated Kimi K3 architecture diagram": "carry S across chunks".
+// Page "Kimi K3 / Architecture", KDA panel: the chunkwise form, in which the
+// state recurs from chunk to chunk and the tokens of a chunk are taken together
+// as dense tensor-core tiles; page "Animated Kimi K3 architecture diagram": the
+// state is carried across chunks.
 //
 // One CTA owns one (sequence, head) and walks its chunks in order; every
 // stage of the layer runs inside it (conv + SiLU + L2, the chunk algebra,

@@ -104,7 +104,8 @@ int kda_oracle_conv_silu(int64_t T_total, int n_ch, const float* x, int64_t x_st
     return 0;
 }
 
-/* [P1] KDA panel "Swish -> L2 norm, 128-d per head": x <- x / sqrt(sum x^2 + eps). */
+/* [P1] KDA panel: q and k are L2-normalised after the activation, per 128-channel
+ * head: x <- x / sqrt(sum x^2 + eps). */
 static void l2norm_vec(int d, double* x, double eps)
 {
     double ss = 0.0;
@@ -118,7 +119,7 @@ void kda_oracle_l2norm(int64_t n_rows, int d, double* x, int64_t row_stride, dou
     for (int64_t r = 0; r < n_rows; ++r) l2norm_vec(d, x + r * row_stride, eps);
 }
 
-/* [P1] KDA panel "head RMSNorm, sigma gate full rank":
+/* [P1] KDA panel: RMSNorm per head, then a sigmoid output gate with one value per channel:
  * y = o / sqrt(mean(o^2) + eps) * w * sigmoid(gate); w NULL = ones, gate NULL = no gate. */
 static void rmsnorm_gate_vec(int d, const double* o, const double* gate, const double* w,
                              double eps, double* y)
@@ -142,7 +143,7 @@ void kda_oracle_rmsnorm_gate(int64_t n_rows, int d, const double* o, const doubl
 }
 
 /* ------------------------------------------------------------------------ */
-/* Token-sequential gated delta rule, [P2] four moves, [P1] "StTqt read".     */
+/* Token-sequential gated delta rule, [P2] four moves, [P1] readout S_t^T q_t. */
 /* S: [Dk][Dv] row-major (row = key channel), updated in place.               */
 /*   DECAY   S_bar = Diag(alpha_t) S,  alpha_t = exp(g_t)                      */
 /*   PROBE   k_t reads S_bar:  S_bar^T k_t                                     */
@@ -192,8 +193,9 @@ int kda_oracle_recurrence(int64_t L, int Dk, int Dv, const double* q, int64_t qs
 }
 
 /* ------------------------------------------------------------------------ */
-/* Chunkwise form, [P1] "recurrent across chunks, parallel within a chunk",   */
-/* [P2] "carry S across chunks".  A second, independent fp64 form of the same */
+/* Chunkwise form, [P1] KDA panel: the state recurs from chunk to chunk while */
+/* the tokens of a chunk are taken together; [P2] the state is carried across */
+/* chunks.  A second, independent fp64 form of the same                       */
 /* recurrence.  Within a chunk of Lc tokens, local index r, with             */
 /* G_r = sum_{s<=r} g_s (per key channel) and w_i = beta_i e_i:              */
 /*   S_r   = Diag(e^{G_r}) S0 + sum_{i<=r} Diag(e^{G_r - G_i}) k_i w_i^T      */
