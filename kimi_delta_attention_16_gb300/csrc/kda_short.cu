@@ -474,55 +474,58 @@ k_prefill_short_pipe(const Tio* __restrict__ q, const Tio* __restrict__ k, const
         };
         // ---- token loop, one barrier per token: the readout of token tau - 1 (before the decay)
         // and the decay and probe of token tau share one pass over the state registers
+        // (row pairs in packed fp32: two partial sums per dot product)
         for (int tau = 0; tau < L; ++tau) {
             const int buf = tau & 1;
             const float ik = snorm[tau][1];
             const float iqp = tau > 0 ? snorm[tau - 1][0] * scale : 0.f;
-            float p = 0.f, po = 0.f;
+            f2 p2 = f2_dup(0.f), po2 = f2_dup(0.f);
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
                 const float4 kq = *reinterpret_cast<const float4*>(&sx[tau][1][r0 + 4 * e4]);
                 const float4 al = *reinterpret_cast<const float4*>(&salpha[tau][r0 + 4 * e4]);
-                const float kk[4] = {kq.x, kq.y, kq.z, kq.w}, aa[4] = {al.x, al.y, al.z, al.w};
+                f2 s01 = f2_of(s[4 * e4], s[4 * e4 + 1]), s23 = f2_of(s[4 * e4 + 2], s[4 * e4 + 3]);
                 if (tau > 0) {
                     const float4 qq = *reinterpret_cast<const float4*>(&sx[tau - 1][0][r0 + 4 * e4]);
-                    const float qv[4] = {qq.x, qq.y, qq.z, qq.w};
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) po = fmaf(qv[m], s[4 * e4 + m], po);
+                    po2 = fma2(f2_of(qq.x, qq.y), s01, po2);
+                    po2 = fma2(f2_of(qq.z, qq.w), s23, po2);
                 }
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    s[4 * e4 + m] *= aa[m];
-                    p = fmaf(kk[m], s[4 * e4 + m], p);
-                }
+                s01 = mul2(s01, f2_of(al.x, al.y));
+                s23 = mul2(s23, f2_of(al.z, al.w));
+                p2 = fma2(f2_of(kq.x, kq.y), s01, p2);
+                p2 = fma2(f2_of(kq.z, kq.w), s23, p2);
+                s[4 * e4] = f2_lo(s01);
+                s[4 * e4 + 1] = f2_hi(s01);
+                s[4 * e4 + 2] = f2_lo(s23);
+                s[4 * e4 + 3] = f2_hi(s23);
             }
-            sredP[buf][rg][c] = p * ik;
-            if (tau > 0) sredO[buf][rg][c] = po * iqp;
+            sredP[buf][rg][c] = (f2_lo(p2) + f2_hi(p2)) * ik;
+            if (tau > 0) sredO[buf][rg][c] = (f2_lo(po2) + f2_hi(po2)) * iqp;
             __syncthreads();
             const float ev = sx[tau][2][c] - (sredP[buf][0][c] + sredP[buf][1][c] + sredP[buf][2][c] + sredP[buf][3][c]);
-            const float bb = sbeta[b][tau] * ik * ev;
+            const f2 bb = f2_dup(sbeta[b][tau] * ik * ev);
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
                 const float4 kq = *reinterpret_cast<const float4*>(&sx[tau][1][r0 + 4 * e4]);
-                s[4 * e4 + 0] = fmaf(bb, kq.x, s[4 * e4 + 0]);
-                s[4 * e4 + 1] = fmaf(bb, kq.y, s[4 * e4 + 1]);
-                s[4 * e4 + 2] = fmaf(bb, kq.z, s[4 * e4 + 2]);
-                s[4 * e4 + 3] = fmaf(bb, kq.w, s[4 * e4 + 3]);
+                const f2 s01 = fma2(bb, f2_of(kq.x, kq.y), f2_of(s[4 * e4], s[4 * e4 + 1]));
+                const f2 s23 = fma2(bb, f2_of(kq.z, kq.w), f2_of(s[4 * e4 + 2], s[4 * e4 + 3]));
+                s[4 * e4] = f2_lo(s01);
+                s[4 * e4 + 1] = f2_hi(s01);
+                s[4 * e4 + 2] = f2_lo(s23);
+                s[4 * e4 + 3] = f2_hi(s23);
             }
             if (tau > 0 && warp == 0) emit(tau - 1, buf);
         }
         if (L > 0) {  // readout of the last token
             const int buf = L & 1;
-            float po = 0.f;
+            f2 po2 = f2_dup(0.f);
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
                 const float4 qq = *reinterpret_cast<const float4*>(&sx[L - 1][0][r0 + 4 * e4]);
-                po = fmaf(qq.x, s[4 * e4 + 0], po);
-                po = fmaf(qq.y, s[4 * e4 + 1], po);
-                po = fmaf(qq.z, s[4 * e4 + 2], po);
-                po = fmaf(qq.w, s[4 * e4 + 3], po);
+                po2 = fma2(f2_of(qq.x, qq.y), f2_of(s[4 * e4], s[4 * e4 + 1]), po2);
+                po2 = fma2(f2_of(qq.z, qq.w), f2_of(s[4 * e4 + 2], s[4 * e4 + 3]), po2);
             }
-            sredO[buf][rg][c] = po * snorm[L - 1][0] * scale;
+            sredO[buf][rg][c] = (f2_lo(po2) + f2_hi(po2)) * snorm[L - 1][0] * scale;
             __syncthreads();
             if (warp == 0) emit(L - 1, buf);
         }
