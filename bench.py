@@ -242,21 +242,7 @@ def run_ours(args):
     tokens_per_s = aggregate_rate(world, T, ms_max)
 
     # roofline of the prefill launch(es)
-    fl = PREFILL_FLOP_PER_TOKEN_HEAD.get((D, inp.chunk), 0) * T * H
-    state_bytes = N * H * D * D * 4 * (2 if inp.initial_state is not None else 1)
-    alg_bytes = T * H * PREFILL_BYTES_PER_TOKEN_HEAD_BF16 + state_bytes
-    gbs = alg_bytes / (ms / 1e3) / 1e9
-    tflops = fl / (ms / 1e3) / 1e12
-    kname = ("fused tcgen05 chunk kernel" if segments == 1 else
-             f"fused tcgen05 chunk kernel, {segments} segments per sequence + composition + fix-up"
-             ) if path == "tc" else "SIMT path: conv + chunk recurrence + epilogue"
-    roof = {"kernel": "kda_prefill (" + kname + ")",
-            "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": peak_src,
-            "traffic": recorded_traffic(f"prefill_{path}_{args.workload}"),
-            "algorithmic_bytes": alg_bytes, "algorithmic_flops": fl,
-            "tensor_tflops": round(tflops, 1),
-            "tensor_frac": round(tflops / peaks["bf16_tflops"], 4)}
+    roof = prefill_roofline(inp, ms, path, segments, peaks, peak_src, args.workload)
 
     # end to end: every step copies its inputs from pinned host memory, runs kda_prefill and
     # reads its output and final state back.  The host link carries ~1.4 GB per step at about
@@ -370,6 +356,14 @@ def run_ours(args):
     mt_launches = 0
     if args.verify_steps > 0:
         mt_obj, mt_launches = time_multi_token(args, pg, dev, stream, peaks, peak_src, world)
+    # the other two prefill workloads, each its own nested key
+    extra, extra_launches = {}, 0
+    if args.extra_workloads and args.mode == "all" and not args.tokens:
+        for name in ("varlen_16", "long_1m"):
+            if name == args.workload:
+                continue
+            extra[name], nl = time_prefill_workload(name, args, pg, dev, stream, peaks, peak_src, world)
+            extra_launches += nl
     clk = clocks.stop()
 
     cpu = None
@@ -394,11 +388,75 @@ def run_ours(args):
                         "ms_per_step": round(e2e_ms, 4),
                         "note": "pinned host buffers; copies on their own streams, double-"
                                 "buffered and overlapped with the neighbouring steps' compute"},
-                "decode": dec_obj, "multi_token_decode": mt_obj, "cpu_baseline": cpu, "clocks": clk,
-                "gpu_launches": prefill_launches(path, segments) * args.steps + dec_launches + mt_launches}
+                "decode": dec_obj, "multi_token_decode": mt_obj, **extra, "cpu_baseline": cpu,
+                "clocks": clk,
+                "gpu_launches": (prefill_launches(path, segments) * args.steps + dec_launches + mt_launches +
+                                 extra_launches)}
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+
+
+def prefill_roofline(inp, ms, path, segments, peaks, peak_src, workload):
+    """Roofline object of one kda_prefill call: algorithmic bytes (and FLOPs) / CUDA-event time."""
+    T, H, D, N = inp.T, inp.H, inp.D, inp.N
+    fl = PREFILL_FLOP_PER_TOKEN_HEAD.get((D, inp.chunk), 0) * T * H
+    state_bytes = N * H * D * D * 4 * (2 if inp.initial_state is not None else 1)
+    alg_bytes = T * H * PREFILL_BYTES_PER_TOKEN_HEAD_BF16 + state_bytes
+    gbs = alg_bytes / (ms / 1e3) / 1e9
+    tflops = fl / (ms / 1e3) / 1e12
+    kname = ("fused tcgen05 chunk kernel" if segments == 1 else
+             f"fused tcgen05 chunk kernel, {segments} segments per sequence + composition + fix-up"
+             ) if path == "tc" else "SIMT path: conv + chunk recurrence + epilogue"
+    return {"kernel": "kda_prefill (" + kname + ")",
+            "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_source": peak_src,
+            "traffic": recorded_traffic(f"prefill_{path}_{workload}"),
+            "algorithmic_bytes": alg_bytes, "algorithmic_flops": fl,
+            "tensor_tflops": round(tflops, 1),
+            "tensor_frac": round(tflops / peaks["bf16_tflops"], 4)}
+
+
+def time_prefill_workload(name, args, pg, dev, stream, peaks, peak_src, world):
+    """One more prefill workload (varlen_16 or long_1m), inputs resident in HBM, timed like the
+    headline: warm-up calls, then K calls between CUDA events; returns (object, launches)."""
+    import torch
+    import kimi_delta_attention_16_gb300 as kda
+    from kimi_delta_attention_16_gb300 import synth
+    inp = synth.make_prefill(name, seed=2 if name == "varlen_16" else 3, device=dev)
+    N, T, H, D = inp.N, inp.T, inp.H, inp.D
+    path, segments, ws_bytes = prefill_path(inp)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    out = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((N, H, D, D), dtype=torch.float32, device=dev)
+    cu_pair = (torch.from_numpy(inp.cu_seqlens).to(dev), inp.cu_seqlens)
+
+    def step():
+        kda.kda_prefill(inp.q, inp.k, inp.v, inp.conv_w, inp.g, inp.beta, cu_pair, chunk=inp.chunk,
+                        gate=inp.gate, rms_w=inp.rms_w, initial_state=inp.initial_state,
+                        final_state=fin, out=out, workspace=ws)
+
+    steps = max(3, min(args.steps, 10))
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(pg)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    ms = max_over_ranks(pg, e0.elapsed_time(e1) / steps, dev)
+    obj = {"metric": f"KDA prefill tokens/s ({name})", "value": round(aggregate_rate(world, T, ms), 1),
+           "unit": "tokens/s", "ms_per_step": round(ms, 4), "steps": steps,
+           "config": {"workload": workload_desc(name), "sequences": N, "tokens": T, "heads": H,
+                      "head_dim": D, "chunk": inp.chunk, "prefill_path": path, "segments": segments},
+           "roofline": prefill_roofline(inp, ms, path, segments, peaks, peak_src, name)}
+    del inp, ws, out, fin
+    torch.cuda.empty_cache()
+    return obj, prefill_launches(path, segments) * steps
 
 
 def time_multi_token(args, pg, dev, stream, peaks, peak_src, world, t_new=4, ring=8):
@@ -565,6 +623,8 @@ def main():
                     help="profiling aid: run only one of the measurements (verify = the "
                          "multi-token decode loop)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-workloads", dest="extra_workloads", action="store_false",
+                    help="skip the nested varlen_16 and long_1m prefill measurements")
     ap.add_argument("--tokens", type=int, default=0,
                     help="profiling aid: total tokens of a shorter case of --workload")
     args = ap.parse_args()

@@ -22,7 +22,7 @@
  *  - Ownership: the caller owns every buffer.  The library allocates nothing
  *    on the device.  Its only device memory of its own is the fixed scratch
  *    array of kda_prefill_noalloc (below), and its only state between calls is
- *    that array's per-device address.
+ *    a per-device cache of device attributes (SM count, compute capability).
  *  - Asynchrony: calls only enqueue work on `stream` (a cudaStream_t; NULL is
  *    the legacy default stream) and never synchronise.
  *  - Errors: invalid arguments return before anything is launched.  A launch
@@ -32,7 +32,10 @@
  *    kernel traps or asserts.
  *  - Value ranges: g is expected in [-5, 0] (the pages bound the log-decay
  *    below by -5) and beta in [0, 1].  They are not range-checked on the
- *    device; g > 0 may overflow.
+ *    device.  Outside that range results may overflow to inf/NaN: on every
+ *    path for g > 0 (growing state), and on the tensor-core path also for
+ *    g < -5, whose split decay factors reach e^{16 |g|} (e^{96} > FLT_MAX at
+ *    g = -6).  Both ends of the range, g = -5 and g = 0, are supported.
  *  - Shapes: D in {16, 32, 64, 128}; the tensor-core prefill path needs
  *    D = 128, chunk = 64 and bf16 inputs, everything else takes the fp32 SIMT
  *    path.
@@ -219,9 +222,11 @@ kda_status kda_prefill_plan(const kda_prefill_args* args, int* path, int* segmen
  * KDA_ERR_WORKSPACE before launching anything (use kda_prefill with a
  * workspace instead).
  *
- * Set-up: the first call on each device looks up the array's device
- * address with that device current; later calls reuse it.  Make that first
- * call before any stream capture begins.
+ * Set-up: every call looks up the array's device address on the current
+ * device (a host-side lookup that allocates nothing), so the address is
+ * right after cudaDeviceReset or under another context too.  The first
+ * lookup in a context also loads the library's device code there: make the
+ * first call on each device before any stream capture begins.
  *
  * Sharing: all calls use the same array, which keeps the previous call's
  * contents.  Nothing in it needs to start at zero (every scratch byte a call

@@ -256,9 +256,23 @@ def kda_prefill_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, conv_
     ``final_state`` are required); the library takes its scratch from a fixed
     array of ``NOALLOC_SCRATCH_BYTES`` per device and allocates nothing.
     Problems needing more scratch than that raise KDAError (status 3).
+
+    ``cu_seqlens`` must already be a prepared pair (int32 CUDA tensor, int32 host
+    array): turning a list or a CPU tensor into a device tensor here would allocate
+    device memory, and reading a device tensor back would synchronise.
     """
     lib = _lib.load()
-    cu_dev, cu_host = _cu_pair(cu_seqlens, q.device)
+    if out is None:
+        raise ValueError("kda_prefill_noalloc allocates nothing: pass `out`")
+    if not (isinstance(cu_seqlens, tuple) and len(cu_seqlens) == 2
+            and isinstance(cu_seqlens[0], torch.Tensor) and cu_seqlens[0].is_cuda
+            and cu_seqlens[0].dtype == torch.int32 and cu_seqlens[0].is_contiguous()):
+        raise ValueError("kda_prefill_noalloc needs cu_seqlens as a prepared "
+                         "(int32 CUDA tensor, int32 host array) pair")
+    cu_dev, cu_host = cu_seqlens
+    cu_host = np.asarray(cu_host)
+    if cu_host.dtype != np.int32 or not cu_host.flags.c_contiguous:
+        raise ValueError("the host half of cu_seqlens must be a contiguous int32 array")
     a = _prefill_args(q, k, v, conv_w, g, beta, cu_dev, cu_host, chunk=chunk, gate=gate,
                       rms_w=rms_w, eps_l2=eps_l2, eps_rms=eps_rms, scale=scale,
                       initial_state=initial_state, final_state=final_state,

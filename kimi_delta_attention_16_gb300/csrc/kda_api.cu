@@ -167,32 +167,41 @@ kda_status validate_prefill(const kda_prefill_args* a) {
 
 // Fixed scratch of kda_prefill_noalloc (see include/kda.h).  In host code
 // this name is only a host-side stand-in: its device address comes from
-// cudaGetSymbolAddress, looked up once per device.
+// cudaGetSymbolAddress with the device current.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 128;
-std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices] = {};
-
-// Device address of the fixed scratch on the current device (looked up on first use).
+// Device address of the fixed scratch on the current device.  Looked up on every call (a
+// host-side lookup, no allocation), so the address is never stale: after cudaDeviceReset, or
+// under another context on the same device, the lookup returns that context's copy.  The
+// first lookup in a context also loads the library's device code there, which is why the
+// first call on each device should come before any stream capture.
 kda_status noalloc_scratch(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= kMaxDevices) return fail(KDA_ERR_UNSUPPORTED, "device ordinal %d", dev);
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(fixed scratch)");
-        if (!p) return fail(KDA_ERR_CUDA, "fixed scratch has no device address");
-        g_noalloc_addr[dev] = p;
-    }
-    *out = g_noalloc_addr[dev];
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(fixed scratch)");
+    if (!p) return fail(KDA_ERR_CUDA, "fixed scratch has no device address");
+    *out = p;
     return KDA_OK;
 }
 
+std::once_flag g_dev_once[kda::kMaxDevices];
+kda::DeviceInfo g_dev_info[kda::kMaxDevices];
+
 }  // namespace
+
+bool kda::current_device_info(kda::DeviceInfo* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kda::kMaxDevices) return false;
+    std::call_once(g_dev_once[dev], [dev] {
+        kda::DeviceInfo d{0, 0, 0};
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+        g_dev_info[dev] = d;
+    });
+    *out = g_dev_info[dev];
+    return out->sm_count > 0;
+}
 
 extern "C" {
 

@@ -389,20 +389,14 @@ k_decode_tma(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int g_sm_count[64];
-
 template <typename Tio, typename To>
 cudaError_t decode_tma_launch(const kda_decode_args& a, cudaStream_t s) {
     using St = DecodeStage<Tio>;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && g_sm_count[dev] == 0)
-        cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
-    const int sms = (dev >= 0 && dev < 64 && g_sm_count[dev] > 0) ? g_sm_count[dev] : 148;
+    DeviceInfo dinfo;
+    const int sms = current_device_info(&dinfo) ? dinfo.sm_count : 148;
     const int units = a.N * a.H;
     auto kern = k_decode_tma<Tio, To>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)St::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)St::kSmem);
     if (e != cudaSuccess) return e;
     const int64_t xs = a.qkv_row_stride ? a.qkv_row_stride : (int64_t)a.H * 128;
     kern<<<units < sms ? units : sms, 256, St::kSmem, s>>>(

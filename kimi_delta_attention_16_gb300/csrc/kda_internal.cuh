@@ -155,6 +155,19 @@ struct QKVParts {
     const void* p[3];
 };
 
+// ------------------------------------------------------------------ device attributes
+// Highest device ordinal + 1 the library serves (its per-device caches are this long).
+constexpr int kMaxDevices = 128;
+struct DeviceInfo {
+    int sm_count;  // streaming multiprocessors
+    int cc_major;  // compute capability
+    int cc_minor;
+};
+// Attributes of the current device, queried once per device (std::call_once, so concurrent
+// first calls from several host threads are race-free) and cached for the process.  False
+// when there is no current device or its ordinal is not below kMaxDevices.
+bool current_device_info(DeviceInfo* out);
+
 // ------------------------------------------------------------------ internal launchers
 // Each returns cudaSuccess or the launch error; arguments are validated by the caller.
 

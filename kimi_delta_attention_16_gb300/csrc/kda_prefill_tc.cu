@@ -34,8 +34,10 @@
 // operand itself that vanishes, so the lost terms are negligible.
 //
 // Precision: every operand is split into bf16 hi + lo parts and products take
-// hi.hi + lo.hi + hi.lo (T . R takes T in bf16 alone), so each contraction is
-// accurate to about 2^-16 relative; the state stays in fp32 registers.
+// hi.hi + lo.hi + hi.lo, so each contraction is accurate to about 2^-16
+// relative; the state stays in fp32 registers.  T is split too: with full-strength
+// writes (beta = 1) and no decay, correlated keys make W = T R cancel, and a bf16 T
+// alone left about 1e-3 of error in the carried state.
 //
 // TMEM (512 columns of 128 lanes):
 //   [  0,128)  S^T operand (hi 0-63, lo 64-127)  |  dS^T accumulator
@@ -86,10 +88,12 @@ constexpr int kTs = 68;    // and of T: conflict-free when 8 lanes read 8 differ
 constexpr uint32_t kOffR1 = kOffKTlo + kTileKT;   // G fp32 (4 swizzled boxes)  |  A fp32 [64][kAs] + T fp32 [64][kTs]
 constexpr uint32_t kR1Bytes = 64 * (kAs + kTs) * 4;
 static_assert(kR1Bytes >= 4 * 8192, "G exceeds R1");
-constexpr uint32_t kOffR2 = kOffR1 + kR1Bytes;     // T bf16 [64][64] | M hi | M lo (K-major, 8 KB each)
+constexpr uint32_t kOffR2 = kOffR1 + kR1Bytes;     // T hi [64][64] | M hi | M lo | T lo (K-major, 8 KB each)
 static_assert(kOffR2 % 1024 == 0, "R2 holds 128-byte-swizzled operand tiles");
 constexpr int kKnS = 132;  // row stride (floats) of the normalized k rows parked in R2 during A3b
-constexpr uint32_t kR2Bytes = 64 * kKnS * 4;       // 33792 >= 3 x 8 KB
+constexpr uint32_t kR2Bytes = 64 * kKnS * 4;       // 33792 >= 4 x 8 KB
+constexpr uint32_t kOffTlo = 24576;                // T lo tile inside R2
+static_assert(kOffTlo + 8192 <= kR2Bytes && kOffTlo % 1024 == 0, "T lo tile exceeds R2");
 constexpr uint32_t kOffMisc = kOffR2 + kR2Bytes;
 // Raw-row staging in operand regions while they are not operands, by 2D TMA boxes with the
 // 128-byte swizzle (a box row is 128 bytes; its 16-byte chunk j sits at chunk j ^ (row & 7),
@@ -558,7 +562,9 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
         // ------------------------------------------------ A3b: L2 norm, decay factors, operand tiles
         {
             const float4 ssv = *reinterpret_cast<const float4*>(&sSS[L * 4]);
-            const float inv = rsqrtf(ssv.x + ssv.y + ssv.z + ssv.w + eps_l2);
+            // rows past the sequence end are zero: give them a zero factor, not 0 * rsqrt(0 + eps)
+            // (which is NaN when eps_l2 = 0 and would reach every token through the MMAs)
+            const float inv = rvalid ? rsqrtf(ssv.x + ssv.y + ssv.z + ssv.w + eps_l2) : 0.f;
             const int hr = r >> 5;
             const float* cA = sConst + (hr ? cA1 : cA0) * kD;
             const float* cE = sConst + (hr ? cE1 : cE0) * kD;
@@ -971,7 +977,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             solver4_sync();
             if (tid < 64) t_quad(3, 0, q_rr, q_jq);
             solver4_sync();
-            // T -> bf16, K-major [r][i]; blocks above the diagonal are zero
+            // T -> bf16 hi and lo, K-major [r][i]; blocks above the diagonal are zero
             for (int idx = tid; idx < 64 * 8; idx += 128) {
                 const int rr = idx >> 3, k8 = idx & 7;
                 const float4 u0 = *reinterpret_cast<const float4*>(&sTf[rr * kTs + 8 * k8]);
@@ -980,12 +986,10 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
                 float t8[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) t8[e] = 8 * k8 + e <= rr ? tv[e] : 0.f;
-                uint4 hv;
-                hv.x = pack_bf16x2(t8[0], t8[1]);
-                hv.y = pack_bf16x2(t8[2], t8[3]);
-                hv.z = pack_bf16x2(t8[4], t8[5]);
-                hv.w = pack_bf16x2(t8[6], t8[7]);
+                uint4 hv, lv;
+                split8(t8, hv, lv);
                 sts128(sTbf, kmajor_off(64, rr, k8), hv);
+                sts128(sTbf + kOffTlo, kmajor_off(64, rr, k8), lv);
             }
             fence_async_smem();
         }
@@ -1073,11 +1077,13 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
             fence_after_sync();
             const uint32_t tbf = sbase + kOffR2;
 #pragma unroll
-            for (int term = 0; term < 2; ++term)
+            for (int term = 0; term < 3; ++term) {  // R hi . T hi, R lo . T hi, R hi . T lo
+                const uint32_t acol = kColR + (term == 1 ? 32 : 0);
+                const uint32_t tt = tbf + (term == 2 ? kOffTlo : 0);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_ts(tb + kColW, tb + kColR + 32 * term + 8 * kk, desc_sw128(tbf + kk * 32, 16, 1024),
-                           id_64, (term | kk) != 0);
+                    mma_ts(tb + kColW, tb + acol + 8 * kk, desc_sw128(tt + kk * 32, 16, 1024), id_64, (term | kk) != 0);
+            }
             mma_commit(&bars[2]);
         }
         // next chunk: g rows and beta into R1 (the solve is done with A and T) and sBeta (D is
@@ -1278,27 +1284,14 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     if (warp == 0) tmem_dealloc(tb, kTmemCols);
 }
 
-int g_tc_arch[64];  // per device: 0 unknown, 1 supported, 2 not supported
-int g_sm_count[64];
-
 bool device_supports_tc() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-    if (g_tc_arch[dev] == 0) {
-        int major = 0, minor = 0, sms = 0;
-        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        g_sm_count[dev] = sms > 0 ? sms : 1;
-        g_tc_arch[dev] = (major == 10 && minor == 3) ? 1 : 2;
-    }
-    return g_tc_arch[dev] == 1;
+    DeviceInfo d;
+    return current_device_info(&d) && d.cc_major == 10 && d.cc_minor == 3;
 }
 
 int device_sm_count() {
-    int dev = 0;
-    if (!device_supports_tc() || cudaGetDevice(&dev) != cudaSuccess) return 1;
-    return g_sm_count[dev];
+    DeviceInfo d;
+    return current_device_info(&d) ? d.sm_count : 1;
 }
 
 // Cost model of the automatic segment choice, in units of one chunk step of one CTA

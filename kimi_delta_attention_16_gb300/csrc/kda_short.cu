@@ -541,13 +541,9 @@ k_prefill_short_pipe(const Tio* __restrict__ q, const Tio* __restrict__ k, const
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int g_short_sms[64];
-
 int device_sms() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (g_short_sms[dev] == 0) cudaDeviceGetAttribute(&g_short_sms[dev], cudaDevAttrMultiProcessorCount, dev);
-    return g_short_sms[dev] > 0 ? g_short_sms[dev] : 148;
+    DeviceInfo d;
+    return current_device_info(&d) ? d.sm_count : 148;
 }
 
 template <typename Tio, typename To>

@@ -15,27 +15,32 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 DEV = "cuda"
 
 
-def _run(inp):
+def _run(inp, out_dtype=None):
     out, fin = kda.kda_prefill(inp.q, inp.k, inp.v, inp.conv_w, inp.g, inp.beta, inp.cu_seqlens,
                                chunk=inp.chunk, gate=inp.gate, rms_w=inp.rms_w,
-                               initial_state=inp.initial_state)
+                               initial_state=inp.initial_state, out_dtype=out_dtype)
     torch.cuda.synchronize()
     return out, fin
 
 
-def _compare(inp, out, fin, heads):
-    ref = oracle_prefill(inp, heads=heads)
+def _compare(inp, out, fin, heads, ref=None):
+    """bf16 `out` gets its own rounding allowance; an fp32 `out` is held to the plain bound."""
+    ref = oracle_prefill(inp, heads=heads) if ref is None else ref
     o = to_np(out[:, heads])
-    check_out(o, ref["out"], 1, TOL_OUT_BF16, bf16_out=True)
+    check_out(o, ref["out"], 1, TOL_OUT_BF16, bf16_out=out.dtype == torch.bfloat16)
     err = per_head_rel(to_np(fin[:, heads]), ref["final_state"], 1)
     assert err.max() <= TOL_STATE_BF16, f"final state err {err.max():.3e}"
+    return ref
 
 
 def test_layer_8k_all_heads():
     """B=1, T=8192, H=96, d=128, chunk 64, bf16 q/k/v/gate, fp32 state: every head."""
     inp = synth.make_prefill("layer_8k", seed=1, device=DEV)
     out, fin = _run(inp)
-    _compare(inp, out, fin, list(range(inp.H)))
+    ref = _compare(inp, out, fin, list(range(inp.H)))
+    # the same call with fp32 outputs, under the plain 2e-3 bound (no rounding allowance)
+    out32, fin32 = _run(inp, out_dtype=torch.float32)
+    _compare(inp, out32, fin32, list(range(inp.H)), ref=ref)
 
 
 def test_varlen_16_sampled_heads():
@@ -46,12 +51,18 @@ def test_varlen_16_sampled_heads():
     _compare(inp, out, fin, [0, 33, 66, 95])
 
 
-def test_long_1m_sampled_head():
-    """B=1, T=1,048,576, H=24, 16384 chunks of 64: the state carried across every chunk
-    of one sampled head, checked at every position and at the end."""
+def test_long_1m_sampled_heads():
+    """B=1, T=1,048,576, H=24, 16384 chunks of 64: the state carried across every chunk of
+    three heads spread over the 24 (first, middle, last), checked at every position and at
+    the end, with bf16 outputs (the benchmarked call) and with fp32 outputs under the plain
+    bound."""
     inp = synth.make_prefill("long_1m", seed=3, device=DEV)
+    heads = [0, 11, 23]
     out, fin = _run(inp)
-    _compare(inp, out, fin, [17])
+    ref = _compare(inp, out, fin, heads)
+    del out, fin
+    out32, fin32 = _run(inp, out_dtype=torch.float32)
+    _compare(inp, out32, fin32, heads, ref=ref)
 
 
 def test_decode_256_sampled_pairs_1000_steps():

@@ -20,7 +20,7 @@ import torch
 
 import kimi_delta_attention_16_gb300 as kda
 from kimi_delta_attention_16_gb300 import _lib, api, synth
-from kda_testlib import TOL_OUT_BF16, TOL_STATE_BF16, per_head_rel, to_np
+from kda_testlib import TOL_OUT_BF16, TOL_STATE_BF16, check_out, oracle_prefill, per_head_rel, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -41,7 +41,8 @@ def _noalloc_call(inp, out, fin, cs_out):
 
 def test_noalloc_matches_prefill_on_two_calls_in_a_row():
     """Two consecutive calls (different inputs, the second reusing the fixed scratch the
-    first one filled) each match the regular entry point within the parity tolerances."""
+    first one filled) each match the regular entry point and the fp64 oracle within the
+    parity tolerances (fp32 outputs, so the plain bound applies)."""
     for call, lengths in enumerate(([100, 37, 200], [65, 1, 129, 64])):
         inp = synth.make_prefill("layer_8k", seed=200 + call, device=DEV, lengths=lengths, H=4,
                                  s0_std=0.02, conv_state=True, rms_w="random")
@@ -59,6 +60,10 @@ def test_noalloc_matches_prefill_on_two_calls_in_a_row():
         assert per_head_rel(to_np(out), to_np(ref_out), 1).max() <= TOL_OUT_BF16
         assert per_head_rel(to_np(fin), to_np(ref_fin), 1).max() <= TOL_STATE_BF16
         assert torch.equal(cs, ref_cs)
+        ref = oracle_prefill(inp)
+        check_out(to_np(out), ref["out"], 1, TOL_OUT_BF16, bf16_out=False)
+        assert per_head_rel(to_np(fin), ref["final_state"], 1).max() <= TOL_STATE_BF16
+        np.testing.assert_array_equal(synth.to_f32_numpy(cs), ref["conv_state_out"].astype(np.float32))
 
 
 def test_noalloc_rejects_problems_beyond_its_fixed_scratch():
