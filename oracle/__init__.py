@@ -241,3 +241,67 @@ def forward(q, k, v, conv_w, cu_seqlens, g, beta, gate=None, rms_w=None, eps_l2=
     if want_o_pre:
         res["o_pre"] = opre
     return res
+
+
+# --------------------------------------------------------------------------- projections around the layer
+# "Kimi K3 / Architecture", KDA panel: the normalized input x_t goes through linear projections
+# to q, k, v and to alpha_t / beta_t (channel-wise retention, one write strength per head, the
+# log-decay bounded below by -5); the head output y_t leaves through W_o.  The gated-MLA panel of
+# the same page writes the output gate as sigmoid(W_g x_t), full rank, one value per channel.
+# Readings (the pages give no activation for alpha and beta): g = -5 sigmoid(z) is the plainest
+# map onto the bounded range (-5, 0); beta = sigmoid(z) onto the write-strength range (0, 1).
+
+def linear(x, w):
+    """x W^T in fp64: x [M, K], w [N, K] (a linear layer's [out, in] weight) -> [M, N]."""
+    return _f64(x) @ _f64(w).T
+
+
+def _sigmoid(z):
+    z = np.asarray(z, dtype=np.float64)
+    e = np.exp(-np.abs(z))             # never overflows
+    return np.where(z >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
+def decay_from_logits(z):
+    """Bounded log-decay g = -5 sigmoid(z), in (-5, 0)."""
+    return -5.0 * _sigmoid(z)
+
+
+def strength_from_logits(z):
+    """Write strength beta = sigmoid(z), in (0, 1)."""
+    return _sigmoid(z)
+
+
+def round_bf16(x):
+    """Round to the nearest bf16 value, ties to even (the layer's bf16 interfaces: gate
+    pre-activations and y leave their producers in bf16).  Returns fp64 values."""
+    f = np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float32))
+    b = f.view(np.uint32).astype(np.uint64)
+    lsb = (b >> 16) & 1
+    r = ((b + 0x7FFF + lsb) >> 16) << 16
+    out = (r & 0xFFFFFFFF).astype(np.uint32).view(np.float32)
+    return np.where(np.isfinite(f), out, f).astype(np.float64)
+
+
+def projected_layer(x, w_alpha, w_beta, w_gate, w_out, q, k, v, conv_w, cu_seqlens, rms_w=None,
+                    eps_l2=1e-6, eps_rms=1e-6, scale=1.0, initial_state=None, conv_state_in=None):
+    """The layer with its projections: g = -5 sigmoid(x W_alpha^T), beta = sigmoid(x W_beta^T),
+    gate = x W_g^T (rounded to bf16, the prefill's gate input dtype), y = the KDA layer, then
+    out = y W_o^T with y rounded to bf16 first (the projection's input dtype).  q, k, v are the
+    raw projections (inputs here).  Shapes: x [T, d_model]; w_alpha [H*D, d_model]; w_beta
+    [H, d_model]; w_gate [H*D, d_model]; w_out [d_out, H*D].  Returns a dict with g, beta,
+    gate, y, out (fp64) and final_state."""
+    q = np.asarray(q)
+    T, H, D = q.shape
+    g = decay_from_logits(linear(x, w_alpha)).reshape(T, H, D)
+    beta = strength_from_logits(linear(x, w_beta)).reshape(T, H)
+    gate = round_bf16(linear(x, w_gate)).reshape(T, H, D)
+    g32 = g.astype(np.float32)           # the prefill takes g and beta in fp32
+    b32 = beta.astype(np.float32)
+    res = forward(q, k, v, conv_w, cu_seqlens, g32, b32, gate=gate.astype(np.float32), rms_w=rms_w,
+                  eps_l2=eps_l2, eps_rms=eps_rms, scale=scale, initial_state=initial_state,
+                  conv_state_in=conv_state_in)
+    y = res["out"]
+    out = linear(round_bf16(y).reshape(T, H * D), w_out)
+    return {"g": g, "beta": beta, "gate": gate, "y": y, "out": out,
+            "final_state": res["final_state"]}

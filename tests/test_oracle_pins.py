@@ -362,3 +362,74 @@ def test_handoff_prefill_prefill_and_decode():
         np.testing.assert_array_equal(step["out"][0], whole["out"][t])
     np.testing.assert_array_equal(st, whole["final_state"])
     np.testing.assert_array_equal(cs, whole["conv_state_out"])
+
+
+# --------------------------------------------------------------------------- projections around the layer
+
+def test_linear_is_the_brute_force_sum():
+    """x W^T by three nested loops on a tiny case, and the identity weight returns x."""
+    rng = np.random.default_rng(11)
+    x, w = rng.standard_normal((3, 5)), rng.standard_normal((4, 5))
+    ref = np.zeros((3, 4))
+    for m in range(3):
+        for n in range(4):
+            for kk in range(5):
+                ref[m, n] += x[m, kk] * w[n, kk]
+    np.testing.assert_allclose(oracle.linear(x, w), ref, rtol=1e-14, atol=1e-14)
+    np.testing.assert_array_equal(oracle.linear(x, np.eye(5)), x)
+
+
+def test_bounded_decay_and_strength_activations():
+    """g = -5 sigmoid(z): -2.5 at 0, the ends of (-5, 0) at the tails, g(z) + g(-z) = -5,
+    increasing towards 0 as z falls; beta = sigmoid(z): 1/2 at 0, beta(z) + beta(-z) = 1,
+    the logistic 1 / (1 + e^-z) at hand-chosen points."""
+    assert oracle.decay_from_logits(0.0) == -2.5
+    z = np.linspace(-30, 30, 121)  # beyond |z| ~ 37 sigmoid(z) rounds to 0 or 1 in fp64
+    g = oracle.decay_from_logits(z)
+    assert np.all(g > -5) and np.all(g < 0)
+    np.testing.assert_allclose(g + oracle.decay_from_logits(-z), -5.0, rtol=0, atol=1e-13)
+    assert np.all(np.diff(g) < 0)
+    assert oracle.decay_from_logits(-800.0) == 0.0 and oracle.decay_from_logits(800.0) == -5.0
+    b = oracle.strength_from_logits(z)
+    np.testing.assert_allclose(b + oracle.strength_from_logits(-z), 1.0, rtol=0, atol=1e-15)
+    for zz in (-3.0, -0.5, 0.0, 1.25, 7.0):
+        assert math.isclose(float(oracle.strength_from_logits(zz)), 1.0 / (1.0 + math.exp(-zz)), rel_tol=1e-15)
+    assert oracle.strength_from_logits(0.0) == 0.5
+
+
+def test_round_bf16_ties_to_even_and_matches_torch():
+    """Hand-worked cases (1 + 2^-8 is a tie -> 1; 1 + 3 * 2^-8 -> 1 + 2^-6; 1 + 2^-7 is exact),
+    and agreement with torch's bf16 cast on random values of every magnitude."""
+    import torch
+    assert oracle.round_bf16(1 + 2 ** -8) == 1.0
+    assert oracle.round_bf16(1 + 3 * 2 ** -8) == 1 + 2 ** -6
+    assert oracle.round_bf16(1 + 2 ** -7) == 1 + 2 ** -7
+    assert oracle.round_bf16(-(1 + 2 ** -8 + 2 ** -20)) == -(1 + 2 ** -7)
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal(4096) * np.exp(rng.uniform(-60, 60, 4096))).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(oracle.round_bf16(x), ref)
+
+
+def test_projected_layer_composes_its_stages():
+    """The layer with its projections is the plain layer fed the activated projections: g and
+    beta from the bounded activations, the gate rounded to bf16, and out = bf16(y) W_o^T."""
+    inp = synth.make_prefill("tiny_fp32", seed=13, lengths=[19, 6], H=2, D=16)
+    a = _np_inputs(inp)
+    T, H, D, dm = 25, 2, 16, 24
+    rng = np.random.default_rng(14)
+    x = rng.standard_normal((T, dm)).astype(np.float32)
+    wa, wb, wg = (rng.standard_normal((n, dm)) / math.sqrt(dm) for n in (H * D, H, H * D))
+    wo = rng.standard_normal((40, H * D)) / math.sqrt(H * D)
+    res = oracle.projected_layer(x, wa, wb, wg, wo, a["q"], a["k"], a["v"], a["conv_w"],
+                                 a["cu_seqlens"], rms_w=a["rms_w"])
+    g = (-5.0 / (1.0 + np.exp(-(x.astype(np.float64) @ wa.T)))).reshape(T, H, D)
+    np.testing.assert_allclose(res["g"], g, rtol=1e-13, atol=1e-15)
+    assert np.all(res["g"] > -5) and np.all(res["g"] < 0)
+    ref = oracle.forward(q=a["q"], k=a["k"], v=a["v"], conv_w=a["conv_w"], cu_seqlens=a["cu_seqlens"],
+                         g=res["g"].astype(np.float32), beta=res["beta"].astype(np.float32),
+                         gate=res["gate"].astype(np.float32), rms_w=a["rms_w"])
+    np.testing.assert_array_equal(res["y"], ref["out"])
+    np.testing.assert_array_equal(res["gate"], oracle.round_bf16(res["gate"]))
+    np.testing.assert_allclose(res["out"], oracle.round_bf16(ref["out"]).reshape(T, H * D) @ wo.T,
+                               rtol=1e-13, atol=1e-13)
