@@ -364,6 +364,8 @@ def run_ours(args):
                 continue
             extra[name], nl = time_prefill_workload(name, args, pg, dev, stream, peaks, peak_src, world)
             extra_launches += nl
+        extra["projected_layer"], nl = time_projected_layer(args, pg, dev, stream, peaks, peak_src, world)
+        extra_launches += nl
     clk = clocks.stop()
 
     cpu = None
@@ -459,6 +461,94 @@ def time_prefill_workload(name, args, pg, dev, stream, peaks, peak_src, world):
     return obj, prefill_launches(path, segments) * steps
 
 
+def time_projected_layer(args, pg, dev, stream, peaks, peak_src, world, d_model=7168):
+    """The layer_8k prefill with the projections around it on the tensor cores: x -> g
+    (-5 sigmoid), beta (sigmoid), gate pre-activations -> kda_prefill -> y -> y W_o.  Weights
+    are random (N(0, 1/fan_in), bf16), x ~ N(0, 1); q, k, v stay the synthetic raw projections.
+    Returns (object, launches)."""
+    import torch
+    import kimi_delta_attention_16_gb300 as kda
+    from kimi_delta_attention_16_gb300 import synth
+    inp = synth.make_prefill("layer_8k", seed=1, device=dev)
+    T, H, D = inp.T, inp.H, inp.D
+    HD = H * D
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+
+    def rnd(n, k, std):
+        return (torch.randn(n, k, generator=gen, device=dev) * std).to(torch.bfloat16)
+
+    x = rnd(T, d_model, 1.0)
+    wa, wb, wg = rnd(HD, d_model, d_model ** -0.5), rnd(H, d_model, d_model ** -0.5), rnd(HD, d_model, d_model ** -0.5)
+    wo = rnd(d_model, HD, HD ** -0.5)
+    g = torch.empty((T, HD), dtype=torch.float32, device=dev)
+    beta = torch.empty((T, H), dtype=torch.float32, device=dev)
+    gate = torch.empty((T, HD), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((T, d_model), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
+    cu_pair = (torch.from_numpy(inp.cu_seqlens).to(dev), inp.cu_seqlens)
+    path, segments, ws_bytes = prefill_path(inp)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    gemms = {
+        "alpha (x W_a^T, -5 sigmoid)": lambda: kda.kda_gemm(x, wa, epilogue="decay", out=g),
+        "beta (x W_b^T, sigmoid)": lambda: kda.kda_gemm(x, wb, epilogue="sigmoid", out=beta),
+        "gate (x W_g^T)": lambda: kda.kda_gemm(x, wg, epilogue="none", out=gate),
+        "output (y W_o^T)": lambda: kda.kda_gemm(y.view(T, HD), wo, epilogue="none", out=out),
+    }
+    flops = {"alpha (x W_a^T, -5 sigmoid)": 2 * T * HD * d_model, "beta (x W_b^T, sigmoid)": 2 * T * H * d_model,
+             "gate (x W_g^T)": 2 * T * HD * d_model, "output (y W_o^T)": 2 * T * d_model * HD}
+
+    def step():
+        for name in ("alpha (x W_a^T, -5 sigmoid)", "beta (x W_b^T, sigmoid)", "gate (x W_g^T)"):
+            gemms[name]()
+        kda.kda_prefill(inp.q, inp.k, inp.v, inp.conv_w, g.view(T, H, D), beta, cu_pair, chunk=inp.chunk,
+                        gate=gate.view(T, H, D), rms_w=inp.rms_w, final_state=fin, out=y, workspace=ws)
+        gemms["output (y W_o^T)"]()
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, n):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        barrier(pg)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(pg)
+        return max_over_ranks(pg, e0.elapsed_time(e1) / n, dev)
+
+    steps = max(3, min(args.steps, 10))
+    per = {}
+    for name, fn in gemms.items():
+        ms = timed(fn, steps)
+        tf = flops[name] / (ms / 1e3) / 1e12
+        per[name] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac": round(tf / peaks["bf16_tflops"], 4)}
+    ms = timed(step, steps)
+    gemm_ms = sum(v["ms"] for v in per.values())
+    gemm_flops = sum(flops.values())
+    gemm_tf = gemm_flops / (gemm_ms / 1e3) / 1e12
+    obj = {"metric": "KDA layer with its projections, tokens/s (layer_8k, d_model 7168)",
+           "value": round(aggregate_rate(world, T, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+           "steps": steps,
+           "config": {"workload": "layer_8k with x [8192, 7168] bf16 ~ N(0,1) and random bf16 weights "
+                                  "N(0, 1/fan_in): W_a, W_g [12288, 7168], W_b [96, 7168], W_o [7168, 12288]; "
+                                  "q, k, v synthetic raw projections", "prefill_path": path, "segments": segments},
+           "gemms": per,
+           "roofline": {"kernel": "k_gemm (tcgen05, 128x256 tiles, 4-stage TMA ring), the four projections",
+                        "bound": "tensor", "achieved": round(gemm_tf, 1), "peak": peaks["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": round(gemm_tf / peaks["bf16_tflops"], 4), "peak_source": peak_src,
+                        "traffic": None, "algorithmic_flops": gemm_flops}}
+    del x, wa, wb, wg, wo, g, beta, gate, y, out, ws, inp
+    torch.cuda.empty_cache()
+    # inside the timed regions: each projection alone, then the whole chain
+    launches = len(gemms) * steps + (len(gemms) + prefill_launches(path, segments)) * steps
+    return obj, launches
+
+
 def time_multi_token(args, pg, dev, stream, peaks, peak_src, world, t_new=4, ring=8):
     """kda_prefill on 256 sequences x t_new tokens continuing from carried states and conv
     states (the recurrent path): the decode workload's inputs, t_new consecutive tokens per
@@ -508,13 +598,13 @@ def time_multi_token(args, pg, dev, stream, peaks, peak_src, world, t_new=4, rin
            "value": round(world / (ms / 1e3), 2), "unit": "steps/s",
            "tokens_per_s": round(world * T / (ms / 1e3), 1), "ms_per_step": round(ms, 4),
            "steps": args.verify_steps, "prefill_path": path,
-           "roofline": {"kernel": "k_prefill_short (recurrent path) + conv-state roll",
+           "roofline": {"kernel": "k_short_tma (recurrent path; rolls the conv state itself)",
                         "bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                         "peak_source": peak_src, "traffic": recorded_traffic("short_verify_256x4"),
                         "algorithmic_bytes": nbytes}}
     del steps_in, dec
-    return obj, 2 * args.verify_steps
+    return obj, args.verify_steps  # one launch per call: the recurrent kernel also rolls the conv state
 
 
 def run_decode_only(args, world, rank, local, pg, dev, peaks, peak_src):

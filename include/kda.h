@@ -266,6 +266,52 @@ typedef struct {
 
 kda_status kda_decode_step(const kda_decode_args* args, kda_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * kda_gemm -- the projections around the layer on the tensor cores, with the
+ * activation of their consumer fused into the epilogue:
+ *
+ *   C[M][N] = epilogue( A[M][K] . W[N][K]^T )
+ *
+ * Page "Kimi K3 / Architecture", KDA panel: the normalized input x_t goes through
+ * linear projections to q, k, v and to alpha_t / beta_t (channel-wise
+ * retention, one write strength per head, log-decay bounded below by -5); the
+ * head output y_t leaves through W_o.  The gated-MLA panel of the same page writes
+ * the output gate as sigmoid(W_g x_t), full rank, one value per output channel.
+ * The pages give no activation for alpha and beta; this library reads "bounded
+ * log-decay >= -5" as g = -5 sigmoid(z) and the write strength as beta =
+ * sigmoid(z), so that g and beta land in the ranges kda_prefill expects.
+ *
+ *   KDA_EPI_NONE     C = acc              (e.g. gate pre-activations x W_g^T, or y W_o^T)
+ *   KDA_EPI_DECAY    C = -5 sigmoid(acc)  (the log-decay g of kda_prefill, fp32)
+ *   KDA_EPI_SIGMOID  C = sigmoid(acc)     (the write strength beta, fp32)
+ *
+ *   A  [M][lda] bf16 row-major (K contiguous); lda >= K, lda * 2 a multiple of 16 bytes.
+ *   W  [N][ldw] bf16 row-major, the [out][in] layout of a linear layer's weight; ldw >= K,
+ *      ldw * 2 a multiple of 16 bytes.
+ *   C  [M][ldc] c_dtype (bf16 or fp32) row-major; ldc >= N; must not overlap A or W.
+ *   K  a positive multiple of 64; M, N >= 0 (any value: ragged tiles are masked).
+ * A, W and C 16-byte aligned.  Accumulation is fp32 on the tensor cores (tcgen05);
+ * the result is rounded once to c_dtype.  Needs an sm_103 device (KDA_ERR_UNSUPPORTED
+ * otherwise).  A wait that times out on the device is reported through d_status
+ * (KDA_ERR_TIMEOUT).
+ * ------------------------------------------------------------------------ */
+typedef enum { KDA_EPI_NONE = 0, KDA_EPI_DECAY = 1, KDA_EPI_SIGMOID = 2 } kda_epilogue;
+
+typedef struct {
+    int M, N, K;
+    const void* A;         /* [M][lda] bf16 */
+    int64_t lda;
+    const void* W;         /* [N][ldw] bf16 */
+    int64_t ldw;
+    void* C;               /* [M][ldc] c_dtype */
+    int64_t ldc;
+    kda_dtype c_dtype;
+    int epilogue;          /* kda_epilogue */
+    int* d_status;         /* optional device int for device-side conditions */
+} kda_gemm_args;
+
+kda_status kda_gemm(const kda_gemm_args* args, kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

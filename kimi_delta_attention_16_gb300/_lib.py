@@ -25,12 +25,13 @@ KDA_FLAG_TEST_DROP_STAGING = 4
 KDA_PATH_SIMT, KDA_PATH_TENSOR_CORE, KDA_PATH_RECURRENT = 0, 1, 2
 KDA_RECURRENT_MAX_LEN = 8
 KDA_MAX_SEGMENTS = 16
-ABI_VERSION = 10200  # kda_prefill_args with the `segments` field; KDA_FLAG_TEST_DROP_STAGING
+KDA_EPI_NONE, KDA_EPI_DECAY, KDA_EPI_SIGMOID = 0, 1, 2
+ABI_VERSION = 10300  # kda_gemm
 
 # Every symbol include/kda.h declares.
 EXPORTED = ("kda_status_string", "kda_last_error", "kda_version", "kda_short_conv",
             "kda_prefill_workspace_size", "kda_prefill", "kda_prefill_plan", "kda_prefill_noalloc",
-            "kda_decode_step")
+            "kda_decode_step", "kda_gemm")
 NOALLOC_SCRATCH_BYTES = 64 << 20  # KDA_NOALLOC_SCRATCH_BYTES in include/kda.h
 
 _vp = ctypes.c_void_p
@@ -67,6 +68,15 @@ class DecodeArgs(ctypes.Structure):
         ("gate", _vp), ("g", _vp), ("beta", _vp), ("conv_w", _vp), ("rms_w", _vp),
         ("eps_l2", _f), ("eps_rms", _f), ("scale", _f),
         ("state", _vp), ("conv_state", _vp), ("out", _vp), ("d_status", _vp),
+    ]
+
+
+class GemmArgs(ctypes.Structure):
+    """Mirror of kda_gemm_args."""
+    _fields_ = [
+        ("M", _int), ("N", _int), ("K", _int),
+        ("A", _vp), ("lda", _i64), ("W", _vp), ("ldw", _i64), ("C", _vp), ("ldc", _i64),
+        ("c_dtype", _int), ("epilogue", _int), ("d_status", _vp),
     ]
 
 
@@ -117,5 +127,7 @@ def load(auto_build: bool = True) -> ctypes.CDLL:
         lib.kda_prefill_noalloc.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
         lib.kda_decode_step.restype = _int
         lib.kda_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
+        lib.kda_gemm.restype = _int
+        lib.kda_gemm.argtypes = [ctypes.POINTER(GemmArgs), _vp]
         _lib = lib
         return lib

@@ -317,3 +317,43 @@ def kda_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.
     if st:
         raise KDAError(st, "kda_decode_step")
     return out
+
+
+_EPI = {"none": _lib.KDA_EPI_NONE, "decay": _lib.KDA_EPI_DECAY, "sigmoid": _lib.KDA_EPI_SIGMOID}
+
+
+def kda_gemm(A: torch.Tensor, W: torch.Tensor, *, epilogue: str = "none",
+             out: Optional[torch.Tensor] = None, out_dtype=None, d_status=None,
+             stream=None) -> torch.Tensor:
+    """C = epilogue(A @ W^T) on the tensor cores: A [M, K] bf16, W [N, K] bf16 (a linear
+    layer's [out, in] weight), K a multiple of 64.  epilogue: "none" (C = A W^T), "decay"
+    (C = -5 sigmoid(A W^T): the bounded log-decay g), "sigmoid" (the write strength beta).
+    C is [M, N] in out_dtype (default bf16 for "none", fp32 otherwise); its rows may be a
+    strided view."""
+    lib = _lib.load()
+    if A.dim() != 2 or W.dim() != 2 or A.shape[1] != W.shape[1]:
+        raise ValueError(f"expected A [M, K] and W [N, K], got {tuple(A.shape)} and {tuple(W.shape)}")
+    if A.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise ValueError("A and W must be bf16")
+    if A.stride(1) != 1 or W.stride(1) != 1:
+        raise ValueError("A and W rows must be contiguous")
+    M, K = A.shape
+    N = W.shape[0]
+    if out is None:
+        dt = out_dtype or (torch.bfloat16 if epilogue == "none" else torch.float32)
+        out = torch.empty((M, N), dtype=dt, device=A.device)
+    if out.shape != (M, N) or out.stride(1) != 1:
+        raise ValueError(f"out must be [{M}, {N}] with contiguous rows")
+    _same_cuda_device(A=A, W=W, out=out, d_status=d_status)
+    g = _lib.GemmArgs()
+    g.M, g.N, g.K = M, N, K
+    g.A, g.lda = A.data_ptr(), A.stride(0) if M else K
+    g.W, g.ldw = W.data_ptr(), W.stride(0) if N else K
+    g.C, g.ldc = out.data_ptr(), out.stride(0) if M else N
+    g.c_dtype = _DT[out.dtype]
+    g.epilogue = _EPI[epilogue]
+    g.d_status = d_status.data_ptr() if d_status is not None else None
+    st = lib.kda_gemm(ctypes.byref(g), _stream(stream))
+    if st:
+        raise KDAError(st, "kda_gemm")
+    return out

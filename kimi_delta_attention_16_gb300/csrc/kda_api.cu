@@ -220,7 +220,7 @@ const char* kda_status_string(int status) {
 
 const char* kda_last_error(void) { return g_last_error.c_str(); }
 
-int kda_version(void) { return 1 * 10000 + 2 * 100 + 0; }
+int kda_version(void) { return 1 * 10000 + 3 * 100 + 0; }
 
 kda_status kda_short_conv(const void* x, int64_t x_row_stride, const float* w,
                           const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int N,
@@ -315,12 +315,15 @@ kda_status kda_prefill(const kda_prefill_args* a, kda_stream_t stream) {
     if (!a->cu_seqlens_host &&
         (e = kda::launch_check_cu(a->cu_seqlens, a->N, a->T_total, a->d_status, s)))
         return cuda_fail(e, "check cu_seqlens");
-    if (a->conv_state_out &&
+    // the pipelined recurrent kernel rolls the conv state itself
+    const bool short_tma = p.path == KDA_PATH_RECURRENT && kda::short_tma_applies(*a);
+    if (a->conv_state_out && !short_tma &&
         (e = kda::launch_conv_state_out(parts, xs, a->io, a->cu_seqlens, a->N, a->T_total,
                                         (int)(3 * HD), a->conv_state_in, a->conv_state_out, s)))
         return cuda_fail(e, "conv state");
     if (p.path == KDA_PATH_RECURRENT) {
-        if ((e = kda::launch_short_prefill(*a, s))) return cuda_fail(e, "recurrent prefill");
+        if ((e = short_tma ? kda::launch_short_tma(*a, s) : kda::launch_short_prefill(*a, s)))
+            return cuda_fail(e, "recurrent prefill");
         return ok();
     }
     if (p.tc) {
@@ -367,6 +370,33 @@ kda_status kda_prefill_noalloc(const kda_prefill_args* args, kda_stream_t stream
         a.workspace_bytes = KDA_NOALLOC_SCRATCH_BYTES;
     }
     return kda_prefill(&a, stream);
+}
+
+kda_status kda_gemm(const kda_gemm_args* g, kda_stream_t stream) {
+    if (!g) return fail(KDA_ERR_INVALID_ARG, "args is NULL");
+    if (g->M < 0 || g->N < 0 || g->K <= 0)
+        return fail(KDA_ERR_INVALID_ARG, "bad sizes M=%d N=%d K=%d", g->M, g->N, g->K);
+    if (g->K % 64) return fail(KDA_ERR_UNSUPPORTED, "K=%d is not a multiple of 64", g->K);
+    if (!valid_dtype(g->c_dtype)) return fail(KDA_ERR_INVALID_ARG, "unknown dtype %d", (int)g->c_dtype);
+    if (g->epilogue < KDA_EPI_NONE || g->epilogue > KDA_EPI_SIGMOID)
+        return fail(KDA_ERR_INVALID_ARG, "unknown epilogue %d", g->epilogue);
+    if (g->M == 0 || g->N == 0) return ok();
+    if (!g->A || !g->W || !g->C) return fail(KDA_ERR_INVALID_ARG, "A, W and C must be non-NULL");
+    if (g->lda < g->K || g->ldw < g->K || g->ldc < g->N)
+        return fail(KDA_ERR_INVALID_ARG, "leading dimensions too small (lda=%lld ldw=%lld ldc=%lld)",
+                    (long long)g->lda, (long long)g->ldw, (long long)g->ldc);
+    if ((g->lda * 2) % 16 || (g->ldw * 2) % 16)
+        return fail(KDA_ERR_INVALID_ARG, "lda and ldw must be multiples of 8 elements");
+    if (!aligned(g->A, 16) || !aligned(g->W, 16) || !aligned(g->C, 16))
+        return fail(KDA_ERR_INVALID_ARG, "A, W and C must be 16-byte aligned");
+    const size_t ab = ((size_t)(g->M - 1) * g->lda + g->K) * 2, wb = ((size_t)(g->N - 1) * g->ldw + g->K) * 2;
+    const size_t cb = ((size_t)(g->M - 1) * g->ldc + g->N) * dsize(g->c_dtype);
+    if (overlap(g->C, cb, g->A, ab) || overlap(g->C, cb, g->W, wb))
+        return fail(KDA_ERR_INVALID_ARG, "C overlaps A or W");
+    if (!kda::gemm_supported_device()) return fail(KDA_ERR_UNSUPPORTED, "kda_gemm needs an sm_103 device");
+    const cudaError_t e = kda::launch_gemm(*g, reinterpret_cast<cudaStream_t>(stream));
+    if (e) return cuda_fail(e, "gemm");
+    return ok();
 }
 
 kda_status kda_decode_step(const kda_decode_args* a, kda_stream_t stream) {

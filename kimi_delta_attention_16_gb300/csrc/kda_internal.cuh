@@ -199,6 +199,10 @@ cudaError_t launch_rms_gate(const float* o, int64_t rows, int D, const void* gat
                             kda_dtype gate_dt, const float* rms_w, float eps, void* out,
                             kda_dtype out_dt, cudaStream_t s);
 
+// Tensor-core projection GEMM with a fused epilogue (arguments validated by the caller).
+bool gemm_supported_device();
+cudaError_t launch_gemm(const kda_gemm_args& g, cudaStream_t s);
+
 // Single-token decode step.
 cudaError_t launch_decode(const kda_decode_args& a, cudaStream_t s);
 
@@ -207,5 +211,9 @@ cudaError_t launch_decode(const kda_decode_args& a, cudaStream_t s);
 constexpr int kShortMaxL = 8;
 bool short_prefill_applies(const kda_prefill_args& a);
 cudaError_t launch_short_prefill(const kda_prefill_args& a, cudaStream_t s);
+// The pipelined TMA kernel of that path (16-byte aligned inputs, T_total > 0): it also writes
+// conv_state_out itself, so no separate conv-state launch is needed when it applies.
+bool short_tma_applies(const kda_prefill_args& a);
+cudaError_t launch_short_tma(const kda_prefill_args& a, cudaStream_t s);
 
 }  // namespace kda

@@ -1345,15 +1345,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // box_c x box_r elements, 128-byte swizzle, zeros outside the tensor.
 bool encode_map(CUtensorMap* m, const void* base, bool fp32, uint64_t cols, uint64_t rows, uint64_t row_bytes,
                 uint32_t box_c, uint32_t box_r) {
-    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {box_c, box_r};
-    const cuuint32_t es[2] = {1, 1};
-    return enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
-               dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_tensor_map_2d(m, base, fp32, cols, rows, row_bytes, box_c, box_r, true);
 }
 
 template <typename To>
@@ -1382,6 +1374,20 @@ cudaError_t tc_launch(const kda_prefill_args& a, const SegPlan& sp, cudaStream_t
 }
 
 }  // namespace
+
+bool encode_tensor_map_2d(CUtensorMap* m, const void* base, bool fp32, uint64_t cols, uint64_t rows,
+                          uint64_t row_bytes, uint32_t box_c, uint32_t box_r, bool swizzle128) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_c, box_r};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+               dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 bool tc_prefill_applies(const kda_prefill_args& a) {
     return a.D == kD && a.chunk == kC && a.io == KDA_BF16 && (int64_t)a.N * a.H <= 0x7fffffffLL &&

@@ -1,9 +1,18 @@
 // kda_tc.cuh -- entry points of the tensor-core (tcgen05) prefill path.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (encoded through the runtime's driver entry point, no libcuda link)
+
 #include "kda_internal.cuh"
 
 namespace kda {
+
+// Encodes a 2D tiled tensor map over a row-major [rows][cols] tensor of bf16 (or fp32)
+// elements with row pitch row_bytes: boxes of box_c x box_r elements, zeros outside the
+// tensor, the 128-byte swizzle or none.  False when the driver entry point is missing or
+// rejects the arguments (base not 16-byte aligned, pitch not a multiple of 16, ...).
+bool encode_tensor_map_2d(CUtensorMap* m, const void* base, bool fp32, uint64_t cols, uint64_t rows,
+                          uint64_t row_bytes, uint32_t box_c, uint32_t box_r, bool swizzle128);
 
 // True when the tensor-core path takes these arguments (D = 128, chunk = 64,
 // bf16 inputs) and this device supports it.

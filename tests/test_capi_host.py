@@ -236,3 +236,44 @@ def test_binding_rejects_host_tensors_before_any_call():
     with pytest.raises(ValueError, match="CUDA device"):
         kda.kda_decode_step(dec.q[0], dec.k[0], dec.v[0], dec.g[0], dec.beta[0], dec.conv_w,
                             dec.state, dec.conv_state, gate=dec.gate[0], rms_w=dec.rms_w)
+
+
+def _gemm_args(**kw):
+    g = _lib.GemmArgs()
+    g.M, g.N, g.K = 128, 256, 128
+    g.A, g.lda = FAKE, 128
+    g.W, g.ldw = FAKE + (1 << 24), 128
+    g.C, g.ldc = FAKE + (1 << 26), 256
+    g.c_dtype = _lib.KDA_BF16
+    g.epilogue = _lib.KDA_EPI_NONE
+    for k, v in kw.items():
+        setattr(g, k, v)
+    return g
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("K", 96, _lib.KDA_ERR_UNSUPPORTED),          # not a multiple of 64
+    ("K", 0, _lib.KDA_ERR_INVALID_ARG),
+    ("M", -1, _lib.KDA_ERR_INVALID_ARG),
+    ("lda", 64, _lib.KDA_ERR_INVALID_ARG),        # < K
+    ("ldw", 132, _lib.KDA_ERR_INVALID_ARG),       # not a multiple of 8 elements
+    ("ldc", 200, _lib.KDA_ERR_INVALID_ARG),       # < N
+    ("A", FAKE + 8, _lib.KDA_ERR_INVALID_ARG),    # misaligned
+    ("A", None, _lib.KDA_ERR_INVALID_ARG),
+    ("C", FAKE + 64, _lib.KDA_ERR_INVALID_ARG),   # overlaps A
+    ("epilogue", 7, _lib.KDA_ERR_INVALID_ARG),
+    ("c_dtype", 5, _lib.KDA_ERR_INVALID_ARG),
+])
+def test_gemm_rejects_bad_arguments(field, value, code):
+    lib = _lib.load()
+    assert lib.kda_gemm(ctypes.byref(_gemm_args(**{field: value})), None) == code
+    assert lib.kda_last_error()
+
+
+def test_gemm_empty_problem_is_a_no_op_and_no_device_is_unsupported():
+    lib = _lib.load()
+    assert lib.kda_gemm(ctypes.byref(_gemm_args(M=0)), None) == _lib.KDA_OK
+    # valid arguments without an sm_103 device in this process: unsupported, nothing launched
+    import torch
+    if not torch.cuda.is_available():
+        assert lib.kda_gemm(ctypes.byref(_gemm_args()), None) == _lib.KDA_ERR_UNSUPPORTED
