@@ -8,6 +8,9 @@
 // S = S_bar + beta k e^T; page "Kimi K3 / Architecture": the short conv with
 // its rolling window, the read o = S^T q, head RMSNorm and the sigmoid gate.
 //
+// This file holds the plain kernel of that path, for inputs the pipelined TMA
+// kernel (kda_short_tma.cu) cannot take because they are not 16-byte aligned.
+//
 // Persistent CTAs (two per SM) walk contiguous head-major ranges of (sequence,
 // head) units.  A unit's D x D fp32 state is read into registers once, takes
 // the sequence's tokens one after another, and is written once; thread
@@ -266,279 +269,6 @@ k_prefill_short(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio*
     }
 }
 
-// ---------------------------------------------------------------------------------------
-// Pipelined variant for 16-byte aligned inputs: one CTA of 512 threads per SM and two stages
-// of shared memory filled by cp.async (every thread copies a few 16-byte pieces).  While a
-// unit computes, the next unit's state slice, conv window and token rows land in the other
-// stage; the state leaves from registers with coalesced stores, so a stage is free as soon as
-// its unit has read it.  Thread (row group rg = warp / 4, column c = 32 (warp % 4) + lane)
-// holds rows 32 rg .. 32 rg + 31 of column c: the sums over rows (S_bar^T k, S^T q) then take
-// four partials per column, and the per-row factors are warp-wide broadcasts.
-template <typename Tio>
-struct PipeStage {
-    static constexpr uint32_t kRowBytes = 128 * sizeof(Tio);
-    static constexpr uint32_t kState = 0;
-    static constexpr uint32_t kConv = 65536;                       // [3][128][3]
-    static constexpr uint32_t kConvPart = 128 * 3 * sizeof(Tio);
-    static constexpr uint32_t kRows = kConv + 3 * kConvPart;       // [L][4][128]: q, k, v, gate
-    static constexpr uint32_t kG = kRows + kShortMaxL * 4 * kRowBytes;  // [L][128] fp32
-    static constexpr uint32_t kBytes = (kG + kShortMaxL * 512 + 127) / 128 * 128;
-    static constexpr uint32_t kRed = 2 * kBytes;                   // probe, readout partials
-    static constexpr uint32_t kRedBytes = 2 * 4 * 128 * 4;          // [2 parities][4 row groups][128]
-    static constexpr uint32_t kSmem = kRed + 2 * kRedBytes + 128;
-};
-constexpr int kPipeThreads = 512;
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-template <typename Tio, typename To>
-__global__ void __launch_bounds__(kPipeThreads, 1)
-k_prefill_short_pipe(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __restrict__ v,
-                     int64_t xs, const Tio* __restrict__ gate, const float* __restrict__ g,
-                     const float* __restrict__ beta, const float* __restrict__ conv_w,
-                     const Tio* __restrict__ cs_in, const float* __restrict__ rms_w, float eps_l2,
-                     float eps_rms, float scale, int N, int H, const int32_t* __restrict__ cu,
-                     int64_t T_total, const float* S0, float* S_fin, To* __restrict__ out,
-                     int* d_status) {
-    using St = PipeStage<Tio>;
-    constexpr int L8 = kShortMaxL;
-    constexpr int kChunksPerRow = (int)(St::kRowBytes / 16);
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(16) float sx[L8][3][kD];  // convolved q, k, v of every token
-    __shared__ __align__(16) float salpha[L8][kD];  // e^g of every token
-    __shared__ __align__(16) float sW[3 * kD * 4];  // conv taps of the current head
-    __shared__ float sRms[kD];
-    __shared__ float snorm[L8][2];
-    __shared__ float sbeta[2][L8];
-    __shared__ int s_head;
-    const uint32_t raw_addr = tc::smem_u32(smem_raw);
-    uint8_t* sm = smem_raw + (((raw_addr + 127u) & ~127u) - raw_addr);
-    const uint32_t sbase = tc::smem_u32(sm);
-    auto sredP = reinterpret_cast<float(*)[4][kD]>(sm + St::kRed);
-    auto sredO = reinterpret_cast<float(*)[4][kD]>(sm + St::kRed + St::kRedBytes);
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rg = warp >> 2, c = 32 * (warp & 3) + lane;
-    const int r0 = 32 * rg;
-    const int64_t HD = (int64_t)H * kD;
-    const int units = N * H;
-    const int per = (units + gridDim.x - 1) / gridDim.x;
-    const int first = blockIdx.x * per;
-    const int my_units = first < units ? (units - first < per ? units - first : per) : 0;
-    auto unit_of = [&](int i, int& n, int& h) {  // head-major: j = h * N + n
-        const int jj = first + i;
-        h = jj / N;
-        n = jj % N;
-    };
-    auto unit_rows = [&](int n, int64_t& a, int& L) {
-        int64_t b;
-        seq_range(cu, n, T_total, a, b);
-        L = (int)((b - a) < L8 ? (b - a) : L8);
-    };
-    if (tid == 0) s_head = -1;
-    for (int cc = tid; cc < kD; cc += kPipeThreads) sRms[cc] = rms_w ? rms_w[cc] : 1.f;
-
-    // unit i -> stage i % 2 (all threads, one cp.async group); its betas -> registers (thread 0)
-    float bnext[L8];
-    auto stage = [&](int i) {
-        int n, h, L;
-        int64_t a;
-        unit_of(i, n, h);
-        unit_rows(n, a, L);
-        const int u = n * H + h;
-        const uint32_t st = sbase + (uint32_t)(i & 1) * St::kBytes;
-        if (S0) {
-            const char* src = reinterpret_cast<const char*>(S0 + (int64_t)u * kD * kD);
-            for (int idx = tid; idx < 4096; idx += kPipeThreads) cp_async16(st + St::kState + 16 * idx, src + 16 * idx);
-        }
-        if (cs_in) {
-            constexpr int kc = (int)(St::kConvPart / 16);
-            for (int idx = tid; idx < 3 * kc; idx += kPipeThreads) {
-                const int p = idx / kc, w = idx % kc;
-                cp_async16(st + St::kConv + p * St::kConvPart + 16 * w,
-                           reinterpret_cast<const char*>(cs_in + (((int64_t)n * 3 + p) * HD + (int64_t)h * kD) * 3) + 16 * w);
-            }
-        }
-        const int nrow = L * 4 * kChunksPerRow;
-        for (int idx = tid; idx < nrow; idx += kPipeThreads) {
-            const int tau = idx / (4 * kChunksPerRow), rem = idx % (4 * kChunksPerRow);
-            const int p = rem / kChunksPerRow, w = rem % kChunksPerRow;
-            const int64_t t = a + tau;
-            const Tio* src = p == 0 ? q : p == 1 ? k : p == 2 ? v : gate;
-            if (src)
-                cp_async16(st + St::kRows + (tau * 4 + p) * St::kRowBytes + 16 * w,
-                           reinterpret_cast<const char*>(src + (p < 3 ? t * xs : t * HD) + (int64_t)h * kD) + 16 * w);
-        }
-        for (int idx = tid; idx < L * 32; idx += kPipeThreads) {
-            const int tau = idx >> 5, w = idx & 31;
-            cp_async16(st + St::kG + tau * 512 + 16 * w,
-                       reinterpret_cast<const char*>(g + ((a + tau) * H + h) * kD) + 16 * w);
-        }
-        cp_async_commit();
-        if (tid == 0) {
-#pragma unroll
-            for (int tau = 0; tau < L8; ++tau) bnext[tau] = tau < L ? beta[(a + tau) * H + h] : 0.f;
-        }
-    };
-    if (my_units > 0) stage(0);
-    if (tid == 0)
-#pragma unroll
-        for (int tau = 0; tau < L8; ++tau) sbeta[0][tau] = bnext[tau];
-    __syncthreads();
-
-    for (int i = 0; i < my_units; ++i) {
-        const int b = i & 1;
-        int n, h, L;
-        int64_t a;
-        unit_of(i, n, h);
-        unit_rows(n, a, L);
-        const int u = n * H + h;
-        {
-            int64_t a2, b2;
-            seq_range(cu, n, T_total, a2, b2);
-            if (b2 - a2 > L8 && tid == 0) flag_status(d_status, KDA_ERR_DEVICE_ARG);
-        }
-        if (h != s_head)  // a new head: its conv taps (uniform branch; read after barrier A)
-            for (int idx = tid; idx < 3 * kD * 4; idx += kPipeThreads) {
-                const int part = idx / (kD * 4), rem = idx % (kD * 4);
-                sW[idx] = conv_w[(part * HD + (int64_t)h * kD) * 4 + rem];
-            }
-        cp_async_wait_all();  // this unit's stage (the only group in flight)
-        __syncthreads();      // A
-        if (tid == 0) s_head = h;
-        // the other stage was read completely by unit i - 1: refill it for unit i + 1
-        if (i + 1 < my_units) stage(i + 1);
-        const uint8_t* st = sm + b * St::kBytes;
-        const Tio* rows = reinterpret_cast<const Tio*>(st + St::kRows);
-        const Tio* cst = reinterpret_cast<const Tio*>(st + St::kConv);
-        const float* grow = reinterpret_cast<const float*>(st + St::kG);
-        // ---- prologue: conv + SiLU and decay factors of every token; the state into registers
-        for (int idx = tid; idx < L * 3 * kD; idx += kPipeThreads) {
-            const int tau = idx / (3 * kD), ch = idx % (3 * kD), part = ch >> 7, d = ch & (kD - 1);
-            const float4 w = *reinterpret_cast<const float4*>(&sW[ch * 4]);
-            float x[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int rel = tau - 3 + m;
-                x[m] = rel >= 0 ? to_f(rows[(rel * 4 + part) * kD + d]) : (cs_in ? to_f(cst[ch * 3 + 3 + rel]) : 0.f);
-            }
-            sx[tau][part][d] = act_silu<Tio>(w.x * x[0] + w.y * x[1] + w.z * x[2] + w.w * x[3]);
-        }
-        for (int idx = tid; idx < L * kD; idx += kPipeThreads) salpha[idx >> 7][idx & (kD - 1)] = decay_exp<Tio>(grow[idx]);
-        float s[32];
-        {
-            const float* Ss = reinterpret_cast<const float*>(st + St::kState);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) s[e] = S0 ? Ss[(r0 + e) * kD + c] : 0.f;
-        }
-        __syncthreads();  // B
-        if (tid == 0 && i + 1 < my_units)  // read by unit i + 1 after its barrier A
-#pragma unroll
-            for (int tau = 0; tau < L8; ++tau) sbeta[(i + 1) & 1][tau] = bnext[tau];
-        for (int rr = warp; rr < 2 * L; rr += kPipeThreads / 32) {  // L2 norms of q and k, per token
-            const int tau = rr >> 1, which = rr & 1;
-            float ss = 0.f;
-#pragma unroll
-            for (int d = lane; d < kD; d += 32) ss += sx[tau][which][d] * sx[tau][which][d];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            if (lane == 0) snorm[tau][which] = 1.0f / sqrtf(ss + eps_l2);
-        }
-        __syncthreads();  // C
-
-        auto emit = [&](int tau, int buf) {  // warp 0: o, RMSNorm, gate, store (columns 4 lane ..)
-            const int c4 = 4 * lane;
-            float o[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) o[m] = 0.f;
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const float4 tt = *reinterpret_cast<const float4*>(&sredO[buf][r][c4]);
-                o[0] += tt.x; o[1] += tt.y; o[2] += tt.z; o[3] += tt.w;
-            }
-            float ss = o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            const float inv = 1.0f / sqrtf(ss / kD + eps_rms);
-            const int64_t row = ((a + tau) * H + h) * kD + c4;
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                float y = o[m] * inv * sRms[c4 + m];
-                if (gate) y *= act_sigmoid<Tio>(to_f(rows[(tau * 4 + 3) * kD + c4 + m]));
-                out[row + m] = from_f<To>(y);
-            }
-        };
-        // ---- token loop, one barrier per token: the readout of token tau - 1 (before the decay)
-        // and the decay and probe of token tau share one pass over the state registers
-        // (row pairs in packed fp32: two partial sums per dot product)
-        for (int tau = 0; tau < L; ++tau) {
-            const int buf = tau & 1;
-            const float ik = snorm[tau][1];
-            const float iqp = tau > 0 ? snorm[tau - 1][0] * scale : 0.f;
-            f2 p2 = f2_dup(0.f), po2 = f2_dup(0.f);
-#pragma unroll
-            for (int e4 = 0; e4 < 8; ++e4) {
-                const float4 kq = *reinterpret_cast<const float4*>(&sx[tau][1][r0 + 4 * e4]);
-                const float4 al = *reinterpret_cast<const float4*>(&salpha[tau][r0 + 4 * e4]);
-                f2 s01 = f2_of(s[4 * e4], s[4 * e4 + 1]), s23 = f2_of(s[4 * e4 + 2], s[4 * e4 + 3]);
-                if (tau > 0) {
-                    const float4 qq = *reinterpret_cast<const float4*>(&sx[tau - 1][0][r0 + 4 * e4]);
-                    po2 = fma2(f2_of(qq.x, qq.y), s01, po2);
-                    po2 = fma2(f2_of(qq.z, qq.w), s23, po2);
-                }
-                s01 = mul2(s01, f2_of(al.x, al.y));
-                s23 = mul2(s23, f2_of(al.z, al.w));
-                p2 = fma2(f2_of(kq.x, kq.y), s01, p2);
-                p2 = fma2(f2_of(kq.z, kq.w), s23, p2);
-                s[4 * e4] = f2_lo(s01);
-                s[4 * e4 + 1] = f2_hi(s01);
-                s[4 * e4 + 2] = f2_lo(s23);
-                s[4 * e4 + 3] = f2_hi(s23);
-            }
-            sredP[buf][rg][c] = (f2_lo(p2) + f2_hi(p2)) * ik;
-            if (tau > 0) sredO[buf][rg][c] = (f2_lo(po2) + f2_hi(po2)) * iqp;
-            __syncthreads();
-            const float ev = sx[tau][2][c] - (sredP[buf][0][c] + sredP[buf][1][c] + sredP[buf][2][c] + sredP[buf][3][c]);
-            const f2 bb = f2_dup(sbeta[b][tau] * ik * ev);
-#pragma unroll
-            for (int e4 = 0; e4 < 8; ++e4) {
-                const float4 kq = *reinterpret_cast<const float4*>(&sx[tau][1][r0 + 4 * e4]);
-                const f2 s01 = fma2(bb, f2_of(kq.x, kq.y), f2_of(s[4 * e4], s[4 * e4 + 1]));
-                const f2 s23 = fma2(bb, f2_of(kq.z, kq.w), f2_of(s[4 * e4 + 2], s[4 * e4 + 3]));
-                s[4 * e4] = f2_lo(s01);
-                s[4 * e4 + 1] = f2_hi(s01);
-                s[4 * e4 + 2] = f2_lo(s23);
-                s[4 * e4 + 3] = f2_hi(s23);
-            }
-            if (tau > 0 && warp == 0) emit(tau - 1, buf);
-        }
-        if (L > 0) {  // readout of the last token
-            const int buf = L & 1;
-            f2 po2 = f2_dup(0.f);
-#pragma unroll
-            for (int e4 = 0; e4 < 8; ++e4) {
-                const float4 qq = *reinterpret_cast<const float4*>(&sx[L - 1][0][r0 + 4 * e4]);
-                po2 = fma2(f2_of(qq.x, qq.y), f2_of(s[4 * e4], s[4 * e4 + 1]), po2);
-                po2 = fma2(f2_of(qq.z, qq.w), f2_of(s[4 * e4 + 2], s[4 * e4 + 3]), po2);
-            }
-            sredO[buf][rg][c] = (f2_lo(po2) + f2_hi(po2)) * snorm[L - 1][0] * scale;
-            __syncthreads();
-            if (warp == 0) emit(L - 1, buf);
-        }
-        if (S_fin) {
-            float* dst = S_fin + (int64_t)u * kD * kD;
-#pragma unroll
-            for (int e = 0; e < 32; ++e) dst[(r0 + e) * kD + c] = s[e];
-        }
-        __syncthreads();  // D: stage b and the shared rows are no longer read
-    }
-    cp_async_wait_all();
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int device_sms() {
@@ -569,43 +299,10 @@ bool short_prefill_applies(const kda_prefill_args& a) {
     return (!a.initial_state || aligned16(a.initial_state)) && (!a.final_state || aligned16(a.final_state));
 }
 
-namespace {
-
-// The pipelined kernel copies 16-byte pieces: every source 16-byte aligned.
-bool short_pipe_ok(const kda_prefill_args& a) {
-    const int64_t xs = a.qkv_row_stride ? a.qkv_row_stride : (int64_t)a.H * kD;
-    const int64_t vec = a.io == KDA_BF16 ? 8 : 4;
-    return xs % vec == 0 && aligned16(a.q) && aligned16(a.k) && aligned16(a.v) && aligned16(a.g) &&
-           (!a.gate || aligned16(a.gate)) && (!a.conv_state_in || aligned16(a.conv_state_in)) &&
-           (!a.initial_state || aligned16(a.initial_state));
-}
-
-template <typename Tio, typename To>
-cudaError_t short_pipe_launch(const kda_prefill_args& a, cudaStream_t s) {
-    const int sms = device_sms();
-    const int units = a.N * a.H;
-    auto kern = k_prefill_short_pipe<Tio, To>;
-    cudaError_t e;
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PipeStage<Tio>::kSmem)))
-        return e;
-    const int64_t xs = a.qkv_row_stride ? a.qkv_row_stride : (int64_t)a.H * kD;
-    kern<<<units < sms ? units : sms, kPipeThreads, PipeStage<Tio>::kSmem, s>>>(
-        (const Tio*)a.q, (const Tio*)a.k, (const Tio*)a.v, xs, (const Tio*)a.gate, a.g, a.beta, a.conv_w,
-        (const Tio*)a.conv_state_in, a.rms_w, a.eps_l2, a.eps_rms, a.scale, a.N, a.H, a.cu_seqlens,
-        a.T_total, a.initial_state, a.final_state, (To*)a.out, a.d_status);
-    return cudaGetLastError();
-}
-
-}  // namespace
-
 cudaError_t launch_short_prefill(const kda_prefill_args& a, cudaStream_t s) {
     if ((int64_t)a.N * a.H == 0) return cudaSuccess;
-    const bool pipe = short_pipe_ok(a);
-    if (a.io == KDA_BF16) {
-        if (pipe) return a.out_dtype == KDA_FP32 ? short_pipe_launch<bf16, float>(a, s) : short_pipe_launch<bf16, bf16>(a, s);
+    if (a.io == KDA_BF16)
         return a.out_dtype == KDA_FP32 ? short_launch<bf16, float>(a, s) : short_launch<bf16, bf16>(a, s);
-    }
-    if (pipe) return a.out_dtype == KDA_FP32 ? short_pipe_launch<float, float>(a, s) : short_pipe_launch<float, bf16>(a, s);
     return a.out_dtype == KDA_FP32 ? short_launch<float, float>(a, s) : short_launch<float, bf16>(a, s);
 }
 

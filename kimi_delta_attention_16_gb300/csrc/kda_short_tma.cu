@@ -11,22 +11,26 @@
 //
 // A unit is one (sequence, head); its bytes are the 64 KB fp32 state in and
 // out, the rolling conv window in and out and a few token rows, so the path is
-// bound by HBM.  Persistent CTAs (one per SM, 256 threads) walk contiguous
-// head-major ranges of units.  Each unit's state and conv window (1D bulk
-// copies) and its token rows (one 2D tensor-map box of Lmax rows for each of
-// q, k, v, gate and g) land in one of two shared-memory stages by the TMA
-// engine, with mbarrier completion.  The state moves into registers at the
-// start of the unit and its rows are converted into working arrays, so the
-// stage is refilled with the unit after next while this one computes: two
-// units' loads are in flight behind every unit's compute.  The state leaves
-// from registers with coalesced stores.
+// bound by HBM.  Persistent CTAs (one per SM) walk contiguous head-major
+// ranges of units with two shared-memory stages.  A producer warp (one
+// thread) fills stage i % 2 with unit i -- the state as four 2D tensor-map
+// boxes of 32 columns with the 128-byte swizzle, the conv window by 1D bulk
+// copies, the token rows as one box of Lmax rows for each of q, k, v, gate
+// and g, the betas by plain loads -- and, once the compute warps have
+// finished unit i - 2 there and written its state back into the stage, sends
+// that state to final_state by four tensor-map stores before reusing the
+// stage.  Neither the request issue nor the 64 KB store stalls a compute warp.
 //
-// Thread (row group = warp, column group = lane) holds rows 16 w .. 16 w + 15
-// of columns 4 l .. 4 l + 3.  One CTA barrier per token: the readout of token
-// t - 1 (S_{t-1}^T q) and the decay and probe of token t (S_bar_t^T k) share
-// one pass over the state registers and go through double-buffered row-group
-// partials; warp (t - 1) mod 8 finishes token t - 1's output (RMSNorm, gate)
-// after that barrier.
+// Sixteen compute warps; warp w owns value columns 8 w .. 8 w + 7 and lane l
+// owns column 8 w + (l & 7) on the rows {8 j + 2 rb, 8 j + 2 rb + 1 : j < 16},
+// rb = l >> 3, as 16 packed fp32 pairs of consecutive rows.  A column's sums
+// over the key rows (the probe S_bar^T k and the readout S^T q) take two
+// shuffles across the four lanes that share it, so no barrier is needed
+// between tokens; with this row choice the state's shared-memory accesses
+// (row r, column c at chunk ((c mod 32) / 4) xor (r mod 8) of the swizzle)
+// are conflict-free.  The per-row factors of every token (q, k, e^g) are
+// kept in shared memory permuted to each lane's pair order.  After the last
+// token, warp t normalises token t's output (RMSNorm, weight, gate).
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 #include "kda_tc_ptx.cuh"
@@ -36,12 +40,19 @@ namespace kda {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kThreads = 256;
+constexpr int kCompute = 512;             // sixteen compute warps
+constexpr int kThreads = kCompute + 32;   // + the producer warp
 constexpr int kL8 = kShortMaxL;
+// per-token stride (floats) of the permuted factor arrays: four row blocks of 32 floats, each
+// padded to 36 so that the blocks the four lanes of a column read fall on different banks
+constexpr int kRb = 36, kFs = 4 * kRb;
+// static shared memory of the kernel (sv, sgate, sW, sRms, snorm, sbeta, barriers)
+constexpr uint32_t kStaticSmem = 4u * (2 * kL8 * kD + 3 * kD * 4 + kD + kL8 * 2 + 2 * kL8) + 32u;
 
 __host__ __device__ constexpr uint32_t align128(uint32_t x) { return (x + 127u) & ~127u; }
 
-// Byte offsets inside one stage for boxes of Lmax token rows.
+// Byte offsets inside one stage for boxes of Lmax token rows.  The state boxes use the
+// 128-byte swizzle, so every stage starts on a 1024-byte boundary.
 template <typename Tio>
 struct TmaStage {
     uint32_t conv, rows, part, g, bytes;
@@ -50,13 +61,20 @@ struct TmaStage {
         rows = conv + align128(3 * kD * 3 * (uint32_t)sizeof(Tio));      // [4][Lmax][128] Tio: q, k, v, gate
         part = (uint32_t)Lmax * kD * (uint32_t)sizeof(Tio);
         g = rows + align128(4 * part);                                    // [Lmax][128] fp32
-        bytes = g + align128((uint32_t)Lmax * kD * 4);
+        bytes = (g + (uint32_t)Lmax * kD * 4 + 1023u) & ~1023u;
     }
 };
+
+// Shared-memory byte offset of state element (row r, column c) in a stage: four boxes of
+// 32 columns x 128 rows, 128-byte rows, 16-byte chunk j of row r at chunk j ^ (r % 8).
+__device__ __forceinline__ uint32_t state_off(int r, int c) {
+    return (uint32_t)((c >> 5) * 16384 + r * 128 + ((((c & 31) >> 2) ^ (r & 7)) << 4) + (c & 3) * 4);
+}
 
 // Tensor maps of the token rows: [T rows][H * 128 columns], boxes of 128 columns x Lmax rows.
 struct ShortMaps {
     CUtensorMap q, k, v, gate, g;
+    CUtensorMap s_in, s_out;  // states as [units * 128 rows][128 columns] fp32, boxes of 32 x 128
 };
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -65,18 +83,12 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
             "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(tc::smem_u32(bar))
         : "memory");
 }
-// 4 bytes, of which the first src_bytes come from global memory and the rest are zero
-__device__ __forceinline__ void cp_async4_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ void fma4(float4& acc, float a, const float4& x) {
-    acc.x = fmaf(a, x.x, acc.x);
-    acc.y = fmaf(a, x.y, acc.y);
-    acc.z = fmaf(a, x.z, acc.z);
-    acc.w = fmaf(a, x.w, acc.w);
+// shared -> global through a tensor map, tracked by the bulk groups of the issuing thread
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
 }
 
 template <typename To>
@@ -90,31 +102,56 @@ __device__ __forceinline__ void store4<bf16>(bf16* p, float a, float b, float c,
     *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(a, b), pack_bf16x2(c, d));
 }
 
+// named barrier 1 of the compute warps (the producer warp never joins it)
+__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory"); }
+__device__ __forceinline__ bool cbar_or(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "n"(kCompute)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+// two packed pairs from / to 16 bytes of shared memory
+__device__ __forceinline__ void lds_f2x2(const void* p, f2& a, f2& b) {
+    asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a.v), "=l"(b.v) : "r"(tc::smem_u32(p)));
+}
+__device__ __forceinline__ void sts_f2x2(void* p, f2 a, f2 b) {
+    asm volatile("st.shared.v2.b64 [%0], {%1, %2};" ::"r"(tc::smem_u32(p)), "l"(a.v), "l"(b.v) : "memory");
+}
+
 template <typename Tio, typename To>
 __global__ void __launch_bounds__(kThreads, 1)
-k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, const Tio* __restrict__ cs_in,
-            Tio* __restrict__ cs_out, const float* __restrict__ beta, const float* __restrict__ conv_w,
-            const float* __restrict__ rms_w, float eps_l2, float eps_rms, float scale, int N, int H,
-            const int32_t* __restrict__ cu, int64_t T_total, const float* S0, float* S_fin,
-            To* __restrict__ out, int* d_status) {
+k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int has_s0, int has_sfin,
+            const Tio* __restrict__ cs_in, Tio* __restrict__ cs_out, const float* __restrict__ beta,
+            const float* __restrict__ conv_w, const float* __restrict__ rms_w, float eps_l2, float eps_rms,
+            float scale, int N, int H, const int32_t* __restrict__ cu, int64_t T_total, To* __restrict__ out,
+            int* d_status) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t bars[2];
-    __shared__ __align__(16) float sx[kL8][3][kD];     // convolved q, k, v of every token
-    __shared__ __align__(16) float salpha[kL8][kD];    // e^g of every token
-    __shared__ __align__(16) float sgate[kL8][kD];     // sigmoid(gate) of every token (1 without a gate)
-    __shared__ __align__(16) float sredP[2][8][kD];    // probe partials per row group, by token parity
-    __shared__ __align__(16) float sredO[2][8][kD];    // readout partials per row group, by token parity
-    __shared__ __align__(16) float sW[3 * kD * 4];     // conv taps of the current head
+    __shared__ uint64_t full[2], done[2];            // stage landed; compute warps done with it
+    __shared__ __align__(16) float sv[kL8][kD];       // convolved v of every token
+    __shared__ __align__(16) float sgate[kL8][kD];    // sigmoid(gate) of every token (1 without a gate)
+    __shared__ __align__(16) float sW[3 * kD * 4];    // conv taps of the current head
     __shared__ __align__(16) float sRms[kD];
-    __shared__ float snorm[kL8][2];                    // 1/|q|, 1/|k| per token
-    __shared__ float sbeta[2][kL8];                    // betas per unit parity
+    __shared__ float snorm[kL8][2];                   // 1/|q|, 1/|k| per token
+    __shared__ float sbeta[2][kL8];                   // betas per stage
 
     const TmaStage<Tio> ST(Lmax);
     const uint32_t raw_addr = tc::smem_u32(smem_raw);
-    uint8_t* sm = smem_raw + (((raw_addr + 127u) & ~127u) - raw_addr);
+    uint8_t* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t sbase = tc::smem_u32(sm);
+    // after the two stages: q, k and e^g ([Lmax][4][kRb]) of every token in each lane's pair
+    // order (pair j of row block rb = rows 8 j + 2 rb, 8 j + 2 rb + 1), then o before its
+    // normalisation ([Lmax][128])
+    float* fq = reinterpret_cast<float*>(sm + 2 * ST.bytes);
+    float* fk = fq + Lmax * kFs;
+    float* fa = fk + Lmax * kFs;
+    float* so = fa + Lmax * kFs;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r0 = 16 * warp, c0 = 4 * lane;
     const int64_t HD = (int64_t)H * kD;
     const int units = N * H;
     const int per = (units + gridDim.x - 1) / gridDim.x;
@@ -126,64 +163,115 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, cons
         n = jj % N;
     };
     const uint32_t cs_bytes = 3u * kD * 3u * (uint32_t)sizeof(Tio);
-    const uint32_t tx = (S0 ? 65536u : 0u) + (cs_in ? cs_bytes : 0u) + (has_gate ? 4u : 3u) * ST.part +
-                        (uint32_t)Lmax * kD * 4u;
 
     if (tid == 0) {
-        tc::mbar_init(&bars[0], 1);
-        tc::mbar_init(&bars[1], 1);
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&full[b], 1);
+            tc::mbar_init(&done[b], kCompute);
+        }
         tc::fence_mbar_init();
     }
     for (int c = tid; c < kD; c += kThreads) sRms[c] = rms_w ? rms_w[c] : 1.f;
     __syncthreads();
 
-    // Loads of this CTA's unit i into stage i & 1 (thread 0).  `pend` bit b: a fill of stage b
-    // is in flight (its phase parity in bit 2 + b), for the exit path.
-    uint32_t pend = 0;
-    auto issue = [&](int i) {
-        const int b = i & 1;
-        int n, h;
-        unit_of(i, n, h);
-        int64_t a, e;
-        seq_range(cu, n, T_total, a, e);
-        const uint32_t st = sbase + (uint32_t)b * ST.bytes;
-        tc::mbar_expect_tx(&bars[b], tx);
-        if (S0) tc::bulk_load(st, S0 + ((int64_t)n * H + h) * kD * kD, 65536u, &bars[b]);
-        if (cs_in)
-            for (int p = 0; p < 3; ++p)
-                tc::bulk_load(st + ST.conv + (uint32_t)p * (cs_bytes / 3u),
-                              cs_in + (((int64_t)n * 3 + p) * HD + (int64_t)h * kD) * 3, cs_bytes / 3u, &bars[b]);
-        const int x = h * kD, y = (int)a;
-        tma_load_2d(st + ST.rows, &maps.q, x, y, &bars[b]);
-        tma_load_2d(st + ST.rows + ST.part, &maps.k, x, y, &bars[b]);
-        tma_load_2d(st + ST.rows + 2 * ST.part, &maps.v, x, y, &bars[b]);
-        if (has_gate) tma_load_2d(st + ST.rows + 3 * ST.part, &maps.gate, x, y, &bars[b]);
-        tma_load_2d(st + ST.g, &maps.g, x, y, &bars[b]);
-        pend = (pend & ~(5u << b)) | ((1u | ((uint32_t)((i >> 1) & 1) << 2)) << b);
-    };
-    // betas of unit i -> sbeta[i & 1] (lanes 0..7 of warp 1, cp.async; zeros past the sequence)
-    auto stage_beta = [&](int i) {
-        int n, h;
-        unit_of(i, n, h);
-        int64_t a, e;
-        seq_range(cu, n, T_total, a, e);
-        const bool ok = lane < e - a;
-        cp_async4_zfill(tc::smem_u32(&sbeta[i & 1][lane]), ok ? beta + (a + lane) * H + h : beta, ok ? 4u : 0u);
-        cp_async_commit();
-    };
-    if (tid == 0) {
-        if (my_units > 0) issue(0);
-        if (my_units > 1) issue(1);
+    if (warp == kCompute / 32) {
+        // ------------------------------------------------------------ producer (one thread)
+        if (lane != 0) return;
+        const CUtensorMap* mp[7] = {&maps.q, &maps.k, &maps.v, &maps.g, &maps.gate, &maps.s_in, &maps.s_out};
+        for (int m = 0; m < 7; ++m)
+            if ((m != 4 || has_gate) && (m != 5 || has_s0) && (m != 6 || has_sfin))
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(mp[m])) : "memory");
+        const uint32_t tx = (has_s0 ? 65536u : 0u) + (cs_in ? cs_bytes : 0u) + (has_gate ? 4u : 3u) * ST.part +
+                            (uint32_t)Lmax * kD * 4u;
+        uint32_t pend = 0;  // bit b: a fill of stage b in flight, its phase parity in bit 2 + b
+        bool failed = false;
+        // unit j is done with stage j % 2 and its state is back there: send it to final_state
+        auto drain = [&](int j) -> bool {
+            const int b = j & 1;
+            if (!tc::mbar_wait(&done[b], (uint32_t)((j >> 1) & 1))) return false;
+            if (has_sfin) {
+                int n, h;
+                unit_of(j, n, h);
+                const int y = (n * H + h) * kD;
+                for (int bx = 0; bx < 4; ++bx) tma_store_2d(&maps.s_out, 32 * bx, y, sbase + (uint32_t)b * ST.bytes + 16384u * bx);
+                tc::bulk_commit();
+                tc::bulk_wait_read<0>();  // the stage may be refilled once the stores have read it
+            }
+            return true;
+        };
+        for (int i = 0; i < my_units; ++i) {
+            const int b = i & 1;
+            if (i >= 2 && !drain(i - 2)) {
+                failed = true;
+                break;
+            }
+            int n, h;
+            unit_of(i, n, h);
+            int64_t a, e;
+            seq_range(cu, n, T_total, a, e);
+#pragma unroll
+            for (int t = 0; t < kL8; ++t) sbeta[b][t] = t < e - a ? beta[(a + t) * H + h] : 0.f;
+            const uint32_t st = sbase + (uint32_t)b * ST.bytes;
+            tc::mbar_expect_tx(&full[b], tx);  // (its arrival also releases the betas above)
+            if (has_s0)
+                for (int bx = 0; bx < 4; ++bx) tma_load_2d(st + 16384u * bx, &maps.s_in, 32 * bx, (n * H + h) * kD, &full[b]);
+            if (cs_in)
+                for (int p = 0; p < 3; ++p)
+                    tc::bulk_load(st + ST.conv + (uint32_t)p * (cs_bytes / 3u),
+                                  cs_in + (((int64_t)n * 3 + p) * HD + (int64_t)h * kD) * 3, cs_bytes / 3u, &full[b]);
+            const int x = h * kD, y = (int)a;
+            tma_load_2d(st + ST.rows, &maps.q, x, y, &full[b]);
+            tma_load_2d(st + ST.rows + ST.part, &maps.k, x, y, &full[b]);
+            tma_load_2d(st + ST.rows + 2 * ST.part, &maps.v, x, y, &full[b]);
+            if (has_gate) tma_load_2d(st + ST.rows + 3 * ST.part, &maps.gate, x, y, &full[b]);
+            tma_load_2d(st + ST.g, &maps.g, x, y, &full[b]);
+            pend = (pend & ~(5u << b)) | ((1u | ((uint32_t)((i >> 1) & 1) << 2)) << b);
+        }
+        if (!failed)
+            for (int j = my_units > 2 ? my_units - 2 : 0; j < my_units; ++j)
+                if (!drain(j)) {
+                    failed = true;
+                    break;
+                }
+        if (failed) {  // fills in flight: wait for them (bounded) before the shared memory goes away
+            for (int b = 0; b < 2; ++b)
+                if ((pend >> b) & 1u) tc::mbar_wait(&full[b], (pend >> (2 + b)) & 1u);
+            flag_status(d_status, KDA_ERR_TIMEOUT);
+        }
+        tc::bulk_wait_all();
+        return;
     }
-    if (warp == 1 && lane < kL8 && my_units > 0) stage_beta(0);
 
-    bool failed = false;
+    // ---------------------------------------------------------------- compute warps
+    const int col = 8 * warp + (lane & 7), rb = lane >> 3;
+    // position of channel d in the pair order of the factor arrays
+    auto perm = [](int d) { return ((d >> 1) & 3) * kRb + (d >> 3) * 2 + (d & 1); };
+    // output of the unit's tokens (warp t for token t): o = scale S^T q / |q| from the readout
+    // sums, RMSNorm, weight, gate
+    auto emit_unit = [&](int64_t ja, int jh, int jL) {
+        const int c0 = 4 * lane;
+        for (int t = warp; t < jL; t += kCompute / 32) {
+            const float sq = scale * snorm[t][0];
+            float4 o = *reinterpret_cast<const float4*>(so + t * kD + c0);
+            o.x *= sq;
+            o.y *= sq;
+            o.z *= sq;
+            o.w *= sq;
+            float ss = o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float inv = 1.0f / sqrtf(ss * (1.0f / kD) + eps_rms);
+            const float4 rw = *reinterpret_cast<const float4*>(&sRms[c0]);
+            const float4 gg = *reinterpret_cast<const float4*>(&sgate[t][c0]);
+            store4<To>(out + ((ja + t) * H + jh) * kD + c0, o.x * inv * rw.x * gg.x, o.y * inv * rw.y * gg.y,
+                       o.z * inv * rw.z * gg.z, o.w * inv * rw.w * gg.w);
+        }
+    };
     int h_prev = -1;
     for (int i = 0; i < my_units; ++i) {
         const int b = i & 1;
         int n, h;
         unit_of(i, n, h);
-        const int u = n * H + h;
         int64_t a, e;
         seq_range(cu, n, T_total, a, e);
         int L = (int)(e - a);
@@ -193,30 +281,29 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, cons
         }
         // ---- A: this unit's stage has landed; conv taps of a new head
         bool ok = true;
-        if (warp == 0) ok = tc::mbar_wait(&bars[b], (uint32_t)((i >> 1) & 1));
-        if (tid == 0) pend &= ~(1u << b);
-        if (warp == 1) cp_async_wait_all();
+        if (warp == 0) ok = tc::mbar_wait(&full[b], (uint32_t)((i >> 1) & 1));
         if (h != h_prev)
-            for (int idx = tid; idx < 3 * kD * 4; idx += kThreads) {
+            for (int idx = tid; idx < 3 * kD * 4; idx += kCompute) {
                 const int part = idx / (kD * 4), rem = idx % (kD * 4);
                 sW[idx] = conv_w[(part * HD + (int64_t)h * kD) * 4 + rem];
             }
         h_prev = h;
-        if (__syncthreads_or(!ok)) {
-            failed = true;
+        if (cbar_or(!ok)) {
+            if (tid == 0) flag_status(d_status, KDA_ERR_TIMEOUT);
             break;
         }
-        const uint8_t* st = sm + (uint32_t)b * ST.bytes;
-        // the state into registers
-        float4 s[16];
-        {
-            const float* Ss = reinterpret_cast<const float*>(st);
+        uint8_t* st = sm + (uint32_t)b * ST.bytes;
+        // the state into registers: pair j = rows 8 j + 2 rb, 8 j + 2 rb + 1 of this lane's column
+        f2 s2[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r)
-                s[r] = S0 ? *reinterpret_cast<const float4*>(Ss + (r0 + r) * kD + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < 16; ++j) {
+            const int r = 8 * j + 2 * rb;
+            s2[j] = has_s0 ? f2_of(*reinterpret_cast<const float*>(st + state_off(r, col)),
+                                   *reinterpret_cast<const float*>(st + state_off(r + 1, col)))
+                           : f2_dup(0.f);
         }
-        // conv + SiLU of every token, one channel per thread and step; the rolled window out
-        for (int ch = tid; ch < 3 * kD; ch += kThreads) {
+        // conv + SiLU of every token, one channel per thread (warps 0-11); the rolled window out
+        for (int ch = tid; ch < 3 * kD; ch += kCompute) {
             const int part = ch >> 7, d = ch & (kD - 1);
             float p0 = 0.f, p1 = 0.f, p2 = 0.f;  // x[-3], x[-2], x[-1]
             if (cs_in) {
@@ -227,9 +314,11 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, cons
             }
             const Tio* rp = reinterpret_cast<const Tio*>(st + ST.rows + (uint32_t)part * ST.part) + d;
             const float4 w = *reinterpret_cast<const float4*>(&sW[ch * 4]);
+            float* dst = part == 0 ? fq + perm(d) : part == 1 ? fk + perm(d) : &sv[0][d];
+            const int dstride = part == 2 ? kD : kFs;
             for (int t = 0; t < L; ++t) {
                 const float x = to_f(rp[t * kD]);
-                sx[t][part][d] = act_silu<Tio>(w.x * p0 + w.y * p1 + w.z * p2 + w.w * x);
+                dst[t * dstride] = act_silu<Tio>(w.x * p0 + w.y * p1 + w.z * p2 + w.w * x);
                 p0 = p1;
                 p1 = p2;
                 p2 = x;
@@ -244,136 +333,84 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, cons
         {  // decay factors and gate sigmoids of every token
             const float* gs = reinterpret_cast<const float*>(st + ST.g);
             const Tio* gt = reinterpret_cast<const Tio*>(st + ST.rows + 3 * ST.part);
-            for (int idx = tid; idx < L * kD; idx += kThreads) {
+            for (int idx = tid; idx < L * kD; idx += kCompute) {
                 const int t = idx >> 7, c = idx & (kD - 1);
-                salpha[t][c] = decay_exp<Tio>(gs[idx]);
+                fa[t * kFs + perm(c)] = decay_exp<Tio>(gs[idx]);
                 sgate[t][c] = has_gate ? act_sigmoid<Tio>(to_f(gt[idx])) : 1.f;
             }
         }
-        __syncthreads();  // B: stage b is read completely
-        if (tid == 0 && i + 2 < my_units) issue(i + 2);
-        if (warp == 1 && lane < kL8 && i + 1 < my_units) stage_beta(i + 1);
-        // L2 norms of q and k, one vector per warp and step
-        for (int vv = warp; vv < 2 * L; vv += kThreads / 32) {
-            const int t = vv >> 1, which = vv & 1;
-            const float4 x4 = *reinterpret_cast<const float4*>(&sx[t][which][c0]);
+        cbar();  // B: the stage is read completely (the state stays there for the write-back)
+        // L2 norms of q and k, one vector per warp
+        if (warp < 2 * L) {
+            const int t = warp >> 1;
+            const float* src = (warp & 1 ? fk : fq) + t * kFs;  // lane: 4 of the 128 (rb = lane / 8)
+            const float4 x4 = *reinterpret_cast<const float4*>(src + (lane >> 3) * kRb + 4 * (lane & 7));
             float ss = x4.x * x4.x + x4.y * x4.y + x4.z * x4.z + x4.w * x4.w;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            if (lane == 0) snorm[t][which] = 1.0f / sqrtf(ss + eps_l2);
+            if (lane == 0) snorm[t][warp & 1] = 1.0f / sqrtf(ss + eps_l2);
         }
-        __syncthreads();  // C
+        cbar();  // C
 
-        // warp-level output of token t: o = scale S_t^T q / |q| from the readout partials, RMSNorm,
-        // weight, gate, 4 columns per lane
-        auto emit = [&](int t) {
-            const float(*po)[kD] = sredO[t & 1];
-            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
-                const float4 x = *reinterpret_cast<const float4*>(&po[w][c0]);
-                o.x += x.x;
-                o.y += x.y;
-                o.z += x.z;
-                o.w += x.w;
-            }
-            const float sq = snorm[t][0] * scale;
-            o.x *= sq;
-            o.y *= sq;
-            o.z *= sq;
-            o.w *= sq;
-            float ss = o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            const float inv = 1.0f / sqrtf(ss * (1.0f / kD) + eps_rms);
-            const float4 rw = *reinterpret_cast<const float4*>(&sRms[c0]);
-            const float4 gg = *reinterpret_cast<const float4*>(&sgate[t][c0]);
-            store4<To>(out + ((a + t) * H + h) * kD + c0, o.x * inv * rw.x * gg.x, o.y * inv * rw.y * gg.y,
-                       o.z * inv * rw.z * gg.z, o.w * inv * rw.w * gg.w);
-        };
-
-        // ---- token loop: one barrier per token
-        float kr[16];
+        // ---- tokens: no barrier between them; a column's sums over its 4 lanes by shuffles
         for (int t = 0; t < L; ++t) {
-            const int buf = t & 1;
-            float4 p = make_float4(0.f, 0.f, 0.f, 0.f), po = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float* kt = fk + t * kFs + rb * kRb;
+            const float* at = fa + t * kFs + rb * kRb;
+            const float* qt = fq + t * kFs + rb * kRb;
+            const float ik = snorm[t][1];
+            f2 kr[16];
+            f2 P0 = f2_dup(0.f), P1 = f2_dup(0.f);  // two chains
 #pragma unroll
-            for (int e4 = 0; e4 < 4; ++e4) {
-                const float4 k4 = *reinterpret_cast<const float4*>(&sx[t][1][r0 + 4 * e4]);
-                const float4 a4 = *reinterpret_cast<const float4*>(&salpha[t][r0 + 4 * e4]);
-                const float kk[4] = {k4.x, k4.y, k4.z, k4.w}, aa[4] = {a4.x, a4.y, a4.z, a4.w};
-                float qq[4] = {0.f, 0.f, 0.f, 0.f};
-                if (t > 0) {
-                    const float4 q4 = *reinterpret_cast<const float4*>(&sx[t - 1][0][r0 + 4 * e4]);
-                    qq[0] = q4.x;
-                    qq[1] = q4.y;
-                    qq[2] = q4.z;
-                    qq[3] = q4.w;
-                }
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    float4& sv = s[4 * e4 + m];
-                    fma4(po, qq[m], sv);  // readout of token t - 1, before this token's decay
-                    sv.x *= aa[m];
-                    sv.y *= aa[m];
-                    sv.z *= aa[m];
-                    sv.w *= aa[m];
-                    fma4(p, kk[m], sv);
-                    kr[4 * e4 + m] = kk[m];
-                }
+            for (int j2 = 0; j2 < 8; ++j2) {  // decay and probe, two pairs per step
+                lds_f2x2(kt + 4 * j2, kr[2 * j2], kr[2 * j2 + 1]);
+                f2 a0, a1;
+                lds_f2x2(at + 4 * j2, a0, a1);
+                s2[2 * j2] = mul2(a0, s2[2 * j2]);
+                s2[2 * j2 + 1] = mul2(a1, s2[2 * j2 + 1]);
+                P0 = fma2(kr[2 * j2], s2[2 * j2], P0);
+                P1 = fma2(kr[2 * j2 + 1], s2[2 * j2 + 1], P1);
             }
-            *reinterpret_cast<float4*>(&sredP[buf][warp][c0]) = p;
-            if (t > 0) *reinterpret_cast<float4*>(&sredO[buf ^ 1][warp][c0]) = po;
-            __syncthreads();
-            // e = v - S_bar^T k / |k| for this thread's columns; the write takes beta e / |k|
-            float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
+            const f2 P = add2(P0, P1);
+            float p = f2_lo(P) + f2_hi(P);
+            p += __shfl_xor_sync(0xffffffffu, p, 8);
+            p += __shfl_xor_sync(0xffffffffu, p, 16);
+            const f2 e2 = f2_dup(sbeta[b][t] * ik * (sv[t][col] - ik * p));
+            f2 O0 = f2_dup(0.f), O1 = f2_dup(0.f);
 #pragma unroll
-            for (int w = 0; w < 8; ++w) {
-                const float4 x = *reinterpret_cast<const float4*>(&sredP[buf][w][c0]);
-                pv.x += x.x;
-                pv.y += x.y;
-                pv.z += x.z;
-                pv.w += x.w;
+            for (int j2 = 0; j2 < 8; ++j2) {  // write and readout
+                f2 q0, q1;
+                lds_f2x2(qt + 4 * j2, q0, q1);
+                s2[2 * j2] = fma2(kr[2 * j2], e2, s2[2 * j2]);
+                s2[2 * j2 + 1] = fma2(kr[2 * j2 + 1], e2, s2[2 * j2 + 1]);
+                O0 = fma2(q0, s2[2 * j2], O0);
+                O1 = fma2(q1, s2[2 * j2 + 1], O1);
             }
-            const float ik = snorm[t][1], bk = sbeta[b][t] * ik;
-            const float4 v4 = *reinterpret_cast<const float4*>(&sx[t][2][c0]);
-            const float4 ev = make_float4(bk * (v4.x - pv.x * ik), bk * (v4.y - pv.y * ik), bk * (v4.z - pv.z * ik),
-                                          bk * (v4.w - pv.w * ik));
-#pragma unroll
-            for (int r = 0; r < 16; ++r) fma4(s[r], kr[r], ev);
-            if (t > 0 && warp == ((t - 1) & 7)) emit(t - 1);
+            const f2 O = add2(O0, O1);
+            float o = f2_lo(O) + f2_hi(O);
+            o += __shfl_xor_sync(0xffffffffu, o, 8);
+            o += __shfl_xor_sync(0xffffffffu, o, 16);
+            if (rb == 0) so[t * kD + col] = o;
         }
-        if (L > 0) {  // readout of the last token
-            float4 po = make_float4(0.f, 0.f, 0.f, 0.f);
+        // the final state back into the stage for the producer's tensor-map stores; release it
+        if (has_sfin) {
 #pragma unroll
-            for (int e4 = 0; e4 < 4; ++e4) {
-                const float4 q4 = *reinterpret_cast<const float4*>(&sx[L - 1][0][r0 + 4 * e4]);
-                fma4(po, q4.x, s[4 * e4]);
-                fma4(po, q4.y, s[4 * e4 + 1]);
-                fma4(po, q4.z, s[4 * e4 + 2]);
-                fma4(po, q4.w, s[4 * e4 + 3]);
+            for (int j = 0; j < 16; ++j) {
+                const int r = 8 * j + 2 * rb;
+                *reinterpret_cast<float*>(st + state_off(r, col)) = f2_lo(s2[j]);
+                *reinterpret_cast<float*>(st + state_off(r + 1, col)) = f2_hi(s2[j]);
             }
-            *reinterpret_cast<float4*>(&sredO[(L - 1) & 1][warp][c0]) = po;
-            __syncthreads();
-            if (warp == ((L - 1) & 7)) emit(L - 1);
+            tc::fence_async_smem();
         }
-        if (S_fin) {
-            float* dst = S_fin + (int64_t)u * kD * kD;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) *reinterpret_cast<float4*>(dst + (r0 + r) * kD + c0) = s[r];
-        }
+        mbar_arrive(&done[b]);
+        cbar();  // D: every token's o is complete
+        emit_unit(a, h, L);
     }
-    // fills still in flight (a wait above timed out): wait for them, bounded, before exiting
-    if (tid == 0)
-        for (int b = 0; b < 2; ++b)
-            if ((pend >> b) & 1u) tc::mbar_wait(&bars[b], (pend >> (2 + b)) & 1u);
-    cp_async_wait_all();
-    if (failed && tid == 0) flag_status(d_status, KDA_ERR_TIMEOUT);
 }
 
+// dynamic shared memory: two stages, the permuted q, k, e^g factors and o, alignment slack
 template <typename Tio>
 uint32_t short_tma_smem(int Lmax) {
-    return 2 * TmaStage<Tio>(Lmax).bytes + 128;
+    return 2 * TmaStage<Tio>(Lmax).bytes + (3u * kFs + kD) * (uint32_t)Lmax * 4u + 1024u;
 }
 
 int max_len(const kda_prefill_args& a) {
@@ -404,14 +441,17 @@ cudaError_t short_tma_launch(const kda_prefill_args& a, cudaStream_t s) {
               encode_tensor_map_2d(&maps.v, a.v, fp32, cols, rows, (uint64_t)xs * es, kD, (uint32_t)Lmax, false) &&
               encode_tensor_map_2d(&maps.g, a.g, true, cols, rows, cols * 4, kD, (uint32_t)Lmax, false);
     if (ok && a.gate) ok = encode_tensor_map_2d(&maps.gate, a.gate, fp32, cols, rows, cols * es, kD, (uint32_t)Lmax, false);
+    const uint64_t srows = (uint64_t)a.N * a.H * kD;  // states as [units * 128][128] fp32
+    if (ok && a.initial_state) ok = encode_tensor_map_2d(&maps.s_in, a.initial_state, true, kD, srows, kD * 4, 32, kD, true);
+    if (ok && a.final_state) ok = encode_tensor_map_2d(&maps.s_out, a.final_state, true, kD, srows, kD * 4, 32, kD, true);
     if (!ok) return cudaErrorInvalidValue;
     DeviceInfo d;
     const int sms = current_device_info(&d) ? d.sm_count : 148;
     const int units = a.N * a.H;
     kern<<<units < sms ? units : sms, kThreads, smem, s>>>(
-        maps, Lmax, a.gate ? 1 : 0, (const Tio*)a.conv_state_in, (Tio*)a.conv_state_out, a.beta, a.conv_w, a.rms_w,
-        a.eps_l2, a.eps_rms, a.scale, a.N, a.H, a.cu_seqlens, a.T_total, a.initial_state, a.final_state, (To*)a.out,
-        a.d_status);
+        maps, Lmax, a.gate ? 1 : 0, a.initial_state ? 1 : 0, a.final_state ? 1 : 0, (const Tio*)a.conv_state_in,
+        (Tio*)a.conv_state_out, a.beta, a.conv_w, a.rms_w, a.eps_l2, a.eps_rms, a.scale, a.N, a.H, a.cu_seqlens,
+        a.T_total, (To*)a.out, a.d_status);
     return cudaGetLastError();
 }
 
@@ -430,7 +470,7 @@ bool short_tma_applies(const kda_prefill_args& a) {
     if (Lmax > kShortMaxL) return false;
     const uint32_t smem = a.io == KDA_BF16 ? short_tma_smem<bf16>(Lmax > 0 ? Lmax : 1)
                                            : short_tma_smem<float>(Lmax > 0 ? Lmax : 1);
-    return smem <= 232448u - 48u * 1024u;  // dynamic stages + the kernel's static arrays
+    return smem + kStaticSmem <= 232448u;  // dynamic + static within the per-block limit
 }
 
 cudaError_t launch_short_tma(const kda_prefill_args& a, cudaStream_t s) {

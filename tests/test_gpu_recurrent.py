@@ -124,3 +124,38 @@ def test_verify_256x4_sampled_pairs():
         ref = oracle_prefill(sub)
         check_out(to_np(out[4 * n:4 * n + 4, h:h + 1]), ref["out"], 1, TOL_OUT_BF16, True)
         assert per_head_rel(to_np(fin[n, h])[None], ref["final_state"][0], 0).max() <= TOL_STATE_BF16
+
+
+def test_recurrent_fallback_kernel_for_unaligned_conv_state():
+    """A conv state that is not 16-byte aligned (a view one element into its buffer) cannot be
+    staged by the TMA engine: the plain recurrent kernel takes the call, with the same results."""
+    inp = synth.make_prefill("layer_8k", seed=72, device=DEV, lengths=[4, 1, 8, 3], H=3, s0_std=0.02,
+                             conv_state=True, rms_w="random")
+    buf = torch.empty(inp.conv_state_in.numel() + 1, dtype=inp.conv_state_in.dtype, device=DEV)
+    cs_in = buf[1:].view_as(inp.conv_state_in)
+    cs_in.copy_(inp.conv_state_in)
+    assert cs_in.data_ptr() % 16 != 0
+    cso = torch.empty_like(inp.conv_state_in)
+    out, fin = kda.kda_prefill(inp.q, inp.k, inp.v, inp.conv_w, inp.g, inp.beta, inp.cu_seqlens,
+                               gate=inp.gate, rms_w=inp.rms_w, initial_state=inp.initial_state,
+                               conv_state_in=cs_in, conv_state_out=cso, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ref = oracle_prefill(inp)
+    check_out(to_np(out), ref["out"], 1, TOL_OUT_BF16, bf16_out=False)
+    assert per_head_rel(to_np(fin), ref["final_state"], 1).max() <= TOL_STATE_BF16
+    np.testing.assert_array_equal(synth.to_f32_numpy(cso), ref["conv_state_out"].astype(np.float32))
+
+
+def test_recurrent_batch_of_empty_sequences_hands_states_through():
+    """Every sequence empty (T_total = 0): final states equal the initial ones and the conv
+    states pass through unchanged."""
+    inp = synth.make_prefill("layer_8k", seed=73, device=DEV, lengths=[0, 0, 0], H=2, s0_std=0.02,
+                             conv_state=True)
+    cso = torch.empty_like(inp.conv_state_in)
+    out, fin = kda.kda_prefill(inp.q, inp.k, inp.v, inp.conv_w, inp.g, inp.beta, inp.cu_seqlens,
+                               gate=inp.gate, rms_w=inp.rms_w, initial_state=inp.initial_state,
+                               conv_state_in=inp.conv_state_in, conv_state_out=cso)
+    torch.cuda.synchronize()
+    assert out.shape[0] == 0
+    assert torch.equal(fin, inp.initial_state)
+    assert torch.equal(cso, inp.conv_state_in)
