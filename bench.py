@@ -201,6 +201,8 @@ def run_ours(args):
             print(f"multi-token decode {obj['metric']}: {obj['ms_per_step']:.4f} ms/step, "
                   f"{obj['roofline']['frac']:.3f} of HBM", flush=True)
         return
+    if args.mode == "gemm":  # profiling aid: only the projection GEMMs of the projected layer
+        return run_gemm_only(args, rank, dev)
     if args.mode == "prefill":
         args.decode_steps = 0
         args.verify_steps = 0
@@ -522,11 +524,14 @@ def time_projected_layer(args, pg, dev, stream, peaks, peak_src, world, d_model=
         return max_over_ranks(pg, e0.elapsed_time(e1) / n, dev)
 
     steps = max(3, min(args.steps, 10))
+    traffic_key = {"alpha (x W_a^T, -5 sigmoid)": "gemm_alpha", "gate (x W_g^T)": "gemm_gate",
+                   "output (y W_o^T)": "gemm_output"}
     per = {}
     for name, fn in gemms.items():
         ms = timed(fn, steps)
         tf = flops[name] / (ms / 1e3) / 1e12
-        per[name] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac": round(tf / peaks["bf16_tflops"], 4)}
+        per[name] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac": round(tf / peaks["bf16_tflops"], 4),
+                     "traffic": recorded_traffic(traffic_key[name]) if name in traffic_key else None}
     ms = timed(step, steps)
     gemm_ms = sum(v["ms"] for v in per.values())
     gemm_flops = sum(flops.values())
@@ -605,6 +610,41 @@ def time_multi_token(args, pg, dev, stream, peaks, peak_src, world, t_new=4, rin
                         "algorithmic_bytes": nbytes}}
     del steps_in, dec
     return obj, args.verify_steps  # one launch per call: the recurrent kernel also rolls the conv state
+
+
+def run_gemm_only(args, rank, dev, d_model=7168, HD=12288):
+    """Profiling aid: the alpha (-5 sigmoid), gate and output projections of the projected layer
+    at T = --tokens (default 8192) tokens; prints each one's time (no JSON line)."""
+    import torch
+    import kimi_delta_attention_16_gb300 as kda
+    T = args.tokens or 8192
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+
+    def rnd(n, k, std):
+        return (torch.randn(n, k, generator=gen, device=dev) * std).to(torch.bfloat16)
+
+    x, y = rnd(T, d_model, 1.0), rnd(T, HD, 1.0)
+    wa, wg, wo = rnd(HD, d_model, d_model ** -0.5), rnd(HD, d_model, d_model ** -0.5), rnd(d_model, HD, HD ** -0.5)
+    g = torch.empty((T, HD), dtype=torch.float32, device=dev)
+    gate = torch.empty((T, HD), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((T, d_model), dtype=torch.bfloat16, device=dev)
+    runs = {"alpha": lambda: kda.kda_gemm(x, wa, epilogue="decay", out=g),
+            "gate": lambda: kda.kda_gemm(x, wg, epilogue="none", out=gate),
+            "output": lambda: kda.kda_gemm(y, wo, epilogue="none", out=out)}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for name, fn in runs.items():
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        if rank == 0:
+            print(f"gemm {name} (T={T}): {ms:.4f} ms, {2 * T * HD * d_model / (ms / 1e3) / 1e12:.1f} TFLOP/s")
 
 
 def run_decode_only(args, world, rank, local, pg, dev, peaks, peak_src):
@@ -709,9 +749,9 @@ def main():
     ap.add_argument("--decode-n", type=int, default=256, help="decode batch (sequences)")
     ap.add_argument("--verify-steps", type=int, default=200,
                     help="multi-token decode steps (256 sequences x 4 tokens) to time; 0 skips")
-    ap.add_argument("--mode", choices=["all", "prefill", "decode", "verify"], default="all",
+    ap.add_argument("--mode", choices=["all", "prefill", "decode", "verify", "gemm"], default="all",
                     help="profiling aid: run only one of the measurements (verify = the "
-                         "multi-token decode loop)")
+                         "multi-token decode loop, gemm = the projection GEMMs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra-workloads", dest="extra_workloads", action="store_false",
                     help="skip the nested varlen_16 and long_1m prefill measurements")
