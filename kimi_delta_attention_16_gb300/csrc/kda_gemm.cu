@@ -12,8 +12,10 @@
 //   KDA_EPI_DECAY    C = -5 sigmoid(acc)         (log-decay g in (-5, 0), fp32)
 //   KDA_EPI_SIGMOID  C = sigmoid(acc)            (write strength beta in (0, 1), fp32)
 //
-// Persistent CTAs, one per SM, walk 128 x 256 output tiles (tile index ->
-// m-block fastest, so CTAs running together share W tiles).  Warp roles in a
+// Persistent CTAs, one per SM, walk 128 x 256 output tiles in bands of 16
+// m-blocks: within a band the m-block runs fastest, then the n-block, so the
+// tiles in flight together share W tiles and one 2048-row slice of A, and the
+// L2 holds both (A is read from DRAM about once, W once per band).  Warp roles in a
 // CTA of 256 threads: warp 0 lane 0 feeds a 4-stage ring of shared-memory
 // stages (A 128 x 64 and W 256 x 64 bf16 boxes, 128-byte swizzle) by TMA;
 // warp 1 lane 0 issues tcgen05.mma (M = 128, N = 256, K = 16) into one of two
@@ -33,6 +35,7 @@ namespace {
 using namespace tc;
 
 constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
+constexpr int kBandM = 16;  // m-blocks per band of the tile order
 constexpr int kThreads = 256;
 constexpr uint32_t kTileA = kBM * kBK * 2;  // 16 KB
 constexpr uint32_t kTileB = kBN * kBK * 2;  // 32 KB
@@ -44,6 +47,14 @@ constexpr uint32_t kTmemCols = 2 * kAccCols;                    // double-buffer
 struct GemmMaps {
     CUtensorMap a, w;
 };
+
+// Output tile t -> (m0, n0) in the banded order described above.
+__device__ __forceinline__ void tile_origin(int t, int m_tiles, int n_tiles, int& m0, int& n0) {
+    const int band = t / (kBandM * n_tiles), r = t % (kBandM * n_tiles);
+    const int rows = m_tiles - band * kBandM < kBandM ? m_tiles - band * kBandM : kBandM;
+    m0 = (band * kBandM + r % rows) * kBM;
+    n0 = (r / rows) * kBN;
+}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     asm volatile(
@@ -106,7 +117,8 @@ k_gemm(const __grid_constant__ GemmMaps maps, int M, int N, int K, To* __restric
         int s = 0;
         uint32_t ph = 0, issued = 0;  // bit s of issued: stage s has had a fill; its last parity in bit 8 + s
         for (int t = blockIdx.x; t < tiles && !failed; t += gridDim.x) {
-            const int m0 = (t % m_tiles) * kBM, n0 = (t / m_tiles) * kBN;
+            int m0, n0;
+            tile_origin(t, m_tiles, n_tiles, m0, n0);
             for (int kb = 0; kb < kb_n; ++kb) {
                 if (!mbar_wait(&empty[s], ph ^ 1u)) {
                     failed = true;
@@ -179,7 +191,8 @@ k_gemm(const __grid_constant__ GemmMaps maps, int M, int N, int K, To* __restric
                 break;
             }
             fence_after_sync();
-            const int m0 = (t % m_tiles) * kBM, n0 = (t / m_tiles) * kBN;
+            int m0, n0;
+            tile_origin(t, m_tiles, n_tiles, m0, n0);
             const int row = m0 + 32 * q + lane;
             To* crow = C + (int64_t)row * ldc + n0;
 #pragma unroll 1
