@@ -72,6 +72,11 @@ def _load():
             lib.kda_oracle_forward.argtypes = [_i64, _int, _int, _int, _i32p, _f32p, _f32p, _f32p,
                                                _f32p, _vp, _f32p, _f32p, _vp, _vp, _dbl, _dbl,
                                                _dbl, _vp, _vp, _vp, _vp, _vp, _int]
+            lib.kda_oracle_backward.restype = _int
+            lib.kda_oracle_backward.argtypes = [_i64, _int, _int, _int, _i32p, _f32p, _f32p, _f32p,
+                                                _f32p, _vp, _f32p, _f32p, _vp, _vp, _dbl, _dbl,
+                                                _dbl, _vp, _f64p, _vp, _f64p, _f64p, _f64p, _f64p,
+                                                _vp, _f64p, _f64p, _vp, _vp, _vp, _int]
             lib.kda_oracle_num_cores.restype = _int
             _lib = lib
     return _lib
@@ -241,6 +246,52 @@ def forward(q, k, v, conv_w, cu_seqlens, g, beta, gate=None, rms_w=None, eps_l2=
     if want_o_pre:
         res["o_pre"] = opre
     return res
+
+
+def backward(q, k, v, conv_w, cu_seqlens, g, beta, dy, gate=None, rms_w=None, eps_l2=1e-6,
+             eps_rms=1e-6, scale=1.0, initial_state=None, conv_state_in=None,
+             d_final_state=None, n_threads=0):
+    """Gradients of loss = sum(dy * out) + sum(d_final_state * final_state) through the whole
+    layer, with respect to every input of ``forward`` (the same shapes; values exact in fp32).
+
+    Returns a dict of fp64 arrays: dq, dk, dv (raw projections, [T, H, D]), dconv_w [3, H*D, 4],
+    dg [T, H, D], dbeta [T, H], and -- for the inputs that were given -- dgate, drms_w [D],
+    dinitial_state [N, H, D, D] (always returned: the state's gradient at the sequence start)
+    and dconv_state_in [N, 3*H*D, 3].
+    """
+    q = np.asarray(q)
+    T, H, D = q.shape
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    N = cu.shape[0] - 1
+    qs, ks, vs = (_exact_f32(a, n) for a, n in ((q, "q"), (k, "k"), (v, "v")))
+    gs, bs, gts = _exact_f32(g, "g"), _exact_f32(beta, "beta"), _exact_f32(gate, "gate")
+    cws = _exact_f32(np.asarray(conv_w).reshape(3, H * D, 4), "conv_w")
+    csi = None if conv_state_in is None else _exact_f32(np.asarray(conv_state_in).reshape(N, 3 * H * D, 3),
+                                                        "conv_state_in")
+    rw = _exact_f32(rms_w, "rms_w")
+    s0 = None if initial_state is None else _f64(initial_state)
+    dyf = _f64(dy).reshape(T, H, D)
+    dsf = None if d_final_state is None else _f64(d_final_state)
+    out = {"dq": np.zeros((T, H, D)), "dk": np.zeros((T, H, D)), "dv": np.zeros((T, H, D)),
+           "dconv_w": np.zeros((3, H * D, 4)), "dg": np.zeros((T, H, D)), "dbeta": np.zeros((T, H)),
+           "dinitial_state": np.zeros((N, H, D, D))}
+    dgate = np.zeros((T, H, D)) if gate is not None else None
+    drms = np.zeros(D) if rms_w is not None else None
+    dcs = np.zeros((N, 3 * H * D, 3)) if conv_state_in is not None else None
+    rc = _load().kda_oracle_backward(T, N, H, D, cu, qs, ks, vs, cws, _ptr(csi), gs, bs, _ptr(gts),
+                                     _ptr(rw), float(eps_l2), float(eps_rms), float(scale), _ptr(s0),
+                                     dyf, _ptr(dsf), out["dq"], out["dk"], out["dv"], out["dconv_w"],
+                                     _ptr(dcs), out["dg"], out["dbeta"], _ptr(dgate), _ptr(drms),
+                                     _ptr(out["dinitial_state"]), int(n_threads))
+    if rc:
+        raise ValueError(f"kda_oracle_backward failed ({rc})")
+    if dgate is not None:
+        out["dgate"] = dgate
+    if drms is not None:
+        out["drms_w"] = drms
+    if dcs is not None:
+        out["dconv_state_in"] = dcs
+    return out
 
 
 # --------------------------------------------------------------------------- projections around the layer

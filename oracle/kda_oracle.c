@@ -419,4 +419,322 @@ int kda_oracle_forward(int64_t T_total, int N, int H, int D, const int32_t* cu_s
     return J.err;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Backward pass of the whole layer (reverse-mode derivatives of the forward  */
+/* above), token-sequential and in fp64.  For one (sequence, head) unit the   */
+/* forward is recomputed keeping every intermediate (the convolved and        */
+/* activated q, k, v, their norms, the states S_0 .. S_L, o, the RMSNorm      */
+/* factors), then the derivatives of loss = sum dy . y + sum dS_L . S_L run   */
+/* backwards through the same steps:                                          */
+/*   y = n w sig(z), n = o r, r = (mean o^2 + eps)^-1/2:                       */
+/*     dz = dy n w sig(1 - sig);  dw += dy n sig;  dn = dy w sig;              */
+/*     do = r dn - r^3 o (dn . o) / D                                         */
+/*   o_t = scale S_t^T q_t:  dS += scale q_t do_t^T;  dq_t = scale S_t do_t    */
+/*   S_t = P + beta k e^T, e = v - P^T k, P = Diag(alpha_t) S_{t-1}:           */
+/*     w = dS^T k;  dv_t = beta w;  dbeta_t = w . e;                           */
+/*     dk_t = beta (dS e - P w);  dP = dS - beta k w^T;                        */
+/*     dg_t[c] = sum_j dP[c][j] P[c][j]  (d/dg of alpha = e^g);               */
+/*     dS_{t-1} = Diag(alpha_t) dP                                            */
+/*   x = a / sqrt(|a|^2 + eps):  da = (dx - x (x . dx)) / sqrt(|a|^2 + eps)    */
+/*   a = u sig(u):  du = da sig(u) (1 + u (1 - sig(u)))                       */
+/*   u_t = sum_j w_j x_{t-3+j}:  dx_{t-3+j} += w_j du_t;  dw_j += x_{t-3+j} du_t */
+/*     (positions before the sequence belong to the rolling conv state).     */
+/* ------------------------------------------------------------------------ */
+typedef struct {
+    fwd_job f;               /* the forward's inputs (outputs unused) */
+    const double* dy;        /* [T_total][H][D] */
+    const double* dS_fin;    /* [N][H][D][D] or NULL */
+    double *dq, *dk, *dv;    /* [T_total][H][D]: d/d raw projections */
+    double* dcw_part;        /* [N*H][3][D][4] per-unit conv-tap partials */
+    double* dcs_in;          /* [N][3*H*D][3] or NULL */
+    double *dg, *dbeta;      /* [T_total][H][D], [T_total][H] */
+    double* dgate;           /* [T_total][H][D] or NULL */
+    double* drms_part;       /* [N*H][D] per-unit RMSNorm-weight partials */
+    double* dS0;             /* [N][H][D][D] or NULL */
+} bwd_job;
+
+static int bwd_unit(bwd_job* B, int n, int h)
+{
+    fwd_job* J = &B->f;
+    const int D = J->D, H = J->H;
+    const int64_t HD = (int64_t)H * D, DD = (int64_t)D * D;
+    const int64_t t0 = J->cu[n], L = (int64_t)J->cu[n + 1] - t0;
+    const int64_t u = (int64_t)n * H + h;
+    const size_t LD = (size_t)(L > 0 ? L : 1) * D;
+    /* per token: raw x, pre-activation u, activation a (3 parts each), q^, k^, norms, alpha,
+       o, r, sig; states S_0..S_L */
+    double* xr = (double*)calloc(3 * LD + 3 * 3 * D, sizeof(double)); /* [3][3 + L][D] incl. the window */
+    double* ua = (double*)malloc(sizeof(double) * 3 * LD);
+    double* aa = (double*)malloc(sizeof(double) * 3 * LD);
+    double* qh = (double*)malloc(sizeof(double) * LD);
+    double* kh = (double*)malloc(sizeof(double) * LD);
+    double* rq = (double*)malloc(sizeof(double) * (size_t)(L + 1));
+    double* rk = (double*)malloc(sizeof(double) * (size_t)(L + 1));
+    double* al = (double*)malloc(sizeof(double) * LD);
+    double* oo = (double*)malloc(sizeof(double) * LD);
+    double* rr = (double*)malloc(sizeof(double) * (size_t)(L + 1));
+    double* sg = (double*)malloc(sizeof(double) * LD);
+    double* SS = (double*)malloc(sizeof(double) * (size_t)(L + 1) * DD);
+    double* dS = (double*)malloc(sizeof(double) * DD);
+    double* dP = (double*)malloc(sizeof(double) * DD);
+    double* vec = (double*)malloc(sizeof(double) * 8 * D);
+    double* da = (double*)calloc(3 * LD, sizeof(double)); /* d/d activation, then d/d u */
+    if (!xr || !ua || !aa || !qh || !kh || !rq || !rk || !al || !oo || !rr || !sg || !SS || !dS || !dP || !vec || !da) {
+        free(xr); free(ua); free(aa); free(qh); free(kh); free(rq); free(rk); free(al); free(oo); free(rr);
+        free(sg); free(SS); free(dS); free(dP); free(vec); free(da);
+        return 2;
+    }
+    const float* src[3] = {J->q, J->k, J->v};
+    const int64_t XS = (L + 3) * D; /* stride of one part in xr: 3 window rows then L token rows */
+    for (int x = 0; x < 3; ++x)
+        for (int d = 0; d < D; ++d) {
+            for (int m = 0; m < 3; ++m)
+                xr[x * XS + m * D + d] =
+                    J->cs_in ? (double)J->cs_in[((int64_t)n * 3 * HD + x * HD + (int64_t)h * D + d) * 3 + m] : 0.0;
+            for (int64_t t = 0; t < L; ++t) xr[x * XS + (3 + t) * D + d] = (double)src[x][(t0 + t) * HD + (int64_t)h * D + d];
+        }
+    /* ---- forward, keeping everything */
+    for (int c = 0; c < D; ++c)
+        for (int j = 0; j < D; ++j) SS[c * D + j] = J->S0 ? J->S0[(u * D + c) * D + j] : 0.0;
+    for (int64_t t = 0; t < L; ++t) {
+        const int64_t tt = t0 + t;
+        for (int x = 0; x < 3; ++x)
+            for (int d = 0; d < D; ++d) {
+                const float* wp = J->conv_w + ((int64_t)x * HD + (int64_t)h * D + d) * 4;
+                double acc = 0.0;
+                for (int j = 0; j < 4; ++j) acc += (double)wp[j] * xr[x * XS + (t + j) * D + d];
+                ua[x * LD + t * D + d] = acc;
+                aa[x * LD + t * D + d] = silu_d(acc);
+            }
+        double sq = 0.0, sk = 0.0;
+        for (int d = 0; d < D; ++d) {
+            sq += aa[t * D + d] * aa[t * D + d];
+            sk += aa[LD + t * D + d] * aa[LD + t * D + d];
+        }
+        rq[t] = sqrt(sq + J->eps_l2);
+        rk[t] = sqrt(sk + J->eps_l2);
+        for (int d = 0; d < D; ++d) {
+            qh[t * D + d] = aa[t * D + d] / rq[t];
+            kh[t * D + d] = aa[LD + t * D + d] / rk[t];
+            al[t * D + d] = exp((double)J->g[(tt * H + h) * D + d]);
+        }
+        const double* Sp = SS + t * DD;
+        double* Sn = SS + (t + 1) * DD;
+        const double bt = (double)J->beta[tt * H + h];
+        double* e = vec;
+        for (int c = 0; c < D; ++c)
+            for (int j = 0; j < D; ++j) Sn[c * D + j] = al[t * D + c] * Sp[c * D + j];
+        for (int j = 0; j < D; ++j) {
+            double p = 0.0;
+            for (int c = 0; c < D; ++c) p += Sn[c * D + j] * kh[t * D + c];
+            e[j] = aa[2 * LD + t * D + j] - p;
+        }
+        for (int c = 0; c < D; ++c)
+            for (int j = 0; j < D; ++j) Sn[c * D + j] += bt * kh[t * D + c] * e[j];
+        double ms = 0.0;
+        for (int j = 0; j < D; ++j) {
+            double r = 0.0;
+            for (int c = 0; c < D; ++c) r += Sn[c * D + j] * qh[t * D + c];
+            oo[t * D + j] = J->scale * r;
+            ms += oo[t * D + j] * oo[t * D + j];
+        }
+        rr[t] = 1.0 / sqrt(ms / D + J->eps_rms);
+        for (int j = 0; j < D; ++j) sg[t * D + j] = J->gate ? sigmoid_d((double)J->gate[(tt * H + h) * D + j]) : 1.0;
+    }
+    /* ---- backward */
+    double* drms = B->drms_part + u * D;
+    double* dcw = B->dcw_part + u * 3 * D * 4;
+    for (int c = 0; c < D; ++c)
+        for (int j = 0; j < D; ++j) dS[c * D + j] = B->dS_fin ? B->dS_fin[(u * D + c) * D + j] : 0.0;
+    double *dn = vec, *dov = vec + D, *w = vec + 2 * D, *e = vec + 3 * D, *dqh = vec + 4 * D, *dkh = vec + 5 * D;
+    for (int64_t t = L - 1; t >= 0; --t) {
+        const int64_t tt = t0 + t;
+        const double* dyt = B->dy + (tt * H + h) * D;
+        /* RMSNorm and gate */
+        double dno = 0.0;
+        for (int j = 0; j < D; ++j) {
+            const double wj = J->rms_w ? (double)J->rms_w[j] : 1.0;
+            const double nj = oo[t * D + j] * rr[t], s = sg[t * D + j];
+            if (B->dgate) B->dgate[(tt * H + h) * D + j] = J->gate ? dyt[j] * nj * wj * s * (1.0 - s) : 0.0;
+            drms[j] += dyt[j] * nj * s;
+            dn[j] = dyt[j] * wj * s;
+            dno += dn[j] * oo[t * D + j];
+        }
+        const double r = rr[t];
+        for (int j = 0; j < D; ++j) dov[j] = r * dn[j] - r * r * r * oo[t * D + j] * dno / D;
+        /* readout o_t = scale S_t^T q_t */
+        const double* St = SS + (t + 1) * DD;
+        for (int c = 0; c < D; ++c) {
+            double acc = 0.0;
+            for (int j = 0; j < D; ++j) {
+                dS[c * D + j] += J->scale * qh[t * D + c] * dov[j];
+                acc += St[c * D + j] * dov[j];
+            }
+            dqh[c] = J->scale * acc;
+        }
+        /* write S_t = P + beta k e^T with P = Diag(alpha_t) S_{t-1} */
+        const double* Sp = SS + t * DD;
+        const double bt = (double)J->beta[tt * H + h];
+        for (int j = 0; j < D; ++j) {
+            double pw = 0.0, ww = 0.0;
+            for (int c = 0; c < D; ++c) {
+                pw += al[t * D + c] * Sp[c * D + j] * kh[t * D + c];
+                ww += dS[c * D + j] * kh[t * D + c];
+            }
+            e[j] = aa[2 * LD + t * D + j] - pw;
+            w[j] = ww;
+        }
+        double db = 0.0;
+        for (int j = 0; j < D; ++j) {
+            da[2 * LD + t * D + j] = bt * w[j]; /* dv (v is the activation itself) */
+            db += w[j] * e[j];
+        }
+        B->dbeta[tt * H + h] = db;
+        for (int c = 0; c < D; ++c) {
+            double de = 0.0, pw = 0.0, dgc = 0.0;
+            for (int j = 0; j < D; ++j) {
+                const double P = al[t * D + c] * Sp[c * D + j];
+                de += dS[c * D + j] * e[j];
+                pw += P * w[j];
+                const double d = dS[c * D + j] - bt * kh[t * D + c] * w[j];
+                dP[c * D + j] = d;
+                dgc += d * P;
+            }
+            dkh[c] = bt * (de - pw);
+            B->dg[(tt * H + h) * D + c] = dgc;
+        }
+        for (int c = 0; c < D; ++c)
+            for (int j = 0; j < D; ++j) dS[c * D + j] = al[t * D + c] * dP[c * D + j];
+        /* L2 norms */
+        double xq = 0.0, xk = 0.0;
+        for (int d = 0; d < D; ++d) {
+            xq += qh[t * D + d] * dqh[d];
+            xk += kh[t * D + d] * dkh[d];
+        }
+        for (int d = 0; d < D; ++d) {
+            da[t * D + d] = (dqh[d] - qh[t * D + d] * xq) / rq[t];
+            da[LD + t * D + d] = (dkh[d] - kh[t * D + d] * xk) / rk[t];
+        }
+    }
+    if (B->dS0)
+        for (int64_t i = 0; i < DD; ++i) B->dS0[u * DD + i] = dS[i];
+    /* SiLU, then the conv: d/d raw x and d/d taps; positions before the sequence -> conv state */
+    double* dxw = (double*)calloc((size_t)3 * XS, sizeof(double)); /* [3][3 + L][D] */
+    if (!dxw) {
+        free(xr); free(ua); free(aa); free(qh); free(kh); free(rq); free(rk); free(al); free(oo); free(rr);
+        free(sg); free(SS); free(dS); free(dP); free(vec); free(da);
+        return 2;
+    }
+    for (int x = 0; x < 3; ++x)
+        for (int64_t t = 0; t < L; ++t)
+            for (int d = 0; d < D; ++d) {
+                const double uu = ua[x * LD + t * D + d], s = sigmoid_d(uu);
+                const double du = da[x * LD + t * D + d] * s * (1.0 + uu * (1.0 - s));
+                const float* wp = J->conv_w + ((int64_t)x * HD + (int64_t)h * D + d) * 4;
+                for (int j = 0; j < 4; ++j) {
+                    dxw[x * XS + (t + j) * D + d] += (double)wp[j] * du;
+                    dcw[(x * D + d) * 4 + j] += xr[x * XS + (t + j) * D + d] * du;
+                }
+            }
+    double* dst[3] = {B->dq, B->dk, B->dv};
+    for (int x = 0; x < 3; ++x)
+        for (int d = 0; d < D; ++d) {
+            for (int64_t t = 0; t < L; ++t) dst[x][(t0 + t) * HD + (int64_t)h * D + d] = dxw[x * XS + (3 + t) * D + d];
+            if (B->dcs_in)
+                for (int m = 0; m < 3; ++m)
+                    B->dcs_in[((int64_t)n * 3 * HD + x * HD + (int64_t)h * D + d) * 3 + m] = dxw[x * XS + m * D + d];
+        }
+    free(dxw);
+    free(xr); free(ua); free(aa); free(qh); free(kh); free(rq); free(rk); free(al); free(oo); free(rr);
+    free(sg); free(SS); free(dS); free(dP); free(vec); free(da);
+    return 0;
+}
+
+typedef struct {
+    bwd_job* B;
+    int64_t next;
+    int err;
+} bwd_pool;
+
+static void* bwd_worker(void* arg)
+{
+    bwd_pool* P = (bwd_pool*)arg;
+    const int64_t units = (int64_t)P->B->f.N * P->B->f.H;
+    for (;;) {
+        int64_t u = __atomic_fetch_add(&P->next, 1, __ATOMIC_RELAXED);
+        if (u >= units) break;
+        int rc = bwd_unit(P->B, (int)(u / P->B->f.H), (int)(u % P->B->f.H));
+        if (rc) __atomic_store_n(&P->err, rc, __ATOMIC_RELAXED);
+    }
+    return NULL;
+}
+
+/* Gradients of loss = sum dy . y + sum dS_fin . S_fin with respect to every input of
+ * kda_oracle_forward.  dconv_w ([3][H*D][4]) and drms_w ([D]) are overwritten with sums over
+ * all units (in unit order, so the result does not depend on the thread count); every other
+ * output has one writer.  Optional outputs may be NULL: dconv_state_in, dgate, drms_w,
+ * dinitial_state; d_final_state may be NULL (zero). */
+int kda_oracle_backward(int64_t T_total, int N, int H, int D, const int32_t* cu_seqlens,
+                        const float* q, const float* k, const float* v, const float* conv_w,
+                        const float* conv_state_in, const float* g, const float* beta,
+                        const float* gate, const float* rms_w, double eps_l2, double eps_rms,
+                        double scale, const double* initial_state, const double* dy,
+                        const double* d_final_state, double* dq, double* dk, double* dv,
+                        double* dconv_w, double* dconv_state_in, double* dg, double* dbeta,
+                        double* dgate, double* drms_w, double* dinitial_state, int n_threads)
+{
+    if (!cu_seqlens || !q || !k || !v || !conv_w || !g || !beta || !dy || !dq || !dk || !dv || !dconv_w ||
+        !dg || !dbeta || N < 0 || H <= 0 || D <= 0)
+        return 1;
+    if (cu_seqlens[0] != 0 || cu_seqlens[N] != T_total) return 1;
+    for (int n = 0; n < N; ++n)
+        if (cu_seqlens[n + 1] < cu_seqlens[n]) return 1;
+    const int64_t units = (int64_t)N * H;
+    double* dcw_part = (double*)calloc((size_t)(units > 0 ? units : 1) * 3 * D * 4, sizeof(double));
+    double* drms_part = (double*)calloc((size_t)(units > 0 ? units : 1) * D, sizeof(double));
+    if (!dcw_part || !drms_part) {
+        free(dcw_part);
+        free(drms_part);
+        return 2;
+    }
+    bwd_job B = {{T_total, N, H, D, cu_seqlens, q, k, v, conv_w, conv_state_in, g, beta, gate, rms_w, eps_l2,
+                  eps_rms, scale, initial_state, NULL, NULL, NULL, NULL, 0, 0},
+                 dy, d_final_state, dq, dk, dv, dcw_part, dconv_state_in, dg, dbeta, dgate, drms_part,
+                 dinitial_state};
+    bwd_pool P = {&B, 0, 0};
+    if (n_threads <= 0) n_threads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > units) n_threads = (int)(units > 0 ? units : 1);
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)n_threads);
+    if (!th) {
+        free(dcw_part);
+        free(drms_part);
+        return 2;
+    }
+    int started = 0;
+    for (int i = 1; i < n_threads; ++i) {
+        pthread_t t;
+        if (pthread_create(&t, NULL, bwd_worker, &P) == 0) th[started++] = t;
+    }
+    bwd_worker(&P);
+    for (int i = 0; i < started; ++i) pthread_join(th[i], NULL);
+    free(th);
+    const int64_t HD = (int64_t)H * D;
+    for (int64_t i = 0; i < 3 * HD * 4; ++i) dconv_w[i] = 0.0;
+    if (drms_w)
+        for (int d = 0; d < D; ++d) drms_w[d] = 0.0;
+    for (int64_t uu = 0; uu < units; ++uu) {
+        const int h = (int)(uu % H);
+        for (int x = 0; x < 3; ++x)
+            for (int d = 0; d < D; ++d)
+                for (int j = 0; j < 4; ++j)
+                    dconv_w[((int64_t)x * HD + (int64_t)h * D + d) * 4 + j] += dcw_part[((uu * 3 + x) * D + d) * 4 + j];
+        if (drms_w)
+            for (int d = 0; d < D; ++d) drms_w[d] += drms_part[uu * D + d];
+    }
+    free(dcw_part);
+    free(drms_part);
+    return P.err;
+}
+
 int kda_oracle_num_cores(void) { return (int)sysconf(_SC_NPROCESSORS_ONLN); }

@@ -433,3 +433,91 @@ def test_projected_layer_composes_its_stages():
     np.testing.assert_array_equal(res["gate"], oracle.round_bf16(res["gate"]))
     np.testing.assert_allclose(res["out"], oracle.round_bf16(ref["out"]).reshape(T, H * D) @ wo.T,
                                rtol=1e-13, atol=1e-13)
+
+
+# --------------------------------------------------------------------------- backward pass
+
+def _fd_case(seed=17, g_range=(-1.0, 0.0)):
+    """A tiny two-sequence case with every optional input present, all values exact in fp32."""
+    inp = synth.make_prefill("tiny_fp32", seed=seed, lengths=[5, 3], H=2, D=4, s0_std=0.5,
+                             conv_state=True, rms_w="random", g_range=g_range)
+    a = _np_inputs(inp)
+    rng = np.random.default_rng(seed + 1)
+    dy = rng.standard_normal(a["q"].shape)
+    dsf = rng.standard_normal(a["initial_state"].shape)
+    return a, dy, dsf
+
+
+def _loss(a, dy, dsf):
+    res = oracle.forward(**a, n_threads=1)
+    return float(np.sum(dy * res["out"]) + np.sum(dsf * res["final_state"]))
+
+
+@pytest.mark.parametrize("g_range", [(-1.0, 0.0), (-5.0, -4.0)])
+def test_backward_matches_central_differences_of_the_forward(g_range):
+    """Every element of every input: central differences of the forward at steps h = 2^-12 and
+    h / 4 (the perturbed values stay exact in fp32, so the forward itself is unchanged),
+    combined by Richardson extrapolation (16 D(h/4) - D(h)) / 15 to remove the h^2 term,
+    against the backward's gradient; loss = sum dy . out + sum dS . final_state.  (With strong
+    decay the RMSNorm of small outputs makes the third derivatives large: plain differences at
+    h = 2^-12 are off by ~1e-4 there, the extrapolated ones by ~1e-8.)"""
+    a, dy, dsf = _fd_case(g_range=g_range)
+    grads = oracle.backward(**a, dy=dy, d_final_state=dsf, n_threads=1)
+    names = {"q": "dq", "k": "dk", "v": "dv", "conv_w": "dconv_w", "g": "dg", "beta": "dbeta",
+             "gate": "dgate", "rms_w": "drms_w", "initial_state": "dinitial_state",
+             "conv_state_in": "dconv_state_in"}
+    def central(x, idx, h):
+        keep = x[idx]
+        x[idx] = keep + h
+        lp = _loss(a, dy, dsf)
+        x[idx] = keep - h
+        lm = _loss(a, dy, dsf)
+        x[idx] = keep
+        return (lp - lm) / (2 * h)
+
+    h = 2.0 ** -12
+    worst = 0.0
+    for name, gname in names.items():
+        x = a[name]
+        gr = grads[gname].reshape(x.shape)
+        for idx in np.ndindex(x.shape):
+            fd = (16.0 * central(x, idx, h / 4) - central(x, idx, h)) / 15.0
+            err = abs(fd - gr[idx])
+            worst = max(worst, err / (1.0 + abs(fd)))
+            assert err <= 1e-6 * (1.0 + abs(fd)), f"{name}{idx}: backward {gr[idx]:.9e}, differences {fd:.9e}"
+    assert worst > 0.0
+
+
+def test_backward_is_linear_in_the_upstream_gradients():
+    a, dy, dsf = _fd_case(seed=19)
+    g1 = oracle.backward(**a, dy=dy, d_final_state=None)
+    g2 = oracle.backward(**a, dy=np.zeros_like(dy), d_final_state=dsf)
+    g12 = oracle.backward(**a, dy=dy, d_final_state=dsf)
+    for key in g12:
+        np.testing.assert_allclose(g12[key], g1[key] + g2[key], rtol=1e-12, atol=1e-12)
+
+
+def test_backward_closed_form_without_decay_or_write():
+    """alpha = 1, beta = 0: the state never changes, o_t = scale S0^T q_t, so the initial
+    state's gradient is sum_t scale q_t do_t^T (do_t the readout's gradient, here with no
+    RMSNorm weight or gate: do = r dy - r^3 o (dy . o) / D), and the log-decay's gradient is
+    dg_t[c] = sum_j dS_t[c][j] S0[c][j] with dS_t = sum_{s >= t} scale q_s do_s^T."""
+    inp = synth.make_prefill("tiny_fp32", seed=23, lengths=[6], H=1, D=4, s0_std=0.5, gate=False,
+                             rms_w=None, g_range=(0.0, 0.0))
+    inp.beta.zero_()
+    a = _np_inputs(inp)
+    dy = np.random.default_rng(24).standard_normal(a["q"].shape)
+    grads = oracle.backward(**a, dy=dy)
+    res = oracle.forward(**a, want_o_pre=True)
+    # q after conv + SiLU + L2, from the oracle's pinned pieces
+    x = a["q"].reshape(6, 4)
+    cq, _ = oracle.conv_silu(x, a["conv_w"][0].reshape(4, 4), a["cu_seqlens"])
+    qh = oracle.l2norm(cq)
+    o = res["o_pre"][:, 0]
+    r = 1.0 / np.sqrt(np.mean(o * o, axis=1) + 1e-6)
+    do = r[:, None] * dy[:, 0] - (r ** 3)[:, None] * o * np.sum(dy[:, 0] * o, axis=1)[:, None] / 4
+    np.testing.assert_allclose(grads["dinitial_state"][0, 0], qh.T @ do, rtol=1e-10, atol=1e-12)
+    S0 = a["initial_state"][0, 0]
+    for t in range(6):
+        dSt = qh[t:].T @ do[t:]
+        np.testing.assert_allclose(grads["dg"][t, 0], np.sum(dSt * S0, axis=1), rtol=1e-10, atol=1e-12)
