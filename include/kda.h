@@ -312,6 +312,73 @@ typedef struct {
 
 kda_status kda_gemm(const kda_gemm_args* args, kda_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * kda_backward -- the gradients of the layer (training).  Page "Kimi K3 /
+ * Architecture": the model is trained, so kda_prefill's layer needs its
+ * reverse-mode derivatives; page "Animated Kimi K3 architecture diagram",
+ * LOCAL MEMORY section: each token's four moves are an affine map of the
+ * state, whose adjoint runs the same moves backwards.
+ *
+ * Given dy = dL/d out and dS_fin = dL/d final_state of one kda_prefill call,
+ * it returns dL/d of every input of that call:
+ *
+ *   dq, dk, dv      [T_total][H][D] fp32 (raw projections, before the conv)
+ *   dconv_w         [3][H*D][4] fp32 (summed over all tokens and sequences)
+ *   dg              [T_total][H][D] fp32;  dbeta  [T_total][H] fp32
+ *   dgate           [T_total][H][D] fp32, or NULL (not wanted; 0 when gate is NULL)
+ *   drms_w          [D] fp32, or NULL (computed as for weights of ones when rms_w is NULL)
+ *   dinitial_state  [N][H][D][D] fp32, or NULL
+ *   dconv_state_in  [N][3*H*D][3] fp32, or NULL (the gradient of the left padding
+ *                   when conv_state_in is NULL)
+ *
+ * The forward is recomputed, not saved: `fwd` holds the kda_prefill arguments
+ * (N, H, T_total, io, cu_seqlens and its host copy, q, k, v, qkv_row_stride,
+ * conv_w, conv_state_in, g, beta, gate, rms_w, eps_l2, eps_rms, scale,
+ * initial_state); out_dtype there is the dtype of dy.  Its out, final_state,
+ * conv_state_out, chunk, flags and segments are ignored; its workspace and
+ * workspace_bytes are this call's scratch (kda_backward_workspace_size).
+ * Supported: D = 128, io bf16 or fp32; arithmetic is fp32 throughout (the
+ * decays e^g, SiLU and sigmoid through the IEEE functions), so the result
+ * does not depend on the forward's path.
+ *
+ * Method: conv + SiLU + L2 norms recomputed per token; the recurrence replayed
+ * once per (sequence, head) storing the state at the start of every 32-token
+ * segment (the checkpoints); the epilogue's derivative per row; then, segment by segment from the end, the segment's
+ * states replayed from its checkpoint and its tokens run backwards carrying
+ * dS (D x D fp32); then the L2 norm's, SiLU's and the conv's derivatives.
+ *
+ * Needs cu_seqlens_host (the checkpoint layout is planned on the host).  The
+ * outputs must not overlap each other or any input.  dconv_w and drms_w are
+ * zeroed by the call and accumulated with atomics, so their last bits depend
+ * on the order blocks finish.  Every pointer 16-byte aligned except beta,
+ * dbeta (4-byte).
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    kda_prefill_args fwd;       /* the forward call (see above) + this call's workspace */
+    const void* dy;             /* [T_total][H][D] fwd.out_dtype */
+    const float* d_final_state; /* [N][H][D][D] fp32, or NULL (zero) */
+    float* dq;
+    float* dk;
+    float* dv;
+    float* dconv_w;
+    float* dg;
+    float* dbeta;
+    float* dgate;
+    float* drms_w;
+    float* dinitial_state;
+    float* dconv_state_in;
+} kda_backward_args;
+
+/* Bytes of workspace kda_backward needs (reads fwd.N, H, D, T_total and
+ * fwd.cu_seqlens_host, which is required):
+ *   T_total H D 28 + T_total H 8 + segs H D^2 4 + N H 32 D^2 4
+ * (each part rounded up to 256), segs = the sum over sequences of ceil(len / 32):
+ * 1.6 GB of checkpoints for 8192 tokens of 96 heads, 2 MiB of replay scratch per
+ * (sequence, head). */
+kda_status kda_backward_workspace_size(const kda_backward_args* args, size_t* bytes);
+
+kda_status kda_backward(const kda_backward_args* args, kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,12 +26,12 @@ KDA_PATH_SIMT, KDA_PATH_TENSOR_CORE, KDA_PATH_RECURRENT = 0, 1, 2
 KDA_RECURRENT_MAX_LEN = 8
 KDA_MAX_SEGMENTS = 16
 KDA_EPI_NONE, KDA_EPI_DECAY, KDA_EPI_SIGMOID = 0, 1, 2
-ABI_VERSION = 10300  # kda_gemm
+ABI_VERSION = 10400  # kda_backward
 
 # Every symbol include/kda.h declares.
 EXPORTED = ("kda_status_string", "kda_last_error", "kda_version", "kda_short_conv",
             "kda_prefill_workspace_size", "kda_prefill", "kda_prefill_plan", "kda_prefill_noalloc",
-            "kda_decode_step", "kda_gemm")
+            "kda_decode_step", "kda_gemm", "kda_backward_workspace_size", "kda_backward")
 NOALLOC_SCRATCH_BYTES = 64 << 20  # KDA_NOALLOC_SCRATCH_BYTES in include/kda.h
 
 _vp = ctypes.c_void_p
@@ -77,6 +77,15 @@ class GemmArgs(ctypes.Structure):
         ("M", _int), ("N", _int), ("K", _int),
         ("A", _vp), ("lda", _i64), ("W", _vp), ("ldw", _i64), ("C", _vp), ("ldc", _i64),
         ("c_dtype", _int), ("epilogue", _int), ("d_status", _vp),
+    ]
+
+
+class BackwardArgs(ctypes.Structure):
+    """Mirror of kda_backward_args."""
+    _fields_ = [
+        ("fwd", PrefillArgs), ("dy", _vp), ("d_final_state", _vp),
+        ("dq", _vp), ("dk", _vp), ("dv", _vp), ("dconv_w", _vp), ("dg", _vp), ("dbeta", _vp),
+        ("dgate", _vp), ("drms_w", _vp), ("dinitial_state", _vp), ("dconv_state_in", _vp),
     ]
 
 
@@ -129,5 +138,10 @@ def load(auto_build: bool = True) -> ctypes.CDLL:
         lib.kda_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
         lib.kda_gemm.restype = _int
         lib.kda_gemm.argtypes = [ctypes.POINTER(GemmArgs), _vp]
+        lib.kda_backward_workspace_size.restype = _int
+        lib.kda_backward_workspace_size.argtypes = [ctypes.POINTER(BackwardArgs),
+                                                    ctypes.POINTER(ctypes.c_size_t)]
+        lib.kda_backward.restype = _int
+        lib.kda_backward.argtypes = [ctypes.POINTER(BackwardArgs), _vp]
         _lib = lib
         return lib

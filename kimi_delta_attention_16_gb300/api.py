@@ -357,3 +357,80 @@ def kda_gemm(A: torch.Tensor, W: torch.Tensor, *, epilogue: str = "none",
     if st:
         raise KDAError(st, "kda_gemm")
     return out
+
+
+def kda_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, conv_w: torch.Tensor,
+                 g: torch.Tensor, beta: torch.Tensor, cu_seqlens, dy: torch.Tensor, *,
+                 gate: Optional[torch.Tensor] = None, rms_w: Optional[torch.Tensor] = None,
+                 eps_l2: float = 1e-6, eps_rms: float = 1e-6, scale: float = 1.0,
+                 initial_state: Optional[torch.Tensor] = None,
+                 conv_state_in: Optional[torch.Tensor] = None,
+                 d_final_state: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                 d_status=None, stream=None) -> dict:
+    """Gradients of sum(dy * out) + sum(d_final_state * final_state) of one kda_prefill call
+    (same inputs) with respect to its inputs.  Returns a dict of fp32 tensors: dq, dk, dv
+    [T, H, D]; dconv_w [3, H*D, 4]; dg [T, H, D]; dbeta [T, H]; dgate (when gate is given);
+    drms_w (when rms_w is given); dinitial_state [N, H, D, D]; dconv_state_in [N, 3*H*D, 3]
+    (when conv_state_in is given).
+    dy has the dtype of the forward's out.  D must be 128."""
+    lib = _lib.load()
+    T, H, D = q.shape
+    cu_dev, cu_host = _cu_pair(cu_seqlens, q.device)
+    N = cu_host.shape[0] - 1
+    if dy.shape != (T, H, D) or not dy.is_contiguous():
+        raise ValueError(f"dy must be a contiguous [{T}, {H}, {D}] tensor")
+    if d_final_state is not None and (d_final_state.dtype != torch.float32 or not d_final_state.is_contiguous()):
+        raise ValueError("d_final_state must be a contiguous fp32 tensor")
+    dev = q.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    res = {"dq": torch.empty((T, H, D), **f32), "dk": torch.empty((T, H, D), **f32),
+           "dv": torch.empty((T, H, D), **f32), "dconv_w": torch.empty((3, H * D, 4), **f32),
+           "dg": torch.empty((T, H, D), **f32), "dbeta": torch.empty((T, H), **f32)}
+    if gate is not None:
+        res["dgate"] = torch.empty((T, H, D), **f32)
+    if rms_w is not None:
+        res["drms_w"] = torch.empty((D,), **f32)
+    res["dinitial_state"] = torch.empty((N, H, D, D), **f32)
+    if conv_state_in is not None:
+        res["dconv_state_in"] = torch.empty((N, 3 * H * D, 3), **f32)
+    _same_cuda_device(dy=dy, d_final_state=d_final_state, **res)
+    b = _lib.BackwardArgs()
+    b.fwd = _prefill_args(q, k, v, conv_w, g, beta, cu_dev, cu_host, chunk=64, gate=gate,
+                          rms_w=rms_w, eps_l2=eps_l2, eps_rms=eps_rms, scale=scale,
+                          initial_state=initial_state, final_state=None,
+                          conv_state_in=conv_state_in, conv_state_out=None, out=None,
+                          workspace=workspace, d_status=d_status, flags=0, check_cu_on_host=True)
+    b.fwd.out_dtype = _DT[dy.dtype]
+    b.dy = dy.data_ptr()
+    b.d_final_state = _p(d_final_state)
+    for name in ("dq", "dk", "dv", "dconv_w", "dg", "dbeta", "dgate", "drms_w", "dinitial_state",
+                 "dconv_state_in"):
+        setattr(b, name, res[name].data_ptr() if name in res else None)
+    if workspace is None:
+        n = ctypes.c_size_t(0)
+        st = lib.kda_backward_workspace_size(ctypes.byref(b), ctypes.byref(n))
+        if st:
+            raise KDAError(st, "kda_backward_workspace_size")
+        if n.value:
+            workspace = torch.empty(n.value, dtype=torch.uint8, device=dev)
+            b.fwd.workspace = workspace.data_ptr()
+            b.fwd.workspace_bytes = n.value
+    st = lib.kda_backward(ctypes.byref(b), _stream(stream))
+    if st:
+        raise KDAError(st, "kda_backward")
+    return res
+
+
+def kda_backward_workspace_size(cu_seqlens, H: int, D: int = 128) -> int:
+    """Workspace bytes kda_backward needs for these sequences and heads."""
+    lib = _lib.load()
+    host = np.ascontiguousarray(np.asarray(
+        cu_seqlens.detach().cpu() if isinstance(cu_seqlens, torch.Tensor) else cu_seqlens, dtype=np.int32))
+    b = _lib.BackwardArgs()
+    b.fwd.N, b.fwd.H, b.fwd.D, b.fwd.T_total = host.shape[0] - 1, H, D, int(host[-1]) if host.size else 0
+    b.fwd.cu_seqlens_host = host.ctypes.data
+    n = ctypes.c_size_t(0)
+    st = lib.kda_backward_workspace_size(ctypes.byref(b), ctypes.byref(n))
+    if st:
+        raise KDAError(st, "kda_backward_workspace_size")
+    return int(n.value)

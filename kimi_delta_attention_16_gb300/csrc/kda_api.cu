@@ -220,7 +220,7 @@ const char* kda_status_string(int status) {
 
 const char* kda_last_error(void) { return g_last_error.c_str(); }
 
-int kda_version(void) { return 1 * 10000 + 3 * 100 + 0; }
+int kda_version(void) { return 1 * 10000 + 4 * 100 + 0; }
 
 kda_status kda_short_conv(const void* x, int64_t x_row_stride, const float* w,
                           const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int N,
@@ -396,6 +396,102 @@ kda_status kda_gemm(const kda_gemm_args* g, kda_stream_t stream) {
     if (!kda::gemm_supported_device()) return fail(KDA_ERR_UNSUPPORTED, "kda_gemm needs an sm_103 device");
     const cudaError_t e = kda::launch_gemm(*g, reinterpret_cast<cudaStream_t>(stream));
     if (e) return cuda_fail(e, "gemm");
+    return ok();
+}
+
+// Validation of kda_backward (include/kda.h): sizes, dtypes, the host copy of cu_seqlens, every
+// required pointer, alignment, and that no output overlaps another output or an input.
+kda_status validate_backward(const kda_backward_args* b, kda::BackwardLayout* L) {
+    if (!b) return fail(KDA_ERR_INVALID_ARG, "args is NULL");
+    const kda_prefill_args& a = b->fwd;
+    if (a.N < 0 || a.H < 1 || a.T_total < 0)
+        return fail(KDA_ERR_INVALID_ARG, "bad sizes N=%d H=%d T_total=%lld", a.N, a.H, (long long)a.T_total);
+    if (a.D != 128) return fail(KDA_ERR_UNSUPPORTED, "kda_backward needs D = 128 (got %d)", a.D);
+    if (!valid_dtype(a.io) || !valid_dtype(a.out_dtype))
+        return fail(KDA_ERR_INVALID_ARG, "unknown dtype (io=%d out=%d)", (int)a.io, (int)a.out_dtype);
+    if ((int64_t)a.H * a.D * 3 > (int64_t)1 << 30 || (int64_t)a.N * a.H > 0x7fffffffLL)
+        return fail(KDA_ERR_UNSUPPORTED, "H*D or N*H too large");
+    if (!a.cu_seqlens_host) return fail(KDA_ERR_INVALID_ARG, "kda_backward needs cu_seqlens_host");
+    if (a.N > 0 && !a.cu_seqlens) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens is NULL");
+    if (kda_status st = check_host_cu(a.cu_seqlens_host, a.N, a.T_total)) return st;
+    *L = kda::backward_layout(*b);
+    if (a.N == 0) return KDA_OK;
+    if (!a.conv_w || !b->dconv_w) return fail(KDA_ERR_INVALID_ARG, "conv_w and dconv_w must be non-NULL");
+    const int64_t HD = (int64_t)a.H * a.D;
+    const size_t T = (size_t)a.T_total;
+    const int64_t xs = a.qkv_row_stride ? a.qkv_row_stride : HD;
+    const size_t rowf = T * HD * 4, sb = (size_t)a.N * HD * a.D * 4, cwb = (size_t)3 * HD * 16;
+    const size_t csb = (size_t)a.N * 3 * HD * 3;
+    size_t xb = 0;
+    if (a.T_total > 0) {
+        if (!a.q || !a.k || !a.v || !a.g || !a.beta || !b->dy || !b->dq || !b->dk || !b->dv || !b->dg ||
+            !b->dbeta)
+            return fail(KDA_ERR_INVALID_ARG, "q, k, v, g, beta, dy, dq, dk, dv, dg and dbeta must be non-NULL");
+        kda_status st;
+        if ((st = check_rows(a.q, xs, HD, a.io, "q")) || (st = check_rows(a.k, xs, HD, a.io, "k")) ||
+            (st = check_rows(a.v, xs, HD, a.io, "v")))
+            return st;
+        xb = (T - 1) * (size_t)xs * dsize(a.io) + HD * dsize(a.io);
+    }
+    const void* a16[] = {a.g, a.gate, a.conv_w, a.initial_state, b->dy, b->d_final_state, b->dq, b->dk, b->dv,
+                         b->dconv_w, b->dg, b->dgate, b->dinitial_state};
+    for (const void* p : a16)
+        if (p && !aligned(p, 16))
+            return fail(KDA_ERR_INVALID_ARG, "g, gate, conv_w, the states, dy and the tensor gradients must be "
+                                             "16-byte aligned");
+    const void* a4[] = {a.beta, a.rms_w, b->dbeta, b->drms_w, b->dconv_state_in};
+    for (const void* p : a4)
+        if (p && !aligned(p, 4)) return fail(KDA_ERR_INVALID_ARG, "beta, rms_w and their gradients must be 4-byte aligned");
+    struct Buf {
+        const void* p;
+        size_t n;
+    };
+    const Buf outs[] = {{b->dq, rowf}, {b->dk, rowf}, {b->dv, rowf}, {b->dconv_w, cwb}, {b->dg, rowf},
+                        {b->dbeta, T * a.H * 4}, {b->dgate, rowf}, {b->drms_w, (size_t)a.D * 4},
+                        {b->dinitial_state, sb}, {b->dconv_state_in, csb * 4}};
+    const Buf ins[] = {{a.q, xb}, {a.k, xb}, {a.v, xb}, {a.g, rowf}, {a.beta, T * a.H * 4},
+                       {a.gate, a.gate ? T * HD * dsize(a.io) : 0}, {a.conv_w, cwb},
+                       {a.conv_state_in, csb * dsize(a.io)}, {a.rms_w, (size_t)a.D * 4}, {a.initial_state, sb},
+                       {b->dy, T * HD * dsize(a.out_dtype)}, {b->d_final_state, sb},
+                       {a.workspace, L->total}};
+    const int no = sizeof(outs) / sizeof(outs[0]);
+    for (int i = 0; i < no; ++i) {
+        for (int j = i + 1; j < no; ++j)
+            if (overlap(outs[i].p, outs[i].n, outs[j].p, outs[j].n))
+                return fail(KDA_ERR_INVALID_ARG, "gradient outputs %d and %d overlap", i, j);
+        for (const Buf& in : ins)
+            if (overlap(outs[i].p, outs[i].n, in.p, in.n))
+                return fail(KDA_ERR_INVALID_ARG, "gradient output %d overlaps an input or the workspace", i);
+    }
+    if (L->total > 0) {
+        if (!a.workspace) return fail(KDA_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", L->total);
+        if (a.workspace_bytes < L->total)
+            return fail(KDA_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", a.workspace_bytes, L->total);
+        if (!aligned(a.workspace, 256)) return fail(KDA_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+    }
+    return KDA_OK;
+}
+
+kda_status kda_backward_workspace_size(const kda_backward_args* b, size_t* bytes) {
+    if (!bytes) return fail(KDA_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = 0;
+    if (!b) return fail(KDA_ERR_INVALID_ARG, "args is NULL");
+    const kda_prefill_args& a = b->fwd;
+    if (a.D != 128) return fail(KDA_ERR_UNSUPPORTED, "kda_backward needs D = 128 (got %d)", a.D);
+    if (a.T_total < 0 || a.H < 1 || a.N < 0) return fail(KDA_ERR_INVALID_ARG, "bad sizes");
+    if (!a.cu_seqlens_host) return fail(KDA_ERR_INVALID_ARG, "kda_backward needs cu_seqlens_host");
+    if (kda_status st = check_host_cu(a.cu_seqlens_host, a.N, a.T_total)) return st;
+    *bytes = kda::backward_layout(*b).total;
+    return ok();
+}
+
+kda_status kda_backward(const kda_backward_args* b, kda_stream_t stream) {
+    kda::BackwardLayout L{};
+    if (kda_status st = validate_backward(b, &L)) return st;
+    if (b->fwd.N == 0) return ok();
+    const cudaError_t e = kda::launch_backward(*b, L, static_cast<char*>(b->fwd.workspace),
+                                               reinterpret_cast<cudaStream_t>(stream));
+    if (e) return cuda_fail(e, "backward");
     return ok();
 }
 

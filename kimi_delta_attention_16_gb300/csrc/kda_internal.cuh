@@ -216,4 +216,19 @@ cudaError_t launch_short_prefill(const kda_prefill_args& a, cudaStream_t s);
 bool short_tma_applies(const kda_prefill_args& a);
 cudaError_t launch_short_tma(const kda_prefill_args& a, cudaStream_t s);
 
+// Backward pass (D = 128): byte offsets of its workspace parts (each 256-byte aligned).
+struct BackwardLayout {
+    size_t x;        // [T][3][H][D] fp32: q^, k^ (after the L2 norm) and v (after the conv)
+    size_t nrm;      // [T][H][2] fp32: the L2 denominators of q and k
+    size_t o;        // [T][H][D] fp32: o before the epilogue, then its gradient
+    size_t dx;       // [T][3][H][D] fp32: gradients of q^, k^, v, then of the conv outputs
+    size_t ckpt;     // [segments][H][D][D] fp32: the state at the start of every segment
+    int64_t slots;   // segments * H: checkpoint slots planned from the host copy of cu_seqlens
+    size_t scratch;  // [N][H][kBwdSeg][D][D] fp32: one segment's replayed states per unit
+    size_t total;
+};
+constexpr int kBwdSeg = 32;  // tokens per checkpointed segment of the backward pass
+BackwardLayout backward_layout(const kda_backward_args& b);  // needs fwd.cu_seqlens_host
+cudaError_t launch_backward(const kda_backward_args& b, const BackwardLayout& L, char* ws, cudaStream_t s);
+
 }  // namespace kda

@@ -277,3 +277,72 @@ def test_gemm_empty_problem_is_a_no_op_and_no_device_is_unsupported():
     import torch
     if not torch.cuda.is_available():
         assert lib.kda_gemm(ctypes.byref(_gemm_args()), None) == _lib.KDA_ERR_UNSUPPORTED
+
+
+def _bwd_args(**kw):
+    """kda_backward arguments for N = 2 sequences (40 + 24 tokens), H = 2, D = 128."""
+    b = _lib.BackwardArgs()
+    a, _ = _args()
+    cu = np.array([0, 40, 64], np.int32)
+    a.N, a.cu_seqlens_host = 2, cu.ctypes.data
+    a.out = None
+    b.fwd = a
+    b._keep = cu
+    b.dy = FAKE + 0x700000
+    base = FAKE + 0x1000000
+    for i, n in enumerate(("dq", "dk", "dv", "dconv_w", "dg", "dbeta")):
+        setattr(b, n, base + i * 0x100000)
+    for k, v in kw.items():
+        if k.startswith("fwd."):
+            setattr(b.fwd, k[4:], v)
+        else:
+            setattr(b, k, v)
+    return b
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("fwd.D", 64, _lib.KDA_ERR_UNSUPPORTED),
+    ("fwd.io", 9, _lib.KDA_ERR_INVALID_ARG),
+    ("fwd.cu_seqlens_host", None, _lib.KDA_ERR_INVALID_ARG),   # the layout is planned on the host
+    ("fwd.T_total", 63, _lib.KDA_ERR_INVALID_ARG),              # cu[N] != T_total
+    ("fwd.q", None, _lib.KDA_ERR_INVALID_ARG),
+    ("dy", None, _lib.KDA_ERR_INVALID_ARG),
+    ("dbeta", None, _lib.KDA_ERR_INVALID_ARG),
+    ("dconv_w", None, _lib.KDA_ERR_INVALID_ARG),
+    ("dq", FAKE + 0x1000004, _lib.KDA_ERR_INVALID_ARG),         # misaligned
+    ("dk", FAKE + 0x1000000 + 4096, _lib.KDA_ERR_INVALID_ARG),  # overlaps dq
+    ("dg", FAKE + 0x400000, _lib.KDA_ERR_INVALID_ARG),          # aliases the input g
+    ("dgate", FAKE + 0x10000000, _lib.KDA_ERR_INVALID_ARG),     # inside the workspace
+    ("fwd.workspace", None, _lib.KDA_ERR_WORKSPACE),
+    ("fwd.workspace_bytes", 1024, _lib.KDA_ERR_WORKSPACE),
+])
+def test_backward_rejects_bad_arguments(field, value, code):
+    lib = _lib.load()
+    b = _bwd_args(**{field: value})
+    assert lib.kda_backward(ctypes.byref(b), None) == code
+    assert lib.kda_last_error()
+
+
+def test_backward_workspace_size_matches_the_stated_layout():
+    """T H D 28 + T H 8 + segs H D^2 4 + N H 32 D^2 4 bytes, each part rounded up to 256,
+    segs = sum over sequences of ceil(len / 32)."""
+    lib = _lib.load()
+    r = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    for lengths, H in [([40, 24], 2), ([0, 1, 33, 0, 64], 3), ([8192], 96), ([], 4)]:
+        cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+        b = _bwd_args(**{"fwd.N": len(lengths), "fwd.H": H, "fwd.T_total": int(cu[-1]),
+                         "fwd.cu_seqlens_host": cu.ctypes.data})
+        n = ctypes.c_size_t()
+        assert lib.kda_backward_workspace_size(ctypes.byref(b), ctypes.byref(n)) == 0
+        T, D = int(cu[-1]), 128
+        segs = sum((L + 31) // 32 for L in lengths)
+        want = (r(T * 3 * H * D * 4) + r(T * H * 2 * 4) + r(T * H * D * 4) + r(T * 3 * H * D * 4)
+                + r(segs * H * D * D * 4) + r(len(lengths) * H * 32 * D * D * 4))
+        assert n.value == want, (lengths, H)
+
+
+def test_backward_with_no_sequences_is_a_no_op():
+    lib = _lib.load()
+    cu = np.array([0], np.int32)
+    b = _bwd_args(**{"fwd.N": 0, "fwd.T_total": 0, "fwd.cu_seqlens_host": cu.ctypes.data})
+    assert lib.kda_backward(ctypes.byref(b), None) == _lib.KDA_OK
