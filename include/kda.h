@@ -342,10 +342,15 @@ kda_status kda_gemm(const kda_gemm_args* args, kda_stream_t stream);
  * does not depend on the forward's path.
  *
  * Method: conv + SiLU + L2 norms recomputed per token; the recurrence replayed
- * once per (sequence, head) storing the state at the start of every 32-token
- * segment (the checkpoints); the epilogue's derivative per row; then, segment by segment from the end, the segment's
- * states replayed from its checkpoint and its tokens run backwards carrying
- * dS (D x D fp32); then the L2 norm's, SiLU's and the conv's derivatives.
+ * once, split by value column (each column of S evolves on its own), saving
+ * o_t, e_t = v_t - S_bar^T k_t and the state at the start of every 64-token
+ * segment; the epilogue's derivative per row; the state gradient run once
+ * backwards, also by column, saving w_t = dS^T k_t and the gradient at the end
+ * of every segment; then every segment in parallel, by row (with e and w known,
+ * each row of S and of dS evolves on its own): dq, dk and the log-decay's
+ * gradient, which follows from g entering only through the decayed read keys
+ * and queries and the un-decayed written keys; last the L2 norm's, SiLU's and
+ * the conv's derivatives.  No per-token state is stored.
  *
  * Needs cu_seqlens_host (the checkpoint layout is planned on the host).  The
  * outputs must not overlap each other or any input.  dconv_w and drms_w are
@@ -370,11 +375,10 @@ typedef struct {
 } kda_backward_args;
 
 /* Bytes of workspace kda_backward needs (reads fwd.N, H, D, T_total and
- * fwd.cu_seqlens_host, which is required):
- *   T_total H D 28 + T_total H 8 + segs H D^2 4 + N H 32 D^2 4
- * (each part rounded up to 256), segs = the sum over sequences of ceil(len / 32):
- * 1.6 GB of checkpoints for 8192 tokens of 96 heads, 2 MiB of replay scratch per
- * (sequence, head). */
+ * fwd.cu_seqlens_host, which is required), each part rounded up to 256:
+ *   36 T_total H D + 12 T_total H + 8 slots D^2 + 4 slots D + 4 N H D + 8 (N + 1),
+ * slots = H times the sum over sequences of ceil(len / 64): 5.2 GB for one
+ * sequence of 8192 tokens with 96 heads. */
 kda_status kda_backward_workspace_size(const kda_backward_args* args, size_t* bytes);
 
 kda_status kda_backward(const kda_backward_args* args, kda_stream_t stream);

@@ -1,6 +1,6 @@
 // kda_backward.cu -- the backward pass of the KDA layer (training): reverse-mode
 // derivatives of sum(dy . out) + sum(dS . final_state) with respect to every
-// input of kda_prefill, D = 128, fp32 arithmetic.
+// input of kda_prefill, D = 128, fp32 arithmetic (IEEE exp, SiLU, sigmoid).
 //
 // Page "Kimi K3 / Architecture", KDA panel (the layer: short conv + SiLU, L2
 // norms of q and k, the recurrent state decayed, corrected and written per
@@ -10,24 +10,21 @@
 // section (the four moves, each an affine map of the state, whose adjoints run
 // the same steps backwards).
 //
-// Steps, for each (sequence, head) unit (P = Diag(alpha_t) S_{t-1},
-// e = v - P^T k, S_t = P + beta k e^T, o_t = scale S_t^T q):
-//   prep       conv + SiLU + L2 norms: q^, k^, v (fp32) and |a_q|, |a_k|   (one warp per token-head)
-//   replay     the forward recurrence token by token: o_t, and the state at the start of
-//              every kSeg-token segment (checkpoints)                        (one CTA per unit)
-//   epilogue   y = n w sig(z), n = o r:  do = r dn - r^3 o (dn . o) / D, dz, dw   (one warp per row)
-//   recurrence segments in reverse; each replays its states from its checkpoint into a per-unit
-//              scratch, then runs the tokens backwards carrying dS in registers:
-//                dS += scale q do^T;  dq = scale S_t do;  w = dS^T k;  dv = beta w;
-//                dbeta = w . e;  dk = beta (dS e - P w);  dP = dS - beta k w^T;
-//                dg = rowsum(dP . P);  dS <- Diag(alpha) dP                (one CTA per unit)
-//   L2         da = (dx - x (x . dx)) / |a|, in place                          (one warp per row)
-//   conv       du = da sig(u) (1 + u (1 - sig(u))); dx_{t-3+j} += w_j du_t; dw_j += x_{t-3+j} du_t;
-//              positions before the sequence give the conv state's gradient (one thread per
-//              (sequence, channel), tokens walked backwards)
-// The recurrence kernels hold the state as in the decode kernel: thread (warp w, lane l) owns rows
-// 16 w .. 16 w + 15 of columns 4 l .. 4 l + 3; column sums over the rows go through per-warp
-// partials in shared memory, row sums over the columns through warp shuffles.
+// Per (sequence, head) unit, with P_t = Diag(alpha_t) S_{t-1}, e_t = v_t - P_t^T k_t,
+// S_t = P_t + beta_t k_t e_t^T, o_t = scale S_t^T q_t:
+//   prep      conv + SiLU + L2 norms: q^, k^, v (fp32) and |a_q|, |a_k|      (warp per token-head)
+//   forward   the recurrence in column layout (each value column of S evolves on its own):
+//             o_t, e_t, and S at the start of every kSeg-token segment          (4 CTAs per unit)
+//   epilogue  y = n w sig(z), n = o r:  do = r dn - r^3 o (dn . o) / D, dgate, drms_w  (warp per row)
+//   backward  the state gradient in column layout, tokens in reverse (each column of dS evolves
+//             on its own): w_t = dS'^T k, dv = beta w, dbeta = w . e, e . do, and dS at the end
+//             of every segment                                                  (4 CTAs per unit)
+//   rows      per (unit, segment), all in parallel, row layout (with e, w and do known, each row
+//             of S and of dS evolves on its own): dq, dk and dg (see k_bwd_rows)
+//   carry     dg's sums over later segments and the final-state term
+//   L2        da = (dx - x (x . dx)) / |a|, in place; dg += carry                 (warp per row)
+//   conv      du = da sig(u) (1 + u (1 - sig(u))); dx, the taps' and the conv state's gradients
+// No token's state is stored: the row kernels replay at most kSeg tokens from the checkpoints.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -36,7 +33,6 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kSeg = kBwdSeg;  // tokens per checkpointed segment
-constexpr int kRecThreads = 256;
 
 __device__ __forceinline__ float4 f4_fma(float a, float4 x, float4 y) {
     return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
@@ -49,53 +45,6 @@ __device__ __forceinline__ float warp_sum(float v) {
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
     return v;
 }
-// Sums 16 per-lane values over the 32 lanes of a warp; afterwards lane l holds the total of
-// value (l >> 1) (lanes 2 i and 2 i + 1 both hold value i).
-__device__ __forceinline__ float reduce16(float (&v)[16], int lane) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const bool up = (lane & 16) != 0;
-        const float send = up ? v[i] : v[i + 8];
-        v[i] = (up ? v[i + 8] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const bool up = (lane & 8) != 0;
-        const float send = up ? v[i] : v[i + 4];
-        v[i] = (up ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const bool up = (lane & 4) != 0;
-        const float send = up ? v[i] : v[i + 2];
-        v[i] = (up ? v[i + 2] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
-    }
-    {
-        const bool up = (lane & 2) != 0;
-        const float send = up ? v[0] : v[1];
-        v[0] = (up ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, send, 2);
-    }
-    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
-}
-
-// First checkpoint slot of unit (n, h): sequences in order, each holding H runs of its segment
-// count.  -1 when the unit's slots would end past `slots` (the host planned the layout from its
-// copy of cu_seqlens; a device copy that disagrees must not send writes out of the workspace).
-__device__ __forceinline__ int64_t ckpt_base(const int32_t* cu, int n, int64_t T_total, int H, int h,
-                                             int64_t slots) {
-    int64_t b = 0;
-    for (int m = 0; m < n; ++m) {
-        int64_t a, e;
-        seq_range(cu, m, T_total, a, e);
-        b += (e - a + kSeg - 1) / kSeg;
-    }
-    int64_t a, e;
-    seq_range(cu, n, T_total, a, e);
-    const int64_t ns = (e - a + kSeg - 1) / kSeg;
-    const int64_t base = b * H + (int64_t)h * ns;
-    return base + ns <= slots ? base : -1;
-}
-
 // ------------------------------------------------------------------------------ prep
 // One warp per (token, head): conv + SiLU of the q, k, v channels of the head (lane l: channels
 // 4 l .. 4 l + 3), the L2 norms of q and k.  X: [T][3][H][D] fp32 (q^, k^, v), nrm: [T][H][2].
@@ -150,95 +99,590 @@ __global__ void k_bwd_prep(const Tio* __restrict__ q, const Tio* __restrict__ k,
     if (lane == 0) *reinterpret_cast<float2*>(nrm + row * 2) = make_float2(nq, nk);
 }
 
-// ------------------------------------------------------------------------------ recurrence pieces
-// Per-token factors of one unit staged in shared memory: q^, k^, v, alpha, and (backward) do.
-struct TokRows {
-    float q[kD], k[kD], v[kD], a[kD];
+// ------------------------------------------------------------------------------ staging helpers
+// 16-byte and 4-byte asynchronous global -> shared copies (cp.async), one group per staged block.
+__device__ __forceinline__ void cp16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// First checkpoint slot of unit (n, h): sequences in order, each holding H runs of its segment
+// count (prefix[n] = segments of the sequences before n).  -1 when the unit's slots would end
+// past `slots` (the host planned the layout from its copy of cu_seqlens; a device copy that
+// disagrees must not send accesses out of the workspace).
+__device__ __forceinline__ int64_t slot_base(const int64_t* prefix, int n, int H, int h, int64_t nseg,
+                                             int64_t slots) {
+    const int64_t base = prefix[n] * H + (int64_t)h * nseg;
+    return (base >= 0 && base + nseg <= slots) ? base : -1;
+}
+
+// prefix[n] = sum over sequences m < n of ceil(len_m / kSeg), n = 0..N.  One block of 256.
+__global__ void k_bwd_seg_prefix(const int32_t* __restrict__ cu, int N, int64_t T_total,
+                                 int64_t* __restrict__ prefix) {
+    __shared__ int64_t part[256];
+    const int tid = threadIdx.x;
+    const int per = (N + 255) / 256;
+    const int a = tid * per < N ? tid * per : N, b = a + per < N ? a + per : N;
+    int64_t sum = 0;
+    for (int n = a; n < b; ++n) {
+        int64_t s0, s1;
+        seq_range(cu, n, T_total, s0, s1);
+        sum += (s1 - s0 + kSeg - 1) / kSeg;
+    }
+    part[tid] = sum;
+    __syncthreads();
+    if (tid == 0) {
+        int64_t run = 0;
+        for (int i = 0; i < 256; ++i) {
+            const int64_t x = part[i];
+            part[i] = run;
+            run += x;
+        }
+        prefix[N] = run;
+    }
+    __syncthreads();
+    int64_t run = part[tid];
+    for (int n = a; n < b; ++n) {
+        prefix[n] = run;
+        int64_t s0, s1;
+        seq_range(cu, n, T_total, s0, s1);
+        run += (s1 - s0 + kSeg - 1) / kSeg;
+    }
+}
+
+// ------------------------------------------------------------------------------ column-layout sweeps
+// One unit's state is split by value column over kColCtas CTAs of 8 warps.  Lane l of warp w owns
+// column c = 32 cq + 4 w + (l >> 3) and rows 16 r .. 16 r + 15, r = l & 7.  A per-column quantity
+// of a token (e, o, w = dS^T k) is a sum over the rows of its column: eight lanes, three shuffles.
+// No CTA barrier inside a token; tokens are staged kTB at a time (double-buffered cp.async), three
+// barriers per block.
+constexpr int kColCtas = 4;           // CTAs per unit (32 columns each)
+constexpr int kCols = kD / kColCtas;  // 32
+constexpr int kTB = 16;               // tokens per staged block
+constexpr int kPerm = 160;            // a staged 128-vector: 8 slices of 16 rows, 20 floats apart
+__device__ __forceinline__ int perm_off(int row) { return (row >> 4) * 20 + (row & 15); }
+
+// One staged token: k^, exp(g), q^ (permuted so that the eight row slices a warp reads at once fall
+// in distinct banks), two slices of the CTA's 32 columns, beta.
+struct ColTok {
+    float k[kPerm], a[kPerm], q[kPerm];
+    float c0[kCols], c1[kCols];  // forward sweep: v; backward sweep: do and e
+    float beta, pad[3];
+};
+constexpr int kColSmem = 2 * kTB * (int)sizeof(ColTok);
+
+struct ColSrc {
+    const float* p;  // element (token 0, head 0, channel 0)
+    int64_t stride;  // elements between tokens
 };
 
-// One forward step of the state held by this thread (rows r0 .. r0+15, columns c0 .. c0+3):
-// s <- P + beta k e^T with P = Diag(alpha) s and e = v - P^T k.  red: [8][kD] partials.
-// Two barriers of the CTA.  Leaves e (this thread's 4 columns) in *e_out.
-__device__ __forceinline__ void fwd_step(float4 (&s)[16], const TokRows& tr, float beta, int r0, int c0, int warp,
-                                         float (*red)[kD], float4* e_out) {
-    float4 cp = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        s[i] = f4_mul(tr.a[r0 + i], s[i]);
-        cp = f4_fma(tr.k[r0 + i], s[i], cp);
-    }
-    *reinterpret_cast<float4*>(&red[warp][c0]) = cp;
-    __syncthreads();
-    float4 pk = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int w = 0; w < 8; ++w) pk = f4_add(pk, *reinterpret_cast<const float4*>(&red[w][c0]));
-    const float4 vv = *reinterpret_cast<const float4*>(&tr.v[c0]);
-    const float4 e = make_float4(vv.x - pk.x, vv.y - pk.y, vv.z - pk.z, vv.w - pk.w);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) s[i] = f4_fma(beta * tr.k[r0 + i], e, s[i]);
-    *e_out = e;
-    __syncthreads();  // red is free again
-}
-
-// Stages token t's rows (threads 0..127: one channel each).
-__device__ __forceinline__ void stage_rows(TokRows& tr, const float* X, const float* g, int64_t t, int H, int h,
-                                           int tid) {
-    if (tid < kD) {
-        const int64_t HD = (int64_t)H * kD;
-        const float* xr = X + t * 3 * HD + (int64_t)h * kD + tid;
-        tr.q[tid] = xr[0];
-        tr.k[tid] = xr[HD];
-        tr.v[tid] = xr[2 * HD];
-        tr.a[tid] = expf(g[(t * H + h) * kD + tid]);
+// Issues the copies of tokens [t0, t0 + nt) of head h into st[0 .. nt): the three row vectors
+// (q^ and k^ from X, g into the alpha slot), `ncs` column slices (the CTA's 32 columns), beta.
+__device__ __forceinline__ void stage_cols(ColTok* st, int64_t t0, int nt, const float* X, const float* g,
+                                           const float* beta, ColSrc s0, ColSrc s1, int ncs, int H, int h,
+                                           int cq, int tid) {
+    const int64_t HD = (int64_t)H * kD;
+    const int per = 96 + 8 * ncs + 1;
+    for (int idx = tid; idx < nt * per; idx += 256) {
+        const int tk = idx / per, j = idx - tk * per;
+        const int64_t t = t0 + tk;
+        ColTok& s = st[tk];
+        if (j < 96) {
+            const int part = j >> 5, jj = j & 31;
+            const float* src = part == 0 ? X + t * 3 * HD + HD + (int64_t)h * kD
+                             : part == 1 ? g + (t * H + h) * kD
+                                         : X + t * 3 * HD + (int64_t)h * kD;
+            float* dst = part == 0 ? s.k : part == 1 ? s.a : s.q;
+            cp16(dst + (jj >> 2) * 20 + (jj & 3) * 4, src + jj * 4);
+        } else if (j < 96 + 8 * ncs) {
+            const int jj = j - 96;
+            const ColSrc& cs = jj < 8 ? s0 : s1;
+            cp16((jj < 8 ? s.c0 : s.c1) + (jj & 7) * 4, cs.p + t * cs.stride + (int64_t)h * kD + cq * kCols + (jj & 7) * 4);
+        } else {
+            cp4(&s.beta, beta + t * H + h);
+        }
     }
 }
 
-// ------------------------------------------------------------------------------ replay
-// The forward recurrence of one unit per CTA: o_t (scale S_t^T q^) for every token into O, and
-// the state at the start of every segment into the checkpoints.
-__global__ void __launch_bounds__(kRecThreads, 1)
-k_bwd_replay(const float* __restrict__ X, const float* __restrict__ g, const float* __restrict__ beta,
-             const int32_t* __restrict__ cu, int64_t T_total, int H, float scale, const float* __restrict__ S0,
-             float* __restrict__ O, float* __restrict__ ckpt, int64_t slots, int* __restrict__ d_status) {
-    __shared__ __align__(16) TokRows tr;
-    __shared__ __align__(16) float red[8][kD];
-    const int u = blockIdx.x, n = u / H, h = u % H;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r0 = 16 * warp, c0 = 4 * lane;
+// exp(g) in place for the staged tokens (after the copies have landed and a barrier).
+__device__ __forceinline__ void stage_exp_cols(ColTok* st, int nt, int tid) {
+    for (int idx = tid; idx < nt * kD; idx += 256) {
+        float& x = st[idx >> 7].a[perm_off(idx & 127)];
+        x = expf(x);
+    }
+}
+
+__device__ __forceinline__ void load16(const float* p, float (&x)[16]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 f = reinterpret_cast<const float4*>(p)[i];
+        x[4 * i] = f.x;
+        x[4 * i + 1] = f.y;
+        x[4 * i + 2] = f.z;
+        x[4 * i + 3] = f.w;
+    }
+}
+__device__ __forceinline__ float sum8(float x) {  // over the 8 lanes of one column (lane bits 0..2)
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    return x;
+}
+
+// Forward sweep: the recurrence from the initial state; o_t and e_t of every token; the state at
+// the start of every kSeg-token segment (Sck).  Grid: units x kColCtas CTAs of 256 threads.
+__global__ void __launch_bounds__(256)
+k_bwd_fwd_cols(const float* __restrict__ X, const float* __restrict__ g, const float* __restrict__ beta,
+               const int32_t* __restrict__ cu, const int64_t* __restrict__ prefix, int64_t T_total, int H,
+               float scale, const float* __restrict__ S0, float* __restrict__ O, float* __restrict__ E,
+               float* __restrict__ Sck, int64_t slots, int* __restrict__ d_status) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    ColTok* buf = reinterpret_cast<ColTok*>(smem_raw);  // [2][kTB]
+    const int u = blockIdx.x / kColCtas, cq = blockIdx.x % kColCtas, n = u / H, h = u % H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane & 7;
+    const int cl = warp * 4 + (lane >> 3), c = cq * kCols + cl;
     int64_t s0, s1;
     seq_range(cu, n, T_total, s0, s1);
-    const int64_t cb = ckpt_base(cu, n, T_total, H, h, slots);
-    if (cb < 0) {
+    const int64_t nseg = (s1 - s0 + kSeg - 1) / kSeg;
+    const int64_t sb = slot_base(prefix, n, H, h, nseg, slots);
+    if (sb < 0) {
         if (tid == 0) flag_status(d_status, KDA_ERR_DEVICE_ARG);
         return;
     }
-    float4 s[16];
+    const int64_t HD = (int64_t)H * kD;
+    const ColSrc vs{X + 2 * HD, 3 * HD};
+    float s[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-        s[i] = S0 ? *reinterpret_cast<const float4*>(S0 + ((int64_t)u * kD + r0 + i) * kD + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t t = s0; t < s1; ++t) {
-        if ((t - s0) % kSeg == 0) {
-            float* dst = ckpt + (cb + (t - s0) / kSeg) * kD * kD;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) *reinterpret_cast<float4*>(dst + (r0 + i) * kD + c0) = s[i];
-        }
-        stage_rows(tr, X, g, t, H, h, tid);
+    for (int m = 0; m < 16; ++m) s[m] = S0 ? S0[((int64_t)u * kD + 16 * r + m) * kD + c] : 0.f;
+    const int64_t nblk = (s1 - s0 + kTB - 1) / kTB;
+    auto nt_of = [&](int64_t b) { return (int)(s1 - (s0 + b * kTB) < kTB ? s1 - (s0 + b * kTB) : kTB); };
+    if (nblk > 0) stage_cols(buf, s0, nt_of(0), X, g, beta, vs, vs, 1, H, h, cq, tid);
+    cp_commit();
+    for (int64_t b = 0; b < nblk; ++b) {
+        __syncthreads();  // block b - 1 is consumed: its buffer takes block b + 1
+        if (b + 1 < nblk)
+            stage_cols(buf + ((b + 1) & 1) * kTB, s0 + (b + 1) * kTB, nt_of(b + 1), X, g, beta, vs, vs, 1, H, h,
+                       cq, tid);
+        cp_commit();
+        cp_wait<1>();
         __syncthreads();
-        float4 e;
-        fwd_step(s, tr, beta[t * H + h], r0, c0, warp, red, &e);
-        // o = scale S_t^T q^: column sums over the rows
-        float4 co = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) co = f4_fma(tr.q[r0 + i], s[i], co);
-        *reinterpret_cast<float4*>(&red[warp][c0]) = co;
+        ColTok* st = buf + (b & 1) * kTB;
+        const int nt = nt_of(b);
+        stage_exp_cols(st, nt, tid);
         __syncthreads();
-        if (warp == 0) {
-            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int tk = 0; tk < nt; ++tk) {
+            const int64_t t = s0 + b * kTB + tk;
+            if ((t - s0) % kSeg == 0) {
+                float* dst = Sck + (sb + (t - s0) / kSeg) * kD * kD;
 #pragma unroll
-            for (int w = 0; w < 8; ++w) o = f4_add(o, *reinterpret_cast<const float4*>(&red[w][c0]));
-            *reinterpret_cast<float4*>(O + (t * H + h) * kD + c0) = f4_mul(scale, o);
+                for (int m = 0; m < 16; ++m) dst[(16 * r + m) * kD + c] = s[m];
+            }
+            const ColTok& T = st[tk];
+            float kk[16], aa[16];
+            load16(T.k + r * 20, kk);
+            load16(T.a + r * 20, aa);
+            float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; m += 2) {
+                s[m] *= aa[m];
+                s[m + 1] *= aa[m + 1];
+                p0 = fmaf(kk[m], s[m], p0);
+                p1 = fmaf(kk[m + 1], s[m + 1], p1);
+            }
+            const float e = T.c0[cl] - sum8(p0 + p1);
+            const float be = T.beta * e;
+            float qq[16];
+            load16(T.q + r * 20, qq);
+            float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; m += 2) {
+                s[m] = fmaf(kk[m], be, s[m]);
+                s[m + 1] = fmaf(kk[m + 1], be, s[m + 1]);
+                o0 = fmaf(qq[m], s[m], o0);
+                o1 = fmaf(qq[m + 1], s[m + 1], o1);
+            }
+            const float o = sum8(o0 + o1);
+            if (r == 0) {
+                O[(t * H + h) * kD + c] = scale * o;
+                E[(t * H + h) * kD + c] = e;
+            }
         }
-        __syncthreads();  // red and tr are reused by the next token
+    }
+}
+
+// Backward sweep of the state gradient, tokens in reverse: dS' = dS + scale q^ do^T,
+// w = dS'^T k^, dv = beta w, then dS <- Diag(alpha) (dS' - beta k^ w^T).  Writes w, dv, the sums
+// dbeta = w . e and e . do of every token (atomics over the CTAs of a unit), the state gradient at
+// the end of every segment (dSck: before that token's own terms) and at the start (dS0).
+__global__ void __launch_bounds__(256)
+k_bwd_bwd_cols(const float* __restrict__ X, const float* __restrict__ g, const float* __restrict__ beta,
+               const float* __restrict__ dO, const float* __restrict__ E, const int32_t* __restrict__ cu,
+               const int64_t* __restrict__ prefix, int64_t T_total, int H, float scale,
+               const float* __restrict__ dS_fin, float* __restrict__ W, float* __restrict__ dX,
+               float* __restrict__ dbeta, float* __restrict__ edo, float* __restrict__ dSck,
+               float* __restrict__ dS0, int64_t slots) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    ColTok* buf = reinterpret_cast<ColTok*>(smem_raw);  // [2][kTB]
+    __shared__ float acc[2][2][kTB];                   // [block parity][dbeta, e.do][token]
+    const int u = blockIdx.x / kColCtas, cq = blockIdx.x % kColCtas, n = u / H, h = u % H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane & 7;
+    const int cl = warp * 4 + (lane >> 3), c = cq * kCols + cl;
+    if (tid < 4 * kTB) (&acc[0][0][0])[tid] = 0.f;
+    int64_t s0, s1;
+    seq_range(cu, n, T_total, s0, s1);
+    const int64_t nseg = (s1 - s0 + kSeg - 1) / kSeg;
+    const int64_t sb = slot_base(prefix, n, H, h, nseg, slots);
+    if (sb < 0) return;  // flagged by the forward sweep
+    const int64_t HD = (int64_t)H * kD;
+    const ColSrc ds_src{dO, HD}, es{E, HD};
+    float ds[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) ds[m] = dS_fin ? dS_fin[((int64_t)u * kD + 16 * r + m) * kD + c] : 0.f;
+    // block b holds tokens [t0(b), s1 - b kTB), t0(b) = max(s0, s1 - (b + 1) kTB)
+    const int64_t nblk = (s1 - s0 + kTB - 1) / kTB;
+    auto t0_of = [&](int64_t b) { return s1 - (b + 1) * kTB > s0 ? s1 - (b + 1) * kTB : s0; };
+    auto nt_of = [&](int64_t b) { return (int)(s1 - b * kTB - t0_of(b)); };
+    if (nblk > 0) stage_cols(buf, t0_of(0), nt_of(0), X, g, beta, ds_src, es, 2, H, h, cq, tid);
+    cp_commit();
+    for (int64_t b = 0; b < nblk; ++b) {
+        __syncthreads();
+        if (b > 0 && tid < nt_of(b - 1)) {  // the sums of block b - 1 are complete
+            const int p = (b - 1) & 1;
+            const int64_t t = t0_of(b - 1) + tid;
+            atomicAdd(dbeta + t * H + h, acc[p][0][tid]);
+            atomicAdd(edo + t * H + h, acc[p][1][tid]);
+            acc[p][0][tid] = 0.f;
+            acc[p][1][tid] = 0.f;
+        }
+        if (b + 1 < nblk)
+            stage_cols(buf + ((b + 1) & 1) * kTB, t0_of(b + 1), nt_of(b + 1), X, g, beta, ds_src, es, 2, H, h,
+                       cq, tid);
+        cp_commit();
+        cp_wait<1>();
+        __syncthreads();
+        ColTok* st = buf + (b & 1) * kTB;
+        const int nt = nt_of(b);
+        const int64_t t0 = t0_of(b);
+        stage_exp_cols(st, nt, tid);
+        __syncthreads();
+        for (int tk = nt - 1; tk >= 0; --tk) {
+            const int64_t t = t0 + tk;
+            if ((t - s0) % kSeg == kSeg - 1 || t == s1 - 1) {
+                float* dst = dSck + (sb + (t - s0) / kSeg) * kD * kD;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) dst[(16 * r + m) * kD + c] = ds[m];
+            }
+            const ColTok& T = st[tk];
+            const float do_c = T.c0[cl], e_c = T.c1[cl], bt = T.beta;
+            float kk[16], qq[16];
+            load16(T.k + r * 20, kk);
+            load16(T.q + r * 20, qq);
+            const float sd = scale * do_c;
+            float w0 = 0.f, w1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; m += 2) {
+                ds[m] = fmaf(qq[m], sd, ds[m]);
+                ds[m + 1] = fmaf(qq[m + 1], sd, ds[m + 1]);
+                w0 = fmaf(kk[m], ds[m], w0);
+                w1 = fmaf(kk[m + 1], ds[m + 1], w1);
+            }
+            const float w = sum8(w0 + w1);
+            float aa[16];
+            load16(T.a + r * 20, aa);
+            const float nbw = -bt * w;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) ds[m] = aa[m] * fmaf(kk[m], nbw, ds[m]);
+            float pb = 0.f, pe = 0.f;
+            if (r == 0) {
+                W[(t * H + h) * kD + c] = w;
+                dX[t * 3 * HD + 2 * HD + (int64_t)h * kD + c] = bt * w;
+                pb = w * e_c;
+                pe = e_c * do_c;
+            }
+            pb += __shfl_xor_sync(0xffffffffu, pb, 8);
+            pb += __shfl_xor_sync(0xffffffffu, pb, 16);
+            pe += __shfl_xor_sync(0xffffffffu, pe, 8);
+            pe += __shfl_xor_sync(0xffffffffu, pe, 16);
+            if (lane == 0) {
+                atomicAdd(&acc[b & 1][0][tk], pb);
+                atomicAdd(&acc[b & 1][1][tk], pe);
+            }
+        }
+    }
+    __syncthreads();
+    if (nblk > 0 && tid < nt_of(nblk - 1)) {
+        const int p = (nblk - 1) & 1;
+        const int64_t t = t0_of(nblk - 1) + tid;
+        atomicAdd(dbeta + t * H + h, acc[p][0][tid]);
+        atomicAdd(edo + t * H + h, acc[p][1][tid]);
+    }
+    if (dS0)
+#pragma unroll
+        for (int m = 0; m < 16; ++m) dS0[((int64_t)u * kD + 16 * r + m) * kD + c] = ds[m];
+}
+
+// ------------------------------------------------------------------------------ row-layout segments
+// One CTA of 512 threads per (unit, segment): thread (rg, cg) owns rows 4 rg .. 4 rg + 3 and columns
+// 8 cg .. 8 cg + 7; the row sums a token needs (S x, dS' e) go over the 16 column groups of a
+// half-warp.  With e, w and do known for every token, both sweeps are row-local:
+//   forward from the segment's start state:  dq = scale (P do + beta k (e . do)),
+//                                            dk_read = -beta P w,   P = Diag(alpha) S_{t-1};
+//   backward from the segment's end gradient: dk_write = beta dS' e.
+// dg follows from the decay entering only through e^{Gamma_t} (read keys and queries) and
+// e^{-Gamma_t} (written keys), Gamma_t = sum_{s <= t} g_s:
+//   dGamma_t = q^ dq + k^ dk_read - k^ dk_write,  dg_t = sum_{s >= t} dGamma_s + rowsum(dS_T . S_T);
+// here the sums within the segment, the segment's total (segtot) and, for the last segment of a
+// sequence, the final-state term (fin).
+constexpr int kRowThreads = 512;
+struct RowTok {
+    float k[kD], a[kD], q[kD], e[kD], d[kD], w[kD];
+    float beta, edo, pad[2];
+};
+constexpr int kRowSmem = kSeg * (int)sizeof(RowTok);
+
+// Sums 8 per-thread values over the 16 lanes of a half-warp (lane bits 0..3); afterwards lane
+// cg holds the total of value cg >> 1.
+__device__ __forceinline__ float reduce8_16(float (&v)[8], int cg) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const bool up = (cg & 8) != 0;
+        const float send = up ? v[i] : v[i + 4];
+        v[i] = (up ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const bool up = (cg & 4) != 0;
+        const float send = up ? v[i] : v[i + 2];
+        v[i] = (up ? v[i + 2] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    {
+        const bool up = (cg & 2) != 0;
+        const float send = up ? v[0] : v[1];
+        v[0] = (up ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+// Same for 4 values; afterwards lane cg holds the total of value cg >> 2.
+__device__ __forceinline__ float reduce4_16(float (&v)[4], int cg) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const bool up = (cg & 8) != 0;
+        const float send = up ? v[i] : v[i + 2];
+        v[i] = (up ? v[i + 2] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    {
+        const bool up = (cg & 4) != 0;
+        const float send = up ? v[0] : v[1];
+        v[0] = (up ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
+__device__ __forceinline__ float pick4(float4 v, int a) {  // component a of v, without local memory
+    return a == 0 ? v.x : a == 1 ? v.y : a == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ void load8f(const float* p, float (&x)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+// Grid: units x max_seg CTAs (CTAs past a sequence's segment count return at once).
+__global__ void __launch_bounds__(kRowThreads, 1)
+k_bwd_rows(const float* __restrict__ X, const float* __restrict__ g, const float* __restrict__ beta,
+           const float* __restrict__ dO, const float* __restrict__ E, const float* __restrict__ W,
+           const float* __restrict__ edo, const int32_t* __restrict__ cu, const int64_t* __restrict__ prefix,
+           int64_t T_total, int H, float scale, int max_seg, const float* __restrict__ Sck,
+           const float* __restrict__ dSck, const float* __restrict__ dS_fin, float* __restrict__ dX,
+           float* __restrict__ dg, float* __restrict__ segtot, float* __restrict__ fin, int64_t slots) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    RowTok* st = reinterpret_cast<RowTok*>(smem_raw);  // [kSeg]
+    const int u = blockIdx.x / max_seg, sg = blockIdx.x % max_seg, n = u / H, h = u % H;
+    const int tid = threadIdx.x, rg = tid >> 4, cg = tid & 15;
+    int64_t s0, s1;
+    seq_range(cu, n, T_total, s0, s1);
+    const int64_t nseg = (s1 - s0 + kSeg - 1) / kSeg;
+    if (sg >= nseg) return;
+    const int64_t sb = slot_base(prefix, n, H, h, nseg, slots);
+    if (sb < 0) return;  // flagged by the forward sweep
+    const int64_t HD = (int64_t)H * kD;
+    const int64_t ta = s0 + (int64_t)sg * kSeg, tb = ta + kSeg < s1 ? ta + kSeg : s1;
+    const int nt = (int)(tb - ta);
+    // stage the segment: six 128-vectors (32 chunks each), beta and e . do per token
+    for (int idx = tid; idx < nt * 194; idx += kRowThreads) {
+        const int tk = idx / 194, j = idx - tk * 194;
+        const int64_t t = ta + tk, th = t * H + h;
+        RowTok& s = st[tk];
+        if (j < 192) {
+            const int part = j >> 5, jj = (j & 31) * 4;
+            const float* src = part == 0 ? X + t * 3 * HD + HD + (int64_t)h * kD
+                             : part == 1 ? g + th * kD
+                             : part == 2 ? X + t * 3 * HD + (int64_t)h * kD
+                             : part == 3 ? E + th * kD
+                             : part == 4 ? dO + th * kD
+                                         : W + th * kD;
+            float* dst = part == 0 ? s.k : part == 1 ? s.a : part == 2 ? s.q : part == 3 ? s.e : part == 4 ? s.d : s.w;
+            cp16(dst + jj, src + jj);
+        } else {
+            cp4(j == 192 ? &s.beta : &s.edo, (j == 192 ? beta : edo) + th);
+        }
+    }
+    cp_commit();
+    cp_wait<0>();
+    __syncthreads();
+    for (int idx = tid; idx < nt * kD; idx += kRowThreads) {
+        float& x = st[idx >> 7].a[idx & 127];
+        x = expf(x);
+    }
+    __syncthreads();
+    const int r0 = 4 * rg, c0 = 8 * cg;
+    const bool writer = (cg & 3) == 0;
+    // ---- forward: S from the segment's start state
+    float s[4][8];
+    {
+        const float* src = Sck + (sb + sg) * kD * kD;
+#pragma unroll
+        for (int a = 0; a < 4; ++a) load8f(src + (r0 + a) * kD + c0, s[a]);
+    }
+    for (int tk = 0; tk < nt; ++tk) {
+        const RowTok& T = st[tk];
+        float e8[8], d8[8], w8[8];
+        load8f(T.e + c0, e8);
+        load8f(T.d + c0, d8);
+        load8f(T.w + c0, w8);
+        const float4 k4 = *reinterpret_cast<const float4*>(T.k + r0);
+        const float4 a4 = *reinterpret_cast<const float4*>(T.a + r0);
+        const float kr[4] = {k4.x, k4.y, k4.z, k4.w}, ar[4] = {a4.x, a4.y, a4.z, a4.w};
+        float v[8];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                x0 = fmaf(s[a][b], d8[b], x0);
+                x1 = fmaf(s[a][b], w8[b], x1);
+            }
+            v[2 * a] = x0;
+            v[2 * a + 1] = x1;
+        }
+        const float sdo = reduce8_16(v, cg);               // (S_{t-1} do)_i   (cg & 2 == 0)
+        const float sw = __shfl_xor_sync(0xffffffffu, sdo, 2);  // (S_{t-1} w)_i on the writer lanes
+        const float bt = T.beta;
+        if (writer) {
+            const int a = cg >> 2, i = r0 + a;
+            const float al = pick4(a4, a), ki = pick4(k4, a);
+            const float dq = scale * (al * sdo + bt * ki * T.edo);
+            const float dkr = -bt * al * sw;
+            const int64_t t = ta + tk;
+            dX[t * 3 * HD + (int64_t)h * kD + i] = dq;
+            dX[t * 3 * HD + HD + (int64_t)h * kD + i] = dkr;
+            dg[(t * H + h) * kD + i] = T.q[i] * dq + ki * dkr;
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const float bk = bt * kr[a];
+#pragma unroll
+            for (int b = 0; b < 8; ++b) s[a][b] = fmaf(bk, e8[b], ar[a] * s[a][b]);
+        }
+    }
+    if (tb == s1) {  // the sequence's final state: rowsum(dS_T . S_T)
+        float f[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            float x = 0.f;
+            if (dS_fin) {
+                float d8[8];
+                load8f(dS_fin + ((int64_t)u * kD + r0 + a) * kD + c0, d8);
+#pragma unroll
+                for (int b = 0; b < 8; ++b) x = fmaf(d8[b], s[a][b], x);
+            }
+            f[a] = x;
+        }
+        const float tot = reduce4_16(f, cg);
+        if (writer) fin[(int64_t)u * kD + r0 + (cg >> 2)] = tot;
+    }
+    // ---- backward: dS from the segment's end gradient
+    float (&ds)[4][8] = s;
+    {
+        const float* src = dSck + (sb + sg) * kD * kD;
+#pragma unroll
+        for (int a = 0; a < 4; ++a) load8f(src + (r0 + a) * kD + c0, ds[a]);
+    }
+    float run = 0.f;  // sum of dGamma over this segment's tokens >= t (writer lanes)
+    for (int tk = nt - 1; tk >= 0; --tk) {
+        const RowTok& T = st[tk];
+        float e8[8], d8[8], w8[8];
+        load8f(T.e + c0, e8);
+        load8f(T.d + c0, d8);
+        load8f(T.w + c0, w8);
+        const float4 k4 = *reinterpret_cast<const float4*>(T.k + r0);
+        const float4 a4 = *reinterpret_cast<const float4*>(T.a + r0);
+        const float4 q4 = *reinterpret_cast<const float4*>(T.q + r0);
+        const float kr[4] = {k4.x, k4.y, k4.z, k4.w}, ar[4] = {a4.x, a4.y, a4.z, a4.w};
+        const float qr[4] = {q4.x, q4.y, q4.z, q4.w};
+        const float bt = T.beta;
+        float y[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const float sq = scale * qr[a];
+            float x = 0.f;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                ds[a][b] = fmaf(sq, d8[b], ds[a][b]);
+                x = fmaf(ds[a][b], e8[b], x);
+            }
+            y[a] = x;
+        }
+        const float dse = reduce4_16(y, cg);  // (dS'_t e_t)_i
+        if (writer) {
+            const int a = cg >> 2, i = r0 + a;
+            const int64_t t = ta + tk;
+            const float dkw = bt * dse;
+            float* pk = dX + t * 3 * HD + HD + (int64_t)h * kD + i;
+            *pk += dkw;
+            float* pg = dg + (t * H + h) * kD + i;
+            run += *pg - pick4(k4, a) * dkw;
+            *pg = run;
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const float nbk = -bt * kr[a];
+#pragma unroll
+            for (int b = 0; b < 8; ++b) ds[a][b] = ar[a] * fmaf(nbk, w8[b], ds[a][b]);
+        }
+    }
+    if (writer) segtot[(sb + sg) * kD + r0 + (cg >> 2)] = run;
+}
+
+// dg carries: for each unit and channel, the segments from the last: the value to add to every
+// token of segment sg is fin + the totals of the segments after it (written over segtot).
+__global__ void k_bwd_dg_carry(const int32_t* __restrict__ cu, const int64_t* __restrict__ prefix, int64_t T_total,
+                               int H, const float* __restrict__ fin, float* __restrict__ segtot, int64_t slots) {
+    const int u = blockIdx.x, i = threadIdx.x, n = u / H, h = u % H;
+    int64_t s0, s1;
+    seq_range(cu, n, T_total, s0, s1);
+    const int64_t nseg = (s1 - s0 + kSeg - 1) / kSeg;
+    const int64_t sb = slot_base(prefix, n, H, h, nseg, slots);
+    if (sb < 0 || nseg == 0) return;
+    float carry = fin[(int64_t)u * kD + i];
+    for (int64_t sg = nseg - 1; sg >= 0; --sg) {
+        float* p = segtot + (sb + sg) * kD + i;
+        const float x = *p;
+        *p = carry;
+        carry += x;
     }
 }
 
@@ -286,121 +730,13 @@ __global__ void k_bwd_epilogue(float* __restrict__ O, const Tdy* __restrict__ dy
         for (int c = threadIdx.x; c < kD; c += blockDim.x) atomicAdd(&drms[c], sdw[c]);
 }
 
-// ------------------------------------------------------------------------------ recurrence backward
-// One unit per CTA; segments in reverse.  For each: replay its states S_{t-1} into the unit's
-// scratch (kSeg x D x D), then the tokens backwards.  dS is carried in registers.
-// Outputs: dX [T][3][H][D] (dq^, dk^ and dv), dg, dbeta, dS0.
-__global__ void __launch_bounds__(kRecThreads, 1)
-k_bwd_recurrence(const float* __restrict__ X, const float* __restrict__ g, const float* __restrict__ beta,
-                 const float* __restrict__ dO, const int32_t* __restrict__ cu, int64_t T_total, int H, float scale,
-                 const float* __restrict__ ckpt, int64_t slots, float* __restrict__ scratch,
-                 const float* __restrict__ dS_fin, float* __restrict__ dX, float* __restrict__ dg,
-                 float* __restrict__ dbeta, float* __restrict__ dS0) {
-    __shared__ __align__(16) TokRows tr;
-    __shared__ __align__(16) float sdo[kD];
-    __shared__ __align__(16) float red[8][kD];
-    __shared__ __align__(16) float red2[8][kD];
-    const int u = blockIdx.x, n = u / H, h = u % H;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int r0 = 16 * warp, c0 = 4 * lane;
-    const int64_t HD = (int64_t)H * kD;
-    int64_t s0, s1;
-    seq_range(cu, n, T_total, s0, s1);
-    const int64_t cb = ckpt_base(cu, n, T_total, H, h, slots);
-    if (cb < 0) return;  // flagged by the replay
-    float* scr = scratch + (int64_t)u * kSeg * kD * kD;
-    float4 ds[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        ds[i] = dS_fin ? *reinterpret_cast<const float4*>(dS_fin + ((int64_t)u * kD + r0 + i) * kD + c0)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-    const int64_t nseg = (s1 - s0 + kSeg - 1) / kSeg;
-    for (int64_t sg = nseg - 1; sg >= 0; --sg) {
-        const int64_t ta = s0 + sg * kSeg, tb = (ta + kSeg < s1) ? ta + kSeg : s1;
-        // replay: S_{t-1} for t in [ta, tb) into the scratch
-        {
-            float4 s[16];
-            const float* src = ckpt + (cb + sg) * kD * kD;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) s[i] = *reinterpret_cast<const float4*>(src + (r0 + i) * kD + c0);
-            for (int64_t t = ta; t < tb; ++t) {
-                float* dst = scr + (t - ta) * kD * kD;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) *reinterpret_cast<float4*>(dst + (r0 + i) * kD + c0) = s[i];
-                if (t + 1 == tb) break;  // the last token's own update is not needed
-                stage_rows(tr, X, g, t, H, h, tid);
-                __syncthreads();
-                float4 e;
-                fwd_step(s, tr, beta[t * H + h], r0, c0, warp, red, &e);
-            }
-        }
-        // the tokens backwards
-        for (int64_t t = tb - 1; t >= ta; --t) {
-            stage_rows(tr, X, g, t, H, h, tid);
-            if (tid < kD) sdo[tid] = dO[(t * H + h) * kD + tid];
-            __syncthreads();
-            const float bt = beta[t * H + h];
-            // P = Diag(alpha) S_{t-1};  dS += scale q do^T
-            float4 p[16];
-            const float* sp = scr + (t - ta) * kD * kD;
-            const float4 dov = *reinterpret_cast<const float4*>(&sdo[c0]);
-            float4 cp = make_float4(0.f, 0.f, 0.f, 0.f), cw = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                p[i] = f4_mul(tr.a[r0 + i], *reinterpret_cast<const float4*>(sp + (r0 + i) * kD + c0));
-                ds[i] = f4_fma(scale * tr.q[r0 + i], dov, ds[i]);
-                cp = f4_fma(tr.k[r0 + i], p[i], cp);   // P^T k
-                cw = f4_fma(tr.k[r0 + i], ds[i], cw);  // w = dS^T k
-            }
-            *reinterpret_cast<float4*>(&red[warp][c0]) = cp;
-            *reinterpret_cast<float4*>(&red2[warp][c0]) = cw;
-            __syncthreads();
-            float4 pk = make_float4(0.f, 0.f, 0.f, 0.f), w = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int ww = 0; ww < 8; ++ww) {
-                pk = f4_add(pk, *reinterpret_cast<const float4*>(&red[ww][c0]));
-                w = f4_add(w, *reinterpret_cast<const float4*>(&red2[ww][c0]));
-            }
-            const float4 vv = *reinterpret_cast<const float4*>(&tr.v[c0]);
-            const float4 e = make_float4(vv.x - pk.x, vv.y - pk.y, vv.z - pk.z, vv.w - pk.w);
-            // dv = beta w (warp 0 writes), dbeta = w . e
-            if (warp == 0) {
-                *reinterpret_cast<float4*>(dX + t * 3 * HD + 2 * HD + (int64_t)h * kD + c0) = f4_mul(bt, w);
-                const float db = warp_sum(dot4(w, e));
-                if (lane == 0) dbeta[t * H + h] = db;
-            }
-            // row sums over the columns: dq = scale S_t do, dk = beta (dS e - P w), dg = rowsum(dP . P)
-            float aq[16], ak[16], ag[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float kr = tr.k[r0 + i];
-                const float4 st = f4_fma(bt * kr, e, p[i]);  // S_t
-                aq[i] = dot4(st, dov);
-                ak[i] = dot4(ds[i], e) - dot4(p[i], w);
-                const float4 dp = f4_fma(-bt * kr, w, ds[i]);
-                ag[i] = dot4(dp, p[i]);
-                ds[i] = f4_mul(tr.a[r0 + i], dp);  // dS_{t-1}
-            }
-            const float sq = reduce16(aq, lane), sk = reduce16(ak, lane), sgv = reduce16(ag, lane);
-            if ((lane & 1) == 0) {
-                const int r = r0 + (lane >> 1);
-                float* dxr = dX + t * 3 * HD + (int64_t)h * kD + r;
-                dxr[0] = scale * sq;
-                dxr[HD] = bt * sk;
-                dg[(t * H + h) * kD + r] = sgv;
-            }
-            __syncthreads();  // tr, sdo, red, red2 are reused by the next token
-        }
-    }
-    if (dS0)
-#pragma unroll
-        for (int i = 0; i < 16; ++i) *reinterpret_cast<float4*>(dS0 + ((int64_t)u * kD + r0 + i) * kD + c0) = ds[i];
-}
-
 // ------------------------------------------------------------------------------ L2 backward
-// One warp per (token, head): dq^ -> d a_q = (dq^ - q^ (q^ . dq^)) / |a_q|, same for k, in place.
-__global__ void k_bwd_l2(const float* __restrict__ X, const float* __restrict__ nrm, int64_t T_total, int H,
-                         float* __restrict__ dX) {
+// One warp per (token, head): dq^ -> d a_q = (dq^ - q^ (q^ . dq^)) / |a_q|, same for k, in place;
+// and dg += the carry of the token's segment.
+__global__ void k_bwd_l2(const float* __restrict__ X, const float* __restrict__ nrm, const int32_t* __restrict__ cu,
+                         const int64_t* __restrict__ prefix, int N, int64_t T_total, int H,
+                         const float* __restrict__ segtot, int64_t slots, float* __restrict__ dX,
+                         float* __restrict__ dg) {
     const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= T_total * H) return;
@@ -417,6 +753,21 @@ __global__ void k_bwd_l2(const float* __restrict__ X, const float* __restrict__ 
         *reinterpret_cast<float4*>(dX + off) = make_float4((d.x - x.x * xd) * inv, (d.y - x.y * xd) * inv,
                                                            (d.z - x.z * xd) * inv, (d.w - x.w * xd) * inv);
     }
+    int lo = 0, hi = N;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cu[mid] <= t) lo = mid;
+        else hi = mid;
+    }
+    int64_t s0, s1;
+    seq_range(cu, lo, T_total, s0, s1);
+    if (t < s0 || t >= s1) return;
+    const int64_t nseg = (s1 - s0 + kSeg - 1) / kSeg;
+    const int64_t sb = slot_base(prefix, lo, H, h, nseg, slots);
+    if (sb < 0) return;
+    float4* p = reinterpret_cast<float4*>(dg + row * kD + 4 * lane);
+    const float4 c = *reinterpret_cast<const float4*>(segtot + (sb + (t - s0) / kSeg) * kD + 4 * lane);
+    *p = f4_add(*p, c);
 }
 
 // ------------------------------------------------------------------------------ activation + conv backward
@@ -515,22 +866,41 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
     float* nrm = reinterpret_cast<float*>(ws + L.nrm);
     float* O = reinterpret_cast<float*>(ws + L.o);
     float* dX = reinterpret_cast<float*>(ws + L.dx);
-    float* ck = reinterpret_cast<float*>(ws + L.ckpt);
-    float* scr = reinterpret_cast<float*>(ws + L.scratch);
+    float* E = reinterpret_cast<float*>(ws + L.e);
+    float* W = reinterpret_cast<float*>(ws + L.w);
+    float* edo = reinterpret_cast<float*>(ws + L.edo);
+    float* Sck = reinterpret_cast<float*>(ws + L.sck);
+    float* dSck = reinterpret_cast<float*>(ws + L.dsck);
+    float* segtot = reinterpret_cast<float*>(ws + L.segtot);
+    float* fin = reinterpret_cast<float*>(ws + L.fin);
+    int64_t* prefix = reinterpret_cast<int64_t*>(ws + L.prefix);
     cudaError_t e;
     if ((e = cudaMemsetAsync(b.dconv_w, 0, sizeof(float) * 3 * a.H * kD * 4, s))) return e;
     if (b.drms_w && (e = cudaMemsetAsync(b.drms_w, 0, sizeof(float) * kD, s))) return e;
+    if (b.dconv_state_in &&
+        (e = cudaMemsetAsync(b.dconv_state_in, 0, sizeof(float) * a.N * 3 * a.H * kD * 3, s)))
+        return e;
     if (rows > 0) {
-        const unsigned rb = (unsigned)((rows + 7) / 8);
+        if ((e = cudaMemsetAsync(b.dbeta, 0, sizeof(float) * rows, s))) return e;
+        if ((e = cudaMemsetAsync(edo, 0, sizeof(float) * rows, s))) return e;
+    }
+    k_bwd_seg_prefix<<<1, 256, 0, s>>>(a.cu_seqlens, a.N, T, prefix);
+    if ((e = cudaGetLastError())) return e;
+    const unsigned rb = (unsigned)((rows + 7) / 8);
+    if (rows > 0) {
         k_bwd_prep<Tio><<<rb, 256, 0, s>>>(cptr<Tio>(a.q), cptr<Tio>(a.k), cptr<Tio>(a.v), xs, a.conv_w,
                                           cptr<Tio>(a.conv_state_in), a.cu_seqlens, a.N, T, a.H, a.eps_l2, X, nrm);
         if ((e = cudaGetLastError())) return e;
     }
-    k_bwd_replay<<<(unsigned)units, kRecThreads, 0, s>>>(X, a.g, a.beta, a.cu_seqlens, T, a.H, a.scale,
-                                                          a.initial_state, O, ck, L.slots, a.d_status);
+    if ((e = cudaFuncSetAttribute(k_bwd_fwd_cols, cudaFuncAttributeMaxDynamicSharedMemorySize, kColSmem)) ||
+        (e = cudaFuncSetAttribute(k_bwd_bwd_cols, cudaFuncAttributeMaxDynamicSharedMemorySize, kColSmem)) ||
+        (e = cudaFuncSetAttribute(k_bwd_rows, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmem)))
+        return e;
+    const unsigned cg = (unsigned)(units * kColCtas);
+    k_bwd_fwd_cols<<<cg, 256, kColSmem, s>>>(X, a.g, a.beta, a.cu_seqlens, prefix, T, a.H, a.scale,
+                                             a.initial_state, O, E, Sck, L.slots, a.d_status);
     if ((e = cudaGetLastError())) return e;
     if (rows > 0) {
-        const unsigned rb = (unsigned)((rows + 7) / 8);
         if (a.out_dtype == KDA_FP32)
             k_bwd_epilogue<Tio, float><<<rb, 256, 0, s>>>(O, cptr<float>(b.dy), cptr<Tio>(a.gate), a.rms_w, a.eps_rms,
                                                            rows, b.dgate, b.drms_w);
@@ -539,18 +909,19 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
                                                           rows, b.dgate, b.drms_w);
         if ((e = cudaGetLastError())) return e;
     }
-    k_bwd_recurrence<<<(unsigned)units, kRecThreads, 0, s>>>(X, a.g, a.beta, O, a.cu_seqlens, T, a.H, a.scale, ck,
-                                                              L.slots, scr, b.d_final_state, dX, b.dg, b.dbeta,
-                                                              b.dinitial_state);
+    k_bwd_bwd_cols<<<cg, 256, kColSmem, s>>>(X, a.g, a.beta, O, E, a.cu_seqlens, prefix, T, a.H, a.scale,
+                                             b.d_final_state, W, dX, b.dbeta, edo, dSck, b.dinitial_state,
+                                             L.slots);
     if ((e = cudaGetLastError())) return e;
-    if (rows > 0) {
-        k_bwd_l2<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(X, nrm, T, a.H, dX);
-        if ((e = cudaGetLastError())) return e;
-    }
-    if (b.dconv_state_in &&
-        (e = cudaMemsetAsync(b.dconv_state_in, 0, sizeof(float) * a.N * 3 * a.H * kD * 3, s)))
-        return e;
     if (rows == 0) return cudaSuccess;
+    k_bwd_rows<<<(unsigned)(units * L.max_seg), kRowThreads, kRowSmem, s>>>(
+        X, a.g, a.beta, O, E, W, edo, a.cu_seqlens, prefix, T, a.H, a.scale, (int)L.max_seg, Sck, dSck,
+        b.d_final_state, dX, b.dg, segtot, fin, L.slots);
+    if ((e = cudaGetLastError())) return e;
+    k_bwd_dg_carry<<<(unsigned)units, kD, 0, s>>>(a.cu_seqlens, prefix, T, a.H, fin, segtot, L.slots);
+    if ((e = cudaGetLastError())) return e;
+    k_bwd_l2<<<rb, 256, 0, s>>>(X, nrm, a.cu_seqlens, prefix, a.N, T, a.H, segtot, L.slots, dX, b.dg);
+    if ((e = cudaGetLastError())) return e;
     const int cblocks = (3 * a.H * kD + 255) / 256;
     const int64_t tiles = (T + kConvTile - 1) / kConvTile;
     k_bwd_conv<Tio><<<(unsigned)(cblocks * tiles), 256, 0, s>>>(
@@ -566,24 +937,35 @@ size_t al256(size_t x) { return (x + 255) / 256 * 256; }
 BackwardLayout backward_layout(const kda_backward_args& b) {
     const kda_prefill_args& a = b.fwd;
     BackwardLayout L{};
-    const size_t T = (size_t)(a.T_total > 0 ? a.T_total : 0), HD = (size_t)a.H * kD;
-    size_t segs = 0;
+    const size_t T = (size_t)(a.T_total > 0 ? a.T_total : 0), H = (size_t)a.H, HD = H * kD;
+    size_t segs = 0, max_seg = 0;
     if (a.cu_seqlens_host)
-        for (int n = 0; n < a.N; ++n) segs += (size_t)(a.cu_seqlens_host[n + 1] - a.cu_seqlens_host[n] + kSeg - 1) / kSeg;
+        for (int n = 0; n < a.N; ++n) {
+            const size_t ns = (size_t)(a.cu_seqlens_host[n + 1] - a.cu_seqlens_host[n] + kSeg - 1) / kSeg;
+            segs += ns;
+            max_seg = ns > max_seg ? ns : max_seg;
+        }
+    const size_t N = (size_t)(a.N > 0 ? a.N : 0);
     size_t off = 0;
-    L.x = off;
-    off += al256(T * 3 * HD * 4);
-    L.nrm = off;
-    off += al256(T * a.H * 2 * 4);
-    L.o = off;
-    off += al256(T * HD * 4);
-    L.dx = off;
-    off += al256(T * 3 * HD * 4);
-    L.ckpt = off;
-    L.slots = (int64_t)(segs * a.H);
-    off += al256(segs * a.H * kD * kD * 4);
-    L.scratch = off;
-    off += al256((size_t)a.N * a.H * kSeg * kD * kD * 4);
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += al256(bytes);
+        return o;
+    };
+    L.x = take(T * 3 * HD * 4);
+    L.nrm = take(T * H * 2 * 4);
+    L.o = take(T * HD * 4);
+    L.dx = take(T * 3 * HD * 4);
+    L.e = take(T * HD * 4);
+    L.w = take(T * HD * 4);
+    L.edo = take(T * H * 4);
+    L.slots = (int64_t)(segs * H);
+    L.max_seg = (int64_t)max_seg;
+    L.sck = take(segs * H * kD * kD * 4);
+    L.dsck = take(segs * H * kD * kD * 4);
+    L.segtot = take(segs * H * kD * 4);
+    L.fin = take(N * H * kD * 4);
+    L.prefix = take((N + 1) * 8);
     L.total = off;
     return L;
 }

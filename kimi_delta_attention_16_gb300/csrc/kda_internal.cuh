@@ -222,12 +222,19 @@ struct BackwardLayout {
     size_t nrm;      // [T][H][2] fp32: the L2 denominators of q and k
     size_t o;        // [T][H][D] fp32: o before the epilogue, then its gradient
     size_t dx;       // [T][3][H][D] fp32: gradients of q^, k^, v, then of the conv outputs
-    size_t ckpt;     // [segments][H][D][D] fp32: the state at the start of every segment
-    int64_t slots;   // segments * H: checkpoint slots planned from the host copy of cu_seqlens
-    size_t scratch;  // [N][H][kBwdSeg][D][D] fp32: one segment's replayed states per unit
+    size_t e;        // [T][H][D] fp32: e_t = v_t - P_t^T k_t
+    size_t w;        // [T][H][D] fp32: w_t = dS'_t^T k_t
+    size_t edo;      // [T][H] fp32: e_t . do_t
+    size_t sck;      // [slots][D][D] fp32: the state at the start of every segment
+    size_t dsck;     // [slots][D][D] fp32: the state gradient at the end of every segment
+    size_t segtot;   // [slots][D] fp32: dg sums per segment, then the carries
+    size_t fin;      // [N][H][D] fp32: rowsum(dS_T . S_T)
+    size_t prefix;   // [N + 1] int64: segments before each sequence
+    int64_t slots;   // checkpoint slots: H times the sum over sequences of ceil(len / kBwdSeg)
+    int64_t max_seg; // the largest segment count of one sequence
     size_t total;
 };
-constexpr int kBwdSeg = 32;  // tokens per checkpointed segment of the backward pass
+constexpr int kBwdSeg = 64;  // tokens per checkpointed segment of the backward pass
 BackwardLayout backward_layout(const kda_backward_args& b);  // needs fwd.cu_seqlens_host
 cudaError_t launch_backward(const kda_backward_args& b, const BackwardLayout& L, char* ws, cudaStream_t s);
 

@@ -324,20 +324,21 @@ def test_backward_rejects_bad_arguments(field, value, code):
 
 
 def test_backward_workspace_size_matches_the_stated_layout():
-    """T H D 28 + T H 8 + segs H D^2 4 + N H 32 D^2 4 bytes, each part rounded up to 256,
-    segs = sum over sequences of ceil(len / 32)."""
+    """36 T H D + 12 T H + 8 slots D^2 + 4 slots D + 4 N H D + 8 (N + 1) bytes, each part rounded
+    up to 256 (in the header's order), slots = H * sum over sequences of ceil(len / 64)."""
     lib = _lib.load()
     r = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    for lengths, H in [([40, 24], 2), ([0, 1, 33, 0, 64], 3), ([8192], 96), ([], 4)]:
+    for lengths, H in [([40, 24], 2), ([0, 1, 65, 0, 128], 3), ([8192], 96), ([], 4)]:
         cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
         b = _bwd_args(**{"fwd.N": len(lengths), "fwd.H": H, "fwd.T_total": int(cu[-1]),
                          "fwd.cu_seqlens_host": cu.ctypes.data})
         n = ctypes.c_size_t()
         assert lib.kda_backward_workspace_size(ctypes.byref(b), ctypes.byref(n)) == 0
-        T, D = int(cu[-1]), 128
-        segs = sum((L + 31) // 32 for L in lengths)
+        T, D, N = int(cu[-1]), 128, len(lengths)
+        slots = H * sum((L + 63) // 64 for L in lengths)
         want = (r(T * 3 * H * D * 4) + r(T * H * 2 * 4) + r(T * H * D * 4) + r(T * 3 * H * D * 4)
-                + r(segs * H * D * D * 4) + r(len(lengths) * H * 32 * D * D * 4))
+                + r(T * H * D * 4) + r(T * H * D * 4) + r(T * H * 4)
+                + 2 * r(slots * D * D * 4) + r(slots * D * 4) + r(N * H * D * 4) + r((N + 1) * 8))
         assert n.value == want, (lengths, H)
 
 
