@@ -201,6 +201,11 @@ def run_ours(args):
             print(f"multi-token decode {obj['metric']}: {obj['ms_per_step']:.4f} ms/step, "
                   f"{obj['roofline']['frac']:.3f} of HBM", flush=True)
         return
+    if args.mode == "backward":  # profiling aid: only the backward pass (prints its object)
+        obj, _ = time_backward(args, pg, dev, torch.cuda.current_stream(), peaks, peak_src, world)
+        if rank == 0:
+            print(json.dumps(obj))
+        return
     if args.mode == "gemm":  # profiling aid: only the projection GEMMs of the projected layer
         return run_gemm_only(args, rank, dev)
     if args.mode == "prefill":
@@ -367,6 +372,8 @@ def run_ours(args):
             extra[name], nl = time_prefill_workload(name, args, pg, dev, stream, peaks, peak_src, world)
             extra_launches += nl
         extra["projected_layer"], nl = time_projected_layer(args, pg, dev, stream, peaks, peak_src, world)
+        extra_launches += nl
+        extra["backward"], nl = time_backward(args, pg, dev, stream, peaks, peak_src, world)
         extra_launches += nl
     clk = clocks.stop()
 
@@ -552,6 +559,59 @@ def time_projected_layer(args, pg, dev, stream, peaks, peak_src, world, d_model=
     # inside the timed regions: each projection alone, then the whole chain
     launches = len(gemms) * steps + (len(gemms) + prefill_launches(path, segments)) * steps
     return obj, launches
+
+
+FP32_SIMT_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # 152 SMs x 128 fp32 lanes x FMA x 2.07 GHz max clock
+BWD_FLOP_PER_TOKEN_HEAD = 28 * 128 * 128              # token-serial adjoint, counted in the design doc
+
+
+def time_backward(args, pg, dev, stream, peaks, peak_src, world):
+    """kda_backward at layer_8k (8192 tokens, 96 heads): the gradients of every input given dy and
+    dS_fin, with the gate, RMSNorm weight, initial state and conv state present.  Workspace and
+    outputs are allocated once, outside the timed region.  Returns (object, launches)."""
+    import torch
+    import kimi_delta_attention_16_gb300 as kda
+    from kimi_delta_attention_16_gb300 import synth
+    inp = synth.make_prefill("layer_8k", seed=1, device=dev, s0_std=0.02, conv_state=True, rms_w="random")
+    T, H, D, N = inp.T, inp.H, inp.D, inp.N
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(9)
+    dy = torch.randn((T, H, D), generator=gen, device=dev).to(torch.bfloat16)
+    dsf = torch.randn((N, H, D, D), generator=gen, device=dev) * 0.02
+    cu_pair = (torch.from_numpy(inp.cu_seqlens).to(dev), inp.cu_seqlens)
+    ws = torch.empty(kda.kda_backward_workspace_size(inp.cu_seqlens, H), dtype=torch.uint8, device=dev)
+
+    def step():
+        kda.kda_backward(inp.q, inp.k, inp.v, inp.conv_w, inp.g, inp.beta, cu_pair, dy, gate=inp.gate,
+                         rms_w=inp.rms_w, initial_state=inp.initial_state, conv_state_in=inp.conv_state_in,
+                         d_final_state=dsf, workspace=ws)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    barrier(pg)
+    steps = max(3, min(args.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    ms = max_over_ranks(pg, e0.elapsed_time(e1) / steps, dev)
+    flops = BWD_FLOP_PER_TOKEN_HEAD * T * H
+    tf = flops / (ms / 1e3) / 1e12
+    obj = {"metric": "KDA backward tokens/s (layer_8k: T=8192, H=96, d=128; all input gradients)",
+           "value": round(aggregate_rate(world, T, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+           "steps": steps, "workspace_bytes": ws.numel(),
+           "roofline": {"kernel": "the whole kda_backward call (fp32 SIMT recurrence sweeps dominate)",
+                        "bound": "alu", "achieved": round(tf, 2), "peak": round(FP32_SIMT_TFLOPS, 1),
+                        "unit": "TFLOP/s", "frac": round(tf / FP32_SIMT_TFLOPS, 4),
+                        "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 x 2.07 GHz",
+                        "traffic": None, "algorithmic_flops": flops}}
+    del inp, dy, dsf, ws
+    torch.cuda.empty_cache()
+    return obj, steps * 9  # nine kernels per call (the five output/partial memsets are not counted)
 
 
 def time_multi_token(args, pg, dev, stream, peaks, peak_src, world, t_new=4, ring=8):
@@ -749,7 +809,7 @@ def main():
     ap.add_argument("--decode-n", type=int, default=256, help="decode batch (sequences)")
     ap.add_argument("--verify-steps", type=int, default=200,
                     help="multi-token decode steps (256 sequences x 4 tokens) to time; 0 skips")
-    ap.add_argument("--mode", choices=["all", "prefill", "decode", "verify", "gemm"], default="all",
+    ap.add_argument("--mode", choices=["all", "prefill", "decode", "verify", "gemm", "backward"], default="all",
                     help="profiling aid: run only one of the measurements (verify = the "
                          "multi-token decode loop, gemm = the projection GEMMs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

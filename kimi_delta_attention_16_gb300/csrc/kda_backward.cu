@@ -162,21 +162,27 @@ __global__ void k_bwd_seg_prefix(const int32_t* __restrict__ cu, int N, int64_t 
 }
 
 // ------------------------------------------------------------------------------ column-layout sweeps
-// One unit's state is split by value column over kColCtas CTAs of 8 warps.  Lane l of warp w owns
-// column c = 32 cq + 4 w + (l >> 3) and rows 16 r .. 16 r + 15, r = l & 7.  A per-column quantity
-// of a token (e, o, w = dS^T k) is a sum over the rows of its column: eight lanes, three shuffles.
-// No CTA barrier inside a token; tokens are staged kTB at a time (double-buffered cp.async), three
-// barriers per block.
-constexpr int kColCtas = 4;           // CTAs per unit (32 columns each)
-constexpr int kCols = kD / kColCtas;  // 32
-constexpr int kTB = 16;               // tokens per staged block
-constexpr int kPerm = 160;            // a staged 128-vector: 8 slices of 16 rows, 20 floats apart
-__device__ __forceinline__ int perm_off(int row) { return (row >> 4) * 20 + (row & 15); }
+// One unit's state is split by value column over kColCtas CTAs of 4 warps (32 columns each).
+// Lane l of warp w owns rows 8 r .. 8 r + 7 (r = l & 15) of the four columns
+// c0 = 32 cq + 8 w + 4 (l >> 4) .. c0 + 3.  A
+// per-column quantity of a token (e, o, w = dS^T k) is a sum over the rows of its column: the
+// sixteen lanes of a column group.  Every (unit, column group) is an independent chain, and the
+// CTAs of all units stay resident together (ten warps per SM at 96 units).  Each token is one pass over the state: the forward sweep
+// finishes token t's update, accumulates o_t and the next token's S^T (alpha k) together; the
+// backward sweep applies the later token's decay and correction, adds token t's readout gradient
+// and accumulates w_t together.  No CTA barrier inside a token; tokens are staged kTB at a time
+// (double-buffered cp.async), three barriers per block.
+constexpr int kColCtas = 4;           // CTAs per unit
+constexpr int kCols = kD / kColCtas;  // 32 columns per CTA
+constexpr int kTB = 8;                // tokens per staged block
+constexpr int kSlice = 12;            // floats between the 8-row slices of a staged 128-vector
+constexpr int kPerm = 16 * kSlice;
+__device__ __forceinline__ int perm_off(int row) { return (row >> 3) * kSlice + (row & 7); }
 
-// One staged token: k^, exp(g), q^ (permuted so that the eight row slices a warp reads at once fall
-// in distinct banks), two slices of the CTA's 32 columns, beta.
+// One staged token: k^, exp(g), q^, exp(g) k^ (8-row slices 12 floats apart, so that the eight
+// slices a quarter-warp reads at once fall in distinct banks), two slices of the CTA's columns, beta.
 struct ColTok {
-    float k[kPerm], a[kPerm], q[kPerm];
+    float k[kPerm], a[kPerm], q[kPerm], ak[kPerm];
     float c0[kCols], c1[kCols];  // forward sweep: v; backward sweep: do and e
     float beta, pad[3];
 };
@@ -188,13 +194,14 @@ struct ColSrc {
 };
 
 // Issues the copies of tokens [t0, t0 + nt) of head h into st[0 .. nt): the three row vectors
-// (q^ and k^ from X, g into the alpha slot), `ncs` column slices (the CTA's 32 columns), beta.
+// (q^ and k^ from X, g into the alpha slot), `ncs` column slices (the CTA's columns), beta.
 __device__ __forceinline__ void stage_cols(ColTok* st, int64_t t0, int nt, const float* X, const float* g,
                                            const float* beta, ColSrc s0, ColSrc s1, int ncs, int H, int h,
                                            int cq, int tid) {
+    constexpr int kCC = kCols / 4;  // 16-byte chunks of one column slice
     const int64_t HD = (int64_t)H * kD;
-    const int per = 96 + 8 * ncs + 1;
-    for (int idx = tid; idx < nt * per; idx += 256) {
+    const int per = 96 + kCC * ncs + 1;
+    for (int idx = tid; idx < nt * per; idx += 128) {
         const int tk = idx / per, j = idx - tk * per;
         const int64_t t = t0 + tk;
         ColTok& s = st[tk];
@@ -204,45 +211,89 @@ __device__ __forceinline__ void stage_cols(ColTok* st, int64_t t0, int nt, const
                              : part == 1 ? g + (t * H + h) * kD
                                          : X + t * 3 * HD + (int64_t)h * kD;
             float* dst = part == 0 ? s.k : part == 1 ? s.a : s.q;
-            cp16(dst + (jj >> 2) * 20 + (jj & 3) * 4, src + jj * 4);
-        } else if (j < 96 + 8 * ncs) {
-            const int jj = j - 96;
-            const ColSrc& cs = jj < 8 ? s0 : s1;
-            cp16((jj < 8 ? s.c0 : s.c1) + (jj & 7) * 4, cs.p + t * cs.stride + (int64_t)h * kD + cq * kCols + (jj & 7) * 4);
+            cp16(dst + (jj >> 1) * kSlice + (jj & 1) * 4, src + jj * 4);
+        } else if (j < 96 + kCC * ncs) {
+            const int jj = j - 96, which = jj / kCC, ch = jj - which * kCC;
+            const ColSrc& cs = which == 0 ? s0 : s1;
+            cp16((which == 0 ? s.c0 : s.c1) + ch * 4, cs.p + t * cs.stride + (int64_t)h * kD + cq * kCols + ch * 4);
         } else {
             cp4(&s.beta, beta + t * H + h);
         }
     }
 }
 
-// exp(g) in place for the staged tokens (after the copies have landed and a barrier).
+// alpha = exp(g) in place and alpha k for the staged tokens (after the copies have landed and a
+// barrier).
 __device__ __forceinline__ void stage_exp_cols(ColTok* st, int nt, int tid) {
-    for (int idx = tid; idx < nt * kD; idx += 256) {
-        float& x = st[idx >> 7].a[perm_off(idx & 127)];
-        x = expf(x);
+    for (int idx = tid; idx < nt * kD; idx += 128) {
+        ColTok& s = st[idx >> 7];
+        const int o = perm_off(idx & 127);
+        const float a = expf(s.a[o]);
+        s.a[o] = a;
+        s.ak[o] = a * s.k[o];
     }
 }
 
-__device__ __forceinline__ void load16(const float* p, float (&x)[16]) {
+// The 8 rows of a lane's slice of a staged vector.
+__device__ __forceinline__ void load_rows(const float* p, float (&x)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+// Four column sums over the sixteen lanes of a column group (lane bits 0..3), every lane gets all
+// four.
+__device__ __forceinline__ void sum16x4(float (&x)[4]) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float4 f = reinterpret_cast<const float4*>(p)[i];
-        x[4 * i] = f.x;
-        x[4 * i + 1] = f.y;
-        x[4 * i + 2] = f.z;
-        x[4 * i + 3] = f.w;
+    for (int off = 1; off < 16; off <<= 1)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] += __shfl_xor_sync(0xffffffffu, x[j], off);
+}
+// Four column sums over the sixteen lanes of a column group; afterwards lanes 4 j .. 4 j + 3 of the
+// group (r = lane & 15) hold the total of value j.
+__device__ __forceinline__ float sum16x4_split(float (&x)[4], int r) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const bool up = (r & 8) != 0;
+        const float send = up ? x[i] : x[i + 2];
+        x[i] = (up ? x[i + 2] : x[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    {
+        const bool up = (r & 4) != 0;
+        const float send = up ? x[0] : x[1];
+        x[0] = (up ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    x[0] += __shfl_xor_sync(0xffffffffu, x[0], 2);
+    return x[0] + __shfl_xor_sync(0xffffffffu, x[0], 1);
+}
+// The four values of sum16x4_split gathered on lane r = 0 of each column group.
+__device__ __forceinline__ float4 gather4(float v, int lane) {
+    const int base = lane & ~15;
+    const float v1 = __shfl_sync(0xffffffffu, v, base + 4), v2 = __shfl_sync(0xffffffffu, v, base + 8),
+                v3 = __shfl_sync(0xffffffffu, v, base + 12);
+    return make_float4(v, v1, v2, v3);
+}
+
+// The state slice of a lane (rows 8 r .. 8 r + 7 of columns c0 .. c0 + 3) to / from a row-major
+// D x D matrix.
+__device__ __forceinline__ void load_slice(const float* M, int r, int c0, float (&s)[8][4]) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const float4 a = *reinterpret_cast<const float4*>(M + (8 * r + m) * kD + c0);
+        s[m][0] = a.x;
+        s[m][1] = a.y;
+        s[m][2] = a.z;
+        s[m][3] = a.w;
     }
 }
-__device__ __forceinline__ float sum8(float x) {  // over the 8 lanes of one column (lane bits 0..2)
-    x += __shfl_xor_sync(0xffffffffu, x, 1);
-    x += __shfl_xor_sync(0xffffffffu, x, 2);
-    x += __shfl_xor_sync(0xffffffffu, x, 4);
-    return x;
+__device__ __forceinline__ void store_slice(float* M, int r, int c0, const float (&s)[8][4]) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+        *reinterpret_cast<float4*>(M + (8 * r + m) * kD + c0) = make_float4(s[m][0], s[m][1], s[m][2], s[m][3]);
 }
 
 // Forward sweep: the recurrence from the initial state; o_t and e_t of every token; the state at
-// the start of every kSeg-token segment (Sck).  Grid: units x kColCtas CTAs of 256 threads.
-__global__ void __launch_bounds__(256)
+// the start of every kSeg-token segment (Sck).  Grid: units x kColCtas CTAs of 128 threads.
+__global__ void __launch_bounds__(128)
 k_bwd_fwd_cols(const float* __restrict__ X, const float* __restrict__ g, const float* __restrict__ beta,
                const int32_t* __restrict__ cu, const int64_t* __restrict__ prefix, int64_t T_total, int H,
                float scale, const float* __restrict__ S0, float* __restrict__ O, float* __restrict__ E,
@@ -250,8 +301,8 @@ k_bwd_fwd_cols(const float* __restrict__ X, const float* __restrict__ g, const f
     extern __shared__ __align__(16) unsigned char smem_raw[];
     ColTok* buf = reinterpret_cast<ColTok*>(smem_raw);  // [2][kTB]
     const int u = blockIdx.x / kColCtas, cq = blockIdx.x % kColCtas, n = u / H, h = u % H;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane & 7;
-    const int cl = warp * 4 + (lane >> 3), c = cq * kCols + cl;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane & 15;
+    const int cl = warp * 8 + 4 * (lane >> 4), c0 = cq * kCols + cl;
     int64_t s0, s1;
     seq_range(cu, n, T_total, s0, s1);
     const int64_t nseg = (s1 - s0 + kSeg - 1) / kSeg;
@@ -262,9 +313,15 @@ k_bwd_fwd_cols(const float* __restrict__ X, const float* __restrict__ g, const f
     }
     const int64_t HD = (int64_t)H * kD;
     const ColSrc vs{X + 2 * HD, 3 * HD};
-    float s[16];
+    float s[8][4];
+    if (S0) {
+        load_slice(S0 + (int64_t)u * kD * kD, r, c0, s);
+    } else {
 #pragma unroll
-    for (int m = 0; m < 16; ++m) s[m] = S0 ? S0[((int64_t)u * kD + 16 * r + m) * kD + c] : 0.f;
+        for (int m = 0; m < 8; ++m)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) s[m][c] = 0.f;
+    }
     const int64_t nblk = (s1 - s0 + kTB - 1) / kTB;
     auto nt_of = [&](int64_t b) { return (int)(s1 - (s0 + b * kTB) < kTB ? s1 - (s0 + b * kTB) : kTB); };
     if (nblk > 0) stage_cols(buf, s0, nt_of(0), X, g, beta, vs, vs, 1, H, h, cq, tid);
@@ -281,51 +338,135 @@ k_bwd_fwd_cols(const float* __restrict__ X, const float* __restrict__ g, const f
         const int nt = nt_of(b);
         stage_exp_cols(st, nt, tid);
         __syncthreads();
+        float x[4];  // (P_t^T k_t) of the lane's columns: alpha_t k_t against S_{t-1}
+        {
+            float ak[8];
+            load_rows(st[0].ak + r * kSlice, ak);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < 8; m += 2) {
+                    a0 = fmaf(ak[m], s[m][c], a0);
+                    a1 = fmaf(ak[m + 1], s[m + 1][c], a1);
+                }
+                x[c] = a0 + a1;
+            }
+            sum16x4(x);
+        }
+        static_assert(kSeg % kTB == 0, "segments start at block starts");
+        if ((b * kTB) % kSeg == 0) store_slice(Sck + (sb + b * kTB / kSeg) * kD * kD, r, c0, s);
         for (int tk = 0; tk < nt; ++tk) {
             const int64_t t = s0 + b * kTB + tk;
-            if ((t - s0) % kSeg == 0) {
-                float* dst = Sck + (sb + (t - s0) / kSeg) * kD * kD;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) dst[(16 * r + m) * kD + c] = s[m];
-            }
             const ColTok& T = st[tk];
-            float kk[16], aa[16];
-            load16(T.k + r * 20, kk);
-            load16(T.a + r * 20, aa);
-            float p0 = 0.f, p1 = 0.f;
+            const ColTok& Nx = st[tk + 1 < nt ? tk + 1 : tk];
+            const float4 v4 = *reinterpret_cast<const float4*>(T.c0 + cl);
+            const float bt = T.beta;
+            const float e[4] = {v4.x - x[0], v4.y - x[1], v4.z - x[2], v4.w - x[3]};
+            const float be[4] = {bt * e[0], bt * e[1], bt * e[2], bt * e[3]};
+            float a2[8], k2[8], q2[8], n2[8];
+            load_rows(T.a + r * kSlice, a2);
+            load_rows(T.k + r * kSlice, k2);
+            load_rows(T.q + r * kSlice, q2);
+            load_rows(Nx.ak + r * kSlice, n2);
+            float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            float p[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-            for (int m = 0; m < 16; m += 2) {
-                s[m] *= aa[m];
-                s[m + 1] *= aa[m + 1];
-                p0 = fmaf(kk[m], s[m], p0);
-                p1 = fmaf(kk[m + 1], s[m + 1], p1);
-            }
-            const float e = T.c0[cl] - sum8(p0 + p1);
-            const float be = T.beta * e;
-            float qq[16];
-            load16(T.q + r * 20, qq);
-            float o0 = 0.f, o1 = 0.f;
+            for (int m = 0; m < 8; ++m)
 #pragma unroll
-            for (int m = 0; m < 16; m += 2) {
-                s[m] = fmaf(kk[m], be, s[m]);
-                s[m + 1] = fmaf(kk[m + 1], be, s[m + 1]);
-                o0 = fmaf(qq[m], s[m], o0);
-                o1 = fmaf(qq[m + 1], s[m + 1], o1);
-            }
-            const float o = sum8(o0 + o1);
+                for (int c = 0; c < 4; ++c) {
+                    s[m][c] = fmaf(a2[m], s[m][c], k2[m] * be[c]);  // S_t = Diag(alpha) S_{t-1} + beta k e^T
+                    o[m & 1][c] = fmaf(q2[m], s[m][c], o[m & 1][c]);
+                    p[m & 1][c] = fmaf(n2[m], s[m][c], p[m & 1][c]);
+                }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) x[c] = p[0][c] + p[1][c];  // unused after a block's last token
+            sum16x4(x);
+            float y[4] = {o[0][0] + o[1][0], o[0][1] + o[1][1], o[0][2] + o[1][2], o[0][3] + o[1][3]};
+            const float4 o4 = gather4(sum16x4_split(y, r), lane);
             if (r == 0) {
-                O[(t * H + h) * kD + c] = scale * o;
-                E[(t * H + h) * kD + c] = e;
+                *reinterpret_cast<float4*>(O + (t * H + h) * kD + c0) =
+                    make_float4(scale * o4.x, scale * o4.y, scale * o4.z, scale * o4.w);
+                *reinterpret_cast<float4*>(E + (t * H + h) * kD + c0) = make_float4(e[0], e[1], e[2], e[3]);
             }
         }
     }
 }
 
+// dS <- Diag(alpha) (dS - beta k w^T) with the factors of a staged token and nbw = -beta w of the
+// lane's columns.
+__device__ __forceinline__ void bwd_decay(float (&ds)[8][4], const float (&a2)[8], const float (&k2)[8],
+                                          const float (&nbw)[4]) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ds[m][c] = a2[m] * fmaf(k2[m], nbw[c], ds[m][c]);
+}
+
+// One token of the backward sweep: dS' = [pending: Diag(alpha') (dS - beta' k' w'^T)] + scale q do^T
+// with (alpha', k', -beta' w') of the later token, w = dS'^T k summed over the column group (all
+// lanes get it); the stores and the dbeta / e.do partials of the token.
+template <bool kPending>
+__device__ __forceinline__ void bwd_token(float (&ds)[8][4], float (&nbw)[4], const ColTok& T, const ColTok& Pv,
+                                          int r, int cl, int c0, int lane, float scale, int64_t t, int H, int h,
+                                          float* W, float* dX, float* accb, float* acce) {
+    const int64_t HD = (int64_t)H * kD;
+    const float4 do4 = *reinterpret_cast<const float4*>(T.c0 + cl);
+    const float4 e4 = *reinterpret_cast<const float4*>(T.c1 + cl);
+    const float bt = T.beta;
+    const float sd[4] = {scale * do4.x, scale * do4.y, scale * do4.z, scale * do4.w};
+    float k2[8], q2[8];
+    load_rows(T.k + r * kSlice, k2);
+    load_rows(T.q + r * kSlice, q2);
+    float wp[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if constexpr (kPending) {
+        float pa[8], pk[8];
+        load_rows(Pv.a + r * kSlice, pa);
+        load_rows(Pv.k + r * kSlice, pk);
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float d = pa[m] * fmaf(pk[m], nbw[c], ds[m][c]);
+                ds[m][c] = fmaf(q2[m], sd[c], d);
+                wp[m & 1][c] = fmaf(k2[m], ds[m][c], wp[m & 1][c]);
+            }
+    } else {
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                ds[m][c] = fmaf(q2[m], sd[c], ds[m][c]);
+                wp[m & 1][c] = fmaf(k2[m], ds[m][c], wp[m & 1][c]);
+            }
+    }
+    float w[4] = {wp[0][0] + wp[1][0], wp[0][1] + wp[1][1], wp[0][2] + wp[1][2], wp[0][3] + wp[1][3]};
+    sum16x4(w);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) nbw[c] = -bt * w[c];
+    const bool lead = r == 0;
+    if (lead) {
+        *reinterpret_cast<float4*>(W + (t * H + h) * kD + c0) = make_float4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<float4*>(dX + t * 3 * HD + 2 * HD + (int64_t)h * kD + c0) =
+            make_float4(bt * w[0], bt * w[1], bt * w[2], bt * w[3]);
+    }
+    float pb = lead ? w[0] * e4.x + w[1] * e4.y + w[2] * e4.z + w[3] * e4.w : 0.f;
+    float pe = lead ? e4.x * do4.x + e4.y * do4.y + e4.z * do4.z + e4.w * do4.w : 0.f;
+    pb += __shfl_xor_sync(0xffffffffu, pb, 16);
+    pe += __shfl_xor_sync(0xffffffffu, pe, 16);
+    if (lane == 0) {
+        atomicAdd(accb, pb);
+        atomicAdd(acce, pe);
+    }
+}
+
 // Backward sweep of the state gradient, tokens in reverse: dS' = dS + scale q^ do^T,
-// w = dS'^T k^, dv = beta w, then dS <- Diag(alpha) (dS' - beta k^ w^T).  Writes w, dv, the sums
-// dbeta = w . e and e . do of every token (atomics over the CTAs of a unit), the state gradient at
-// the end of every segment (dSck: before that token's own terms) and at the start (dS0).
-__global__ void __launch_bounds__(256)
+// w = dS'^T k^, dv = beta w, then dS <- Diag(alpha) (dS' - beta k^ w^T) (applied in the next
+// token's pass).  Writes w, dv, the sums dbeta = w . e and e . do of every token (atomics over the
+// CTAs of a unit), the state gradient at the end of every segment (dSck: before that token's own
+// terms) and at the start (dS0).  Blocks are the forward sweep's, taken last to first, so that
+// every segment ends at the last token of a block.
+__global__ void __launch_bounds__(128)
 k_bwd_bwd_cols(const float* __restrict__ X, const float* __restrict__ g, const float* __restrict__ beta,
                const float* __restrict__ dO, const float* __restrict__ E, const int32_t* __restrict__ cu,
                const int64_t* __restrict__ prefix, int64_t T_total, int H, float scale,
@@ -336,8 +477,8 @@ k_bwd_bwd_cols(const float* __restrict__ X, const float* __restrict__ g, const f
     ColTok* buf = reinterpret_cast<ColTok*>(smem_raw);  // [2][kTB]
     __shared__ float acc[2][2][kTB];                   // [block parity][dbeta, e.do][token]
     const int u = blockIdx.x / kColCtas, cq = blockIdx.x % kColCtas, n = u / H, h = u % H;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane & 7;
-    const int cl = warp * 4 + (lane >> 3), c = cq * kCols + cl;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane & 15;
+    const int cl = warp * 8 + 4 * (lane >> 4), c0 = cq * kCols + cl;
     if (tid < 4 * kTB) (&acc[0][0][0])[tid] = 0.f;
     int64_t s0, s1;
     seq_range(cu, n, T_total, s0, s1);
@@ -345,79 +486,59 @@ k_bwd_bwd_cols(const float* __restrict__ X, const float* __restrict__ g, const f
     const int64_t sb = slot_base(prefix, n, H, h, nseg, slots);
     if (sb < 0) return;  // flagged by the forward sweep
     const int64_t HD = (int64_t)H * kD;
-    const ColSrc ds_src{dO, HD}, es{E, HD};
-    float ds[16];
+    const ColSrc dos{dO, HD}, es{E, HD};
+    float ds[8][4];
+    if (dS_fin) {
+        load_slice(dS_fin + (int64_t)u * kD * kD, r, c0, ds);
+    } else {
 #pragma unroll
-    for (int m = 0; m < 16; ++m) ds[m] = dS_fin ? dS_fin[((int64_t)u * kD + 16 * r + m) * kD + c] : 0.f;
-    // block b holds tokens [t0(b), s1 - b kTB), t0(b) = max(s0, s1 - (b + 1) kTB)
+        for (int m = 0; m < 8; ++m)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ds[m][c] = 0.f;
+    }
+    // step i takes block j = nblk - 1 - i: tokens [s0 + j kTB, min(s0 + (j + 1) kTB, s1))
     const int64_t nblk = (s1 - s0 + kTB - 1) / kTB;
-    auto t0_of = [&](int64_t b) { return s1 - (b + 1) * kTB > s0 ? s1 - (b + 1) * kTB : s0; };
-    auto nt_of = [&](int64_t b) { return (int)(s1 - b * kTB - t0_of(b)); };
-    if (nblk > 0) stage_cols(buf, t0_of(0), nt_of(0), X, g, beta, ds_src, es, 2, H, h, cq, tid);
+    auto t0_of = [&](int64_t i) { return s0 + (nblk - 1 - i) * kTB; };
+    auto nt_of = [&](int64_t i) { return (int)(s1 - t0_of(i) < kTB ? s1 - t0_of(i) : kTB); };
+    if (nblk > 0) stage_cols(buf, t0_of(0), nt_of(0), X, g, beta, dos, es, 2, H, h, cq, tid);
     cp_commit();
-    for (int64_t b = 0; b < nblk; ++b) {
+    for (int64_t i = 0; i < nblk; ++i) {
         __syncthreads();
-        if (b > 0 && tid < nt_of(b - 1)) {  // the sums of block b - 1 are complete
-            const int p = (b - 1) & 1;
-            const int64_t t = t0_of(b - 1) + tid;
+        if (i > 0 && tid < nt_of(i - 1)) {  // the sums of the previous step are complete
+            const int p = (i - 1) & 1;
+            const int64_t t = t0_of(i - 1) + tid;
             atomicAdd(dbeta + t * H + h, acc[p][0][tid]);
             atomicAdd(edo + t * H + h, acc[p][1][tid]);
             acc[p][0][tid] = 0.f;
             acc[p][1][tid] = 0.f;
         }
-        if (b + 1 < nblk)
-            stage_cols(buf + ((b + 1) & 1) * kTB, t0_of(b + 1), nt_of(b + 1), X, g, beta, ds_src, es, 2, H, h,
-                       cq, tid);
+        if (i + 1 < nblk)
+            stage_cols(buf + ((i + 1) & 1) * kTB, t0_of(i + 1), nt_of(i + 1), X, g, beta, dos, es, 2, H, h, cq,
+                       tid);
         cp_commit();
         cp_wait<1>();
         __syncthreads();
-        ColTok* st = buf + (b & 1) * kTB;
-        const int nt = nt_of(b);
-        const int64_t t0 = t0_of(b);
+        ColTok* st = buf + (i & 1) * kTB;
+        const int nt = nt_of(i);
+        const int64_t t0 = t0_of(i);
         stage_exp_cols(st, nt, tid);
         __syncthreads();
-        for (int tk = nt - 1; tk >= 0; --tk) {
-            const int64_t t = t0 + tk;
-            if ((t - s0) % kSeg == kSeg - 1 || t == s1 - 1) {
-                float* dst = dSck + (sb + (t - s0) / kSeg) * kD * kD;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) dst[(16 * r + m) * kD + c] = ds[m];
-            }
-            const ColTok& T = st[tk];
-            const float do_c = T.c0[cl], e_c = T.c1[cl], bt = T.beta;
-            float kk[16], qq[16];
-            load16(T.k + r * 20, kk);
-            load16(T.q + r * 20, qq);
-            const float sd = scale * do_c;
-            float w0 = 0.f, w1 = 0.f;
-#pragma unroll
-            for (int m = 0; m < 16; m += 2) {
-                ds[m] = fmaf(qq[m], sd, ds[m]);
-                ds[m + 1] = fmaf(qq[m + 1], sd, ds[m + 1]);
-                w0 = fmaf(kk[m], ds[m], w0);
-                w1 = fmaf(kk[m + 1], ds[m + 1], w1);
-            }
-            const float w = sum8(w0 + w1);
-            float aa[16];
-            load16(T.a + r * 20, aa);
-            const float nbw = -bt * w;
-#pragma unroll
-            for (int m = 0; m < 16; ++m) ds[m] = aa[m] * fmaf(kk[m], nbw, ds[m]);
-            float pb = 0.f, pe = 0.f;
-            if (r == 0) {
-                W[(t * H + h) * kD + c] = w;
-                dX[t * 3 * HD + 2 * HD + (int64_t)h * kD + c] = bt * w;
-                pb = w * e_c;
-                pe = e_c * do_c;
-            }
-            pb += __shfl_xor_sync(0xffffffffu, pb, 8);
-            pb += __shfl_xor_sync(0xffffffffu, pb, 16);
-            pe += __shfl_xor_sync(0xffffffffu, pe, 8);
-            pe += __shfl_xor_sync(0xffffffffu, pe, 16);
-            if (lane == 0) {
-                atomicAdd(&acc[b & 1][0][tk], pb);
-                atomicAdd(&acc[b & 1][1][tk], pe);
-            }
+        // the block's last token ends a segment when the segment is full or the sequence ends there
+        const int64_t tl = t0 + nt - 1;
+        if ((tl - s0) % kSeg == kSeg - 1 || tl == s1 - 1) store_slice(dSck + (sb + (tl - s0) / kSeg) * kD * kD, r, c0, ds);
+        float nbw[4];  // -beta w of the later token, whose decay is pending
+        float* ab = &acc[i & 1][0][0];
+        float* ae = &acc[i & 1][1][0];
+        bwd_token<false>(ds, nbw, st[nt - 1], st[nt - 1], r, cl, c0, lane, scale, tl, H, h, W, dX, ab + nt - 1,
+                         ae + nt - 1);
+        for (int tk = nt - 2; tk >= 0; --tk)
+            bwd_token<true>(ds, nbw, st[tk], st[tk + 1], r, cl, c0, lane, scale, t0 + tk, H, h, W, dX, ab + tk,
+                            ae + tk);
+        {  // the block's first token's decay, before its buffer is refilled
+            float pa[8], pk[8];
+            load_rows(st[0].a + r * kSlice, pa);
+            load_rows(st[0].k + r * kSlice, pk);
+            bwd_decay(ds, pa, pk, nbw);
         }
     }
     __syncthreads();
@@ -427,32 +548,70 @@ k_bwd_bwd_cols(const float* __restrict__ X, const float* __restrict__ g, const f
         atomicAdd(dbeta + t * H + h, acc[p][0][tid]);
         atomicAdd(edo + t * H + h, acc[p][1][tid]);
     }
-    if (dS0)
-#pragma unroll
-        for (int m = 0; m < 16; ++m) dS0[((int64_t)u * kD + 16 * r + m) * kD + c] = ds[m];
+    if (dS0) store_slice(dS0 + (int64_t)u * kD * kD, r, c0, ds);
 }
 
 // ------------------------------------------------------------------------------ row-layout segments
-// One CTA of 512 threads per (unit, segment): thread (rg, cg) owns rows 4 rg .. 4 rg + 3 and columns
-// 8 cg .. 8 cg + 7; the row sums a token needs (S x, dS' e) go over the 16 column groups of a
-// half-warp.  With e, w and do known for every token, both sweeps are row-local:
+// One CTA of 256 threads per (unit, segment): thread (rg, cg) owns rows 8 rg .. 8 rg + 7 and columns
+// 8 cg .. 8 cg + 7 (packed fp32 pairs); the row sums a token needs (S x, dS' e) go over the 16
+// column groups of a half-warp.  With e, w and do known for every token, both sweeps are row-local:
 //   forward from the segment's start state:  dq = scale (P do + beta k (e . do)),
 //                                            dk_read = -beta P w,   P = Diag(alpha) S_{t-1};
 //   backward from the segment's end gradient: dk_write = beta dS' e.
 // dg follows from the decay entering only through e^{Gamma_t} (read keys and queries) and
 // e^{-Gamma_t} (written keys), Gamma_t = sum_{s <= t} g_s:
 //   dGamma_t = q^ dq + k^ dk_read - k^ dk_write,  dg_t = sum_{s >= t} dGamma_s + rowsum(dS_T . S_T);
-// here the sums within the segment, the segment's total (segtot) and, for the last segment of a
-// sequence, the final-state term (fin).
-constexpr int kRowThreads = 512;
+// here the parts within the segment: dg <- -(sum of q dq + k dk_read over earlier tokens), the
+// global rows of e and w (staged, so free) <- dk_write and the suffix sums of -k dk_write; per
+// segment its sum of dGamma (segtot) and of the read part (segown); for the last segment of a
+// sequence the final-state term (fin).  The sweeps only write global memory.
+constexpr int kRowThreads = 256;
+constexpr int kColVec = kD + 12;  // column vectors skewed by 4 floats every 32, so that the eight
+                                  // column groups a quarter-warp reads fall in distinct banks
 struct RowTok {
-    float k[kD], a[kD], q[kD], e[kD], d[kD], w[kD];
+    float k[kD], a[kD], q[kD];
+    float e[kColVec], d[kColVec], w[kColVec];
     float beta, edo, pad[2];
 };
 constexpr int kRowSmem = kSeg * (int)sizeof(RowTok);
 
-// Sums 8 per-thread values over the 16 lanes of a half-warp (lane bits 0..3); afterwards lane
-// cg holds the total of value cg >> 1.
+// Sums 16 per-thread values over the 16 lanes of a half-warp (lane bits 0..3); afterwards lane
+// cg holds the total of value cg.
+__device__ __forceinline__ float reduce16_16(float (&v)[16], int cg) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const bool up = (cg & 8) != 0;
+        const float send = up ? v[i] : v[i + 8];
+        v[i] = (up ? v[i + 8] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const bool up = (cg & 4) != 0;
+        const float send = up ? v[i] : v[i + 4];
+        v[i] = (up ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const bool up = (cg & 2) != 0;
+        const float send = up ? v[i] : v[i + 2];
+        v[i] = (up ? v[i + 2] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    const bool up = (cg & 1) != 0;
+    const float send = up ? v[0] : v[1];
+    return (up ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, send, 1);
+}
+__device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ float pick8(const float (&x)[8], int a) {  // x[a] without local memory
+    float r = x[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) r = a == i ? x[i] : r;
+    return r;
+}
+// Same for 8 values; afterwards lanes cg hold the total of value cg >> 1.
 __device__ __forceinline__ float reduce8_16(float (&v)[8], int cg) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -473,41 +632,25 @@ __device__ __forceinline__ float reduce8_16(float (&v)[8], int cg) {
     }
     return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
-// Same for 4 values; afterwards lane cg holds the total of value cg >> 2.
-__device__ __forceinline__ float reduce4_16(float (&v)[4], int cg) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const bool up = (cg & 8) != 0;
-        const float send = up ? v[i] : v[i + 2];
-        v[i] = (up ? v[i + 2] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-    {
-        const bool up = (cg & 4) != 0;
-        const float send = up ? v[0] : v[1];
-        v[0] = (up ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
-    }
-    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
-    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
-}
 
-__device__ __forceinline__ float pick4(float4 v, int a) {  // component a of v, without local memory
-    return a == 0 ? v.x : a == 1 ? v.y : a == 2 ? v.z : v.w;
+__device__ __forceinline__ void load8p(const float* p, f2 (&x)[4]) {  // 8 floats as 4 pairs
+    const ulonglong2 a = reinterpret_cast<const ulonglong2*>(p)[0], b = reinterpret_cast<const ulonglong2*>(p)[1];
+    x[0].v = a.x;
+    x[1].v = a.y;
+    x[2].v = b.x;
+    x[3].v = b.y;
 }
-
-__device__ __forceinline__ void load8f(const float* p, float (&x)[8]) {
-    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
+__device__ __forceinline__ float hsum(f2 x) { return f2_lo(x) + f2_hi(x); }
 
 // Grid: units x max_seg CTAs (CTAs past a sequence's segment count return at once).
 __global__ void __launch_bounds__(kRowThreads, 1)
 k_bwd_rows(const float* __restrict__ X, const float* __restrict__ g, const float* __restrict__ beta,
-           const float* __restrict__ dO, const float* __restrict__ E, const float* __restrict__ W,
+           const float* __restrict__ dO, float* __restrict__ E, float* __restrict__ W,
            const float* __restrict__ edo, const int32_t* __restrict__ cu, const int64_t* __restrict__ prefix,
            int64_t T_total, int H, float scale, int max_seg, const float* __restrict__ Sck,
            const float* __restrict__ dSck, const float* __restrict__ dS_fin, float* __restrict__ dX,
-           float* __restrict__ dg, float* __restrict__ segtot, float* __restrict__ fin, int64_t slots) {
+           float* __restrict__ dg, float* __restrict__ segtot, float* __restrict__ segown, float* __restrict__ fin,
+           int64_t slots) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     RowTok* st = reinterpret_cast<RowTok*>(smem_raw);  // [kSeg]
     const int u = blockIdx.x / max_seg, sg = blockIdx.x % max_seg, n = u / H, h = u % H;
@@ -527,7 +670,7 @@ k_bwd_rows(const float* __restrict__ X, const float* __restrict__ g, const float
         const int64_t t = ta + tk, th = t * H + h;
         RowTok& s = st[tk];
         if (j < 192) {
-            const int part = j >> 5, jj = (j & 31) * 4;
+            const int part = j >> 5, jj = j & 31;
             const float* src = part == 0 ? X + t * 3 * HD + HD + (int64_t)h * kD
                              : part == 1 ? g + th * kD
                              : part == 2 ? X + t * 3 * HD + (int64_t)h * kD
@@ -535,7 +678,7 @@ k_bwd_rows(const float* __restrict__ X, const float* __restrict__ g, const float
                              : part == 4 ? dO + th * kD
                                          : W + th * kD;
             float* dst = part == 0 ? s.k : part == 1 ? s.a : part == 2 ? s.q : part == 3 ? s.e : part == 4 ? s.d : s.w;
-            cp16(dst + jj, src + jj);
+            cp16(dst + 4 * jj + (part >= 3 ? (jj >> 3) * 4 : 0), src + 4 * jj);
         } else {
             cp4(j == 192 ? &s.beta : &s.edo, (j == 192 ? beta : edo) + th);
         }
@@ -548,129 +691,142 @@ k_bwd_rows(const float* __restrict__ X, const float* __restrict__ g, const float
         x = expf(x);
     }
     __syncthreads();
-    const int r0 = 4 * rg, c0 = 8 * cg;
-    const bool writer = (cg & 3) == 0;
+    const int r0 = 8 * rg, cs = 8 * cg + (cg >> 2) * 4;  // first row; column offset in a skewed vector
+    const bool writer = (cg & 1) == 0;                  // lanes holding row r0 + (cg >> 1)
+    const int ra = cg >> 1;
     // ---- forward: S from the segment's start state
-    float s[4][8];
+    float pre = 0.f;  // writer lanes: sum over this segment's earlier tokens of q dq + k dk_read
+    f2 s[8][4];
     {
-        const float* src = Sck + (sb + sg) * kD * kD;
+        const float* src = Sck + (sb + sg) * kD * kD + 8 * cg;
 #pragma unroll
-        for (int a = 0; a < 4; ++a) load8f(src + (r0 + a) * kD + c0, s[a]);
+        for (int a = 0; a < 8; ++a) load8p(src + (r0 + a) * kD, s[a]);
     }
     for (int tk = 0; tk < nt; ++tk) {
         const RowTok& T = st[tk];
-        float e8[8], d8[8], w8[8];
-        load8f(T.e + c0, e8);
-        load8f(T.d + c0, d8);
-        load8f(T.w + c0, w8);
-        const float4 k4 = *reinterpret_cast<const float4*>(T.k + r0);
-        const float4 a4 = *reinterpret_cast<const float4*>(T.a + r0);
-        const float kr[4] = {k4.x, k4.y, k4.z, k4.w}, ar[4] = {a4.x, a4.y, a4.z, a4.w};
-        float v[8];
+        f2 e2[4], d2[4], w2[4];
+        load8p(T.e + cs, e2);
+        load8p(T.d + cs, d2);
+        load8p(T.w + cs, w2);
+        float kr[8], ar[8];
+        load8(T.k + r0, kr);
+        load8(T.a + r0, ar);
+        float v[16];
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            float x0 = 0.f, x1 = 0.f;
+        for (int a = 0; a < 8; ++a) {
+            f2 x0 = mul2(s[a][0], d2[0]), x1 = mul2(s[a][0], w2[0]);
 #pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                x0 = fmaf(s[a][b], d8[b], x0);
-                x1 = fmaf(s[a][b], w8[b], x1);
+            for (int p = 1; p < 4; ++p) {
+                x0 = fma2(s[a][p], d2[p], x0);
+                x1 = fma2(s[a][p], w2[p], x1);
             }
-            v[2 * a] = x0;
-            v[2 * a + 1] = x1;
+            v[2 * a] = hsum(x0);
+            v[2 * a + 1] = hsum(x1);
         }
-        const float sdo = reduce8_16(v, cg);               // (S_{t-1} do)_i   (cg & 2 == 0)
-        const float sw = __shfl_xor_sync(0xffffffffu, sdo, 2);  // (S_{t-1} w)_i on the writer lanes
+        const float red = reduce16_16(v, cg);  // lane cg: value cg (row cg >> 1; S do if even, S w if odd)
+        const float sw = __shfl_xor_sync(0xffffffffu, red, 1);
         const float bt = T.beta;
-        if (writer) {
-            const int a = cg >> 2, i = r0 + a;
-            const float al = pick4(a4, a), ki = pick4(k4, a);
-            const float dq = scale * (al * sdo + bt * ki * T.edo);
+        {  // computed on every lane, stored by the writer lanes
+            const int i = r0 + ra;
+            const float al = pick8(ar, ra), ki = pick8(kr, ra);
+            const float dq = scale * (al * red + bt * ki * T.edo);
             const float dkr = -bt * al * sw;
             const int64_t t = ta + tk;
-            dX[t * 3 * HD + (int64_t)h * kD + i] = dq;
-            dX[t * 3 * HD + HD + (int64_t)h * kD + i] = dkr;
-            dg[(t * H + h) * kD + i] = T.q[i] * dq + ki * dkr;
+            if (writer) {
+                dX[t * 3 * HD + (int64_t)h * kD + i] = dq;
+                dX[t * 3 * HD + HD + (int64_t)h * kD + i] = dkr;
+                dg[(t * H + h) * kD + i] = -pre;  // minus the sum of dGamma_read over earlier tokens
+            }
+            pre += T.q[i] * dq + ki * dkr;
         }
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const float bk = bt * kr[a];
+        for (int a = 0; a < 8; ++a) {
+            const f2 a2 = f2_dup(ar[a]), bk2 = f2_dup(bt * kr[a]);
 #pragma unroll
-            for (int b = 0; b < 8; ++b) s[a][b] = fmaf(bk, e8[b], ar[a] * s[a][b]);
+            for (int p = 0; p < 4; ++p) s[a][p] = fma2(bk2, e2[p], mul2(a2, s[a][p]));
         }
     }
     if (tb == s1) {  // the sequence's final state: rowsum(dS_T . S_T)
-        float f[4];
+        float f[8];
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
+        for (int a = 0; a < 8; ++a) {
             float x = 0.f;
             if (dS_fin) {
-                float d8[8];
-                load8f(dS_fin + ((int64_t)u * kD + r0 + a) * kD + c0, d8);
+                f2 d2[4];
+                load8p(dS_fin + ((int64_t)u * kD + r0 + a) * kD + 8 * cg, d2);
+                f2 y = mul2(d2[0], s[a][0]);
 #pragma unroll
-                for (int b = 0; b < 8; ++b) x = fmaf(d8[b], s[a][b], x);
+                for (int p = 1; p < 4; ++p) y = fma2(d2[p], s[a][p], y);
+                x = hsum(y);
             }
             f[a] = x;
         }
-        const float tot = reduce4_16(f, cg);
-        if (writer) fin[(int64_t)u * kD + r0 + (cg >> 2)] = tot;
+        const float tot = reduce8_16(f, cg);
+        if (writer) fin[(int64_t)u * kD + r0 + ra] = tot;
     }
     // ---- backward: dS from the segment's end gradient
-    float (&ds)[4][8] = s;
+    f2 (&ds)[8][4] = s;
     {
-        const float* src = dSck + (sb + sg) * kD * kD;
+        const float* src = dSck + (sb + sg) * kD * kD + 8 * cg;
 #pragma unroll
-        for (int a = 0; a < 4; ++a) load8f(src + (r0 + a) * kD + c0, ds[a]);
+        for (int a = 0; a < 8; ++a) load8p(src + (r0 + a) * kD, ds[a]);
     }
-    float run = 0.f;  // sum of dGamma over this segment's tokens >= t (writer lanes)
+    float run = 0.f;  // writer lanes: sum over this segment's tokens >= t of -k dk_write
     for (int tk = nt - 1; tk >= 0; --tk) {
         const RowTok& T = st[tk];
-        float e8[8], d8[8], w8[8];
-        load8f(T.e + c0, e8);
-        load8f(T.d + c0, d8);
-        load8f(T.w + c0, w8);
-        const float4 k4 = *reinterpret_cast<const float4*>(T.k + r0);
-        const float4 a4 = *reinterpret_cast<const float4*>(T.a + r0);
-        const float4 q4 = *reinterpret_cast<const float4*>(T.q + r0);
-        const float kr[4] = {k4.x, k4.y, k4.z, k4.w}, ar[4] = {a4.x, a4.y, a4.z, a4.w};
-        const float qr[4] = {q4.x, q4.y, q4.z, q4.w};
+        f2 e2[4], d2[4], w2[4];
+        load8p(T.e + cs, e2);
+        load8p(T.d + cs, d2);
+        load8p(T.w + cs, w2);
+        float kr[8], ar[8], qr[8];
+        load8(T.k + r0, kr);
+        load8(T.a + r0, ar);
+        load8(T.q + r0, qr);
         const float bt = T.beta;
-        float y[4];
+        float y[8];
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const float sq = scale * qr[a];
-            float x = 0.f;
+        for (int a = 0; a < 8; ++a) {
+            const f2 sq2 = f2_dup(scale * qr[a]);
+            ds[a][0] = fma2(sq2, d2[0], ds[a][0]);
+            f2 x = mul2(ds[a][0], e2[0]);
 #pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                ds[a][b] = fmaf(sq, d8[b], ds[a][b]);
-                x = fmaf(ds[a][b], e8[b], x);
+            for (int p = 1; p < 4; ++p) {
+                ds[a][p] = fma2(sq2, d2[p], ds[a][p]);
+                x = fma2(ds[a][p], e2[p], x);
             }
-            y[a] = x;
+            y[a] = hsum(x);
         }
-        const float dse = reduce4_16(y, cg);  // (dS'_t e_t)_i
-        if (writer) {
-            const int a = cg >> 2, i = r0 + a;
-            const int64_t t = ta + tk;
+        const float dse = reduce8_16(y, cg);  // (dS'_t e_t) of row cg >> 1
+        {  // the token's e and w rows are staged, so their global rows take dk_write and the suffix
+           // sums of -k dk_write (combined by the L2 kernel); stored by the writer lanes
+            const int i = r0 + ra;
+            const int64_t th = (ta + tk) * H + h;
             const float dkw = bt * dse;
-            float* pk = dX + t * 3 * HD + HD + (int64_t)h * kD + i;
-            *pk += dkw;
-            float* pg = dg + (t * H + h) * kD + i;
-            run += *pg - pick4(k4, a) * dkw;
-            *pg = run;
+            run -= pick8(kr, ra) * dkw;
+            if (writer) {
+                E[th * kD + i] = dkw;
+                W[th * kD + i] = run;
+            }
         }
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const float nbk = -bt * kr[a];
+        for (int a = 0; a < 8; ++a) {
+            const f2 a2 = f2_dup(ar[a]), nbk2 = f2_dup(-bt * kr[a]);
 #pragma unroll
-            for (int b = 0; b < 8; ++b) ds[a][b] = ar[a] * fmaf(nbk, w8[b], ds[a][b]);
+            for (int p = 0; p < 4; ++p) ds[a][p] = mul2(a2, fma2(nbk2, w2[p], ds[a][p]));
         }
     }
-    if (writer) segtot[(sb + sg) * kD + r0 + (cg >> 2)] = run;
+    if (writer) {
+        segtot[(sb + sg) * kD + r0 + ra] = pre + run;  // the segment's sum of dGamma
+        segown[(sb + sg) * kD + r0 + ra] = pre;        // added to its own tokens (dg = -pre_t + run_t + ...)
+    }
 }
 
 // dg carries: for each unit and channel, the segments from the last: the value to add to every
-// token of segment sg is fin + the totals of the segments after it (written over segtot).
+// token of segment sg is fin + the totals of the segments after it + its own read part (written
+// over segtot).
 __global__ void k_bwd_dg_carry(const int32_t* __restrict__ cu, const int64_t* __restrict__ prefix, int64_t T_total,
-                               int H, const float* __restrict__ fin, float* __restrict__ segtot, int64_t slots) {
+                               int H, const float* __restrict__ fin, float* __restrict__ segtot,
+                               const float* __restrict__ segown, int64_t slots) {
     const int u = blockIdx.x, i = threadIdx.x, n = u / H, h = u % H;
     int64_t s0, s1;
     seq_range(cu, n, T_total, s0, s1);
@@ -681,7 +837,7 @@ __global__ void k_bwd_dg_carry(const int32_t* __restrict__ cu, const int64_t* __
     for (int64_t sg = nseg - 1; sg >= 0; --sg) {
         float* p = segtot + (sb + sg) * kD + i;
         const float x = *p;
-        *p = carry;
+        *p = carry + segown[(sb + sg) * kD + i];
         carry += x;
     }
 }
@@ -731,11 +887,13 @@ __global__ void k_bwd_epilogue(float* __restrict__ O, const Tdy* __restrict__ dy
 }
 
 // ------------------------------------------------------------------------------ L2 backward
-// One warp per (token, head): dq^ -> d a_q = (dq^ - q^ (q^ . dq^)) / |a_q|, same for k, in place;
-// and dg += the carry of the token's segment.
+// One warp per (token, head): dk^ = dk_read + dk_write (the latter in dkw); dq^ -> d a_q =
+// (dq^ - q^ (q^ . dq^)) / |a_q|, same for k, in place; dg += the write part's suffix sum (dgw) and
+// the carry of the token's segment.
 __global__ void k_bwd_l2(const float* __restrict__ X, const float* __restrict__ nrm, const int32_t* __restrict__ cu,
                          const int64_t* __restrict__ prefix, int N, int64_t T_total, int H,
-                         const float* __restrict__ segtot, int64_t slots, float* __restrict__ dX,
+                         const float* __restrict__ segtot, const float* __restrict__ dkw,
+                         const float* __restrict__ dgw, int64_t slots, float* __restrict__ dX,
                          float* __restrict__ dg) {
     const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -747,7 +905,8 @@ __global__ void k_bwd_l2(const float* __restrict__ X, const float* __restrict__ 
     for (int part = 0; part < 2; ++part) {
         const int64_t off = t * 3 * HD + part * HD + (int64_t)h * kD + 4 * lane;
         const float4 x = *reinterpret_cast<const float4*>(X + off);
-        const float4 d = *reinterpret_cast<const float4*>(dX + off);
+        float4 d = *reinterpret_cast<const float4*>(dX + off);
+        if (part == 1) d = f4_add(d, *reinterpret_cast<const float4*>(dkw + row * kD + 4 * lane));
         const float xd = warp_sum(dot4(x, d));
         const float inv = 1.0f / (part == 0 ? nn.x : nn.y);
         *reinterpret_cast<float4*>(dX + off) = make_float4((d.x - x.x * xd) * inv, (d.y - x.y * xd) * inv,
@@ -767,7 +926,8 @@ __global__ void k_bwd_l2(const float* __restrict__ X, const float* __restrict__ 
     if (sb < 0) return;
     float4* p = reinterpret_cast<float4*>(dg + row * kD + 4 * lane);
     const float4 c = *reinterpret_cast<const float4*>(segtot + (sb + (t - s0) / kSeg) * kD + 4 * lane);
-    *p = f4_add(*p, c);
+    const float4 w = *reinterpret_cast<const float4*>(dgw + row * kD + 4 * lane);
+    *p = f4_add(f4_add(*p, c), w);
 }
 
 // ------------------------------------------------------------------------------ activation + conv backward
@@ -821,6 +981,8 @@ __global__ void k_bwd_conv(const Tio* __restrict__ q, const Tio* __restrict__ k,
     };
     float du1 = 0.f, du2 = 0.f, du3 = 0.f;  // du_{t+1}, du_{t+2}, du_{t+3}
     float gw0 = 0.f, gw1 = 0.f, gw2 = 0.f, gw3 = 0.f;
+    float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;  // raw inputs at t - 3 .. t (a sliding window)
+    bool fresh = true;
     for (int64_t t = (tb + 3 < s1 ? tb + 3 : s1) - 1; t >= ta; --t) {
         if (t < s0) {  // crossed the start of sequence n (which lies inside the tile)
             emit_state_grad(du1, du2, du3);
@@ -830,8 +992,20 @@ __global__ void k_bwd_conv(const Tio* __restrict__ q, const Tio* __restrict__ k,
                 seq_range(cu, n, T_total, s0, s1);
                 if (s0 <= t) break;
             }
+            fresh = true;
         }
-        const float x0 = raw(t - 3), x1 = raw(t - 2), x2 = raw(t - 1), x3 = raw(t);
+        if (fresh) {
+            x0 = raw(t - 3);
+            x1 = raw(t - 2);
+            x2 = raw(t - 1);
+            x3 = raw(t);
+            fresh = false;
+        } else {
+            x3 = x2;
+            x2 = x1;
+            x1 = x0;
+            x0 = raw(t - 3);
+        }
         const float uu = w.x * x0 + w.y * x1 + w.z * x2 + w.w * x3;
         const float sg = 1.0f / (1.0f + expf(-uu));
         const float du = dA[t * 3 * HD + ch] * sg * (1.0f + uu * (1.0f - sg));
@@ -872,6 +1046,7 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
     float* Sck = reinterpret_cast<float*>(ws + L.sck);
     float* dSck = reinterpret_cast<float*>(ws + L.dsck);
     float* segtot = reinterpret_cast<float*>(ws + L.segtot);
+    float* segown = reinterpret_cast<float*>(ws + L.segown);
     float* fin = reinterpret_cast<float*>(ws + L.fin);
     int64_t* prefix = reinterpret_cast<int64_t*>(ws + L.prefix);
     cudaError_t e;
@@ -897,7 +1072,7 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
         (e = cudaFuncSetAttribute(k_bwd_rows, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmem)))
         return e;
     const unsigned cg = (unsigned)(units * kColCtas);
-    k_bwd_fwd_cols<<<cg, 256, kColSmem, s>>>(X, a.g, a.beta, a.cu_seqlens, prefix, T, a.H, a.scale,
+    k_bwd_fwd_cols<<<cg, 128, kColSmem, s>>>(X, a.g, a.beta, a.cu_seqlens, prefix, T, a.H, a.scale,
                                              a.initial_state, O, E, Sck, L.slots, a.d_status);
     if ((e = cudaGetLastError())) return e;
     if (rows > 0) {
@@ -909,18 +1084,18 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
                                                           rows, b.dgate, b.drms_w);
         if ((e = cudaGetLastError())) return e;
     }
-    k_bwd_bwd_cols<<<cg, 256, kColSmem, s>>>(X, a.g, a.beta, O, E, a.cu_seqlens, prefix, T, a.H, a.scale,
+    k_bwd_bwd_cols<<<cg, 128, kColSmem, s>>>(X, a.g, a.beta, O, E, a.cu_seqlens, prefix, T, a.H, a.scale,
                                              b.d_final_state, W, dX, b.dbeta, edo, dSck, b.dinitial_state,
                                              L.slots);
     if ((e = cudaGetLastError())) return e;
     if (rows == 0) return cudaSuccess;
     k_bwd_rows<<<(unsigned)(units * L.max_seg), kRowThreads, kRowSmem, s>>>(
         X, a.g, a.beta, O, E, W, edo, a.cu_seqlens, prefix, T, a.H, a.scale, (int)L.max_seg, Sck, dSck,
-        b.d_final_state, dX, b.dg, segtot, fin, L.slots);
+        b.d_final_state, dX, b.dg, segtot, segown, fin, L.slots);
     if ((e = cudaGetLastError())) return e;
-    k_bwd_dg_carry<<<(unsigned)units, kD, 0, s>>>(a.cu_seqlens, prefix, T, a.H, fin, segtot, L.slots);
+    k_bwd_dg_carry<<<(unsigned)units, kD, 0, s>>>(a.cu_seqlens, prefix, T, a.H, fin, segtot, segown, L.slots);
     if ((e = cudaGetLastError())) return e;
-    k_bwd_l2<<<rb, 256, 0, s>>>(X, nrm, a.cu_seqlens, prefix, a.N, T, a.H, segtot, L.slots, dX, b.dg);
+    k_bwd_l2<<<rb, 256, 0, s>>>(X, nrm, a.cu_seqlens, prefix, a.N, T, a.H, segtot, E, W, L.slots, dX, b.dg);
     if ((e = cudaGetLastError())) return e;
     const int cblocks = (3 * a.H * kD + 255) / 256;
     const int64_t tiles = (T + kConvTile - 1) / kConvTile;
@@ -964,6 +1139,7 @@ BackwardLayout backward_layout(const kda_backward_args& b) {
     L.sck = take(segs * H * kD * kD * 4);
     L.dsck = take(segs * H * kD * kD * 4);
     L.segtot = take(segs * H * kD * 4);
+    L.segown = take(segs * H * kD * 4);
     L.fin = take(N * H * kD * 4);
     L.prefix = take((N + 1) * 8);
     L.total = off;

@@ -222,12 +222,13 @@ struct BackwardLayout {
     size_t nrm;      // [T][H][2] fp32: the L2 denominators of q and k
     size_t o;        // [T][H][D] fp32: o before the epilogue, then its gradient
     size_t dx;       // [T][3][H][D] fp32: gradients of q^, k^, v, then of the conv outputs
-    size_t e;        // [T][H][D] fp32: e_t = v_t - P_t^T k_t
-    size_t w;        // [T][H][D] fp32: w_t = dS'_t^T k_t
+    size_t e;        // [T][H][D] fp32: e_t = v_t - P_t^T k_t, then dk_write
+    size_t w;        // [T][H][D] fp32: w_t = dS'_t^T k_t, then the write part of dg
     size_t edo;      // [T][H] fp32: e_t . do_t
     size_t sck;      // [slots][D][D] fp32: the state at the start of every segment
     size_t dsck;     // [slots][D][D] fp32: the state gradient at the end of every segment
     size_t segtot;   // [slots][D] fp32: dg sums per segment, then the carries
+    size_t segown;   // [slots][D] fp32: the read part of each segment's dg sum
     size_t fin;      // [N][H][D] fp32: rowsum(dS_T . S_T)
     size_t prefix;   // [N + 1] int64: segments before each sequence
     int64_t slots;   // checkpoint slots: H times the sum over sequences of ceil(len / kBwdSeg)
