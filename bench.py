@@ -572,7 +572,9 @@ def time_backward(args, pg, dev, stream, peaks, peak_src, world):
     import torch
     import kimi_delta_attention_16_gb300 as kda
     from kimi_delta_attention_16_gb300 import synth
-    inp = synth.make_prefill("layer_8k", seed=1, device=dev, s0_std=0.02, conv_state=True, rms_w="random")
+    short = {"T": args.tokens} if args.tokens else {}  # a shorter case of the same workload (profiles)
+    inp = synth.make_prefill("layer_8k", seed=1, device=dev, s0_std=0.02, conv_state=True, rms_w="random",
+                             **short)
     T, H, D, N = inp.T, inp.H, inp.D, inp.N
     gen = torch.Generator(device=dev)
     gen.manual_seed(9)
@@ -601,7 +603,7 @@ def time_backward(args, pg, dev, stream, peaks, peak_src, world):
     ms = max_over_ranks(pg, e0.elapsed_time(e1) / steps, dev)
     flops = BWD_FLOP_PER_TOKEN_HEAD * T * H
     tf = flops / (ms / 1e3) / 1e12
-    obj = {"metric": "KDA backward tokens/s (layer_8k: T=8192, H=96, d=128; all input gradients)",
+    obj = {"metric": f"KDA backward tokens/s (layer_8k: T={T}, H=96, d=128; all input gradients)",
            "value": round(aggregate_rate(world, T, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
            "steps": steps, "workspace_bytes": ws.numel(),
            "roofline": {"kernel": "the whole kda_backward call (fp32 SIMT recurrence sweeps dominate)",
