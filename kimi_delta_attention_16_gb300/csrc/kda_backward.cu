@@ -45,6 +45,22 @@ __device__ __forceinline__ float warp_sum(float v) {
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
     return v;
 }
+// Four consecutive inputs as floats (one 8-byte or 16-byte load).
+__device__ __forceinline__ void load4(const bf16* p, float (&x)[4]) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    x[0] = __uint_as_float(u.x << 16);
+    x[1] = __uint_as_float(u.x & 0xffff0000u);
+    x[2] = __uint_as_float(u.y << 16);
+    x[3] = __uint_as_float(u.y & 0xffff0000u);
+}
+__device__ __forceinline__ void load4(const float* p, float (&x)[4]) {
+    const float4 f = *reinterpret_cast<const float4*>(p);
+    x[0] = f.x;
+    x[1] = f.y;
+    x[2] = f.z;
+    x[3] = f.w;
+}
+
 // ------------------------------------------------------------------------------ prep
 // One warp per (token, head): conv + SiLU of the q, k, v channels of the head (lane l: channels
 // 4 l .. 4 l + 3), the L2 norms of q and k.  X: [T][3][H][D] fp32 (q^, k^, v), nrm: [T][H][2].
@@ -74,19 +90,26 @@ __global__ void k_bwd_prep(const Tio* __restrict__ q, const Tio* __restrict__ k,
     float ss[2] = {0.f, 0.f};
 #pragma unroll
     for (int part = 0; part < 3; ++part) {
+        // the raw inputs of the lane's 4 channels at t - 3 .. t: one vector load per token
+        float x[4][4];  // [token j][channel m]
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t p = t - 3 + j;
+            if (p >= s0) {
+                load4(src[part] + p * xs + (int64_t)h * kD + 4 * lane, x[j]);
+            } else {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const int64_t ch = (int64_t)part * HD + (int64_t)h * kD + 4 * lane + m;
+                    x[j][m] = cs_in ? to_f(cs_in[((int64_t)n * 3 * HD + ch) * 3 + 3 + (p - s0)]) : 0.f;
+                }
+            }
+        }
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            const int d = 4 * lane + m;
-            const int64_t ch = (int64_t)part * HD + (int64_t)h * kD + d;
+            const int64_t ch = (int64_t)part * HD + (int64_t)h * kD + 4 * lane + m;
             const float4 w = *reinterpret_cast<const float4*>(conv_w + ch * 4);
-            float x[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int64_t p = t - 3 + j;
-                if (p >= s0) x[j] = to_f(src[part][p * xs + (int64_t)h * kD + d]);
-                else x[j] = cs_in ? to_f(cs_in[((int64_t)n * 3 * HD + ch) * 3 + 3 + (p - s0)]) : 0.f;
-            }
-            const float u = w.x * x[0] + w.y * x[1] + w.z * x[2] + w.w * x[3];
+            const float u = w.x * x[0][m] + w.y * x[1][m] + w.z * x[2][m] + w.w * x[3][m];
             out[part][m] = u / (1.0f + expf(-u));
             if (part < 2) ss[part] += out[part][m] * out[part][m];
         }
@@ -982,8 +1005,29 @@ __global__ void k_bwd_conv(const Tio* __restrict__ q, const Tio* __restrict__ k,
     float du1 = 0.f, du2 = 0.f, du3 = 0.f;  // du_{t+1}, du_{t+2}, du_{t+3}
     float gw0 = 0.f, gw1 = 0.f, gw2 = 0.f, gw3 = 0.f;
     float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;  // raw inputs at t - 3 .. t (a sliding window)
+    // token t, given its oldest window input raw(t - 3) and its da (the window holds t - 2 .. t + 1)
+    auto step = [&](int64_t t, float xnew, float da) {
+        x3 = x2;
+        x2 = x1;
+        x1 = x0;
+        x0 = xnew;
+        const float uu = w.x * x0 + w.y * x1 + w.z * x2 + w.w * x3;
+        const float sg = 1.0f / (1.0f + expf(-uu));
+        const float du = da * sg * (1.0f + uu * (1.0f - sg));
+        if (t < tb) {
+            dst[t * HD + hc] = w.w * du + w.z * du1 + w.y * du2 + w.x * du3;
+            gw0 += x0 * du;
+            gw1 += x1 * du;
+            gw2 += x2 * du;
+            gw3 += x3 * du;
+        }
+        du3 = du2;
+        du2 = du1;
+        du1 = du;
+    };
+    const int64_t HD3 = 3 * HD;
     bool fresh = true;
-    for (int64_t t = (tb + 3 < s1 ? tb + 3 : s1) - 1; t >= ta; --t) {
+    for (int64_t t = (tb + 3 < s1 ? tb + 3 : s1) - 1; t >= ta;) {
         if (t < s0) {  // crossed the start of sequence n (which lies inside the tile)
             emit_state_grad(du1, du2, du3);
             du1 = du2 = du3 = 0.f;
@@ -995,30 +1039,25 @@ __global__ void k_bwd_conv(const Tio* __restrict__ q, const Tio* __restrict__ k,
             fresh = true;
         }
         if (fresh) {
-            x0 = raw(t - 3);
-            x1 = raw(t - 2);
-            x2 = raw(t - 1);
-            x3 = raw(t);
+            x0 = raw(t - 2);
+            x1 = raw(t - 1);
+            x2 = raw(t);
             fresh = false;
+        }
+        if (t - 6 >= s0 && t - 3 >= ta) {  // four tokens inside the sequence: their loads first
+            const float r0 = to_f(src[(t - 3) * xs + hc]), r1 = to_f(src[(t - 4) * xs + hc]);
+            const float r2 = to_f(src[(t - 5) * xs + hc]), r3 = to_f(src[(t - 6) * xs + hc]);
+            const float d0 = dA[t * HD3 + ch], d1 = dA[(t - 1) * HD3 + ch];
+            const float d2 = dA[(t - 2) * HD3 + ch], d3 = dA[(t - 3) * HD3 + ch];
+            step(t, r0, d0);
+            step(t - 1, r1, d1);
+            step(t - 2, r2, d2);
+            step(t - 3, r3, d3);
+            t -= 4;
         } else {
-            x3 = x2;
-            x2 = x1;
-            x1 = x0;
-            x0 = raw(t - 3);
+            step(t, raw(t - 3), dA[t * HD3 + ch]);
+            --t;
         }
-        const float uu = w.x * x0 + w.y * x1 + w.z * x2 + w.w * x3;
-        const float sg = 1.0f / (1.0f + expf(-uu));
-        const float du = dA[t * 3 * HD + ch] * sg * (1.0f + uu * (1.0f - sg));
-        if (t < tb) {
-            dst[t * HD + hc] = w.w * du + w.z * du1 + w.y * du2 + w.x * du3;
-            gw0 += x0 * du;
-            gw1 += x1 * du;
-            gw2 += x2 * du;
-            gw3 += x3 * du;
-        }
-        du3 = du2;
-        du2 = du1;
-        du1 = du;
     }
     if (s0 == ta) emit_state_grad(du1, du2, du3);  // sequence n starts at the tile's first token
     float* dw = dconv_w + (int64_t)ch * 4;
