@@ -22,15 +22,17 @@
 // stage.  Neither the request issue nor the 64 KB store stalls a compute warp.
 //
 // Sixteen compute warps; warp w owns value columns 8 w .. 8 w + 7 and lane l
-// owns column 8 w + (l & 7) on the rows {8 j + 2 rb, 8 j + 2 rb + 1 : j < 16},
-// rb = l >> 3, as 16 packed fp32 pairs of consecutive rows.  A column's sums
-// over the key rows (the probe S_bar^T k and the readout S^T q) take two
-// shuffles across the four lanes that share it, so no barrier is needed
-// between tokens; with this row choice the state's shared-memory accesses
-// (row r, column c at chunk ((c mod 32) / 4) xor (r mod 8) of the swizzle)
-// are conflict-free.  The per-row factors of every token (q, k, e^g) are
-// kept in shared memory permuted to each lane's pair order.  After the last
-// token, warp t normalises token t's output (RMSNorm, weight, gate).
+// owns the rows l, l + 32, l + 64, l + 96 of all eight, as packed fp32 pairs of
+// adjacent columns.  A token's per-row factors (q, k, e^g) are then read by
+// the 32 lanes of a warp from 32 consecutive floats (one shared-memory
+// wavefront per 32 values, instead of the eight-lane broadcasts a
+// column-per-lane layout needs), and the column sums over the key rows (the
+// probe S_bar^T k and the readout S^T q) are one transposed reduction of the
+// eight columns over the warp; no barrier is needed between tokens.  The
+// state's shared-memory accesses (row r, column c at 16-byte chunk
+// ((c mod 32) / 4) xor (r mod 8) of the swizzle) are conflict-free: the eight
+// lanes of a quarter-warp read eight consecutive rows.  After the last token,
+// warp t normalises token t's output (RMSNorm, weight, gate).
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 #include "kda_tc_ptx.cuh"
@@ -43,9 +45,7 @@ constexpr int kD = 128;
 constexpr int kCompute = 512;             // sixteen compute warps
 constexpr int kThreads = kCompute + 32;   // + the producer warp
 constexpr int kL8 = kShortMaxL;
-// per-token stride (floats) of the permuted factor arrays: four row blocks of 32 floats, each
-// padded to 36 so that the blocks the four lanes of a column read fall on different banks
-constexpr int kRb = 36, kFs = 4 * kRb;
+constexpr int kFs = kD;  // per-token stride (floats) of the factor arrays
 // static shared memory of the kernel (sv, sgate, sW, sRms, snorm, sbeta, barriers)
 constexpr uint32_t kStaticSmem = 4u * (2 * kL8 * kD + 3 * kD * 4 + kD + kL8 * 2 + 2 * kL8) + 32u;
 
@@ -124,6 +124,59 @@ __device__ __forceinline__ void sts_f2x2(void* p, f2 a, f2 b) {
     asm volatile("st.shared.v2.b64 [%0], {%1, %2};" ::"r"(tc::smem_u32(p)), "l"(a.v), "l"(b.v) : "memory");
 }
 
+// Sums 8 per-lane values over the 32 lanes of a warp; afterwards lane l holds the total of value
+// (l >> 2) & 7 (lanes 4 c .. 4 c + 3 hold value c).
+__device__ __forceinline__ float reduce8_32(float (&v)[8], int lane) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const bool up = (lane & 16) != 0;
+        const float send = up ? v[i] : v[i + 4];
+        v[i] = (up ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const bool up = (lane & 8) != 0;
+        const float send = up ? v[i] : v[i + 2];
+        v[i] = (up ? v[i + 2] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    {
+        const bool up = (lane & 4) != 0;
+        const float send = up ? v[0] : v[1];
+        v[0] = (up ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
+// Sums 16 per-lane values over the 32 lanes of a warp; afterwards lane l holds the total of value
+// l >> 1.
+__device__ __forceinline__ float reduce16_32(float (&v)[16], int lane) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const bool up = (lane & 16) != 0;
+        const float send = up ? v[i] : v[i + 8];
+        v[i] = (up ? v[i + 8] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const bool up = (lane & 8) != 0;
+        const float send = up ? v[i] : v[i + 4];
+        v[i] = (up ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const bool up = (lane & 4) != 0;
+        const float send = up ? v[i] : v[i + 2];
+        v[i] = (up ? v[i + 2] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    {
+        const bool up = (lane & 2) != 0;
+        const float send = up ? v[0] : v[1];
+        v[0] = (up ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
 template <typename Tio, typename To>
 __global__ void __launch_bounds__(kThreads, 1)
 k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int has_s0, int has_sfin,
@@ -144,8 +197,7 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
     const uint32_t raw_addr = tc::smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t sbase = tc::smem_u32(sm);
-    // after the two stages: q, k and e^g ([Lmax][4][kRb]) of every token in each lane's pair
-    // order (pair j of row block rb = rows 8 j + 2 rb, 8 j + 2 rb + 1), then o before its
+    // after the two stages: q, k and e^g ([Lmax][128]) of every token, then o before its
     // normalisation ([Lmax][128])
     float* fq = reinterpret_cast<float*>(sm + 2 * ST.bytes);
     float* fk = fq + Lmax * kFs;
@@ -243,9 +295,7 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
     }
 
     // ---------------------------------------------------------------- compute warps
-    const int col = 8 * warp + (lane & 7), rb = lane >> 3;
-    // position of channel d in the pair order of the factor arrays
-    auto perm = [](int d) { return ((d >> 1) & 3) * kRb + (d >> 3) * 2 + (d & 1); };
+    const int c0w = 8 * warp;  // the warp's first value column
     // output of the unit's tokens (warp t for token t): o = scale S^T q / |q| from the readout
     // sums, RMSNorm, weight, gate
     auto emit_unit = [&](int64_t ja, int jh, int jL) {
@@ -293,14 +343,18 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
             break;
         }
         uint8_t* st = sm + (uint32_t)b * ST.bytes;
-        // the state into registers: pair j = rows 8 j + 2 rb, 8 j + 2 rb + 1 of this lane's column
-        f2 s2[16];
+        // the state into registers: s2[m][p] = columns c0w + 2 p, c0w + 2 p + 1 of row lane + 32 m
+        f2 s2[4][4];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const int r = 8 * j + 2 * rb;
-            s2[j] = has_s0 ? f2_of(*reinterpret_cast<const float*>(st + state_off(r, col)),
-                                   *reinterpret_cast<const float*>(st + state_off(r + 1, col)))
-                           : f2_dup(0.f);
+        for (int m = 0; m < 4; ++m) {
+            const int r = lane + 32 * m;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (has_s0) x = *reinterpret_cast<const float4*>(st + state_off(r, c0w + 4 * hf));
+                s2[m][2 * hf] = f2_of(x.x, x.y);
+                s2[m][2 * hf + 1] = f2_of(x.z, x.w);
+            }
         }
         // conv + SiLU of every token, one channel per thread (warps 0-11); the rolled window out
         for (int ch = tid; ch < 3 * kD; ch += kCompute) {
@@ -314,7 +368,7 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
             }
             const Tio* rp = reinterpret_cast<const Tio*>(st + ST.rows + (uint32_t)part * ST.part) + d;
             const float4 w = *reinterpret_cast<const float4*>(&sW[ch * 4]);
-            float* dst = part == 0 ? fq + perm(d) : part == 1 ? fk + perm(d) : &sv[0][d];
+            float* dst = part == 0 ? fq + d : part == 1 ? fk + d : &sv[0][d];
             const int dstride = part == 2 ? kD : kFs;
             for (int t = 0; t < L; ++t) {
                 const float x = to_f(rp[t * kD]);
@@ -335,7 +389,7 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
             const Tio* gt = reinterpret_cast<const Tio*>(st + ST.rows + 3 * ST.part);
             for (int idx = tid; idx < L * kD; idx += kCompute) {
                 const int t = idx >> 7, c = idx & (kD - 1);
-                fa[t * kFs + perm(c)] = decay_exp<Tio>(gs[idx]);
+                fa[t * kFs + c] = decay_exp<Tio>(gs[idx]);
                 sgate[t][c] = has_gate ? act_sigmoid<Tio>(to_f(gt[idx])) : 1.f;
             }
         }
@@ -343,8 +397,8 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
         // L2 norms of q and k, one vector per warp
         if (warp < 2 * L) {
             const int t = warp >> 1;
-            const float* src = (warp & 1 ? fk : fq) + t * kFs;  // lane: 4 of the 128 (rb = lane / 8)
-            const float4 x4 = *reinterpret_cast<const float4*>(src + (lane >> 3) * kRb + 4 * (lane & 7));
+            const float* src = (warp & 1 ? fk : fq) + t * kFs;  // lane: channels 4 lane .. 4 lane + 3
+            const float4 x4 = *reinterpret_cast<const float4*>(src + 4 * lane);
             float ss = x4.x * x4.x + x4.y * x4.y + x4.z * x4.z + x4.w * x4.w;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
@@ -352,52 +406,67 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
         }
         cbar();  // C
 
-        // ---- tokens: no barrier between them; a column's sums over its 4 lanes by shuffles
+        // ---- tokens: no barrier between them.  The eight columns' sums over the warp go through one
+        // transposed reduction per token, which carries token t's probe together with token
+        // t - 1's readout (so the readout never adds a reduction of its own to the chain).
+        f2 O[4] = {f2_dup(0.f), f2_dup(0.f), f2_dup(0.f), f2_dup(0.f)};  // readout of the previous token
         for (int t = 0; t < L; ++t) {
-            const float* kt = fk + t * kFs + rb * kRb;
-            const float* at = fa + t * kFs + rb * kRb;
-            const float* qt = fq + t * kFs + rb * kRb;
+            const float* kt = fk + t * kFs + lane;
+            const float* at = fa + t * kFs + lane;
+            const float* qt = fq + t * kFs + lane;
             const float ik = snorm[t][1];
-            f2 kr[16];
-            f2 P0 = f2_dup(0.f), P1 = f2_dup(0.f);  // two chains
+            f2 k2[4], P[4] = {f2_dup(0.f), f2_dup(0.f), f2_dup(0.f), f2_dup(0.f)};
 #pragma unroll
-            for (int j2 = 0; j2 < 8; ++j2) {  // decay and probe, two pairs per step
-                lds_f2x2(kt + 4 * j2, kr[2 * j2], kr[2 * j2 + 1]);
-                f2 a0, a1;
-                lds_f2x2(at + 4 * j2, a0, a1);
-                s2[2 * j2] = mul2(a0, s2[2 * j2]);
-                s2[2 * j2 + 1] = mul2(a1, s2[2 * j2 + 1]);
-                P0 = fma2(kr[2 * j2], s2[2 * j2], P0);
-                P1 = fma2(kr[2 * j2 + 1], s2[2 * j2 + 1], P1);
-            }
-            const f2 P = add2(P0, P1);
-            float p = f2_lo(P) + f2_hi(P);
-            p += __shfl_xor_sync(0xffffffffu, p, 8);
-            p += __shfl_xor_sync(0xffffffffu, p, 16);
-            const f2 e2 = f2_dup(sbeta[b][t] * ik * (sv[t][col] - ik * p));
-            f2 O0 = f2_dup(0.f), O1 = f2_dup(0.f);
+            for (int m = 0; m < 4; ++m) {  // decay and probe
+                k2[m] = f2_dup(kt[32 * m]);
+                const f2 a2 = f2_dup(at[32 * m]);
 #pragma unroll
-            for (int j2 = 0; j2 < 8; ++j2) {  // write and readout
-                f2 q0, q1;
-                lds_f2x2(qt + 4 * j2, q0, q1);
-                s2[2 * j2] = fma2(kr[2 * j2], e2, s2[2 * j2]);
-                s2[2 * j2 + 1] = fma2(kr[2 * j2 + 1], e2, s2[2 * j2 + 1]);
-                O0 = fma2(q0, s2[2 * j2], O0);
-                O1 = fma2(q1, s2[2 * j2 + 1], O1);
+                for (int p = 0; p < 4; ++p) {
+                    s2[m][p] = mul2(a2, s2[m][p]);
+                    P[p] = fma2(k2[m], s2[m][p], P[p]);
+                }
             }
-            const f2 O = add2(O0, O1);
-            float o = f2_lo(O) + f2_hi(O);
-            o += __shfl_xor_sync(0xffffffffu, o, 8);
-            o += __shfl_xor_sync(0xffffffffu, o, 16);
-            if (rb == 0) so[t * kD + col] = o;
+            float v16[16] = {f2_lo(P[0]), f2_hi(P[0]), f2_lo(P[1]), f2_hi(P[1]),
+                             f2_lo(P[2]), f2_hi(P[2]), f2_lo(P[3]), f2_hi(P[3]),
+                             f2_lo(O[0]), f2_hi(O[0]), f2_lo(O[1]), f2_hi(O[1]),
+                             f2_lo(O[2]), f2_hi(O[2]), f2_lo(O[3]), f2_hi(O[3])};
+            const float red = reduce16_32(v16, lane);  // lane l: value l >> 1
+            if (t > 0 && lane >= 16 && (lane & 1) == 0) so[(t - 1) * kD + c0w + ((lane >> 1) - 8)] = red;
+            const float bk = sbeta[b][t] * ik;
+            const float4 va = *reinterpret_cast<const float4*>(&sv[t][c0w]);
+            const float4 vb = *reinterpret_cast<const float4*>(&sv[t][c0w + 4]);
+            const float vv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+            float e[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) e[c] = bk * (vv[c] - ik * __shfl_sync(0xffffffffu, red, 2 * c));
+#pragma unroll
+            for (int p = 0; p < 4; ++p) O[p] = f2_dup(0.f);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {  // write and readout
+                const f2 q2 = f2_dup(qt[32 * m]);
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    s2[m][p] = fma2(k2[m], f2_of(e[2 * p], e[2 * p + 1]), s2[m][p]);
+                    O[p] = fma2(q2, s2[m][p], O[p]);
+                }
+            }
+        }
+        if (L > 0) {  // the last token's readout
+            float o8[8] = {f2_lo(O[0]), f2_hi(O[0]), f2_lo(O[1]), f2_hi(O[1]),
+                           f2_lo(O[2]), f2_hi(O[2]), f2_lo(O[3]), f2_hi(O[3])};
+            const float ot = reduce8_32(o8, lane);
+            if ((lane & 3) == 0) so[(L - 1) * kD + c0w + ((lane >> 2) & 7)] = ot;
         }
         // the final state back into the stage for the producer's tensor-map stores; release it
         if (has_sfin) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int r = 8 * j + 2 * rb;
-                *reinterpret_cast<float*>(st + state_off(r, col)) = f2_lo(s2[j]);
-                *reinterpret_cast<float*>(st + state_off(r + 1, col)) = f2_hi(s2[j]);
+            for (int m = 0; m < 4; ++m) {
+                const int r = lane + 32 * m;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+                    *reinterpret_cast<float4*>(st + state_off(r, c0w + 4 * hf)) =
+                        make_float4(f2_lo(s2[m][2 * hf]), f2_hi(s2[m][2 * hf]), f2_lo(s2[m][2 * hf + 1]),
+                                    f2_hi(s2[m][2 * hf + 1]));
             }
             tc::fence_async_smem();
         }
