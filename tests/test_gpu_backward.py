@@ -87,8 +87,9 @@ def _case(io, lengths, H=2, seed=0, g_range=(-5.0, 0.0), beta_one=False, out_dt=
 
 @pytest.mark.parametrize("io", ["bf16", "fp32"])
 def test_backward_parity_varlen_all_inputs(io):
-    """Ragged batch (segments of 32 tokens cut mid-sequence, a 1-token and an empty sequence),
-    every optional input given: gate, RMSNorm weight, initial state, conv state, dS_fin."""
+    """Ragged batch (64-token checkpoint segments and 8-token staging blocks cut mid-sequence, a
+    1-token and an empty sequence), every optional input given: gate, RMSNorm weight, initial
+    state, conv state, dS_fin."""
     inp, dy, dsf = _case(io, [70, 1, 0, 33, 130], seed=11)
     _check(_gpu_backward(inp, dy, dsf), _oracle_backward(inp, dy, dsf))
 
@@ -120,7 +121,7 @@ def test_backward_parity_decay_extremes(g_range, beta_one):
 
 
 def test_backward_parity_long_sequence():
-    """One sequence of 1000 tokens (32 segments of the replay) and one head."""
+    """One sequence of 1000 tokens (16 checkpoint segments, the last one partial) and one head."""
     inp, dy, dsf = _case("bf16", [1000], H=1, seed=51, g_range=(-0.5, 0.0))
     _check(_gpu_backward(inp, dy, dsf), _oracle_backward(inp, dy, dsf))
 
@@ -162,3 +163,20 @@ def test_backward_rejects_unsupported_shapes():
     with pytest.raises(kda.KDAError) as e:
         kda.kda_backward(inp.q, inp.k, inp.v, inp.conv_w, inp.g, inp.beta, inp.cu_seqlens, dy)
     assert e.value.status == 2
+
+
+def test_backward_reports_a_device_cu_seqlens_that_disagrees_with_the_host_copy():
+    """The checkpoint layout is planned from the host copy of cu_seqlens; a device copy with other
+    sequence lengths (same total) must be reported through d_status (KDA_ERR_DEVICE_ARG), with no
+    access outside the planned checkpoint slots, and the next correct call on the same context
+    must still match the oracle."""
+    inp, dy, dsf = _case("bf16", [64, 64], seed=81)
+    host = np.array([0, 64, 128], np.int32)
+    bad_dev = torch.tensor([0, 100, 128], dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kda.kda_backward(inp.q, inp.k, inp.v, inp.conv_w, inp.g, inp.beta, (bad_dev, host), dy, gate=inp.gate,
+                     rms_w=inp.rms_w, initial_state=inp.initial_state, conv_state_in=inp.conv_state_in,
+                     d_final_state=dsf, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 6  # KDA_ERR_DEVICE_ARG
+    _check(_gpu_backward(inp, dy, dsf), _oracle_backward(inp, dy, dsf))
