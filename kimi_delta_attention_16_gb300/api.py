@@ -434,3 +434,53 @@ def kda_backward_workspace_size(cu_seqlens, H: int, D: int = 128) -> int:
     if st:
         raise KDAError(st, "kda_backward_workspace_size")
     return int(n.value)
+
+
+class _KDALayer(torch.autograd.Function):
+    """kda_prefill forward, kda_backward backward (marshalling only; both run in libkda)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, conv_w, g, beta, gate, rms_w, initial_state, conv_state_in, cu_pair,
+                eps_l2, eps_rms, scale):
+        out, fin = kda_prefill(q, k, v, conv_w, g, beta, cu_pair, gate=gate, rms_w=rms_w, eps_l2=eps_l2,
+                               eps_rms=eps_rms, scale=scale, initial_state=initial_state,
+                               conv_state_in=conv_state_in)
+        ctx.save_for_backward(q, k, v, conv_w, g, beta, gate, rms_w, initial_state, conv_state_in)
+        ctx.cu_pair = cu_pair
+        ctx.hp = (eps_l2, eps_rms, scale)
+        return out, fin
+
+    @staticmethod
+    def backward(ctx, dout, dfin):
+        q, k, v, conv_w, g, beta, gate, rms_w, initial_state, conv_state_in = ctx.saved_tensors
+        eps_l2, eps_rms, scale = ctx.hp
+        if dout is None:
+            dout = torch.zeros(q.shape, dtype=q.dtype, device=q.device)
+        gr = kda_backward(q, k, v, conv_w, g, beta, ctx.cu_pair, dout.contiguous(), gate=gate, rms_w=rms_w,
+                          eps_l2=eps_l2, eps_rms=eps_rms, scale=scale, initial_state=initial_state,
+                          conv_state_in=conv_state_in,
+                          d_final_state=None if dfin is None else dfin.contiguous())
+
+        def cast(name, like):
+            if like is None or not ctx.needs_input_grad[names.index(name)]:
+                return None
+            return gr[name].to(like.dtype).view(like.shape)
+
+        names = ["dq", "dk", "dv", "dconv_w", "dg", "dbeta", "dgate", "drms_w", "dinitial_state",
+                 "dconv_state_in"]
+        ins = [q, k, v, conv_w, g, beta, gate, rms_w, initial_state, conv_state_in]
+        return (*(cast(n, t) for n, t in zip(names, ins)), None, None, None, None)
+
+
+def kda_layer(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, conv_w: torch.Tensor, g: torch.Tensor,
+              beta: torch.Tensor, cu_seqlens, *, gate: Optional[torch.Tensor] = None,
+              rms_w: Optional[torch.Tensor] = None, eps_l2: float = 1e-6, eps_rms: float = 1e-6,
+              scale: float = 1.0, initial_state: Optional[torch.Tensor] = None,
+              conv_state_in: Optional[torch.Tensor] = None):
+    """The KDA layer as a differentiable PyTorch operation: returns (out, final_state) from
+    kda_prefill, and on backward runs kda_backward (D = 128) for every input that requires a
+    gradient (q, k, v, conv_w, g, beta, gate, rms_w, initial_state, conv_state_in).  The
+    gradients are those of the exact layer in fp32, cast to each input's dtype."""
+    cu_pair = _cu_pair(cu_seqlens, q.device)
+    return _KDALayer.apply(q, k, v, conv_w, g, beta, gate, rms_w, initial_state, conv_state_in, cu_pair,
+                           float(eps_l2), float(eps_rms), float(scale))

@@ -180,3 +180,39 @@ def test_backward_reports_a_device_cu_seqlens_that_disagrees_with_the_host_copy(
     torch.cuda.synchronize()
     assert int(status.item()) == 6  # KDA_ERR_DEVICE_ARG
     _check(_gpu_backward(inp, dy, dsf), _oracle_backward(inp, dy, dsf))
+
+
+def test_autograd_layer_matches_the_oracle_gradients():
+    """kda_layer (kda_prefill forward, kda_backward backward) under torch.autograd: every input's
+    .grad equals the oracle's gradient of loss = sum(dy . out) + sum(dS_fin . final_state).
+    fp32 inputs, so the gradients are not rounded to a narrower dtype."""
+    inp, dy, dsf = _case("fp32", [50, 21], seed=91)
+    leaves = {name: getattr(inp, name).clone().requires_grad_(True)
+              for name in ("q", "k", "v", "conv_w", "g", "beta", "gate", "rms_w", "initial_state", "conv_state_in")}
+    out, fin = kda.kda_layer(leaves["q"], leaves["k"], leaves["v"], leaves["conv_w"], leaves["g"], leaves["beta"],
+                             inp.cu_seqlens, gate=leaves["gate"], rms_w=leaves["rms_w"],
+                             initial_state=leaves["initial_state"], conv_state_in=leaves["conv_state_in"])
+    loss = (out * dy).sum() + (fin * dsf).sum()
+    loss.backward()
+    torch.cuda.synchronize()
+    ref = _oracle_backward(inp, dy, dsf)
+    got = {"d" + n: to_np(t.grad).reshape(ref["d" + n].shape) for n, t in leaves.items()}
+    _check(got, ref)
+
+
+def test_autograd_layer_bf16_gradients_have_the_input_dtypes():
+    """bf16 inputs: each .grad is the fp32 gradient rounded to bf16 (within the bf16 unit roundoff
+    of the oracle's value, plus the fp32 tolerance), and inputs that do not require a gradient get
+    none."""
+    inp, dy, dsf = _case("bf16", [40], seed=93)
+    q = inp.q.clone().requires_grad_(True)
+    g = inp.g.clone().requires_grad_(True)
+    out, fin = kda.kda_layer(q, inp.k, inp.v, inp.conv_w, g, inp.beta, inp.cu_seqlens, gate=inp.gate,
+                             rms_w=inp.rms_w, initial_state=inp.initial_state, conv_state_in=inp.conv_state_in)
+    ((out.float() * dy.float()).sum() + (fin * dsf).sum()).backward()
+    torch.cuda.synchronize()
+    assert q.grad.dtype == torch.bfloat16 and g.grad.dtype == torch.float32
+    ref = _oracle_backward(inp, dy, dsf)
+    dq, rq = to_np(q.grad), ref["dq"]
+    assert np.all(np.abs(dq - rq) <= 2.0 ** -8 * np.abs(rq) + TOL_BWD * np.abs(rq).max())
+    _check({"dg": to_np(g.grad)}, ref, names=["dg"])
