@@ -416,6 +416,623 @@ k_bwd_fwd_cols(const float* __restrict__ X, const float* __restrict__ g, const f
     }
 }
 
+// ------------------------------------------------------------------------------ chunk form
+// The forward sweep and the state-gradient sweep in chunks of kCk = 16 tokens.  A chunk's products
+// run on the warp-level tensor cores (mma.sync m16n8k8 TF32): tiles of 16 tokens are below what
+// tcgen05 takes.  Each operand x is split into hi = tf32(x) and lo = x - hi, and each product takes
+// a_lo b_hi + a_hi b_lo + a_hi b_hi, close to fp32 accuracy.
+// Per chunk, with G_t the running sum of the chunk's log decays up to token t (per key channel),
+// C_t = exp(G_t), C'_t = exp(G_t - G_7) (anchored at the chunk's middle, so that no factor
+// leaves e^{+-40} for g >= -5) and B = Diag(beta):
+//   Kr_t = C_t k^_t,  Qr_t = C_t q^_t,  Kbar_t = k^_t C_last / C_t,
+//   A0_ts = (C'_t k^_t) . (k^_s / C'_s) for s < t,  M0_ts = (C'_t q^_t) . (k^_s / C'_s) for s <= t,
+//   T = (I + A0 B)^-1.
+// Forward (the decay / probe / correct / write / read steps of the chunk's tokens, unrolled):
+//   E = T (V - Kr S),  O = scale (Qr S + M0 B E),  S <- Diag(C_last) S + Kbar^T B E.
+// State gradient, D the gradient of the state after the chunk (each token's adjoint unrolled):
+//   Y = Kbar D + scale M0^T dO,  dV = T^T B Y,  W = Y - A0^T dV,
+//   D <- Diag(C_last) D + Qr^T (scale dO) - Kr^T dV.
+// Everything that does not involve the state (the factors, A0, M0, T) is formed for all chunks at
+// once by k_bwd_chunk_prep into one record per (chunk, head); the two sweeps read the records.
+constexpr int kCk = kBwdChunk;  // tokens per chunk
+static_assert(kSeg % kCk == 0, "segments start at chunk starts");
+constexpr int kChunksPerSeg = kSeg / kCk;
+constexpr int kRecKr = 0, kRecQr = kCk * kD, kRecKb = 2 * kCk * kD, kRecM0 = 3 * kCk * kD,
+              kRecA0 = kRecM0 + kCk * kCk, kRecT = kRecA0 + kCk * kCk, kRecCL = kRecT + kCk * kCk,
+              kRecBeta = kRecCL + kD, kRec = kRecBeta + kCk;
+static_assert(kRec == kBwdRecFloats && kRec % 4 == 0, "record layout");
+
+__device__ __forceinline__ uint32_t tf32_of(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+// hi = tf32(x); lo = x - hi, passed as plain fp32 bits (the tensor core reads the leading 19 bits)
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+    hi = tf32_of(x);
+    lo = __float_as_uint(x - __uint_as_float(hi));
+}
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+struct Frag4 {
+    uint32_t h[4], l[4];
+};
+struct Frag2 {
+    uint32_t h[2], l[2];
+};
+// Accumulator fragments: lane (g = lane / 4, t = lane % 4) holds (row g, cols 2t, 2t + 1) in c[0], c[1]
+// and (row g + 8, same cols) in c[2], c[3].  Such a fragment is an A operand unchanged when the k
+// index within the tile is permuted (logical k = t <-> physical col 2 t, k = t + 4 <-> 2 t + 1);
+// every B operand below is read with the same permutation.
+__device__ __forceinline__ Frag4 afrag_acc(const float (&c)[4]) {
+    Frag4 f;
+    split_tf32(c[0], f.h[0], f.l[0]);
+    split_tf32(c[2], f.h[1], f.l[1]);
+    split_tf32(c[1], f.h[2], f.l[2]);
+    split_tf32(c[3], f.h[3], f.l[3]);
+    return f;
+}
+// B operand, n = row n0 + g of a row array, k = physical columns c0 + 2 t, c0 + 2 t + 1 (one float2).
+__device__ __forceinline__ Frag2 bfrag_rows(const float* base, int stride, int n0, int c0, int g, int t) {
+    const float2 x = *reinterpret_cast<const float2*>(base + (n0 + g) * stride + c0 + 2 * t);
+    Frag2 f;
+    split_tf32(x.x, f.h[0], f.l[0]);
+    split_tf32(x.y, f.h[1], f.l[1]);
+    return f;
+}
+// B operand, n = column n0 + g of a row array, k = physical rows r0 + 2 t, r0 + 2 t + 1.
+__device__ __forceinline__ Frag2 bfrag_cols(const float* base, int stride, int r0, int n0, int g, int t) {
+    Frag2 f;
+    split_tf32(base[(r0 + 2 * t) * stride + n0 + g], f.h[0], f.l[0]);
+    split_tf32(base[(r0 + 2 * t + 1) * stride + n0 + g], f.h[1], f.l[1]);
+    return f;
+}
+// c += a b, split operands, the small terms first.
+__device__ __forceinline__ void mma3(float (&c)[4], const Frag4& a, const Frag2& b) {
+    mma_tf32(c, a.l, b.h);
+    mma_tf32(c, a.h, b.l);
+    mma_tf32(c, a.h, b.h);
+}
+// The same with the high product in `c` and the two corrections in `d` (two shorter chains).
+__device__ __forceinline__ void mma3x(float (&c)[4], float (&d)[4], const Frag4& a, const Frag2& b) {
+    mma_tf32(d, a.l, b.h);
+    mma_tf32(c, a.h, b.h);
+    mma_tf32(d, a.h, b.l);
+}
+
+// Record of chunk c of unit (n, h): slot-major, kChunksPerSeg records per checkpoint slot.
+__device__ __forceinline__ int64_t rec_index(int64_t sb, int64_t c) { return sb * kChunksPerSeg + c; }
+
+constexpr int kPs = kD + 4;  // row stride of the prep kernel's staged factor rows
+// One CTA of 128 threads (thread = key channel) per (unit, chunk); grid units x max_chunks.
+__global__ void __launch_bounds__(128)
+k_bwd_chunk_prep(const float* __restrict__ X, const float* __restrict__ g, const float* __restrict__ beta,
+                 const int32_t* __restrict__ cu, const int64_t* __restrict__ prefix, int64_t T_total, int H,
+                 int max_ch, float* __restrict__ Rec, int64_t slots) {
+    __shared__ __align__(16) float ka[kCk][kPs], qa[kCk][kPs], ki[kCk][kPs];
+    __shared__ float a0[kCk][kCk + 1], bs[kCk];
+    const int u = (int)(blockIdx.x / max_ch), c = (int)(blockIdx.x % max_ch), n = u / H, h = u % H;
+    int64_t s0, s1;
+    seq_range(cu, n, T_total, s0, s1);
+    const int64_t nch = (s1 - s0 + kCk - 1) / kCk;
+    if (c >= nch) return;
+    const int64_t sb = slot_base(prefix, n, H, h, (s1 - s0 + kSeg - 1) / kSeg, slots);
+    if (sb < 0) return;  // flagged by the forward sweep
+    float* R = Rec + rec_index(sb, c) * kRec;
+    const int i = threadIdx.x;
+    const int64_t t0 = s0 + (int64_t)c * kCk, HD = (int64_t)H * kD;
+    const int nt = (int)(s1 - t0 < kCk ? s1 - t0 : kCk);
+    float qv[kCk], kv[kCk], G[kCk];
+#pragma unroll
+    for (int t = 0; t < kCk; ++t) {
+        const bool live = t < nt;
+        const int64_t tok = t0 + t;
+        qv[t] = live ? X[tok * 3 * HD + (int64_t)h * kD + i] : 0.f;
+        kv[t] = live ? X[tok * 3 * HD + HD + (int64_t)h * kD + i] : 0.f;
+        G[t] = live ? g[(tok * H + h) * kD + i] : 0.f;
+    }
+    if (i < kCk) {
+        const float b = i < nt ? beta[(t0 + i) * H + h] : 0.f;
+        bs[i] = b;
+        R[kRecBeta + i] = b;
+    }
+#pragma unroll
+    for (int t = 1; t < kCk; ++t) G[t] += G[t - 1];
+    const float gm = G[7], gl = G[kCk - 1];
+#pragma unroll
+    for (int t = 0; t < kCk; ++t) {
+        const float ct = expf(G[t]), ca = expf(G[t] - gm);
+        R[kRecKr + t * kD + i] = ct * kv[t];
+        R[kRecQr + t * kD + i] = ct * qv[t];
+        R[kRecKb + t * kD + i] = kv[t] * expf(gl - G[t]);
+        ka[t][i] = ca * kv[t];
+        qa[t][i] = ca * qv[t];
+        ki[t][i] = kv[t] * expf(gm - G[t]);
+    }
+    R[kRecCL + i] = expf(gl);
+    __syncthreads();
+    {  // A0 (threads 0-63) and M0 (64-127): row t, columns s = sq + 4 m
+        const int mat = i >> 6, t = (i >> 2) & 15, sq = i & 3;
+        const float* xr = mat ? &qa[t][0] : &ka[t][0];
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+        for (int c4 = 0; c4 < kD; c4 += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(xr + c4);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float4 y = *reinterpret_cast<const float4*>(&ki[sq + 4 * m][c4]);
+                acc[m] = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc[m]))));
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int s = sq + 4 * m;
+            const float val = (mat ? s <= t : s < t) ? acc[m] : 0.f;
+            R[(mat ? kRecM0 : kRecA0) + t * kCk + s] = val;
+            if (!mat) a0[t][s] = val;
+        }
+    }
+    __syncthreads();
+    if (i < 32) {  // T = (I + A0 B)^-1, right-looking substitution, lane = column j
+        const int j = i & 15;
+        float ac[kCk];
+#pragma unroll
+        for (int t = 0; t < kCk; ++t) ac[t] = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < kCk; ++s2) {
+            const float ts = (s2 == j ? 1.f : 0.f) - ac[s2];
+            if (i < 16) R[kRecT + s2 * kCk + j] = ts;
+            const float bts = bs[s2] * ts;
+#pragma unroll
+            for (int t = s2 + 1; t < kCk; ++t) ac[t] = fmaf(a0[t][s2], bts, ac[t]);
+        }
+    }
+}
+
+constexpr int kChCols = 64;  // value columns per CTA of the sweeps (4 warps x 16)
+constexpr int kChCtas = kD / kChCols;
+constexpr int kFs = kD + 8;  // rows read as float2 pairs at 8 g + 2 t: no bank conflicts
+constexpr int kTs = kCk + 8; // 16-wide matrices read as float2 pairs
+constexpr int kTc = kCk + 4; // 16-wide matrices read by column
+constexpr int kChV = kChCols + 4;
+
+struct FwdStage {
+    float Kr[kCk][kFs], Qr[kCk][kFs];
+    float Kb[kCk][kPs];
+    float M0[kCk][kTs], T[kCk][kTs];
+    float CL[kD], beta[kCk];
+    float V[kCk][kChV];
+};
+constexpr int kFwdSmem = 2 * (int)sizeof(FwdStage);
+
+// Issues the copies of one chunk's record and the CTA's v columns (nt rows, `vsrc` at the chunk's
+// first token, rows vstride floats apart).
+__device__ __forceinline__ void stage_fwd(FwdStage& st, const float* R, const float* vsrc, int64_t vstride, int nt,
+                                          int tid) {
+    for (int idx = tid; idx < kCk * (kD / 4); idx += 128) {
+        const int r = idx >> 5, c4 = (idx & 31) * 4;
+        cp16(&st.Kr[r][c4], R + kRecKr + r * kD + c4);
+        cp16(&st.Qr[r][c4], R + kRecQr + r * kD + c4);
+        cp16(&st.Kb[r][c4], R + kRecKb + r * kD + c4);
+    }
+    if (tid < 64) {
+        const int r = tid >> 2, c4 = (tid & 3) * 4;
+        cp16(&st.M0[r][c4], R + kRecM0 + r * kCk + c4);
+        cp16(&st.T[r][c4], R + kRecT + r * kCk + c4);
+    } else if (tid < 96) {
+        cp16(&st.CL[(tid - 64) * 4], R + kRecCL + (tid - 64) * 4);
+    } else if (tid < 100) {
+        cp16(&st.beta[(tid - 96) * 4], R + kRecBeta + (tid - 96) * 4);
+    }
+    for (int idx = tid; idx < nt * (kChCols / 4); idx += 128) {
+        const int r = idx >> 4, c4 = (idx & 15) * 4;
+        cp16(&st.V[r][c4], vsrc + r * vstride + c4);
+    }
+}
+
+// Forward sweep in chunks: the recurrence from the initial state; o_t (times scale) and e_t of every
+// token; the state at the start of every kSeg-token segment (Sck).  One CTA of 4 warps per (unit,
+// 64 value columns); warp w keeps S^T of its 16 columns cw .. cw + 15 as the accumulator fragments
+// of 16 key tiles: s[n] = (col g, keys 8 n + 2 t, + 1), (col g + 8, same keys).
+__global__ void __launch_bounds__(128, 2)
+k_bwd_fwd_chunks(const float* __restrict__ X, const float* __restrict__ Rec, const int32_t* __restrict__ cu,
+                 const int64_t* __restrict__ prefix, int64_t T_total, int H, float scale,
+                 const float* __restrict__ S0, float* __restrict__ O, float* __restrict__ E,
+                 float* __restrict__ Sck, int64_t slots, int* __restrict__ d_status) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    FwdStage* stg = reinterpret_cast<FwdStage*>(smem_raw);
+    const int u = blockIdx.x / kChCtas, cq = blockIdx.x % kChCtas, n = u / H, h = u % H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+    const int cl = 16 * warp, cw = cq * kChCols + cl;  // the warp's first column in the CTA / the head
+    int64_t s0, s1;
+    seq_range(cu, n, T_total, s0, s1);
+    const int64_t sb = slot_base(prefix, n, H, h, (s1 - s0 + kSeg - 1) / kSeg, slots);
+    if (sb < 0) {
+        if (tid == 0) flag_status(d_status, KDA_ERR_DEVICE_ARG);
+        return;
+    }
+    const int64_t HD = (int64_t)H * kD;
+    float s[16][4];
+    if (S0) {
+        const float* S = S0 + (int64_t)u * kD * kD + cw + gq;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            const int r = 8 * nt + 2 * tq;
+            s[nt][0] = S[r * kD];
+            s[nt][1] = S[(r + 1) * kD];
+            s[nt][2] = S[r * kD + 8];
+            s[nt][3] = S[(r + 1) * kD + 8];
+        }
+    } else {
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    }
+    const int64_t nch = (s1 - s0 + kCk - 1) / kCk;
+    auto nt_of = [&](int64_t c) { return (int)(s1 - (s0 + c * kCk) < kCk ? s1 - (s0 + c * kCk) : kCk); };
+    const float* vb = X + 2 * HD + (int64_t)h * kD + cq * kChCols;
+    if (nch > 0) stage_fwd(stg[0], Rec + rec_index(sb, 0) * kRec, vb + s0 * 3 * HD, 3 * HD, nt_of(0), tid);
+    cp_commit();
+    for (int64_t c = 0; c < nch; ++c) {
+        const int nt = nt_of(c);
+        const int64_t t0 = s0 + c * kCk;
+        const FwdStage& st = stg[c & 1];
+        if (c % kChunksPerSeg == 0) {  // the state at the start of a segment
+            float* S = Sck + (sb + c / kChunksPerSeg) * kD * kD + cw + gq;
+#pragma unroll
+            for (int nt2 = 0; nt2 < 16; ++nt2) {
+                const int r = 8 * nt2 + 2 * tq;
+                S[r * kD] = s[nt2][0];
+                S[(r + 1) * kD] = s[nt2][1];
+                S[r * kD + 8] = s[nt2][2];
+                S[(r + 1) * kD + 8] = s[nt2][3];
+            }
+        }
+        cp_wait<0>();
+        __syncthreads();  // chunk c has landed; chunk c - 1's buffer is free
+        if (c + 1 < nch)
+            stage_fwd(stg[(c + 1) & 1], Rec + rec_index(sb, c + 1) * kRec, vb + (t0 + kCk) * 3 * HD, 3 * HD,
+                      nt_of(c + 1), tid);
+        cp_commit();
+        // R^T = S^T Kr^T, (Qr S)^T = S^T Qr^T; tokens as two n tiles
+        float r[2][4], rc[2][4], p[2][4], pc[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) r[j][e] = rc[j][e] = p[j][e] = pc[j][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            const Frag4 a = afrag_acc(s[kk]);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                mma3x(r[j], rc[j], a, bfrag_rows(&st.Kr[0][0], kFs, 8 * j, 8 * kk, gq, tq));
+                mma3x(p[j], pc[j], a, bfrag_rows(&st.Qr[0][0], kFs, 8 * j, 8 * kk, gq, tq));
+            }
+        }
+        // X = V - R; E = T X; Eb = B E
+        float x[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int tk = 8 * j + 2 * tq;
+            const bool l0 = tk < nt, l1 = tk + 1 < nt;
+            x[j][0] = (l0 ? st.V[tk][cl + gq] : 0.f) - (r[j][0] + rc[j][0]);
+            x[j][1] = (l1 ? st.V[tk + 1][cl + gq] : 0.f) - (r[j][1] + rc[j][1]);
+            x[j][2] = (l0 ? st.V[tk][cl + gq + 8] : 0.f) - (r[j][2] + rc[j][2]);
+            x[j][3] = (l1 ? st.V[tk + 1][cl + gq + 8] : 0.f) - (r[j][3] + rc[j][3]);
+        }
+        float e[2][4];
+        {
+            const Frag4 x0 = afrag_acc(x[0]), x1 = afrag_acc(x[1]);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) e[0][q4] = e[1][q4] = 0.f;
+            mma3(e[0], x0, bfrag_rows(&st.T[0][0], kTs, 0, 0, gq, tq));
+            mma3(e[1], x0, bfrag_rows(&st.T[0][0], kTs, 8, 0, gq, tq));
+            mma3(e[1], x1, bfrag_rows(&st.T[0][0], kTs, 8, 8, gq, tq));
+        }
+        float eb[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float2 b2 = *reinterpret_cast<const float2*>(&st.beta[8 * j + 2 * tq]);
+            eb[j][0] = b2.x * e[j][0];
+            eb[j][1] = b2.y * e[j][1];
+            eb[j][2] = b2.x * e[j][2];
+            eb[j][3] = b2.y * e[j][3];
+        }
+        const Frag4 e0 = afrag_acc(eb[0]), e1 = afrag_acc(eb[1]);
+        {  // O = scale (Qr S + M0 Eb)
+            float o[2][4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) o[j][q4] = p[j][q4] + pc[j][q4];
+            mma3(o[0], e0, bfrag_rows(&st.M0[0][0], kTs, 0, 0, gq, tq));
+            mma3(o[1], e0, bfrag_rows(&st.M0[0][0], kTs, 8, 0, gq, tq));
+            mma3(o[1], e1, bfrag_rows(&st.M0[0][0], kTs, 8, 8, gq, tq));
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int tk = 8 * j + 2 * tq;
+                if (tk < nt) {
+                    const int64_t off = ((t0 + tk) * H + h) * kD + cw + gq;
+                    O[off] = scale * o[j][0];
+                    O[off + 8] = scale * o[j][2];
+                    E[off] = e[j][0];
+                    E[off + 8] = e[j][2];
+                }
+                if (tk + 1 < nt) {
+                    const int64_t off = ((t0 + tk + 1) * H + h) * kD + cw + gq;
+                    O[off] = scale * o[j][1];
+                    O[off + 8] = scale * o[j][3];
+                    E[off] = e[j][1];
+                    E[off + 8] = e[j][3];
+                }
+            }
+        }
+        // S <- Diag(C_last) S + Kbar^T Eb
+#pragma unroll
+        for (int nt2 = 0; nt2 < 16; ++nt2) {
+            const float2 c2 = *reinterpret_cast<const float2*>(&st.CL[8 * nt2 + 2 * tq]);
+            s[nt2][0] *= c2.x;
+            s[nt2][1] *= c2.y;
+            s[nt2][2] *= c2.x;
+            s[nt2][3] *= c2.y;
+            mma3(s[nt2], e0, bfrag_cols(&st.Kb[0][0], kPs, 0, 8 * nt2, gq, tq));
+            mma3(s[nt2], e1, bfrag_cols(&st.Kb[0][0], kPs, 8, 8 * nt2, gq, tq));
+        }
+    }
+}
+
+struct BwdStage {
+    float Kb[kCk][kFs];
+    float Qr[kCk][kPs], Kr[kCk][kPs];
+    float M0[kCk][kTc], A0[kCk][kTc], T[kCk][kTc];
+    float CL[kD], beta[kCk];
+    float dO[kCk][kChV], E[kCk][kChV];
+};
+constexpr int kBwdSmem = 2 * (int)sizeof(BwdStage);
+
+__device__ __forceinline__ void stage_bwd(BwdStage& st, const float* R, const float* dosrc, const float* esrc,
+                                          int64_t stride, int nt, int tid) {
+    for (int idx = tid; idx < kCk * (kD / 4); idx += 128) {
+        const int r = idx >> 5, c4 = (idx & 31) * 4;
+        cp16(&st.Kb[r][c4], R + kRecKb + r * kD + c4);
+        cp16(&st.Qr[r][c4], R + kRecQr + r * kD + c4);
+        cp16(&st.Kr[r][c4], R + kRecKr + r * kD + c4);
+    }
+    if (tid < 64) {
+        const int r = tid >> 2, c4 = (tid & 3) * 4;
+        cp16(&st.M0[r][c4], R + kRecM0 + r * kCk + c4);
+        cp16(&st.A0[r][c4], R + kRecA0 + r * kCk + c4);
+        cp16(&st.T[r][c4], R + kRecT + r * kCk + c4);
+    } else if (tid < 96) {
+        cp16(&st.CL[(tid - 64) * 4], R + kRecCL + (tid - 64) * 4);
+    } else if (tid < 100) {
+        cp16(&st.beta[(tid - 96) * 4], R + kRecBeta + (tid - 96) * 4);
+    }
+    for (int idx = tid; idx < nt * (kChCols / 4); idx += 128) {
+        const int r = idx >> 4, c4 = (idx & 15) * 4;
+        cp16(&st.dO[r][c4], dosrc + r * stride + c4);
+        cp16(&st.E[r][c4], esrc + r * stride + c4);
+    }
+}
+
+// State-gradient sweep in chunks, last chunk first: w_t = dS'^T k^_t, dv = beta w, the sums
+// dbeta = w . e and e . do of every token (atomics over the CTAs of a unit), the state gradient at
+// the end of every segment (dSck: before that token's own terms) and at the start (dS0).  Layout as
+// in k_bwd_fwd_chunks, with D = dS in place of S.
+__global__ void __launch_bounds__(128, 2)
+k_bwd_bwd_chunks(const float* __restrict__ Rec, const float* __restrict__ dO, const float* __restrict__ E,
+                 const int32_t* __restrict__ cu, const int64_t* __restrict__ prefix, int64_t T_total, int H,
+                 float scale, const float* __restrict__ dS_fin, float* __restrict__ W, float* __restrict__ dX,
+                 float* __restrict__ dbeta, float* __restrict__ edo, float* __restrict__ dSck,
+                 float* __restrict__ dS0, int64_t slots) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    BwdStage* stg = reinterpret_cast<BwdStage*>(smem_raw);
+    __shared__ float acc[2][2][kCk];  // [chunk parity][dbeta, e.do][token]
+    const int u = blockIdx.x / kChCtas, cq = blockIdx.x % kChCtas, n = u / H, h = u % H;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+    const int cl = 16 * warp, cw = cq * kChCols + cl;
+    if (tid < 4 * kCk) (&acc[0][0][0])[tid] = 0.f;
+    int64_t s0, s1;
+    seq_range(cu, n, T_total, s0, s1);
+    const int64_t sb = slot_base(prefix, n, H, h, (s1 - s0 + kSeg - 1) / kSeg, slots);
+    if (sb < 0) return;  // flagged by the forward sweep
+    const int64_t HD = (int64_t)H * kD;
+    float d[16][4];
+    if (dS_fin) {
+        const float* S = dS_fin + (int64_t)u * kD * kD + cw + gq;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            const int r = 8 * nt + 2 * tq;
+            d[nt][0] = S[r * kD];
+            d[nt][1] = S[(r + 1) * kD];
+            d[nt][2] = S[r * kD + 8];
+            d[nt][3] = S[(r + 1) * kD + 8];
+        }
+    } else {
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+    }
+    const int64_t nch = (s1 - s0 + kCk - 1) / kCk;
+    auto nt_of = [&](int64_t c) { return (int)(s1 - (s0 + c * kCk) < kCk ? s1 - (s0 + c * kCk) : kCk); };
+    const int64_t coff = (int64_t)h * kD + cq * kChCols;
+    auto stage = [&](int64_t c) {
+        const int64_t t0 = s0 + c * kCk;
+        stage_bwd(stg[c & 1], Rec + rec_index(sb, c) * kRec, dO + t0 * HD + coff, E + t0 * HD + coff, HD,
+                  nt_of(c), tid);
+    };
+    if (nch > 0) stage(nch - 1);
+    cp_commit();
+    for (int64_t c = nch - 1; c >= 0; --c) {
+        const int nt = nt_of(c);
+        const int64_t t0 = s0 + c * kCk;
+        const BwdStage& st = stg[c & 1];
+        if (c % kChunksPerSeg == kChunksPerSeg - 1 || c == nch - 1) {  // the chunk ends a segment
+            float* S = dSck + (sb + c / kChunksPerSeg) * kD * kD + cw + gq;
+#pragma unroll
+            for (int nt2 = 0; nt2 < 16; ++nt2) {
+                const int r = 8 * nt2 + 2 * tq;
+                S[r * kD] = d[nt2][0];
+                S[(r + 1) * kD] = d[nt2][1];
+                S[r * kD + 8] = d[nt2][2];
+                S[(r + 1) * kD + 8] = d[nt2][3];
+            }
+        }
+        cp_wait<0>();
+        __syncthreads();  // chunk c has landed; chunk c + 1's buffer and sums are complete
+        if (c + 1 < nch && tid < nt_of(c + 1)) {
+            const int p = (int)((c + 1) & 1);
+            const int64_t t = s0 + (c + 1) * kCk + tid;
+            atomicAdd(dbeta + t * H + h, acc[p][0][tid]);
+            atomicAdd(edo + t * H + h, acc[p][1][tid]);
+            acc[p][0][tid] = 0.f;
+            acc[p][1][tid] = 0.f;
+        }
+        if (c > 0) stage(c - 1);
+        cp_commit();
+        // Y^T = D^T Kbar^T + scale dO^T M0 (tokens as two n tiles)
+        float y[2][4], yc[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) y[j][e] = yc[j][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+            const Frag4 a = afrag_acc(d[kk]);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) mma3x(y[j], yc[j], a, bfrag_rows(&st.Kb[0][0], kFs, 8 * j, 8 * kk, gq, tq));
+        }
+        Frag4 sdo[2];  // scale dO^T as A operands (k = tokens 8 kj ..), rows past the sequence zero
+#pragma unroll
+        for (int kj = 0; kj < 2; ++kj) {
+            const int tk = 8 * kj + 2 * tq;
+            const bool l0 = tk < nt, l1 = tk + 1 < nt;
+            const float v[4] = {l0 ? scale * st.dO[tk][cl + gq] : 0.f, l1 ? scale * st.dO[tk + 1][cl + gq] : 0.f,
+                                l0 ? scale * st.dO[tk][cl + gq + 8] : 0.f,
+                                l1 ? scale * st.dO[tk + 1][cl + gq + 8] : 0.f};
+            sdo[kj] = afrag_acc(v);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) y[j][e] += yc[j][e];
+        mma3(y[0], sdo[0], bfrag_cols(&st.M0[0][0], kTc, 0, 0, gq, tq));
+        mma3(y[0], sdo[1], bfrag_cols(&st.M0[0][0], kTc, 8, 0, gq, tq));
+        mma3(y[1], sdo[1], bfrag_cols(&st.M0[0][0], kTc, 8, 8, gq, tq));
+        // dV^T = (B Y)^T T, W^T = Y^T - dV^T A0
+        float dv[2][4], w[2][4];
+        {
+            float yb[2][4];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float2 b2 = *reinterpret_cast<const float2*>(&st.beta[8 * j + 2 * tq]);
+                yb[j][0] = b2.x * y[j][0];
+                yb[j][1] = b2.y * y[j][1];
+                yb[j][2] = b2.x * y[j][2];
+                yb[j][3] = b2.y * y[j][3];
+            }
+            const Frag4 y0 = afrag_acc(yb[0]), y1 = afrag_acc(yb[1]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dv[0][e] = dv[1][e] = 0.f;
+            mma3(dv[0], y0, bfrag_cols(&st.T[0][0], kTc, 0, 0, gq, tq));
+            mma3(dv[0], y1, bfrag_cols(&st.T[0][0], kTc, 8, 0, gq, tq));
+            mma3(dv[1], y1, bfrag_cols(&st.T[0][0], kTc, 8, 8, gq, tq));
+        }
+        Frag4 ndv[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float nv[4] = {-dv[j][0], -dv[j][1], -dv[j][2], -dv[j][3]};
+            ndv[j] = afrag_acc(nv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[j][e] = y[j][e];
+        }
+        mma3(w[0], ndv[0], bfrag_cols(&st.A0[0][0], kTc, 0, 0, gq, tq));
+        mma3(w[0], ndv[1], bfrag_cols(&st.A0[0][0], kTc, 8, 0, gq, tq));
+        mma3(w[1], ndv[1], bfrag_cols(&st.A0[0][0], kTc, 8, 8, gq, tq));
+        // stores and the per-token sums w . e, e . do over the warp's 16 columns
+        {
+            float pb[2][2], pe[2][2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int hlf = 0; hlf < 2; ++hlf) {
+                    const int tk = 8 * j + 2 * tq + hlf;
+                    pb[j][hlf] = pe[j][hlf] = 0.f;
+                    if (tk < nt) {
+                        const float e0 = st.E[tk][cl + gq], e1 = st.E[tk][cl + gq + 8];
+                        const float o0 = st.dO[tk][cl + gq], o1 = st.dO[tk][cl + gq + 8];
+                        const float w0 = w[j][hlf], w1 = w[j][2 + hlf];
+                        pb[j][hlf] = w0 * e0 + w1 * e1;
+                        pe[j][hlf] = e0 * o0 + e1 * o1;
+                        const int64_t t = t0 + tk;
+                        const int64_t off = (t * H + h) * kD + cw + gq;
+                        W[off] = w0;
+                        W[off + 8] = w1;
+                        float* dv_row = dX + t * 3 * HD + 2 * HD + (int64_t)h * kD + cw + gq;
+                        dv_row[0] = dv[j][hlf];
+                        dv_row[8] = dv[j][2 + hlf];
+                    }
+                }
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int hlf = 0; hlf < 2; ++hlf)
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        pb[j][hlf] += __shfl_xor_sync(0xffffffffu, pb[j][hlf], off);
+                        pe[j][hlf] += __shfl_xor_sync(0xffffffffu, pe[j][hlf], off);
+                    }
+            if (gq == 0) {
+                const int p = (int)(c & 1);
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int hlf = 0; hlf < 2; ++hlf) {
+                        const int tk = 8 * j + 2 * tq + hlf;
+                        if (tk < nt) {
+                            atomicAdd(&acc[p][0][tk], pb[j][hlf]);
+                            atomicAdd(&acc[p][1][tk], pe[j][hlf]);
+                        }
+                    }
+            }
+        }
+        // D <- Diag(C_last) D + Qr^T (scale dO) - Kr^T dV
+#pragma unroll
+        for (int nt2 = 0; nt2 < 16; ++nt2) {
+            const float2 c2 = *reinterpret_cast<const float2*>(&st.CL[8 * nt2 + 2 * tq]);
+            d[nt2][0] *= c2.x;
+            d[nt2][1] *= c2.y;
+            d[nt2][2] *= c2.x;
+            d[nt2][3] *= c2.y;
+#pragma unroll
+            for (int kj = 0; kj < 2; ++kj) {
+                mma3(d[nt2], sdo[kj], bfrag_cols(&st.Qr[0][0], kPs, 8 * kj, 8 * nt2, gq, tq));
+                mma3(d[nt2], ndv[kj], bfrag_cols(&st.Kr[0][0], kPs, 8 * kj, 8 * nt2, gq, tq));
+            }
+        }
+    }
+    __syncthreads();
+    if (nch > 0 && tid < nt_of(0)) {
+        const int64_t t = s0 + tid;
+        atomicAdd(dbeta + t * H + h, acc[0][0][tid]);
+        atomicAdd(edo + t * H + h, acc[0][1][tid]);
+    }
+    if (dS0) {
+        float* S = dS0 + (int64_t)u * kD * kD + cw + gq;
+#pragma unroll
+        for (int nt2 = 0; nt2 < 16; ++nt2) {
+            const int r = 8 * nt2 + 2 * tq;
+            S[r * kD] = d[nt2][0];
+            S[(r + 1) * kD] = d[nt2][1];
+            S[r * kD + 8] = d[nt2][2];
+            S[(r + 1) * kD + 8] = d[nt2][3];
+        }
+    }
+}
+
 // dS <- Diag(alpha) (dS - beta k w^T) with the factors of a staged token and nbw = -beta w of the
 // lane's columns.
 __device__ __forceinline__ void bwd_decay(float (&ds)[8][4], const float (&a2)[8], const float (&k2)[8],
@@ -1110,9 +1727,18 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
         (e = cudaFuncSetAttribute(k_bwd_bwd_cols, cudaFuncAttributeMaxDynamicSharedMemorySize, kColSmem)) ||
         (e = cudaFuncSetAttribute(k_bwd_rows, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmem)))
         return e;
-    const unsigned cg = (unsigned)(units * kColCtas);
-    k_bwd_fwd_cols<<<cg, 128, kColSmem, s>>>(X, a.g, a.beta, a.cu_seqlens, prefix, T, a.H, a.scale,
-                                             a.initial_state, O, E, Sck, L.slots, a.d_status);
+    float* Rec = reinterpret_cast<float*>(ws + L.rec);
+    if (rows > 0 && L.max_ch > 0) {
+        k_bwd_chunk_prep<<<(unsigned)(units * L.max_ch), 128, 0, s>>>(X, a.g, a.beta, a.cu_seqlens, prefix, T, a.H,
+                                                                       (int)L.max_ch, Rec, L.slots);
+        if ((e = cudaGetLastError())) return e;
+    }
+    if ((e = cudaFuncSetAttribute(k_bwd_fwd_chunks, cudaFuncAttributeMaxDynamicSharedMemorySize, kFwdSmem)) ||
+        (e = cudaFuncSetAttribute(k_bwd_bwd_chunks, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmem)))
+        return e;
+    k_bwd_fwd_chunks<<<(unsigned)(units * kChCtas), 128, kFwdSmem, s>>>(X, Rec, a.cu_seqlens, prefix, T, a.H, a.scale,
+                                                                        a.initial_state, O, E, Sck, L.slots,
+                                                                        a.d_status);
     if ((e = cudaGetLastError())) return e;
     if (rows > 0) {
         if (a.out_dtype == KDA_FP32)
@@ -1123,9 +1749,9 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
                                                           rows, b.dgate, b.drms_w);
         if ((e = cudaGetLastError())) return e;
     }
-    k_bwd_bwd_cols<<<cg, 128, kColSmem, s>>>(X, a.g, a.beta, O, E, a.cu_seqlens, prefix, T, a.H, a.scale,
-                                             b.d_final_state, W, dX, b.dbeta, edo, dSck, b.dinitial_state,
-                                             L.slots);
+    k_bwd_bwd_chunks<<<(unsigned)(units * kChCtas), 128, kBwdSmem, s>>>(Rec, O, E, a.cu_seqlens, prefix, T, a.H,
+                                                                        a.scale, b.d_final_state, W, dX, b.dbeta,
+                                                                        edo, dSck, b.dinitial_state, L.slots);
     if ((e = cudaGetLastError())) return e;
     if (rows == 0) return cudaSuccess;
     k_bwd_rows<<<(unsigned)(units * L.max_seg), kRowThreads, kRowSmem, s>>>(
@@ -1152,12 +1778,14 @@ BackwardLayout backward_layout(const kda_backward_args& b) {
     const kda_prefill_args& a = b.fwd;
     BackwardLayout L{};
     const size_t T = (size_t)(a.T_total > 0 ? a.T_total : 0), H = (size_t)a.H, HD = H * kD;
-    size_t segs = 0, max_seg = 0;
+    size_t segs = 0, max_seg = 0, max_ch = 0;
     if (a.cu_seqlens_host)
         for (int n = 0; n < a.N; ++n) {
             const size_t ns = (size_t)(a.cu_seqlens_host[n + 1] - a.cu_seqlens_host[n] + kSeg - 1) / kSeg;
             segs += ns;
             max_seg = ns > max_seg ? ns : max_seg;
+            const size_t nc = (size_t)(a.cu_seqlens_host[n + 1] - a.cu_seqlens_host[n] + kBwdChunk - 1) / kBwdChunk;
+            max_ch = nc > max_ch ? nc : max_ch;
         }
     const size_t N = (size_t)(a.N > 0 ? a.N : 0);
     size_t off = 0;
@@ -1175,10 +1803,12 @@ BackwardLayout backward_layout(const kda_backward_args& b) {
     L.edo = take(T * H * 4);
     L.slots = (int64_t)(segs * H);
     L.max_seg = (int64_t)max_seg;
+    L.max_ch = (int64_t)max_ch;
     L.sck = take(segs * H * kD * kD * 4);
     L.dsck = take(segs * H * kD * kD * 4);
     L.segtot = take(segs * H * kD * 4);
     L.segown = take(segs * H * kD * 4);
+    L.rec = take(segs * H * kBwdSeg / kBwdChunk * kBwdRecFloats * 4);
     L.fin = take(N * H * kD * 4);
     L.prefix = take((N + 1) * 8);
     L.total = off;

@@ -231,11 +231,17 @@ struct BackwardLayout {
     size_t segown;   // [slots][D] fp32: the read part of each segment's dg sum
     size_t fin;      // [N][H][D] fp32: rowsum(dS_T . S_T)
     size_t prefix;   // [N + 1] int64: segments before each sequence
+    size_t rec;      // [slots][kBwdSeg / kBwdChunk][kBwdRecFloats] fp32: the chunk records
     int64_t slots;   // checkpoint slots: H times the sum over sequences of ceil(len / kBwdSeg)
     int64_t max_seg; // the largest segment count of one sequence
+    int64_t max_ch;  // the largest chunk count of one sequence
     size_t total;
 };
 constexpr int kBwdSeg = 64;  // tokens per checkpointed segment of the backward pass
+constexpr int kBwdChunk = 16;  // tokens per chunk of the backward's sweeps
+// floats of one chunk record: Kr, Qr, Kbar (16 x 128 each), M0, A0, T (16 x 16 each), C_last (128),
+// beta (16)
+constexpr int kBwdRecFloats = 3 * kBwdChunk * 128 + 3 * kBwdChunk * kBwdChunk + 128 + kBwdChunk;
 BackwardLayout backward_layout(const kda_backward_args& b);  // needs fwd.cu_seqlens_host
 cudaError_t launch_backward(const kda_backward_args& b, const BackwardLayout& L, char* ws, cudaStream_t s);
 
