@@ -1,6 +1,7 @@
 // kda_backward.cu -- the backward pass of the KDA layer (training): reverse-mode
 // derivatives of sum(dy . out) + sum(dS . final_state) with respect to every
-// input of kda_prefill, D = 128, fp32 arithmetic (IEEE exp, SiLU, sigmoid).
+// input of kda_prefill, D = 128, fp32 arithmetic (IEEE exp, SiLU, sigmoid; the
+// chunk products on the tensor cores as TF32 hi/lo splits, close to fp32).
 //
 // Page "Kimi K3 / Architecture", KDA panel (the layer: short conv + SiLU, L2
 // norms of q and k, the recurrent state decayed, corrected and written per
@@ -13,12 +14,13 @@
 // Per (sequence, head) unit, with P_t = Diag(alpha_t) S_{t-1}, e_t = v_t - P_t^T k_t,
 // S_t = P_t + beta_t k_t e_t^T, o_t = scale S_t^T q_t:
 //   prep      conv + SiLU + L2 norms: q^, k^, v (fp32) and |a_q|, |a_k|      (warp per token-head)
-//   forward   the recurrence in column layout (each value column of S evolves on its own):
-//             o_t, e_t, and S at the start of every kSeg-token segment          (4 CTAs per unit)
+//   records   per 16-token chunk, all in parallel: decayed keys and queries, the chunk's
+//             triangular products and (I + A)^-1 (see "chunk form")          (CTA per chunk-head)
+//   forward   the recurrence chunk by chunk: o_t, e_t, and S at the start of every
+//             kSeg-token segment                                              (2 CTAs per unit)
 //   epilogue  y = n w sig(z), n = o r:  do = r dn - r^3 o (dn . o) / D, dgate, drms_w  (warp per row)
-//   backward  the state gradient in column layout, tokens in reverse (each column of dS evolves
-//             on its own): w_t = dS'^T k, dv = beta w, dbeta = w . e, e . do, and dS at the end
-//             of every segment                                                  (4 CTAs per unit)
+//   backward  the state gradient chunk by chunk, last chunk first: w_t = dS'^T k, dv = beta w,
+//             dbeta = w . e, e . do, and dS at the end of every segment        (2 CTAs per unit)
 //   rows      per (unit, segment), all in parallel, row layout (with e, w and do known, each row
 //             of S and of dS evolves on its own): dq, dk and dg (see k_bwd_rows)
 //   carry     dg's sums over later segments and the final-state term
@@ -34,10 +36,6 @@ namespace {
 constexpr int kD = 128;
 constexpr int kSeg = kBwdSeg;  // tokens per checkpointed segment
 
-__device__ __forceinline__ float4 f4_fma(float a, float4 x, float4 y) {
-    return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
-}
-__device__ __forceinline__ float4 f4_mul(float a, float4 x) { return make_float4(a * x.x, a * x.y, a * x.z, a * x.w); }
 __device__ __forceinline__ float4 f4_add(float4 x, float4 y) { return make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w); }
 __device__ __forceinline__ float dot4(float4 x, float4 y) { return x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w; }
 __device__ __forceinline__ float warp_sum(float v) {
@@ -181,238 +179,6 @@ __global__ void k_bwd_seg_prefix(const int32_t* __restrict__ cu, int N, int64_t 
         int64_t s0, s1;
         seq_range(cu, n, T_total, s0, s1);
         run += (s1 - s0 + kSeg - 1) / kSeg;
-    }
-}
-
-// ------------------------------------------------------------------------------ column-layout sweeps
-// One unit's state is split by value column over kColCtas CTAs of 4 warps (32 columns each).
-// Lane l of warp w owns rows 8 r .. 8 r + 7 (r = l & 15) of the four columns
-// c0 = 32 cq + 8 w + 4 (l >> 4) .. c0 + 3.  A
-// per-column quantity of a token (e, o, w = dS^T k) is a sum over the rows of its column: the
-// sixteen lanes of a column group.  Every (unit, column group) is an independent chain, and the
-// CTAs of all units stay resident together (ten warps per SM at 96 units).  Each token is one pass over the state: the forward sweep
-// finishes token t's update, accumulates o_t and the next token's S^T (alpha k) together; the
-// backward sweep applies the later token's decay and correction, adds token t's readout gradient
-// and accumulates w_t together.  No CTA barrier inside a token; tokens are staged kTB at a time
-// (double-buffered cp.async), three barriers per block.
-constexpr int kColCtas = 4;           // CTAs per unit
-constexpr int kCols = kD / kColCtas;  // 32 columns per CTA
-constexpr int kTB = 8;                // tokens per staged block
-constexpr int kSlice = 12;            // floats between the 8-row slices of a staged 128-vector
-constexpr int kPerm = 16 * kSlice;
-__device__ __forceinline__ int perm_off(int row) { return (row >> 3) * kSlice + (row & 7); }
-
-// One staged token: k^, exp(g), q^, exp(g) k^ (8-row slices 12 floats apart, so that the eight
-// slices a quarter-warp reads at once fall in distinct banks), two slices of the CTA's columns, beta.
-struct ColTok {
-    float k[kPerm], a[kPerm], q[kPerm], ak[kPerm];
-    float c0[kCols], c1[kCols];  // forward sweep: v; backward sweep: do and e
-    float beta, pad[3];
-};
-constexpr int kColSmem = 2 * kTB * (int)sizeof(ColTok);
-
-struct ColSrc {
-    const float* p;  // element (token 0, head 0, channel 0)
-    int64_t stride;  // elements between tokens
-};
-
-// Issues the copies of tokens [t0, t0 + nt) of head h into st[0 .. nt): the three row vectors
-// (q^ and k^ from X, g into the alpha slot), `ncs` column slices (the CTA's columns), beta.
-__device__ __forceinline__ void stage_cols(ColTok* st, int64_t t0, int nt, const float* X, const float* g,
-                                           const float* beta, ColSrc s0, ColSrc s1, int ncs, int H, int h,
-                                           int cq, int tid) {
-    constexpr int kCC = kCols / 4;  // 16-byte chunks of one column slice
-    const int64_t HD = (int64_t)H * kD;
-    const int per = 96 + kCC * ncs + 1;
-    for (int idx = tid; idx < nt * per; idx += 128) {
-        const int tk = idx / per, j = idx - tk * per;
-        const int64_t t = t0 + tk;
-        ColTok& s = st[tk];
-        if (j < 96) {
-            const int part = j >> 5, jj = j & 31;
-            const float* src = part == 0 ? X + t * 3 * HD + HD + (int64_t)h * kD
-                             : part == 1 ? g + (t * H + h) * kD
-                                         : X + t * 3 * HD + (int64_t)h * kD;
-            float* dst = part == 0 ? s.k : part == 1 ? s.a : s.q;
-            cp16(dst + (jj >> 1) * kSlice + (jj & 1) * 4, src + jj * 4);
-        } else if (j < 96 + kCC * ncs) {
-            const int jj = j - 96, which = jj / kCC, ch = jj - which * kCC;
-            const ColSrc& cs = which == 0 ? s0 : s1;
-            cp16((which == 0 ? s.c0 : s.c1) + ch * 4, cs.p + t * cs.stride + (int64_t)h * kD + cq * kCols + ch * 4);
-        } else {
-            cp4(&s.beta, beta + t * H + h);
-        }
-    }
-}
-
-// alpha = exp(g) in place and alpha k for the staged tokens (after the copies have landed and a
-// barrier).
-__device__ __forceinline__ void stage_exp_cols(ColTok* st, int nt, int tid) {
-    for (int idx = tid; idx < nt * kD; idx += 128) {
-        ColTok& s = st[idx >> 7];
-        const int o = perm_off(idx & 127);
-        const float a = expf(s.a[o]);
-        s.a[o] = a;
-        s.ak[o] = a * s.k[o];
-    }
-}
-
-// The 8 rows of a lane's slice of a staged vector.
-__device__ __forceinline__ void load_rows(const float* p, float (&x)[8]) {
-    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-// Four column sums over the sixteen lanes of a column group (lane bits 0..3), every lane gets all
-// four.
-__device__ __forceinline__ void sum16x4(float (&x)[4]) {
-#pragma unroll
-    for (int off = 1; off < 16; off <<= 1)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) x[j] += __shfl_xor_sync(0xffffffffu, x[j], off);
-}
-// Four column sums over the sixteen lanes of a column group; afterwards lanes 4 j .. 4 j + 3 of the
-// group (r = lane & 15) hold the total of value j.
-__device__ __forceinline__ float sum16x4_split(float (&x)[4], int r) {
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const bool up = (r & 8) != 0;
-        const float send = up ? x[i] : x[i + 2];
-        x[i] = (up ? x[i + 2] : x[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-    {
-        const bool up = (r & 4) != 0;
-        const float send = up ? x[0] : x[1];
-        x[0] = (up ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
-    }
-    x[0] += __shfl_xor_sync(0xffffffffu, x[0], 2);
-    return x[0] + __shfl_xor_sync(0xffffffffu, x[0], 1);
-}
-// The four values of sum16x4_split gathered on lane r = 0 of each column group.
-__device__ __forceinline__ float4 gather4(float v, int lane) {
-    const int base = lane & ~15;
-    const float v1 = __shfl_sync(0xffffffffu, v, base + 4), v2 = __shfl_sync(0xffffffffu, v, base + 8),
-                v3 = __shfl_sync(0xffffffffu, v, base + 12);
-    return make_float4(v, v1, v2, v3);
-}
-
-// The state slice of a lane (rows 8 r .. 8 r + 7 of columns c0 .. c0 + 3) to / from a row-major
-// D x D matrix.
-__device__ __forceinline__ void load_slice(const float* M, int r, int c0, float (&s)[8][4]) {
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        const float4 a = *reinterpret_cast<const float4*>(M + (8 * r + m) * kD + c0);
-        s[m][0] = a.x;
-        s[m][1] = a.y;
-        s[m][2] = a.z;
-        s[m][3] = a.w;
-    }
-}
-__device__ __forceinline__ void store_slice(float* M, int r, int c0, const float (&s)[8][4]) {
-#pragma unroll
-    for (int m = 0; m < 8; ++m)
-        *reinterpret_cast<float4*>(M + (8 * r + m) * kD + c0) = make_float4(s[m][0], s[m][1], s[m][2], s[m][3]);
-}
-
-// Forward sweep: the recurrence from the initial state; o_t and e_t of every token; the state at
-// the start of every kSeg-token segment (Sck).  Grid: units x kColCtas CTAs of 128 threads.
-__global__ void __launch_bounds__(128)
-k_bwd_fwd_cols(const float* __restrict__ X, const float* __restrict__ g, const float* __restrict__ beta,
-               const int32_t* __restrict__ cu, const int64_t* __restrict__ prefix, int64_t T_total, int H,
-               float scale, const float* __restrict__ S0, float* __restrict__ O, float* __restrict__ E,
-               float* __restrict__ Sck, int64_t slots, int* __restrict__ d_status) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    ColTok* buf = reinterpret_cast<ColTok*>(smem_raw);  // [2][kTB]
-    const int u = blockIdx.x / kColCtas, cq = blockIdx.x % kColCtas, n = u / H, h = u % H;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane & 15;
-    const int cl = warp * 8 + 4 * (lane >> 4), c0 = cq * kCols + cl;
-    int64_t s0, s1;
-    seq_range(cu, n, T_total, s0, s1);
-    const int64_t nseg = (s1 - s0 + kSeg - 1) / kSeg;
-    const int64_t sb = slot_base(prefix, n, H, h, nseg, slots);
-    if (sb < 0) {
-        if (tid == 0) flag_status(d_status, KDA_ERR_DEVICE_ARG);
-        return;
-    }
-    const int64_t HD = (int64_t)H * kD;
-    const ColSrc vs{X + 2 * HD, 3 * HD};
-    float s[8][4];
-    if (S0) {
-        load_slice(S0 + (int64_t)u * kD * kD, r, c0, s);
-    } else {
-#pragma unroll
-        for (int m = 0; m < 8; ++m)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) s[m][c] = 0.f;
-    }
-    const int64_t nblk = (s1 - s0 + kTB - 1) / kTB;
-    auto nt_of = [&](int64_t b) { return (int)(s1 - (s0 + b * kTB) < kTB ? s1 - (s0 + b * kTB) : kTB); };
-    if (nblk > 0) stage_cols(buf, s0, nt_of(0), X, g, beta, vs, vs, 1, H, h, cq, tid);
-    cp_commit();
-    for (int64_t b = 0; b < nblk; ++b) {
-        __syncthreads();  // block b - 1 is consumed: its buffer takes block b + 1
-        if (b + 1 < nblk)
-            stage_cols(buf + ((b + 1) & 1) * kTB, s0 + (b + 1) * kTB, nt_of(b + 1), X, g, beta, vs, vs, 1, H, h,
-                       cq, tid);
-        cp_commit();
-        cp_wait<1>();
-        __syncthreads();
-        ColTok* st = buf + (b & 1) * kTB;
-        const int nt = nt_of(b);
-        stage_exp_cols(st, nt, tid);
-        __syncthreads();
-        float x[4];  // (P_t^T k_t) of the lane's columns: alpha_t k_t against S_{t-1}
-        {
-            float ak[8];
-            load_rows(st[0].ak + r * kSlice, ak);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-                for (int m = 0; m < 8; m += 2) {
-                    a0 = fmaf(ak[m], s[m][c], a0);
-                    a1 = fmaf(ak[m + 1], s[m + 1][c], a1);
-                }
-                x[c] = a0 + a1;
-            }
-            sum16x4(x);
-        }
-        static_assert(kSeg % kTB == 0, "segments start at block starts");
-        if ((b * kTB) % kSeg == 0) store_slice(Sck + (sb + b * kTB / kSeg) * kD * kD, r, c0, s);
-        for (int tk = 0; tk < nt; ++tk) {
-            const int64_t t = s0 + b * kTB + tk;
-            const ColTok& T = st[tk];
-            const ColTok& Nx = st[tk + 1 < nt ? tk + 1 : tk];
-            const float4 v4 = *reinterpret_cast<const float4*>(T.c0 + cl);
-            const float bt = T.beta;
-            const float e[4] = {v4.x - x[0], v4.y - x[1], v4.z - x[2], v4.w - x[3]};
-            const float be[4] = {bt * e[0], bt * e[1], bt * e[2], bt * e[3]};
-            float a2[8], k2[8], q2[8], n2[8];
-            load_rows(T.a + r * kSlice, a2);
-            load_rows(T.k + r * kSlice, k2);
-            load_rows(T.q + r * kSlice, q2);
-            load_rows(Nx.ak + r * kSlice, n2);
-            float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            float p[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-            for (int m = 0; m < 8; ++m)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    s[m][c] = fmaf(a2[m], s[m][c], k2[m] * be[c]);  // S_t = Diag(alpha) S_{t-1} + beta k e^T
-                    o[m & 1][c] = fmaf(q2[m], s[m][c], o[m & 1][c]);
-                    p[m & 1][c] = fmaf(n2[m], s[m][c], p[m & 1][c]);
-                }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) x[c] = p[0][c] + p[1][c];  // unused after a block's last token
-            sum16x4(x);
-            float y[4] = {o[0][0] + o[1][0], o[0][1] + o[1][1], o[0][2] + o[1][2], o[0][3] + o[1][3]};
-            const float4 o4 = gather4(sum16x4_split(y, r), lane);
-            if (r == 0) {
-                *reinterpret_cast<float4*>(O + (t * H + h) * kD + c0) =
-                    make_float4(scale * o4.x, scale * o4.y, scale * o4.z, scale * o4.w);
-                *reinterpret_cast<float4*>(E + (t * H + h) * kD + c0) = make_float4(e[0], e[1], e[2], e[3]);
-            }
-        }
     }
 }
 
@@ -1033,164 +799,6 @@ k_bwd_bwd_chunks(const float* __restrict__ Rec, const float* __restrict__ dO, co
     }
 }
 
-// dS <- Diag(alpha) (dS - beta k w^T) with the factors of a staged token and nbw = -beta w of the
-// lane's columns.
-__device__ __forceinline__ void bwd_decay(float (&ds)[8][4], const float (&a2)[8], const float (&k2)[8],
-                                          const float (&nbw)[4]) {
-#pragma unroll
-    for (int m = 0; m < 8; ++m)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) ds[m][c] = a2[m] * fmaf(k2[m], nbw[c], ds[m][c]);
-}
-
-// One token of the backward sweep: dS' = [pending: Diag(alpha') (dS - beta' k' w'^T)] + scale q do^T
-// with (alpha', k', -beta' w') of the later token, w = dS'^T k summed over the column group (all
-// lanes get it); the stores and the dbeta / e.do partials of the token.
-template <bool kPending>
-__device__ __forceinline__ void bwd_token(float (&ds)[8][4], float (&nbw)[4], const ColTok& T, const ColTok& Pv,
-                                          int r, int cl, int c0, int lane, float scale, int64_t t, int H, int h,
-                                          float* W, float* dX, float* accb, float* acce) {
-    const int64_t HD = (int64_t)H * kD;
-    const float4 do4 = *reinterpret_cast<const float4*>(T.c0 + cl);
-    const float4 e4 = *reinterpret_cast<const float4*>(T.c1 + cl);
-    const float bt = T.beta;
-    const float sd[4] = {scale * do4.x, scale * do4.y, scale * do4.z, scale * do4.w};
-    float k2[8], q2[8];
-    load_rows(T.k + r * kSlice, k2);
-    load_rows(T.q + r * kSlice, q2);
-    float wp[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    if constexpr (kPending) {
-        float pa[8], pk[8];
-        load_rows(Pv.a + r * kSlice, pa);
-        load_rows(Pv.k + r * kSlice, pk);
-#pragma unroll
-        for (int m = 0; m < 8; ++m)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float d = pa[m] * fmaf(pk[m], nbw[c], ds[m][c]);
-                ds[m][c] = fmaf(q2[m], sd[c], d);
-                wp[m & 1][c] = fmaf(k2[m], ds[m][c], wp[m & 1][c]);
-            }
-    } else {
-#pragma unroll
-        for (int m = 0; m < 8; ++m)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                ds[m][c] = fmaf(q2[m], sd[c], ds[m][c]);
-                wp[m & 1][c] = fmaf(k2[m], ds[m][c], wp[m & 1][c]);
-            }
-    }
-    float w[4] = {wp[0][0] + wp[1][0], wp[0][1] + wp[1][1], wp[0][2] + wp[1][2], wp[0][3] + wp[1][3]};
-    sum16x4(w);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) nbw[c] = -bt * w[c];
-    const bool lead = r == 0;
-    if (lead) {
-        *reinterpret_cast<float4*>(W + (t * H + h) * kD + c0) = make_float4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<float4*>(dX + t * 3 * HD + 2 * HD + (int64_t)h * kD + c0) =
-            make_float4(bt * w[0], bt * w[1], bt * w[2], bt * w[3]);
-    }
-    float pb = lead ? w[0] * e4.x + w[1] * e4.y + w[2] * e4.z + w[3] * e4.w : 0.f;
-    float pe = lead ? e4.x * do4.x + e4.y * do4.y + e4.z * do4.z + e4.w * do4.w : 0.f;
-    pb += __shfl_xor_sync(0xffffffffu, pb, 16);
-    pe += __shfl_xor_sync(0xffffffffu, pe, 16);
-    if (lane == 0) {
-        atomicAdd(accb, pb);
-        atomicAdd(acce, pe);
-    }
-}
-
-// Backward sweep of the state gradient, tokens in reverse: dS' = dS + scale q^ do^T,
-// w = dS'^T k^, dv = beta w, then dS <- Diag(alpha) (dS' - beta k^ w^T) (applied in the next
-// token's pass).  Writes w, dv, the sums dbeta = w . e and e . do of every token (atomics over the
-// CTAs of a unit), the state gradient at the end of every segment (dSck: before that token's own
-// terms) and at the start (dS0).  Blocks are the forward sweep's, taken last to first, so that
-// every segment ends at the last token of a block.
-__global__ void __launch_bounds__(128)
-k_bwd_bwd_cols(const float* __restrict__ X, const float* __restrict__ g, const float* __restrict__ beta,
-               const float* __restrict__ dO, const float* __restrict__ E, const int32_t* __restrict__ cu,
-               const int64_t* __restrict__ prefix, int64_t T_total, int H, float scale,
-               const float* __restrict__ dS_fin, float* __restrict__ W, float* __restrict__ dX,
-               float* __restrict__ dbeta, float* __restrict__ edo, float* __restrict__ dSck,
-               float* __restrict__ dS0, int64_t slots) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    ColTok* buf = reinterpret_cast<ColTok*>(smem_raw);  // [2][kTB]
-    __shared__ float acc[2][2][kTB];                   // [block parity][dbeta, e.do][token]
-    const int u = blockIdx.x / kColCtas, cq = blockIdx.x % kColCtas, n = u / H, h = u % H;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane & 15;
-    const int cl = warp * 8 + 4 * (lane >> 4), c0 = cq * kCols + cl;
-    if (tid < 4 * kTB) (&acc[0][0][0])[tid] = 0.f;
-    int64_t s0, s1;
-    seq_range(cu, n, T_total, s0, s1);
-    const int64_t nseg = (s1 - s0 + kSeg - 1) / kSeg;
-    const int64_t sb = slot_base(prefix, n, H, h, nseg, slots);
-    if (sb < 0) return;  // flagged by the forward sweep
-    const int64_t HD = (int64_t)H * kD;
-    const ColSrc dos{dO, HD}, es{E, HD};
-    float ds[8][4];
-    if (dS_fin) {
-        load_slice(dS_fin + (int64_t)u * kD * kD, r, c0, ds);
-    } else {
-#pragma unroll
-        for (int m = 0; m < 8; ++m)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) ds[m][c] = 0.f;
-    }
-    // step i takes block j = nblk - 1 - i: tokens [s0 + j kTB, min(s0 + (j + 1) kTB, s1))
-    const int64_t nblk = (s1 - s0 + kTB - 1) / kTB;
-    auto t0_of = [&](int64_t i) { return s0 + (nblk - 1 - i) * kTB; };
-    auto nt_of = [&](int64_t i) { return (int)(s1 - t0_of(i) < kTB ? s1 - t0_of(i) : kTB); };
-    if (nblk > 0) stage_cols(buf, t0_of(0), nt_of(0), X, g, beta, dos, es, 2, H, h, cq, tid);
-    cp_commit();
-    for (int64_t i = 0; i < nblk; ++i) {
-        __syncthreads();
-        if (i > 0 && tid < nt_of(i - 1)) {  // the sums of the previous step are complete
-            const int p = (i - 1) & 1;
-            const int64_t t = t0_of(i - 1) + tid;
-            atomicAdd(dbeta + t * H + h, acc[p][0][tid]);
-            atomicAdd(edo + t * H + h, acc[p][1][tid]);
-            acc[p][0][tid] = 0.f;
-            acc[p][1][tid] = 0.f;
-        }
-        if (i + 1 < nblk)
-            stage_cols(buf + ((i + 1) & 1) * kTB, t0_of(i + 1), nt_of(i + 1), X, g, beta, dos, es, 2, H, h, cq,
-                       tid);
-        cp_commit();
-        cp_wait<1>();
-        __syncthreads();
-        ColTok* st = buf + (i & 1) * kTB;
-        const int nt = nt_of(i);
-        const int64_t t0 = t0_of(i);
-        stage_exp_cols(st, nt, tid);
-        __syncthreads();
-        // the block's last token ends a segment when the segment is full or the sequence ends there
-        const int64_t tl = t0 + nt - 1;
-        if ((tl - s0) % kSeg == kSeg - 1 || tl == s1 - 1) store_slice(dSck + (sb + (tl - s0) / kSeg) * kD * kD, r, c0, ds);
-        float nbw[4];  // -beta w of the later token, whose decay is pending
-        float* ab = &acc[i & 1][0][0];
-        float* ae = &acc[i & 1][1][0];
-        bwd_token<false>(ds, nbw, st[nt - 1], st[nt - 1], r, cl, c0, lane, scale, tl, H, h, W, dX, ab + nt - 1,
-                         ae + nt - 1);
-        for (int tk = nt - 2; tk >= 0; --tk)
-            bwd_token<true>(ds, nbw, st[tk], st[tk + 1], r, cl, c0, lane, scale, t0 + tk, H, h, W, dX, ab + tk,
-                            ae + tk);
-        {  // the block's first token's decay, before its buffer is refilled
-            float pa[8], pk[8];
-            load_rows(st[0].a + r * kSlice, pa);
-            load_rows(st[0].k + r * kSlice, pk);
-            bwd_decay(ds, pa, pk, nbw);
-        }
-    }
-    __syncthreads();
-    if (nblk > 0 && tid < nt_of(nblk - 1)) {
-        const int p = (nblk - 1) & 1;
-        const int64_t t = t0_of(nblk - 1) + tid;
-        atomicAdd(dbeta + t * H + h, acc[p][0][tid]);
-        atomicAdd(edo + t * H + h, acc[p][1][tid]);
-    }
-    if (dS0) store_slice(dS0 + (int64_t)u * kD * kD, r, c0, ds);
-}
-
 // ------------------------------------------------------------------------------ row-layout segments
 // One CTA of 256 threads per (unit, segment): thread (rg, cg) owns rows 8 rg .. 8 rg + 7 and columns
 // 8 cg .. 8 cg + 7 (packed fp32 pairs); the row sums a token needs (S x, dS' e) go over the 16
@@ -1497,22 +1105,28 @@ __global__ void k_bwd_epilogue(float* __restrict__ O, const Tdy* __restrict__ dy
     if (row < rows) {
         const int c0 = 4 * lane;
         float* orow = O + row * kD + c0;
+        // every load of the row first: o, dy, the gate pre-activations, the RMSNorm weight
         const float4 o = *reinterpret_cast<const float4*>(orow);
+        float dyv[4], gv[4] = {0.f, 0.f, 0.f, 0.f};
+        float4 wv = make_float4(1.f, 1.f, 1.f, 1.f);
+        load4(dy + row * kD + c0, dyv);
+        if (gate) load4(gate + row * kD + c0, gv);
+        if (rms_w) wv = make_float4(rms_w[c0], rms_w[c0 + 1], rms_w[c0 + 2], rms_w[c0 + 3]);  // 4-byte aligned
         const float r = 1.0f / sqrtf(warp_sum(dot4(o, o)) * (1.0f / kD) + eps_rms);
-        float dn[4], dw[4];
-        const float ov[4] = {o.x, o.y, o.z, o.w};
+        float dn[4], dw[4], dgv[4];
+        const float ov[4] = {o.x, o.y, o.z, o.w}, wm[4] = {wv.x, wv.y, wv.z, wv.w};
         float dno = 0.f;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            const float w = rms_w ? rms_w[c0 + m] : 1.f;
-            const float sg = gate ? 1.0f / (1.0f + expf(-to_f(gate[row * kD + c0 + m]))) : 1.f;
-            const float d = to_f(dy[row * kD + c0 + m]);
+            const float sg = gate ? 1.0f / (1.0f + expf(-gv[m])) : 1.f;
+            const float d = dyv[m];
             const float nv = ov[m] * r;
-            if (dgate) dgate[row * kD + c0 + m] = gate ? d * nv * w * sg * (1.f - sg) : 0.f;
+            dgv[m] = gate ? d * nv * wm[m] * sg * (1.f - sg) : 0.f;
             dw[m] = d * nv * sg;
-            dn[m] = d * w * sg;
+            dn[m] = d * wm[m] * sg;
             dno += dn[m] * ov[m];
         }
+        if (dgate) *reinterpret_cast<float4*>(dgate + row * kD + c0) = make_float4(dgv[0], dgv[1], dgv[2], dgv[3]);
         dno = warp_sum(dno);
         const float r3 = r * r * r * dno * (1.0f / kD);
         *reinterpret_cast<float4*>(orow) =
@@ -1577,6 +1191,7 @@ __global__ void k_bwd_l2(const float* __restrict__ X, const float* __restrict__ 
 // every sequence that starts in the tile.  The du of the three tokens after the tile (same
 // sequence) are recomputed as a look-ahead.  Grid: cblocks channel blocks x tiles.
 constexpr int kConvTile = 128;
+constexpr int kConvBatch = 8;  // tokens whose loads are issued together
 
 template <typename Tio>
 __global__ void k_bwd_conv(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __restrict__ v,
@@ -1661,16 +1276,17 @@ __global__ void k_bwd_conv(const Tio* __restrict__ q, const Tio* __restrict__ k,
             x2 = raw(t);
             fresh = false;
         }
-        if (t - 6 >= s0 && t - 3 >= ta) {  // four tokens inside the sequence: their loads first
-            const float r0 = to_f(src[(t - 3) * xs + hc]), r1 = to_f(src[(t - 4) * xs + hc]);
-            const float r2 = to_f(src[(t - 5) * xs + hc]), r3 = to_f(src[(t - 6) * xs + hc]);
-            const float d0 = dA[t * HD3 + ch], d1 = dA[(t - 1) * HD3 + ch];
-            const float d2 = dA[(t - 2) * HD3 + ch], d3 = dA[(t - 3) * HD3 + ch];
-            step(t, r0, d0);
-            step(t - 1, r1, d1);
-            step(t - 2, r2, d2);
-            step(t - 3, r3, d3);
-            t -= 4;
+        if (t - (kConvBatch + 2) >= s0 && t - (kConvBatch - 1) >= ta) {
+            // kConvBatch tokens inside the sequence: all their loads first
+            float rr[kConvBatch], dd[kConvBatch];
+#pragma unroll
+            for (int i = 0; i < kConvBatch; ++i) {
+                rr[i] = to_f(src[(t - 3 - i) * xs + hc]);
+                dd[i] = dA[(t - i) * HD3 + ch];
+            }
+#pragma unroll
+            for (int i = 0; i < kConvBatch; ++i) step(t - i, rr[i], dd[i]);
+            t -= kConvBatch;
         } else {
             step(t, raw(t - 3), dA[t * HD3 + ch]);
             --t;
@@ -1723,10 +1339,7 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
                                           cptr<Tio>(a.conv_state_in), a.cu_seqlens, a.N, T, a.H, a.eps_l2, X, nrm);
         if ((e = cudaGetLastError())) return e;
     }
-    if ((e = cudaFuncSetAttribute(k_bwd_fwd_cols, cudaFuncAttributeMaxDynamicSharedMemorySize, kColSmem)) ||
-        (e = cudaFuncSetAttribute(k_bwd_bwd_cols, cudaFuncAttributeMaxDynamicSharedMemorySize, kColSmem)) ||
-        (e = cudaFuncSetAttribute(k_bwd_rows, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmem)))
-        return e;
+    if ((e = cudaFuncSetAttribute(k_bwd_rows, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmem))) return e;
     float* Rec = reinterpret_cast<float*>(ws + L.rec);
     if (rows > 0 && L.max_ch > 0) {
         k_bwd_chunk_prep<<<(unsigned)(units * L.max_ch), 128, 0, s>>>(X, a.g, a.beta, a.cu_seqlens, prefix, T, a.H,
