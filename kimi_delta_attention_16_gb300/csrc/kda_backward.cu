@@ -62,16 +62,20 @@ __device__ __forceinline__ void load4(const float* p, float (&x)[4]) {
 // ------------------------------------------------------------------------------ prep
 // One warp per (token, head): conv + SiLU of the q, k, v channels of the head (lane l: channels
 // 4 l .. 4 l + 3), the L2 norms of q and k.  X: [T][3][H][D] fp32 (q^, k^, v), nrm: [T][H][2].
+// Grid: ceil(T / 8) x H blocks of 8 warps.
 template <typename Tio>
 __global__ void k_bwd_prep(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __restrict__ v,
                            int64_t xs, const float* __restrict__ conv_w, const Tio* __restrict__ cs_in,
                            const int32_t* __restrict__ cu, int N, int64_t T_total, int H, float eps_l2,
                            float* __restrict__ X, float* __restrict__ nrm) {
-    const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    // the warps of a block take consecutive tokens of one head, so that the head's conv taps and
+    // the overlapping input windows are served from L1
+    const int wpb = blockDim.x / 32;
+    const int h = (int)(blockIdx.x % H);
+    const int64_t t = (int64_t)(blockIdx.x / H) * wpb + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (row >= T_total * H) return;
-    const int64_t t = row / H;
-    const int h = (int)(row % H);
+    if (t >= T_total) return;
+    const int64_t row = t * H + h;
     // the sequence of token t (binary search over cu_seqlens)
     int lo = 0, hi = N;
     while (hi - lo > 1) {
@@ -93,9 +97,10 @@ __global__ void k_bwd_prep(const Tio* __restrict__ q, const Tio* __restrict__ k,
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int64_t p = t - 3 + j;
-            if (p >= s0) {
-                load4(src[part] + p * xs + (int64_t)h * kD + 4 * lane, x[j]);
-            } else {
+            // loaded whatever the sequence start (rows 0 .. t exist), so that the loads do not wait
+            // for cu_seqlens; rows before the start are replaced below
+            load4(src[part] + (p > 0 ? p : 0) * xs + (int64_t)h * kD + 4 * lane, x[j]);
+            if (p < s0) {
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const int64_t ch = (int64_t)part * HD + (int64_t)h * kD + 4 * lane + m;
@@ -1335,7 +1340,7 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
     if ((e = cudaGetLastError())) return e;
     const unsigned rb = (unsigned)((rows + 7) / 8);
     if (rows > 0) {
-        k_bwd_prep<Tio><<<rb, 256, 0, s>>>(cptr<Tio>(a.q), cptr<Tio>(a.k), cptr<Tio>(a.v), xs, a.conv_w,
+        k_bwd_prep<Tio><<<(unsigned)((T + 7) / 8 * a.H), 256, 0, s>>>(cptr<Tio>(a.q), cptr<Tio>(a.k), cptr<Tio>(a.v), xs, a.conv_w,
                                           cptr<Tio>(a.conv_state_in), a.cu_seqlens, a.N, T, a.H, a.eps_l2, X, nrm);
         if ((e = cudaGetLastError())) return e;
     }
