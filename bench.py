@@ -606,14 +606,15 @@ def time_backward(args, pg, dev, stream, peaks, peak_src, world):
     obj = {"metric": f"KDA backward tokens/s (layer_8k: T={T}, H=96, d=128; all input gradients)",
            "value": round(aggregate_rate(world, T, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
            "steps": steps, "workspace_bytes": ws.numel(),
-           "roofline": {"kernel": "the whole kda_backward call (fp32 SIMT recurrence sweeps dominate)",
+           "roofline": {"kernel": "the whole kda_backward call (fp32 SIMT row sweeps and 3-term TF32 "
+                                  "mma.sync chunk sweeps dominate)",
                         "bound": "alu", "achieved": round(tf, 2), "peak": round(FP32_SIMT_TFLOPS, 1),
                         "unit": "TFLOP/s", "frac": round(tf / FP32_SIMT_TFLOPS, 4),
                         "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 x 2.07 GHz",
                         "traffic": None, "algorithmic_flops": flops}}
     del inp, dy, dsf, ws
     torch.cuda.empty_cache()
-    return obj, steps * 9  # nine kernels per call (the five output/partial memsets are not counted)
+    return obj, steps * 10  # ten kernels per call (the five output/partial memsets are not counted)
 
 
 def time_multi_token(args, pg, dev, stream, peaks, peak_src, world, t_new=4, ring=8):

@@ -337,20 +337,23 @@ kda_status kda_gemm(const kda_gemm_args* args, kda_stream_t stream);
  * initial_state); out_dtype there is the dtype of dy.  Its out, final_state,
  * conv_state_out, chunk, flags and segments are ignored; its workspace and
  * workspace_bytes are this call's scratch (kda_backward_workspace_size).
- * Supported: D = 128, io bf16 or fp32; arithmetic is fp32 throughout (the
- * decays e^g, SiLU and sigmoid through the IEEE functions), so the result
- * does not depend on the forward's path.
+ * Supported: D = 128, io bf16 or fp32; arithmetic is fp32 (the decays e^g,
+ * SiLU and sigmoid through the IEEE functions; the chunk products on the
+ * tensor cores as three TF32 terms of hi/lo splits, close to fp32), so the
+ * result does not depend on the forward's path.
  *
- * Method: conv + SiLU + L2 norms recomputed per token; the recurrence replayed
- * once, split by value column (each column of S evolves on its own), saving
- * o_t, e_t = v_t - S_bar^T k_t and the state at the start of every 64-token
- * segment; the epilogue's derivative per row; the state gradient run once
- * backwards, also by column, saving w_t = dS^T k_t and the gradient at the end
- * of every segment; then every segment in parallel, by row (with e and w known,
- * each row of S and of dS evolves on its own): dq, dk and the log-decay's
- * gradient, which follows from g entering only through the decayed read keys
- * and queries and the un-decayed written keys; last the L2 norm's, SiLU's and
- * the conv's derivatives.  No per-token state is stored.
+ * Method: conv + SiLU + L2 norms recomputed per token; for every 16-token
+ * chunk, all at once, the parts that do not involve the state (decayed keys
+ * and queries, the chunk's triangular products and (I + A)^-1); the
+ * recurrence replayed chunk by chunk, saving o_t, e_t = v_t - S_bar^T k_t and
+ * the state at the start of every 64-token segment; the epilogue's derivative
+ * per row; the state gradient run backwards chunk by chunk, saving
+ * w_t = dS^T k_t and the gradient at the end of every segment; then every
+ * segment in parallel, by row (with e and w known, each row of S and of dS
+ * evolves on its own): dq, dk and the log-decay's gradient, which follows from
+ * g entering only through the decayed read keys and queries and the un-decayed
+ * written keys; last the L2 norm's, SiLU's and the conv's derivatives.  No
+ * per-token state is stored.
  *
  * Needs cu_seqlens_host (the checkpoint layout is planned on the host).  The
  * outputs must not overlap each other or any input.  dconv_w and drms_w are
