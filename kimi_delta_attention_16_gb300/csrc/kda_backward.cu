@@ -28,6 +28,7 @@
 //   conv      du = da sig(u) (1 + u (1 - sig(u))); dx, the taps' and the conv state's gradients
 // No token's state is stored: the row kernels replay at most kSeg tokens from the checkpoints.
 #include "kda_internal.cuh"
+#include "kda_tc_ptx.cuh"
 
 namespace kda {
 
@@ -804,6 +805,604 @@ k_bwd_bwd_chunks(const float* __restrict__ Rec, const float* __restrict__ dO, co
     }
 }
 
+// ------------------------------------------------------------------------------ tcgen05 chunk sweeps
+// The same chunk algebra with the products on the 5th-generation tensor cores (tcgen05.mma
+// kind::tf32, accumulators in tensor memory).  One CTA of 4 warps per unit: thread j owns value
+// column j, which is TMEM lane j.  M = 128 value columns; the state (S^T, lanes = columns,
+// TMEM columns = keys) stays in TMEM as the accumulator of the update and, split into its TF32
+// high part and remainder, as the A operand of the reads.  B operands are K-major tiles with the
+// 128-byte swizzle (32 fp32 per row), built by the threads from the plain records one chunk ahead
+// while the tensor core runs; both hi and lo parts (3 MMA terms per product, as above).
+namespace tcs {
+using namespace kda::tc;
+
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+    return (1u << 4)                      // D: fp32
+           | (2u << 7) | (2u << 10)       // A, B: tf32 (both K-major)
+           | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::tf32
+__device__ __forceinline__ void mma_tf32_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
+// Byte offset of fp32 elements (r, k .. k + 3), k % 4 == 0, in a K-major 128-byte-swizzled tile of
+// `rows` rows: K-blocks of 32 elements, each rows x 128 bytes; within an 8-row atom the 16-byte
+// chunk c of row r sits at chunk position c ^ (r % 8).
+__device__ __forceinline__ uint32_t kmaj(int rows, int r, int k) {
+    return (uint32_t)((k >> 5) * rows * 128 + r * 128 + ((((k & 31) >> 2) ^ (r & 7)) << 4));
+}
+// B descriptor for K-step ks (8 elements) of a K-major tile of `rows` rows.
+__device__ __forceinline__ uint64_t bdesc(uint32_t base, int rows, int ks) {
+    return desc_sw128(base + (uint32_t)((ks >> 2) * rows * 128 + (ks & 3) * 32), 16, 1024);
+}
+__device__ __forceinline__ float4 hi4(float4 x, float4& lo) {
+    float4 h;
+    h.x = __uint_as_float(tf32_of(x.x));
+    h.y = __uint_as_float(tf32_of(x.y));
+    h.z = __uint_as_float(tf32_of(x.z));
+    h.w = __uint_as_float(tf32_of(x.w));
+    lo = make_float4(x.x - h.x, x.y - h.y, x.z - h.z, x.w - h.w);
+    return h;
+}
+__device__ __forceinline__ void sts128(unsigned char* base, uint32_t off, float4 v) {
+    *reinterpret_cast<float4*>(base + off) = v;
+}
+// Waits on an MMA barrier: lane 0 of each warp polls (bounded), the warp follows.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    fence_after_sync();
+    return ok;
+}
+// 32 consecutive TMEM columns of the thread's lane <-> registers.
+__device__ __forceinline__ void tld32(uint32_t ta, float (&v)[32]) {
+    uint32_t r[32];
+    tmem_ld32(ta, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tst32(uint32_t ta, const float (&v)[32]) {
+    uint32_t a[16], b[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        a[i] = __float_as_uint(v[i]);
+        b[i] = __float_as_uint(v[16 + i]);
+    }
+    tmem_st16(ta, a);
+    tmem_st16(ta + 16, b);
+}
+__device__ __forceinline__ void tst16(uint32_t ta, const float (&v)[16]) {
+    uint32_t a[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a[i] = __float_as_uint(v[i]);
+    tmem_st16(ta, a);
+}
+}  // namespace tcs
+
+// ------------------------------------------------------------------------------ tcgen05 row sweeps
+// The row kernel's quantities in chunk form, per (unit, 64-token segment), with S_c the state at a
+// chunk's start (from the segment's checkpoint, carried forward) and D the state gradient at its end
+// (from the segment's checkpoint, carried backward); per token t of the chunk, with C, C', B as in
+// the records and the chunk's Grams P = E dO^T, Q = E W^T (16 x 16):
+//   dq_t   = scale (C_t (S_c do_t) + C'_t sum_{s<=t} beta_s P_st k^_s / C'_s),
+//   dkr_t  = -beta_t (C_t (S_c w_t) + C'_t sum_{s<t} beta_s Q_st k^_s / C'_s),
+//   dkw_t  = beta_t ((C_last / C_t) (D e_t) + (1 / C'_t) (sum_{tau>=t} scale P_t,tau C'_tau q^_tau
+//                                                  - sum_{tau>t} beta_tau Q_t,tau C'_tau k^_tau)),
+//   S_{c+1} = Diag(C_last) S_c + Kbar^T B E,   D <- Diag(C_last) D + Qr^T (scale dO) - Kr^T B W
+// (each token's forward and adjoint steps unrolled; checked against the token loop in fp64 before
+// it was written).  The products S_c [dO; W]^T (N = 32), D E^T (N = 16) and the two updates
+// (N = 128) run on tcgen05 (kind::tf32, hi/lo terms); keys are TMEM lanes.  8 warps: warps w and
+// w + 4 share lanes 32 (w % 4) ..; the per-token vector work is split between them.  dg's pieces
+// and the other outputs are the row kernel's.
+constexpr int kRtThreads = 256;
+constexpr int kRs = kD + 4;  // row stride of the staged E, dO, W rows (conflict-free Gram reads)
+struct RtStage {
+    float E[kCk][kRs], DO[kCk][kRs], W[kCk][kRs];
+    float q[kCk][kD], k[kCk][kD], g[kCk][kD], R1[kCk][kD], R2[kCk][kD];
+    float CL[kD], beta[kCk];
+};
+struct RowsTcSmem {
+    unsigned char b1h[16384], b1l[16384];  // fwd: [dO; W] (32 x 128); bwd: E (16 x 128); K-major
+    unsigned char b2h[16384], b2l[16384];  // fwd: (B E)^T (128 x 16); bwd: [scale dO; -B W]^T (128 x 32)
+    RtStage st[2];
+    float P[kChunksPerSeg][kCk][kCk], Q[kChunksPerSeg][kCk][kCk];
+    float xch[kCk][kD];
+    uint64_t barP, barU;
+    uint32_t tbase;
+    int fail;
+};
+constexpr int kRowsTcSmem = (int)sizeof(RowsTcSmem) + 1024;
+static_assert(kRowsTcSmem <= 227 * 1024, "rows kernel shared memory");
+
+// Issues the copies of one chunk: rows t0 .. t0 + nt - 1 of E, dO, W, q^, k^, g; two record rows
+// (r1, r2 offsets in the record; r2 < 0: none), C_last and beta.  Threads 0-191 own one (row kind,
+// 16-byte column) each and walk the rows; threads 192-255 the record rows, C_last and beta.
+__device__ __forceinline__ void rt_stage(RtStage& s, const float* X, const float* g, const float* E, const float* dO,
+                                         const float* W, const float* R, int r1, int r2, int64_t t0, int nt, int H,
+                                         int h, int tid) {
+    const int64_t HD = (int64_t)H * kD;
+    if (tid < 192) {
+        const int part = tid >> 5, c4 = (tid & 31) * 4;
+        const float* src;
+        int64_t step;
+        float* dst;
+        int dstep;
+        switch (part) {
+            case 0: src = E + (t0 * H + h) * kD; step = HD; dst = &s.E[0][0]; dstep = kRs; break;
+            case 1: src = dO + (t0 * H + h) * kD; step = HD; dst = &s.DO[0][0]; dstep = kRs; break;
+            case 2: src = W + (t0 * H + h) * kD; step = HD; dst = &s.W[0][0]; dstep = kRs; break;
+            case 3: src = X + t0 * 3 * HD + (int64_t)h * kD; step = 3 * HD; dst = &s.q[0][0]; dstep = kD; break;
+            case 4: src = X + t0 * 3 * HD + HD + (int64_t)h * kD; step = 3 * HD; dst = &s.k[0][0]; dstep = kD; break;
+            default: src = g + (t0 * H + h) * kD; step = HD; dst = &s.g[0][0]; dstep = kD; break;
+        }
+        src += c4;
+        dst += c4;
+        for (int row = 0; row < nt; ++row, src += step, dst += dstep) cp16(dst, src);
+    } else {
+        const int q = tid - 192, c4 = (q & 31) * 4;  // 0-31: R1, 32-63: R2
+        const int ro = q < 32 ? r1 : r2;
+        if (ro >= 0) {
+            float* dst = (q < 32 ? &s.R1[0][0] : &s.R2[0][0]) + c4;
+            const float* src = R + ro + c4;
+#pragma unroll 4
+            for (int row = 0; row < kCk; ++row) cp16(dst + row * kD, src + row * kD);
+        }
+        if (q < 32) cp16(&s.CL[c4], R + kRecCL + c4);
+        else if (q < 36) cp16(&s.beta[4 * (q - 32)], R + kRecBeta + 4 * (q - 32));
+    }
+}
+
+__global__ void __launch_bounds__(kRtThreads, 1)
+k_bwd_rows_tc(const float* __restrict__ X, const float* __restrict__ g, const float* __restrict__ Rec,
+              const float* __restrict__ dO, float* __restrict__ E, float* __restrict__ W,
+              const int32_t* __restrict__ cu, const int64_t* __restrict__ prefix, int64_t T_total, int H,
+              float scale, int max_seg, const float* __restrict__ Sck, const float* __restrict__ dSck,
+              const float* __restrict__ dS_fin, float* __restrict__ dX, float* __restrict__ dg,
+              float* __restrict__ segtot, float* __restrict__ segown, float* __restrict__ fin, int64_t slots,
+              int* __restrict__ d_status) {
+    using namespace tcs;
+    extern __shared__ unsigned char smem_raw[];
+    RowsTcSmem& sm = *reinterpret_cast<RowsTcSmem*>(smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023));
+    const int u = blockIdx.x / max_seg, sg = blockIdx.x % max_seg, n = u / H, h = u % H;
+    const int tid = threadIdx.x, warp = tid >> 5, role = warp >> 2, key = 32 * (warp & 3) + (tid & 31);
+    int64_t s0, s1;
+    seq_range(cu, n, T_total, s0, s1);
+    const int64_t nseg = (s1 - s0 + kSeg - 1) / kSeg;
+    if (sg >= nseg) return;
+    const int64_t sb = slot_base(prefix, n, H, h, nseg, slots);
+    if (sb < 0) return;  // flagged by the forward sweep
+    const int64_t HD = (int64_t)H * kD;
+    const int64_t ta = s0 + (int64_t)sg * kSeg, tb = ta + kSeg < s1 ? ta + kSeg : s1;
+    const int ncs = (int)((tb - ta + kCk - 1) / kCk);
+    auto nt_of = [&](int cc) { return (int)(tb - (ta + cc * kCk) < kCk ? tb - (ta + cc * kCk) : kCk); };
+    if (tid == 0) {
+        mbar_init(&sm.barP, 1);
+        mbar_init(&sm.barU, 1);
+        sm.fail = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&sm.tbase, 512);
+    // stage k < ncs: forward chunk k (record row Kbar); k >= ncs: backward chunk 2 ncs - 1 - k (Qr, Kr)
+    auto stage = [&](int k) {
+        const bool fw = k < ncs;
+        const int cc = fw ? k : 2 * ncs - 1 - k;
+        const float* R = Rec + rec_index(sb, (int64_t)sg * kChunksPerSeg + cc) * kRec;
+        rt_stage(sm.st[k & 1], X, g, E, dO, W, R, fw ? kRecKb : kRecQr, fw ? -1 : kRecKr, ta + (int64_t)cc * kCk,
+                 nt_of(cc), H, h, tid);
+    };
+    stage(0);
+    cp_commit();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tm = sm.tbase, tl = tm + ((uint32_t)(32 * (warp & 3)) << 16);
+    const int cb = 64 * role;  // this thread's half of the state's 128 value columns in the TMEM passes
+    {  // the segment's start state: lane = key, columns = value columns
+        const float* Sg = Sck + ((sb + sg) * kD + key) * kD + cb;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(Sg + c0 + i);
+                v[i] = x.x;
+                v[i + 1] = x.y;
+                v[i + 2] = x.z;
+                v[i + 3] = x.w;
+            }
+            tst32(tl + cb + c0, v);
+        }
+        tmem_st_wait();
+    }
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    float pre_q = 0.f, pre_k = 0.f, run = 0.f;  // role 0: the segment's running sums for its key
+    // the state pass: high part and remainder of the state (A operand of the reads), then the decay
+    auto state_pass = [&](const RtStage& s) {
+        const float cl = s.CL[key];
+#pragma unroll 1
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+            float v[32], hv[32], lv[32];
+            tld32(tl + cb + c0, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                hv[i] = __uint_as_float(tf32_of(v[i]));
+                lv[i] = v[i] - hv[i];
+                v[i] *= cl;
+            }
+            tst32(tl + 128 + cb + c0, hv);
+            tst32(tl + 256 + cb + c0, lv);
+            tst32(tl + cb + c0, v);
+        }
+    };
+    auto sync_tc = [&]() {
+        tmem_st_wait();
+        fence_async_smem();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+    };
+    // ---------------- forward: dq, dk_read, the read part of dg
+#pragma unroll 1
+    for (int cc = 0; cc < ncs; ++cc) {
+        const int k = cc, nt = nt_of(cc);
+        const int64_t t0 = ta + (int64_t)cc * kCk;
+        const RtStage& s = sm.st[k & 1];
+        if (cc > 0 && !sm.fail && !warp_wait(&sm.barU, (uint32_t)((k - 1) & 1))) sm.fail = 1;  // the state is complete
+        cp_wait<0>();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+        if (k + 1 < 2 * ncs) stage(k + 1);
+        cp_commit();
+        if (role == 1) {  // warps 4-7: b1 = [dO; W] (rows 0-15 dO, 16-31 W) and b2 = (B E)^T, K-major
+            const int rt = tid - 128;
+            for (int i4 = rt; i4 < 32 * 32; i4 += 128) {
+                const int row = i4 >> 5, c4 = (i4 & 31) * 4, t = row & 15;
+                const float4 x = t < nt ? *reinterpret_cast<const float4*>(row < 16 ? &s.DO[t][c4] : &s.W[t][c4]) : z4;
+                float4 lo;
+                const float4 hi = hi4(x, lo);
+                const uint32_t off = kmaj(32, row, c4);
+                sts128(sm.b1h, off, hi);
+                sts128(sm.b1l, off, lo);
+            }
+#pragma unroll
+            for (int m = 0; m < kCk; m += 4) {  // row = value column rt, K = token
+                float x[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = m + e;
+                    x[e] = t < nt ? s.beta[t] * s.E[t][rt] : 0.f;
+                }
+                float4 lo;
+                const float4 hi = hi4(make_float4(x[0], x[1], x[2], x[3]), lo);
+                const uint32_t off = kmaj(128, rt, m);
+                sts128(sm.b2h, off, hi);
+                sts128(sm.b2l, off, lo);
+            }
+        } else {  // warps 0-3: the chunk's Grams P = E dO^T (warps 0, 2), Q = E W^T (1, 3) on mma.sync
+            const int gq = (tid & 31) >> 2, tq = tid & 3, nt8 = 8 * (warp >> 1);
+            const float(*Bm)[kRs] = (warp & 1) ? s.W : s.DO;
+            const bool ar0 = gq < nt, ar1 = gq + 8 < nt, bn = nt8 + gq < nt;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int kc = 0; kc < kD; kc += 8) {
+                const float2 x0 = ar0 ? *reinterpret_cast<const float2*>(&s.E[gq][kc + 2 * tq]) : make_float2(0.f, 0.f);
+                const float2 x1 = ar1 ? *reinterpret_cast<const float2*>(&s.E[gq + 8][kc + 2 * tq]) : make_float2(0.f, 0.f);
+                const float2 y = bn ? *reinterpret_cast<const float2*>(&Bm[nt8 + gq][kc + 2 * tq]) : make_float2(0.f, 0.f);
+                const float av[4] = {x0.x, x0.y, x1.x, x1.y};  // accumulator order: (g, 2t), (g, 2t+1), (g+8, ..)
+                const Frag4 a = afrag_acc(av);
+                Frag2 b;
+                split_tf32(y.x, b.h[0], b.l[0]);
+                split_tf32(y.y, b.h[1], b.l[1]);
+                mma3(acc, a, b);
+            }
+            float(*G)[kCk] = (warp & 1) ? sm.Q[cc] : sm.P[cc];
+            G[gq][nt8 + 2 * tq] = acc[0];
+            G[gq][nt8 + 2 * tq + 1] = acc[1];
+            G[gq + 8][nt8 + 2 * tq] = acc[2];
+            G[gq + 8][nt8 + 2 * tq + 1] = acc[3];
+        }
+        if (role == 0) {  // A of the update: Kbar^T (lane = key, 16 tokens)
+            float hv[16], lv[16];
+#pragma unroll
+            for (int t = 0; t < kCk; ++t) {
+                const float x = s.R1[t][key];
+                hv[t] = __uint_as_float(tf32_of(x));
+                lv[t] = x - hv[t];
+            }
+            tst16(tl + 416, hv);
+            tst16(tl + 448, lv);
+        }
+        // the key's decay factors over the chunk
+        float C[kCk], Ca[kCk], Ki[kCk];
+        {
+            float G[kCk], acc = 0.f;
+#pragma unroll
+            for (int t = 0; t < kCk; ++t) {
+                acc += t < nt ? s.g[t][key] : 0.f;
+                G[t] = acc;
+            }
+#pragma unroll
+            for (int t = 0; t < kCk; ++t) {
+                C[t] = expf(G[t]);
+                Ca[t] = expf(G[t] - G[7]);
+                Ki[t] = (t < nt ? s.k[t][key] : 0.f) * expf(G[7] - G[t]);
+            }
+        }
+        state_pass(s);
+        sync_tc();
+        if (tid == 0 && !sm.fail) {
+            const uint32_t id32 = idesc_tf32(128, 32), id128 = idesc_tf32(128, 128);
+            const uint32_t h1 = smem_u32(sm.b1h), l1 = smem_u32(sm.b1l), h2 = smem_u32(sm.b2h), l2 = smem_u32(sm.b2l);
+#pragma unroll 1
+            for (int ks = 0; ks < kD / 8; ++ks) {  // [S do | S w]: A = S (high, low), B = [dO; W]
+                mma_tf32_ts(tm + 384, tm + 256 + 8 * ks, bdesc(h1, 32, ks), id32, ks > 0);
+                mma_tf32_ts(tm + 384, tm + 128 + 8 * ks, bdesc(l1, 32, ks), id32, 1);
+                mma_tf32_ts(tm + 384, tm + 128 + 8 * ks, bdesc(h1, 32, ks), id32, 1);
+            }
+            mma_commit(&sm.barP);
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {  // S += Kbar^T (B E)
+                mma_tf32_ts(tm, tm + 448 + 8 * ks, bdesc(h2, 128, ks), id128, 1);
+                mma_tf32_ts(tm, tm + 416 + 8 * ks, bdesc(l2, 128, ks), id128, 1);
+                mma_tf32_ts(tm, tm + 416 + 8 * ks, bdesc(h2, 128, ks), id128, 1);
+            }
+            mma_commit(&sm.barU);
+        }
+        if (!sm.fail && !warp_wait(&sm.barP, (uint32_t)(k & 1))) sm.fail = 1;
+        float z[kCk];
+        {
+            uint32_t r[16];
+            tmem_ld16(tl + 384 + 16 * role, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int t = 0; t < kCk; ++t) z[t] = __uint_as_float(r[t]);
+        }
+        float cq[kCk], acc[kCk];
+#pragma unroll
+        for (int t = 0; t < kCk; ++t) acc[t] = 0.f;
+        {  // right-looking over the Gram's rows: acc_t += beta_s (k^_s / C'_s) G_st (s <= t for dq, s < t for dk_read)
+            const float(*G)[kCk] = role == 0 ? sm.P[cc] : sm.Q[cc];
+#pragma unroll
+            for (int s2 = 0; s2 < kCk; ++s2) {
+                const float bk = s.beta[s2] * Ki[s2];
+#pragma unroll
+                for (int q4 = 0; q4 < kCk; q4 += 4) {
+                    if (q4 + 3 < s2) continue;
+                    const float4 p4 = *reinterpret_cast<const float4*>(&G[s2][q4]);
+                    const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int t = q4 + e;
+                        if (role == 0 ? t >= s2 : t > s2) acc[t] = fmaf(pv[e], bk, acc[t]);
+                    }
+                }
+            }
+        }
+        if (role == 0) {  // dq
+#pragma unroll
+            for (int t = 0; t < kCk; ++t) {
+                const float dq = scale * (C[t] * z[t] + Ca[t] * acc[t]);
+                cq[t] = t < nt ? s.q[t][key] * dq : 0.f;
+                if (t < nt) dX[(t0 + t) * 3 * HD + (int64_t)h * kD + key] = dq;
+            }
+        } else {  // dk_read
+#pragma unroll
+            for (int t = 0; t < kCk; ++t) {
+                const float dkr = -s.beta[t] * (C[t] * z[t] + Ca[t] * acc[t]);
+                sm.xch[t][key] = t < nt ? s.k[t][key] * dkr : 0.f;
+                if (t < nt) dX[(t0 + t) * 3 * HD + HD + (int64_t)h * kD + key] = dkr;
+            }
+        }
+        __syncthreads();
+        if (role == 0) {
+#pragma unroll
+            for (int t = 0; t < kCk; ++t) {
+                if (t < nt) dg[((t0 + t) * H + h) * kD + key] = -(pre_q + pre_k);  // minus the earlier read part
+                pre_q += cq[t];
+                pre_k += sm.xch[t][key];
+            }
+        }
+    }
+    if (!sm.fail && !warp_wait(&sm.barU, (uint32_t)((ncs - 1) & 1))) sm.fail = 1;  // the segment's end state
+    if (tb == s1) {  // the sequence's final state: rowsum(dS_T . S_T)
+        float x = 0.f;
+        if (dS_fin) {
+            const float* Dr = dS_fin + ((int64_t)u * kD + key) * kD + cb;
+#pragma unroll 1
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                float v[32];
+                tld32(tl + cb + c0, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x = fmaf(Dr[c0 + i], v[i], x);
+            }
+        }
+        if (role == 1) sm.xch[0][key] = x;
+        __syncthreads();
+        if (role == 0) fin[(int64_t)u * kD + key] = x + sm.xch[0][key];
+    }
+    fence_before_sync();
+    __syncthreads();  // every read of the end state is done
+    fence_after_sync();
+    {  // the segment's end gradient replaces the state in TMEM
+        const float* Dg = dSck + ((sb + sg) * kD + key) * kD + cb;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(Dg + c0 + i);
+                v[i] = x.x;
+                v[i + 1] = x.y;
+                v[i + 2] = x.z;
+                v[i + 3] = x.w;
+            }
+            tst32(tl + cb + c0, v);
+        }
+        tmem_st_wait();
+    }
+    // ---------------- backward: dk_write and the write part of dg, chunks last to first
+#pragma unroll 1
+    for (int k = ncs; k < 2 * ncs; ++k) {
+        const int cc = 2 * ncs - 1 - k, nt = nt_of(cc);
+        const int64_t t0 = ta + (int64_t)cc * kCk;
+        const RtStage& s = sm.st[k & 1];
+        if (k > ncs && !sm.fail && !warp_wait(&sm.barU, (uint32_t)((k - 1) & 1))) sm.fail = 1;
+        cp_wait<0>();
+        fence_before_sync();
+        __syncthreads();
+        fence_after_sync();
+        if (k + 1 < 2 * ncs) stage(k + 1);
+        cp_commit();
+        // b1 = E (16 rows), K-major
+        for (int i4 = tid; i4 < 16 * 32; i4 += kRtThreads) {
+            const int t = i4 >> 5, c4 = (i4 & 31) * 4;
+            const float4 x = t < nt ? *reinterpret_cast<const float4*>(&s.E[t][c4]) : z4;
+            float4 lo;
+            const float4 hi = hi4(x, lo);
+            const uint32_t off = kmaj(16, t, c4);
+            sts128(sm.b1h, off, hi);
+            sts128(sm.b1l, off, lo);
+        }
+        {  // b2 = [scale dO; -B W]^T: row = value column j, K = 32 (tokens of dO, then of W)
+            const int j = tid & 127, half = tid >> 7;
+#pragma unroll
+            for (int m = 0; m < 16; m += 4) {
+                float x[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = m + e;
+                    x[e] = t >= nt ? 0.f : half == 0 ? scale * s.DO[t][j] : -s.beta[t] * s.W[t][j];
+                }
+                float4 lo;
+                const float4 hi = hi4(make_float4(x[0], x[1], x[2], x[3]), lo);
+                const uint32_t off = kmaj(128, j, 16 * half + m);
+                sts128(sm.b2h, off, hi);
+                sts128(sm.b2l, off, lo);
+            }
+        }
+        {  // A of the update: [Qr | Kr]^T (lane = key, 32 tokens); role 0 the Qr half, role 1 the Kr half
+            float hv[16], lv[16];
+#pragma unroll
+            for (int t = 0; t < kCk; ++t) {
+                const float x = role == 0 ? s.R1[t][key] : s.R2[t][key];
+                hv[t] = __uint_as_float(tf32_of(x));
+                lv[t] = x - hv[t];
+            }
+            tst16(tl + 416 + 16 * role, hv);
+            tst16(tl + 448 + 16 * role, lv);
+        }
+        float CLr[kCk], iCa[kCk], Xa[kCk];  // C_last / C_t, 1 / C'_t, C'_t x_t (x = q for role 0, k for role 1)
+        {
+            float G[kCk], acc = 0.f;
+#pragma unroll
+            for (int t = 0; t < kCk; ++t) {
+                acc += t < nt ? s.g[t][key] : 0.f;
+                G[t] = acc;
+            }
+#pragma unroll
+            for (int t = 0; t < kCk; ++t) {
+                CLr[t] = expf(G[kCk - 1] - G[t]);
+                iCa[t] = expf(G[7] - G[t]);
+                const float xv = t < nt ? (role == 0 ? s.q[t][key] : s.k[t][key]) : 0.f;
+                Xa[t] = xv * expf(G[t] - G[7]);
+            }
+        }
+        state_pass(s);
+        sync_tc();
+        if (tid == 0 && !sm.fail) {
+            const uint32_t id16 = idesc_tf32(128, 16), id128 = idesc_tf32(128, 128);
+            const uint32_t h1 = smem_u32(sm.b1h), l1 = smem_u32(sm.b1l), h2 = smem_u32(sm.b2h), l2 = smem_u32(sm.b2l);
+#pragma unroll 1
+            for (int ks = 0; ks < kD / 8; ++ks) {  // D E^T: A = D (high, low), B = E
+                mma_tf32_ts(tm + 384, tm + 256 + 8 * ks, bdesc(h1, 16, ks), id16, ks > 0);
+                mma_tf32_ts(tm + 384, tm + 128 + 8 * ks, bdesc(l1, 16, ks), id16, 1);
+                mma_tf32_ts(tm + 384, tm + 128 + 8 * ks, bdesc(h1, 16, ks), id16, 1);
+            }
+            mma_commit(&sm.barP);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {  // D += [Qr | Kr]^T [scale dO; -B W]
+                mma_tf32_ts(tm, tm + 448 + 8 * ks, bdesc(h2, 128, ks), id128, 1);
+                mma_tf32_ts(tm, tm + 416 + 8 * ks, bdesc(l2, 128, ks), id128, 1);
+                mma_tf32_ts(tm, tm + 416 + 8 * ks, bdesc(h2, 128, ks), id128, 1);
+            }
+            mma_commit(&sm.barU);
+        }
+        if (!sm.fail && !warp_wait(&sm.barP, (uint32_t)(k & 1))) sm.fail = 1;
+        float x0[kCk];
+        if (role == 0) {  // (C_last / C_t) (D e_t) + (1 / C'_t) scale sum_{tau >= t} P_t,tau C'_tau q^_tau
+            uint32_t r[16];
+            tmem_ld16(tl + 384, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int t = 0; t < kCk; ++t) {
+                float acc = 0.f;
+#pragma unroll
+                for (int q4 = 0; q4 < kCk; q4 += 4) {
+                    if (q4 + 3 < t) continue;
+                    const float4 p4 = *reinterpret_cast<const float4*>(&sm.P[cc][t][q4]);
+                    const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (q4 + e >= t) acc = fmaf(pv[e], Xa[q4 + e], acc);
+                }
+                x0[t] = CLr[t] * __uint_as_float(r[t]) + iCa[t] * scale * acc;
+            }
+        } else {  // -(1 / C'_t) sum_{tau > t} beta_tau Q_t,tau C'_tau k^_tau
+#pragma unroll
+            for (int t = 0; t < kCk; ++t) Xa[t] *= s.beta[t];
+#pragma unroll
+            for (int t = 0; t < kCk; ++t) {
+                float acc = 0.f;
+#pragma unroll
+                for (int q4 = 0; q4 < kCk; q4 += 4) {
+                    if (q4 + 3 <= t) continue;
+                    const float4 p4 = *reinterpret_cast<const float4*>(&sm.Q[cc][t][q4]);
+                    const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (q4 + e > t) acc = fmaf(pv[e], Xa[q4 + e], acc);
+                }
+                sm.xch[t][key] = -iCa[t] * acc;
+            }
+        }
+        __syncthreads();
+        if (role == 0) {  // dk_write; its global E row and the suffix sum of -k dk_write in the W row
+#pragma unroll
+            for (int t = kCk - 1; t >= 0; --t) {
+                if (t >= nt) continue;
+                const float dkw = s.beta[t] * (x0[t] + sm.xch[t][key]);
+                run -= s.k[t][key] * dkw;
+                const int64_t off = ((t0 + t) * H + h) * kD + key;
+                E[off] = dkw;
+                W[off] = run;
+            }
+        }
+    }
+    if (!sm.fail && !warp_wait(&sm.barU, (uint32_t)((2 * ncs - 1) & 1))) sm.fail = 1;
+    if (role == 0) {
+        segtot[(sb + sg) * kD + key] = pre_q + pre_k + run;  // the segment's sum of dGamma
+        segown[(sb + sg) * kD + key] = pre_q + pre_k;        // its read part
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (sm.fail) {
+        if (tid == 0) flag_status(d_status, KDA_ERR_TIMEOUT);
+        __syncthreads();
+    }
+    fence_after_sync();
+    if (warp == 0) {
+        tmem_dealloc(tm, 512);
+        tmem_relinquish();
+    }
+}
+
 // ------------------------------------------------------------------------------ row-layout segments
 // One CTA of 256 threads per (unit, segment): thread (rg, cg) owns rows 8 rg .. 8 rg + 7 and columns
 // 8 cg .. 8 cg + 7 (packed fp32 pairs); the row sums a token needs (S x, dS' e) go over the 16
@@ -1372,9 +1971,10 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
                                                                         edo, dSck, b.dinitial_state, L.slots);
     if ((e = cudaGetLastError())) return e;
     if (rows == 0) return cudaSuccess;
-    k_bwd_rows<<<(unsigned)(units * L.max_seg), kRowThreads, kRowSmem, s>>>(
-        X, a.g, a.beta, O, E, W, edo, a.cu_seqlens, prefix, T, a.H, a.scale, (int)L.max_seg, Sck, dSck,
-        b.d_final_state, dX, b.dg, segtot, segown, fin, L.slots);
+    if ((e = cudaFuncSetAttribute(k_bwd_rows_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsTcSmem))) return e;
+    k_bwd_rows_tc<<<(unsigned)(units * L.max_seg), kRtThreads, kRowsTcSmem, s>>>(
+        X, a.g, Rec, O, E, W, a.cu_seqlens, prefix, T, a.H, a.scale, (int)L.max_seg, Sck, dSck, b.d_final_state, dX,
+        b.dg, segtot, segown, fin, L.slots, a.d_status);
     if ((e = cudaGetLastError())) return e;
     k_bwd_dg_carry<<<(unsigned)units, kD, 0, s>>>(a.cu_seqlens, prefix, T, a.H, fin, segtot, segown, L.slots);
     if ((e = cudaGetLastError())) return e;
