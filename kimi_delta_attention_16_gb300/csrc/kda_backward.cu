@@ -921,14 +921,15 @@ constexpr int kRowsTcSmem = (int)sizeof(RowsTcSmem) + 1024;
 static_assert(kRowsTcSmem <= 227 * 1024, "rows kernel shared memory");
 
 // Issues the copies of one chunk: rows t0 .. t0 + nt - 1 of E, dO, W, q^, k^, g; two record rows
-// (r1, r2 offsets in the record; r2 < 0: none), C_last and beta.  Threads 0-191 own one (row kind,
-// 16-byte column) each and walk the rows; threads 192-255 the record rows, C_last and beta.
+// (r1, r2 offsets in the record; r2 < 0: none), C_last and beta.  Run by 224 threads (q = 0 .. 223):
+// q < 192 owns one (row kind, 16-byte column) and walks the rows; the last 32 the record rows.
 __device__ __forceinline__ void rt_stage(RtStage& s, const float* X, const float* g, const float* E, const float* dO,
                                          const float* W, const float* R, int r1, int r2, int64_t t0, int nt, int H,
-                                         int h, int tid) {
+                                         int h, int q) {
     const int64_t HD = (int64_t)H * kD;
-    if (tid < 192) {
-        const int part = tid >> 5, c4 = (tid & 31) * 4;
+    const int c4 = (q & 31) * 4;
+    if (q < 192) {
+        const int part = q >> 5;
         const float* src;
         int64_t step;
         float* dst;
@@ -945,16 +946,13 @@ __device__ __forceinline__ void rt_stage(RtStage& s, const float* X, const float
         dst += c4;
         for (int row = 0; row < nt; ++row, src += step, dst += dstep) cp16(dst, src);
     } else {
-        const int q = tid - 192, c4 = (q & 31) * 4;  // 0-31: R1, 32-63: R2
-        const int ro = q < 32 ? r1 : r2;
-        if (ro >= 0) {
-            float* dst = (q < 32 ? &s.R1[0][0] : &s.R2[0][0]) + c4;
-            const float* src = R + ro + c4;
 #pragma unroll 4
-            for (int row = 0; row < kCk; ++row) cp16(dst + row * kD, src + row * kD);
+        for (int row = 0; row < kCk; ++row) {
+            cp16(&s.R1[row][c4], R + r1 + row * kD + c4);
+            if (r2 >= 0) cp16(&s.R2[row][c4], R + r2 + row * kD + c4);
         }
-        if (q < 32) cp16(&s.CL[c4], R + kRecCL + c4);
-        else if (q < 36) cp16(&s.beta[4 * (q - 32)], R + kRecBeta + 4 * (q - 32));
+        cp16(&s.CL[c4], R + kRecCL + c4);
+        if (q < 196) cp16(&s.beta[4 * (q - 192)], R + kRecBeta + 4 * (q - 192));
     }
 }
 
@@ -993,8 +991,9 @@ k_bwd_rows_tc(const float* __restrict__ X, const float* __restrict__ g, const fl
         const bool fw = k < ncs;
         const int cc = fw ? k : 2 * ncs - 1 - k;
         const float* R = Rec + rec_index(sb, (int64_t)sg * kChunksPerSeg + cc) * kRec;
-        rt_stage(sm.st[k & 1], X, g, E, dO, W, R, fw ? kRecKb : kRecQr, fw ? -1 : kRecKr, ta + (int64_t)cc * kCk,
-                 nt_of(cc), H, h, tid);
+        if (tid >= 32)
+            rt_stage(sm.st[k & 1], X, g, E, dO, W, R, fw ? kRecKb : kRecQr, fw ? -1 : kRecKr,
+                     ta + (int64_t)cc * kCk, nt_of(cc), H, h, tid - 32);
     };
     stage(0);
     cp_commit();
@@ -1058,42 +1057,40 @@ k_bwd_rows_tc(const float* __restrict__ X, const float* __restrict__ g, const fl
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
-        if (k + 1 < 2 * ncs) stage(k + 1);
-        cp_commit();
-        if (role == 1) {  // warps 4-7: b1 = [dO; W] (rows 0-15 dO, 16-31 W) and b2 = (B E)^T, K-major
-            const int rt = tid - 128;
-            for (int i4 = rt; i4 < 32 * 32; i4 += 128) {
-                const int row = i4 >> 5, c4 = (i4 & 31) * 4, t = row & 15;
-                const float4 x = t < nt ? *reinterpret_cast<const float4*>(row < 16 ? &s.DO[t][c4] : &s.W[t][c4]) : z4;
-                float4 lo;
-                const float4 hi = hi4(x, lo);
-                const uint32_t off = kmaj(32, row, c4);
-                sts128(sm.b1h, off, hi);
-                sts128(sm.b1l, off, lo);
+        // phase 1: the state's high part and remainder (then the decay); b1 = [dO; W] (rows 0-15 dO, 16-31 W)
+        state_pass(s);
+        for (int i4 = tid; i4 < 32 * 32; i4 += kRtThreads) {
+            const int row = i4 >> 5, c4 = (i4 & 31) * 4, t = row & 15;
+            const float4 x = t < nt ? *reinterpret_cast<const float4*>(row < 16 ? &s.DO[t][c4] : &s.W[t][c4]) : z4;
+            float4 lo;
+            const float4 hi = hi4(x, lo);
+            const uint32_t off = kmaj(32, row, c4);
+            sts128(sm.b1h, off, hi);
+            sts128(sm.b1l, off, lo);
+        }
+        sync_tc();
+        if (tid == 0 && !sm.fail) {  // [S do | S w]: A = S (high, low), B = [dO; W]
+            const uint32_t id32 = idesc_tf32(128, 32), h1 = smem_u32(sm.b1h), l1 = smem_u32(sm.b1l);
+#pragma unroll 1
+            for (int ks = 0; ks < kD / 8; ++ks) {
+                mma_tf32_ts(tm + 384, tm + 256 + 8 * ks, bdesc(h1, 32, ks), id32, ks > 0);
+                mma_tf32_ts(tm + 384, tm + 128 + 8 * ks, bdesc(l1, 32, ks), id32, 1);
+                mma_tf32_ts(tm + 384, tm + 128 + 8 * ks, bdesc(h1, 32, ks), id32, 1);
             }
-#pragma unroll
-            for (int m = 0; m < kCk; m += 4) {  // row = value column rt, K = token
-                float x[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int t = m + e;
-                    x[e] = t < nt ? s.beta[t] * s.E[t][rt] : 0.f;
-                }
-                float4 lo;
-                const float4 hi = hi4(make_float4(x[0], x[1], x[2], x[3]), lo);
-                const uint32_t off = kmaj(128, rt, m);
-                sts128(sm.b2h, off, hi);
-                sts128(sm.b2l, off, lo);
-            }
-        } else {  // warps 0-3: the chunk's Grams P = E dO^T (warps 0, 2), Q = E W^T (1, 3) on mma.sync
-            const int gq = (tid & 31) >> 2, tq = tid & 3, nt8 = 8 * (warp >> 1);
-            const float(*Bm)[kRs] = (warp & 1) ? s.W : s.DO;
+            mma_commit(&sm.barP);
+        }
+        // phase 2, while the reads run (warp 0 issues them): warps 4-7 the Grams and the update's A
+        // operand, warps 1-3 b2 = (B E)^T; then every warp but warp 0 the next chunk's copies
+        if (role == 1) {
+            const int w4 = warp - 4, gq = (tid & 31) >> 2, tq = tid & 3, nt8 = 8 * (w4 >> 1);
+            const float(*Bm)[kRs] = (w4 & 1) ? s.W : s.DO;  // P = E dO^T (tasks 0, 2), Q = E W^T (1, 3)
             const bool ar0 = gq < nt, ar1 = gq + 8 < nt, bn = nt8 + gq < nt;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
             for (int kc = 0; kc < kD; kc += 8) {
                 const float2 x0 = ar0 ? *reinterpret_cast<const float2*>(&s.E[gq][kc + 2 * tq]) : make_float2(0.f, 0.f);
-                const float2 x1 = ar1 ? *reinterpret_cast<const float2*>(&s.E[gq + 8][kc + 2 * tq]) : make_float2(0.f, 0.f);
+                const float2 x1 =
+                    ar1 ? *reinterpret_cast<const float2*>(&s.E[gq + 8][kc + 2 * tq]) : make_float2(0.f, 0.f);
                 const float2 y = bn ? *reinterpret_cast<const float2*>(&Bm[nt8 + gq][kc + 2 * tq]) : make_float2(0.f, 0.f);
                 const float av[4] = {x0.x, x0.y, x1.x, x1.y};  // accumulator order: (g, 2t), (g, 2t+1), (g+8, ..)
                 const Frag4 a = afrag_acc(av);
@@ -1102,14 +1099,12 @@ k_bwd_rows_tc(const float* __restrict__ X, const float* __restrict__ g, const fl
                 split_tf32(y.y, b.h[1], b.l[1]);
                 mma3(acc, a, b);
             }
-            float(*G)[kCk] = (warp & 1) ? sm.Q[cc] : sm.P[cc];
+            float(*G)[kCk] = (w4 & 1) ? sm.Q[cc] : sm.P[cc];
             G[gq][nt8 + 2 * tq] = acc[0];
             G[gq][nt8 + 2 * tq + 1] = acc[1];
             G[gq + 8][nt8 + 2 * tq] = acc[2];
             G[gq + 8][nt8 + 2 * tq + 1] = acc[3];
-        }
-        if (role == 0) {  // A of the update: Kbar^T (lane = key, 16 tokens)
-            float hv[16], lv[16];
+            float hv[16], lv[16];  // A of the update: Kbar^T (lane = key, 16 tokens)
 #pragma unroll
             for (int t = 0; t < kCk; ++t) {
                 const float x = s.R1[t][key];
@@ -1118,7 +1113,26 @@ k_bwd_rows_tc(const float* __restrict__ X, const float* __restrict__ g, const fl
             }
             tst16(tl + 416, hv);
             tst16(tl + 448, lv);
+        } else if (warp > 0) {
+            for (int j = tid - 32; j < kD; j += 96) {  // row = value column j, K = token
+#pragma unroll
+                for (int m = 0; m < kCk; m += 4) {
+                    float x[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int t = m + e;
+                        x[e] = t < nt ? s.beta[t] * s.E[t][j] : 0.f;
+                    }
+                    float4 lo;
+                    const float4 hi = hi4(make_float4(x[0], x[1], x[2], x[3]), lo);
+                    const uint32_t off = kmaj(128, j, m);
+                    sts128(sm.b2h, off, hi);
+                    sts128(sm.b2l, off, lo);
+                }
+            }
         }
+        if (k + 1 < 2 * ncs) stage(k + 1);
+        cp_commit();
         // the key's decay factors over the chunk
         float C[kCk], Ca[kCk], Ki[kCk];
         {
@@ -1135,20 +1149,11 @@ k_bwd_rows_tc(const float* __restrict__ X, const float* __restrict__ g, const fl
                 Ki[t] = (t < nt ? s.k[t][key] : 0.f) * expf(G[7] - G[t]);
             }
         }
-        state_pass(s);
         sync_tc();
-        if (tid == 0 && !sm.fail) {
-            const uint32_t id32 = idesc_tf32(128, 32), id128 = idesc_tf32(128, 128);
-            const uint32_t h1 = smem_u32(sm.b1h), l1 = smem_u32(sm.b1l), h2 = smem_u32(sm.b2h), l2 = smem_u32(sm.b2l);
-#pragma unroll 1
-            for (int ks = 0; ks < kD / 8; ++ks) {  // [S do | S w]: A = S (high, low), B = [dO; W]
-                mma_tf32_ts(tm + 384, tm + 256 + 8 * ks, bdesc(h1, 32, ks), id32, ks > 0);
-                mma_tf32_ts(tm + 384, tm + 128 + 8 * ks, bdesc(l1, 32, ks), id32, 1);
-                mma_tf32_ts(tm + 384, tm + 128 + 8 * ks, bdesc(h1, 32, ks), id32, 1);
-            }
-            mma_commit(&sm.barP);
+        if (tid == 0 && !sm.fail) {  // S += Kbar^T (B E)
+            const uint32_t id128 = idesc_tf32(128, 128), h2 = smem_u32(sm.b2h), l2 = smem_u32(sm.b2l);
 #pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {  // S += Kbar^T (B E)
+            for (int ks = 0; ks < 2; ++ks) {
                 mma_tf32_ts(tm, tm + 448 + 8 * ks, bdesc(h2, 128, ks), id128, 1);
                 mma_tf32_ts(tm, tm + 416 + 8 * ks, bdesc(l2, 128, ks), id128, 1);
                 mma_tf32_ts(tm, tm + 416 + 8 * ks, bdesc(h2, 128, ks), id128, 1);
@@ -1258,9 +1263,8 @@ k_bwd_rows_tc(const float* __restrict__ X, const float* __restrict__ g, const fl
         fence_before_sync();
         __syncthreads();
         fence_after_sync();
-        if (k + 1 < 2 * ncs) stage(k + 1);
-        cp_commit();
-        // b1 = E (16 rows), K-major
+        // phase 1: the gradient's high part and remainder (then the decay); b1 = E (16 rows)
+        state_pass(s);
         for (int i4 = tid; i4 < 16 * 32; i4 += kRtThreads) {
             const int t = i4 >> 5, c4 = (i4 & 31) * 4;
             const float4 x = t < nt ? *reinterpret_cast<const float4*>(&s.E[t][c4]) : z4;
@@ -1270,34 +1274,52 @@ k_bwd_rows_tc(const float* __restrict__ X, const float* __restrict__ g, const fl
             sts128(sm.b1h, off, hi);
             sts128(sm.b1l, off, lo);
         }
-        {  // b2 = [scale dO; -B W]^T: row = value column j, K = 32 (tokens of dO, then of W)
-            const int j = tid & 127, half = tid >> 7;
+        sync_tc();
+        if (tid == 0 && !sm.fail) {  // D E^T: A = D (high, low), B = E
+            const uint32_t id16 = idesc_tf32(128, 16), h1 = smem_u32(sm.b1h), l1 = smem_u32(sm.b1l);
+#pragma unroll 1
+            for (int ks = 0; ks < kD / 8; ++ks) {
+                mma_tf32_ts(tm + 384, tm + 256 + 8 * ks, bdesc(h1, 16, ks), id16, ks > 0);
+                mma_tf32_ts(tm + 384, tm + 128 + 8 * ks, bdesc(l1, 16, ks), id16, 1);
+                mma_tf32_ts(tm + 384, tm + 128 + 8 * ks, bdesc(h1, 16, ks), id16, 1);
+            }
+            mma_commit(&sm.barP);
+        }
+        // phase 2, while D E^T runs: warps 4-7 the update's A operand [Qr | Kr]^T (lane = key,
+        // 32 tokens), warps 1-3 b2 = [scale dO; -B W]^T (row = value column, K = 32); the next copies
+        if (role == 1) {
 #pragma unroll
-            for (int m = 0; m < 16; m += 4) {
-                float x[4];
+            for (int half = 0; half < 2; ++half) {
+                float hv[16], lv[16];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int t = m + e;
-                    x[e] = t >= nt ? 0.f : half == 0 ? scale * s.DO[t][j] : -s.beta[t] * s.W[t][j];
+                for (int t = 0; t < kCk; ++t) {
+                    const float x = half == 0 ? s.R1[t][key] : s.R2[t][key];
+                    hv[t] = __uint_as_float(tf32_of(x));
+                    lv[t] = x - hv[t];
                 }
-                float4 lo;
-                const float4 hi = hi4(make_float4(x[0], x[1], x[2], x[3]), lo);
-                const uint32_t off = kmaj(128, j, 16 * half + m);
-                sts128(sm.b2h, off, hi);
-                sts128(sm.b2l, off, lo);
+                tst16(tl + 416 + 16 * half, hv);
+                tst16(tl + 448 + 16 * half, lv);
             }
-        }
-        {  // A of the update: [Qr | Kr]^T (lane = key, 32 tokens); role 0 the Qr half, role 1 the Kr half
-            float hv[16], lv[16];
+        } else if (warp > 0) {
+            for (int j = tid - 32; j < kD; j += 96) {
 #pragma unroll
-            for (int t = 0; t < kCk; ++t) {
-                const float x = role == 0 ? s.R1[t][key] : s.R2[t][key];
-                hv[t] = __uint_as_float(tf32_of(x));
-                lv[t] = x - hv[t];
+                for (int m = 0; m < 2 * kCk; m += 4) {
+                    float x[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int kk = m + e, t = kk & 15;
+                        x[e] = t >= nt ? 0.f : kk < kCk ? scale * s.DO[t][j] : -s.beta[t] * s.W[t][j];
+                    }
+                    float4 lo;
+                    const float4 hi = hi4(make_float4(x[0], x[1], x[2], x[3]), lo);
+                    const uint32_t off = kmaj(128, j, m);
+                    sts128(sm.b2h, off, hi);
+                    sts128(sm.b2l, off, lo);
+                }
             }
-            tst16(tl + 416 + 16 * role, hv);
-            tst16(tl + 448 + 16 * role, lv);
         }
+        if (k + 1 < 2 * ncs) stage(k + 1);
+        cp_commit();
         float CLr[kCk], iCa[kCk], Xa[kCk];  // C_last / C_t, 1 / C'_t, C'_t x_t (x = q for role 0, k for role 1)
         {
             float G[kCk], acc = 0.f;
@@ -1314,20 +1336,11 @@ k_bwd_rows_tc(const float* __restrict__ X, const float* __restrict__ g, const fl
                 Xa[t] = xv * expf(G[t] - G[7]);
             }
         }
-        state_pass(s);
         sync_tc();
-        if (tid == 0 && !sm.fail) {
-            const uint32_t id16 = idesc_tf32(128, 16), id128 = idesc_tf32(128, 128);
-            const uint32_t h1 = smem_u32(sm.b1h), l1 = smem_u32(sm.b1l), h2 = smem_u32(sm.b2h), l2 = smem_u32(sm.b2l);
-#pragma unroll 1
-            for (int ks = 0; ks < kD / 8; ++ks) {  // D E^T: A = D (high, low), B = E
-                mma_tf32_ts(tm + 384, tm + 256 + 8 * ks, bdesc(h1, 16, ks), id16, ks > 0);
-                mma_tf32_ts(tm + 384, tm + 128 + 8 * ks, bdesc(l1, 16, ks), id16, 1);
-                mma_tf32_ts(tm + 384, tm + 128 + 8 * ks, bdesc(h1, 16, ks), id16, 1);
-            }
-            mma_commit(&sm.barP);
+        if (tid == 0 && !sm.fail) {  // D += [Qr | Kr]^T [scale dO; -B W]
+            const uint32_t id128 = idesc_tf32(128, 128), h2 = smem_u32(sm.b2h), l2 = smem_u32(sm.b2l);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {  // D += [Qr | Kr]^T [scale dO; -B W]
+            for (int ks = 0; ks < 4; ++ks) {
                 mma_tf32_ts(tm, tm + 448 + 8 * ks, bdesc(h2, 128, ks), id128, 1);
                 mma_tf32_ts(tm, tm + 416 + 8 * ks, bdesc(l2, 128, ks), id128, 1);
                 mma_tf32_ts(tm, tm + 416 + 8 * ks, bdesc(h2, 128, ks), id128, 1);
