@@ -379,7 +379,7 @@ typedef struct {
 
 /* Bytes of workspace kda_backward needs (reads fwd.N, H, D, T_total and
  * fwd.cu_seqlens_host, which is required), each part rounded up to 256:
- *   36 T_total H D + 12 T_total H + 8 slots D^2 + 8 slots D
+ *   36 T_total H D + 8 T_total H + 8 slots D^2 + 8 slots D
  *   + 16 slots (49 D + 784) + 4 N H D + 8 (N + 1),
  * slots = H times the sum over sequences of ceil(len / 64): 6.6 GB for one
  * sequence of 8192 tokens with 96 heads. */

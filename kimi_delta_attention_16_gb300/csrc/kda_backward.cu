@@ -20,9 +20,9 @@
 //             kSeg-token segment                                              (2 CTAs per unit)
 //   epilogue  y = n w sig(z), n = o r:  do = r dn - r^3 o (dn . o) / D, dgate, drms_w  (warp per row)
 //   backward  the state gradient chunk by chunk, last chunk first: w_t = dS'^T k, dv = beta w,
-//             dbeta = w . e, e . do, and dS at the end of every segment        (2 CTAs per unit)
-//   rows      per (unit, segment), all in parallel, row layout (with e, w and do known, each row
-//             of S and of dS evolves on its own): dq, dk and dg (see k_bwd_rows)
+//             dbeta = w . e, and dS at the end of every segment               (2 CTAs per unit)
+//   rows      per (unit, segment), all in parallel, chunk by chunk on tcgen05 with keys as TMEM
+//             lanes (with e, w and do known): dq, dk and dg's pieces (see k_bwd_rows_tc)
 //   carry     dg's sums over later segments and the final-state term
 //   L2        da = (dx - x (x . dx)) / |a|, in place; dg += carry                 (warp per row)
 //   conv      du = da sig(u) (1 + u (1 - sig(u))); dx, the taps' and the conv state's gradients
@@ -130,11 +130,6 @@ __global__ void k_bwd_prep(const Tio* __restrict__ q, const Tio* __restrict__ k,
 // 16-byte and 4-byte asynchronous global -> shared copies (cp.async), one group per staged block.
 __device__ __forceinline__ void cp16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
-                 "l"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void cp4(void* dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
                  "l"(src)
                  : "memory");
 }
@@ -591,23 +586,22 @@ __device__ __forceinline__ void stage_bwd(BwdStage& st, const float* R, const fl
     }
 }
 
-// State-gradient sweep in chunks, last chunk first: w_t = dS'^T k^_t, dv = beta w, the sums
-// dbeta = w . e and e . do of every token (atomics over the CTAs of a unit), the state gradient at
+// State-gradient sweep in chunks, last chunk first: w_t = dS'^T k^_t, dv = beta w, the sum
+// dbeta = w . e of every token (atomics over the CTAs of a unit), the state gradient at
 // the end of every segment (dSck: before that token's own terms) and at the start (dS0).  Layout as
 // in k_bwd_fwd_chunks, with D = dS in place of S.
 __global__ void __launch_bounds__(128, 2)
 k_bwd_bwd_chunks(const float* __restrict__ Rec, const float* __restrict__ dO, const float* __restrict__ E,
                  const int32_t* __restrict__ cu, const int64_t* __restrict__ prefix, int64_t T_total, int H,
                  float scale, const float* __restrict__ dS_fin, float* __restrict__ W, float* __restrict__ dX,
-                 float* __restrict__ dbeta, float* __restrict__ edo, float* __restrict__ dSck,
-                 float* __restrict__ dS0, int64_t slots) {
+                 float* __restrict__ dbeta, float* __restrict__ dSck, float* __restrict__ dS0, int64_t slots) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     BwdStage* stg = reinterpret_cast<BwdStage*>(smem_raw);
-    __shared__ float acc[2][2][kCk];  // [chunk parity][dbeta, e.do][token]
+    __shared__ float acc[2][kCk];  // [chunk parity][token]: dbeta
     const int u = blockIdx.x / kChCtas, cq = blockIdx.x % kChCtas, n = u / H, h = u % H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
     const int cl = 16 * warp, cw = cq * kChCols + cl;
-    if (tid < 4 * kCk) (&acc[0][0][0])[tid] = 0.f;
+    if (tid < 2 * kCk) (&acc[0][0])[tid] = 0.f;
     int64_t s0, s1;
     seq_range(cu, n, T_total, s0, s1);
     const int64_t sb = slot_base(prefix, n, H, h, (s1 - s0 + kSeg - 1) / kSeg, slots);
@@ -658,10 +652,8 @@ k_bwd_bwd_chunks(const float* __restrict__ Rec, const float* __restrict__ dO, co
         if (c + 1 < nch && tid < nt_of(c + 1)) {
             const int p = (int)((c + 1) & 1);
             const int64_t t = s0 + (c + 1) * kCk + tid;
-            atomicAdd(dbeta + t * H + h, acc[p][0][tid]);
-            atomicAdd(edo + t * H + h, acc[p][1][tid]);
-            acc[p][0][tid] = 0.f;
-            acc[p][1][tid] = 0.f;
+            atomicAdd(dbeta + t * H + h, acc[p][tid]);
+            acc[p][tid] = 0.f;
         }
         if (c > 0) stage(c - 1);
         cp_commit();
@@ -724,21 +716,19 @@ k_bwd_bwd_chunks(const float* __restrict__ Rec, const float* __restrict__ dO, co
         mma3(w[0], ndv[0], bfrag_cols(&st.A0[0][0], kTc, 0, 0, gq, tq));
         mma3(w[0], ndv[1], bfrag_cols(&st.A0[0][0], kTc, 8, 0, gq, tq));
         mma3(w[1], ndv[1], bfrag_cols(&st.A0[0][0], kTc, 8, 8, gq, tq));
-        // stores and the per-token sums w . e, e . do over the warp's 16 columns
+        // stores and the per-token sums w . e over the warp's 16 columns
         {
-            float pb[2][2], pe[2][2];
+            float pb[2][2];
 #pragma unroll
             for (int j = 0; j < 2; ++j)
 #pragma unroll
                 for (int hlf = 0; hlf < 2; ++hlf) {
                     const int tk = 8 * j + 2 * tq + hlf;
-                    pb[j][hlf] = pe[j][hlf] = 0.f;
+                    pb[j][hlf] = 0.f;
                     if (tk < nt) {
                         const float e0 = st.E[tk][cl + gq], e1 = st.E[tk][cl + gq + 8];
-                        const float o0 = st.dO[tk][cl + gq], o1 = st.dO[tk][cl + gq + 8];
                         const float w0 = w[j][hlf], w1 = w[j][2 + hlf];
                         pb[j][hlf] = w0 * e0 + w1 * e1;
-                        pe[j][hlf] = e0 * o0 + e1 * o1;
                         const int64_t t = t0 + tk;
                         const int64_t off = (t * H + h) * kD + cw + gq;
                         W[off] = w0;
@@ -753,10 +743,7 @@ k_bwd_bwd_chunks(const float* __restrict__ Rec, const float* __restrict__ dO, co
 #pragma unroll
                 for (int hlf = 0; hlf < 2; ++hlf)
 #pragma unroll
-                    for (int off = 4; off < 32; off <<= 1) {
-                        pb[j][hlf] += __shfl_xor_sync(0xffffffffu, pb[j][hlf], off);
-                        pe[j][hlf] += __shfl_xor_sync(0xffffffffu, pe[j][hlf], off);
-                    }
+                    for (int off = 4; off < 32; off <<= 1) pb[j][hlf] += __shfl_xor_sync(0xffffffffu, pb[j][hlf], off);
             if (gq == 0) {
                 const int p = (int)(c & 1);
 #pragma unroll
@@ -764,10 +751,7 @@ k_bwd_bwd_chunks(const float* __restrict__ Rec, const float* __restrict__ dO, co
 #pragma unroll
                     for (int hlf = 0; hlf < 2; ++hlf) {
                         const int tk = 8 * j + 2 * tq + hlf;
-                        if (tk < nt) {
-                            atomicAdd(&acc[p][0][tk], pb[j][hlf]);
-                            atomicAdd(&acc[p][1][tk], pe[j][hlf]);
-                        }
+                        if (tk < nt) atomicAdd(&acc[p][tk], pb[j][hlf]);
                     }
             }
         }
@@ -789,8 +773,7 @@ k_bwd_bwd_chunks(const float* __restrict__ Rec, const float* __restrict__ dO, co
     __syncthreads();
     if (nch > 0 && tid < nt_of(0)) {
         const int64_t t = s0 + tid;
-        atomicAdd(dbeta + t * H + h, acc[0][0][tid]);
-        atomicAdd(edo + t * H + h, acc[0][1][tid]);
+        atomicAdd(dbeta + t * H + h, acc[0][tid]);
     }
     if (dS0) {
         float* S = dS0 + (int64_t)u * kD * kD + cw + gq;
@@ -898,8 +881,14 @@ __device__ __forceinline__ void tst16(uint32_t ta, const float (&v)[16]) {
 // (each token's forward and adjoint steps unrolled; checked against the token loop in fp64 before
 // it was written).  The products S_c [dO; W]^T (N = 32), D E^T (N = 16) and the two updates
 // (N = 128) run on tcgen05 (kind::tf32, hi/lo terms); keys are TMEM lanes.  8 warps: warps w and
-// w + 4 share lanes 32 (w % 4) ..; the per-token vector work is split between them.  dg's pieces
-// and the other outputs are the row kernel's.
+// w + 4 share lanes 32 (w % 4) ..; the per-token vector work is split between them.
+// dg follows from the decay entering only through e^{Gamma_t} (read keys and queries) and
+// e^{-Gamma_t} (written keys), Gamma_t = sum_{s <= t} g_s:
+//   dGamma_t = q^ dq + k^ dk_read - k^ dk_write,  dg_t = sum_{s >= t} dGamma_s + rowsum(dS_T . S_T);
+// here the parts within the segment: dg <- -(sum of q dq + k dk_read over earlier tokens), the global
+// rows of e and w (staged, so free) <- dk_write and the suffix sums of -k dk_write; per segment its sum
+// of dGamma (segtot) and of the read part (segown); for the last segment of a sequence the final-state
+// term (fin).
 constexpr int kRtThreads = 256;
 constexpr int kRs = kD + 4;  // row stride of the staged E, dO, W rows (conflict-free Gram reads)
 struct RtStage {
@@ -1085,7 +1074,7 @@ k_bwd_rows_tc(const float* __restrict__ X, const float* __restrict__ g, const fl
             const int w4 = warp - 4, gq = (tid & 31) >> 2, tq = tid & 3, nt8 = 8 * (w4 >> 1);
             const float(*Bm)[kRs] = (w4 & 1) ? s.W : s.DO;  // P = E dO^T (tasks 0, 2), Q = E W^T (1, 3)
             const bool ar0 = gq < nt, ar1 = gq + 8 < nt, bn = nt8 + gq < nt;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            float acc[4] = {0.f, 0.f, 0.f, 0.f}, accc[4] = {0.f, 0.f, 0.f, 0.f};  // high products, corrections
 #pragma unroll 4
             for (int kc = 0; kc < kD; kc += 8) {
                 const float2 x0 = ar0 ? *reinterpret_cast<const float2*>(&s.E[gq][kc + 2 * tq]) : make_float2(0.f, 0.f);
@@ -1097,13 +1086,13 @@ k_bwd_rows_tc(const float* __restrict__ X, const float* __restrict__ g, const fl
                 Frag2 b;
                 split_tf32(y.x, b.h[0], b.l[0]);
                 split_tf32(y.y, b.h[1], b.l[1]);
-                mma3(acc, a, b);
+                mma3x(acc, accc, a, b);
             }
             float(*G)[kCk] = (w4 & 1) ? sm.Q[cc] : sm.P[cc];
-            G[gq][nt8 + 2 * tq] = acc[0];
-            G[gq][nt8 + 2 * tq + 1] = acc[1];
-            G[gq + 8][nt8 + 2 * tq] = acc[2];
-            G[gq + 8][nt8 + 2 * tq + 1] = acc[3];
+            G[gq][nt8 + 2 * tq] = acc[0] + accc[0];
+            G[gq][nt8 + 2 * tq + 1] = acc[1] + accc[1];
+            G[gq + 8][nt8 + 2 * tq] = acc[2] + accc[2];
+            G[gq + 8][nt8 + 2 * tq + 1] = acc[3] + accc[3];
             float hv[16], lv[16];  // A of the update: Kbar^T (lane = key, 16 tokens)
 #pragma unroll
             for (int t = 0; t < kCk; ++t) {
@@ -1190,26 +1179,28 @@ k_bwd_rows_tc(const float* __restrict__ X, const float* __restrict__ g, const fl
                 }
             }
         }
+        float* dxr = dX + t0 * 3 * HD + role * HD + (int64_t)h * kD + key;  // dq (role 0) / dk_read rows
         if (role == 0) {  // dq
 #pragma unroll
-            for (int t = 0; t < kCk; ++t) {
+            for (int t = 0; t < kCk; ++t, dxr += 3 * HD) {
                 const float dq = scale * (C[t] * z[t] + Ca[t] * acc[t]);
                 cq[t] = t < nt ? s.q[t][key] * dq : 0.f;
-                if (t < nt) dX[(t0 + t) * 3 * HD + (int64_t)h * kD + key] = dq;
+                if (t < nt) *dxr = dq;
             }
         } else {  // dk_read
 #pragma unroll
-            for (int t = 0; t < kCk; ++t) {
+            for (int t = 0; t < kCk; ++t, dxr += 3 * HD) {
                 const float dkr = -s.beta[t] * (C[t] * z[t] + Ca[t] * acc[t]);
                 sm.xch[t][key] = t < nt ? s.k[t][key] * dkr : 0.f;
-                if (t < nt) dX[(t0 + t) * 3 * HD + HD + (int64_t)h * kD + key] = dkr;
+                if (t < nt) *dxr = dkr;
             }
         }
         __syncthreads();
         if (role == 0) {
+            float* dgr = dg + (t0 * H + h) * kD + key;
 #pragma unroll
-            for (int t = 0; t < kCk; ++t) {
-                if (t < nt) dg[((t0 + t) * H + h) * kD + key] = -(pre_q + pre_k);  // minus the earlier read part
+            for (int t = 0; t < kCk; ++t, dgr += HD) {
+                if (t < nt) *dgr = -(pre_q + pre_k);  // minus the earlier read part
                 pre_q += cq[t];
                 pre_k += sm.xch[t][key];
             }
@@ -1387,14 +1378,14 @@ k_bwd_rows_tc(const float* __restrict__ X, const float* __restrict__ g, const fl
         }
         __syncthreads();
         if (role == 0) {  // dk_write; its global E row and the suffix sum of -k dk_write in the W row
+            const int64_t off0 = (t0 * H + h) * kD + key;
 #pragma unroll
             for (int t = kCk - 1; t >= 0; --t) {
                 if (t >= nt) continue;
                 const float dkw = s.beta[t] * (x0[t] + sm.xch[t][key]);
                 run -= s.k[t][key] * dkw;
-                const int64_t off = ((t0 + t) * H + h) * kD + key;
-                E[off] = dkw;
-                W[off] = run;
+                E[off0 + t * HD] = dkw;
+                W[off0 + t * HD] = run;
             }
         }
     }
@@ -1413,276 +1404,6 @@ k_bwd_rows_tc(const float* __restrict__ X, const float* __restrict__ g, const fl
     if (warp == 0) {
         tmem_dealloc(tm, 512);
         tmem_relinquish();
-    }
-}
-
-// ------------------------------------------------------------------------------ row-layout segments
-// One CTA of 256 threads per (unit, segment): thread (rg, cg) owns rows 8 rg .. 8 rg + 7 and columns
-// 8 cg .. 8 cg + 7 (packed fp32 pairs); the row sums a token needs (S x, dS' e) go over the 16
-// column groups of a half-warp.  With e, w and do known for every token, both sweeps are row-local:
-//   forward from the segment's start state:  dq = scale (P do + beta k (e . do)),
-//                                            dk_read = -beta P w,   P = Diag(alpha) S_{t-1};
-//   backward from the segment's end gradient: dk_write = beta dS' e.
-// dg follows from the decay entering only through e^{Gamma_t} (read keys and queries) and
-// e^{-Gamma_t} (written keys), Gamma_t = sum_{s <= t} g_s:
-//   dGamma_t = q^ dq + k^ dk_read - k^ dk_write,  dg_t = sum_{s >= t} dGamma_s + rowsum(dS_T . S_T);
-// here the parts within the segment: dg <- -(sum of q dq + k dk_read over earlier tokens), the
-// global rows of e and w (staged, so free) <- dk_write and the suffix sums of -k dk_write; per
-// segment its sum of dGamma (segtot) and of the read part (segown); for the last segment of a
-// sequence the final-state term (fin).  The sweeps only write global memory.
-constexpr int kRowThreads = 256;
-constexpr int kColVec = kD + 12;  // column vectors skewed by 4 floats every 32, so that the eight
-                                  // column groups a quarter-warp reads fall in distinct banks
-struct RowTok {
-    float k[kD], a[kD], q[kD];
-    float e[kColVec], d[kColVec], w[kColVec];
-    float beta, edo, pad[2];
-};
-constexpr int kRowSmem = kSeg * (int)sizeof(RowTok);
-
-// Sums 16 per-thread values over the 16 lanes of a half-warp (lane bits 0..3); afterwards lane
-// cg holds the total of value cg.
-__device__ __forceinline__ float reduce16_16(float (&v)[16], int cg) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const bool up = (cg & 8) != 0;
-        const float send = up ? v[i] : v[i + 8];
-        v[i] = (up ? v[i + 8] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const bool up = (cg & 4) != 0;
-        const float send = up ? v[i] : v[i + 4];
-        v[i] = (up ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const bool up = (cg & 2) != 0;
-        const float send = up ? v[i] : v[i + 2];
-        v[i] = (up ? v[i + 2] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 2);
-    }
-    const bool up = (cg & 1) != 0;
-    const float send = up ? v[0] : v[1];
-    return (up ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, send, 1);
-}
-__device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
-    const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-__device__ __forceinline__ float pick8(const float (&x)[8], int a) {  // x[a] without local memory
-    float r = x[0];
-#pragma unroll
-    for (int i = 1; i < 8; ++i) r = a == i ? x[i] : r;
-    return r;
-}
-// Same for 8 values; afterwards lanes cg hold the total of value cg >> 1.
-__device__ __forceinline__ float reduce8_16(float (&v)[8], int cg) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const bool up = (cg & 8) != 0;
-        const float send = up ? v[i] : v[i + 4];
-        v[i] = (up ? v[i + 4] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const bool up = (cg & 4) != 0;
-        const float send = up ? v[i] : v[i + 2];
-        v[i] = (up ? v[i + 2] : v[i]) + __shfl_xor_sync(0xffffffffu, send, 4);
-    }
-    {
-        const bool up = (cg & 2) != 0;
-        const float send = up ? v[0] : v[1];
-        v[0] = (up ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, send, 2);
-    }
-    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
-}
-
-__device__ __forceinline__ void load8p(const float* p, f2 (&x)[4]) {  // 8 floats as 4 pairs
-    const ulonglong2 a = reinterpret_cast<const ulonglong2*>(p)[0], b = reinterpret_cast<const ulonglong2*>(p)[1];
-    x[0].v = a.x;
-    x[1].v = a.y;
-    x[2].v = b.x;
-    x[3].v = b.y;
-}
-__device__ __forceinline__ float hsum(f2 x) { return f2_lo(x) + f2_hi(x); }
-
-// Grid: units x max_seg CTAs (CTAs past a sequence's segment count return at once).
-__global__ void __launch_bounds__(kRowThreads, 1)
-k_bwd_rows(const float* __restrict__ X, const float* __restrict__ g, const float* __restrict__ beta,
-           const float* __restrict__ dO, float* __restrict__ E, float* __restrict__ W,
-           const float* __restrict__ edo, const int32_t* __restrict__ cu, const int64_t* __restrict__ prefix,
-           int64_t T_total, int H, float scale, int max_seg, const float* __restrict__ Sck,
-           const float* __restrict__ dSck, const float* __restrict__ dS_fin, float* __restrict__ dX,
-           float* __restrict__ dg, float* __restrict__ segtot, float* __restrict__ segown, float* __restrict__ fin,
-           int64_t slots) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    RowTok* st = reinterpret_cast<RowTok*>(smem_raw);  // [kSeg]
-    const int u = blockIdx.x / max_seg, sg = blockIdx.x % max_seg, n = u / H, h = u % H;
-    const int tid = threadIdx.x, rg = tid >> 4, cg = tid & 15;
-    int64_t s0, s1;
-    seq_range(cu, n, T_total, s0, s1);
-    const int64_t nseg = (s1 - s0 + kSeg - 1) / kSeg;
-    if (sg >= nseg) return;
-    const int64_t sb = slot_base(prefix, n, H, h, nseg, slots);
-    if (sb < 0) return;  // flagged by the forward sweep
-    const int64_t HD = (int64_t)H * kD;
-    const int64_t ta = s0 + (int64_t)sg * kSeg, tb = ta + kSeg < s1 ? ta + kSeg : s1;
-    const int nt = (int)(tb - ta);
-    // stage the segment: six 128-vectors (32 chunks each), beta and e . do per token
-    for (int idx = tid; idx < nt * 194; idx += kRowThreads) {
-        const int tk = idx / 194, j = idx - tk * 194;
-        const int64_t t = ta + tk, th = t * H + h;
-        RowTok& s = st[tk];
-        if (j < 192) {
-            const int part = j >> 5, jj = j & 31;
-            const float* src = part == 0 ? X + t * 3 * HD + HD + (int64_t)h * kD
-                             : part == 1 ? g + th * kD
-                             : part == 2 ? X + t * 3 * HD + (int64_t)h * kD
-                             : part == 3 ? E + th * kD
-                             : part == 4 ? dO + th * kD
-                                         : W + th * kD;
-            float* dst = part == 0 ? s.k : part == 1 ? s.a : part == 2 ? s.q : part == 3 ? s.e : part == 4 ? s.d : s.w;
-            cp16(dst + 4 * jj + (part >= 3 ? (jj >> 3) * 4 : 0), src + 4 * jj);
-        } else {
-            cp4(j == 192 ? &s.beta : &s.edo, (j == 192 ? beta : edo) + th);
-        }
-    }
-    cp_commit();
-    cp_wait<0>();
-    __syncthreads();
-    for (int idx = tid; idx < nt * kD; idx += kRowThreads) {
-        float& x = st[idx >> 7].a[idx & 127];
-        x = expf(x);
-    }
-    __syncthreads();
-    const int r0 = 8 * rg, cs = 8 * cg + (cg >> 2) * 4;  // first row; column offset in a skewed vector
-    const bool writer = (cg & 1) == 0;                  // lanes holding row r0 + (cg >> 1)
-    const int ra = cg >> 1;
-    // ---- forward: S from the segment's start state
-    float pre = 0.f;  // writer lanes: sum over this segment's earlier tokens of q dq + k dk_read
-    f2 s[8][4];
-    {
-        const float* src = Sck + (sb + sg) * kD * kD + 8 * cg;
-#pragma unroll
-        for (int a = 0; a < 8; ++a) load8p(src + (r0 + a) * kD, s[a]);
-    }
-    for (int tk = 0; tk < nt; ++tk) {
-        const RowTok& T = st[tk];
-        f2 e2[4], d2[4], w2[4];
-        load8p(T.e + cs, e2);
-        load8p(T.d + cs, d2);
-        load8p(T.w + cs, w2);
-        float kr[8], ar[8];
-        load8(T.k + r0, kr);
-        load8(T.a + r0, ar);
-        float v[16];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) {
-            f2 x0 = mul2(s[a][0], d2[0]), x1 = mul2(s[a][0], w2[0]);
-#pragma unroll
-            for (int p = 1; p < 4; ++p) {
-                x0 = fma2(s[a][p], d2[p], x0);
-                x1 = fma2(s[a][p], w2[p], x1);
-            }
-            v[2 * a] = hsum(x0);
-            v[2 * a + 1] = hsum(x1);
-        }
-        const float red = reduce16_16(v, cg);  // lane cg: value cg (row cg >> 1; S do if even, S w if odd)
-        const float sw = __shfl_xor_sync(0xffffffffu, red, 1);
-        const float bt = T.beta;
-        {  // computed on every lane, stored by the writer lanes
-            const int i = r0 + ra;
-            const float al = pick8(ar, ra), ki = pick8(kr, ra);
-            const float dq = scale * (al * red + bt * ki * T.edo);
-            const float dkr = -bt * al * sw;
-            const int64_t t = ta + tk;
-            if (writer) {
-                dX[t * 3 * HD + (int64_t)h * kD + i] = dq;
-                dX[t * 3 * HD + HD + (int64_t)h * kD + i] = dkr;
-                dg[(t * H + h) * kD + i] = -pre;  // minus the sum of dGamma_read over earlier tokens
-            }
-            pre += T.q[i] * dq + ki * dkr;
-        }
-#pragma unroll
-        for (int a = 0; a < 8; ++a) {
-            const f2 a2 = f2_dup(ar[a]), bk2 = f2_dup(bt * kr[a]);
-#pragma unroll
-            for (int p = 0; p < 4; ++p) s[a][p] = fma2(bk2, e2[p], mul2(a2, s[a][p]));
-        }
-    }
-    if (tb == s1) {  // the sequence's final state: rowsum(dS_T . S_T)
-        float f[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) {
-            float x = 0.f;
-            if (dS_fin) {
-                f2 d2[4];
-                load8p(dS_fin + ((int64_t)u * kD + r0 + a) * kD + 8 * cg, d2);
-                f2 y = mul2(d2[0], s[a][0]);
-#pragma unroll
-                for (int p = 1; p < 4; ++p) y = fma2(d2[p], s[a][p], y);
-                x = hsum(y);
-            }
-            f[a] = x;
-        }
-        const float tot = reduce8_16(f, cg);
-        if (writer) fin[(int64_t)u * kD + r0 + ra] = tot;
-    }
-    // ---- backward: dS from the segment's end gradient
-    f2 (&ds)[8][4] = s;
-    {
-        const float* src = dSck + (sb + sg) * kD * kD + 8 * cg;
-#pragma unroll
-        for (int a = 0; a < 8; ++a) load8p(src + (r0 + a) * kD, ds[a]);
-    }
-    float run = 0.f;  // writer lanes: sum over this segment's tokens >= t of -k dk_write
-    for (int tk = nt - 1; tk >= 0; --tk) {
-        const RowTok& T = st[tk];
-        f2 e2[4], d2[4], w2[4];
-        load8p(T.e + cs, e2);
-        load8p(T.d + cs, d2);
-        load8p(T.w + cs, w2);
-        float kr[8], ar[8], qr[8];
-        load8(T.k + r0, kr);
-        load8(T.a + r0, ar);
-        load8(T.q + r0, qr);
-        const float bt = T.beta;
-        float y[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) {
-            const f2 sq2 = f2_dup(scale * qr[a]);
-            ds[a][0] = fma2(sq2, d2[0], ds[a][0]);
-            f2 x = mul2(ds[a][0], e2[0]);
-#pragma unroll
-            for (int p = 1; p < 4; ++p) {
-                ds[a][p] = fma2(sq2, d2[p], ds[a][p]);
-                x = fma2(ds[a][p], e2[p], x);
-            }
-            y[a] = hsum(x);
-        }
-        const float dse = reduce8_16(y, cg);  // (dS'_t e_t) of row cg >> 1
-        {  // the token's e and w rows are staged, so their global rows take dk_write and the suffix
-           // sums of -k dk_write (combined by the L2 kernel); stored by the writer lanes
-            const int i = r0 + ra;
-            const int64_t th = (ta + tk) * H + h;
-            const float dkw = bt * dse;
-            run -= pick8(kr, ra) * dkw;
-            if (writer) {
-                E[th * kD + i] = dkw;
-                W[th * kD + i] = run;
-            }
-        }
-#pragma unroll
-        for (int a = 0; a < 8; ++a) {
-            const f2 a2 = f2_dup(ar[a]), nbk2 = f2_dup(-bt * kr[a]);
-#pragma unroll
-            for (int p = 0; p < 4; ++p) ds[a][p] = mul2(a2, fma2(nbk2, w2[p], ds[a][p]));
-        }
-    }
-    if (writer) {
-        segtot[(sb + sg) * kD + r0 + ra] = pre + run;  // the segment's sum of dGamma
-        segown[(sb + sg) * kD + r0 + ra] = pre;        // added to its own tokens (dg = -pre_t + run_t + ...)
     }
 }
 
@@ -1931,7 +1652,6 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
     float* dX = reinterpret_cast<float*>(ws + L.dx);
     float* E = reinterpret_cast<float*>(ws + L.e);
     float* W = reinterpret_cast<float*>(ws + L.w);
-    float* edo = reinterpret_cast<float*>(ws + L.edo);
     float* Sck = reinterpret_cast<float*>(ws + L.sck);
     float* dSck = reinterpret_cast<float*>(ws + L.dsck);
     float* segtot = reinterpret_cast<float*>(ws + L.segtot);
@@ -1946,7 +1666,6 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
         return e;
     if (rows > 0) {
         if ((e = cudaMemsetAsync(b.dbeta, 0, sizeof(float) * rows, s))) return e;
-        if ((e = cudaMemsetAsync(edo, 0, sizeof(float) * rows, s))) return e;
     }
     k_bwd_seg_prefix<<<1, 256, 0, s>>>(a.cu_seqlens, a.N, T, prefix);
     if ((e = cudaGetLastError())) return e;
@@ -1956,7 +1675,6 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
                                           cptr<Tio>(a.conv_state_in), a.cu_seqlens, a.N, T, a.H, a.eps_l2, X, nrm);
         if ((e = cudaGetLastError())) return e;
     }
-    if ((e = cudaFuncSetAttribute(k_bwd_rows, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowSmem))) return e;
     float* Rec = reinterpret_cast<float*>(ws + L.rec);
     if (rows > 0 && L.max_ch > 0) {
         k_bwd_chunk_prep<<<(unsigned)(units * L.max_ch), 128, 0, s>>>(X, a.g, a.beta, a.cu_seqlens, prefix, T, a.H,
@@ -1981,7 +1699,7 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
     }
     k_bwd_bwd_chunks<<<(unsigned)(units * kChCtas), 128, kBwdSmem, s>>>(Rec, O, E, a.cu_seqlens, prefix, T, a.H,
                                                                         a.scale, b.d_final_state, W, dX, b.dbeta,
-                                                                        edo, dSck, b.dinitial_state, L.slots);
+                                                                        dSck, b.dinitial_state, L.slots);
     if ((e = cudaGetLastError())) return e;
     if (rows == 0) return cudaSuccess;
     if ((e = cudaFuncSetAttribute(k_bwd_rows_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kRowsTcSmem))) return e;
@@ -2031,7 +1749,6 @@ BackwardLayout backward_layout(const kda_backward_args& b) {
     L.dx = take(T * 3 * HD * 4);
     L.e = take(T * HD * 4);
     L.w = take(T * HD * 4);
-    L.edo = take(T * H * 4);
     L.slots = (int64_t)(segs * H);
     L.max_seg = (int64_t)max_seg;
     L.max_ch = (int64_t)max_ch;

@@ -224,7 +224,6 @@ struct BackwardLayout {
     size_t dx;       // [T][3][H][D] fp32: gradients of q^, k^, v, then of the conv outputs
     size_t e;        // [T][H][D] fp32: e_t = v_t - P_t^T k_t, then dk_write
     size_t w;        // [T][H][D] fp32: w_t = dS'_t^T k_t, then the write part of dg
-    size_t edo;      // [T][H] fp32: e_t . do_t
     size_t sck;      // [slots][D][D] fp32: the state at the start of every segment
     size_t dsck;     // [slots][D][D] fp32: the state gradient at the end of every segment
     size_t segtot;   // [slots][D] fp32: dg sums per segment, then the carries

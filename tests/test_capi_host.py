@@ -324,7 +324,7 @@ def test_backward_rejects_bad_arguments(field, value, code):
 
 
 def test_backward_workspace_size_matches_the_stated_layout():
-    """36 T H D + 12 T H + 8 slots D^2 + 8 slots D + 16 slots (49 D + 784) + 4 N H D + 8 (N + 1)
+    """36 T H D + 8 T H + 8 slots D^2 + 8 slots D + 16 slots (49 D + 784) + 4 N H D + 8 (N + 1)
     bytes, each part rounded up to 256 (in the header's order), slots = H * sum over sequences of
     ceil(len / 64)."""
     lib = _lib.load()
@@ -338,7 +338,7 @@ def test_backward_workspace_size_matches_the_stated_layout():
         T, D, N = int(cu[-1]), 128, len(lengths)
         slots = H * sum((L + 63) // 64 for L in lengths)
         want = (r(T * 3 * H * D * 4) + r(T * H * 2 * 4) + r(T * H * D * 4) + r(T * 3 * H * D * 4)
-                + r(T * H * D * 4) + r(T * H * D * 4) + r(T * H * 4)
+                + r(T * H * D * 4) + r(T * H * D * 4)
                 + 2 * r(slots * D * D * 4) + 2 * r(slots * D * 4) + r(16 * slots * (49 * D + 784))
                 + r(N * H * D * 4) + r((N + 1) * 8))
         assert n.value == want, (lengths, H)
