@@ -562,6 +562,7 @@ def time_projected_layer(args, pg, dev, stream, peaks, peak_src, world, d_model=
 
 
 FP32_SIMT_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # 152 SMs x 128 fp32 lanes x FMA x 2.07 GHz max clock
+TF32_PER_BF16 = 1.1 / 2.25                            # nominal dense TF32 / bf16 tensor rates
 BWD_FLOP_PER_TOKEN_HEAD = 28 * 128 * 128              # token-serial adjoint, counted in the design doc
 
 
@@ -603,14 +604,18 @@ def time_backward(args, pg, dev, stream, peaks, peak_src, world):
     ms = max_over_ranks(pg, e0.elapsed_time(e1) / steps, dev)
     flops = BWD_FLOP_PER_TOKEN_HEAD * T * H
     tf = flops / (ms / 1e3) / 1e12
+    # the recurrence products run on the tensor cores as TF32 (three hi/lo terms each): the peak of
+    # that dtype is the measured bf16 peak times the nominal dense TF32 / bf16 ratio (1.1 / 2.25)
+    tf32_peak = peaks["bf16_tflops"] * TF32_PER_BF16
     obj = {"metric": f"KDA backward tokens/s (layer_8k: T={T}, H=96, d=128; all input gradients)",
            "value": round(aggregate_rate(world, T, ms), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
            "steps": steps, "workspace_bytes": ws.numel(),
-           "roofline": {"kernel": "the whole kda_backward call (fp32 SIMT row sweeps and 3-term TF32 "
-                                  "mma.sync chunk sweeps dominate)",
-                        "bound": "alu", "achieved": round(tf, 2), "peak": round(FP32_SIMT_TFLOPS, 1),
-                        "unit": "TFLOP/s", "frac": round(tf / FP32_SIMT_TFLOPS, 4),
-                        "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 x 2.07 GHz",
+           "roofline": {"kernel": "the whole kda_backward call (TF32 tcgen05 row sweeps and mma.sync chunk "
+                                  "sweeps dominate, 3 hi/lo terms per product)",
+                        "bound": "tensor", "achieved": round(tf, 2), "peak": round(tf32_peak, 1),
+                        "unit": "TFLOP/s", "frac": round(tf / tf32_peak, 4),
+                        "peak_source": f"{peak_src} bf16 x 1.1/2.25 (nominal dense TF32 / bf16)",
+                        "fp32_simt_frac": round(tf / FP32_SIMT_TFLOPS, 4),
                         "traffic": None, "algorithmic_flops": flops}}
     del inp, dy, dsf, ws
     torch.cuda.empty_cache()
