@@ -63,18 +63,30 @@ __device__ __forceinline__ void load4(const float* p, float (&x)[4]) {
 // ------------------------------------------------------------------------------ prep
 // One warp per (token, head): conv + SiLU of the q, k, v channels of the head (lane l: channels
 // 4 l .. 4 l + 3), the L2 norms of q and k.  X: [T][3][H][D] fp32 (q^, k^, v), nrm: [T][H][2].
-// Grid: ceil(T / 8) x H blocks of 8 warps.
+// Grid: ceil(T / 8) x H blocks of 8 warps taking consecutive tokens of one head.
 template <typename Tio>
 __global__ void k_bwd_prep(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __restrict__ v,
                            int64_t xs, const float* __restrict__ conv_w, const Tio* __restrict__ cs_in,
                            const int32_t* __restrict__ cu, int N, int64_t T_total, int H, float eps_l2,
                            float* __restrict__ X, float* __restrict__ nrm) {
-    // the warps of a block take consecutive tokens of one head, so that the head's conv taps and
+    // the warps of a block take consecutive tokens of one head: the head's conv taps are staged in
+    // shared memory once per block (tap-major, so that a lane's four channels are one float4), and
     // the overlapping input windows are served from L1
+    __shared__ __align__(16) float wt[3][4][kD];  // [part][tap][channel]
     const int wpb = blockDim.x / 32;
     const int h = (int)(blockIdx.x % H);
     const int64_t t = (int64_t)(blockIdx.x / H) * wpb + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    const int64_t HD = (int64_t)H * kD;
+    for (int i = threadIdx.x; i < 3 * kD; i += blockDim.x) {
+        const int part = i / kD, ch = i - part * kD;
+        const float4 w4 = *reinterpret_cast<const float4*>(conv_w + ((int64_t)part * HD + (int64_t)h * kD + ch) * 4);
+        wt[part][0][ch] = w4.x;
+        wt[part][1][ch] = w4.y;
+        wt[part][2][ch] = w4.z;
+        wt[part][3][ch] = w4.w;
+    }
+    __syncthreads();
     if (t >= T_total) return;
     const int64_t row = t * H + h;
     // the sequence of token t (binary search over cu_seqlens)
@@ -87,7 +99,6 @@ __global__ void k_bwd_prep(const Tio* __restrict__ q, const Tio* __restrict__ k,
     const int n = lo;
     int64_t s0 = cu[n];
     s0 = s0 < 0 ? 0 : (s0 > t ? t : s0);  // keeps every index in bounds if cu is inconsistent
-    const int64_t HD = (int64_t)H * kD;
     const Tio* src[3] = {q, k, v};
     float out[3][4];
     float ss[2] = {0.f, 0.f};
@@ -109,11 +120,18 @@ __global__ void k_bwd_prep(const Tio* __restrict__ q, const Tio* __restrict__ k,
                 }
             }
         }
+        float w[4][4];  // [tap][channel m]
+#pragma unroll
+        for (int tap = 0; tap < 4; ++tap) {
+            const float4 w4 = *reinterpret_cast<const float4*>(&wt[part][tap][4 * lane]);
+            w[tap][0] = w4.x;
+            w[tap][1] = w4.y;
+            w[tap][2] = w4.z;
+            w[tap][3] = w4.w;
+        }
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            const int64_t ch = (int64_t)part * HD + (int64_t)h * kD + 4 * lane + m;
-            const float4 w = *reinterpret_cast<const float4*>(conv_w + ch * 4);
-            const float u = w.x * x[0][m] + w.y * x[1][m] + w.z * x[2][m] + w.w * x[3][m];
+            const float u = w[0][m] * x[0][m] + w[1][m] * x[1][m] + w[2][m] * x[2][m] + w[3][m] * x[3][m];
             out[part][m] = u / (1.0f + expf(-u));
             if (part < 2) ss[part] += out[part][m] * out[part][m];
         }
