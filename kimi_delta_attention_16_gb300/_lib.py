@@ -26,7 +26,7 @@ KDA_PATH_SIMT, KDA_PATH_TENSOR_CORE, KDA_PATH_RECURRENT = 0, 1, 2
 KDA_RECURRENT_MAX_LEN = 8
 KDA_MAX_SEGMENTS = 16
 KDA_EPI_NONE, KDA_EPI_DECAY, KDA_EPI_SIGMOID = 0, 1, 2
-ABI_VERSION = 10400  # kda_backward
+ABI_VERSION = 10401  # kda_backward with chunk records in its workspace
 
 # Every symbol include/kda.h declares.
 EXPORTED = ("kda_status_string", "kda_last_error", "kda_version", "kda_short_conv",

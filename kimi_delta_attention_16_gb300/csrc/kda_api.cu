@@ -220,7 +220,7 @@ const char* kda_status_string(int status) {
 
 const char* kda_last_error(void) { return g_last_error.c_str(); }
 
-int kda_version(void) { return 1 * 10000 + 4 * 100 + 0; }
+int kda_version(void) { return 1 * 10000 + 4 * 100 + 1; }
 
 kda_status kda_short_conv(const void* x, int64_t x_row_stride, const float* w,
                           const int32_t* cu_seqlens, const int32_t* cu_seqlens_host, int N,
