@@ -349,11 +349,11 @@ kda_status kda_gemm(const kda_gemm_args* args, kda_stream_t stream);
  * the state at the start of every 64-token segment; the epilogue's derivative
  * per row; the state gradient run backwards chunk by chunk, saving
  * w_t = dS^T k_t and the gradient at the end of every segment; then every
- * segment in parallel, by row (with e and w known, each row of S and of dS
- * evolves on its own): dq, dk and the log-decay's gradient, which follows from
- * g entering only through the decayed read keys and queries and the un-decayed
- * written keys; last the L2 norm's, SiLU's and the conv's derivatives.  No
- * per-token state is stored.
+ * segment in parallel, chunk by chunk from its two checkpoints (with e and w
+ * known): dq, dk and the log-decay's gradient, which follows from g entering
+ * only through the decayed read keys and queries and the un-decayed written
+ * keys; last the L2 norm's, SiLU's and the conv's derivatives.  No per-token
+ * state is stored.
  *
  * Needs cu_seqlens_host (the checkpoint layout is planned on the host).  The
  * outputs must not overlap each other or any input.  dconv_w and drms_w are
