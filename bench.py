@@ -563,7 +563,7 @@ def time_projected_layer(args, pg, dev, stream, peaks, peak_src, world, d_model=
 
 FP32_SIMT_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # 152 SMs x 128 fp32 lanes x FMA x 2.07 GHz max clock
 TF32_PER_BF16 = 1.1 / 2.25                            # nominal dense TF32 / bf16 tensor rates
-BWD_FLOP_PER_TOKEN_HEAD = 28 * 128 * 128              # token-serial adjoint, counted in the design doc
+BWD_FLOP_PER_TOKEN_HEAD = 28 * 128 * 128              # four token-serial sweeps of the state, 7 d^2 each
 
 
 def time_backward(args, pg, dev, stream, peaks, peak_src, world):
