@@ -4,8 +4,9 @@ The oracle's backward is pinned to central differences of the fp64 forward (see 
 tests); here every gradient the library returns is compared with it on the same seeded inputs.
 
 Tolerance.  The library recomputes the forward and runs its adjoint in fp32 (IEEE exp, SiLU
-and sigmoid; bf16 inputs are exact in fp32), so the errors are fp32 roundoff carried through
-the recurrence.  Each step is a contraction of the state and of its adjoint (0 < e^g <= 1,
+and sigmoid; bf16 inputs are exact in fp32; the chunk products on the tensor cores as three TF32
+terms of hi/lo splits, about 2^-21 relative per product), so the errors are fp32-level roundoff
+carried through the recurrence.  Each step is a contraction of the state and of its adjoint (0 < e^g <= 1,
 |k| = 1 after the L2 norm, 0 <= beta <= 1), so roundoff does not grow from step to step; it
 accumulates over the D = 128 terms of each dot product and over the tokens of a sequence.
 With the fp32 unit roundoff 6e-8 and a few hundred tokens that is ~1e-6 of the tensor's scale
@@ -91,6 +92,14 @@ def test_backward_parity_varlen_all_inputs(io):
     1-token and an empty sequence), every optional input given: gate, RMSNorm weight, initial
     state, conv state, dS_fin."""
     inp, dy, dsf = _case(io, [70, 1, 0, 33, 130], seed=11)
+    _check(_gpu_backward(inp, dy, dsf), _oracle_backward(inp, dy, dsf))
+
+
+def test_backward_parity_chunk_and_segment_boundaries():
+    """Lengths on either side of every 16-token chunk and 64-token checkpoint segment boundary in
+    one batch: partial last chunks, segments of one to four chunks, a segment of a single token."""
+    lengths = [15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 193]
+    inp, dy, dsf = _case("bf16", lengths, seed=61)
     _check(_gpu_backward(inp, dy, dsf), _oracle_backward(inp, dy, dsf))
 
 
