@@ -1447,8 +1447,10 @@ __global__ void k_bwd_dg_carry(const int32_t* __restrict__ cu, const int64_t* __
 }
 
 // ------------------------------------------------------------------------------ epilogue backward
-// One warp per (token, head) row: do (written over o), dgate, and the RMSNorm weight's gradient
-// (block partials in shared memory, one atomic per channel and block).
+constexpr int kEpiRows = 2;  // rows per warp
+// Each warp takes kEpiRows consecutive (token, head) rows, all their loads issued first: do (written
+// over o), dgate, and the RMSNorm weight's gradient (block partials in shared memory, one atomic per
+// channel and block).
 template <typename Tg, typename Tdy>
 __global__ void k_bwd_epilogue(float* __restrict__ O, const Tdy* __restrict__ dy, const Tg* __restrict__ gate,
                                const float* __restrict__ rms_w, float eps_rms, int64_t rows,
@@ -1456,41 +1458,55 @@ __global__ void k_bwd_epilogue(float* __restrict__ O, const Tdy* __restrict__ dy
     __shared__ float sdw[kD];
     for (int c = threadIdx.x; c < kD; c += blockDim.x) sdw[c] = 0.f;
     __syncthreads();
-    const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-    if (row < rows) {
-        const int c0 = 4 * lane;
-        float* orow = O + row * kD + c0;
-        // every load of the row first: o, dy, the gate pre-activations, the RMSNorm weight
-        const float4 o = *reinterpret_cast<const float4*>(orow);
-        float dyv[4], gv[4] = {0.f, 0.f, 0.f, 0.f};
-        float4 wv = make_float4(1.f, 1.f, 1.f, 1.f);
-        load4(dy + row * kD + c0, dyv);
-        if (gate) load4(gate + row * kD + c0, gv);
-        if (rms_w) wv = make_float4(rms_w[c0], rms_w[c0 + 1], rms_w[c0 + 2], rms_w[c0 + 3]);  // 4-byte aligned
-        const float r = 1.0f / sqrtf(warp_sum(dot4(o, o)) * (1.0f / kD) + eps_rms);
-        float dn[4], dw[4], dgv[4];
-        const float ov[4] = {o.x, o.y, o.z, o.w}, wm[4] = {wv.x, wv.y, wv.z, wv.w};
+    const int lane = threadIdx.x & 31, c0 = 4 * lane;
+    // two consecutive rows per warp, every load of both issued before any arithmetic: o, dy, the
+    // gate pre-activations, the RMSNorm weight
+    const int64_t r0 = kEpiRows * ((int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5));
+    float4 o[kEpiRows];
+    float dyv[kEpiRows][4], gv[kEpiRows][4];
+#pragma unroll
+    for (int i = 0; i < kEpiRows; ++i) {
+        const int64_t row = r0 + i;
+        o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) dyv[i][m] = gv[i][m] = 0.f;
+        if (row < rows) {
+            o[i] = *reinterpret_cast<const float4*>(O + row * kD + c0);
+            load4(dy + row * kD + c0, dyv[i]);
+            if (gate) load4(gate + row * kD + c0, gv[i]);
+        }
+    }
+    float4 wv = make_float4(1.f, 1.f, 1.f, 1.f);
+    if (rms_w) wv = make_float4(rms_w[c0], rms_w[c0 + 1], rms_w[c0 + 2], rms_w[c0 + 3]);  // 4-byte aligned
+    const float wm[4] = {wv.x, wv.y, wv.z, wv.w};
+    float dw[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < kEpiRows; ++i) {
+        const int64_t row = r0 + i;
+        if (row >= rows) break;  // warp-uniform
+        const float r = 1.0f / sqrtf(warp_sum(dot4(o[i], o[i])) * (1.0f / kD) + eps_rms);
+        float dn[4], dgv[4];
+        const float ov[4] = {o[i].x, o[i].y, o[i].z, o[i].w};
         float dno = 0.f;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            const float sg = gate ? 1.0f / (1.0f + expf(-gv[m])) : 1.f;
-            const float d = dyv[m];
+            const float sg = gate ? 1.0f / (1.0f + expf(-gv[i][m])) : 1.f;
+            const float d = dyv[i][m];
             const float nv = ov[m] * r;
             dgv[m] = gate ? d * nv * wm[m] * sg * (1.f - sg) : 0.f;
-            dw[m] = d * nv * sg;
+            dw[m] += d * nv * sg;
             dn[m] = d * wm[m] * sg;
             dno += dn[m] * ov[m];
         }
         if (dgate) *reinterpret_cast<float4*>(dgate + row * kD + c0) = make_float4(dgv[0], dgv[1], dgv[2], dgv[3]);
         dno = warp_sum(dno);
         const float r3 = r * r * r * dno * (1.0f / kD);
-        *reinterpret_cast<float4*>(orow) =
+        *reinterpret_cast<float4*>(O + row * kD + c0) =
             make_float4(r * dn[0] - r3 * ov[0], r * dn[1] - r3 * ov[1], r * dn[2] - r3 * ov[2], r * dn[3] - r3 * ov[3]);
-        if (drms)
-#pragma unroll
-            for (int m = 0; m < 4; ++m) atomicAdd(&sdw[c0 + m], dw[m]);
     }
+    if (drms)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) atomicAdd(&sdw[c0 + m], dw[m]);
     __syncthreads();
     if (drms)
         for (int c = threadIdx.x; c < kD; c += blockDim.x) atomicAdd(&drms[c], sdw[c]);
@@ -1708,10 +1724,10 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
     if ((e = cudaGetLastError())) return e;
     if (rows > 0) {
         if (a.out_dtype == KDA_FP32)
-            k_bwd_epilogue<Tio, float><<<rb, 256, 0, s>>>(O, cptr<float>(b.dy), cptr<Tio>(a.gate), a.rms_w, a.eps_rms,
+            k_bwd_epilogue<Tio, float><<<(unsigned)((rows + 8 * kEpiRows - 1) / (8 * kEpiRows)), 256, 0, s>>>(O, cptr<float>(b.dy), cptr<Tio>(a.gate), a.rms_w, a.eps_rms,
                                                            rows, b.dgate, b.drms_w);
         else
-            k_bwd_epilogue<Tio, bf16><<<rb, 256, 0, s>>>(O, cptr<bf16>(b.dy), cptr<Tio>(a.gate), a.rms_w, a.eps_rms,
+            k_bwd_epilogue<Tio, bf16><<<(unsigned)((rows + 8 * kEpiRows - 1) / (8 * kEpiRows)), 256, 0, s>>>(O, cptr<bf16>(b.dy), cptr<Tio>(a.gate), a.rms_w, a.eps_rms,
                                                           rows, b.dgate, b.drms_w);
         if ((e = cudaGetLastError())) return e;
     }
