@@ -1447,7 +1447,7 @@ __global__ void k_bwd_dg_carry(const int32_t* __restrict__ cu, const int64_t* __
 }
 
 // ------------------------------------------------------------------------------ epilogue backward
-constexpr int kEpiRows = 2;  // rows per warp
+constexpr int kEpiRows = 4;  // rows per warp
 // Each warp takes kEpiRows consecutive (token, head) rows, all their loads issued first: do (written
 // over o), dgate, and the RMSNorm weight's gradient (block partials in shared memory, one atomic per
 // channel and block).
