@@ -31,8 +31,9 @@
 // eight columns over the warp; no barrier is needed between tokens.  The
 // state's shared-memory accesses (row r, column c at 16-byte chunk
 // ((c mod 32) / 4) xor (r mod 8) of the swizzle) are conflict-free: the eight
-// lanes of a quarter-warp read eight consecutive rows.  After the last token,
-// warp t normalises token t's output (RMSNorm, weight, gate).
+// lanes of a quarter-warp read eight consecutive rows.  A unit's outputs are
+// normalised (RMSNorm, weight, gate) during the next unit's conv, by the four
+// warps that have no conv channel.
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 #include "kda_tc_ptx.cuh"
@@ -46,8 +47,12 @@ constexpr int kCompute = 512;             // sixteen compute warps
 constexpr int kThreads = kCompute + 32;   // + the producer warp
 constexpr int kL8 = kShortMaxL;
 constexpr int kFs = kD;  // per-token stride (floats) of the factor arrays
-// static shared memory of the kernel (sv, sgate, sW, sRms, snorm, sbeta, barriers)
-constexpr uint32_t kStaticSmem = 4u * (2 * kL8 * kD + 3 * kD * 4 + kD + kL8 * 2 + 2 * kL8) + 32u;
+// static shared memory of the kernel (sv, sgate[2], sW, sRms, snorm, sbeta, barriers)
+constexpr uint32_t kStaticSmem = 4u * (3 * kL8 * kD + 3 * kD * 4 + kD + kL8 * 2 + 2 * kL8) + 32u;
+// the warps that have no conv channel (3 * 128 channels over the first twelve warps); they
+// normalise the previous unit's outputs while the others convolve
+constexpr int kEmitWarp0 = 3 * kD / 32;
+constexpr int kEmitWarps = kCompute / 32 - kEmitWarp0;
 
 __host__ __device__ constexpr uint32_t align128(uint32_t x) { return (x + 127u) & ~127u; }
 
@@ -116,14 +121,6 @@ __device__ __forceinline__ bool cbar_or(bool v) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
 }
-// two packed pairs from / to 16 bytes of shared memory
-__device__ __forceinline__ void lds_f2x2(const void* p, f2& a, f2& b) {
-    asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a.v), "=l"(b.v) : "r"(tc::smem_u32(p)));
-}
-__device__ __forceinline__ void sts_f2x2(void* p, f2 a, f2 b) {
-    asm volatile("st.shared.v2.b64 [%0], {%1, %2};" ::"r"(tc::smem_u32(p)), "l"(a.v), "l"(b.v) : "memory");
-}
-
 // Sums 8 per-lane values over the 32 lanes of a warp; afterwards lane l holds the total of value
 // (l >> 2) & 7 (lanes 4 c .. 4 c + 3 hold value c).
 __device__ __forceinline__ float reduce8_32(float (&v)[8], int lane) {
@@ -187,7 +184,7 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full[2], done[2];            // stage landed; compute warps done with it
     __shared__ __align__(16) float sv[kL8][kD];       // convolved v of every token
-    __shared__ __align__(16) float sgate[kL8][kD];    // sigmoid(gate) of every token (1 without a gate)
+    __shared__ __align__(16) float sgate[2][kL8][kD]; // sigmoid(gate) of every token (1 without a gate), per unit parity
     __shared__ __align__(16) float sW[3 * kD * 4];    // conv taps of the current head
     __shared__ __align__(16) float sRms[kD];
     __shared__ float snorm[kL8][2];                   // 1/|q|, 1/|k| per token
@@ -296,11 +293,11 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
 
     // ---------------------------------------------------------------- compute warps
     const int c0w = 8 * warp;  // the warp's first value column
-    // output of the unit's tokens (warp t for token t): o = scale S^T q / |q| from the readout
-    // sums, RMSNorm, weight, gate
-    auto emit_unit = [&](int64_t ja, int jh, int jL) {
+    // output of a unit's tokens (warp w0 + t for token t, then every nw-th): o = scale S^T q / |q|
+    // from the readout sums, RMSNorm, weight, gate
+    auto emit_unit = [&](int64_t ja, int jh, int jL, int jb, int w0, int nw) {
         const int c0 = 4 * lane;
-        for (int t = warp; t < jL; t += kCompute / 32) {
+        for (int t = warp - w0; t < jL; t += nw) {
             const float sq = scale * snorm[t][0];
             float4 o = *reinterpret_cast<const float4*>(so + t * kD + c0);
             o.x *= sq;
@@ -312,12 +309,15 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
             for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
             const float inv = 1.0f / sqrtf(ss * (1.0f / kD) + eps_rms);
             const float4 rw = *reinterpret_cast<const float4*>(&sRms[c0]);
-            const float4 gg = *reinterpret_cast<const float4*>(&sgate[t][c0]);
+            const float4 gg = *reinterpret_cast<const float4*>(&sgate[jb][t][c0]);
             store4<To>(out + ((ja + t) * H + jh) * kD + c0, o.x * inv * rw.x * gg.x, o.y * inv * rw.y * gg.y,
                        o.z * inv * rw.z * gg.z, o.w * inv * rw.w * gg.w);
         }
     };
     int h_prev = -1;
+    int64_t a_prev = 0;  // the previous unit (its outputs are emitted during this unit's conv)
+    int L_prev = 0;
+    bool failed = false;
     for (int i = 0; i < my_units; ++i) {
         const int b = i & 1;
         int n, h;
@@ -337,25 +337,14 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
                 const int part = idx / (kD * 4), rem = idx % (kD * 4);
                 sW[idx] = conv_w[(part * HD + (int64_t)h * kD) * 4 + rem];
             }
+        const int hp = h_prev;
         h_prev = h;
         if (cbar_or(!ok)) {
             if (tid == 0) flag_status(d_status, KDA_ERR_TIMEOUT);
+            failed = true;
             break;
         }
         uint8_t* st = sm + (uint32_t)b * ST.bytes;
-        // the state into registers: s2[m][p] = columns c0w + 2 p, c0w + 2 p + 1 of row lane + 32 m
-        f2 s2[4][4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int r = lane + 32 * m;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (has_s0) x = *reinterpret_cast<const float4*>(st + state_off(r, c0w + 4 * hf));
-                s2[m][2 * hf] = f2_of(x.x, x.y);
-                s2[m][2 * hf + 1] = f2_of(x.z, x.w);
-            }
-        }
         // conv + SiLU of every token, one channel per thread (warps 0-11); the rolled window out
         for (int ch = tid; ch < 3 * kD; ch += kCompute) {
             const int part = ch >> 7, d = ch & (kD - 1);
@@ -370,13 +359,17 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
             const float4 w = *reinterpret_cast<const float4*>(&sW[ch * 4]);
             float* dst = part == 0 ? fq + d : part == 1 ? fk + d : &sv[0][d];
             const int dstride = part == 2 ? kD : kFs;
-            for (int t = 0; t < L; ++t) {
-                const float x = to_f(rp[t * kD]);
-                dst[t * dstride] = act_silu<Tio>(w.x * p0 + w.y * p1 + w.z * p2 + w.w * x);
-                p0 = p1;
-                p1 = p2;
-                p2 = x;
-            }
+            float xr[kL8];  // every token's raw value first: one shared-memory round trip
+#pragma unroll
+            for (int t = 0; t < kL8; ++t) xr[t] = t < L ? to_f(rp[t * kD]) : 0.f;
+#pragma unroll
+            for (int t = 0; t < kL8; ++t)
+                if (t < L) {
+                    dst[t * dstride] = act_silu<Tio>(w.x * p0 + w.y * p1 + w.z * p2 + w.w * xr[t]);
+                    p0 = p1;
+                    p1 = p2;
+                    p2 = xr[t];
+                }
             if (cs_out) {  // last three raw values of the sequence (exact copies of Tio values)
                 Tio* o3 = cs_out + (((int64_t)n * 3 + part) * HD + (int64_t)h * kD + d) * 3;
                 o3[0] = from_f<Tio>(p0);
@@ -390,7 +383,27 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
             for (int idx = tid; idx < L * kD; idx += kCompute) {
                 const int t = idx >> 7, c = idx & (kD - 1);
                 fa[t * kFs + c] = decay_exp<Tio>(gs[idx]);
-                sgate[t][c] = has_gate ? act_sigmoid<Tio>(to_f(gt[idx])) : 1.f;
+                sgate[b][t][c] = has_gate ? act_sigmoid<Tio>(to_f(gt[idx])) : 1.f;
+            }
+        }
+        // the previous unit's outputs (its o, norms and gates are complete: every warp has passed
+        // barrier A since; this unit writes o and the norms only after barrier B, and its gates
+        // to the other parity)
+        if (i > 0 && warp >= kEmitWarp0) emit_unit(a_prev, hp, L_prev, b ^ 1, kEmitWarp0, kEmitWarps);
+        a_prev = a;
+        L_prev = L;
+        // the state into registers (after the conv, whose row loads it would otherwise queue
+        // behind): s2[m][p] = columns c0w + 2 p, c0w + 2 p + 1 of row lane + 32 m
+        f2 s2[4][4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int r = lane + 32 * m;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (has_s0) x = *reinterpret_cast<const float4*>(st + state_off(r, c0w + 4 * hf));
+                s2[m][2 * hf] = f2_of(x.x, x.y);
+                s2[m][2 * hf + 1] = f2_of(x.z, x.w);
             }
         }
         cbar();  // B: the stage is read completely (the state stays there for the write-back)
@@ -471,8 +484,10 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
             tc::fence_async_smem();
         }
         mbar_arrive(&done[b]);
-        cbar();  // D: every token's o is complete
-        emit_unit(a, h, L);
+    }
+    if (my_units > 0 && !failed) {  // the last unit's outputs, once every token's o is complete
+        cbar();
+        emit_unit(a_prev, h_prev, L_prev, (my_units - 1) & 1, 0, kCompute / 32);
     }
 }
 
