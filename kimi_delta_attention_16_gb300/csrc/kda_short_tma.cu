@@ -445,13 +445,12 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
                              f2_lo(O[2]), f2_hi(O[2]), f2_lo(O[3]), f2_hi(O[3])};
             const float red = reduce16_32(v16, lane);  // lane l: value l >> 1
             if (t > 0 && lane >= 16 && (lane & 1) == 0) so[(t - 1) * kD + c0w + ((lane >> 1) - 8)] = red;
-            const float bk = sbeta[b][t] * ik;
-            const float4 va = *reinterpret_cast<const float4*>(&sv[t][c0w]);
-            const float4 vb = *reinterpret_cast<const float4*>(&sv[t][c0w + 4]);
-            const float vv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+            // lanes 2c, 2c + 1 hold column c's probe: each lane forms the correction of the column
+            // it holds (lanes 16-31 form unused values), then the eight are passed round
+            const float el = sbeta[b][t] * ik * (sv[t][c0w + ((lane >> 1) & 7)] - ik * red);
             float e[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) e[c] = bk * (vv[c] - ik * __shfl_sync(0xffffffffu, red, 2 * c));
+            for (int c = 0; c < 8; ++c) e[c] = __shfl_sync(0xffffffffu, el, 2 * c);
 #pragma unroll
             for (int p = 0; p < 4; ++p) O[p] = f2_dup(0.f);
 #pragma unroll
