@@ -132,14 +132,15 @@ __global__ void k_bwd_prep(const Tio* __restrict__ q, const Tio* __restrict__ k,
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             const float u = w[0][m] * x[0][m] + w[1][m] * x[1][m] + w[2][m] * x[2][m] + w[3][m] * x[3][m];
-            out[part][m] = u / (1.0f + expf(-u));
+            out[part][m] = __fdividef(u, 1.0f + __expf(-u));  // (u -> -inf: u / inf = 0)
             if (part < 2) ss[part] += out[part][m] * out[part][m];
         }
     }
     const float nq = sqrtf(warp_sum(ss[0]) + eps_l2), nk = sqrtf(warp_sum(ss[1]) + eps_l2);
+    const float rq = 1.0f / nq, rk = 1.0f / nk;
     float* xr = X + t * 3 * HD + (int64_t)h * kD + 4 * lane;
-    *reinterpret_cast<float4*>(xr) = make_float4(out[0][0] / nq, out[0][1] / nq, out[0][2] / nq, out[0][3] / nq);
-    *reinterpret_cast<float4*>(xr + HD) = make_float4(out[1][0] / nk, out[1][1] / nk, out[1][2] / nk, out[1][3] / nk);
+    *reinterpret_cast<float4*>(xr) = make_float4(out[0][0] * rq, out[0][1] * rq, out[0][2] * rq, out[0][3] * rq);
+    *reinterpret_cast<float4*>(xr + HD) = make_float4(out[1][0] * rk, out[1][1] * rk, out[1][2] * rk, out[1][3] * rk);
     *reinterpret_cast<float4*>(xr + 2 * HD) = make_float4(out[2][0], out[2][1], out[2][2], out[2][3]);
     if (lane == 0) *reinterpret_cast<float2*>(nrm + row * 2) = make_float2(nq, nk);
 }
@@ -155,6 +156,114 @@ __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_grou
 template <int N>
 __device__ __forceinline__ void cp_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ------------------------------------------------------------------------------ prep, tiled
+// The same outputs as k_bwd_prep, with the same arithmetic, for inputs whose rows start on
+// 16-byte boundaries: one block of 8 warps per (64-token tile, head) first stages the tile's raw
+// q, k, v rows t0 - 3 .. t0 + 63 in shared memory with one burst of cp.async (51 KB for bf16
+// inputs, all in flight at once instead of each warp's twelve dependent row loads), then each warp
+// takes every eighth token of the tile and reads its windows there.
+constexpr int kPrepTile = 64;
+constexpr int kPrepRows = kPrepTile + 3;
+template <typename Tio>
+constexpr uint32_t prep_tile_smem() { return 3u * kPrepRows * kD * (uint32_t)sizeof(Tio); }
+
+template <typename Tio>
+__global__ void __launch_bounds__(256)
+k_bwd_prep_tile(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __restrict__ v,
+                int64_t xs, const float* __restrict__ conv_w, const Tio* __restrict__ cs_in,
+                const int32_t* __restrict__ cu, int N, int64_t T_total, int H, float eps_l2,
+                float* __restrict__ X, float* __restrict__ nrm) {
+    extern __shared__ __align__(16) uint8_t prep_sm[];
+    Tio* raw = reinterpret_cast<Tio*>(prep_sm);  // [part][row r][D], row r = token t0 - 3 + r
+    __shared__ __align__(16) float wt[3][4][kD];  // [part][tap][channel]
+    __shared__ int s_n0;
+    const int h = (int)(blockIdx.x % H);
+    const int64_t t0 = (int64_t)(blockIdx.x / H) * kPrepTile;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t HD = (int64_t)H * kD;
+    constexpr int kPieces = kD * (int)sizeof(Tio) / 16;  // 16-byte pieces per row
+    constexpr int kElems = 16 / (int)sizeof(Tio);
+    for (int i = tid; i < 3 * kPrepRows * kPieces; i += blockDim.x) {
+        const int part = i / (kPrepRows * kPieces), rem = i - part * (kPrepRows * kPieces);
+        const int r = rem / kPieces, c = rem - r * kPieces;
+        const int64_t p = t0 - 3 + r;
+        const Tio* sp = part == 0 ? q : (part == 1 ? k : v);
+        if (p >= 0 && p < T_total)  // rows before 0 lie before every sequence start: replaced below
+            cp16(raw + ((size_t)part * kPrepRows + r) * kD + c * kElems, sp + p * xs + (int64_t)h * kD + c * kElems);
+    }
+    cp_commit();
+    for (int i = tid; i < 3 * kD; i += blockDim.x) {
+        const int part = i / kD, ch = i - part * kD;
+        const float4 w4 = *reinterpret_cast<const float4*>(conv_w + ((int64_t)part * HD + (int64_t)h * kD + ch) * 4);
+        wt[part][0][ch] = w4.x;
+        wt[part][1][ch] = w4.y;
+        wt[part][2][ch] = w4.z;
+        wt[part][3][ch] = w4.w;
+    }
+    if (tid == 0) {  // the sequence of the tile's first token (binary search over cu_seqlens)
+        const int64_t tf = t0 < T_total ? t0 : T_total - 1;
+        int lo = 0, hi = N;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (cu[mid] <= tf) lo = mid;
+            else hi = mid;
+        }
+        s_n0 = lo;
+    }
+    cp_wait<0>();
+    __syncthreads();
+    int n = s_n0;
+    for (int j = warp; j < kPrepTile; j += 8) {
+        const int64_t t = t0 + j;
+        if (t >= T_total) break;
+        while (n + 1 < N && cu[n + 1] <= t) ++n;  // the sequence of token t
+        int64_t s0 = cu[n];
+        s0 = s0 < 0 ? 0 : (s0 > t ? t : s0);  // keeps every index in bounds if cu is inconsistent
+        const int64_t row = t * H + h;
+        float out[3][4];
+        float ss[2] = {0.f, 0.f};
+#pragma unroll
+        for (int part = 0; part < 3; ++part) {
+            float x[4][4];  // [token t - 3 + m][channel]
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int64_t p = t - 3 + m;
+                if (p >= s0) {
+                    load4(raw + ((size_t)part * kPrepRows + j + m) * kD + 4 * lane, x[m]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int64_t ch = (int64_t)part * HD + (int64_t)h * kD + 4 * lane + c;
+                        x[m][c] = cs_in ? to_f(cs_in[((int64_t)n * 3 * HD + ch) * 3 + 3 + (p - s0)]) : 0.f;
+                    }
+                }
+            }
+            float w[4][4];  // [tap][channel]
+#pragma unroll
+            for (int tap = 0; tap < 4; ++tap) {
+                const float4 w4 = *reinterpret_cast<const float4*>(&wt[part][tap][4 * lane]);
+                w[tap][0] = w4.x;
+                w[tap][1] = w4.y;
+                w[tap][2] = w4.z;
+                w[tap][3] = w4.w;
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float u = w[0][c] * x[0][c] + w[1][c] * x[1][c] + w[2][c] * x[2][c] + w[3][c] * x[3][c];
+                out[part][c] = __fdividef(u, 1.0f + __expf(-u));  // (u -> -inf: u / inf = 0)
+                if (part < 2) ss[part] += out[part][c] * out[part][c];
+            }
+        }
+        const float nq = sqrtf(warp_sum(ss[0]) + eps_l2), nk = sqrtf(warp_sum(ss[1]) + eps_l2);
+        const float rq = 1.0f / nq, rk = 1.0f / nk;
+        float* xr = X + t * 3 * HD + (int64_t)h * kD + 4 * lane;
+        *reinterpret_cast<float4*>(xr) = make_float4(out[0][0] * rq, out[0][1] * rq, out[0][2] * rq, out[0][3] * rq);
+        *reinterpret_cast<float4*>(xr + HD) = make_float4(out[1][0] * rk, out[1][1] * rk, out[1][2] * rk, out[1][3] * rk);
+        *reinterpret_cast<float4*>(xr + 2 * HD) = make_float4(out[2][0], out[2][1], out[2][2], out[2][3]);
+        if (lane == 0) *reinterpret_cast<float2*>(nrm + row * 2) = make_float2(nq, nk);
+    }
 }
 
 // First checkpoint slot of unit (n, h): sequences in order, each holding H runs of its segment
@@ -1616,7 +1725,7 @@ __global__ void k_bwd_conv(const Tio* __restrict__ q, const Tio* __restrict__ k,
         x1 = x0;
         x0 = xnew;
         const float uu = w.x * x0 + w.y * x1 + w.z * x2 + w.w * x3;
-        const float sg = 1.0f / (1.0f + expf(-uu));
+        const float sg = __fdividef(1.0f, 1.0f + __expf(-uu));  // (uu -> -inf: 1 / inf = 0)
         const float du = da * sg * (1.0f + uu * (1.0f - sg));
         if (t < tb) {
             dst[t * HD + hc] = w.w * du + w.z * du1 + w.y * du2 + w.x * du3;
@@ -1705,8 +1814,21 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
     if ((e = cudaGetLastError())) return e;
     const unsigned rb = (unsigned)((rows + 7) / 8);
     if (rows > 0) {
-        k_bwd_prep<Tio><<<(unsigned)((T + 7) / 8 * a.H), 256, 0, s>>>(cptr<Tio>(a.q), cptr<Tio>(a.k), cptr<Tio>(a.v), xs, a.conv_w,
-                                          cptr<Tio>(a.conv_state_in), a.cu_seqlens, a.N, T, a.H, a.eps_l2, X, nrm);
+        // rows on 16-byte boundaries take the tiled form (staged by cp.async)
+        const bool tiled = (xs * (int64_t)sizeof(Tio)) % 16 == 0 && ((reinterpret_cast<uintptr_t>(a.q) |
+                            reinterpret_cast<uintptr_t>(a.k) | reinterpret_cast<uintptr_t>(a.v)) & 15u) == 0;
+        if (tiled) {
+            if ((e = cudaFuncSetAttribute(k_bwd_prep_tile<Tio>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)prep_tile_smem<Tio>())))
+                return e;
+            k_bwd_prep_tile<Tio><<<(unsigned)((T + kPrepTile - 1) / kPrepTile * a.H), 256, prep_tile_smem<Tio>(), s>>>(
+                cptr<Tio>(a.q), cptr<Tio>(a.k), cptr<Tio>(a.v), xs, a.conv_w, cptr<Tio>(a.conv_state_in), a.cu_seqlens,
+                a.N, T, a.H, a.eps_l2, X, nrm);
+        } else {
+            k_bwd_prep<Tio><<<(unsigned)((T + 7) / 8 * a.H), 256, 0, s>>>(cptr<Tio>(a.q), cptr<Tio>(a.k), cptr<Tio>(a.v), xs,
+                                                                      a.conv_w, cptr<Tio>(a.conv_state_in), a.cu_seqlens,
+                                                                      a.N, T, a.H, a.eps_l2, X, nrm);
+        }
         if ((e = cudaGetLastError())) return e;
     }
     float* Rec = reinterpret_cast<float*>(ws + L.rec);
