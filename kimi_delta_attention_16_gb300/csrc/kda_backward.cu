@@ -170,7 +170,7 @@ template <typename Tio>
 constexpr uint32_t prep_tile_smem() { return 3u * kPrepRows * kD * (uint32_t)sizeof(Tio); }
 
 template <typename Tio>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 k_bwd_prep_tile(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __restrict__ v,
                 int64_t xs, const float* __restrict__ conv_w, const Tio* __restrict__ cs_in,
                 const int32_t* __restrict__ cu, int N, int64_t T_total, int H, float eps_l2,
