@@ -337,10 +337,11 @@ kda_status kda_gemm(const kda_gemm_args* args, kda_stream_t stream);
  * initial_state); out_dtype there is the dtype of dy.  Its out, final_state,
  * conv_state_out, chunk, flags and segments are ignored; its workspace and
  * workspace_bytes are this call's scratch (kda_backward_workspace_size).
- * Supported: D = 128, io bf16 or fp32; arithmetic is fp32 (the decays e^g,
- * SiLU and sigmoid through the IEEE functions; the chunk products on the
- * tensor cores as three TF32 terms of hi/lo splits, close to fp32), so the
- * result does not depend on the forward's path.
+ * Supported: D = 128, io bf16 or fp32; arithmetic is fp32 (the decays e^g
+ * and the gate sigmoid through the IEEE functions, the recomputed SiLU and its
+ * derivative through the fast exponential and reciprocal, a few ulp; the
+ * chunk products on the tensor cores as three TF32 terms of hi/lo splits,
+ * close to fp32), so the result does not depend on the forward's path.
  *
  * Method: conv + SiLU + L2 norms recomputed per token; for every 16-token
  * chunk, all at once, the parts that do not involve the state (decayed keys

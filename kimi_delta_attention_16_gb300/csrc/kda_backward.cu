@@ -60,91 +60,6 @@ __device__ __forceinline__ void load4(const float* p, float (&x)[4]) {
     x[3] = f.w;
 }
 
-// ------------------------------------------------------------------------------ prep
-// One warp per (token, head): conv + SiLU of the q, k, v channels of the head (lane l: channels
-// 4 l .. 4 l + 3), the L2 norms of q and k.  X: [T][3][H][D] fp32 (q^, k^, v), nrm: [T][H][2].
-// Grid: ceil(T / 8) x H blocks of 8 warps taking consecutive tokens of one head.
-template <typename Tio>
-__global__ void k_bwd_prep(const Tio* __restrict__ q, const Tio* __restrict__ k, const Tio* __restrict__ v,
-                           int64_t xs, const float* __restrict__ conv_w, const Tio* __restrict__ cs_in,
-                           const int32_t* __restrict__ cu, int N, int64_t T_total, int H, float eps_l2,
-                           float* __restrict__ X, float* __restrict__ nrm) {
-    // the warps of a block take consecutive tokens of one head: the head's conv taps are staged in
-    // shared memory once per block (tap-major, so that a lane's four channels are one float4), and
-    // the overlapping input windows are served from L1
-    __shared__ __align__(16) float wt[3][4][kD];  // [part][tap][channel]
-    const int wpb = blockDim.x / 32;
-    const int h = (int)(blockIdx.x % H);
-    const int64_t t = (int64_t)(blockIdx.x / H) * wpb + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    const int64_t HD = (int64_t)H * kD;
-    for (int i = threadIdx.x; i < 3 * kD; i += blockDim.x) {
-        const int part = i / kD, ch = i - part * kD;
-        const float4 w4 = *reinterpret_cast<const float4*>(conv_w + ((int64_t)part * HD + (int64_t)h * kD + ch) * 4);
-        wt[part][0][ch] = w4.x;
-        wt[part][1][ch] = w4.y;
-        wt[part][2][ch] = w4.z;
-        wt[part][3][ch] = w4.w;
-    }
-    __syncthreads();
-    if (t >= T_total) return;
-    const int64_t row = t * H + h;
-    // the sequence of token t (binary search over cu_seqlens)
-    int lo = 0, hi = N;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (cu[mid] <= t) lo = mid;
-        else hi = mid;
-    }
-    const int n = lo;
-    int64_t s0 = cu[n];
-    s0 = s0 < 0 ? 0 : (s0 > t ? t : s0);  // keeps every index in bounds if cu is inconsistent
-    const Tio* src[3] = {q, k, v};
-    float out[3][4];
-    float ss[2] = {0.f, 0.f};
-#pragma unroll
-    for (int part = 0; part < 3; ++part) {
-        // the raw inputs of the lane's 4 channels at t - 3 .. t: one vector load per token
-        float x[4][4];  // [token j][channel m]
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t p = t - 3 + j;
-            // loaded whatever the sequence start (rows 0 .. t exist), so that the loads do not wait
-            // for cu_seqlens; rows before the start are replaced below
-            load4(src[part] + (p > 0 ? p : 0) * xs + (int64_t)h * kD + 4 * lane, x[j]);
-            if (p < s0) {
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int64_t ch = (int64_t)part * HD + (int64_t)h * kD + 4 * lane + m;
-                    x[j][m] = cs_in ? to_f(cs_in[((int64_t)n * 3 * HD + ch) * 3 + 3 + (p - s0)]) : 0.f;
-                }
-            }
-        }
-        float w[4][4];  // [tap][channel m]
-#pragma unroll
-        for (int tap = 0; tap < 4; ++tap) {
-            const float4 w4 = *reinterpret_cast<const float4*>(&wt[part][tap][4 * lane]);
-            w[tap][0] = w4.x;
-            w[tap][1] = w4.y;
-            w[tap][2] = w4.z;
-            w[tap][3] = w4.w;
-        }
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float u = w[0][m] * x[0][m] + w[1][m] * x[1][m] + w[2][m] * x[2][m] + w[3][m] * x[3][m];
-            out[part][m] = __fdividef(u, 1.0f + __expf(-u));  // (u -> -inf: u / inf = 0)
-            if (part < 2) ss[part] += out[part][m] * out[part][m];
-        }
-    }
-    const float nq = sqrtf(warp_sum(ss[0]) + eps_l2), nk = sqrtf(warp_sum(ss[1]) + eps_l2);
-    const float rq = 1.0f / nq, rk = 1.0f / nk;
-    float* xr = X + t * 3 * HD + (int64_t)h * kD + 4 * lane;
-    *reinterpret_cast<float4*>(xr) = make_float4(out[0][0] * rq, out[0][1] * rq, out[0][2] * rq, out[0][3] * rq);
-    *reinterpret_cast<float4*>(xr + HD) = make_float4(out[1][0] * rk, out[1][1] * rk, out[1][2] * rk, out[1][3] * rk);
-    *reinterpret_cast<float4*>(xr + 2 * HD) = make_float4(out[2][0], out[2][1], out[2][2], out[2][3]);
-    if (lane == 0) *reinterpret_cast<float2*>(nrm + row * 2) = make_float2(nq, nk);
-}
-
 // ------------------------------------------------------------------------------ staging helpers
 // 16-byte and 4-byte asynchronous global -> shared copies (cp.async), one group per staged block.
 __device__ __forceinline__ void cp16(void* dst, const void* src) {
@@ -158,12 +73,13 @@ __device__ __forceinline__ void cp_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// ------------------------------------------------------------------------------ prep, tiled
-// The same outputs as k_bwd_prep, with the same arithmetic, for inputs whose rows start on
-// 16-byte boundaries: one block of 8 warps per (64-token tile, head) first stages the tile's raw
-// q, k, v rows t0 - 3 .. t0 + 63 in shared memory with one burst of cp.async (51 KB for bf16
-// inputs, all in flight at once instead of each warp's twelve dependent row loads), then each warp
-// takes every eighth token of the tile and reads its windows there.
+// ------------------------------------------------------------------------------ prep
+// Conv + SiLU of the q, k, v channels of a head and the L2 norms of q and k, recomputed in fp32.
+// X: [T][3][H][D] fp32 (q^, k^, v), nrm: [T][H][2].  One block of 8 warps per (64-token tile,
+// head) first stages the tile's raw q, k, v rows t0 - 3 .. t0 + 63 in shared memory with one burst
+// of cp.async (51 KB for bf16 inputs, all in flight at once; the C ABI's row rules put every row on
+// a 16-byte boundary), then each warp takes every eighth token of the tile (lane l: channels
+// 4 l .. 4 l + 3) and reads its windows there.
 constexpr int kPrepTile = 64;
 constexpr int kPrepRows = kPrepTile + 3;
 template <typename Tio>
@@ -1813,22 +1729,13 @@ cudaError_t backward_launch(const kda_backward_args& b, const BackwardLayout& L,
     k_bwd_seg_prefix<<<1, 256, 0, s>>>(a.cu_seqlens, a.N, T, prefix);
     if ((e = cudaGetLastError())) return e;
     const unsigned rb = (unsigned)((rows + 7) / 8);
-    if (rows > 0) {
-        // rows on 16-byte boundaries take the tiled form (staged by cp.async)
-        const bool tiled = (xs * (int64_t)sizeof(Tio)) % 16 == 0 && ((reinterpret_cast<uintptr_t>(a.q) |
-                            reinterpret_cast<uintptr_t>(a.k) | reinterpret_cast<uintptr_t>(a.v)) & 15u) == 0;
-        if (tiled) {
-            if ((e = cudaFuncSetAttribute(k_bwd_prep_tile<Tio>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)prep_tile_smem<Tio>())))
-                return e;
-            k_bwd_prep_tile<Tio><<<(unsigned)((T + kPrepTile - 1) / kPrepTile * a.H), 256, prep_tile_smem<Tio>(), s>>>(
-                cptr<Tio>(a.q), cptr<Tio>(a.k), cptr<Tio>(a.v), xs, a.conv_w, cptr<Tio>(a.conv_state_in), a.cu_seqlens,
-                a.N, T, a.H, a.eps_l2, X, nrm);
-        } else {
-            k_bwd_prep<Tio><<<(unsigned)((T + 7) / 8 * a.H), 256, 0, s>>>(cptr<Tio>(a.q), cptr<Tio>(a.k), cptr<Tio>(a.v), xs,
-                                                                      a.conv_w, cptr<Tio>(a.conv_state_in), a.cu_seqlens,
-                                                                      a.N, T, a.H, a.eps_l2, X, nrm);
-        }
+    if (rows > 0) {  // (rows start on 16-byte boundaries: the row rules of the C ABI)
+        if ((e = cudaFuncSetAttribute(k_bwd_prep_tile<Tio>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)prep_tile_smem<Tio>())))
+            return e;
+        k_bwd_prep_tile<Tio><<<(unsigned)((T + kPrepTile - 1) / kPrepTile * a.H), 256, prep_tile_smem<Tio>(), s>>>(
+            cptr<Tio>(a.q), cptr<Tio>(a.k), cptr<Tio>(a.v), xs, a.conv_w, cptr<Tio>(a.conv_state_in), a.cu_seqlens,
+            a.N, T, a.H, a.eps_l2, X, nrm);
         if ((e = cudaGetLastError())) return e;
     }
     float* Rec = reinterpret_cast<float*>(ws + L.rec);

@@ -3,10 +3,11 @@
 The oracle's backward is pinned to central differences of the fp64 forward (see the oracle pin
 tests); here every gradient the library returns is compared with it on the same seeded inputs.
 
-Tolerance.  The library recomputes the forward and runs its adjoint in fp32 (IEEE exp, SiLU
-and sigmoid; bf16 inputs are exact in fp32; the chunk products on the tensor cores as three TF32
-terms of hi/lo splits, about 2^-21 relative per product), so the errors are fp32-level roundoff
-carried through the recurrence.  Each step is a contraction of the state and of its adjoint (0 < e^g <= 1,
+Tolerance.  The library recomputes the forward and runs its adjoint in fp32 (IEEE exp for the
+decays and the gate sigmoid, the fast exponential and reciprocal for the recomputed SiLU and its
+derivative, a few ulp; bf16 inputs are exact in fp32; the chunk products on the tensor cores as
+three TF32 terms of hi/lo splits, about 2^-21 relative per product), so the errors are fp32-level
+roundoff carried through the recurrence.  Each step is a contraction of the state and of its adjoint (0 < e^g <= 1,
 |k| = 1 after the L2 norm, 0 <= beta <= 1), so roundoff does not grow from step to step; it
 accumulates over the D = 128 terms of each dot product and over the tokens of a sequence.
 With the fp32 unit roundoff 6e-8 and a few hundred tokens that is ~1e-6 of the tensor's scale
@@ -93,6 +94,26 @@ def test_backward_parity_varlen_all_inputs(io):
     state, conv state, dS_fin."""
     inp, dy, dsf = _case(io, [70, 1, 0, 33, 130], seed=11)
     _check(_gpu_backward(inp, dy, dsf), _oracle_backward(inp, dy, dsf))
+
+
+@pytest.mark.parametrize("io,pad", [("bf16", 0), ("bf16", 8), ("fp32", 4)])
+def test_backward_parity_fused_qkv_rows(io, pad):
+    """q, k and v as views of one [T, 3 H D + pad] buffer (a fused projection, padded rows within
+    the ABI's row rules: 16-byte multiples), read by the recompute's staged row copies; against the
+    oracle."""
+    inp, dy, dsf = _case(io, [70, 1, 33], seed=41)
+    T, H, D = inp.q.shape
+    HD = H * D
+    buf = torch.zeros((T, 3 * HD + pad), dtype=inp.q.dtype, device=DEV)
+    views = []
+    for i, x in enumerate((inp.q, inp.k, inp.v)):
+        buf[:, i * HD:(i + 1) * HD] = x.reshape(T, HD)
+        views.append(buf[:, i * HD:(i + 1) * HD].unflatten(1, (H, D)))
+    res = kda.kda_backward(views[0], views[1], views[2], inp.conv_w, inp.g, inp.beta, inp.cu_seqlens, dy,
+                           gate=inp.gate, rms_w=inp.rms_w, initial_state=inp.initial_state,
+                           conv_state_in=inp.conv_state_in, d_final_state=dsf)
+    torch.cuda.synchronize()
+    _check({k: to_np(v) for k, v in res.items()}, _oracle_backward(inp, dy, dsf))
 
 
 def test_backward_parity_chunk_and_segment_boundaries():
