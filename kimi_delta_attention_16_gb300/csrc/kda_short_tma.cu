@@ -12,28 +12,38 @@
 // A unit is one (sequence, head); its bytes are the 64 KB fp32 state in and
 // out, the rolling conv window in and out and a few token rows, so the path is
 // bound by HBM.  Persistent CTAs (one per SM) walk contiguous head-major
-// ranges of units with two shared-memory stages.  A producer warp (one
-// thread) fills stage i % 2 with unit i -- the state as four 2D tensor-map
-// boxes of 32 columns with the 128-byte swizzle, the conv window by 1D bulk
-// copies, the token rows as one box of Lmax rows for each of q, k, v, gate
-// and g, the betas by plain loads -- and, once the compute warps have
-// finished unit i - 2 there and written its state back into the stage, sends
-// that state to final_state by four tensor-map stores before reusing the
-// stage.  Neither the request issue nor the 64 KB store stalls a compute warp.
+// ranges of units with three kinds of warps and two rings in shared memory:
 //
-// Sixteen compute warps; warp w owns value columns 8 w .. 8 w + 7 and lane l
-// owns the rows l, l + 32, l + 64, l + 96 of all eight, as packed fp32 pairs of
-// adjacent columns.  A token's per-row factors (q, k, e^g) are then read by
-// the 32 lanes of a warp from 32 consecutive floats (one shared-memory
-// wavefront per 32 values, instead of the eight-lane broadcasts a
-// column-per-lane layout needs), and the column sums over the key rows (the
-// probe S_bar^T k and the readout S^T q) are one transposed reduction of the
-// eight columns over the warp; no barrier is needed between tokens.  The
-// state's shared-memory accesses (row r, column c at 16-byte chunk
-// ((c mod 32) / 4) xor (r mod 8) of the swizzle) are conflict-free: the eight
-// lanes of a quarter-warp read eight consecutive rows.  A unit's outputs are
-// normalised (RMSNorm, weight, gate) during the next unit's conv, by the four
-// warps that have no conv channel.
+//  - a producer warp (one thread) fills row slot i % 2 with unit i's token rows
+//    (one box of Lmax rows for each of q, k, v, gate and g, the conv window by
+//    1D bulk copies, the betas by plain loads) as soon as the prep warps have
+//    read unit i - 2's rows there, and state slot i % 2 with its state (four 2D
+//    tensor-map boxes of 32 columns with the 128-byte swizzle) once the compute
+//    warps are through unit i - 2, whose final state it first sends out by
+//    four tensor-map stores;
+//  - four prep warps form everything of a unit that does not involve the state
+//    (conv + SiLU, e^g, the gate sigmoids, the L2 norms, the betas) into the
+//    factor buffers of the unit's parity, ahead of the compute warps, and
+//    normalise a unit's outputs (RMSNorm, weight, gate) once its tokens are
+//    through;
+//  - sixteen compute warps run the token chain of each unit from its state
+//    slot and write the final state back there; they never wait for one
+//    another.
+//
+// Because the rows have a ring of their own, a unit's factors are ready long
+// before its tokens run, and the state ring alone paces the unit.  Every
+// hand-over is an mbarrier with a bounded wait.
+//
+// Compute warp w owns value columns 8 w .. 8 w + 7 and lane l owns the rows
+// l, l + 32, l + 64, l + 96 of all eight, as packed fp32 pairs of adjacent
+// columns.  A token's per-row factors (q, k, e^g) are then read by the 32
+// lanes of a warp from 32 consecutive floats (one shared-memory wavefront per
+// 32 values), and the column sums over the key rows (the probe S_bar^T k and
+// the readout S^T q) are one transposed reduction of the eight columns over
+// the warp; no barrier is needed between tokens.  The state's shared-memory
+// accesses (row r, column c at 16-byte chunk ((c mod 32) / 4) xor (r mod 8) of
+// the swizzle) are conflict-free: the eight lanes of a quarter-warp read eight
+// consecutive rows.
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 #include "kda_tc_ptx.cuh"
@@ -44,26 +54,26 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kCompute = 512;             // sixteen compute warps
-constexpr int kThreads = kCompute + 32;   // + the producer warp
+constexpr int kPrep = 128;                // four prep warps
+constexpr int kThreads = kCompute + kPrep + 32;  // + the producer warp
 constexpr int kL8 = kShortMaxL;
 constexpr int kFs = kD;  // per-token stride (floats) of the factor arrays
-// static shared memory of the kernel (sv, sgate[2], sW, sRms, snorm, sbeta, barriers)
-constexpr uint32_t kStaticSmem = 4u * (3 * kL8 * kD + 3 * kD * 4 + kD + kL8 * 2 + 2 * kL8) + 32u;
-// the warps that have no conv channel (3 * 128 channels over the first twelve warps); they
-// normalise the previous unit's outputs while the others convolve
-constexpr int kEmitWarp0 = 3 * kD / 32;
-constexpr int kEmitWarps = kCompute / 32 - kEmitWarp0;
+// static shared memory of the kernel (sv[2], sgate[2], sW, sRms, snorm[2], sbeta, sbf, spart,
+// ten barriers)
+constexpr uint32_t kStaticSmem =
+    4u * (4 * kL8 * kD + 3 * kD * 4 + kD + 2 * kL8 * 2 + 2 * kL8 + 2 * kL8 + (kPrep / 32) * kL8 * 2) + 80u;
+constexpr uint32_t kStateSlot = 65536;  // one state: four 2D boxes of 32 columns x 128 rows, fp32
 
 __host__ __device__ constexpr uint32_t align128(uint32_t x) { return (x + 127u) & ~127u; }
 
-// Byte offsets inside one stage for boxes of Lmax token rows.  The state boxes use the
-// 128-byte swizzle, so every stage starts on a 1024-byte boundary.
+// Byte offsets inside one slot of the row ring for boxes of Lmax token rows (the states have a
+// ring of their own, two 64 KB slots with the 128-byte swizzle ahead of the row slots).
 template <typename Tio>
-struct TmaStage {
+struct RowSlot {
     uint32_t conv, rows, part, g, bytes;
-    __host__ __device__ explicit TmaStage(int Lmax) {
-        conv = 65536;                                                     // [3][128][3] Tio
-        rows = conv + align128(3 * kD * 3 * (uint32_t)sizeof(Tio));      // [4][Lmax][128] Tio: q, k, v, gate
+    __host__ __device__ explicit RowSlot(int Lmax) {
+        conv = 0;                                                         // [3][128][3] Tio
+        rows = align128(3 * kD * 3 * (uint32_t)sizeof(Tio));             // [4][Lmax][128] Tio: q, k, v, gate
         part = (uint32_t)Lmax * kD * (uint32_t)sizeof(Tio);
         g = rows + align128(4 * part);                                    // [Lmax][128] fp32
         bytes = (g + (uint32_t)Lmax * kD * 4 + 1023u) & ~1023u;
@@ -107,14 +117,14 @@ __device__ __forceinline__ void store4<bf16>(bf16* p, float a, float b, float c,
     *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(a, b), pack_bf16x2(c, d));
 }
 
-// named barrier 1 of the compute warps (the producer warp never joins it)
-__device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kCompute) : "memory"); }
-__device__ __forceinline__ bool cbar_or(bool v) {
+// named barrier 1 of the prep warps (no other warp joins it)
+__device__ __forceinline__ void pbar() { asm volatile("bar.sync 1, %0;" ::"n"(kPrep) : "memory"); }
+__device__ __forceinline__ bool pbar_or(bool v) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"(v ? 1u : 0u), "n"(kCompute)
+        : "r"(v ? 1u : 0u), "n"(kPrep)
         : "memory");
     return r != 0;
 }
@@ -182,24 +192,30 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
             float scale, int N, int H, const int32_t* __restrict__ cu, int64_t T_total, To* __restrict__ out,
             int* d_status) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t full[2], done[2];            // stage landed; compute warps done with it
-    __shared__ __align__(16) float sv[kL8][kD];       // convolved v of every token
-    __shared__ __align__(16) float sgate[2][kL8][kD]; // sigmoid(gate) of every token (1 without a gate), per unit parity
-    __shared__ __align__(16) float sW[3 * kD * 4];    // conv taps of the current head
+    // state slot landed; compute warps done with a unit (its state slot and its factor buffers);
+    // row slot landed; prep warps done reading a row slot; prep warps done forming a unit's factors
+    __shared__ uint64_t sfull[2], done[2], rfull[2], rdone[2], ready[2];
+    __shared__ __align__(16) float sv[2][kL8][kD];    // convolved v of every token, per unit parity
+    __shared__ __align__(16) float sgate[2][kL8][kD]; // sigmoid(gate) of every token (1 without a gate)
+    __shared__ __align__(16) float sW[3 * kD * 4];    // conv taps of the prep warps' current head
     __shared__ __align__(16) float sRms[kD];
-    __shared__ float snorm[kL8][2];                   // 1/|q|, 1/|k| per token
-    __shared__ float sbeta[2][kL8];                   // betas per stage
+    __shared__ float snorm[2][kL8][2];                // 1/|q|, 1/|k| per token
+    __shared__ float sbeta[2][kL8];                   // betas per row slot (written by the producer)
+    __shared__ float sbf[2][kL8];                     // betas per unit parity (copied by the prep warps)
+    __shared__ float spart[kPrep / 32][kL8][2];       // per prep warp: partial sums of q^2, k^2
 
-    const TmaStage<Tio> ST(Lmax);
+    const RowSlot<Tio> ST(Lmax);
     const uint32_t raw_addr = tc::smem_u32(smem_raw);
     uint8_t* sm = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
     const uint32_t sbase = tc::smem_u32(sm);
-    // after the two stages: q, k and e^g ([Lmax][128]) of every token, then o before its
-    // normalisation ([Lmax][128])
-    float* fq = reinterpret_cast<float*>(sm + 2 * ST.bytes);
-    float* fk = fq + Lmax * kFs;
-    float* fa = fk + Lmax * kFs;
-    float* so = fa + Lmax * kFs;
+    // two state slots, two row slots, then per unit parity pb: q, k and e^g ([Lmax][kFs]) of every
+    // token, then o before its normalisation ([Lmax][128])
+    const uint32_t rbase = 2 * kStateSlot;  // first row slot
+    float* const fbase = reinterpret_cast<float*>(sm + rbase + 2 * ST.bytes);
+    auto fq = [&](int pb) { return fbase + (size_t)pb * 3 * Lmax * kFs; };
+    auto fk = [&](int pb) { return fbase + ((size_t)pb * 3 + 1) * Lmax * kFs; };
+    auto fa = [&](int pb) { return fbase + ((size_t)pb * 3 + 2) * Lmax * kFs; };
+    auto so = [&](int pb) { return fbase + (size_t)6 * Lmax * kFs + (size_t)pb * Lmax * kD; };
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t HD = (int64_t)H * kD;
     const int units = N * H;
@@ -211,30 +227,52 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
         h = jj / N;
         n = jj % N;
     };
+    // unit i: (n, h), its first token a and its token count (at most Lmax: a device cu_seqlens
+    // that disagrees with the host copy that sized the boxes is flagged by the prep warps)
+    auto unit_rows = [&](int i, int& n, int& h, int64_t& a, bool flag) -> int {
+        unit_of(i, n, h);
+        int64_t e;
+        seq_range(cu, n, T_total, a, e);
+        int L = (int)(e - a);
+        if (L > Lmax) {
+            if (flag) flag_status(d_status, KDA_ERR_DEVICE_ARG);
+            L = Lmax;
+        }
+        return L;
+    };
     const uint32_t cs_bytes = 3u * kD * 3u * (uint32_t)sizeof(Tio);
 
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
-            tc::mbar_init(&full[b], 1);
+            tc::mbar_init(&sfull[b], 1);
             tc::mbar_init(&done[b], kCompute);
+            tc::mbar_init(&rfull[b], 1);
+            tc::mbar_init(&rdone[b], kPrep);
+            tc::mbar_init(&ready[b], kPrep);
         }
         tc::fence_mbar_init();
     }
     for (int c = tid; c < kD; c += kThreads) sRms[c] = rms_w ? rms_w[c] : 1.f;
     __syncthreads();
 
-    if (warp == kCompute / 32) {
+    if (warp == (kCompute + kPrep) / 32) {
         // ------------------------------------------------------------ producer (one thread)
+        // Unit i: its token rows into row slot i % 2 once the prep warps have read unit i - 2's
+        // there, then its state into state slot i % 2 once the compute warps are through unit
+        // i - 2, whose final state leaves first.  The rows of unit i + 1 are therefore issued as
+        // soon as unit i - 2's tokens are done, well before the compute warps reach unit i + 1.
         if (lane != 0) return;
         const CUtensorMap* mp[7] = {&maps.q, &maps.k, &maps.v, &maps.g, &maps.gate, &maps.s_in, &maps.s_out};
         for (int m = 0; m < 7; ++m)
             if ((m != 4 || has_gate) && (m != 5 || has_s0) && (m != 6 || has_sfin))
                 asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(mp[m])) : "memory");
-        const uint32_t tx = (has_s0 ? 65536u : 0u) + (cs_in ? cs_bytes : 0u) + (has_gate ? 4u : 3u) * ST.part +
-                            (uint32_t)Lmax * kD * 4u;
-        uint32_t pend = 0;  // bit b: a fill of stage b in flight, its phase parity in bit 2 + b
+        const uint32_t tx_rows = (cs_in ? cs_bytes : 0u) + (has_gate ? 4u : 3u) * ST.part + (uint32_t)Lmax * kD * 4u;
+        const uint32_t tx_state = has_s0 ? kStateSlot : 0u;
+        // bit b: a fill of state slot b in flight, its parity in bit 2 + b; bits 4 + r and 6 + r
+        // the same for row slot r
+        uint32_t pend = 0;
         bool failed = false;
-        // unit j is done with stage j % 2 and its state is back there: send it to final_state
+        // unit j's tokens are through and its state is back in its slot: send it to final_state
         auto drain = [&](int j) -> bool {
             const int b = j & 1;
             if (!tc::mbar_wait(&done[b], (uint32_t)((j >> 1) & 1))) return false;
@@ -242,38 +280,47 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
                 int n, h;
                 unit_of(j, n, h);
                 const int y = (n * H + h) * kD;
-                for (int bx = 0; bx < 4; ++bx) tma_store_2d(&maps.s_out, 32 * bx, y, sbase + (uint32_t)b * ST.bytes + 16384u * bx);
+                for (int bx = 0; bx < 4; ++bx) tma_store_2d(&maps.s_out, 32 * bx, y, sbase + (uint32_t)b * kStateSlot + 16384u * bx);
                 tc::bulk_commit();
-                tc::bulk_wait_read<0>();  // the stage may be refilled once the stores have read it
+                tc::bulk_wait_read<0>();  // the slot may be refilled once the stores have read it
             }
             return true;
         };
         for (int i = 0; i < my_units; ++i) {
             const int b = i & 1;
-            if (i >= 2 && !drain(i - 2)) {
-                failed = true;
-                break;
-            }
             int n, h;
             unit_of(i, n, h);
             int64_t a, e;
             seq_range(cu, n, T_total, a, e);
+            // the rows (and betas) of unit i
+            if (i >= 2 && !tc::mbar_wait(&rdone[b], (uint32_t)(((i - 2) >> 1) & 1))) {
+                failed = true;
+                break;
+            }
 #pragma unroll
             for (int t = 0; t < kL8; ++t) sbeta[b][t] = t < e - a ? beta[(a + t) * H + h] : 0.f;
-            const uint32_t st = sbase + (uint32_t)b * ST.bytes;
-            tc::mbar_expect_tx(&full[b], tx);  // (its arrival also releases the betas above)
-            if (has_s0)
-                for (int bx = 0; bx < 4; ++bx) tma_load_2d(st + 16384u * bx, &maps.s_in, 32 * bx, (n * H + h) * kD, &full[b]);
+            const uint32_t rs = sbase + rbase + (uint32_t)b * ST.bytes;
+            tc::mbar_expect_tx(&rfull[b], tx_rows);  // (its arrival also releases the betas above)
             if (cs_in)
                 for (int p = 0; p < 3; ++p)
-                    tc::bulk_load(st + ST.conv + (uint32_t)p * (cs_bytes / 3u),
-                                  cs_in + (((int64_t)n * 3 + p) * HD + (int64_t)h * kD) * 3, cs_bytes / 3u, &full[b]);
+                    tc::bulk_load(rs + ST.conv + (uint32_t)p * (cs_bytes / 3u),
+                                  cs_in + (((int64_t)n * 3 + p) * HD + (int64_t)h * kD) * 3, cs_bytes / 3u, &rfull[b]);
             const int x = h * kD, y = (int)a;
-            tma_load_2d(st + ST.rows, &maps.q, x, y, &full[b]);
-            tma_load_2d(st + ST.rows + ST.part, &maps.k, x, y, &full[b]);
-            tma_load_2d(st + ST.rows + 2 * ST.part, &maps.v, x, y, &full[b]);
-            if (has_gate) tma_load_2d(st + ST.rows + 3 * ST.part, &maps.gate, x, y, &full[b]);
-            tma_load_2d(st + ST.g, &maps.g, x, y, &full[b]);
+            tma_load_2d(rs + ST.rows, &maps.q, x, y, &rfull[b]);
+            tma_load_2d(rs + ST.rows + ST.part, &maps.k, x, y, &rfull[b]);
+            tma_load_2d(rs + ST.rows + 2 * ST.part, &maps.v, x, y, &rfull[b]);
+            if (has_gate) tma_load_2d(rs + ST.rows + 3 * ST.part, &maps.gate, x, y, &rfull[b]);
+            tma_load_2d(rs + ST.g, &maps.g, x, y, &rfull[b]);
+            pend = (pend & ~(0x50u << b)) | ((1u | ((uint32_t)((i >> 1) & 1) << 2)) << (4 + b));
+            // the state of unit i
+            if (i >= 2 && !drain(i - 2)) {
+                failed = true;
+                break;
+            }
+            tc::mbar_expect_tx(&sfull[b], tx_state);
+            if (has_s0)
+                for (int bx = 0; bx < 4; ++bx)
+                    tma_load_2d(sbase + (uint32_t)b * kStateSlot + 16384u * bx, &maps.s_in, 32 * bx, (n * H + h) * kD, &sfull[b]);
             pend = (pend & ~(5u << b)) | ((1u | ((uint32_t)((i >> 1) & 1) << 2)) << b);
         }
         if (!failed)
@@ -283,117 +330,185 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
                     break;
                 }
         if (failed) {  // fills in flight: wait for them (bounded) before the shared memory goes away
-            for (int b = 0; b < 2; ++b)
-                if ((pend >> b) & 1u) tc::mbar_wait(&full[b], (pend >> (2 + b)) & 1u);
+            for (int b = 0; b < 2; ++b) {
+                if ((pend >> b) & 1u) tc::mbar_wait(&sfull[b], (pend >> (2 + b)) & 1u);
+                if ((pend >> (4 + b)) & 1u) tc::mbar_wait(&rfull[b], (pend >> (6 + b)) & 1u);
+            }
             flag_status(d_status, KDA_ERR_TIMEOUT);
         }
         tc::bulk_wait_all();
         return;
     }
 
-    // ---------------------------------------------------------------- compute warps
-    const int c0w = 8 * warp;  // the warp's first value column
-    // output of a unit's tokens (warp w0 + t for token t, then every nw-th): o = scale S^T q / |q|
-    // from the readout sums, RMSNorm, weight, gate
-    auto emit_unit = [&](int64_t ja, int jh, int jL, int jb, int w0, int nw) {
-        const int c0 = 4 * lane;
-        for (int t = warp - w0; t < jL; t += nw) {
-            const float sq = scale * snorm[t][0];
-            float4 o = *reinterpret_cast<const float4*>(so + t * kD + c0);
-            o.x *= sq;
-            o.y *= sq;
-            o.z *= sq;
-            o.w *= sq;
-            float ss = o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w;
+    if (warp >= kCompute / 32) {
+        // ------------------------------------------------------------ prep warps
+        // Per unit j, ahead of the compute warps: conv + SiLU of the q, k, v channels (thread d:
+        // channel d of each part), e^g and the gate sigmoids, the L2 norms and the betas, from
+        // row slot j % 2 into the buffers of parity j & 1, then `rdone` (the row slot is free)
+        // and `ready`.  Those buffers held unit j - 2: its outputs are normalised first, once
+        // `done` shows that its tokens are through.
+        const int ptid = tid - kCompute, pw = ptid >> 5, d = ptid;
+        // outputs of unit j (warp pw for tokens pw, pw + 4): o = scale S^T q / |q| from the
+        // readout sums, RMSNorm, weight, gate
+        auto emit_unit = [&](int j) {
+            int n, h;
+            int64_t a;
+            const int L = unit_rows(j, n, h, a, false), pb = j & 1, c0 = 4 * lane;
+            for (int t = pw; t < L; t += kPrep / 32) {
+                const float sq = scale * snorm[pb][t][0];
+                float4 o = *reinterpret_cast<const float4*>(so(pb) + t * kD + c0);
+                o.x *= sq;
+                o.y *= sq;
+                o.z *= sq;
+                o.w *= sq;
+                float ss = o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            const float inv = 1.0f / sqrtf(ss * (1.0f / kD) + eps_rms);
-            const float4 rw = *reinterpret_cast<const float4*>(&sRms[c0]);
-            const float4 gg = *reinterpret_cast<const float4*>(&sgate[jb][t][c0]);
-            store4<To>(out + ((ja + t) * H + jh) * kD + c0, o.x * inv * rw.x * gg.x, o.y * inv * rw.y * gg.y,
-                       o.z * inv * rw.z * gg.z, o.w * inv * rw.w * gg.w);
+                for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                const float inv = 1.0f / sqrtf(ss * (1.0f / kD) + eps_rms);
+                const float4 rw = *reinterpret_cast<const float4*>(&sRms[c0]);
+                const float4 gg = *reinterpret_cast<const float4*>(&sgate[pb][t][c0]);
+                store4<To>(out + ((a + t) * H + h) * kD + c0, o.x * inv * rw.x * gg.x, o.y * inv * rw.y * gg.y,
+                           o.z * inv * rw.z * gg.z, o.w * inv * rw.w * gg.w);
+            }
+        };
+        int h_prev = -1;
+        bool failed = false;
+        for (int j = 0; j < my_units; ++j) {
+            const int b = j & 1;
+            int n, h;
+            int64_t a;
+            const int L = unit_rows(j, n, h, a, ptid == 0);
+            if (j >= 2) {  // the buffers of parity b held unit j - 2: its tokens are through first
+                const bool ok = ptid == 0 ? tc::mbar_wait(&done[b], (uint32_t)(((j - 2) >> 1) & 1)) : true;
+                if (pbar_or(!ok)) {
+                    failed = true;
+                    break;
+                }
+                emit_unit(j - 2);
+            }
+            {  // the unit's rows have landed; conv taps of a new head
+                const bool ok = ptid == 0 ? tc::mbar_wait(&rfull[b], (uint32_t)((j >> 1) & 1)) : true;
+                if (h != h_prev)
+                    for (int idx = ptid; idx < 3 * kD * 4; idx += kPrep) {
+                        const int part = idx / (kD * 4), rem = idx % (kD * 4);
+                        sW[idx] = conv_w[(part * HD + (int64_t)h * kD) * 4 + rem];
+                    }
+                h_prev = h;
+                if (pbar_or(!ok)) {
+                    failed = true;
+                    break;
+                }
+            }
+            const uint8_t* st = sm + rbase + (uint32_t)b * ST.bytes;
+            if (ptid < kL8) sbf[b][ptid] = sbeta[b][ptid];  // (the row slot may be refilled before the tokens run)
+            float sq2[kL8], sk2[kL8];  // squares of this channel's q and k per token
+#pragma unroll
+            for (int part = 0; part < 3; ++part) {  // conv + SiLU; the rolled window out
+                const int ch = part * kD + d;
+                float p0 = 0.f, p1 = 0.f, p2 = 0.f;  // x[-3], x[-2], x[-1]
+                if (cs_in) {
+                    const Tio* c3 = reinterpret_cast<const Tio*>(st + ST.conv) + ch * 3;
+                    p0 = to_f(c3[0]);
+                    p1 = to_f(c3[1]);
+                    p2 = to_f(c3[2]);
+                }
+                const Tio* rp = reinterpret_cast<const Tio*>(st + ST.rows + (uint32_t)part * ST.part) + d;
+                const float4 w = *reinterpret_cast<const float4*>(&sW[ch * 4]);
+                float* dst = part == 0 ? fq(b) + d : part == 1 ? fk(b) + d : &sv[b][0][d];
+                const int dstride = part == 2 ? kD : kFs;
+                float xr[kL8];  // every token's raw value first: one shared-memory round trip
+#pragma unroll
+                for (int t = 0; t < kL8; ++t) xr[t] = t < L ? to_f(rp[t * kD]) : 0.f;
+#pragma unroll
+                for (int t = 0; t < kL8; ++t) {
+                    float y = 0.f;
+                    if (t < L) {
+                        y = act_silu<Tio>(w.x * p0 + w.y * p1 + w.z * p2 + w.w * xr[t]);
+                        dst[t * dstride] = y;
+                        p0 = p1;
+                        p1 = p2;
+                        p2 = xr[t];
+                    }
+                    if (part == 0) sq2[t] = y * y;
+                    if (part == 1) sk2[t] = y * y;
+                }
+                if (cs_out) {  // last three raw values of the sequence (exact copies of Tio values)
+                    Tio* o3 = cs_out + (((int64_t)n * 3 + part) * HD + (int64_t)h * kD + d) * 3;
+                    o3[0] = from_f<Tio>(p0);
+                    o3[1] = from_f<Tio>(p1);
+                    o3[2] = from_f<Tio>(p2);
+                }
+            }
+            {  // decay factors and gate sigmoids of every token (channel d)
+                const float* gs = reinterpret_cast<const float*>(st + ST.g);
+                const Tio* gt = reinterpret_cast<const Tio*>(st + ST.rows + 3 * ST.part);
+                for (int t = 0; t < L; ++t) {
+                    fa(b)[t * kFs + d] = decay_exp<Tio>(gs[t * kD + d]);
+                    sgate[b][t][d] = has_gate ? act_sigmoid<Tio>(to_f(gt[t * kD + d])) : 1.f;
+                }
+            }
+            // L2 norms of q and k: sums over the warp, then over the four warps
+#pragma unroll
+            for (int t = 0; t < kL8; ++t) {
+                if (t < L) {
+                    float x = sq2[t], y = sk2[t];
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) {
+                        x += __shfl_xor_sync(0xffffffffu, x, off);
+                        y += __shfl_xor_sync(0xffffffffu, y, off);
+                    }
+                    if (lane == 0) {
+                        spart[pw][t][0] = x;
+                        spart[pw][t][1] = y;
+                    }
+                }
+            }
+            pbar();
+            if (ptid < 2 * L) {
+                const int t = ptid >> 1, qk = ptid & 1;
+                float ssum = 0.f;
+#pragma unroll
+                for (int w4 = 0; w4 < kPrep / 32; ++w4) ssum += spart[w4][t][qk];
+                snorm[b][t][qk] = 1.0f / sqrtf(ssum + eps_l2);
+            }
+            mbar_arrive(&rdone[b]);  // every read of the row slot is done
+            mbar_arrive(&ready[b]);  // (releases every prep thread's writes of the unit's factors)
         }
-    };
-    int h_prev = -1;
-    int64_t a_prev = 0;  // the previous unit (its outputs are emitted during this unit's conv)
-    int L_prev = 0;
-    bool failed = false;
+        if (!failed)  // the last two units' outputs
+            for (int j = my_units > 2 ? my_units - 2 : 0; j < my_units; ++j) {
+                const bool ok = ptid == 0 ? tc::mbar_wait(&done[j & 1], (uint32_t)((j >> 1) & 1)) : true;
+                if (pbar_or(!ok)) {
+                    failed = true;
+                    break;
+                }
+                emit_unit(j);
+            }
+        if (failed && ptid == 0) flag_status(d_status, KDA_ERR_TIMEOUT);
+        return;
+    }
+
+    // ---------------------------------------------------------------- compute warps
+    // Per unit i: the state from its slot into registers, the tokens, the readouts into o, the
+    // final state back into the slot, then `done`.  The warps never wait for one another: each
+    // owns its eight value columns, and lane 0 of each warp polls the barriers for it.
+    const int c0w = 8 * warp;  // the warp's first value column
     for (int i = 0; i < my_units; ++i) {
         const int b = i & 1;
         int n, h;
-        unit_of(i, n, h);
-        int64_t a, e;
-        seq_range(cu, n, T_total, a, e);
-        int L = (int)(e - a);
-        if (L > Lmax) {  // the device cu_seqlens disagrees with the host copy that sized the boxes
-            if (tid == 0) flag_status(d_status, KDA_ERR_DEVICE_ARG);
-            L = Lmax;
-        }
-        // ---- A: this unit's stage has landed; conv taps of a new head
-        bool ok = true;
-        if (warp == 0) ok = tc::mbar_wait(&full[b], (uint32_t)((i >> 1) & 1));
-        if (h != h_prev)
-            for (int idx = tid; idx < 3 * kD * 4; idx += kCompute) {
-                const int part = idx / (kD * 4), rem = idx % (kD * 4);
-                sW[idx] = conv_w[(part * HD + (int64_t)h * kD) * 4 + rem];
+        int64_t a;
+        const int L = unit_rows(i, n, h, a, false);
+        {
+            bool ok = true;
+            if (lane == 0)
+                ok = tc::mbar_wait(&sfull[b], (uint32_t)((i >> 1) & 1)) && tc::mbar_wait(&ready[b], (uint32_t)((i >> 1) & 1));
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) flag_status(d_status, KDA_ERR_TIMEOUT);
+                break;
             }
-        const int hp = h_prev;
-        h_prev = h;
-        if (cbar_or(!ok)) {
-            if (tid == 0) flag_status(d_status, KDA_ERR_TIMEOUT);
-            failed = true;
-            break;
+            __syncwarp();
         }
-        uint8_t* st = sm + (uint32_t)b * ST.bytes;
-        // conv + SiLU of every token, one channel per thread (warps 0-11); the rolled window out
-        for (int ch = tid; ch < 3 * kD; ch += kCompute) {
-            const int part = ch >> 7, d = ch & (kD - 1);
-            float p0 = 0.f, p1 = 0.f, p2 = 0.f;  // x[-3], x[-2], x[-1]
-            if (cs_in) {
-                const Tio* c3 = reinterpret_cast<const Tio*>(st + ST.conv) + ch * 3;
-                p0 = to_f(c3[0]);
-                p1 = to_f(c3[1]);
-                p2 = to_f(c3[2]);
-            }
-            const Tio* rp = reinterpret_cast<const Tio*>(st + ST.rows + (uint32_t)part * ST.part) + d;
-            const float4 w = *reinterpret_cast<const float4*>(&sW[ch * 4]);
-            float* dst = part == 0 ? fq + d : part == 1 ? fk + d : &sv[0][d];
-            const int dstride = part == 2 ? kD : kFs;
-            float xr[kL8];  // every token's raw value first: one shared-memory round trip
-#pragma unroll
-            for (int t = 0; t < kL8; ++t) xr[t] = t < L ? to_f(rp[t * kD]) : 0.f;
-#pragma unroll
-            for (int t = 0; t < kL8; ++t)
-                if (t < L) {
-                    dst[t * dstride] = act_silu<Tio>(w.x * p0 + w.y * p1 + w.z * p2 + w.w * xr[t]);
-                    p0 = p1;
-                    p1 = p2;
-                    p2 = xr[t];
-                }
-            if (cs_out) {  // last three raw values of the sequence (exact copies of Tio values)
-                Tio* o3 = cs_out + (((int64_t)n * 3 + part) * HD + (int64_t)h * kD + d) * 3;
-                o3[0] = from_f<Tio>(p0);
-                o3[1] = from_f<Tio>(p1);
-                o3[2] = from_f<Tio>(p2);
-            }
-        }
-        {  // decay factors and gate sigmoids of every token
-            const float* gs = reinterpret_cast<const float*>(st + ST.g);
-            const Tio* gt = reinterpret_cast<const Tio*>(st + ST.rows + 3 * ST.part);
-            for (int idx = tid; idx < L * kD; idx += kCompute) {
-                const int t = idx >> 7, c = idx & (kD - 1);
-                fa[t * kFs + c] = decay_exp<Tio>(gs[idx]);
-                sgate[b][t][c] = has_gate ? act_sigmoid<Tio>(to_f(gt[idx])) : 1.f;
-            }
-        }
-        // the previous unit's outputs (its o, norms and gates are complete: every warp has passed
-        // barrier A since; this unit writes o and the norms only after barrier B, and its gates
-        // to the other parity)
-        if (i > 0 && warp >= kEmitWarp0) emit_unit(a_prev, hp, L_prev, b ^ 1, kEmitWarp0, kEmitWarps);
-        a_prev = a;
-        L_prev = L;
-        // the state into registers (after the conv, whose row loads it would otherwise queue
-        // behind): s2[m][p] = columns c0w + 2 p, c0w + 2 p + 1 of row lane + 32 m
+        uint8_t* st = sm + (uint32_t)b * kStateSlot;
+        // the state into registers: s2[m][p] = columns c0w + 2 p, c0w + 2 p + 1 of row lane + 32 m
         f2 s2[4][4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
@@ -406,28 +521,19 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
                 s2[m][2 * hf + 1] = f2_of(x.z, x.w);
             }
         }
-        cbar();  // B: the stage is read completely (the state stays there for the write-back)
-        // L2 norms of q and k, one vector per warp
-        if (warp < 2 * L) {
-            const int t = warp >> 1;
-            const float* src = (warp & 1 ? fk : fq) + t * kFs;  // lane: channels 4 lane .. 4 lane + 3
-            const float4 x4 = *reinterpret_cast<const float4*>(src + 4 * lane);
-            float ss = x4.x * x4.x + x4.y * x4.y + x4.z * x4.z + x4.w * x4.w;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            if (lane == 0) snorm[t][warp & 1] = 1.0f / sqrtf(ss + eps_l2);
-        }
-        cbar();  // C
-
         // ---- tokens: no barrier between them.  The eight columns' sums over the warp go through one
         // transposed reduction per token, which carries token t's probe together with token
         // t - 1's readout (so the readout never adds a reduction of its own to the chain).
+        const float* fqb = fq(b);
+        const float* fkb = fk(b);
+        const float* fab = fa(b);
+        float* sob = so(b);
         f2 O[4] = {f2_dup(0.f), f2_dup(0.f), f2_dup(0.f), f2_dup(0.f)};  // readout of the previous token
         for (int t = 0; t < L; ++t) {
-            const float* kt = fk + t * kFs + lane;
-            const float* at = fa + t * kFs + lane;
-            const float* qt = fq + t * kFs + lane;
-            const float ik = snorm[t][1];
+            const float* kt = fkb + t * kFs + lane;
+            const float* at = fab + t * kFs + lane;
+            const float* qt = fqb + t * kFs + lane;
+            const float ik = snorm[b][t][1];
             f2 k2[4], P[4] = {f2_dup(0.f), f2_dup(0.f), f2_dup(0.f), f2_dup(0.f)};
 #pragma unroll
             for (int m = 0; m < 4; ++m) {  // decay and probe
@@ -444,10 +550,10 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
                              f2_lo(O[0]), f2_hi(O[0]), f2_lo(O[1]), f2_hi(O[1]),
                              f2_lo(O[2]), f2_hi(O[2]), f2_lo(O[3]), f2_hi(O[3])};
             const float red = reduce16_32(v16, lane);  // lane l: value l >> 1
-            if (t > 0 && lane >= 16 && (lane & 1) == 0) so[(t - 1) * kD + c0w + ((lane >> 1) - 8)] = red;
+            if (t > 0 && lane >= 16 && (lane & 1) == 0) sob[(t - 1) * kD + c0w + ((lane >> 1) - 8)] = red;
             // lanes 2c, 2c + 1 hold column c's probe: each lane forms the correction of the column
             // it holds (lanes 16-31 form unused values), then the eight are passed round
-            const float el = sbeta[b][t] * ik * (sv[t][c0w + ((lane >> 1) & 7)] - ik * red);
+            const float el = sbf[b][t] * ik * (sv[b][t][c0w + ((lane >> 1) & 7)] - ik * red);
             float e[8];
 #pragma unroll
             for (int c = 0; c < 8; ++c) e[c] = __shfl_sync(0xffffffffu, el, 2 * c);
@@ -467,9 +573,10 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
             float o8[8] = {f2_lo(O[0]), f2_hi(O[0]), f2_lo(O[1]), f2_hi(O[1]),
                            f2_lo(O[2]), f2_hi(O[2]), f2_lo(O[3]), f2_hi(O[3])};
             const float ot = reduce8_32(o8, lane);
-            if ((lane & 3) == 0) so[(L - 1) * kD + c0w + ((lane >> 2) & 7)] = ot;
+            if ((lane & 3) == 0) sob[(L - 1) * kD + c0w + ((lane >> 2) & 7)] = ot;
         }
-        // the final state back into the stage for the producer's tensor-map stores; release it
+        // the final state back into its slot for the producer's tensor-map stores; release the
+        // slot and the unit's factor buffers
         if (has_sfin) {
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -484,16 +591,13 @@ k_short_tma(const __grid_constant__ ShortMaps maps, int Lmax, int has_gate, int 
         }
         mbar_arrive(&done[b]);
     }
-    if (my_units > 0 && !failed) {  // the last unit's outputs, once every token's o is complete
-        cbar();
-        emit_unit(a_prev, h_prev, L_prev, (my_units - 1) & 1, 0, kCompute / 32);
-    }
 }
 
-// dynamic shared memory: two stages, the permuted q, k, e^g factors and o, alignment slack
+// dynamic shared memory: two state slots, two row slots, two sets (per unit parity) of the q, k,
+// e^g factors and o, alignment slack
 template <typename Tio>
 uint32_t short_tma_smem(int Lmax) {
-    return 2 * TmaStage<Tio>(Lmax).bytes + (3u * kFs + kD) * (uint32_t)Lmax * 4u + 1024u;
+    return 2 * kStateSlot + 2 * RowSlot<Tio>(Lmax).bytes + 2 * (3u * kFs + kD) * (uint32_t)Lmax * 4u + 1024u;
 }
 
 int max_len(const kda_prefill_args& a) {
