@@ -31,7 +31,9 @@ def _run(inp, flags=0, out_dtype=None, final_state=None, conv_out=False, initial
     return out, fin, cso
 
 
-LENGTHS = [[1], [2], [4] * 8, [8] * 5, [1, 8, 0, 3, 5, 7]]
+# (7 tokens at most: the largest batch whose fp32 rows and states still fit the pipelined kernel's
+# shared memory; 8 with fp32 inputs takes the plainer kernel)
+LENGTHS = [[1], [2], [4] * 8, [7, 2, 6, 7], [8] * 5, [1, 8, 0, 3, 5, 7]]
 
 
 @pytest.mark.parametrize("lengths", LENGTHS)
