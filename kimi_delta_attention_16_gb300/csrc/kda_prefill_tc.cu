@@ -296,7 +296,7 @@ k_tc_prefill(const bf16* __restrict__ q, const bf16* __restrict__ k, const bf16*
     int64_t s0, s1;
     seq_range(cu, n, T_total, s0, s1);
     int64_t cb, ce;  // this CTA's chunks [cb, ce) of the sequence
-    seg_chunk_range((s1 - s0 + kC - 1) / kC, sp.P, sp.w, seg, cb, ce);
+    seg_chunk_range((s1 - s0 + kC - 1) / kC, sp.P, sp.w, sp.wd, seg, cb, ce);
 
     if (warp == 0) {
         tmem_alloc(&s_tbase, kTmemCols);
@@ -1421,6 +1421,43 @@ int tc_segments(const kda_prefill_args& a) { return tc_seg_choice(a).P; }
 
 size_t tc_prefill_workspace(const kda_prefill_args& a) { return seg_layout(a, tc_segments(a)).total; }
 
+// Segment 0's share of the chunks, as w / wd: with the later segments' CTAs in w waves, it
+// balances segment 0 against them.  Measured, a later segment's chunk step costs about 14/15 of
+// segment 0's (its runs write raw readouts without the RMSNorm and gate epilogue; the identity-
+// start run also skips the v conv) and each of its CTAs about 0.4 chunk steps of start-up, so for
+// a sequence of the batch's mean chunk count nc the share is the c0 / nc that minimises
+// max(c0, w (14/15 ceil((nc - c0) / (P - 1)) + 0.4)) near the balance point.  A forced P
+// (w = 1) keeps equal segments.
+static void seg_share(const kda_prefill_args& a, const SegChoice& sc, int& w, int& wd) {
+    const int P = sc.P;
+    w = 1;
+    wd = P;
+    if (P <= 1 || a.segments > 0 || a.N <= 0) return;
+    const double mean = (double)a.T_total / ((double)a.N * kC);
+    const int64_t nc = mean < 1.0 ? 1 : (int64_t)(mean + 0.5);
+    if (nc > 0x3fffffffLL) {  // (keeps w / wd in int; the plain wave share there)
+        w = sc.w;
+        wd = sc.w + P - 1;
+        return;
+    }
+    constexpr int64_t kLaterStep = 14, kStartUp = 6;  // fifteenths of a segment-0 chunk step
+    const int64_t W = sc.w;
+    const int64_t est = W * (kLaterStep * nc + kStartUp * (P - 1)) / (15 * (int64_t)(P - 1) + kLaterStep * W);
+    int64_t c0 = est < nc ? est : nc, best = -1;
+    for (int64_t c = est - 1; c <= est + 3; ++c) {
+        if (c < 0 || c > nc) continue;
+        const int64_t sl = (nc - c + P - 2) / (P - 1);
+        const int64_t t0 = 15 * c, t1 = W * (kLaterStep * sl + kStartUp);
+        const int64_t cost = t0 > t1 ? t0 : t1;
+        if (best < 0 || cost < best) {
+            best = cost;
+            c0 = c;
+        }
+    }
+    w = (int)c0;
+    wd = (int)nc;
+}
+
 cudaError_t launch_tc_prefill(const kda_prefill_args& a, char* ws, cudaStream_t s) {
     const int64_t units = (int64_t)a.N * a.H;
     if (units == 0) return cudaSuccess;
@@ -1428,7 +1465,7 @@ cudaError_t launch_tc_prefill(const kda_prefill_args& a, char* ws, cudaStream_t 
     const int P = sc.P;
     SegPlan sp{};
     sp.P = P;
-    sp.w = sc.w;
+    seg_share(a, sc, sp.w, sp.wd);
     if (P > 1) {
         const SegLayout l = seg_layout(a, P);
         sp.end_state = reinterpret_cast<float*>(ws + l.end_state);

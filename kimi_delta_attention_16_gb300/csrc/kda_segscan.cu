@@ -218,7 +218,7 @@ k_seg_fixup(SegPlan sp, const int32_t* __restrict__ cu, int64_t T_total, int H,
     int64_t s0, s1;
     seq_range(cu, n, T_total, s0, s1);
     int64_t cb, ce;
-    seg_chunk_range((s1 - s0 + 63) / 64, sp.P, sp.w, s, cb, ce);
+    seg_chunk_range((s1 - s0 + 63) / 64, sp.P, sp.w, sp.wd, s, cb, ce);
     const int64_t ta = s0 + cb * 64;
     const int64_t tz = s0 + ce * 64 < s1 ? s0 + ce * 64 : s1;
     const int64_t ntiles = tz > ta ? (tz - ta + kFixTile - 1) / kFixTile : 0;

@@ -40,7 +40,7 @@ cudaError_t launch_tc_prefill(const kda_prefill_args& a, char* ws, cudaStream_t 
 // unit u = n * H + h is one (sequence, head).
 struct SegPlan {
     int P;             // segments per unit; 1 = one CTA walks each whole sequence
-    int w;             // segment 0 takes w / (w + P - 1) of the chunks
+    int w, wd;         // segment 0 takes the first ceil(nc * w / wd) of a sequence's nc chunks
     float* end_state;  // [units][P][D][D]: segment 0's end state, then B_s (zero-start runs)
     float* trans;      // [units][P][D][D]: M_s, the end states of the identity-start runs
     float* start;      // [units][P][D][D]: S_s, the composed start state of segment s >= 1
@@ -49,17 +49,17 @@ struct SegPlan {
 };
 
 // Chunks [cb, ce) of segment s when a sequence of nc chunks is cut into P
-// segments: segment 0 is the first ceil(nc * w / (w + P - 1)) chunks, the
-// others split the rest into runs of ceil(rest / (P - 1)) (trailing segments
-// may be short or empty).  w = 1 gives P segments of about nc / P.
-__host__ __device__ __forceinline__ void seg_chunk_range(int64_t nc, int P, int w, int s, int64_t& cb,
+// segments: segment 0 is the first ceil(nc * w / wd) chunks, the others split
+// the rest into runs of ceil(rest / (P - 1)) (trailing segments may be short or
+// empty).  w = 1, wd = P gives P segments of about nc / P.
+__host__ __device__ __forceinline__ void seg_chunk_range(int64_t nc, int P, int w, int wd, int s, int64_t& cb,
                                                          int64_t& ce) {
     if (P <= 1) {
         cb = 0;
         ce = nc;
         return;
     }
-    const int64_t den = (int64_t)w + P - 1;
+    const int64_t den = wd;
     int64_t c0 = (nc * w + den - 1) / den;
     c0 = c0 < nc ? c0 : nc;
     if (s == 0) {
